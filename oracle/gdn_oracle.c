@@ -1,0 +1,478 @@
+/*
+ * gdn_oracle.c -- float64 CPU oracle for the Gated DeltaNet ("gated delta rule",
+ * GDR) linear-attention layer of the Qwen3.5 / Qwen3-Next hybrid models.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, calls or
+ * includes this file; only the tests, the smoke entry point and the benchmark's
+ * CPU-baseline leg load it (through ctypes).  It shares no code, header, table
+ * or helper with the CUDA path.
+ *
+ * What it computes, and where that is stated:
+ *   - "pegainfer issue #1001", Split 2 and Split 3 bullets: one batched decode
+ *     call over all decode rows, per-request recurrent/conv state addressed by
+ *     a scheduler-owned slot index, device-to-device compaction on retire.
+ *   - "pegainfer PR #1003", description bullets: rank-local head counts feed the
+ *     GDR decode / conv / chunkwise prefill chains, gated RMSNorm at the local
+ *     value heads, norm weight shared by all heads.
+ *   - "helexa/cortex commit 95dc874 (tp_qwen3_5)", TpQwen3_5GatedDeltaNet
+ *     bullet: the fused [q | k | v] channel layout (first key_dim, second
+ *     key_dim, value_dim) and the delta-rule loop over V-heads; helpers
+ *     softplus, repeat_interleave, l2norm and the gated RmsNormGated tail.
+ *   - The per-token arithmetic the pages name but do not print is the published
+ *     gated delta rule (Yang, Kautz & Hatamizadeh, "Gated Delta Networks:
+ *     Improving Mamba2 with Delta Rule", ICLR 2025): decay the state by exp(g),
+ *     then write value v under key k with strength beta,
+ *         S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,
+ *         o_t = S_t^T q_t,
+ *     with g = -exp(A_log) * softplus(a + dt_bias), beta = sigmoid(b).
+ *   - The chunkwise WY/UT form (oracle_prefill_chunkwise) follows Yang et al.,
+ *     "Parallelizing Linear Transformers with the Delta Rule over Sequence
+ *     Length" (NeurIPS 2024), section 3 (the UT transform), with the gate
+ *     factors of the gated variant.  It exists only so that the tests can pin
+ *     the chunk algebra the GPU prefill uses against the sequential definition.
+ *
+ * Readings taken where the pages are silent (each listed in the design notes):
+ *   conv: depthwise causal cross-correlation, no bias, tap K-1 weights the
+ *         current token, the conv state holds the previous K-1 RAW inputs,
+ *         oldest first; SiLU after the conv.
+ *   GQA:  V-head h uses K-head floor(h / (Hv/Hk))  (repeat_interleave).
+ *   q:    l2-normalised, then scaled by q_scale (1/sqrt(dk) by default).
+ *   l2norm: x / sqrt(sum x^2 + eps).   gated norm: o / sqrt(mean o^2 + eps)
+ *         * w * SiLU(z), all in full precision, one rounding at the end.
+ *   state layout: [slot][Hv][dk][dv], dv fastest.
+ *   padding rows: slot_idx < 0 -> no state read or write, output zero.
+ *
+ * Parity status: every function here is pinned by the CPU test suite
+ * (tests/test_oracle_pins.py): closed forms, the associative-memory and
+ * beta = 0 special cases, brute force against an independently written
+ * dense-matrix form, chunkwise == sequential, prefill/decode continuation.
+ * The readings above are not pinned by the pages (they print no numbers).
+ *
+ * All arithmetic is IEEE double; exp/log1p/sqrt come from libm.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ scalars */
+
+/* softplus(x) = log(1 + e^x), evaluated without overflow for large x. */
+double oracle_softplus(double x) {
+  if (x > 0.0) return x + log1p(exp(-x));
+  return log1p(exp(x));
+}
+
+double oracle_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+double oracle_silu(double x) { return x * oracle_sigmoid(x); }
+
+/* Decay and write strength of one V-head for one token:
+ *   g    = -exp(A_log) * softplus(a + dt_bias)
+ *   beta = sigmoid(b)                                                        */
+void oracle_gates(double A_log, double dt_bias, double a, double b, double* g,
+                  double* beta) {
+  *g = -exp(A_log) * oracle_softplus(a + dt_bias);
+  *beta = oracle_sigmoid(b);
+}
+
+/* ------------------------------------------------------------ conv1d update */
+
+/* One token of the depthwise causal conv over C channels with kernel K.
+ *   state: [K-1][C], row 0 = oldest previous raw input, row K-2 = newest.
+ *   w:     [C][K],   w[c][K-1] multiplies the current input x[c].
+ *   y[c] = SiLU( sum_{j<K-1} w[c][j] * state[j][c]  +  w[c][K-1] * x[c] ).
+ * Afterwards the state holds the last K-1 raw inputs including x.           */
+void oracle_conv_step(int C, int K, double* state, const double* w,
+                      const double* x, double* y) {
+  for (int c = 0; c < C; ++c) {
+    double acc = w[(size_t)c * K + (K - 1)] * x[c];
+    for (int j = 0; j < K - 1; ++j) acc += w[(size_t)c * K + j] * state[(size_t)j * C + c];
+    y[c] = oracle_silu(acc);
+  }
+  for (int c = 0; c < C; ++c) {
+    for (int j = 0; j + 1 < K - 1; ++j) state[(size_t)j * C + c] = state[(size_t)(j + 1) * C + c];
+    if (K > 1) state[(size_t)(K - 2) * C + c] = x[c];
+  }
+}
+
+/* y = scale * x / sqrt(sum x^2 + eps). */
+void oracle_l2norm(int n, const double* x, double eps, double scale, double* y) {
+  double ss = 0.0;
+  for (int i = 0; i < n; ++i) ss += x[i] * x[i];
+  const double inv = 1.0 / sqrt(ss + eps);
+  for (int i = 0; i < n; ++i) y[i] = x[i] * inv * scale;
+}
+
+/* ------------------------------------------------------------ delta rule */
+
+/* One token of the gated delta rule on a dk x dv state S (row-major, dv fastest).
+ *   S <- exp(g) S
+ *   delta = beta * (v - S^T k)
+ *   S <- S + k delta^T
+ *   o = S^T q                                (o may be NULL)
+ * which is S_t = exp(g)(I - beta k k^T) S_{t-1} + beta k v^T, o_t = S_t^T q.  */
+void oracle_core_step(int dk, int dv, double* S, const double* k, const double* v,
+                      const double* q, double g, double beta, double* o) {
+  const double decay = exp(g);
+  for (size_t i = 0; i < (size_t)dk * dv; ++i) S[i] *= decay;
+  double* delta = (double*)malloc(sizeof(double) * (size_t)dv);
+  for (int j = 0; j < dv; ++j) {
+    double kv = 0.0;
+    for (int i = 0; i < dk; ++i) kv += S[(size_t)i * dv + j] * k[i];
+    delta[j] = beta * (v[j] - kv);
+  }
+  for (int i = 0; i < dk; ++i)
+    for (int j = 0; j < dv; ++j) S[(size_t)i * dv + j] += k[i] * delta[j];
+  if (o) {
+    for (int j = 0; j < dv; ++j) {
+      double acc = 0.0;
+      for (int i = 0; i < dk; ++i) acc += S[(size_t)i * dv + j] * q[i];
+      o[j] = acc;
+    }
+  }
+  free(delta);
+}
+
+/* out = o / sqrt(mean(o^2) + eps) * w * SiLU(z), over one V-head of dv. */
+void oracle_gated_rmsnorm(int dv, const double* o, const double* z, const double* w,
+                          double eps, double* out) {
+  double ss = 0.0;
+  for (int j = 0; j < dv; ++j) ss += o[j] * o[j];
+  const double inv = 1.0 / sqrt(ss / dv + eps);
+  for (int j = 0; j < dv; ++j) out[j] = o[j] * inv * w[j] * oracle_silu(z[j]);
+}
+
+/* ------------------------------------------------------------ one token */
+
+typedef struct {
+  int Hk, Hv, dk, dv, K;
+  double q_scale, l2_eps, norm_eps;
+} oracle_dims;
+
+static size_t qkv_channels(const oracle_dims* d) {
+  return (size_t)2 * d->Hk * d->dk + (size_t)d->Hv * d->dv;
+}
+
+/* Runs one token of the whole layer for one request whose recurrent state is
+ * S_slot ([Hv][dk][dv]) and conv state conv_slot ([K-1][Cqkv]).
+ *   qkv [Cqkv], z [Hv*dv], a [Hv], b [Hv] -> out [Hv*dv].                    */
+static void layer_token(const oracle_dims* d, const double* A_log, const double* dt_bias,
+                        const double* conv_w, const double* norm_w, double* S_slot,
+                        double* conv_slot, const double* qkv, const double* z,
+                        const double* a, const double* b, double* out) {
+  const size_t C = qkv_channels(d);
+  const int r = d->Hv / d->Hk;
+  double* y = (double*)malloc(sizeof(double) * C);
+  double* qn = (double*)malloc(sizeof(double) * (size_t)d->Hk * d->dk);
+  double* kn = (double*)malloc(sizeof(double) * (size_t)d->Hk * d->dk);
+  double* o = (double*)malloc(sizeof(double) * (size_t)d->dv);
+  oracle_conv_step((int)C, d->K, conv_slot, conv_w, qkv, y);
+  const double* yq = y;
+  const double* yk = y + (size_t)d->Hk * d->dk;
+  const double* yv = y + (size_t)2 * d->Hk * d->dk;
+  for (int hk = 0; hk < d->Hk; ++hk) {
+    oracle_l2norm(d->dk, yq + (size_t)hk * d->dk, d->l2_eps, d->q_scale, qn + (size_t)hk * d->dk);
+    oracle_l2norm(d->dk, yk + (size_t)hk * d->dk, d->l2_eps, 1.0, kn + (size_t)hk * d->dk);
+  }
+  for (int h = 0; h < d->Hv; ++h) {
+    const int hk = h / r; /* repeat_interleave */
+    double g, beta;
+    oracle_gates(A_log[h], dt_bias[h], a[h], b[h], &g, &beta);
+    oracle_core_step(d->dk, d->dv, S_slot + (size_t)h * d->dk * d->dv, kn + (size_t)hk * d->dk,
+                     yv + (size_t)h * d->dv, qn + (size_t)hk * d->dk, g, beta, o);
+    oracle_gated_rmsnorm(d->dv, o, z + (size_t)h * d->dv, norm_w, d->norm_eps,
+                         out + (size_t)h * d->dv);
+  }
+  free(y);
+  free(qn);
+  free(kn);
+  free(o);
+}
+
+static int dims_ok(const oracle_dims* d) {
+  return d->Hk > 0 && d->Hv > 0 && d->dk > 0 && d->dv > 0 && d->K >= 1 && d->Hv % d->Hk == 0;
+}
+
+/* ------------------------------------------------------------ batched decode */
+
+/* One batched decode step over B rows.  Row i uses slot slot_idx[i]; a negative
+ * slot marks a padding row (its output is zero, no state is touched).
+ * rec_state: [num_slots][Hv][dk][dv]; conv_state: [num_slots][K-1][Cqkv].
+ * qkv [B][Cqkv], z [B][Hv*dv], a/b [B][Hv], out [B][Hv*dv].
+ * Returns 0, or -1 on bad dims / a slot >= num_slots (that row is skipped).  */
+int oracle_decode_step(int Hk, int Hv, int dk, int dv, int K, double q_scale, double l2_eps,
+                       double norm_eps, const double* A_log, const double* dt_bias,
+                       const double* conv_w, const double* norm_w, double* rec_state,
+                       double* conv_state, int num_slots, const int32_t* slot_idx, int B,
+                       const double* qkv, const double* z, const double* a, const double* b,
+                       double* out) {
+  const oracle_dims d = {Hk, Hv, dk, dv, K, q_scale, l2_eps, norm_eps};
+  if (!dims_ok(&d)) return -1;
+  const size_t C = qkv_channels(&d);
+  const size_t rec_slot = (size_t)Hv * dk * dv, conv_slot = (size_t)(K - 1) * C;
+  const size_t zw = (size_t)Hv * dv;
+  int rc = 0;
+  for (int i = 0; i < B; ++i) {
+    const int s = slot_idx[i];
+    if (s < 0 || s >= num_slots) {
+      memset(out + (size_t)i * zw, 0, sizeof(double) * zw);
+      if (s >= num_slots) rc = -1;
+      continue;
+    }
+    layer_token(&d, A_log, dt_bias, conv_w, norm_w, rec_state + (size_t)s * rec_slot,
+                conv_state + (size_t)s * conv_slot, qkv + (size_t)i * C, z + (size_t)i * zw,
+                a + (size_t)i * Hv, b + (size_t)i * Hv, out + (size_t)i * zw);
+  }
+  return rc;
+}
+
+/* Standalone conv update for B rows: qkv_out[i] = SiLU(conv(qkv_in[i])), state rolled. */
+int oracle_conv1d_update(int C, int K, const double* conv_w, double* conv_state, int num_slots,
+                         const int32_t* slot_idx, int B, const double* qkv_in, double* qkv_out) {
+  int rc = 0;
+  for (int i = 0; i < B; ++i) {
+    const int s = slot_idx[i];
+    if (s < 0 || s >= num_slots) {
+      memset(qkv_out + (size_t)i * C, 0, sizeof(double) * (size_t)C);
+      if (s >= num_slots) rc = -1;
+      continue;
+    }
+    oracle_conv_step(C, K, conv_state + (size_t)s * (size_t)(K - 1) * C, conv_w,
+                     qkv_in + (size_t)i * C, qkv_out + (size_t)i * C);
+  }
+  return rc;
+}
+
+/* ------------------------------------------------------------ prefill */
+
+/* Sequential prefill: sequence n covers packed tokens [cu_seqlens[n], cu_seqlens[n+1]),
+ * writes its final recurrent and conv state into slot slot_idx[n].  When
+ * has_init[n] is 0 the sequence starts from zero recurrent and conv state;
+ * otherwise it continues from what the slot holds.  Token by token: the
+ * definition itself.                                                          */
+int oracle_prefill(int Hk, int Hv, int dk, int dv, int K, double q_scale, double l2_eps,
+                   double norm_eps, const double* A_log, const double* dt_bias,
+                   const double* conv_w, const double* norm_w, double* rec_state,
+                   double* conv_state, int num_slots, const int32_t* cu_seqlens,
+                   const int32_t* slot_idx, const uint8_t* has_init, int num_seqs,
+                   const double* qkv, const double* z, const double* a, const double* b,
+                   double* out) {
+  const oracle_dims d = {Hk, Hv, dk, dv, K, q_scale, l2_eps, norm_eps};
+  if (!dims_ok(&d)) return -1;
+  const size_t C = qkv_channels(&d);
+  const size_t rec_slot = (size_t)Hv * dk * dv, conv_slot = (size_t)(K - 1) * C;
+  const size_t zw = (size_t)Hv * dv;
+  int rc = 0;
+  for (int n = 0; n < num_seqs; ++n) {
+    const int s = slot_idx[n];
+    const int t0 = cu_seqlens[n], t1 = cu_seqlens[n + 1];
+    if (s < 0 || s >= num_slots) {
+      memset(out + (size_t)t0 * zw, 0, sizeof(double) * zw * (size_t)(t1 - t0));
+      if (s >= num_slots) rc = -1;
+      continue;
+    }
+    double* S = rec_state + (size_t)s * rec_slot;
+    double* cs = conv_state + (size_t)s * conv_slot;
+    if (!has_init || !has_init[n]) {
+      memset(S, 0, sizeof(double) * rec_slot);
+      memset(cs, 0, sizeof(double) * conv_slot);
+    }
+    for (int t = t0; t < t1; ++t)
+      layer_token(&d, A_log, dt_bias, conv_w, norm_w, S, cs, qkv + (size_t)t * C,
+                  z + (size_t)t * zw, a + (size_t)t * Hv, b + (size_t)t * Hv,
+                  out + (size_t)t * zw);
+  }
+  return rc;
+}
+
+/* Chunkwise (WY / UT-transform) form of the same prefill, chunk size Cc.
+ * Per sequence, per V-head h, per chunk of L <= Cc tokens starting from state S0:
+ *   gamma_i = sum_{j<=i} g_j                       (within the chunk)
+ *   A_ij    = beta_i exp(gamma_i - gamma_j) k_i.k_j   for j < i, else 0
+ *   T       = (I + A)^{-1}                           (forward substitution)
+ *   W       = T diag(beta exp(gamma)) K             [L x dk]
+ *   Ut      = T diag(beta) V                         [L x dv]
+ *   U       = Ut - W S0
+ *   O       = diag(exp(gamma)) Q S0 + ((Q K^T) o Gamma o M) U,
+ *             Gamma_ij = exp(gamma_i - gamma_j), M_ij = [j <= i]
+ *   S_L     = exp(gamma_L) S0 + (diag(exp(gamma_L - gamma)) K)^T U
+ * Every exponent above is <= 0.  The conv, l2norm, gates and gated norm are
+ * the per-token ones; the conv is run token by token first.                  */
+int oracle_prefill_chunkwise(int Hk, int Hv, int dk, int dv, int K, double q_scale,
+                             double l2_eps, double norm_eps, const double* A_log,
+                             const double* dt_bias, const double* conv_w, const double* norm_w,
+                             double* rec_state, double* conv_state, int num_slots,
+                             const int32_t* cu_seqlens, const int32_t* slot_idx,
+                             const uint8_t* has_init, int num_seqs, const double* qkv,
+                             const double* z, const double* a, const double* b, double* out,
+                             int Cc) {
+  const oracle_dims d = {Hk, Hv, dk, dv, K, q_scale, l2_eps, norm_eps};
+  if (!dims_ok(&d) || Cc < 1) return -1;
+  const size_t C = qkv_channels(&d);
+  const size_t rec_slot = (size_t)Hv * dk * dv, conv_slot = (size_t)(K - 1) * C;
+  const size_t zw = (size_t)Hv * dv;
+  const int r = Hv / Hk;
+  int rc = 0;
+  for (int n = 0; n < num_seqs; ++n) {
+    const int s = slot_idx[n];
+    const int t0 = cu_seqlens[n], t1 = cu_seqlens[n + 1], T = t1 - t0;
+    if (s < 0 || s >= num_slots) {
+      memset(out + (size_t)t0 * zw, 0, sizeof(double) * zw * (size_t)T);
+      if (s >= num_slots) rc = -1;
+      continue;
+    }
+    double* S = rec_state + (size_t)s * rec_slot;
+    double* cs = conv_state + (size_t)s * conv_slot;
+    if (!has_init || !has_init[n]) {
+      memset(S, 0, sizeof(double) * rec_slot);
+      memset(cs, 0, sizeof(double) * conv_slot);
+    }
+    if (T <= 0) continue;
+    /* token-wise prologue: conv + SiLU, l2norm, gates */
+    double* Y = (double*)malloc(sizeof(double) * C * (size_t)T);
+    double* Qn = (double*)malloc(sizeof(double) * (size_t)T * Hk * dk);
+    double* Kn = (double*)malloc(sizeof(double) * (size_t)T * Hk * dk);
+    double* G = (double*)malloc(sizeof(double) * (size_t)T * Hv);
+    double* Bt = (double*)malloc(sizeof(double) * (size_t)T * Hv);
+    for (int t = 0; t < T; ++t) {
+      oracle_conv_step((int)C, K, cs, conv_w, qkv + (size_t)(t0 + t) * C, Y + (size_t)t * C);
+      for (int hk = 0; hk < Hk; ++hk) {
+        oracle_l2norm(dk, Y + (size_t)t * C + (size_t)hk * dk, l2_eps, q_scale,
+                      Qn + ((size_t)t * Hk + hk) * dk);
+        oracle_l2norm(dk, Y + (size_t)t * C + (size_t)(Hk + hk) * dk, l2_eps, 1.0,
+                      Kn + ((size_t)t * Hk + hk) * dk);
+      }
+      for (int h = 0; h < Hv; ++h)
+        oracle_gates(A_log[h], dt_bias[h], a[(size_t)(t0 + t) * Hv + h],
+                     b[(size_t)(t0 + t) * Hv + h], &G[(size_t)t * Hv + h],
+                     &Bt[(size_t)t * Hv + h]);
+    }
+    double* gam = (double*)malloc(sizeof(double) * (size_t)Cc);
+    double* Am = (double*)malloc(sizeof(double) * (size_t)Cc * Cc);
+    double* Tm = (double*)malloc(sizeof(double) * (size_t)Cc * Cc);
+    double* Wm = (double*)malloc(sizeof(double) * (size_t)Cc * dk);
+    double* Um = (double*)malloc(sizeof(double) * (size_t)Cc * dv);
+    double* Om = (double*)malloc(sizeof(double) * (size_t)Cc * dv);
+    double* Snew = (double*)malloc(sizeof(double) * (size_t)dk * dv);
+    for (int h = 0; h < Hv; ++h) {
+      const int hk = h / r;
+      double* S0 = S + (size_t)h * dk * dv;
+      for (int c0 = 0; c0 < T; c0 += Cc) {
+        const int L = (T - c0 < Cc) ? (T - c0) : Cc;
+#define KROW(i) (Kn + ((size_t)(c0 + (i)) * Hk + hk) * dk)
+#define QROW(i) (Qn + ((size_t)(c0 + (i)) * Hk + hk) * dk)
+#define VROW(i) (Y + (size_t)(c0 + (i)) * C + (size_t)2 * Hk * dk + (size_t)h * dv)
+#define BETA(i) (Bt[(size_t)(c0 + (i)) * Hv + h])
+        double acc = 0.0;
+        for (int i = 0; i < L; ++i) {
+          acc += G[(size_t)(c0 + i) * Hv + h];
+          gam[i] = acc;
+        }
+        for (int i = 0; i < L; ++i)
+          for (int j = 0; j < L; ++j) {
+            double v = 0.0;
+            if (j < i) {
+              double kk = 0.0;
+              for (int e = 0; e < dk; ++e) kk += KROW(i)[e] * KROW(j)[e];
+              v = BETA(i) * exp(gam[i] - gam[j]) * kk;
+            }
+            Am[(size_t)i * L + j] = v;
+          }
+        /* (I + A) T = I, row by row: T_i = e_i - sum_{j<i} A_ij T_j */
+        for (int i = 0; i < L; ++i)
+          for (int c = 0; c < L; ++c) {
+            double v = (i == c) ? 1.0 : 0.0;
+            for (int j = 0; j < i; ++j) v -= Am[(size_t)i * L + j] * Tm[(size_t)j * L + c];
+            Tm[(size_t)i * L + c] = v;
+          }
+        /* W = T diag(beta e^gamma) K ; Ut = T diag(beta) V */
+        for (int i = 0; i < L; ++i) {
+          for (int e = 0; e < dk; ++e) {
+            double v = 0.0;
+            for (int j = 0; j < L; ++j)
+              v += Tm[(size_t)i * L + j] * BETA(j) * exp(gam[j]) * KROW(j)[e];
+            Wm[(size_t)i * dk + e] = v;
+          }
+          for (int e = 0; e < dv; ++e) {
+            double v = 0.0;
+            for (int j = 0; j < L; ++j) v += Tm[(size_t)i * L + j] * BETA(j) * VROW(j)[e];
+            Um[(size_t)i * dv + e] = v;
+          }
+        }
+        /* U = Ut - W S0 */
+        for (int i = 0; i < L; ++i)
+          for (int e = 0; e < dv; ++e) {
+            double v = 0.0;
+            for (int f = 0; f < dk; ++f) v += Wm[(size_t)i * dk + f] * S0[(size_t)f * dv + e];
+            Um[(size_t)i * dv + e] -= v;
+          }
+        /* O = diag(e^gamma) Q S0 + ((Q K^T) o Gamma o M) U */
+        for (int i = 0; i < L; ++i)
+          for (int e = 0; e < dv; ++e) {
+            double v = 0.0;
+            for (int f = 0; f < dk; ++f) v += QROW(i)[f] * S0[(size_t)f * dv + e];
+            v *= exp(gam[i]);
+            for (int j = 0; j <= i; ++j) {
+              double qk = 0.0;
+              for (int f = 0; f < dk; ++f) qk += QROW(i)[f] * KROW(j)[f];
+              v += qk * exp(gam[i] - gam[j]) * Um[(size_t)j * dv + e];
+            }
+            Om[(size_t)i * dv + e] = v;
+          }
+        /* S_L = e^{gamma_L} S0 + (diag(e^{gamma_L - gamma}) K)^T U */
+        for (int f = 0; f < dk; ++f)
+          for (int e = 0; e < dv; ++e) {
+            double v = exp(gam[L - 1]) * S0[(size_t)f * dv + e];
+            for (int j = 0; j < L; ++j)
+              v += exp(gam[L - 1] - gam[j]) * KROW(j)[f] * Um[(size_t)j * dv + e];
+            Snew[(size_t)f * dv + e] = v;
+          }
+        memcpy(S0, Snew, sizeof(double) * (size_t)dk * dv);
+        for (int i = 0; i < L; ++i)
+          oracle_gated_rmsnorm(dv, Om + (size_t)i * dv,
+                               z + (size_t)(t0 + c0 + i) * zw + (size_t)h * dv, norm_w, norm_eps,
+                               out + (size_t)(t0 + c0 + i) * zw + (size_t)h * dv);
+#undef KROW
+#undef QROW
+#undef VROW
+#undef BETA
+      }
+    }
+    free(gam); free(Am); free(Tm); free(Wm); free(Um); free(Om); free(Snew);
+    free(Y); free(Qn); free(Kn); free(G); free(Bt);
+  }
+  return rc;
+}
+
+/* ------------------------------------------------------------ compaction */
+
+/* new[dst[i]] = old[src[i]] for both pools, every source read before any
+ * destination is written (a snapshot gather).  Slots that are no dst keep their
+ * contents.  Returns -1 on an out-of-range or duplicate dst.                  */
+int oracle_state_compact(double* rec_state, double* conv_state, int num_slots,
+                         int64_t rec_slot_elems, int64_t conv_slot_elems, const int32_t* src,
+                         const int32_t* dst, int n) {
+  for (int i = 0; i < n; ++i) {
+    if (src[i] < 0 || src[i] >= num_slots || dst[i] < 0 || dst[i] >= num_slots) return -1;
+    for (int j = 0; j < i; ++j)
+      if (dst[j] == dst[i]) return -1;
+  }
+  double* snap_r = (double*)malloc(sizeof(double) * (size_t)rec_slot_elems * (n > 0 ? n : 1));
+  double* snap_c = (double*)malloc(sizeof(double) * (size_t)conv_slot_elems * (n > 0 ? n : 1));
+  for (int i = 0; i < n; ++i) {
+    memcpy(snap_r + (size_t)i * rec_slot_elems, rec_state + (size_t)src[i] * rec_slot_elems,
+           sizeof(double) * (size_t)rec_slot_elems);
+    memcpy(snap_c + (size_t)i * conv_slot_elems, conv_state + (size_t)src[i] * conv_slot_elems,
+           sizeof(double) * (size_t)conv_slot_elems);
+  }
+  for (int i = 0; i < n; ++i) {
+    memcpy(rec_state + (size_t)dst[i] * rec_slot_elems, snap_r + (size_t)i * rec_slot_elems,
+           sizeof(double) * (size_t)rec_slot_elems);
+    memcpy(conv_state + (size_t)dst[i] * conv_slot_elems, snap_c + (size_t)i * conv_slot_elems,
+           sizeof(double) * (size_t)conv_slot_elems);
+  }
+  free(snap_r);
+  free(snap_c);
+  return 0;
+}
