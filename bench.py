@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 Gated DeltaNet layer library.
+
+Headline: batched decode at B=64 rows (K-heads 16, V-heads 48, dk = dv = 128, bf16 inputs,
+f32 state pool of 128 slots), reported as GB/s of recurrent-state traffic (each step reads and
+writes 64 x 48 x 128 x 128 x 4 B = 402.65 MB) and as a fraction of the measured HBM peak.  The
+same JSON line carries the chunked prefill of one T = 4096 sequence (tokens/s, contraction
+TFLOP/s) and the slot compaction on retire (GB/s).  A step is one batched decode step; the
+state working set (402.65 MB) exceeds the 129 MB L2, so no L2 flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the float64 CPU oracle on the same decode workload on this host's cores.
+Under torchrun (N > 1) every rank runs its own independent replica (weak scaling: decode rows
+and slots shard with no exchange); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "GDN decode state GB/s (% of HBM peak) at B=64; chunked prefill tokens/s"
+UNIT = "GB/s"
+DECODE_WL = 2
+PREFILL_WL = 3
+
+# Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the decode kernel
+# from one ncu capture at B=64, keyed by the SHA-256 of the kernel source it was taken on.  A
+# changed kernel reports null until it is captured again.
+DECODE_TRAFFIC = {}
+
+
+def _src_sha(name: str) -> str:
+    p = os.path.join(ROOT, "gated_deltanet_linear_09_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while the GPU is busy."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = sorted(sm)[len(sm) // 2:]        # upper half: samples taken under load
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ ours
+
+def run_ours(args, ws, rank, local):
+    import torch
+    from gated_deltanet_linear_09_gb300 import build as gbuild
+    from gated_deltanet_linear_09_gb300 import gdn, synth
+    from gated_deltanet_linear_09_gb300.runtime import GatedDeltaNetLayer
+
+    gbuild.build()
+    gdn.load()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    hbm_peak, bf16_peak, peak_kind = peaks()
+
+    # ---------------- decode, B = 64
+    wl = synth.workloads()[DECODE_WL]
+    geo = wl.geo
+    w = synth.make_weights(geo, wl.seed)
+    layer = GatedDeltaNetLayer(geo, w, wl.num_slots)
+    rec, conv = synth.make_pool(geo, wl.num_slots, wl.seed, True)
+    layer.load_state(rec, conv)
+    del rec, conv
+    slots = torch.from_numpy(synth.make_slot_idx(wl.num_slots, wl.batch, wl.seed)).cuda()
+    # a ring of distinct per-step inputs resident in HBM
+    ring = [layer.inputs(synth.decode_step_inputs(wl, t)) for t in range(8)]
+    out = torch.empty((wl.batch, geo.zdim), dtype=layer.act, device="cuda")
+    stream = torch.cuda.current_stream()
+    state_bytes = 2 * wl.batch * geo.Hv * geo.dk * geo.dv * 4
+    total_bytes = state_bytes + wl.batch * (2 * 3 * geo.cqkv * 2 + geo.cqkv * 2 + 2 * geo.zdim * 2
+                                            + 2 * geo.Hv * 2)
+
+    def step(i):
+        x = ring[i % len(ring)]
+        layer.decode_step(slots, x["qkv"], x["z"], x["a"], x["b"], out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    # keep the same load a little longer so the clock sampler sees it
+    t_end = time.time() + (1.0 if args.only == "all" else 0.0)
+    i = 0
+    while time.time() < t_end:
+        for _ in range(200):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    gbs = state_bytes * args.steps * ws / (ms * 1e-3) / 1e9
+    per_launch_gbs = state_bytes / (ms_step * 1e-3) / 1e9
+
+    if args.only == "decode":
+        if rank == 0:
+            print(json.dumps({"only": "decode", "ms_per_step": ms_step, "gbs": gbs}), flush=True)
+        if dist:
+            dist.destroy_process_group()
+        return
+    # ---------------- e2e: the same step through the public API with host buffers
+    host = [{k: v.cpu().pin_memory() for k, v in ring[j].items()} for j in range(len(ring))]
+    dev_in = {k: torch.empty_like(v) for k, v in ring[0].items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step(i):
+        hx = host[i % len(host)]
+        for k in dev_in:
+            dev_in[k].copy_(hx[k], non_blocking=True)
+        layer.decode_step(slots, dev_in["qkv"], dev_in["z"], dev_in["a"], dev_in["b"], out)
+        host_out.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_gbs = state_bytes * args.steps * ws / (e2e_ms * 1e-3) / 1e9
+    del ring, host, dev_in
+
+    # ---------------- compaction at step 256 of the B=64 workload (56 survivors -> [0,56))
+    retire = synth.retire_choice(wl.seed, wl.batch, 8, 256)
+    keep = [i for i in range(wl.batch) if i not in set(retire.tolist())]
+    src = slots.cpu().numpy()[keep].tolist()
+    dst = list(range(len(keep)))
+    slot_bytes = gdn.gdn_state_slot_bytes(layer.dims, gdn.act_code(layer.act))
+    comp_bytes = 2 * len(keep) * slot_bytes
+    for _ in range(3):
+        layer.compact(src, dst)
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    c0.record(stream)
+    for _ in range(reps):
+        layer.compact(src, dst)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    comp_ms = c0.elapsed_time(c1) / reps
+    del layer
+    torch.cuda.empty_cache()
+
+    # ---------------- chunked prefill, one sequence of T = 4096
+    pwl = synth.workloads()[PREFILL_WL]
+    pgeo = pwl.geo
+    player = GatedDeltaNetLayer(pgeo, synth.make_weights(pgeo, pwl.seed), pwl.num_slots)
+    T = pwl.seq_lens[0]
+    px = player.inputs(synth.make_token_inputs(pgeo, T, pwl.seed, 0))
+    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    psl = torch.tensor([0], dtype=torch.int32, device="cuda")
+    pout = torch.empty((T, pgeo.zdim), dtype=player.act, device="cuda")
+    for _ in range(3):
+        player.prefill(cu, psl, None, px["qkv"], px["z"], px["a"], px["b"], pout)
+    torch.cuda.synchronize()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    preps = 10
+    p0.record(stream)
+    for _ in range(preps):
+        player.prefill(cu, psl, None, px["qkv"], px["z"], px["a"], px["b"], pout)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    p_ms = p0.elapsed_time(p1) / preps
+    Hk, Hv, d, C = pgeo.Hk, pgeo.Hv, pgeo.dk, pwl.chunk
+    flops = T * (Hv * (8 * C * d + 6 * d * d) + Hk * 4 * C * d)
+    p_tflops = flops / (p_ms * 1e-3) / 1e12
+    p_bytes = T * (pgeo.cqkv * 2 + pgeo.zdim * 2 * 2 + 2 * Hv * 2) + Hv * d * d * 4
+    del player, px
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    traffic = None
+    ent = DECODE_TRAFFIC.get(_src_sha("gdn_decode.cu"))
+    if ent:
+        traffic = ent
+    line = {
+        "metric": METRIC, "value": round(gbs, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "batch_rows": wl.batch, "k_heads": geo.Hk,
+                   "v_heads": geo.Hv, "head_dim": geo.dk, "slots": wl.num_slots,
+                   "act_dtype": "bf16", "state_dtype": "f32",
+                   "l2": "no flush: 402.65 MB state working set per step > 129 MB L2",
+                   "parallelism": f"replicas x{ws} (rows/slots shard, no exchange)"},
+        "row_steps_per_s": round(wl.batch * ws * args.steps / (ms * 1e-3), 1),
+        "hbm_frac_state": round(per_launch_gbs / hbm_peak, 4),
+        "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": hbm_peak,
+                     "unit": "GB/s", "frac": round(per_launch_gbs / hbm_peak, 4),
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": state_bytes,
+                     "total_bytes_per_launch_incl_conv_io": total_bytes,
+                     "kernel": "decode_kernel<128,128,bf16>"},
+        "e2e": {"value": round(e2e_gbs, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 5)},
+        "gpu_launches": args.steps,
+        "prefill": {"workload": pwl.name, "tokens_per_s": round(T / (p_ms * 1e-3), 1),
+                    "ms": round(p_ms, 4), "contraction_gflop": round(flops / 1e9, 3),
+                    "tflops": round(p_tflops, 3),
+                    "roofline": {"bound": "tensor", "achieved": round(p_tflops, 3),
+                                 "peak": bf16_peak, "unit": "TFLOP/s",
+                                 "frac": round(p_tflops / bf16_peak, 5), "peak_kind": peak_kind},
+                    "io_bytes": p_bytes, "launches_per_call": 4},
+        "compact": {"pairs": len(keep), "bytes": comp_bytes, "ms": round(comp_ms, 4),
+                    "gbs": round(comp_bytes / (comp_ms * 1e-3) / 1e9, 1),
+                    "hbm_frac": round(comp_bytes / (comp_ms * 1e-3) / 1e9 / hbm_peak, 4)},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------ oracle timing
+
+def _oracle_decode_setup(rows):
+    import oracle
+    from gated_deltanet_linear_09_gb300 import synth
+    wl = synth.workloads()[DECODE_WL]
+    geo = wl.geo
+    w = {k: np.asarray(v, np.float64) for k, v in synth.make_weights(geo, wl.seed).items()}
+    rng = np.random.default_rng(0)
+    rec = rng.normal(0, 0.02, (rows, geo.Hv, geo.dk, geo.dv))
+    conv = np.asarray(synth.in_dtype(rng.normal(0, 1, (rows, geo.K - 1, geo.cqkv)), geo.act),
+                      np.float64)
+    return oracle, wl, geo, w, rec, conv
+
+
+def _oracle_decode_steps(n_steps, rows):
+    oracle, wl, geo, w, rec, conv = _oracle_decode_setup(rows)
+    slots = np.arange(rows, dtype=np.int32)
+    xs = [{k: np.asarray(v, np.float64) for k, v in
+           synth_inputs(wl, t, rows).items()} for t in range(min(n_steps, 4))]
+    t0 = time.perf_counter()
+    for t in range(n_steps):
+        oracle.decode_step(geo.oracle_dims(), w, rec, conv, slots, **xs[t % len(xs)])
+    return time.perf_counter() - t0, geo
+
+
+def synth_inputs(wl, t, rows):
+    from gated_deltanet_linear_09_gb300 import synth
+    return synth.make_token_inputs(wl.geo, rows, wl.seed, 100, t)
+
+
+def cpu_baseline(args):
+    """The oracle as it stands (float64, one thread) on a bounded sample of the decode workload."""
+    import oracle
+    oracle.build()
+    rows, n_steps = 64, 48
+    sec, geo = _oracle_decode_steps(n_steps, rows)
+    state_bytes = 2 * rows * n_steps * geo.Hv * geo.dk * geo.dv * 4
+    return {"value": round(state_bytes / sec / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n_steps} decode steps x {rows} rows of the B=64 workload "
+                      f"({rows * n_steps} row-steps), float64 C oracle, single thread",
+            "seconds": round(sec, 2)}
+
+
+def run_reference(args, ws, rank):
+    """--impl reference: the oracle on the host cores, same metric and workload shape."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    rows = 64
+    # one step = one full B=64 decode step of the oracle
+    _oracle_decode_steps(max(1, min(args.warmup, 2)), rows)
+    sec, geo = _oracle_decode_steps(args.steps, rows)
+    state_bytes = 2 * rows * args.steps * geo.Hv * geo.dk * geo.dv * 4
+    v = state_bytes / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "decode_B64_Hk16_Hv48_d128_bf16", "batch_rows": rows},
+        "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} full B=64 decode steps, float64 C oracle, "
+                                   "single thread"},
+        "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="all", choices=["all", "decode"],
+                    help="decode: only the B=64 decode timing (used for profiling captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+// gdn_api.cu -- the extern "C" boundary of libgdn.so: host-side argument checks, then one or
+// more kernel launches on the caller's stream.  The contract of every call is documented in
+// include/gdn.h; this file only enforces it.
+#include <math.h>
+
+#include <vector>
+
+#include "gdn_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Geometry checks shared by every call.  Linear-head divisibility fails closed, as the
+// tensor-parallel config of "pegainfer PR #1003" does.
+int check_dims(const gdn_dims* dims, gdn::KDims* out) {
+  if (!dims) return GDN_ERR_INVALID_ARG;
+  const gdn_dims& d = *dims;
+  if (d.num_k_heads <= 0 || d.num_v_heads <= 0) return GDN_ERR_INVALID_ARG;
+  if (d.num_v_heads % d.num_k_heads != 0) return GDN_ERR_HEAD_DIVISIBILITY;
+  if ((d.head_k_dim != 64 && d.head_k_dim != 128) || (d.head_v_dim != 64 && d.head_v_dim != 128))
+    return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (d.conv_kernel != 4) return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (!(d.l2_eps >= 0.f) || !(d.norm_eps >= 0.f) || !(d.q_scale >= 0.f) || !isfinite(d.q_scale))
+    return GDN_ERR_INVALID_ARG;
+  const long long cqkv = 2LL * d.num_k_heads * d.head_k_dim + (long long)d.num_v_heads * d.head_v_dim;
+  if (cqkv > (1LL << 30)) return GDN_ERR_TOO_LARGE;
+  if (out) {
+    out->Hk = d.num_k_heads;
+    out->Hv = d.num_v_heads;
+    out->dk = d.head_k_dim;
+    out->dv = d.head_v_dim;
+    out->K = d.conv_kernel;
+    out->r = d.num_v_heads / d.num_k_heads;
+    out->cqkv = (int)cqkv;
+    out->q_scale = d.q_scale > 0.f ? d.q_scale : 1.0f / sqrtf((float)d.head_k_dim);
+    out->l2_eps = d.l2_eps;
+    out->norm_eps = d.norm_eps;
+  }
+  return GDN_OK;
+}
+
+size_t act_size(gdn_dtype t) { return t == GDN_BF16 ? 2 : 4; }
+bool act_ok(gdn_dtype t) { return t == GDN_F32 || t == GDN_BF16; }
+
+int check_weights(const gdn_weights* w) {
+  if (!w || !act_ok(w->act)) return GDN_ERR_INVALID_ARG;
+  if (!w->A_log || !w->dt_bias || !w->conv_weight || !w->norm_weight) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(w->conv_weight) || !aligned16(w->norm_weight)) return GDN_ERR_MISALIGNED;
+  return GDN_OK;
+}
+
+int check_pool(const gdn_pool* p) {
+  if (!p || !p->rec_state || !p->conv_state || p->num_slots <= 0) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(p->rec_state) || !aligned16(p->conv_state)) return GDN_ERR_MISALIGNED;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_state_slot_bytes(const gdn_dims* dims, gdn_dtype act) {
+  gdn::KDims d;
+  if (check_dims(dims, &d) != GDN_OK || !act_ok(act)) return 0;
+  return sizeof(float) * (size_t)d.Hv * d.dk * d.dv + act_size(act) * (size_t)(d.K - 1) * d.cqkv;
+}
+
+int gdn_conv1d_update(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
+                      const int32_t* slot_idx, int32_t B, const void* qkv_in, void* qkv_out,
+                      cudaStream_t stream) {
+  gdn::KDims d;
+  int rc;
+  if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
+  if (!w || !act_ok(w->act) || !w->conv_weight) return GDN_ERR_INVALID_ARG;
+  if ((rc = check_pool(pool)) != GDN_OK) return rc;
+  if (B < 0 || B > 65535) return B < 0 ? GDN_ERR_INVALID_ARG : GDN_ERR_TOO_LARGE;
+  if (B == 0) return GDN_OK;
+  if (!slot_idx || !qkv_in || !qkv_out) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(qkv_in) || !aligned16(qkv_out) || !aligned16(slot_idx)) return GDN_ERR_MISALIGNED;
+  return gdn::launch_conv1d_update(d, w, pool, slot_idx, B, qkv_in, qkv_out, stream);
+}
+
+int gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
+                    const int32_t* slot_idx, int32_t B, const void* qkv, const void* z,
+                    const void* a, const void* b, void* out, cudaStream_t stream) {
+  gdn::KDims d;
+  int rc;
+  if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
+  if ((rc = check_weights(w)) != GDN_OK) return rc;
+  if ((rc = check_pool(pool)) != GDN_OK) return rc;
+  if (B < 0 || B > 65535) return B < 0 ? GDN_ERR_INVALID_ARG : GDN_ERR_TOO_LARGE;
+  if (B == 0) return GDN_OK;
+  if (!slot_idx || !qkv || !z || !a || !b || !out) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(z) || !aligned16(out) || !aligned16(slot_idx))
+    return GDN_ERR_MISALIGNED;
+  return gdn::launch_decode(d, w, pool, slot_idx, B, qkv, z, a, b, out, stream);
+}
+
+size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t num_seqs, int32_t total_tokens) {
+  gdn::KDims d;
+  if (check_dims(dims, &d) != GDN_OK || num_seqs < 0 || total_tokens < 0) return 0;
+  return gdn::prefill_ws_layout(d, num_seqs, total_tokens, nullptr).bytes;
+}
+
+int gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
+                        const int32_t* cu_seqlens, const int32_t* slot_idx,
+                        const uint8_t* has_initial_state, int32_t num_seqs, int32_t total_tokens,
+                        const void* qkv, const void* z, const void* a, const void* b, void* out,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  gdn::KDims d;
+  int rc;
+  if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
+  if ((rc = check_weights(w)) != GDN_OK) return rc;
+  if ((rc = check_pool(pool)) != GDN_OK) return rc;
+  if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  if (num_seqs > 65535) return GDN_ERR_TOO_LARGE;
+  if (num_seqs == 0) return total_tokens == 0 ? GDN_OK : GDN_ERR_INVALID_ARG;
+  if (!cu_seqlens || !slot_idx) return GDN_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!qkv || !z || !a || !b || !out)) return GDN_ERR_INVALID_ARG;
+  if (total_tokens > 0 && (!aligned16(qkv) || !aligned16(z) || !aligned16(out)))
+    return GDN_ERR_MISALIGNED;
+  const gdn::PrefillWs need = gdn::prefill_ws_layout(d, num_seqs, total_tokens, nullptr);
+  if (!workspace || workspace_bytes < need.bytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_MISALIGNED;
+  const gdn::PrefillWs ws = gdn::prefill_ws_layout(d, num_seqs, total_tokens, workspace);
+  return gdn::launch_prefill(d, w, pool, cu_seqlens, slot_idx, has_initial_state, num_seqs,
+                             total_tokens, qkv, z, a, b, out, ws, stream);
+}
+
+int gdn_state_compact(const gdn_dims* dims, gdn_dtype act, const gdn_pool* pool,
+                      const int32_t* src_slots, const int32_t* dst_slots, int32_t n,
+                      cudaStream_t stream) {
+  gdn::KDims d;
+  int rc;
+  if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
+  if (!act_ok(act)) return GDN_ERR_INVALID_ARG;
+  if ((rc = check_pool(pool)) != GDN_OK) return rc;
+  if (n < 0) return GDN_ERR_INVALID_ARG;
+  if (n > GDN_MAX_COMPACT_PAIRS) return GDN_ERR_TOO_LARGE;
+  if (n == 0) return GDN_OK;
+  if (!src_slots || !dst_slots) return GDN_ERR_INVALID_ARG;
+  std::vector<unsigned char> seen((size_t)pool->num_slots, 0);
+  gdn::CompactPairs pairs;
+  for (int i = 0; i < n; ++i) {
+    const int s = src_slots[i], t = dst_slots[i];
+    if (s < 0 || s >= pool->num_slots || t < 0 || t >= pool->num_slots) return GDN_ERR_SLOT_RANGE;
+    if (seen[(size_t)t]) return GDN_ERR_OVERLAP;
+    seen[(size_t)t] = 1;
+    pairs.src[i] = s;
+    pairs.dst[i] = t;
+  }
+  const size_t rec_bytes = sizeof(float) * (size_t)d.Hv * d.dk * d.dv;
+  const size_t conv_bytes = act_size(act) * (size_t)(d.K - 1) * d.cqkv;
+  return gdn::launch_compact(pairs, n, pool->rec_state, rec_bytes, pool->conv_state, conv_bytes,
+                             stream);
+}
+
+const char* gdn_status_string(int code) {
+  switch (code) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID_ARG: return "invalid argument";
+    case GDN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (head dims must be 64 or 128, conv kernel 4)";
+    case GDN_ERR_HEAD_DIVISIBILITY: return "num_v_heads is not a multiple of num_k_heads";
+    case GDN_ERR_SLOT_RANGE: return "slot index out of range";
+    case GDN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case GDN_ERR_OVERLAP: return "duplicate destination slot";
+    case GDN_ERR_MISALIGNED: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case GDN_ERR_CUDA: return "CUDA launch failed";
+    case GDN_ERR_TOO_LARGE: return "size beyond a per-call maximum";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

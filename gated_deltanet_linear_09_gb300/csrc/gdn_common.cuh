@@ -1,0 +1,67 @@
+// gdn_common.cuh -- device helpers shared by the Gated DeltaNet kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// ------------------------------------------------------------------ activation dtypes
+
+template <typename T> struct Act;
+
+template <> struct Act<float> {
+  static __device__ __forceinline__ float load(const float* p) { return *p; }
+  static __device__ __forceinline__ float ldg(const float* p) { return __ldg(p); }
+  static __device__ __forceinline__ void store(float* p, float v) { *p = v; }
+  static __device__ __forceinline__ float cvt(float v) { return v; }
+};
+
+template <> struct Act<__nv_bfloat16> {
+  static __device__ __forceinline__ float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+  static __device__ __forceinline__ float ldg(const __nv_bfloat16* p) {
+    return __bfloat162float(__ldg(p));
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, float v) {
+    *p = __float2bfloat16_rn(v);
+  }
+  static __device__ __forceinline__ __nv_bfloat16 cvt(float v) { return __float2bfloat16_rn(v); }
+};
+
+// ------------------------------------------------------------------ scalar math
+// Plain calls of the CUDA math library (expf, log1pf); nothing here restates their internals.
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float siluf_(float x) { return x / (1.0f + expf(-x)); }
+// softplus(x) = log(1 + e^x) in a form that does not overflow for large x.
+__device__ __forceinline__ float softplusf_(float x) { return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x))); }
+
+// g = -exp(A_log) * softplus(a + dt_bias);  beta = sigmoid(b)
+__device__ __forceinline__ void gates(float A_log, float dt_bias, float a, float b, float& g,
+                                      float& beta) {
+  g = -expf(A_log) * softplusf_(a + dt_bias);
+  beta = sigmoidf_(b);
+}
+
+// ------------------------------------------------------------------ reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// Runtime dims passed by value to every kernel.
+struct KDims {
+  int Hk, Hv, dk, dv, K, r, cqkv;
+  float q_scale, l2_eps, norm_eps;
+};
+
+}  // namespace gdn

@@ -1,0 +1,291 @@
+// gdn_decode.cu -- batched Gated DeltaNet decode step and standalone conv1d update (sm_103a).
+//
+// The batched GDR decode over all decode rows ("pegainfer issue #1001", Split 2 bullet) with
+// slot-indexed per-request recurrent and conv state ("pegainfer issue #1001", Split 3 bullet),
+// rank-local head counts and the gated RMSNorm at the local V-heads ("pegainfer PR #1003",
+// description bullets), fused [q | k | v] channel regions and repeat_interleave of K-heads
+// ("helexa/cortex commit 95dc874 (tp_qwen3_5)", TpQwen3_5GatedDeltaNet bullet).
+//
+// One CTA owns one (row, K-head) unit: the conv channels of that K-head's q and k, the v
+// channels of its r = Hv/Hk V-heads, and those V-heads' dk x dv f32 states.  Owning all the
+// channels a K-head touches makes the conv-state update race-free without a second launch.
+// The state of each V-head is read once and written once (the decode's whole HBM cost):
+//   kv = S^T k,  sq = S^T q           (one pass over the old S, held in registers)
+//   delta = beta (v - e^g kv),  o = e^g sq + (k.q) delta
+//   S' = e^g S + k delta^T            (written back from the same registers)
+#include "gdn_internal.h"
+
+namespace gdn {
+
+namespace {
+
+template <int N> struct VecF;
+template <> struct VecF<4> {
+  static __device__ __forceinline__ void ld(const float* p, float* v) {
+    const float4 t = __ldcs(reinterpret_cast<const float4*>(p));
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  }
+  static __device__ __forceinline__ void st(float* p, const float* v) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+  }
+};
+template <> struct VecF<2> {
+  static __device__ __forceinline__ void ld(const float* p, float* v) {
+    const float2 t = __ldcs(reinterpret_cast<const float2*>(p));
+    v[0] = t.x; v[1] = t.y;
+  }
+  static __device__ __forceinline__ void st(float* p, const float* v) {
+    __stcs(reinterpret_cast<float2*>(p), make_float2(v[0], v[1]));
+  }
+};
+
+constexpr int kDecodeThreads = 256;
+constexpr int kDecodeWarps = kDecodeThreads / 32;
+
+// One token of the causal conv for channel ch of the row's conv state cs ([K-1][cqkv],
+// K = 4): returns SiLU(sum_j w[j] x_{t-3+j}) and shifts the state by one raw input.
+template <typename T>
+__device__ __forceinline__ float conv_channel(const T* __restrict__ conv_w, T* __restrict__ cs,
+                                              int cqkv, int ch, T xraw) {
+  const T* wc = conv_w + (size_t)ch * 4;
+  const T s0 = cs[ch], s1 = cs[cqkv + ch], s2 = cs[2 * cqkv + ch];
+  float acc = Act<T>::ldg(wc + 3) * Act<T>::load(&xraw);
+  acc = fmaf(Act<T>::ldg(wc + 0), Act<T>::load(&s0), acc);
+  acc = fmaf(Act<T>::ldg(wc + 1), Act<T>::load(&s1), acc);
+  acc = fmaf(Act<T>::ldg(wc + 2), Act<T>::load(&s2), acc);
+  cs[ch] = s1;
+  cs[cqkv + ch] = s2;
+  cs[2 * cqkv + ch] = xraw;
+  return siluf_(acc);
+}
+
+template <int DK, int DV, typename T>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+decode_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict__ dt_bias,
+              const T* __restrict__ conv_w, const T* __restrict__ norm_w, float* __restrict__ rec,
+              T* __restrict__ conv_state, int num_slots, int32_t* __restrict__ status,
+              const int32_t* __restrict__ slot_idx, const T* __restrict__ qkv,
+              const T* __restrict__ z, const T* __restrict__ a, const T* __restrict__ b,
+              T* __restrict__ out) {
+  constexpr int NW = kDecodeWarps;
+  constexpr int CPT = DV / 32;   // state columns per lane
+  constexpr int RPW = DK / NW;   // state rows per warp
+  extern __shared__ float smem[];
+  const int kh = blockIdx.x, row = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = d.r;
+  float* qs = smem;
+  float* ks = qs + DK;
+  float* vs = ks + DK;
+  float* red = vs + r * DV;          // [2 buffers][kv|sq][NW][DV]
+  float* misc = red + 4 * NW * DV;   // iq, ik, k.q
+
+  const int s = slot_idx[row];
+  T* out_row = out + (size_t)row * d.Hv * DV;
+  if (s < 0 || s >= num_slots) {
+    if (s >= num_slots && tid == 0 && kh == 0) set_status(status, GDN_STATUS_SLOT_RANGE);
+    for (int e = tid; e < r * DV; e += kDecodeThreads) out_row[kh * r * DV + e] = Act<T>::cvt(0.f);
+    return;
+  }
+
+  // ---- conv update + SiLU over the channels this unit owns
+  const T* x_row = qkv + (size_t)row * d.cqkv;
+  T* cs = conv_state + (size_t)s * 3 * d.cqkv;
+  const int nch = 2 * DK + r * DV;
+  for (int c = tid; c < nch; c += kDecodeThreads) {
+    int ch;
+    float* dst;
+    if (c < DK) {
+      ch = kh * DK + c;
+      dst = qs + c;
+    } else if (c < 2 * DK) {
+      ch = d.Hk * DK + kh * DK + (c - DK);
+      dst = ks + (c - DK);
+    } else {
+      ch = 2 * d.Hk * DK + kh * r * DV + (c - 2 * DK);
+      dst = vs + (c - 2 * DK);
+    }
+    *dst = conv_channel<T>(conv_w, cs, d.cqkv, ch, x_row[ch]);
+  }
+  __syncthreads();
+
+  // ---- l2norm of q (times q_scale) and k, and k.q of the normalised vectors
+  if (warp == 0) {
+    float sq = 0.f, sk = 0.f, sqk = 0.f;
+    for (int i = lane; i < DK; i += 32) {
+      const float q = qs[i], k = ks[i];
+      sq = fmaf(q, q, sq);
+      sk = fmaf(k, k, sk);
+      sqk = fmaf(q, k, sqk);
+    }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    sqk = warp_sum(sqk);
+    if (lane == 0) {
+      const float iq = d.q_scale / sqrtf(sq + d.l2_eps);
+      const float ik = 1.0f / sqrtf(sk + d.l2_eps);
+      misc[0] = iq;
+      misc[1] = ik;
+      misc[2] = sqk * iq * ik;
+    }
+  }
+  __syncthreads();
+  const float iq = misc[0], ik = misc[1], kq = misc[2];
+  float kr[RPW], qr[RPW];
+#pragma unroll
+  for (int i = 0; i < RPW; ++i) {
+    kr[i] = ks[warp * RPW + i] * ik;
+    qr[i] = qs[warp * RPW + i] * iq;
+  }
+
+  // ---- the r V-heads of this K-head
+  for (int hh = 0; hh < r; ++hh) {
+    const int h = kh * r + hh;
+    float* Sp = rec + (((size_t)s * d.Hv + h) * DK) * DV;
+    float st[RPW][CPT];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) VecF<CPT>::ld(Sp + (size_t)(warp * RPW + i) * DV + lane * CPT, st[i]);
+
+    float g, beta;
+    gates(__ldg(A_log + h), __ldg(dt_bias + h), Act<T>::ldg(a + (size_t)row * d.Hv + h),
+          Act<T>::ldg(b + (size_t)row * d.Hv + h), g, beta);
+    const float eg = expf(g);
+
+    float pk[CPT], pq[CPT];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) pk[c] = pq[c] = 0.f;
+#pragma unroll
+    for (int i = 0; i < RPW; ++i)
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {
+        pk[c] = fmaf(st[i][c], kr[i], pk[c]);
+        pq[c] = fmaf(st[i][c], qr[i], pq[c]);
+      }
+    float* rb = red + (hh & 1) * 2 * NW * DV;
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+      rb[warp * DV + lane * CPT + c] = pk[c];
+      rb[NW * DV + warp * DV + lane * CPT + c] = pq[c];
+    }
+    __syncthreads();
+    float delta[CPT], o[CPT];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+      float kv = 0.f, sqv = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        kv += rb[w * DV + lane * CPT + c];
+        sqv += rb[NW * DV + w * DV + lane * CPT + c];
+      }
+      delta[c] = beta * (vs[hh * DV + lane * CPT + c] - eg * kv);
+      o[c] = fmaf(eg, sqv, kq * delta[c]);
+    }
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) st[i][c] = fmaf(eg, st[i][c], kr[i] * delta[c]);
+      VecF<CPT>::st(Sp + (size_t)(warp * RPW + i) * DV + lane * CPT, st[i]);
+    }
+    // ---- z-gated RMSNorm over this V-head's dv outputs (one warp)
+    if (warp == (hh % NW)) {
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) ss = fmaf(o[c], o[c], ss);
+      ss = warp_sum(ss);
+      const float inv = 1.0f / sqrtf(ss / (float)DV + d.norm_eps);
+      const T* zr = z + (size_t)row * d.Hv * DV + (size_t)h * DV;
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {
+        const int j = lane * CPT + c;
+        const float zz = Act<T>::ldg(zr + j);
+        Act<T>::store(out_row + (size_t)h * DV + j, o[c] * inv * Act<T>::ldg(norm_w + j) * siluf_(zz));
+      }
+    }
+  }
+}
+
+template <typename T>
+__global__ void conv1d_update_kernel(int cqkv, const T* __restrict__ conv_w,
+                                     T* __restrict__ conv_state, int num_slots,
+                                     int32_t* __restrict__ status,
+                                     const int32_t* __restrict__ slot_idx,
+                                     const T* __restrict__ in, T* __restrict__ out) {
+  const int row = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cqkv) return;
+  const int s = slot_idx[row];
+  if (s < 0 || s >= num_slots) {
+    if (s >= num_slots && c == 0) set_status(status, GDN_STATUS_SLOT_RANGE);
+    out[(size_t)row * cqkv + c] = Act<T>::cvt(0.f);
+    return;
+  }
+  T* cs = conv_state + (size_t)s * 3 * cqkv;
+  const float y = conv_channel<T>(conv_w, cs, cqkv, c, in[(size_t)row * cqkv + c]);
+  Act<T>::store(out + (size_t)row * cqkv + c, y);
+}
+
+template <int DK, int DV, typename T>
+int launch_decode_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
+                    const int32_t* slot_idx, int B, const void* qkv, const void* z, const void* a,
+                    const void* b, void* out, cudaStream_t stream) {
+  const size_t smem = sizeof(float) * (2 * DK + d.r * DV + 4 * kDecodeWarps * DV + 4);
+  auto kern = decode_kernel<DK, DV, T>;
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return GDN_ERR_TOO_LARGE;
+  }
+  dim3 grid(d.Hk, B);
+  kern<<<grid, kDecodeThreads, smem, stream>>>(
+      d, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
+      static_cast<const T*>(w->norm_weight), pool->rec_state, static_cast<T*>(pool->conv_state),
+      pool->num_slots, pool->status, slot_idx, static_cast<const T*>(qkv),
+      static_cast<const T*>(z), static_cast<const T*>(a), static_cast<const T*>(b),
+      static_cast<T*>(out));
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+template <typename T>
+int launch_decode_dims(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
+                       const int32_t* slot_idx, int B, const void* qkv, const void* z,
+                       const void* a, const void* b, void* out, cudaStream_t stream) {
+  if (d.dk == 128 && d.dv == 128)
+    return launch_decode_t<128, 128, T>(d, w, pool, slot_idx, B, qkv, z, a, b, out, stream);
+  if (d.dk == 64 && d.dv == 64)
+    return launch_decode_t<64, 64, T>(d, w, pool, slot_idx, B, qkv, z, a, b, out, stream);
+  if (d.dk == 128 && d.dv == 64)
+    return launch_decode_t<128, 64, T>(d, w, pool, slot_idx, B, qkv, z, a, b, out, stream);
+  if (d.dk == 64 && d.dv == 128)
+    return launch_decode_t<64, 128, T>(d, w, pool, slot_idx, B, qkv, z, a, b, out, stream);
+  return GDN_ERR_UNSUPPORTED_SHAPE;
+}
+
+}  // namespace
+
+int launch_decode(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
+                  const int32_t* slot_idx, int B, const void* qkv, const void* z, const void* a,
+                  const void* b, void* out, cudaStream_t stream) {
+  if (w->act == GDN_BF16)
+    return launch_decode_dims<__nv_bfloat16>(d, w, pool, slot_idx, B, qkv, z, a, b, out, stream);
+  return launch_decode_dims<float>(d, w, pool, slot_idx, B, qkv, z, a, b, out, stream);
+}
+
+int launch_conv1d_update(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
+                         const int32_t* slot_idx, int B, const void* in, void* out,
+                         cudaStream_t stream) {
+  dim3 grid((d.cqkv + 255) / 256, B);
+  if (w->act == GDN_BF16) {
+    conv1d_update_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+        d.cqkv, static_cast<const __nv_bfloat16*>(w->conv_weight),
+        static_cast<__nv_bfloat16*>(pool->conv_state), pool->num_slots, pool->status, slot_idx,
+        static_cast<const __nv_bfloat16*>(in), static_cast<__nv_bfloat16*>(out));
+  } else {
+    conv1d_update_kernel<float><<<grid, 256, 0, stream>>>(
+        d.cqkv, static_cast<const float*>(w->conv_weight), static_cast<float*>(pool->conv_state),
+        pool->num_slots, pool->status, slot_idx, static_cast<const float*>(in),
+        static_cast<float*>(out));
+  }
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace gdn

@@ -1,0 +1,41 @@
+// gdn_internal.h -- declarations shared by the host API and the kernel translation units.
+#pragma once
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+int launch_decode(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
+                  const int32_t* slot_idx, int B, const void* qkv, const void* z, const void* a,
+                  const void* b, void* out, cudaStream_t stream);
+
+int launch_conv1d_update(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
+                         const int32_t* slot_idx, int B, const void* in, void* out,
+                         cudaStream_t stream);
+
+struct CompactPairs {
+  int32_t src[GDN_MAX_COMPACT_PAIRS];
+  int32_t dst[GDN_MAX_COMPACT_PAIRS];
+};
+
+int launch_compact(const CompactPairs& pairs, int n, void* rec, size_t rec_slot_bytes, void* conv,
+                   size_t conv_slot_bytes, cudaStream_t stream);
+
+// Workspace carve-up of the chunkwise prefill.
+struct PrefillWs {
+  float* qk;      // [T][Hk][2][dk]   l2-normalised q (scaled) and k
+  float* vu;      // [T][Hv][dv]      v after conv+SiLU, then U~ = T diag(beta) V, then U
+  float* w;       // [T][Hv][dk]      W = T diag(beta e^gamma) K
+  float* gb;      // [T][Hv][2]       (g, beta), g replaced by the in-chunk cumulative gamma
+  float* sc;      // [NCmax][Hv][dk][dv] state at the start of every chunk
+  size_t bytes;
+};
+
+PrefillWs prefill_ws_layout(const KDims& d, int num_seqs, int total_tokens, void* base);
+
+int launch_prefill(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
+                   const int32_t* cu_seqlens, const int32_t* slot_idx, const uint8_t* has_init,
+                   int num_seqs, int total_tokens, const void* qkv, const void* z, const void* a,
+                   const void* b, void* out, const PrefillWs& ws, cudaStream_t stream);
+
+}  // namespace gdn

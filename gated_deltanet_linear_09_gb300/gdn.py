@@ -1,0 +1,185 @@
+"""Thin ctypes binding of libgdn.so (the C ABI declared in include/gdn.h).
+
+Argument marshalling only: every function passes device pointers (``tensor.data_ptr()``),
+sizes and the current CUDA stream to the C entry point of the same name and raises on a
+non-zero return code.  Every step of the computation runs in the library's CUDA kernels.
+There is no fallback: if the library has not been built, or cannot be loaded, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+GDN_F32 = 0
+GDN_BF16 = 1
+GDN_MAX_COMPACT_PAIRS = 2048
+GDN_STATUS_SLOT_RANGE = 1
+GDN_STATUS_BAD_SEQLENS = 2
+
+_CODES = {
+    0: "GDN_OK", -1: "GDN_ERR_INVALID_ARG", -2: "GDN_ERR_UNSUPPORTED_SHAPE",
+    -3: "GDN_ERR_HEAD_DIVISIBILITY", -4: "GDN_ERR_SLOT_RANGE", -5: "GDN_ERR_WORKSPACE_TOO_SMALL",
+    -6: "GDN_ERR_OVERLAP", -7: "GDN_ERR_MISALIGNED", -8: "GDN_ERR_CUDA", -9: "GDN_ERR_TOO_LARGE",
+}
+
+# Every symbol include/gdn.h declares.
+EXPORTED = ("gdn_state_slot_bytes", "gdn_conv1d_update", "gdn_decode_step",
+            "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_state_compact",
+            "gdn_status_string")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed: {_CODES.get(code, code)} ({msg})")
+        self.code = code
+
+
+class gdn_dims(ctypes.Structure):
+    _fields_ = [("num_k_heads", ctypes.c_int32), ("num_v_heads", ctypes.c_int32),
+                ("head_k_dim", ctypes.c_int32), ("head_v_dim", ctypes.c_int32),
+                ("conv_kernel", ctypes.c_int32), ("q_scale", ctypes.c_float),
+                ("l2_eps", ctypes.c_float), ("norm_eps", ctypes.c_float)]
+
+
+class gdn_weights(ctypes.Structure):
+    _fields_ = [("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("conv_weight", ctypes.c_void_p), ("norm_weight", ctypes.c_void_p),
+                ("act", ctypes.c_int)]
+
+
+class gdn_pool(ctypes.Structure):
+    _fields_ = [("rec_state", ctypes.c_void_p), ("conv_state", ctypes.c_void_p),
+                ("num_slots", ctypes.c_int32), ("status", ctypes.c_void_p)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load libgdn.so (optionally building it first).  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libgdn.so is not built ({path}); run __graft_entry__.build() or "
+                           "python -m gated_deltanet_linear_09_gb300.build")
+    lib = ctypes.CDLL(path)
+    lib.gdn_state_slot_bytes.restype = ctypes.c_size_t
+    lib.gdn_state_slot_bytes.argtypes = [_P, ctypes.c_int]
+    lib.gdn_conv1d_update.restype = ctypes.c_int
+    lib.gdn_conv1d_update.argtypes = [_P, _P, _P, _P, _I32, _P, _P, _P]
+    lib.gdn_decode_step.restype = ctypes.c_int
+    lib.gdn_decode_step.argtypes = [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P]
+    lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_prefill_workspace_bytes.argtypes = [_P, _I32, _I32]
+    lib.gdn_prefill_chunked.restype = ctypes.c_int
+    lib.gdn_prefill_chunked.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P,
+                                        _P, ctypes.c_size_t, _P]
+    lib.gdn_state_compact.restype = ctypes.c_int
+    lib.gdn_state_compact.argtypes = [_P, ctypes.c_int, _P, _P, _P, _I32, _P]
+    lib.gdn_status_string.restype = ctypes.c_char_p
+    lib.gdn_status_string.argtypes = [ctypes.c_int]
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise GdnError(fn, rc, load().gdn_status_string(rc).decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def act_code(dtype) -> int:
+    if dtype == torch.bfloat16:
+        return GDN_BF16
+    if dtype == torch.float32:
+        return GDN_F32
+    raise ValueError(f"unsupported activation dtype {dtype}")
+
+
+def make_dims(Hk, Hv, dk, dv, K=4, q_scale=0.0, l2_eps=1e-6, norm_eps=1e-6) -> gdn_dims:
+    return gdn_dims(Hk, Hv, dk, dv, K, q_scale, l2_eps, norm_eps)
+
+
+def make_weights(A_log, dt_bias, conv_weight, norm_weight) -> gdn_weights:
+    return gdn_weights(_ptr(A_log), _ptr(dt_bias), _ptr(conv_weight), _ptr(norm_weight),
+                       act_code(conv_weight.dtype))
+
+
+def make_pool(rec_state, conv_state, status=None) -> gdn_pool:
+    return gdn_pool(_ptr(rec_state), _ptr(conv_state), rec_state.shape[0], _ptr(status))
+
+
+# ---------------------------------------------------------------- the C entry points
+
+def gdn_state_slot_bytes(dims: gdn_dims, act: int) -> int:
+    return int(load().gdn_state_slot_bytes(ctypes.byref(dims), act))
+
+
+def gdn_conv1d_update(dims, weights, pool, slot_idx, qkv_in, qkv_out, stream=None):
+    B = qkv_in.shape[0] if qkv_in is not None else 0
+    _check("gdn_conv1d_update", load().gdn_conv1d_update(
+        ctypes.byref(dims), ctypes.byref(weights), ctypes.byref(pool), _ptr(slot_idx), B,
+        _ptr(qkv_in), _ptr(qkv_out), _stream(stream)))
+
+
+def gdn_decode_step(dims, weights, pool, slot_idx, qkv, z, a, b, out, stream=None):
+    B = slot_idx.shape[0]
+    _check("gdn_decode_step", load().gdn_decode_step(
+        ctypes.byref(dims), ctypes.byref(weights), ctypes.byref(pool), _ptr(slot_idx), B,
+        _ptr(qkv), _ptr(z), _ptr(a), _ptr(b), _ptr(out), _stream(stream)))
+
+
+def gdn_prefill_workspace_bytes(dims, num_seqs: int, total_tokens: int) -> int:
+    return int(load().gdn_prefill_workspace_bytes(ctypes.byref(dims), num_seqs, total_tokens))
+
+
+def gdn_prefill_chunked(dims, weights, pool, cu_seqlens, slot_idx, has_initial_state, num_seqs,
+                        total_tokens, qkv, z, a, b, out, workspace, stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("gdn_prefill_chunked", load().gdn_prefill_chunked(
+        ctypes.byref(dims), ctypes.byref(weights), ctypes.byref(pool), _ptr(cu_seqlens),
+        _ptr(slot_idx), _ptr(has_initial_state), num_seqs, total_tokens, _ptr(qkv), _ptr(z),
+        _ptr(a), _ptr(b), _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def gdn_state_compact(dims, act: int, pool, src_slots, dst_slots, stream=None):
+    src = (ctypes.c_int32 * len(src_slots))(*[int(x) for x in src_slots])
+    dst = (ctypes.c_int32 * len(dst_slots))(*[int(x) for x in dst_slots])
+    if len(src_slots) != len(dst_slots):
+        raise ValueError("src_slots and dst_slots differ in length")
+    _check("gdn_state_compact", load().gdn_state_compact(
+        ctypes.byref(dims), act, ctypes.byref(pool), src, dst, len(src_slots), _stream(stream)))
+
+
+def gdn_status_string(code: int) -> str:
+    return load().gdn_status_string(code).decode()

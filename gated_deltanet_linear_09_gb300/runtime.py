@@ -1,0 +1,88 @@
+"""Device-memory helper around the C ABI: one Gated DeltaNet layer with its slot pool.
+
+Allocation of the weights, the state pool and the prefill workspace happens here (torch owns
+device memory); every computation is a call into libgdn.so through ``gdn``.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import gdn
+from .synth import BF16, Geometry
+
+
+def torch_act(geo: Geometry):
+    return torch.bfloat16 if geo.act == BF16 else torch.float32
+
+
+def to_device(x: np.ndarray, dtype, device="cuda") -> torch.Tensor:
+    """float32 ndarray holding act-dtype values -> device tensor of that dtype (exact)."""
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(device=device, dtype=dtype)
+
+
+class GatedDeltaNetLayer:
+    """Weights, state pool (rec f32 [N][Hv][dk][dv], conv act [N][K-1][Cqkv]) and status word."""
+
+    def __init__(self, geo: Geometry, weights: dict, num_slots: int, device="cuda"):
+        self.geo = geo
+        self.device = device
+        self.act = torch_act(geo)
+        self.dims = gdn.make_dims(geo.Hk, geo.Hv, geo.dk, geo.dv, geo.K, geo.q_scale, geo.l2_eps,
+                                  geo.norm_eps)
+        self.A_log = to_device(weights["A_log"], torch.float32, device)
+        self.dt_bias = to_device(weights["dt_bias"], torch.float32, device)
+        self.conv_w = to_device(weights["conv_w"], self.act, device)
+        self.norm_w = to_device(weights["norm_w"], self.act, device)
+        self.w = gdn.make_weights(self.A_log, self.dt_bias, self.conv_w, self.norm_w)
+        self.rec_state = torch.zeros((num_slots, geo.Hv, geo.dk, geo.dv), dtype=torch.float32,
+                                     device=device)
+        self.conv_state = torch.zeros((num_slots, geo.K - 1, geo.cqkv), dtype=self.act,
+                                      device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.pool = gdn.make_pool(self.rec_state, self.conv_state, self.status)
+        self._ws = None
+
+    @property
+    def num_slots(self) -> int:
+        return self.rec_state.shape[0]
+
+    def load_state(self, rec: np.ndarray, conv: np.ndarray):
+        self.rec_state.copy_(torch.from_numpy(np.ascontiguousarray(rec, np.float32)))
+        self.conv_state.copy_(torch.from_numpy(np.ascontiguousarray(conv, np.float32)).to(self.act))
+
+    def inputs(self, xs: dict) -> dict:
+        return {k: to_device(v, self.act, self.device) for k, v in xs.items()}
+
+    def decode_step(self, slot_idx: torch.Tensor, qkv, z, a, b, out=None, stream=None):
+        if out is None:
+            out = torch.empty((slot_idx.shape[0], self.geo.zdim), dtype=self.act, device=self.device)
+        gdn.gdn_decode_step(self.dims, self.w, self.pool, slot_idx, qkv, z, a, b, out, stream)
+        return out
+
+    def conv1d_update(self, slot_idx: torch.Tensor, qkv_in, out=None, stream=None):
+        if out is None:
+            out = torch.empty_like(qkv_in)
+        gdn.gdn_conv1d_update(self.dims, self.w, self.pool, slot_idx, qkv_in, out, stream)
+        return out
+
+    def workspace(self, num_seqs: int, total_tokens: int) -> torch.Tensor:
+        need = gdn.gdn_prefill_workspace_bytes(self.dims, num_seqs, total_tokens)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+        return self._ws
+
+    def prefill(self, cu_seqlens, slot_idx, has_init, qkv, z, a, b, out=None, stream=None):
+        """cu_seqlens/slot_idx/has_init: device tensors (int32, int32, uint8 or None)."""
+        total = qkv.shape[0]
+        n = slot_idx.shape[0]
+        if out is None:
+            out = torch.empty((total, self.geo.zdim), dtype=self.act, device=self.device)
+        ws = self.workspace(n, total)
+        gdn.gdn_prefill_chunked(self.dims, self.w, self.pool, cu_seqlens, slot_idx, has_init, n,
+                                total, qkv, z, a, b, out, ws, stream)
+        return out
+
+    def compact(self, src, dst, stream=None):
+        gdn.gdn_state_compact(self.dims, gdn.act_code(self.act), self.pool, list(src), list(dst),
+                              stream)

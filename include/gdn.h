@@ -1,0 +1,174 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) Gated DeltaNet layer library (libgdn.so).
+ *
+ * The layer is the linear-attention block of the Qwen3.5 / Qwen3-Next hybrid models:
+ * a causal depthwise conv over the fused [q | k | v] projection channels, l2-normalised
+ * q and k, per-V-head gates g = -exp(A_log) * softplus(a + dt_bias) and
+ * beta = sigmoid(b), the gated delta rule on a per-request dk x dv recurrent state
+ *     S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,   o_t = S_t^T q_t,
+ * and a z-gated RMSNorm over each V-head's output.
+ *
+ * Where the operations are stated:
+ *   "pegainfer issue #1001", Split 2 bullet -- one batched decode call over all decode rows
+ *       through a step-scoped table of per-row state addresses (here: slot_idx);
+ *   "pegainfer issue #1001", Split 3 bullet -- slot-indexed recurrent/conv state with a
+ *       scheduler-owned slot index, device-to-device compaction on retire;
+ *   "pegainfer PR #1003", description bullets -- rank-local head counts fed to the GDR
+ *       decode / conv / chunkwise prefill chains, gated RMSNorm at the local value heads with
+ *       a head-shared norm weight, linear-head divisibility failing closed, state and
+ *       scratch sized from allocation bytes;
+ *   "helexa/cortex commit 95dc874 (tp_qwen3_5)", TpQwen3_5GatedDeltaNet bullet -- the fused
+ *       [q | k | v] channel regions (first key_dim, second key_dim, value_dim), the
+ *       delta-rule loop per V-head, repeat_interleave of K-heads onto V-heads, l2norm,
+ *       softplus and the RmsNormGated tail.
+ *
+ * Conventions shared by every call
+ *   Ownership: the caller owns every buffer.  The library allocates and frees no memory,
+ *     never synchronises the device and launches only on the given stream.
+ *   Pointers: device pointers unless marked "host"; base addresses 16-byte aligned; all
+ *     tensors dense, row-major, in the layouts below.
+ *   Layouts (Cqkv = 2*Hk*dk + Hv*dv, r = Hv/Hk):
+ *     rec_state  f32  [num_slots][Hv][dk][dv]        dv fastest
+ *     conv_state act  [num_slots][K-1][Cqkv]         previous K-1 raw inputs, oldest first
+ *     conv_weight act [Cqkv][K]                      tap K-1 multiplies the current token
+ *     norm_weight act [dv]                           shared by all V-heads
+ *     A_log, dt_bias f32 [Hv]
+ *     qkv act [rows][Cqkv] channels [q heads | k heads | v heads], head-major in each region
+ *     z act [rows][Hv*dv];  a, b act [rows][Hv];  out act [rows][Hv*dv]
+ *     V-head h reads K-head h / r (repeat_interleave).
+ *   Supported: dk, dv in {64, 128}; K = 4; act in {GDN_F32, GDN_BF16}; Hv % Hk == 0.
+ *   Errors: negative return codes (below); nothing is launched when a call fails its host
+ *     checks.  Errors found on the device (a slot index out of range) never trap: the row
+ *     is skipped, its output zeroed, and a bit is OR-ed into *pool->status when that
+ *     optional device word is given.
+ *   Thread safety: no global mutable state; concurrent calls on different streams are safe
+ *     when they touch disjoint slots and buffers.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Return codes. */
+#define GDN_OK 0
+#define GDN_ERR_INVALID_ARG (-1)         /* null pointer, negative size, bad eps, bad dtype   */
+#define GDN_ERR_UNSUPPORTED_SHAPE (-2)   /* dk or dv not in {64,128}, K != 4                 */
+#define GDN_ERR_HEAD_DIVISIBILITY (-3)   /* Hv % Hk != 0 (fails closed)                      */
+#define GDN_ERR_SLOT_RANGE (-4)          /* a host-visible slot index outside [0, num_slots) */
+#define GDN_ERR_WORKSPACE_TOO_SMALL (-5) /* workspace_bytes below the required size          */
+#define GDN_ERR_OVERLAP (-6)             /* duplicate destination slot in a compaction       */
+#define GDN_ERR_MISALIGNED (-7)          /* a base pointer not 16-byte aligned               */
+#define GDN_ERR_CUDA (-8)                /* a CUDA launch failed (see cudaGetLastError)      */
+#define GDN_ERR_TOO_LARGE (-9)           /* a size beyond a documented per-call maximum      */
+
+/* Bits the kernels OR into *gdn_pool.status. */
+#define GDN_STATUS_SLOT_RANGE 1
+#define GDN_STATUS_BAD_SEQLENS 2
+
+/* Rank-local layer geometry ("local_linear_*" head counts of one tensor-parallel rank; one
+ * GPU holds them all here).  q_scale = 0 selects 1/sqrt(head_k_dim).  l2norm divides by
+ * sqrt(sum x^2 + l2_eps); the gated RMSNorm divides by sqrt(mean o^2 + norm_eps). */
+typedef struct {
+  int32_t num_k_heads;
+  int32_t num_v_heads;
+  int32_t head_k_dim;
+  int32_t head_v_dim;
+  int32_t conv_kernel;
+  float q_scale;
+  float l2_eps;
+  float norm_eps;
+} gdn_dims;
+
+/* Layer parameters (device pointers, layouts above). */
+typedef struct {
+  const float* A_log;
+  const float* dt_bias;
+  const void* conv_weight;
+  const void* norm_weight;
+  gdn_dtype act;
+} gdn_weights;
+
+/* The per-request state pool.  status: optional device int32 error word (may be NULL). */
+typedef struct {
+  float* rec_state;
+  void* conv_state;
+  int32_t num_slots;
+  int32_t* status;
+} gdn_pool;
+
+/* Bytes of one slot: recurrent state (f32) plus conv state (act dtype).  Capacity math of
+ * "pegainfer PR #1003" (allocation bytes).  Returns 0 for unsupported geometry. */
+size_t gdn_state_slot_bytes(const gdn_dims* dims, gdn_dtype act);
+
+/* Standalone causal conv1d update (the "conv" chain of "pegainfer PR #1003"):
+ *   qkv_out[i][c] = SiLU( sum_{j<K-1} w[c][j] * conv_state[s][j][c] + w[c][K-1] * qkv_in[i][c] )
+ * with s = slot_idx[i] (device int32[B]); then the slot's conv state is shifted by one and
+ * holds qkv_in[i] as its newest row.  Rows with s < 0 are padding: qkv_out row zeroed, no
+ * state touched.  qkv_in / qkv_out: act [B][Cqkv].  Slots must be distinct across rows. */
+int gdn_conv1d_update(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
+                      const int32_t* slot_idx, int32_t B, const void* qkv_in, void* qkv_out,
+                      cudaStream_t stream);
+
+/* One batched decode step over B rows (the batched GDR decode of "pegainfer issue #1001",
+ * Split 2, with the slot-indexed state of Split 3): for row i with slot s = slot_idx[i]
+ * (device int32[B], values distinct; s < 0 = padding row: output zeroed, no state read or
+ * written), run conv update + SiLU, l2norm of q (times q_scale) and k, the gates, the gated
+ * delta rule on every V-head's state rec_state[s][h], o = S_t^T q, and
+ *   out = o / sqrt(mean(o^2) + norm_eps) * norm_weight * SiLU(z)  (one rounding to act).
+ * qkv act [B][Cqkv]; z act [B][Hv*dv]; a, b act [B][Hv]; out act [B][Hv*dv].  B <= 65535.
+ * One kernel launch; no host reads of device data, so the call can be captured in a CUDA
+ * graph.  An out-of-range s sets GDN_STATUS_SLOT_RANGE and skips the row. */
+int gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
+                    const int32_t* slot_idx, int32_t B, const void* qkv, const void* z,
+                    const void* a, const void* b, void* out, cudaStream_t stream);
+
+/* Workspace bytes gdn_prefill_chunked needs for num_seqs sequences of total_tokens tokens
+ * (the chunkwise scratch, "GdrChunkwiseScratch35" of "pegainfer PR #1003"). */
+size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t num_seqs, int32_t total_tokens);
+
+/* Chunkwise prefill (the chunked prefill chain of "pegainfer PR #1003"): sequence n covers
+ * packed tokens [cu_seqlens[n], cu_seqlens[n+1]) of qkv/z/a/b/out (device int32[num_seqs+1],
+ * non-decreasing, cu_seqlens[0] = 0, cu_seqlens[num_seqs] = total_tokens) and runs every
+ * token through the same layer as gdn_decode_step, in chunks of 64 tokens (WY / UT form of
+ * the gated delta rule).  has_initial_state (device uint8[num_seqs], or NULL = all zero):
+ * 0 starts from zero recurrent and conv state, 1 continues from slot slot_idx[n] (device
+ * int32[num_seqs]).  On return the slot holds the state after the sequence's last token and
+ * its last K-1 raw inputs.  workspace: device, >= gdn_prefill_workspace_bytes(...), 256-byte
+ * aligned, contents undefined on entry and exit.  Several kernels on `stream`; no host reads
+ * of device data. */
+int gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
+                        const int32_t* cu_seqlens, const int32_t* slot_idx,
+                        const uint8_t* has_initial_state, int32_t num_seqs, int32_t total_tokens,
+                        const void* qkv, const void* z, const void* a, const void* b, void* out,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Maximum number of (src, dst) pairs of one gdn_state_compact call. */
+#define GDN_MAX_COMPACT_PAIRS 2048
+
+/* Device-to-device slot compaction on retire ("pegainfer issue #1001", Split 3):
+ *   new[dst_slots[i]] = old[src_slots[i]]   for the recurrent and the conv state,
+ * every source read before any destination is written, so source and destination sets may
+ * overlap (e.g. gathering live slots into a prefix).  src_slots / dst_slots: HOST int32[n],
+ * values in [0, num_slots), destinations distinct (GDN_ERR_OVERLAP otherwise), n <=
+ * GDN_MAX_COMPACT_PAIRS (GDN_ERR_TOO_LARGE).  Slots that are no destination keep their bytes.
+ * Bit-exact copy, one kernel launch, no workspace. */
+int gdn_state_compact(const gdn_dims* dims, gdn_dtype act, const gdn_pool* pool,
+                      const int32_t* src_slots, const int32_t* dst_slots, int32_t n,
+                      cudaStream_t stream);
+
+/* Text for a return code. */
+const char* gdn_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

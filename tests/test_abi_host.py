@@ -1,0 +1,128 @@
+"""CPU-side checks of the C ABI: the library loads, exports every symbol include/gdn.h declares,
+and every host-side argument check returns its documented code without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_deltanet_linear_09_gb300 import build as gbuild
+from gated_deltanet_linear_09_gb300 import gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdn.load()
+
+
+def _declared_functions():
+    txt = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(gdn_\w+)\s*\(", txt, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_functions()
+    assert len(declared) >= 7
+    assert set(declared) == set(gdn.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+    # and they are exported with C linkage from the shared object itself
+    handle = ctypes.CDLL(gdn.lib_path())
+    for name in declared:
+        getattr(handle, name)
+
+
+def D(**kw):
+    base = dict(Hk=16, Hv=32, dk=128, dv=128, K=4)
+    base.update(kw)
+    return gdn.make_dims(base["Hk"], base["Hv"], base["dk"], base["dv"], base["K"])
+
+
+def test_slot_and_workspace_bytes(lib):
+    d = D(Hv=48)
+    # 48 V-heads x 128 x 128 f32 + 3 rows x 10240 channels bf16
+    assert gdn.gdn_state_slot_bytes(d, gdn.GDN_BF16) == 48 * 128 * 128 * 4 + 3 * 10240 * 2
+    assert gdn.gdn_state_slot_bytes(d, gdn.GDN_F32) == 48 * 128 * 128 * 4 + 3 * 10240 * 4
+    assert gdn.gdn_state_slot_bytes(D(Hv=33), gdn.GDN_BF16) == 0       # not divisible
+    assert gdn.gdn_state_slot_bytes(D(dk=96), gdn.GDN_BF16) == 0       # unsupported
+    w1 = gdn.gdn_prefill_workspace_bytes(D(), 1, 4096)
+    w2 = gdn.gdn_prefill_workspace_bytes(D(), 1, 8192)
+    assert 0 < w1 < w2
+    assert w1 % 256 == 0
+    assert gdn.gdn_prefill_workspace_bytes(D(), -1, 10) == 0
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -9):
+        assert gdn.gdn_status_string(code)
+    assert "unknown" in gdn.gdn_status_string(12345)
+
+
+def _call_decode(lib, dims, B=1, aligned=True, null_w=False):
+    # host pointers that are never dereferenced: every case below fails the host checks first
+    fake = 0x10000 if aligned else 0x10008 + 2
+    w = gdn.gdn_weights(0 if null_w else 0x20000, 0x20000, 0x20000, 0x20000, gdn.GDN_BF16)
+    p = gdn.gdn_pool(0x30000, 0x30000, 4, None)
+    return lib.gdn_decode_step(ctypes.byref(dims), ctypes.byref(w), ctypes.byref(p), 0x40000, B,
+                               fake, fake, fake, fake, fake, None)
+
+
+def test_decode_host_checks(lib):
+    assert _call_decode(lib, D(Hv=33)) == -3          # fail closed on head divisibility
+    assert _call_decode(lib, D(dk=96)) == -2
+    assert _call_decode(lib, D(K=3)) == -2
+    assert _call_decode(lib, D(Hk=0)) == -1
+    assert _call_decode(lib, D(), B=-1) == -1
+    assert _call_decode(lib, D(), B=70000) == -9
+    assert _call_decode(lib, D(), B=0) == 0           # empty batch: no-op
+    assert _call_decode(lib, D(), null_w=True) == -1
+    assert _call_decode(lib, D(), aligned=False) == -7
+
+
+def test_prefill_and_compact_host_checks(lib):
+    d = D()
+    w = gdn.gdn_weights(0x20000, 0x20000, 0x20000, 0x20000, gdn.GDN_BF16)
+    p = gdn.gdn_pool(0x30000, 0x30000, 4, None)
+    need = lib.gdn_prefill_workspace_bytes(ctypes.byref(d), 2, 100)
+    f = 0x10000
+    rc = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(w), ctypes.byref(p), f, f, None, 2,
+                                 100, f, f, f, f, f, 0x50000, need - 1, None)
+    assert rc == -5
+    rc = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(w), ctypes.byref(p), f, f, None, 2,
+                                 100, f, f, f, f, f, 0x50000 + 16, need, None)
+    assert rc == -7                                   # workspace must be 256-byte aligned
+    rc = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(w), ctypes.byref(p), f, f, None, 0,
+                                 0, None, None, None, None, None, None, 0, None)
+    assert rc == 0
+    assert lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(w), ctypes.byref(p), f, f, None,
+                                   0, 5, f, f, f, f, f, None, 0, None) == -1
+
+    def compact(src, dst, slots=4):
+        pp = gdn.gdn_pool(0x30000, 0x30000, slots, None)
+        s = (ctypes.c_int32 * len(src))(*src)
+        t = (ctypes.c_int32 * len(dst))(*dst)
+        return lib.gdn_state_compact(ctypes.byref(d), gdn.GDN_BF16, ctypes.byref(pp), s, t,
+                                     len(src), None)
+    assert compact([0, 1], [1, 1]) == -6              # duplicate destination
+    assert compact([0, 4], [1, 2]) == -4              # source out of range
+    assert compact([0, 1], [1, -1]) == -4
+    assert compact([], []) == 0
+    big = list(range(2049))
+    assert compact(big, big, slots=4096) == -9
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The library and its binding never reach the CPU oracle."""
+    pkg = os.path.join(ROOT, "gated_deltanet_linear_09_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        if "_build" in dirpath:
+            continue
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), fn
+                assert "liboracle" not in src and "gdn_oracle" not in src, fn

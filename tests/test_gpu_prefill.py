@@ -1,0 +1,136 @@
+"""GPU parity of the chunkwise prefill against the float64 token-by-token oracle, through the
+C ABI: varlen packing with ragged tails, continuation from a slot's state, the full-size
+T=4096 single sequence (sampled by K-heads), and prefill followed by decode."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_linear_09_gb300 import synth
+from gated_deltanet_linear_09_gb300.runtime import GatedDeltaNetLayer
+from gpu_util import HeadSlice, assert_out_close, assert_state_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from gated_deltanet_linear_09_gb300 import build, gdn
+    build.build()
+    gdn.load()
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy()
+
+
+def _dev_i32(x):
+    return torch.from_numpy(np.asarray(x, np.int32)).cuda()
+
+
+@pytest.mark.parametrize("geo", [
+    synth.Geometry(2, 4, 128, 128, 4, synth.BF16),
+    synth.Geometry(2, 2, 64, 64, 4, synth.F32),
+    synth.Geometry(1, 3, 128, 64, 4, synth.BF16),
+    synth.Geometry(2, 4, 64, 128, 4, synth.F32),
+], ids=lambda g: f"Hk{g.Hk}Hv{g.Hv}dk{g.dk}dv{g.dv}{g.act}")
+def test_prefill_varlen_full_compare(geo):
+    lens = [1, 63, 0, 64, 65, 130, 2, 200]
+    has_init = np.array([0, 1, 1, 0, 1, 0, 1, 1], np.uint8)
+    n = len(lens)
+    N = n + 3
+    w = synth.make_weights(geo, 600)
+    rec, conv = synth.make_pool(geo, N, 601, True)
+    layer = GatedDeltaNetLayer(geo, w, N)
+    layer.load_state(rec, conv)
+    cu = synth.cu_seqlens(lens)
+    slots = np.array([9, 0, 4, 2, 10, 5, 1, 7], np.int32)
+    xs = synth.make_token_inputs(geo, int(cu[-1]), 602)
+    out = layer.prefill(_dev_i32(cu), _dev_i32(slots), torch.from_numpy(has_init).cuda(),
+                        **layer.inputs(xs))
+    r64, c64 = rec.astype(np.float64), conv.astype(np.float64)
+    rc, ref = oracle.prefill(geo.oracle_dims(), f64(w), r64, c64, cu, slots, has_init, **f64(xs))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert_out_close(_np(out), ref, geo.act, "prefill outputs")
+    g_rec, g_conv = _np(layer.rec_state), _np(layer.conv_state)
+    for s in slots:
+        assert_state_close(g_rec[s], r64[s], f"slot {s}")
+        np.testing.assert_array_equal(g_conv[s], c64[s])
+    for s in (3, 6, 8):
+        np.testing.assert_array_equal(g_rec[s], rec[s])
+        np.testing.assert_array_equal(g_conv[s], conv[s])
+    assert int(layer.status.item()) == 0
+
+
+def test_prefill_full_size_T4096_sampled_heads():
+    wl = synth.workloads()[3]
+    geo = wl.geo
+    w = synth.make_weights(geo, wl.seed)
+    layer = GatedDeltaNetLayer(geo, w, wl.num_slots)
+    cu = synth.cu_seqlens(wl.seq_lens)
+    T = int(cu[-1])
+    xs = synth.make_token_inputs(geo, T, wl.seed, 0)
+    slots = np.array([0], np.int32)
+    out = layer.prefill(_dev_i32(cu), _dev_i32(slots), None, **layer.inputs(xs))
+    torch.cuda.synchronize()
+    got = _np(out)
+    g_rec = _np(layer.rec_state)
+    g_conv = _np(layer.conv_state)
+    for k_heads in ([0], [7, 15]):
+        hs = HeadSlice(geo, k_heads)
+        r64 = np.zeros((1, hs.sub.Hv, geo.dk, geo.dv))
+        c64 = np.zeros((1, geo.K - 1, hs.sub.cqkv))
+        rc, ref = oracle.prefill(hs.sub.oracle_dims(), hs.weights(w), r64, c64, cu, slots, None,
+                                 **hs.inputs(xs))
+        assert rc == 0
+        assert_out_close(hs.out_cols(got), ref, geo.act, f"heads {k_heads}")
+        assert_state_close(hs.rec(g_rec)[0], r64[0], f"final state heads {k_heads}")
+        np.testing.assert_array_equal(hs.conv(g_conv)[0], c64[0])
+
+
+def test_prefill_then_decode_continues():
+    geo = synth.Geometry(2, 4, 128, 128, 4, synth.BF16)
+    w = synth.make_weights(geo, 610)
+    T = 150
+    xs = synth.make_token_inputs(geo, T + 1, 611)
+    layer = GatedDeltaNetLayer(geo, w, 3)
+    head = {k: v[:T] for k, v in xs.items()}
+    tail = {k: v[T:] for k, v in xs.items()}
+    layer.prefill(_dev_i32([0, T]), _dev_i32([2]), None, **layer.inputs(head))
+    out = layer.decode_step(_dev_i32([2]), **layer.inputs(tail))
+    r64 = np.zeros((3, geo.Hv, geo.dk, geo.dv))
+    c64 = np.zeros((3, geo.K - 1, geo.cqkv))
+    _, ref = oracle.prefill(geo.oracle_dims(), f64(w), r64, c64, [0, T + 1], [2], None, **f64(xs))
+    torch.cuda.synchronize()
+    assert_out_close(_np(out), ref[T:], geo.act, "decode after prefill")
+    assert_state_close(_np(layer.rec_state)[2], r64[2], "state")
+    np.testing.assert_array_equal(_np(layer.conv_state)[2], c64[2])
+
+
+def test_prefill_bad_slot_and_bad_seqlens():
+    geo = synth.Geometry(1, 2, 64, 64, 4, synth.BF16)
+    w = synth.make_weights(geo, 620)
+    rec, conv = synth.make_pool(geo, 2, 621, True)
+    layer = GatedDeltaNetLayer(geo, w, 2)
+    layer.load_state(rec, conv)
+    xs = synth.make_token_inputs(geo, 70, 622)
+    out = layer.prefill(_dev_i32([0, 30, 70]), _dev_i32([5, 1]), None, **layer.inputs(xs))
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) & 1
+    got = _np(out)
+    assert np.all(got[:30] == 0.0)
+    np.testing.assert_array_equal(_np(layer.rec_state)[0], rec[0])
+    r64, c64 = rec.astype(np.float64), conv.astype(np.float64)
+    _, ref = oracle.prefill(geo.oracle_dims(), f64(w), r64, c64, [0, 30, 70], [5, 1], None,
+                            **f64(xs))
+    assert_out_close(got[30:], ref[30:], geo.act)
+    # decreasing cu_seqlens: reported on the status word, nothing written
+    layer.status.zero_()
+    layer.load_state(rec, conv)
+    sentinel = torch.full((70, geo.zdim), 7.0, dtype=torch.bfloat16, device="cuda")
+    layer.prefill(_dev_i32([0, 50, 40]), _dev_i32([0, 1]), None, out=sentinel, **layer.inputs(xs))
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) & 2
+    assert torch.all(sentinel == 7.0)
+    np.testing.assert_array_equal(_np(layer.rec_state), rec)
