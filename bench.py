@@ -38,7 +38,7 @@ PREFILL_WL = 3
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the decode kernel
 # from one ncu capture at B=64, keyed by the SHA-256 of the kernel source it was taken on.  A
 # changed kernel reports null until it is captured again.
-DECODE_TRAFFIC = {"c8531eb24f993892": 353084928}
+DECODE_TRAFFIC = {"c8531eb24f993892": 353085184}
 
 
 def _src_sha(name: str) -> str:
@@ -130,6 +130,11 @@ def run_ours(args, ws, rank, local):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     hbm_peak, bf16_peak, peak_kind = peaks()
 
+    if args.only == "prefill":
+        p_ms, T = time_prefill(torch, synth, GatedDeltaNetLayer, args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"only": "prefill", "ms": p_ms, "tokens_per_s": T / (p_ms * 1e-3)}))
+        return
     # ---------------- decode, B = 64
     wl = synth.workloads()[DECODE_WL]
     geo = wl.geo
@@ -247,30 +252,13 @@ def run_ours(args, ws, rank, local):
     torch.cuda.empty_cache()
 
     # ---------------- chunked prefill, one sequence of T = 4096
+    p_ms, T = time_prefill(torch, synth, GatedDeltaNetLayer, 10, 3)
     pwl = synth.workloads()[PREFILL_WL]
     pgeo = pwl.geo
-    player = GatedDeltaNetLayer(pgeo, synth.make_weights(pgeo, pwl.seed), pwl.num_slots)
-    T = pwl.seq_lens[0]
-    px = player.inputs(synth.make_token_inputs(pgeo, T, pwl.seed, 0))
-    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
-    psl = torch.tensor([0], dtype=torch.int32, device="cuda")
-    pout = torch.empty((T, pgeo.zdim), dtype=player.act, device="cuda")
-    for _ in range(3):
-        player.prefill(cu, psl, None, px["qkv"], px["z"], px["a"], px["b"], pout)
-    torch.cuda.synchronize()
-    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    preps = 10
-    p0.record(stream)
-    for _ in range(preps):
-        player.prefill(cu, psl, None, px["qkv"], px["z"], px["a"], px["b"], pout)
-    p1.record(stream)
-    torch.cuda.synchronize()
-    p_ms = p0.elapsed_time(p1) / preps
     Hk, Hv, d, C = pgeo.Hk, pgeo.Hv, pgeo.dk, pwl.chunk
     flops = T * (Hv * (8 * C * d + 6 * d * d) + Hk * 4 * C * d)
     p_tflops = flops / (p_ms * 1e-3) / 1e12
     p_bytes = T * (pgeo.cqkv * 2 + pgeo.zdim * 2 * 2 + 2 * Hv * 2) + Hv * d * d * 4
-    del player, px
 
     if rank != 0:
         if dist:
@@ -317,6 +305,29 @@ def run_ours(args, ws, rank, local):
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def time_prefill(torch, synth, GatedDeltaNetLayer, reps, warmup):
+    """Average time of one chunked prefill of the T = 4096 sequence (inputs resident in HBM)."""
+    pwl = synth.workloads()[PREFILL_WL]
+    pgeo = pwl.geo
+    player = GatedDeltaNetLayer(pgeo, synth.make_weights(pgeo, pwl.seed), pwl.num_slots)
+    T = pwl.seq_lens[0]
+    px = player.inputs(synth.make_token_inputs(pgeo, T, pwl.seed, 0))
+    cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+    psl = torch.tensor([0], dtype=torch.int32, device="cuda")
+    pout = torch.empty((T, pgeo.zdim), dtype=player.act, device="cuda")
+    for _ in range(warmup):
+        player.prefill(cu, psl, None, px["qkv"], px["z"], px["a"], px["b"], pout)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(reps):
+        player.prefill(cu, psl, None, px["qkv"], px["z"], px["a"], px["b"], pout)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    return p0.elapsed_time(p1) / reps, T
 
 
 # ------------------------------------------------------------------------------ oracle timing
@@ -397,7 +408,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="all", choices=["all", "decode"],
+    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill"],
                     help="decode: only the B=64 decode timing (used for profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -30,7 +30,8 @@ _CODES = {
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_state_slot_bytes", "gdn_conv1d_update", "gdn_decode_step",
             "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_state_compact",
-            "gdn_status_string")
+            "gdn_status_string", "gdn_prefill_chunked_noalloc")
+GDN_NOALLOC_PREFILL_SCRATCH_BYTES = 64 << 20
 
 
 class GdnError(RuntimeError):
@@ -89,6 +90,9 @@ def load(build_if_missing: bool = False):
     lib.gdn_prefill_chunked.restype = ctypes.c_int
     lib.gdn_prefill_chunked.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P,
                                         _P, ctypes.c_size_t, _P]
+    lib.gdn_prefill_chunked_noalloc.restype = ctypes.c_int
+    lib.gdn_prefill_chunked_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _P, _P, _P, _P,
+                                                _P, _P]
     lib.gdn_state_compact.restype = ctypes.c_int
     lib.gdn_state_compact.argtypes = [_P, ctypes.c_int, _P, _P, _P, _I32, _P]
     lib.gdn_status_string.restype = ctypes.c_char_p
@@ -170,6 +174,15 @@ def gdn_prefill_chunked(dims, weights, pool, cu_seqlens, slot_idx, has_initial_s
         ctypes.byref(dims), ctypes.byref(weights), ctypes.byref(pool), _ptr(cu_seqlens),
         _ptr(slot_idx), _ptr(has_initial_state), num_seqs, total_tokens, _ptr(qkv), _ptr(z),
         _ptr(a), _ptr(b), _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def gdn_prefill_chunked_noalloc(dims, weights, pool, cu_seqlens, slot_idx, has_initial_state,
+                                num_seqs, total_tokens, qkv, z, a, b, out, stream=None):
+    """Prefill whose scratch is the library's fixed device array: allocates nothing."""
+    _check("gdn_prefill_chunked_noalloc", load().gdn_prefill_chunked_noalloc(
+        ctypes.byref(dims), ctypes.byref(weights), ctypes.byref(pool), _ptr(cu_seqlens),
+        _ptr(slot_idx), _ptr(has_initial_state), num_seqs, total_tokens, _ptr(qkv), _ptr(z),
+        _ptr(a), _ptr(b), _ptr(out), _stream(stream)))
 
 
 def gdn_state_compact(dims, act: int, pool, src_slots, dst_slots, stream=None):

@@ -150,6 +150,30 @@ int gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, const gdn_po
                         const void* qkv, const void* z, const void* a, const void* b, void* out,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Size of the fixed device scratch array behind gdn_prefill_chunked_noalloc (64 MiB). */
+#define GDN_NOALLOC_PREFILL_SCRATCH_BYTES (64u << 20)
+
+/* Allocation-free variant of gdn_prefill_chunked (the pages have no counterpart: this serves
+ * callers that cannot allocate device memory -- code running inside an allocator or memory
+ * pool callback, a server that reserved all HBM for state slots at start-up, or a host
+ * runtime that hands out raw pointers only).  Same arguments and results as
+ * gdn_prefill_chunked minus the workspace: the scratch is a file-scope static __device__
+ * array of GDN_NOALLOC_PREFILL_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits.  The call itself allocates and frees nothing.
+ *   Size limit: returns GDN_ERR_TOO_LARGE, launching nothing, when
+ *     gdn_prefill_workspace_bytes(dims, num_seqs, total_tokens) > GDN_NOALLOC_PREFILL_SCRATCH_BYTES.
+ *   First call per device: looks up the array's device address (cudaGetSymbolAddress, with that
+ *     device current) and caches it; make that first call before any stream capture.
+ *   Sharing: every call uses the same array, which keeps the last call's contents; the prefill
+ *     writes every scratch value before it reads it, so nothing needs clearing.  Calls whose
+ *     kernels overlap on the GPU (other streams, other host threads) race on the array:
+ *     serialise them. */
+int gdn_prefill_chunked_noalloc(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
+                                const int32_t* cu_seqlens, const int32_t* slot_idx,
+                                const uint8_t* has_initial_state, int32_t num_seqs,
+                                int32_t total_tokens, const void* qkv, const void* z,
+                                const void* a, const void* b, void* out, cudaStream_t stream);
+
 /* Maximum number of (src, dst) pairs of one gdn_state_compact call. */
 #define GDN_MAX_COMPACT_PAIRS 2048
 
