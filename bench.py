@@ -294,7 +294,7 @@ def run_ours(args, ws, rank, local):
                     "roofline": {"bound": "tensor", "achieved": round(p_tflops, 3),
                                  "peak": bf16_peak, "unit": "TFLOP/s",
                                  "frac": round(p_tflops / bf16_peak, 5), "peak_kind": peak_kind},
-                    "io_bytes": p_bytes, "launches_per_call": 4},
+                    "io_bytes": p_bytes, "launches_per_call": 2},
         "compact": {"pairs": len(keep), "bytes": comp_bytes, "ms": round(comp_ms, 4),
                     "gbs": round(comp_bytes / (comp_ms * 1e-3) / 1e9, 1),
                     "hbm_frac": round(comp_bytes / (comp_ms * 1e-3) / 1e9 / hbm_peak, 4)},

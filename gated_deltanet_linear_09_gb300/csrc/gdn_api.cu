@@ -100,6 +100,7 @@ int gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* 
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t num_seqs, int32_t total_tokens) {
   gdn::KDims d;
   if (check_dims(dims, &d) != GDN_OK || num_seqs < 0 || total_tokens < 0) return 0;
+  if (gdn::prefill_tc_supported(d)) return gdn::prefill_tc_ws_bytes(d, num_seqs, total_tokens);
   return gdn::prefill_ws_layout(d, num_seqs, total_tokens, nullptr).bytes;
 }
 
@@ -120,9 +121,14 @@ int gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, const gdn_po
   if (total_tokens > 0 && (!qkv || !z || !a || !b || !out)) return GDN_ERR_INVALID_ARG;
   if (total_tokens > 0 && (!aligned16(qkv) || !aligned16(z) || !aligned16(out)))
     return GDN_ERR_MISALIGNED;
-  const gdn::PrefillWs need = gdn::prefill_ws_layout(d, num_seqs, total_tokens, nullptr);
-  if (!workspace || workspace_bytes < need.bytes) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  const bool tc = gdn::prefill_tc_supported(d);
+  const size_t need = tc ? gdn::prefill_tc_ws_bytes(d, num_seqs, total_tokens)
+                         : gdn::prefill_ws_layout(d, num_seqs, total_tokens, nullptr).bytes;
+  if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE_TOO_SMALL;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_MISALIGNED;
+  if (tc)
+    return gdn::launch_prefill_tc(d, w, pool, cu_seqlens, slot_idx, has_initial_state, num_seqs,
+                                  total_tokens, qkv, z, a, b, out, workspace, stream);
   const gdn::PrefillWs ws = gdn::prefill_ws_layout(d, num_seqs, total_tokens, workspace);
   return gdn::launch_prefill(d, w, pool, cu_seqlens, slot_idx, has_initial_state, num_seqs,
                              total_tokens, qkv, z, a, b, out, ws, stream);

@@ -38,4 +38,12 @@ int launch_prefill(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
                    int num_seqs, int total_tokens, const void* qkv, const void* z, const void* a,
                    const void* b, void* out, const PrefillWs& ws, cudaStream_t stream);
 
+// Tensor-core (tcgen05) prefill for dk = dv = 128.
+bool prefill_tc_supported(const KDims& d);
+size_t prefill_tc_ws_bytes(const KDims& d, int num_seqs, int total_tokens);
+int launch_prefill_tc(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
+                      const int32_t* cu_seqlens, const int32_t* slot_idx, const uint8_t* has_init,
+                      int num_seqs, int total_tokens, const void* qkv, const void* z, const void* a,
+                      const void* b, void* out, void* ws, cudaStream_t stream);
+
 }  // namespace gdn

@@ -1,0 +1,875 @@
+// gdn_prefill_tc.cu -- chunkwise prefill on the sm_103a tensor cores (tcgen05 + TMEM), for
+// head dims dk = dv = 128.
+//
+// Same chunk algebra as the CUDA-core path (UT transform of the gated delta rule; Yang et al.,
+// "Parallelizing Linear Transformers with the Delta Rule over Sequence Length", NeurIPS 2024,
+// section 3; chunked prefill chain and its scratch from "pegainfer PR #1003"), arranged so that
+// every tensor-core product has M = 128 by working with transposed state S^T (dv x dk):
+//
+//   intra kernel (chunk x V-head, all in parallel):
+//     conv + SiLU + l2norm + gates of the chunk's 64 tokens,
+//     D1 = [K;Q] K^T                     -> A = beta_i e^{g_i-g_j} KK^T (j<i),  P = QK^T o Gamma
+//     T  = (I + A)^{-1}                  (blocked 16 x 16 forward substitution, CUDA cores)
+//     D2 = (beta e^gamma K)^T T^T, (beta V)^T T^T   -> W, U~
+//     writes Q~ = e^gamma Q, W, K~ = e^{gamma_L - gamma} K, U~, P, e^{gamma_L}  (f32)
+//   state kernel (sequence x V-head, serial over the chunks, S^T held in TMEM):
+//     D3 = S^T [Q~^T | W^T]              -> (Q~ S)^T, (W S)^T
+//     U^T = U~^T - (W S)^T
+//     S^T <- e^{gamma_L} S^T + U^T K~ ;  O^T = (Q~ S)^T + U^T P^T   (one MMA group, N = 192)
+//     z-gated RMSNorm of O -> out
+//
+// Precision: every product runs as three bf16 passes on split operands
+// (x = hi + lo, hi = bf16(x), lo = bf16(x - hi): A_hi B_hi + A_hi B_lo + A_lo B_hi) with f32
+// accumulation in TMEM, which keeps about 16 significant bits per operand.
+#include "gdn_internal.h"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int CH = 64;
+constexpr int D = 128;
+
+// Per (chunk, V-head) record of the workspace, in floats.
+constexpr int R_QT = 0;                  // [64][128] Q~ rows
+constexpr int R_WR = R_QT + CH * D;      // [64][128] W rows
+constexpr int R_KT = R_WR + CH * D;      // [64][128] K~ rows
+constexpr int R_UT = R_KT + CH * D;      // [64][128] U~ rows
+constexpr int R_PM = R_UT + CH * D;      // [64][64]  P rows
+constexpr int R_SC = R_PM + CH * CH;     // e^{gamma_L}
+constexpr int REC = R_SC + 64;           // 147,712 bytes (multiple of 256)
+
+__device__ __forceinline__ void bar_sync_main() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+// Bounded wait shared by every thread of the CTA: after one timeout the CTA stops waiting and
+// stops issuing work (control flow stays uniform so that every barrier is still reached).
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              int32_t* status) {
+  if (*abort) return false;
+  if (tc::mbar_wait(bar, parity)) return true;
+  *abort = 1;
+  set_status(status, GDN_STATUS_TIMEOUT);
+  return false;
+}
+
+// Packs 8 floats as split bf16 hi / lo 16-byte units.
+__device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
+  __nv_bfloat16 h[8], l[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) tc::split_bf16(v[q], h[q], l[q]);
+  hi = *reinterpret_cast<const uint4*>(h);
+  lo = *reinterpret_cast<const uint4*>(l);
+}
+
+__device__ __forceinline__ void st_unit(unsigned char* tile, uint32_t off, const uint4& v) {
+  *reinterpret_cast<uint4*>(tile + off) = v;
+}
+
+// Warp-wide: global chunk -> (sequence, first token, length); false if cu_seqlens is invalid.
+__device__ bool find_chunk(const int32_t* __restrict__ cu, int num_seqs, int total, int c, int& seq,
+                           int& t0, int& len, int& seq_start) {
+  const int lane = threadIdx.x & 31;
+  bool ok = (__ldg(cu) == 0) && (__ldg(cu + num_seqs) == total);
+  int base = 0;
+  seq = -1;
+  for (int n0 = 0; n0 < num_seqs; n0 += 32) {
+    const int n = n0 + lane;
+    int lo = 0, hi = 0, nch = 0;
+    if (n < num_seqs) {
+      lo = __ldg(cu + n);
+      hi = __ldg(cu + n + 1);
+      if (hi < lo) ok = false;
+      else nch = (hi - lo + CH - 1) / CH;
+    }
+    int incl = nch;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const bool mine = (n < num_seqs) && (c >= base + incl - nch) && (c < base + incl);
+    const unsigned m = __ballot_sync(0xffffffffu, mine);
+    if (m && seq < 0) {
+      const int src = __ffs(m) - 1;
+      seq = __shfl_sync(0xffffffffu, n, src);
+      seq_start = __shfl_sync(0xffffffffu, lo, src);
+      const int hi_s = __shfl_sync(0xffffffffu, hi, src);
+      const int ex = __shfl_sync(0xffffffffu, base + incl - nch, src);
+      t0 = seq_start + (c - ex) * CH;
+      len = min(CH, hi_s - t0);
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ bool seq_chunk_offset(const int32_t* __restrict__ cu, int num_seqs, int total, int seq,
+                                 int& off) {
+  const int lane = threadIdx.x & 31;
+  bool ok = (__ldg(cu) == 0) && (__ldg(cu + num_seqs) == total);
+  int acc = 0;
+  for (int n0 = 0; n0 < num_seqs; n0 += 32) {
+    const int n = n0 + lane;
+    if (n < num_seqs) {
+      const int lo = __ldg(cu + n), hi = __ldg(cu + n + 1);
+      if (hi < lo) ok = false;
+      else if (n < seq) acc += (hi - lo + CH - 1) / CH;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  off = acc;
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ================================================================== intra-chunk kernel
+
+constexpr int XS = 132;   // row stride (floats) of the f32 staging tile
+constexpr int AS = 65;    // row stride of the A / T matrices
+
+struct IntraSmem {
+  static constexpr uint32_t A1 = 0;                    // hi [128x128] then lo
+  static constexpr uint32_t A2A = A1 + 2 * 32768;      // (beta e^g K)^T, hi then lo [128x64]
+  static constexpr uint32_t A2B = A2A + 2 * 16384;     // (beta V)^T
+  static constexpr uint32_t B2 = A2B + 2 * 16384;      // T rows [64x64]
+  static constexpr uint32_t X = B2 + 2 * 8192;         // f32 [64][XS]
+  static constexpr uint32_t AM = X + 4 * 64 * XS;      // f32 [64][AS]
+  static constexpr uint32_t TM = AM + 4 * 64 * AS;     // f32 [64][AS]
+  static constexpr uint32_t MT = TM + 4 * 64 * AS;     // f32 [3][256]
+  static constexpr uint32_t VEC = MT + 4 * 3 * 256;    // f32 gam, bet, eg, dec, bgk [5][64]
+  static constexpr uint32_t BAR = VEC + 4 * 5 * 64;    // mbarrier
+  static constexpr uint32_t MISC = BAR + 16;           // tmem slot, flags
+  static constexpr uint32_t BYTES = MISC + 64;
+};
+
+// conv + SiLU of 128 channels [cb, cb+128) over the chunk's tokens into X (rows >= L zero).
+template <typename T>
+__device__ __forceinline__ void conv_group(const KDims& d, const T* __restrict__ qkv,
+                                           const T* __restrict__ conv_w, const T* __restrict__ cs,
+                                           bool init, int cb, int seq_start, int seq_len,
+                                           int t0, int L, float* X) {
+  const int tid = threadIdx.x;
+  const int f = tid & 127, half = tid >> 7;
+  const int ch = cb + f;
+  const float w0 = Act<T>::ldg(conv_w + (size_t)ch * 4 + 0), w1 = Act<T>::ldg(conv_w + (size_t)ch * 4 + 1);
+  const float w2 = Act<T>::ldg(conv_w + (size_t)ch * 4 + 2), w3 = Act<T>::ldg(conv_w + (size_t)ch * 4 + 3);
+  const int i0 = half * 32;
+  const int p0 = (t0 - seq_start) + i0;   // position of token i0 inside its sequence
+  // raw input at position p of the sequence: the slot's conv state before it, zero past its end
+  auto fetch = [&](int p) -> float {
+    if (p >= seq_len) return 0.f;
+    if (p >= 0) return Act<T>::ldg(qkv + (size_t)(seq_start + p) * d.cqkv + ch);
+    return init ? Act<T>::ldg(cs + (size_t)(3 + p) * d.cqkv + ch) : 0.f;
+  };
+  float xm3 = fetch(p0 - 3), xm2 = fetch(p0 - 2), xm1 = fetch(p0 - 1);
+  float xs[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) xs[k] = (i0 + k < L) ? Act<T>::ldg(qkv + (size_t)(seq_start + p0 + k) * d.cqkv + ch) : 0.f;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    float acc = w3 * xs[k];
+    acc = fmaf(w0, xm3, acc);
+    acc = fmaf(w1, xm2, acc);
+    acc = fmaf(w2, xm1, acc);
+    X[(i0 + k) * XS + f] = (i0 + k < L) ? siluf_(acc) : 0.f;
+    xm3 = xm2;
+    xm2 = xm1;
+    xm1 = xs[k];
+  }
+}
+
+// Per-row l2 normalisation of X (64 rows x 128), times scale.
+__device__ __forceinline__ void l2norm_rows(float* X, float eps, float scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < CH; i += 8) {
+    float v[4], ss = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      v[m] = X[i * XS + lane + 32 * m];
+      ss = fmaf(v[m], v[m], ss);
+    }
+    ss = warp_sum(ss);
+    const float inv = scale / sqrtf(ss + eps);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) X[i * XS + lane + 32 * m] = v[m] * inv;
+  }
+}
+
+// Rows of X -> K-major tile rows [row0, row0+64) of a 128-column tile (hi / lo).
+__device__ __forceinline__ void x_rows_to_tile(const float* X, unsigned char* hi, unsigned char* lo,
+                                               int row0) {
+  const int t = threadIdx.x;
+  const int r = t >> 2, kq = t & 3;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const int kg = kq * 4 + g;
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = X[r * XS + kg * 8 + q];
+    uint4 h, l;
+    split8(v, h, l);
+    const uint32_t off = tc::kmajor_off(row0 + r, kg * 8, 128);
+    st_unit(hi, off, h);
+    st_unit(lo, off, l);
+  }
+}
+
+// Columns of X scaled per token -> K-major tile [128 features][64 tokens] (hi / lo).
+__device__ __forceinline__ void x_cols_to_tile(const float* X, const float* scale,
+                                               unsigned char* hi, unsigned char* lo) {
+  const int t = threadIdx.x;
+  const int f = t & 127, jh = t >> 7;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const int jg = jh * 4 + g;
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = X[(jg * 8 + q) * XS + f] * scale[jg * 8 + q];
+    uint4 h, l;
+    split8(v, h, l);
+    const uint32_t off = tc::kmajor_off(f, jg * 8, 64);
+    st_unit(hi, off, h);
+    st_unit(lo, off, l);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256, 1)
+tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict__ dt_bias,
+                const T* __restrict__ conv_w, const T* __restrict__ conv_state, int num_slots,
+                const int32_t* __restrict__ cu, const int32_t* __restrict__ slot_idx,
+                const uint8_t* __restrict__ has_init, int num_seqs, int total,
+                const T* __restrict__ qkv, const T* __restrict__ a, const T* __restrict__ b,
+                float* __restrict__ ws, int32_t* __restrict__ status) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  using S = IntraSmem;
+  unsigned char* a1h = sm + S::A1;
+  unsigned char* a1l = a1h + 32768;
+  unsigned char* a2ah = sm + S::A2A;
+  unsigned char* a2al = a2ah + 16384;
+  unsigned char* a2bh = sm + S::A2B;
+  unsigned char* a2bl = a2bh + 16384;
+  unsigned char* b2h = sm + S::B2;
+  unsigned char* b2l = b2h + 8192;
+  float* X = reinterpret_cast<float*>(sm + S::X);
+  float* Am = reinterpret_cast<float*>(sm + S::AM);
+  float* Tm = reinterpret_cast<float*>(sm + S::TM);
+  float* Mt = reinterpret_cast<float*>(sm + S::MT);
+  float* gam = reinterpret_cast<float*>(sm + S::VEC);
+  float* bet = gam + 64;
+  float* eg = bet + 64;
+  float* dec = eg + 64;
+  float* bgk = dec + 64;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S::BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
+  int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);   // ok, t0, L, seq, seq_start, abort
+
+  const int c = blockIdx.x, h = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 0) {
+    int seq, t0 = 0, len = 0, ss = 0;
+    const bool ok = find_chunk(cu, num_seqs, total, c, seq, t0, len, ss);
+    if (lane == 0 && !ok && c == 0 && h == 0) set_status(status, GDN_STATUS_BAD_SEQLENS);
+    if (lane == 0) {
+      sh[0] = ok && seq >= 0;
+      sh[1] = t0;
+      sh[2] = len;
+      sh[3] = seq;
+      sh[4] = ss;
+      sh[5] = 0;
+    }
+  }
+  __syncthreads();
+  if (!sh[0]) return;
+  const int t0 = sh[1], L = sh[2], seq = sh[3], seq_start = sh[4];
+  const int seq_len = __ldg(cu + seq + 1) - seq_start;
+  volatile int* abort = sh + 5;
+  const int s = __ldg(slot_idx + seq);
+  const bool valid = s >= 0 && s < num_slots;
+  const bool init = valid && has_init != nullptr && __ldg(has_init + seq) != 0;
+  const T* cs = conv_state + (size_t)(valid ? s : 0) * 3 * d.cqkv;
+  const int kh = h / d.r;
+  float* rec = ws + ((size_t)c * d.Hv + h) * REC;
+
+  if (tid == 0) {
+    tc::mbar_init(bar, 1);
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) tc::tmem_alloc(tslot, 256);
+
+  // ---- gates of the chunk: gamma (cumulative g), beta and the derived per-token scales
+  if (warp == 0) {
+    float g2[2], b2[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int i = 2 * lane + q;
+      g2[q] = 0.f;
+      b2[q] = 0.f;
+      if (i < L) {
+        gates(__ldg(A_log + h), __ldg(dt_bias + h), Act<T>::ldg(a + (size_t)(t0 + i) * d.Hv + h),
+              Act<T>::ldg(b + (size_t)(t0 + i) * d.Hv + h), g2[q], b2[q]);
+      }
+    }
+    const float pair = g2[0] + g2[1];
+    float incl = pair;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const float ex = incl - pair;
+    gam[2 * lane] = ex + g2[0];
+    gam[2 * lane + 1] = ex + g2[0] + g2[1];
+    bet[2 * lane] = b2[0];
+    bet[2 * lane + 1] = b2[1];
+  }
+  __syncthreads();
+  const float gL = gam[L - 1];
+  if (tid < CH) {
+    eg[tid] = expf(gam[tid]);
+    dec[tid] = tid < L ? expf(gL - gam[tid]) : 0.f;
+    bgk[tid] = bet[tid] * expf(gam[tid]);
+  }
+
+  // ---- K: conv, l2norm, A1 rows 0-63, (beta e^g K)^T, K~ rows
+  conv_group<T>(d, qkv, conv_w, cs, init, d.Hk * D + kh * D, seq_start, seq_len, t0, L, X);
+  __syncthreads();
+  l2norm_rows(X, d.l2_eps, 1.0f);
+  __syncthreads();
+  x_rows_to_tile(X, a1h, a1l, 0);
+  x_cols_to_tile(X, bgk, a2ah, a2al);
+  for (int idx = tid; idx < CH * D; idx += 256) {
+    const int j = idx >> 7;
+    rec[R_KT + idx] = X[j * XS + (idx & 127)] * dec[j];
+  }
+  __syncthreads();
+  // ---- Q: conv, l2norm (times q_scale), A1 rows 64-127, Q~ rows
+  conv_group<T>(d, qkv, conv_w, cs, init, kh * D, seq_start, seq_len, t0, L, X);
+  __syncthreads();
+  l2norm_rows(X, d.l2_eps, d.q_scale);
+  __syncthreads();
+  x_rows_to_tile(X, a1h, a1l, 64);
+  for (int idx = tid; idx < CH * D; idx += 256) {
+    const int i = idx >> 7;
+    rec[R_QT + idx] = X[i * XS + (idx & 127)] * eg[i];
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tb = *tslot;
+  // ---- D1 = [K;Q] K^T  (cols [0,64))
+  if (tid == 0) {
+    const uint32_t id = tc::idesc_bf16(128, 64);
+    const uint32_t ah = tc::smem_u32(a1h), al = tc::smem_u32(a1l);
+    for (int k = 0; k < 8; ++k) {
+      tc::mma_bf16(tb, tc::kstep_desc(ah, 128, k), tc::kstep_desc(ah, 128, k), id, k > 0);
+      tc::mma_bf16(tb, tc::kstep_desc(ah, 128, k), tc::kstep_desc(al, 128, k), id, 1);
+      tc::mma_bf16(tb, tc::kstep_desc(al, 128, k), tc::kstep_desc(ah, 128, k), id, 1);
+    }
+    tc::mma_commit(bar);
+  }
+  // ---- V (overlaps the MMA): conv, (beta V)^T
+  conv_group<T>(d, qkv, conv_w, cs, init, 2 * d.Hk * D + h * D, seq_start, seq_len, t0, L, X);
+  __syncthreads();
+  x_cols_to_tile(X, bet, a2bh, a2bl);
+  // ---- A and P from D1
+  wait_or_abort(bar, 0, abort, status);
+  tc::fence_after_sync();
+  if (warp < 4) {
+    const int r = warp * 32 + lane;
+    float v[64];
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16) tc::tmem_ld16(tc::taddr(tb, warp * 32, c0), v + c0);
+    if (r < 64) {
+      const int i = r;
+      const float gi = gam[i], bi = bet[i];
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        Am[i * AS + j] = (j < i && i < L) ? bi * expf(gi - gam[j]) * v[j] : 0.f;
+    } else {
+      const int i = r - 64;
+      const float gi = gam[i];
+      float* prow = rec + R_PM + i * 64;
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        float4 p;
+        p.x = (j + 0 <= i && i < L) ? v[j + 0] * expf(gi - gam[j + 0]) : 0.f;
+        p.y = (j + 1 <= i && i < L) ? v[j + 1] * expf(gi - gam[j + 1]) : 0.f;
+        p.z = (j + 2 <= i && i < L) ? v[j + 2] * expf(gi - gam[j + 2]) : 0.f;
+        p.w = (j + 3 <= i && i < L) ? v[j + 3] * expf(gi - gam[j + 3]) : 0.f;
+        *reinterpret_cast<float4*>(prow + j) = p;
+      }
+    }
+  }
+  // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks per warp, then the off-diagonal blocks
+  for (int idx = tid; idx < 64 * AS; idx += 256) Tm[idx] = 0.f;
+  __syncthreads();
+  if (warp < 4 && lane < 16) {
+    const int b0 = warp * 16, col = lane;
+    float tcol[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float v = (i == col) ? 1.f : 0.f;
+#pragma unroll
+      for (int j = 0; j < i; ++j) v = fmaf(-Am[(b0 + i) * AS + b0 + j], tcol[j], v);
+      tcol[i] = (i >= col) ? v : 0.f;
+      Tm[(b0 + i) * AS + b0 + col] = tcol[i];
+    }
+  }
+  __syncthreads();
+  for (int dd = 1; dd < 4; ++dd) {
+    const int nblk = 4 - dd;
+    for (int idx = tid; idx < nblk * 256; idx += 256) {
+      const int j = idx >> 8, i = j + dd, r = (idx >> 4) & 15, cc = idx & 15;
+      float sacc = 0.f;
+      for (int k = j; k < i; ++k)
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          sacc = fmaf(Am[(16 * i + r) * AS + 16 * k + x], Tm[(16 * k + x) * AS + 16 * j + cc], sacc);
+      Mt[idx] = sacc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nblk * 256; idx += 256) {
+      const int j = idx >> 8, i = j + dd, r = (idx >> 4) & 15, cc = idx & 15;
+      float sacc = 0.f;
+#pragma unroll
+      for (int x = 0; x < 16; ++x)
+        sacc = fmaf(Tm[(16 * i + r) * AS + 16 * i + x], Mt[(j << 8) + x * 16 + cc], sacc);
+      Tm[(16 * i + r) * AS + 16 * j + cc] = -sacc;
+    }
+    __syncthreads();
+  }
+  // ---- B2 = T rows (K-major, 64 x 64)
+  {
+    const int i = tid >> 2, kq = tid & 3;
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+      const int kg = kq * 2 + g;
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = Tm[i * AS + kg * 8 + q];
+      uint4 hh, ll;
+      split8(v, hh, ll);
+      const uint32_t off = tc::kmajor_off(i, kg * 8, 64);
+      st_unit(b2h, off, hh);
+      st_unit(b2l, off, ll);
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  // ---- D2a = (beta e^g K)^T T^T = W^T (cols [64,128)),  D2b = (beta V)^T T^T = U~^T ([128,192))
+  if (tid == 0 && !*abort) {
+    const uint32_t id = tc::idesc_bf16(128, 64);
+    const uint32_t bh = tc::smem_u32(b2h), bl = tc::smem_u32(b2l);
+    const uint32_t srcs[2][2] = {{tc::smem_u32(a2ah), tc::smem_u32(a2al)},
+                                 {tc::smem_u32(a2bh), tc::smem_u32(a2bl)}};
+    for (int m = 0; m < 2; ++m) {
+      const uint32_t dt = tb + 64 + 64 * m;
+      for (int k = 0; k < 4; ++k) {
+        tc::mma_bf16(dt, tc::kstep_desc(srcs[m][0], 64, k), tc::kstep_desc(bh, 64, k), id, k > 0);
+        tc::mma_bf16(dt, tc::kstep_desc(srcs[m][0], 64, k), tc::kstep_desc(bl, 64, k), id, 1);
+        tc::mma_bf16(dt, tc::kstep_desc(srcs[m][1], 64, k), tc::kstep_desc(bh, 64, k), id, 1);
+      }
+    }
+    tc::mma_commit(bar);
+  }
+  wait_or_abort(bar, 1, abort, status);
+  tc::fence_after_sync();
+  if (warp < 4) {
+    const int r = warp * 32 + lane;   // feature index (dk for W, dv for U~)
+    float v[64];
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16) tc::tmem_ld16(tc::taddr(tb, warp * 32, 64 + c0), v + c0);
+#pragma unroll
+    for (int i = 0; i < 64; ++i) rec[R_WR + i * D + r] = v[i];
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16) tc::tmem_ld16(tc::taddr(tb, warp * 32, 128 + c0), v + c0);
+#pragma unroll
+    for (int i = 0; i < 64; ++i) rec[R_UT + i * D + r] = v[i];
+  }
+  if (tid == 0) rec[R_SC] = expf(gL);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tb, 256);
+}
+
+// ================================================================== serial state kernel
+
+struct StateSmem {
+  static constexpr uint32_t A3 = 0;                 // S^T   [128 x 128] hi then lo
+  static constexpr uint32_t B3 = A3 + 2 * 32768;    // [Q~ ; W] rows [128 x 128]
+  static constexpr uint32_t A4 = B3 + 2 * 32768;    // U^T   [128 x 64]
+  static constexpr uint32_t B4 = A4 + 2 * 16384;    // [K~^T ; P] rows [192 x 64]
+  static constexpr uint32_t PART = B4 + 2 * 24576;  // f32 [4][64] partial sums of squares
+  static constexpr uint32_t INV = PART + 4 * 4 * 64; // f32 [64]
+  static constexpr uint32_t BAR = INV + 4 * 64;     // 4 mbarriers
+  static constexpr uint32_t MISC = BAR + 32;
+  static constexpr uint32_t BYTES = MISC + 64;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256, 1)
+tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_state,
+                T* __restrict__ conv_state, int num_slots, const int32_t* __restrict__ cu,
+                const int32_t* __restrict__ slot_idx, const uint8_t* __restrict__ has_init,
+                int num_seqs, int total, const T* __restrict__ qkv, const T* __restrict__ z,
+                T* __restrict__ out, const float* __restrict__ ws, int32_t* __restrict__ status) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  using S = StateSmem;
+  unsigned char* a3h = sm + S::A3;
+  unsigned char* a3l = a3h + 32768;
+  unsigned char* b3h = sm + S::B3;
+  unsigned char* b3l = b3h + 32768;
+  unsigned char* a4h = sm + S::A4;
+  unsigned char* a4l = a4h + 16384;
+  unsigned char* b4h = sm + S::B4;
+  unsigned char* b4l = b4h + 24576;
+  float* part = reinterpret_cast<float*>(sm + S::PART);
+  float* invs = reinterpret_cast<float*>(sm + S::INV);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::BAR);
+  uint64_t* b3full = bars + 0;
+  uint64_t* b4full = bars + 1;
+  uint64_t* mma3 = bars + 2;
+  uint64_t* mma4 = bars + 3;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
+  int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);
+
+  const int n = blockIdx.x, h = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 0) {
+    int off = 0;
+    const bool ok = seq_chunk_offset(cu, num_seqs, total, n, off);
+    if (lane == 0 && !ok && n == 0 && h == 0) set_status(status, GDN_STATUS_BAD_SEQLENS);
+    if (lane == 0) {
+      sh[0] = ok;
+      sh[1] = off;
+      sh[2] = 0;
+    }
+  }
+  if (tid == 0) {
+    tc::mbar_init(b3full, 128);
+    tc::mbar_init(b4full, 128);
+    tc::mbar_init(mma3, 1);
+    tc::mbar_init(mma4, 1);
+    tc::mbar_fence_init();
+  }
+  __syncthreads();
+  if (!sh[0]) return;
+  if (warp == 0) tc::tmem_alloc(tslot, 256);
+  const int choff = sh[1];
+  volatile int* abort = sh + 2;
+  const int seq_start = __ldg(cu + n), len = __ldg(cu + n + 1) - seq_start;
+  const int nch = (len + CH - 1) / CH;
+  const int s = __ldg(slot_idx + n);
+  const bool valid = s >= 0 && s < num_slots;
+  if (!valid && s >= num_slots && h == 0 && tid == 0) set_status(status, GDN_STATUS_SLOT_RANGE);
+  const bool init = valid && has_init != nullptr && __ldg(has_init + n) != 0;
+  float* Sg = rec_state + ((size_t)(valid ? s : 0) * d.Hv + h) * D * D;
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tb = *tslot;
+
+  if (warp < 4) {
+    // ================= main warps: thread e owns TMEM lane e = row e of S^T (dv index)
+    const int e = tid;
+    const uint32_t lane_base = tc::taddr(tb, warp * 32, 0);
+#pragma unroll
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = init ? Sg[(size_t)(c0 + k) * D + e] : 0.f;
+      tc::tmem_st16(lane_base + c0, v);
+    }
+    const float wn = Act<T>::ldg(norm_w + e);
+    for (int c = 0; c < nch; ++c) {
+      const float* rec = ws + ((size_t)(choff + c) * d.Hv + h) * REC;
+      const int t0 = seq_start + c * CH, L = min(CH, len - c * CH);
+      const uint32_t par = c & 1;
+      // A3 = split(S^T) from TMEM
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(lane_base + c0, v);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint4 hh, ll;
+          split8(v + 8 * g, hh, ll);
+          const uint32_t off = tc::kmajor_off(e, c0 + 8 * g, 128);
+          st_unit(a3h, off, hh);
+          st_unit(a3l, off, ll);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      bar_sync_main();
+      tc::fence_after_sync();
+      if (e == 0 && wait_or_abort(b3full, par, abort, status)) {
+        tc::fence_after_sync();
+        const uint32_t id = tc::idesc_bf16(128, 128);
+        const uint32_t ah = tc::smem_u32(a3h), al = tc::smem_u32(a3l);
+        const uint32_t bh = tc::smem_u32(b3h), bl = tc::smem_u32(b3l);
+        for (int k = 0; k < 8; ++k) {
+          tc::mma_bf16(tb + 128, tc::kstep_desc(ah, 128, k), tc::kstep_desc(bh, 128, k), id, k > 0);
+          tc::mma_bf16(tb + 128, tc::kstep_desc(ah, 128, k), tc::kstep_desc(bl, 128, k), id, 1);
+          tc::mma_bf16(tb + 128, tc::kstep_desc(al, 128, k), tc::kstep_desc(bh, 128, k), id, 1);
+        }
+        tc::mma_commit(mma3);
+      }
+      // meanwhile: S^T *= e^{gamma_L};  U~ column e into registers
+      const float egL = rec[R_SC];
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(lane_base + c0, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] *= egL;
+        tc::tmem_st16(lane_base + c0, v);
+      }
+      float ut[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) ut[i] = rec[R_UT + i * D + e];
+      wait_or_abort(mma3, par, abort, status);
+      tc::fence_after_sync();
+      // U^T = U~^T - (W S)^T  -> A4
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(lane_base + 192 + c0, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = ut[c0 + k] - v[k];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint4 hh, ll;
+          split8(v + 8 * g, hh, ll);
+          const uint32_t off = tc::kmajor_off(e, c0 + 8 * g, 64);
+          st_unit(a4h, off, hh);
+          st_unit(a4l, off, ll);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      bar_sync_main();
+      tc::fence_after_sync();
+      if (e == 0 && wait_or_abort(b4full, par, abort, status)) {
+        tc::fence_after_sync();
+        const uint32_t id = tc::idesc_bf16(128, 192);
+        const uint32_t ah = tc::smem_u32(a4h), al = tc::smem_u32(a4l);
+        const uint32_t bh = tc::smem_u32(b4h), bl = tc::smem_u32(b4l);
+        for (int k = 0; k < 4; ++k) {
+          tc::mma_bf16(tb, tc::kstep_desc(ah, 64, k), tc::kstep_desc(bh, 64, k), id, 1);
+          tc::mma_bf16(tb, tc::kstep_desc(ah, 64, k), tc::kstep_desc(bl, 64, k), id, 1);
+          tc::mma_bf16(tb, tc::kstep_desc(al, 64, k), tc::kstep_desc(bh, 64, k), id, 1);
+        }
+        tc::mma_commit(mma4);
+      }
+      wait_or_abort(mma4, par, abort, status);
+      tc::fence_after_sync();
+      // O^T row e (tokens 0..63) -> z-gated RMSNorm over e for every token
+      float o[64];
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 16) tc::tmem_ld16(lane_base + 128 + c0, o + c0);
+      float v[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) v[i] = o[i] * o[i];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const bool up = lane & 16;
+        const float send = up ? v[k] : v[32 + k];
+        const float keep = up ? v[32 + k] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const bool up = lane & 8;
+        const float send = up ? v[k] : v[16 + k];
+        const float keep = up ? v[16 + k] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const bool up = lane & 4;
+        const float send = up ? v[k] : v[8 + k];
+        const float keep = up ? v[8 + k] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const bool up = lane & 2;
+        const float send = up ? v[k] : v[4 + k];
+        const float keep = up ? v[4 + k] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const bool up = lane & 1;
+        const float send = up ? v[k] : v[2 + k];
+        const float keep = up ? v[2 + k] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+      }
+      part[warp * 64 + 2 * lane] = v[0];
+      part[warp * 64 + 2 * lane + 1] = v[1];
+      bar_sync_main();
+      if (warp == 0) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int i = 2 * lane + q;
+          const float ss = part[i] + part[64 + i] + part[128 + i] + part[192 + i];
+          invs[i] = 1.0f / sqrtf(ss / (float)D + d.norm_eps);
+        }
+      }
+      bar_sync_main();
+      const size_t ld = (size_t)d.Hv * D;
+      T* orow = out + (size_t)t0 * ld + (size_t)h * D + e;
+      const T* zrow = z + (size_t)t0 * ld + (size_t)h * D + e;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        if (i < L) {
+          const float zz = Act<T>::ldg(zrow + (size_t)i * ld);
+          const float val = valid ? o[i] * invs[i] * wn * siluf_(zz) : 0.f;
+          Act<T>::store(orow + (size_t)i * ld, val);
+        }
+      }
+      tc::fence_before_sync();
+      bar_sync_main();
+    }
+    // final state back to the slot
+    if (valid) {
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(lane_base + c0, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) Sg[(size_t)(c0 + k) * D + e] = v[k];
+      }
+    }
+  } else {
+    // ================= loader warps: stage the B operands of every chunk
+    const int lt = tid - 128;
+    for (int c = 0; c < nch; ++c) {
+      const float* rec = ws + ((size_t)(choff + c) * d.Hv + h) * REC;
+      if (c > 0) wait_or_abort(mma3, (c - 1) & 1, abort, status);
+      // B3 rows 0-63 = Q~ rows, rows 64-127 = W rows   (K = dk)
+#pragma unroll 4
+      for (int m = 0; m < 16; ++m) {
+        const int u = lt + 128 * m, row = u >> 4, kg = u & 15;
+        const float* src = (row < 64 ? rec + R_QT + row * D : rec + R_WR + (row - 64) * D) + kg * 8;
+        const float4 p0 = *reinterpret_cast<const float4*>(src);
+        const float4 p1 = *reinterpret_cast<const float4*>(src + 4);
+        const float vv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        uint4 hh, ll;
+        split8(vv, hh, ll);
+        const uint32_t off = tc::kmajor_off(row, kg * 8, 128);
+        st_unit(b3h, off, hh);
+        st_unit(b3l, off, ll);
+      }
+      tc::fence_proxy_async_smem();
+      mbar_arrive(b3full);
+      if (c > 0) wait_or_abort(mma4, (c - 1) & 1, abort, status);
+      // B4 rows 0-127 = K~^T rows (feature f, K = token), rows 128-191 = P rows
+      {
+        const int f = lt;
+#pragma unroll
+        for (int jg = 0; jg < 8; ++jg) {
+          float vv[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) vv[q] = rec[R_KT + (jg * 8 + q) * D + f];
+          uint4 hh, ll;
+          split8(vv, hh, ll);
+          const uint32_t off = tc::kmajor_off(f, jg * 8, 64);
+          st_unit(b4h, off, hh);
+          st_unit(b4l, off, ll);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int u = lt + 128 * m, i = u >> 3, jg = u & 7;
+        const float* src = rec + R_PM + i * 64 + jg * 8;
+        const float4 p0 = *reinterpret_cast<const float4*>(src);
+        const float4 p1 = *reinterpret_cast<const float4*>(src + 4);
+        const float vv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        uint4 hh, ll;
+        split8(vv, hh, ll);
+        const uint32_t off = tc::kmajor_off(128 + i, jg * 8, 64);
+        st_unit(b4h, off, hh);
+        st_unit(b4l, off, ll);
+      }
+      tc::fence_proxy_async_smem();
+      mbar_arrive(b4full);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tb, 256);
+  // conv state <- the sequence's last K-1 raw inputs (older ones kept when continuing)
+  if (valid && h == 0) {
+    T* csw = conv_state + (size_t)s * 3 * d.cqkv;
+    for (int cch = tid; cch < d.cqkv; cch += 256) {
+      T v3[3];
+#pragma unroll
+      for (int m = 0; m < 3; ++m) {
+        const int rel = len - 3 + m;
+        if (rel >= 0) v3[m] = qkv[(size_t)(seq_start + rel) * d.cqkv + cch];
+        else v3[m] = init ? csw[(size_t)(3 + rel) * d.cqkv + cch] : Act<T>::cvt(0.f);
+      }
+#pragma unroll
+      for (int m = 0; m < 3; ++m) csw[(size_t)m * d.cqkv + cch] = v3[m];
+    }
+  }
+}
+
+template <typename T>
+int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const int32_t* cu,
+             const int32_t* slot_idx, const uint8_t* has_init, int num_seqs, int total,
+             const void* qkv, const void* z, const void* a, const void* b, void* out, void* ws,
+             cudaStream_t stream) {
+  const int nc_max = total / CH + num_seqs;
+  auto k1 = tc_intra_kernel<T>;
+  auto k2 = tc_state_kernel<T>;
+  if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IntraSmem::BYTES) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)StateSmem::BYTES) !=
+          cudaSuccess)
+    return GDN_ERR_CUDA;
+  float* wsf = static_cast<float*>(ws);
+  if (total > 0)
+    k1<<<dim3(nc_max, d.Hv), 256, IntraSmem::BYTES, stream>>>(
+        d, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
+        static_cast<const T*>(pool->conv_state), pool->num_slots, cu, slot_idx, has_init, num_seqs,
+        total, static_cast<const T*>(qkv), static_cast<const T*>(a), static_cast<const T*>(b), wsf,
+        pool->status);
+  k2<<<dim3(num_seqs, d.Hv), 256, StateSmem::BYTES, stream>>>(
+      d, static_cast<const T*>(w->norm_weight), pool->rec_state, static_cast<T*>(pool->conv_state),
+      pool->num_slots, cu, slot_idx, has_init, num_seqs, total, static_cast<const T*>(qkv),
+      static_cast<const T*>(z), static_cast<T*>(out), wsf, pool->status);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const KDims& d) { return d.dk == D && d.dv == D; }
+
+size_t prefill_tc_ws_bytes(const KDims& d, int num_seqs, int total) {
+  return sizeof(float) * (size_t)(total / CH + num_seqs) * d.Hv * REC;
+}
+
+int launch_prefill_tc(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
+                      const int32_t* cu, const int32_t* slot_idx, const uint8_t* has_init,
+                      int num_seqs, int total, const void* qkv, const void* z, const void* a,
+                      const void* b, void* out, void* ws, cudaStream_t stream) {
+  if (w->act == GDN_BF16)
+    return launch_t<__nv_bfloat16>(d, w, pool, cu, slot_idx, has_init, num_seqs, total, qkv, z, a,
+                                   b, out, ws, stream);
+  return launch_t<float>(d, w, pool, cu, slot_idx, has_init, num_seqs, total, qkv, z, a, b, out,
+                         ws, stream);
+}
+
+}  // namespace gdn

@@ -72,6 +72,7 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 /* Bits the kernels OR into *gdn_pool.status. */
 #define GDN_STATUS_SLOT_RANGE 1
 #define GDN_STATUS_BAD_SEQLENS 2
+#define GDN_STATUS_TIMEOUT 4       /* a bounded device-side wait gave up; outputs are invalid */
 
 /* Rank-local layer geometry ("local_linear_*" head counts of one tensor-parallel rank; one
  * GPU holds them all here).  q_scale = 0 selects 1/sqrt(head_k_dim).  l2norm divides by

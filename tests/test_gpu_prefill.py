@@ -33,6 +33,8 @@ def _dev_i32(x):
     synth.Geometry(2, 2, 64, 64, 4, synth.F32),
     synth.Geometry(1, 3, 128, 64, 4, synth.BF16),
     synth.Geometry(2, 4, 64, 128, 4, synth.F32),
+    synth.Geometry(2, 4, 128, 128, 4, synth.F32),
+    synth.Geometry(1, 3, 128, 128, 4, synth.BF16),
 ], ids=lambda g: f"Hk{g.Hk}Hv{g.Hv}dk{g.dk}dv{g.dv}{g.act}")
 def test_prefill_varlen_full_compare(geo):
     lens = [1, 63, 0, 64, 65, 130, 2, 200]
@@ -108,8 +110,9 @@ def test_prefill_then_decode_continues():
     np.testing.assert_array_equal(_np(layer.conv_state)[2], c64[2])
 
 
-def test_prefill_bad_slot_and_bad_seqlens():
-    geo = synth.Geometry(1, 2, 64, 64, 4, synth.BF16)
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_bad_slot_and_bad_seqlens(d):
+    geo = synth.Geometry(1, 2, d, d, 4, synth.BF16)
     w = synth.make_weights(geo, 620)
     rec, conv = synth.make_pool(geo, 2, 621, True)
     layer = GatedDeltaNetLayer(geo, w, 2)

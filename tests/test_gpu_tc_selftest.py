@@ -1,0 +1,58 @@
+"""The tcgen05 / TMEM / shared-memory-descriptor primitives the prefill uses, checked in
+isolation: a 128 x N x K GEMM with bf16 operands (one pass) and with split-bf16 operands
+(hi*hi + hi*lo + lo*hi, three passes) against float64 products on the CPU."""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_deltanet_linear_09_gb300 import build as gbuild
+    out_dir = os.path.join(HERE, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    so = os.path.join(out_dir, "libtcselftest.so")
+    cmd = [gbuild.nvcc()] + gbuild.flags() + ["-shared", "-o", so,
+                                              os.path.join(HERE, "csrc", "tc_selftest.cu")]
+    subprocess.run(cmd, check=True)
+    l = ctypes.CDLL(so)
+    l.tc_gemm.restype = ctypes.c_int
+    l.tc_gemm.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    return l
+
+
+def _bf16(x):
+    return torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("N,K", [(64, 128), (128, 128), (192, 64), (256, 64), (16, 16)])
+def test_tc_gemm(lib, N, K):
+    rng = np.random.default_rng(N * 1000 + K)
+    A = rng.standard_normal((128, K)).astype(np.float32)
+    B = rng.standard_normal((N, K)).astype(np.float32)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = A.astype(np.float64) @ B.astype(np.float64).T
+    # one pass: exactly the product of the bf16-rounded operands (f32 accumulation)
+    D = torch.zeros((128, N), dtype=torch.float32, device="cuda")
+    assert lib.tc_gemm(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, K, 1, err.data_ptr()) == 0
+    assert int(err.item()) == 0
+    ref1 = _bf16(A) @ _bf16(B).T
+    np.testing.assert_allclose(D.cpu().numpy(), ref1, rtol=0, atol=2e-4 * np.sqrt(K))
+    # three passes: close to the float32 operands' product
+    D.zero_()
+    assert lib.tc_gemm(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, K, 3, err.data_ptr()) == 0
+    assert int(err.item()) == 0
+    e3 = np.max(np.abs(D.cpu().numpy() - ref)) / np.max(np.abs(ref))
+    e1 = np.max(np.abs(ref1 - ref)) / np.max(np.abs(ref))
+    assert e3 < 2e-5, e3
+    assert e3 < e1 / 20
