@@ -14,6 +14,13 @@ namespace gdn {
 template <typename T> struct Act;
 
 template <> struct Act<float> {
+  // 4 consecutive values (16-byte aligned address)
+  static __device__ __forceinline__ float4 ldg4(const float* p) {
+    return __ldg(reinterpret_cast<const float4*>(p));
+  }
+  static __device__ __forceinline__ void store4(float* p, float4 v) {
+    *reinterpret_cast<float4*>(p) = v;
+  }
   static __device__ __forceinline__ float load(const float* p) { return *p; }
   static __device__ __forceinline__ float ldg(const float* p) { return __ldg(p); }
   static __device__ __forceinline__ void store(float* p, float v) { *p = v; }
@@ -21,6 +28,21 @@ template <> struct Act<float> {
 };
 
 template <> struct Act<__nv_bfloat16> {
+  // 4 consecutive values (8-byte aligned address)
+  static __device__ __forceinline__ float4 ldg4(const __nv_bfloat16* p) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+  }
+  static __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&lo);
+    u.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
   static __device__ __forceinline__ float load(const __nv_bfloat16* p) { return __bfloat162float(*p); }
   static __device__ __forceinline__ float ldg(const __nv_bfloat16* p) {
     return __bfloat162float(__ldg(p));
@@ -38,6 +60,12 @@ __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf
 __device__ __forceinline__ float siluf_(float x) { return x / (1.0f + expf(-x)); }
 // softplus(x) = log(1 + e^x) in a form that does not overflow for large x.
 __device__ __forceinline__ float softplusf_(float x) { return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x))); }
+
+// Hot-loop variants built on the approximate CUDA intrinsics __expf / __fdividef (relative error
+// ~1e-6 here).  Used only for per-element work inside the prefill; every per-chunk decay scalar
+// keeps the exact expf because its error would compound across chunks.
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+__device__ __forceinline__ float exp_fast(float x) { return __expf(x); }
 
 // g = -exp(A_log) * softplus(a + dt_bias);  beta = sigmoid(b)
 __device__ __forceinline__ void gates(float A_log, float dt_bias, float a, float b, float& g,

@@ -31,14 +31,15 @@ namespace {
 constexpr int CH = 64;
 constexpr int D = 128;
 
-// Per (chunk, V-head) record of the workspace, in floats.
-constexpr int R_QT = 0;                  // [64][128] Q~ rows
-constexpr int R_WR = R_QT + CH * D;      // [64][128] W rows
-constexpr int R_KT = R_WR + CH * D;      // [64][128] K~ rows
-constexpr int R_UT = R_KT + CH * D;      // [64][128] U~ rows
-constexpr int R_PM = R_UT + CH * D;      // [64][64]  P rows
-constexpr int R_SC = R_PM + CH * CH;     // e^{gamma_L}
-constexpr int REC = R_SC + 64;           // 147,712 bytes (multiple of 256)
+// Per (chunk, V-head) record of the workspace.  B3 and B4 are stored as the exact shared-memory
+// images of the state kernel's B operands (split bf16, K-major core-matrix layout, hi then lo), so
+// the state kernel brings each in with one bulk copy.  Offsets in bytes.
+constexpr uint32_t R_B3 = 0;                     // [Q~ ; W] rows, 128 x 128: hi 32 KiB, lo 32 KiB
+constexpr uint32_t R_B4 = R_B3 + 65536;          // [K~^T ; P] rows, 192 x 64: hi 24 KiB, lo 24 KiB
+constexpr uint32_t R_UT = R_B4 + 49152;          // f32 [64][128] U~ rows
+constexpr uint32_t R_SC = R_UT + 32768;          // f32 e^{gamma_L}
+constexpr uint32_t REC_BYTES = R_SC + 256;       // 147,712 bytes (multiple of 256)
+constexpr uint32_t B3_HALF = 32768, B4_HALF = 24576;
 
 __device__ __forceinline__ void bar_sync_main() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
 
@@ -68,6 +69,45 @@ __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
 
 __device__ __forceinline__ void st_unit(unsigned char* tile, uint32_t off, const uint4& v) {
   *reinterpret_cast<uint4*>(tile + off) = v;
+}
+
+__device__ __forceinline__ void gst_unit(unsigned char* g, uint32_t off, const uint4& v) {
+  *reinterpret_cast<uint4*>(g + off) = v;
+}
+
+// Rows [0,64) of X (f32 [64][XS], each row scaled by rs[row]) -> rows [row0, row0+64) of a
+// 128-column K-major tile image in global memory.  Consecutive threads write consecutive
+// 16-byte units (unit u: row & 7 = u & 7, k-group = (u >> 3) & 15, row group = u >> 7).
+__device__ __forceinline__ void x_rows_to_gtile128(const float* X, const float* rs,
+                                                   unsigned char* ghi, unsigned char* glo, int row0) {
+  for (int u = threadIdx.x; u < 1024; u += 256) {
+    const int r = ((u >> 7) << 3) + (u & 7), kg = (u >> 3) & 15;
+    const float sc = rs ? rs[r] : 1.f;
+    const float4 a = *reinterpret_cast<const float4*>(X + r * 132 + kg * 8);
+    const float4 b = *reinterpret_cast<const float4*>(X + r * 132 + kg * 8 + 4);
+    const float v[8] = {a.x * sc, a.y * sc, a.z * sc, a.w * sc, b.x * sc, b.y * sc, b.z * sc, b.w * sc};
+    uint4 hh, ll;
+    split8(v, hh, ll);
+    const uint32_t off = (uint32_t)(row0 * 16 * 16) + (uint32_t)u * 16u;   // row0 is a multiple of 8
+    gst_unit(ghi, off, hh);
+    gst_unit(glo, off, ll);
+  }
+}
+
+// Columns of X scaled per token by cs[j] -> a [128 features][64 tokens] K-major tile image in
+// global memory (unit u: feature & 7 = u & 7, token group = (u >> 3) & 7, feature group = u >> 6).
+__device__ __forceinline__ void x_cols_to_gtile64(const float* X, const float* cs,
+                                                  unsigned char* ghi, unsigned char* glo) {
+  for (int u = threadIdx.x; u < 1024; u += 256) {
+    const int f = ((u >> 6) << 3) + (u & 7), jg = (u >> 3) & 7;
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = X[(jg * 8 + q) * 132 + f] * cs[jg * 8 + q];
+    uint4 hh, ll;
+    split8(v, hh, ll);
+    gst_unit(ghi, (uint32_t)u * 16u, hh);
+    gst_unit(glo, (uint32_t)u * 16u, ll);
+  }
 }
 
 // Warp-wide: global chunk -> (sequence, first token, length); false if cu_seqlens is invalid.
@@ -160,23 +200,30 @@ __device__ __forceinline__ void conv_group(const KDims& d, const T* __restrict__
   const float w2 = Act<T>::ldg(conv_w + (size_t)ch * 4 + 2), w3 = Act<T>::ldg(conv_w + (size_t)ch * 4 + 3);
   const int i0 = half * 32;
   const int p0 = (t0 - seq_start) + i0;   // position of token i0 inside its sequence
-  // raw input at position p of the sequence: the slot's conv state before it, zero past its end
-  auto fetch = [&](int p) -> float {
-    if (p >= seq_len) return 0.f;
-    if (p >= 0) return Act<T>::ldg(qkv + (size_t)(seq_start + p) * d.cqkv + ch);
-    return init ? Act<T>::ldg(cs + (size_t)(3 + p) * d.cqkv + ch) : 0.f;
-  };
-  float xm3 = fetch(p0 - 3), xm2 = fetch(p0 - 2), xm1 = fetch(p0 - 1);
+  // Every load below reads a valid address (rows clamped into the sequence / the conv state)
+  // and is selected afterwards, so all of them can be in flight at once.
+  float hist[3];
+#pragma unroll
+  for (int m = 0; m < 3; ++m) {
+    const int p = p0 - 3 + m;
+    const int pr = min(max(p, 0), seq_len - 1);
+    const int pc = min(max(p, -3), -1);
+    const float xq = Act<T>::ldg(qkv + (size_t)(seq_start + pr) * d.cqkv + ch);
+    const float xc = Act<T>::ldg(cs + (size_t)(3 + pc) * d.cqkv + ch);
+    hist[m] = (p >= seq_len) ? 0.f : (p >= 0 ? xq : (init ? xc : 0.f));
+  }
+  float xm3 = hist[0], xm2 = hist[1], xm1 = hist[2];
   float xs[32];
 #pragma unroll
-  for (int k = 0; k < 32; ++k) xs[k] = (i0 + k < L) ? Act<T>::ldg(qkv + (size_t)(seq_start + p0 + k) * d.cqkv + ch) : 0.f;
+  for (int k = 0; k < 32; ++k)
+    xs[k] = Act<T>::ldg(qkv + (size_t)(t0 + min(i0 + k, L - 1)) * d.cqkv + ch);
 #pragma unroll
   for (int k = 0; k < 32; ++k) {
     float acc = w3 * xs[k];
     acc = fmaf(w0, xm3, acc);
     acc = fmaf(w1, xm2, acc);
     acc = fmaf(w2, xm1, acc);
-    X[(i0 + k) * XS + f] = (i0 + k < L) ? siluf_(acc) : 0.f;
+    X[(i0 + k) * XS + f] = (i0 + k < L) ? silu_fast(acc) : 0.f;
     xm3 = xm2;
     xm2 = xm1;
     xm1 = xs[k];
@@ -294,7 +341,8 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   const bool init = valid && has_init != nullptr && __ldg(has_init + seq) != 0;
   const T* cs = conv_state + (size_t)(valid ? s : 0) * 3 * d.cqkv;
   const int kh = h / d.r;
-  float* rec = ws + ((size_t)c * d.Hv + h) * REC;
+  unsigned char* rec = reinterpret_cast<unsigned char*>(ws) + ((size_t)c * d.Hv + h) * REC_BYTES;
+  float* rec_ut = reinterpret_cast<float*>(rec + R_UT);
 
   if (tid == 0) {
     tc::mbar_init(bar, 1);
@@ -308,11 +356,12 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int i = 2 * lane + q;
-      g2[q] = 0.f;
-      b2[q] = 0.f;
-      if (i < L) {
-        gates(__ldg(A_log + h), __ldg(dt_bias + h), Act<T>::ldg(a + (size_t)(t0 + i) * d.Hv + h),
-              Act<T>::ldg(b + (size_t)(t0 + i) * d.Hv + h), g2[q], b2[q]);
+      const int ic = min(i, L - 1);
+      gates(__ldg(A_log + h), __ldg(dt_bias + h), Act<T>::ldg(a + (size_t)(t0 + ic) * d.Hv + h),
+            Act<T>::ldg(b + (size_t)(t0 + ic) * d.Hv + h), g2[q], b2[q]);
+      if (i >= L) {
+        g2[q] = 0.f;
+        b2[q] = 0.f;
       }
     }
     const float pair = g2[0] + g2[1];
@@ -343,10 +392,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   __syncthreads();
   x_rows_to_tile(X, a1h, a1l, 0);
   x_cols_to_tile(X, bgk, a2ah, a2al);
-  for (int idx = tid; idx < CH * D; idx += 256) {
-    const int j = idx >> 7;
-    rec[R_KT + idx] = X[j * XS + (idx & 127)] * dec[j];
-  }
+  x_cols_to_gtile64(X, dec, rec + R_B4, rec + R_B4 + B4_HALF);   // K~^T rows of B4
   __syncthreads();
   // ---- Q: conv, l2norm (times q_scale), A1 rows 64-127, Q~ rows
   conv_group<T>(d, qkv, conv_w, cs, init, kh * D, seq_start, seq_len, t0, L, X);
@@ -354,10 +400,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   l2norm_rows(X, d.l2_eps, d.q_scale);
   __syncthreads();
   x_rows_to_tile(X, a1h, a1l, 64);
-  for (int idx = tid; idx < CH * D; idx += 256) {
-    const int i = idx >> 7;
-    rec[R_QT + idx] = X[i * XS + (idx & 127)] * eg[i];
-  }
+  x_rows_to_gtile128(X, eg, rec + R_B3, rec + R_B3 + B3_HALF, 0);   // Q~ rows of B3
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
@@ -381,29 +424,38 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   // ---- A and P from D1
   wait_or_abort(bar, 0, abort, status);
   tc::fence_after_sync();
-  if (warp < 4) {
-    const int r = warp * 32 + lane;
-    float v[64];
-#pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16) tc::tmem_ld16(tc::taddr(tb, warp * 32, c0), v + c0);
+  {
+    // all 8 warps: warp w reads TMEM lanes 32 (w % 4) .. +31 and the 32 columns of half w / 4
+    const int r = (warp & 3) * 32 + lane, j0 = (warp >> 2) * 32;
+    float v[32];
+    tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, j0), v);
+    tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, j0 + 16), v + 16);
+    // branch-free: exponents clamped to <= 0, masked entries multiplied by zero
     if (r < 64) {
       const int i = r;
-      const float gi = gam[i], bi = bet[i];
+      const float gi = gam[i], bi = (i < L) ? bet[i] : 0.f;
 #pragma unroll
-      for (int j = 0; j < 64; ++j)
-        Am[i * AS + j] = (j < i && i < L) ? bi * expf(gi - gam[j]) * v[j] : 0.f;
+      for (int q = 0; q < 32; ++q) {
+        const int j = j0 + q;
+        const float m = (j < i) ? bi : 0.f;
+        Am[i * AS + j] = m * exp_fast(fminf(gi - gam[j], 0.f)) * v[q];
+      }
     } else {
       const int i = r - 64;
-      const float gi = gam[i];
-      float* prow = rec + R_PM + i * 64;
+      const float gi = gam[i], vi = (i < L) ? 1.f : 0.f;
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) {
-        float4 p;
-        p.x = (j + 0 <= i && i < L) ? v[j + 0] * expf(gi - gam[j + 0]) : 0.f;
-        p.y = (j + 1 <= i && i < L) ? v[j + 1] * expf(gi - gam[j + 1]) : 0.f;
-        p.z = (j + 2 <= i && i < L) ? v[j + 2] * expf(gi - gam[j + 2]) : 0.f;
-        p.w = (j + 3 <= i && i < L) ? v[j + 3] * expf(gi - gam[j + 3]) : 0.f;
-        *reinterpret_cast<float4*>(prow + j) = p;
+      for (int q = 0; q < 32; q += 8) {
+        float p8[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + q + u;
+          p8[u] = ((j <= i) ? vi : 0.f) * exp_fast(fminf(gi - gam[j], 0.f)) * v[q + u];
+        }
+        uint4 hh, ll;
+        split8(p8, hh, ll);
+        const uint32_t off = tc::kmajor_off(128 + i, j0 + q, 64);   // P rows of B4
+        gst_unit(rec + R_B4, off, hh);
+        gst_unit(rec + R_B4 + B4_HALF, off, ll);
       }
     }
   }
@@ -483,19 +535,24 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   }
   wait_or_abort(bar, 1, abort, status);
   tc::fence_after_sync();
-  if (warp < 4) {
-    const int r = warp * 32 + lane;   // feature index (dk for W, dv for U~)
+  {
+    // warps 0-3: W^T lanes -> X staging [token][feature]; warps 4-7: U~^T lanes -> U~ rows
+    const int r = (warp & 3) * 32 + lane;
     float v[64];
 #pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16) tc::tmem_ld16(tc::taddr(tb, warp * 32, 64 + c0), v + c0);
+    for (int c0 = 0; c0 < 64; c0 += 16)
+      tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, (warp < 4 ? 64 : 128) + c0), v + c0);
+    if (warp < 4) {
 #pragma unroll
-    for (int i = 0; i < 64; ++i) rec[R_WR + i * D + r] = v[i];
+      for (int i = 0; i < 64; ++i) X[i * XS + r] = v[i];
+    } else {
 #pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16) tc::tmem_ld16(tc::taddr(tb, warp * 32, 128 + c0), v + c0);
-#pragma unroll
-    for (int i = 0; i < 64; ++i) rec[R_UT + i * D + r] = v[i];
+      for (int i = 0; i < 64; ++i) rec_ut[i * D + r] = v[i];
+    }
   }
-  if (tid == 0) rec[R_SC] = expf(gL);
+  __syncthreads();
+  x_rows_to_gtile128(X, nullptr, rec + R_B3, rec + R_B3 + B3_HALF, 64);   // W rows of B3
+  if (tid == 0) *reinterpret_cast<float*>(rec + R_SC) = expf(gL);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, 256);
@@ -508,12 +565,37 @@ struct StateSmem {
   static constexpr uint32_t B3 = A3 + 2 * 32768;    // [Q~ ; W] rows [128 x 128]
   static constexpr uint32_t A4 = B3 + 2 * 32768;    // U^T   [128 x 64]
   static constexpr uint32_t B4 = A4 + 2 * 16384;    // [K~^T ; P] rows [192 x 64]
-  static constexpr uint32_t PART = B4 + 2 * 24576;  // f32 [4][64] partial sums of squares
-  static constexpr uint32_t INV = PART + 4 * 4 * 64; // f32 [64]
-  static constexpr uint32_t BAR = INV + 4 * 64;     // 4 mbarriers
-  static constexpr uint32_t MISC = BAR + 32;
+  static constexpr uint32_t BAR = B4 + 2 * 24576;   // 6 mbarriers
+  static constexpr uint32_t MISC = BAR + 48;
   static constexpr uint32_t BYTES = MISC + 64;
 };
+
+// z-gated RMSNorm of one chunk's outputs, by the four loader warps: O (f32 [64 tokens][128],
+// staged in shared memory) -> out.  Warp w takes tokens w, w+4, ...; lane l the 4 channels 4l..4l+3.
+template <typename T>
+__device__ __forceinline__ void chunk_epilogue(const float* Ost, const T* __restrict__ z,
+                                               T* __restrict__ out, const float4 wn4, int t0, int L,
+                                               int h, int Hv, float eps, bool valid) {
+  const int w = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const size_t ld = (size_t)Hv * D;
+  float4 zz[16];
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const int i = min(w + 4 * m, L - 1);
+    zz[m] = Act<T>::ldg4(z + (size_t)(t0 + i) * ld + (size_t)h * D + 4 * lane);
+  }
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const int i = w + 4 * m;
+    const float4 o = *reinterpret_cast<const float4*>(Ost + i * D + 4 * lane);
+    float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
+    ss = warp_sum(ss);
+    const float inv = valid ? 1.0f / sqrtf(ss / (float)D + eps) : 0.f;
+    const float4 r = make_float4(o.x * inv * wn4.x * silu_fast(zz[m].x), o.y * inv * wn4.y * silu_fast(zz[m].y),
+                                 o.z * inv * wn4.z * silu_fast(zz[m].z), o.w * inv * wn4.w * silu_fast(zz[m].w));
+    if (i < L) Act<T>::store4(out + (size_t)(t0 + i) * ld + (size_t)h * D + 4 * lane, r);
+  }
+}
 
 template <typename T>
 __global__ void __launch_bounds__(256, 1)
@@ -532,13 +614,14 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   unsigned char* a4l = a4h + 16384;
   unsigned char* b4h = sm + S::B4;
   unsigned char* b4l = b4h + 24576;
-  float* part = reinterpret_cast<float*>(sm + S::PART);
-  float* invs = reinterpret_cast<float*>(sm + S::INV);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::BAR);
   uint64_t* b3full = bars + 0;
   uint64_t* b4full = bars + 1;
   uint64_t* mma3 = bars + 2;
   uint64_t* mma4 = bars + 3;
+  uint64_t* ofull = bars + 4;    // O of the chunk staged (main -> loaders)
+  uint64_t* oempty = bars + 5;   // staged O consumed (loaders -> main)
+  float* Ost = reinterpret_cast<float*>(a4h);   // O staging aliases the U^T operand
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
   int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);
 
@@ -555,10 +638,12 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     }
   }
   if (tid == 0) {
-    tc::mbar_init(b3full, 128);
-    tc::mbar_init(b4full, 128);
+    tc::mbar_init(b3full, 1);
+    tc::mbar_init(b4full, 1);
     tc::mbar_init(mma3, 1);
     tc::mbar_init(mma4, 1);
+    tc::mbar_init(ofull, 128);
+    tc::mbar_init(oempty, 128);
     tc::mbar_fence_init();
   }
   __syncthreads();
@@ -582,17 +667,35 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     // ================= main warps: thread e owns TMEM lane e = row e of S^T (dv index)
     const int e = tid;
     const uint32_t lane_base = tc::taddr(tb, warp * 32, 0);
+    // B operands of chunk c arrive by bulk copy from the workspace (one per tile image)
+    auto rec_of = [&](int c) {
+      return reinterpret_cast<const unsigned char*>(ws) + ((size_t)(choff + c) * d.Hv + h) * REC_BYTES;
+    };
+    auto load_b3 = [&](int c) {
+      tc::mbar_arrive_expect_tx(b3full, 2 * B3_HALF);
+      tc::bulk_g2s(b3h, rec_of(c) + R_B3, 2 * B3_HALF, b3full);
+    };
+    auto load_b4 = [&](int c) {
+      tc::mbar_arrive_expect_tx(b4full, 2 * B4_HALF);
+      tc::bulk_g2s(b4h, rec_of(c) + R_B4, 2 * B4_HALF, b4full);
+    };
+    int issued3 = 0, issued4 = 0;   // bulk copies issued (thread 0); chunk c waits copy c
+    if (e == 0 && nch > 0) {
+      load_b3(0);
+      load_b4(0);
+      issued3 = issued4 = 1;
+    }
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 16) {
       float v[16];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) v[k] = init ? Sg[(size_t)(c0 + k) * D + e] : 0.f;
+      for (int k = 0; k < 16; ++k) v[k] = Sg[(size_t)(c0 + k) * D + e];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = init ? v[k] : 0.f;
       tc::tmem_st16(lane_base + c0, v);
     }
-    const float wn = Act<T>::ldg(norm_w + e);
     for (int c = 0; c < nch; ++c) {
-      const float* rec = ws + ((size_t)(choff + c) * d.Hv + h) * REC;
-      const int t0 = seq_start + c * CH, L = min(CH, len - c * CH);
+      const unsigned char* rec = rec_of(c);
       const uint32_t par = c & 1;
       // A3 = split(S^T) from TMEM
 #pragma unroll
@@ -625,7 +728,7 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         tc::mma_commit(mma3);
       }
       // meanwhile: S^T *= e^{gamma_L};  U~ column e into registers
-      const float egL = rec[R_SC];
+      const float egL = *reinterpret_cast<const float*>(rec + R_SC);
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 16) {
         float v[16];
@@ -636,8 +739,13 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       }
       float ut[64];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) ut[i] = rec[R_UT + i * D + e];
+      for (int i = 0; i < 64; ++i) ut[i] = reinterpret_cast<const float*>(rec + R_UT)[i * D + e];
       wait_or_abort(mma3, par, abort, status);
+      if (e == 0 && c + 1 < nch && !*abort) {                          // B3 free again
+        load_b3(c + 1);
+        ++issued3;
+      }
+      if (c > 0) wait_or_abort(oempty, (c - 1) & 1, abort, status);   // staging read by loaders
       tc::fence_after_sync();
       // U^T = U~^T - (W S)^T  -> A4
 #pragma unroll
@@ -672,74 +780,25 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         tc::mma_commit(mma4);
       }
       wait_or_abort(mma4, par, abort, status);
+      if (e == 0 && c + 1 < nch && !*abort) {                          // B4 free again
+        load_b4(c + 1);
+        ++issued4;
+      }
       tc::fence_after_sync();
-      // O^T row e (tokens 0..63) -> z-gated RMSNorm over e for every token
+      // O^T row e (tokens 0..63) -> staging (A4 is free once MMA4 completed); loaders normalise
       float o[64];
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 16) tc::tmem_ld16(lane_base + 128 + c0, o + c0);
-      float v[64];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) v[i] = o[i] * o[i];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const bool up = lane & 16;
-        const float send = up ? v[k] : v[32 + k];
-        const float keep = up ? v[32 + k] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-      }
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const bool up = lane & 8;
-        const float send = up ? v[k] : v[16 + k];
-        const float keep = up ? v[16 + k] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const bool up = lane & 4;
-        const float send = up ? v[k] : v[8 + k];
-        const float keep = up ? v[8 + k] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const bool up = lane & 2;
-        const float send = up ? v[k] : v[4 + k];
-        const float keep = up ? v[4 + k] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-      }
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const bool up = lane & 1;
-        const float send = up ? v[k] : v[2 + k];
-        const float keep = up ? v[2 + k] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-      }
-      part[warp * 64 + 2 * lane] = v[0];
-      part[warp * 64 + 2 * lane + 1] = v[1];
-      bar_sync_main();
-      if (warp == 0) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int i = 2 * lane + q;
-          const float ss = part[i] + part[64 + i] + part[128 + i] + part[192 + i];
-          invs[i] = 1.0f / sqrtf(ss / (float)D + d.norm_eps);
-        }
-      }
-      bar_sync_main();
-      const size_t ld = (size_t)d.Hv * D;
-      T* orow = out + (size_t)t0 * ld + (size_t)h * D + e;
-      const T* zrow = z + (size_t)t0 * ld + (size_t)h * D + e;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        if (i < L) {
-          const float zz = Act<T>::ldg(zrow + (size_t)i * ld);
-          const float val = valid ? o[i] * invs[i] * wn * siluf_(zz) : 0.f;
-          Act<T>::store(orow + (size_t)i * ld, val);
-        }
-      }
+      for (int i = 0; i < 64; ++i) Ost[i * D + e] = o[i];
+      mbar_arrive(ofull);
       tc::fence_before_sync();
       bar_sync_main();
+    }
+    // after a timeout: wait (bounded) for bulk copies still in flight before the CTA exits
+    if (e == 0 && *abort) {
+      for (int c = 0; c < issued3; ++c) tc::mbar_wait(b3full, c & 1, 100000000ull);
+      for (int c = 0; c < issued4; ++c) tc::mbar_wait(b4full, c & 1, 100000000ull);
     }
     // final state back to the slot
     if (valid) {
@@ -752,58 +811,14 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       }
     }
   } else {
-    // ================= loader warps: stage the B operands of every chunk
+    // ================= epilogue warps: z-gated RMSNorm of every chunk's staged outputs
     const int lt = tid - 128;
+    const float4 wn4 = Act<T>::ldg4(norm_w + 4 * (lt & 31));
     for (int c = 0; c < nch; ++c) {
-      const float* rec = ws + ((size_t)(choff + c) * d.Hv + h) * REC;
-      if (c > 0) wait_or_abort(mma3, (c - 1) & 1, abort, status);
-      // B3 rows 0-63 = Q~ rows, rows 64-127 = W rows   (K = dk)
-#pragma unroll 4
-      for (int m = 0; m < 16; ++m) {
-        const int u = lt + 128 * m, row = u >> 4, kg = u & 15;
-        const float* src = (row < 64 ? rec + R_QT + row * D : rec + R_WR + (row - 64) * D) + kg * 8;
-        const float4 p0 = *reinterpret_cast<const float4*>(src);
-        const float4 p1 = *reinterpret_cast<const float4*>(src + 4);
-        const float vv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-        uint4 hh, ll;
-        split8(vv, hh, ll);
-        const uint32_t off = tc::kmajor_off(row, kg * 8, 128);
-        st_unit(b3h, off, hh);
-        st_unit(b3l, off, ll);
-      }
-      tc::fence_proxy_async_smem();
-      mbar_arrive(b3full);
-      if (c > 0) wait_or_abort(mma4, (c - 1) & 1, abort, status);
-      // B4 rows 0-127 = K~^T rows (feature f, K = token), rows 128-191 = P rows
-      {
-        const int f = lt;
-#pragma unroll
-        for (int jg = 0; jg < 8; ++jg) {
-          float vv[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) vv[q] = rec[R_KT + (jg * 8 + q) * D + f];
-          uint4 hh, ll;
-          split8(vv, hh, ll);
-          const uint32_t off = tc::kmajor_off(f, jg * 8, 64);
-          st_unit(b4h, off, hh);
-          st_unit(b4l, off, ll);
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int u = lt + 128 * m, i = u >> 3, jg = u & 7;
-        const float* src = rec + R_PM + i * 64 + jg * 8;
-        const float4 p0 = *reinterpret_cast<const float4*>(src);
-        const float4 p1 = *reinterpret_cast<const float4*>(src + 4);
-        const float vv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-        uint4 hh, ll;
-        split8(vv, hh, ll);
-        const uint32_t off = tc::kmajor_off(128 + i, jg * 8, 64);
-        st_unit(b4h, off, hh);
-        st_unit(b4l, off, ll);
-      }
-      tc::fence_proxy_async_smem();
-      mbar_arrive(b4full);
+      wait_or_abort(ofull, c & 1, abort, status);
+      chunk_epilogue<T>(Ost, z, out, wn4, seq_start + c * CH, min(CH, len - c * CH), h, d.Hv,
+                        d.norm_eps, valid);
+      mbar_arrive(oempty);
     }
   }
   tc::fence_before_sync();
@@ -858,7 +873,7 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
 bool prefill_tc_supported(const KDims& d) { return d.dk == D && d.dv == D; }
 
 size_t prefill_tc_ws_bytes(const KDims& d, int num_seqs, int total) {
-  return sizeof(float) * (size_t)(total / CH + num_seqs) * d.Hv * REC;
+  return (size_t)(total / CH + num_seqs) * d.Hv * REC_BYTES;
 }
 
 int launch_prefill_tc(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
