@@ -80,7 +80,7 @@ __device__ __forceinline__ void gst_unit(unsigned char* g, uint32_t off, const u
 // 16-byte units (unit u: row & 7 = u & 7, k-group = (u >> 3) & 15, row group = u >> 7).
 __device__ __forceinline__ void x_rows_to_gtile128(const float* X, const float* rs,
                                                    unsigned char* ghi, unsigned char* glo, int row0) {
-  for (int u = threadIdx.x; u < 1024; u += 256) {
+  for (int u = threadIdx.x; u < 1024; u += blockDim.x) {
     const int r = ((u >> 7) << 3) + (u & 7), kg = (u >> 3) & 15;
     const float sc = rs ? rs[r] : 1.f;
     const float4 a = *reinterpret_cast<const float4*>(X + r * 132 + kg * 8);
@@ -98,7 +98,7 @@ __device__ __forceinline__ void x_rows_to_gtile128(const float* X, const float* 
 // global memory (unit u: feature & 7 = u & 7, token group = (u >> 3) & 7, feature group = u >> 6).
 __device__ __forceinline__ void x_cols_to_gtile64(const float* X, const float* cs,
                                                   unsigned char* ghi, unsigned char* glo) {
-  for (int u = threadIdx.x; u < 1024; u += 256) {
+  for (int u = threadIdx.x; u < 1024; u += blockDim.x) {
     const int f = ((u >> 6) << 3) + (u & 7), jg = (u >> 3) & 7;
     float v[8];
 #pragma unroll
@@ -170,7 +170,7 @@ __device__ bool seq_chunk_offset(const int32_t* __restrict__ cu, int num_seqs, i
 // ================================================================== intra-chunk kernel
 
 constexpr int XS = 132;   // row stride (floats) of the f32 staging tile
-constexpr int AS = 65;    // row stride of the A / T matrices
+constexpr int AS = 68;    // row stride of the A matrix (16-byte aligned rows)
 
 struct IntraSmem {
   static constexpr uint32_t A1 = 0;                    // hi [128x128] then lo
@@ -179,30 +179,37 @@ struct IntraSmem {
   static constexpr uint32_t B2 = A2B + 2 * 16384;      // T rows [64x64]
   static constexpr uint32_t X = B2 + 2 * 8192;         // f32 [64][XS]
   static constexpr uint32_t AM = X + 4 * 64 * XS;      // f32 [64][AS]
-  static constexpr uint32_t TM = AM + 4 * 64 * AS;     // f32 [64][AS]
-  static constexpr uint32_t MT = TM + 4 * 64 * AS;     // f32 [3][256]
-  static constexpr uint32_t VEC = MT + 4 * 3 * 256;    // f32 gam, bet, eg, dec, bgk [5][64]
+  static constexpr uint32_t VEC = AM + 4 * 64 * AS;    // f32 gam, bet, eg, dec, bgk [5][64]
   static constexpr uint32_t BAR = VEC + 4 * 5 * 64;    // mbarrier
   static constexpr uint32_t MISC = BAR + 16;           // tmem slot, flags
   static constexpr uint32_t BYTES = MISC + 64;
 };
 
-// conv + SiLU of 128 channels [cb, cb+128) over the chunk's tokens into X (rows >= L zero).
-template <typename T>
-__device__ __forceinline__ void conv_group(const KDims& d, const T* __restrict__ qkv,
-                                           const T* __restrict__ conv_w, const T* __restrict__ cs,
-                                           bool init, int cb, int seq_start, int seq_len,
-                                           int t0, int L, float* X) {
-  const int tid = threadIdx.x;
-  const int f = tid & 127, half = tid >> 7;
-  const int ch = cb + f;
-  const float w0 = Act<T>::ldg(conv_w + (size_t)ch * 4 + 0), w1 = Act<T>::ldg(conv_w + (size_t)ch * 4 + 1);
-  const float w2 = Act<T>::ldg(conv_w + (size_t)ch * 4 + 2), w3 = Act<T>::ldg(conv_w + (size_t)ch * 4 + 3);
-  const int i0 = half * 32;
-  const int p0 = (t0 - seq_start) + i0;   // position of token i0 inside its sequence
-  // Every load below reads a valid address (rows clamped into the sequence / the conv state)
-  // and is selected afterwards, so all of them can be in flight at once.
+constexpr int NTI = 512;   // threads of the intra kernel (16 warps)
+
+// conv + SiLU of 128 channels [cb, cb+128) over the chunk's tokens into X (rows >= L zero), split
+// into a load step (all loads in flight, results in registers) and a compute step, so that the
+// next channel group's loads overlap the current group's processing.
+// Thread t: channel t & 127, tokens [16 (t >> 7), +16).
+struct ConvIn {
+  float w[4];
   float hist[3];
+  float xs[16];
+};
+
+template <typename T>
+__device__ __forceinline__ void conv_load(const KDims& d, const T* __restrict__ qkv,
+                                          const T* __restrict__ conv_w, const T* __restrict__ cs,
+                                          bool init, int cb, int seq_start, int seq_len, int t0,
+                                          int L, ConvIn& in) {
+  const int tid = threadIdx.x;
+  const int f = tid & 127, i0 = (tid >> 7) * 16;
+  const int ch = cb + f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) in.w[q] = Act<T>::ldg(conv_w + (size_t)ch * 4 + q);
+  const int p0 = (t0 - seq_start) + i0;   // position of token i0 inside its sequence
+  // Every load reads a valid address (rows clamped into the sequence / the conv state) and is
+  // selected afterwards, so all of them can be in flight at once.
 #pragma unroll
   for (int m = 0; m < 3; ++m) {
     const int p = p0 - 3 + m;
@@ -210,83 +217,77 @@ __device__ __forceinline__ void conv_group(const KDims& d, const T* __restrict__
     const int pc = min(max(p, -3), -1);
     const float xq = Act<T>::ldg(qkv + (size_t)(seq_start + pr) * d.cqkv + ch);
     const float xc = Act<T>::ldg(cs + (size_t)(3 + pc) * d.cqkv + ch);
-    hist[m] = (p >= seq_len) ? 0.f : (p >= 0 ? xq : (init ? xc : 0.f));
+    in.hist[m] = (p >= seq_len) ? 0.f : (p >= 0 ? xq : (init ? xc : 0.f));
   }
-  float xm3 = hist[0], xm2 = hist[1], xm1 = hist[2];
-  float xs[32];
 #pragma unroll
-  for (int k = 0; k < 32; ++k)
-    xs[k] = Act<T>::ldg(qkv + (size_t)(t0 + min(i0 + k, L - 1)) * d.cqkv + ch);
+  for (int k = 0; k < 16; ++k)
+    in.xs[k] = Act<T>::ldg(qkv + (size_t)(t0 + min(i0 + k, L - 1)) * d.cqkv + ch);
+}
+
+__device__ __forceinline__ void conv_compute(const ConvIn& in, int L, float* X) {
+  const int tid = threadIdx.x;
+  const int f = tid & 127, i0 = (tid >> 7) * 16;
+  float xm3 = in.hist[0], xm2 = in.hist[1], xm1 = in.hist[2];
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    float acc = w3 * xs[k];
-    acc = fmaf(w0, xm3, acc);
-    acc = fmaf(w1, xm2, acc);
-    acc = fmaf(w2, xm1, acc);
+  for (int k = 0; k < 16; ++k) {
+    float acc = in.w[3] * in.xs[k];
+    acc = fmaf(in.w[0], xm3, acc);
+    acc = fmaf(in.w[1], xm2, acc);
+    acc = fmaf(in.w[2], xm1, acc);
     X[(i0 + k) * XS + f] = (i0 + k < L) ? silu_fast(acc) : 0.f;
     xm3 = xm2;
     xm2 = xm1;
-    xm1 = xs[k];
+    xm1 = in.xs[k];
   }
 }
 
 // Per-row l2 normalisation of X (64 rows x 128), times scale.
 __device__ __forceinline__ void l2norm_rows(float* X, float eps, float scale) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = warp; i < CH; i += 8) {
-    float v[4], ss = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      v[m] = X[i * XS + lane + 32 * m];
-      ss = fmaf(v[m], v[m], ss);
-    }
+  for (int i = warp; i < CH; i += NTI / 32) {
+    const float4 v = *reinterpret_cast<const float4*>(X + i * XS + 4 * lane);
+    float ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
     ss = warp_sum(ss);
     const float inv = scale / sqrtf(ss + eps);
-#pragma unroll
-    for (int m = 0; m < 4; ++m) X[i * XS + lane + 32 * m] = v[m] * inv;
+    *reinterpret_cast<float4*>(X + i * XS + 4 * lane) = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
   }
 }
 
-// Rows of X -> K-major tile rows [row0, row0+64) of a 128-column tile (hi / lo).
+// Rows of X -> rows [row0, row0+64) of a 128-column K-major shared tile (hi / lo).
+// Unit u: row & 7 = u & 7, k-group = (u >> 3) & 15, row group = u >> 7 (conflict-free stores).
 __device__ __forceinline__ void x_rows_to_tile(const float* X, unsigned char* hi, unsigned char* lo,
                                                int row0) {
-  const int t = threadIdx.x;
-  const int r = t >> 2, kq = t & 3;
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    const int kg = kq * 4 + g;
-    float v[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = X[r * XS + kg * 8 + q];
-    uint4 h, l;
-    split8(v, h, l);
-    const uint32_t off = tc::kmajor_off(row0 + r, kg * 8, 128);
-    st_unit(hi, off, h);
-    st_unit(lo, off, l);
+  for (int u = threadIdx.x; u < 1024; u += NTI) {
+    const int r = ((u >> 7) << 3) + (u & 7), kg = (u >> 3) & 15;
+    const float4 a = *reinterpret_cast<const float4*>(X + r * XS + kg * 8);
+    const float4 b = *reinterpret_cast<const float4*>(X + r * XS + kg * 8 + 4);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint4 hh, ll;
+    split8(v, hh, ll);
+    const uint32_t off = (uint32_t)(row0 * 256) + (uint32_t)u * 16u;
+    st_unit(hi, off, hh);
+    st_unit(lo, off, ll);
   }
 }
 
-// Columns of X scaled per token -> K-major tile [128 features][64 tokens] (hi / lo).
+// Columns of X scaled per token -> K-major shared tile [128 features][64 tokens] (hi / lo).
+// Unit u: feature & 7 = u & 7, token group = (u >> 3) & 7, feature group = u >> 6.
 __device__ __forceinline__ void x_cols_to_tile(const float* X, const float* scale,
                                                unsigned char* hi, unsigned char* lo) {
-  const int t = threadIdx.x;
-  const int f = t & 127, jh = t >> 7;
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    const int jg = jh * 4 + g;
+  for (int u = threadIdx.x; u < 1024; u += NTI) {
+    const int f = ((u >> 6) << 3) + (u & 7), jg = (u >> 3) & 7;
     float v[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) v[q] = X[(jg * 8 + q) * XS + f] * scale[jg * 8 + q];
-    uint4 h, l;
-    split8(v, h, l);
-    const uint32_t off = tc::kmajor_off(f, jg * 8, 64);
-    st_unit(hi, off, h);
-    st_unit(lo, off, l);
+    uint4 hh, ll;
+    split8(v, hh, ll);
+    st_unit(hi, (uint32_t)u * 16u, hh);
+    st_unit(lo, (uint32_t)u * 16u, ll);
   }
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(NTI, 1)
 tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict__ dt_bias,
                 const T* __restrict__ conv_w, const T* __restrict__ conv_state, int num_slots,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ slot_idx,
@@ -305,8 +306,6 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   unsigned char* b2l = b2h + 8192;
   float* X = reinterpret_cast<float*>(sm + S::X);
   float* Am = reinterpret_cast<float*>(sm + S::AM);
-  float* Tm = reinterpret_cast<float*>(sm + S::TM);
-  float* Mt = reinterpret_cast<float*>(sm + S::MT);
   float* gam = reinterpret_cast<float*>(sm + S::VEC);
   float* bet = gam + 64;
   float* eg = bet + 64;
@@ -385,22 +384,26 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     bgk[tid] = bet[tid] * expf(gam[tid]);
   }
 
-  // ---- K: conv, l2norm, A1 rows 0-63, (beta e^g K)^T, K~ rows
-  conv_group<T>(d, qkv, conv_w, cs, init, d.Hk * D + kh * D, seq_start, seq_len, t0, L, X);
+  // ---- K: conv, l2norm, A1 rows 0-63, (beta e^g K)^T, K~^T rows of B4
+  ConvIn cin, cnext;
+  conv_load<T>(d, qkv, conv_w, cs, init, d.Hk * D + kh * D, seq_start, seq_len, t0, L, cin);
+  conv_load<T>(d, qkv, conv_w, cs, init, kh * D, seq_start, seq_len, t0, L, cnext);
+  conv_compute(cin, L, X);
   __syncthreads();
   l2norm_rows(X, d.l2_eps, 1.0f);
   __syncthreads();
   x_rows_to_tile(X, a1h, a1l, 0);
   x_cols_to_tile(X, bgk, a2ah, a2al);
-  x_cols_to_gtile64(X, dec, rec + R_B4, rec + R_B4 + B4_HALF);   // K~^T rows of B4
+  x_cols_to_gtile64(X, dec, rec + R_B4, rec + R_B4 + B4_HALF);
   __syncthreads();
-  // ---- Q: conv, l2norm (times q_scale), A1 rows 64-127, Q~ rows
-  conv_group<T>(d, qkv, conv_w, cs, init, kh * D, seq_start, seq_len, t0, L, X);
+  // ---- Q: conv, l2norm (times q_scale), A1 rows 64-127, Q~ rows of B3
+  conv_compute(cnext, L, X);
+  conv_load<T>(d, qkv, conv_w, cs, init, 2 * d.Hk * D + h * D, seq_start, seq_len, t0, L, cin);
   __syncthreads();
   l2norm_rows(X, d.l2_eps, d.q_scale);
   __syncthreads();
   x_rows_to_tile(X, a1h, a1l, 64);
-  x_rows_to_gtile128(X, eg, rec + R_B3, rec + R_B3 + B3_HALF, 0);   // Q~ rows of B3
+  x_rows_to_gtile128(X, eg, rec + R_B3, rec + R_B3 + B3_HALF, 0);
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
@@ -418,24 +421,23 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     tc::mma_commit(bar);
   }
   // ---- V (overlaps the MMA): conv, (beta V)^T
-  conv_group<T>(d, qkv, conv_w, cs, init, 2 * d.Hk * D + h * D, seq_start, seq_len, t0, L, X);
+  conv_compute(cin, L, X);
   __syncthreads();
   x_cols_to_tile(X, bet, a2bh, a2bl);
   // ---- A and P from D1
   wait_or_abort(bar, 0, abort, status);
   tc::fence_after_sync();
   {
-    // all 8 warps: warp w reads TMEM lanes 32 (w % 4) .. +31 and the 32 columns of half w / 4
-    const int r = (warp & 3) * 32 + lane, j0 = (warp >> 2) * 32;
-    float v[32];
+    // warp w reads TMEM lanes 32 (w % 4) .. +31 and the 16 columns of quarter w / 4
+    const int r = (warp & 3) * 32 + lane, j0 = (warp >> 2) * 16;
+    float v[16];
     tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, j0), v);
-    tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, j0 + 16), v + 16);
     // branch-free: exponents clamped to <= 0, masked entries multiplied by zero
     if (r < 64) {
       const int i = r;
       const float gi = gam[i], bi = (i < L) ? bet[i] : 0.f;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
+      for (int q = 0; q < 16; ++q) {
         const int j = j0 + q;
         const float m = (j < i) ? bi : 0.f;
         Am[i * AS + j] = m * exp_fast(fminf(gi - gam[j], 0.f)) * v[q];
@@ -444,7 +446,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
       const int i = r - 64;
       const float gi = gam[i], vi = (i < L) ? 1.f : 0.f;
 #pragma unroll
-      for (int q = 0; q < 32; q += 8) {
+      for (int q = 0; q < 16; q += 8) {
         float p8[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -459,58 +461,46 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
       }
     }
   }
-  // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks per warp, then the off-diagonal blocks
-  for (int idx = tid; idx < 64 * AS; idx += 256) Tm[idx] = 0.f;
   __syncthreads();
-  if (warp < 4 && lane < 16) {
-    const int b0 = warp * 16, col = lane;
-    float tcol[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float v = (i == col) ? 1.f : 0.f;
-#pragma unroll
-      for (int j = 0; j < i; ++j) v = fmaf(-Am[(b0 + i) * AS + b0 + j], tcol[j], v);
-      tcol[i] = (i >= col) ? v : 0.f;
-      Tm[(b0 + i) * AS + b0 + col] = tcol[i];
-    }
-  }
-  __syncthreads();
-  for (int dd = 1; dd < 4; ++dd) {
-    const int nblk = 4 - dd;
-    for (int idx = tid; idx < nblk * 256; idx += 256) {
-      const int j = idx >> 8, i = j + dd, r = (idx >> 4) & 15, cc = idx & 15;
-      float sacc = 0.f;
-      for (int k = j; k < i; ++k)
-#pragma unroll
-        for (int x = 0; x < 16; ++x)
-          sacc = fmaf(Am[(16 * i + r) * AS + 16 * k + x], Tm[(16 * k + x) * AS + 16 * j + cc], sacc);
-      Mt[idx] = sacc;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < nblk * 256; idx += 256) {
-      const int j = idx >> 8, i = j + dd, r = (idx >> 4) & 15, cc = idx & 15;
-      float sacc = 0.f;
-#pragma unroll
-      for (int x = 0; x < 16; ++x)
-        sacc = fmaf(Tm[(16 * i + r) * AS + 16 * i + x], Mt[(j << 8) + x * 16 + cc], sacc);
-      Tm[(16 * i + r) * AS + 16 * j + cc] = -sacc;
-    }
-    __syncthreads();
-  }
-  // ---- B2 = T rows (K-major, 64 x 64)
+  // ---- T = (I + A)^{-1} by forward substitution, T_i = e_i - sum_{j<i} A_ij T_j.  Warp w owns
+  // columns 4w..4w+3, lane l rows l and l + 32; at step j the owner of row j (already final)
+  // broadcasts it.  A_ij = 0 for j >= i, so rows <= j are left unchanged.  T goes straight into
+  // the split-bf16 B2 tile (rows i, K = j): 4 consecutive columns are half a 16-byte unit.
   {
-    const int i = tid >> 2, kq = tid & 3;
+    const int c0 = 4 * warp;
+    float t0[4], t1[4];
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-      const int kg = kq * 2 + g;
-      float v[8];
+    for (int q = 0; q < 4; ++q) {
+      t0[q] = (lane == c0 + q) ? 1.f : 0.f;
+      t1[q] = (lane + 32 == c0 + q) ? 1.f : 0.f;
+    }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = Tm[i * AS + kg * 8 + q];
-      uint4 hh, ll;
-      split8(v, hh, ll);
-      const uint32_t off = tc::kmajor_off(i, kg * 8, 64);
-      st_unit(b2h, off, hh);
-      st_unit(b2l, off, ll);
+    for (int j4 = 0; j4 < 64; j4 += 4) {
+      const float4 a04 = *reinterpret_cast<const float4*>(Am + lane * AS + j4);
+      const float4 a14 = *reinterpret_cast<const float4*>(Am + (lane + 32) * AS + j4);
+      const float a0s[4] = {a04.x, a04.y, a04.z, a04.w}, a1s[4] = {a14.x, a14.y, a14.z, a14.w};
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = j4 + jj;
+        float tj[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tj[q] = __shfl_sync(0xffffffffu, j < 32 ? t0[q] : t1[q], j & 31);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          t0[q] = fmaf(-a0s[jj], tj[q], t0[q]);
+          t1[q] = fmaf(-a1s[jj], tj[q], t1[q]);
+        }
+      }
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const float* tv = half ? t1 : t0;
+      __nv_bfloat16 hq[4], lq[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tc::split_bf16(tv[q], hq[q], lq[q]);
+      const uint32_t off = tc::kmajor_off(lane + 32 * half, c0, 64);
+      *reinterpret_cast<uint2*>(b2h + off) = *reinterpret_cast<const uint2*>(hq);
+      *reinterpret_cast<uint2*>(b2l + off) = *reinterpret_cast<const uint2*>(lq);
     }
   }
   tc::fence_proxy_async_smem();
@@ -536,18 +526,19 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   wait_or_abort(bar, 1, abort, status);
   tc::fence_after_sync();
   {
-    // warps 0-3: W^T lanes -> X staging [token][feature]; warps 4-7: U~^T lanes -> U~ rows
-    const int r = (warp & 3) * 32 + lane;
-    float v[64];
+    // warp w: lanes 32 (w % 4); w / 4 = 0, 1: W^T column halves -> X staging [token][feature];
+    // w / 4 = 2, 3: U~^T column halves -> U~ rows
+    const int r = (warp & 3) * 32 + lane, part = warp >> 2, i0 = (part & 1) * 32;
+    float v[32];
+    const int col = (part < 2 ? 64 : 128) + i0;
+    tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, col), v);
+    tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, col + 16), v + 16);
+    if (part < 2) {
 #pragma unroll
-    for (int c0 = 0; c0 < 64; c0 += 16)
-      tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, (warp < 4 ? 64 : 128) + c0), v + c0);
-    if (warp < 4) {
-#pragma unroll
-      for (int i = 0; i < 64; ++i) X[i * XS + r] = v[i];
+      for (int i = 0; i < 32; ++i) X[(i0 + i) * XS + r] = v[i];
     } else {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) rec_ut[i * D + r] = v[i];
+      for (int i = 0; i < 32; ++i) rec_ut[(i0 + i) * D + r] = v[i];
     }
   }
   __syncthreads();
@@ -570,29 +561,43 @@ struct StateSmem {
   static constexpr uint32_t BYTES = MISC + 64;
 };
 
-// z-gated RMSNorm of one chunk's outputs, by the four loader warps: O (f32 [64 tokens][128],
+// z-gated RMSNorm of one chunk's outputs, by the four epilogue warps: O (f32 [64 tokens][128],
 // staged in shared memory) -> out.  Warp w takes tokens w, w+4, ...; lane l the 4 channels 4l..4l+3.
 template <typename T>
-__device__ __forceinline__ void chunk_epilogue(const float* Ost, const T* __restrict__ z,
-                                               T* __restrict__ out, const float4 wn4, int t0, int L,
-                                               int h, int Hv, float eps, bool valid) {
+__device__ __forceinline__ void chunk_load_z(const T* __restrict__ z, float4* zz, int t0, int L,
+                                             int h, int Hv) {
   const int w = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
   const size_t ld = (size_t)Hv * D;
-  float4 zz[16];
 #pragma unroll
   for (int m = 0; m < 16; ++m) {
     const int i = min(w + 4 * m, L - 1);
     zz[m] = Act<T>::ldg4(z + (size_t)(t0 + i) * ld + (size_t)h * D + 4 * lane);
   }
+}
+
+template <typename T>
+__device__ __forceinline__ void chunk_epilogue(const float* Ost, const float4* zz,
+                                               T* __restrict__ out, const float4 wn4, int t0, int L,
+                                               int h, int Hv, float eps, bool valid) {
+  const int w = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+  const size_t ld = (size_t)Hv * D;
+  float4 o[16];
+  float ss[16];
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    o[m] = *reinterpret_cast<const float4*>(Ost + (w + 4 * m) * D + 4 * lane);
+    ss[m] = o[m].x * o[m].x + o[m].y * o[m].y + o[m].z * o[m].z + o[m].w * o[m].w;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int m = 0; m < 16; ++m) ss[m] += __shfl_xor_sync(0xffffffffu, ss[m], off);
 #pragma unroll
   for (int m = 0; m < 16; ++m) {
     const int i = w + 4 * m;
-    const float4 o = *reinterpret_cast<const float4*>(Ost + i * D + 4 * lane);
-    float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
-    ss = warp_sum(ss);
-    const float inv = valid ? 1.0f / sqrtf(ss / (float)D + eps) : 0.f;
-    const float4 r = make_float4(o.x * inv * wn4.x * silu_fast(zz[m].x), o.y * inv * wn4.y * silu_fast(zz[m].y),
-                                 o.z * inv * wn4.z * silu_fast(zz[m].z), o.w * inv * wn4.w * silu_fast(zz[m].w));
+    const float inv = valid ? rsqrtf(ss[m] * (1.0f / (float)D) + eps) : 0.f;
+    const float4 r = make_float4(o[m].x * inv * wn4.x * silu_fast(zz[m].x), o[m].y * inv * wn4.y * silu_fast(zz[m].y),
+                                 o[m].z * inv * wn4.z * silu_fast(zz[m].z), o[m].w * inv * wn4.w * silu_fast(zz[m].w));
     if (i < L) Act<T>::store4(out + (size_t)(t0 + i) * ld + (size_t)h * D + 4 * lane, r);
   }
 }
@@ -694,23 +699,42 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       for (int k = 0; k < 16; ++k) v[k] = init ? v[k] : 0.f;
       tc::tmem_st16(lane_base + c0, v);
     }
+    float ut[64];   // U~ column e of the current chunk, loaded one chunk ahead
+    if (nch > 0) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) ut[i] = reinterpret_cast<const float*>(rec_of(0) + R_UT)[i * D + e];
+    }
     for (int c = 0; c < nch; ++c) {
       const unsigned char* rec = rec_of(c);
       const uint32_t par = c & 1;
-      // A3 = split(S^T) from TMEM
+      // A3 = split(S^T) from TMEM, and S^T <- e^{gamma_L} S^T in the same pass (MMA3 reads the
+      // unscaled copy in shared memory; MMA4 accumulates onto the scaled one)
+      const float egL = *reinterpret_cast<const float*>(rec + R_SC);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        float v[16];
-        tc::tmem_ld16(lane_base + c0, v);
+      for (int hb = 0; hb < D; hb += 64) {
+        uint32_t rv[64];
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nw(lane_base + hb + 16 * q, rv + 16 * q);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::reg_fence16(rv + 16 * q);
+        float v[64];
+#pragma unroll
+        for (int k = 0; k < 64; ++k) v[k] = __uint_as_float(rv[k]);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
           uint4 hh, ll;
           split8(v + 8 * g, hh, ll);
-          const uint32_t off = tc::kmajor_off(e, c0 + 8 * g, 128);
+          const uint32_t off = tc::kmajor_off(e, hb + 8 * g, 128);
           st_unit(a3h, off, hh);
           st_unit(a3l, off, ll);
         }
+#pragma unroll
+        for (int k = 0; k < 64; ++k) v[k] *= egL;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::tmem_st16_nw(lane_base + hb + 16 * q, v + 16 * q);
       }
+      tc::tmem_wait_st();
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       bar_sync_main();
@@ -727,19 +751,6 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         }
         tc::mma_commit(mma3);
       }
-      // meanwhile: S^T *= e^{gamma_L};  U~ column e into registers
-      const float egL = *reinterpret_cast<const float*>(rec + R_SC);
-#pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        float v[16];
-        tc::tmem_ld16(lane_base + c0, v);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] *= egL;
-        tc::tmem_st16(lane_base + c0, v);
-      }
-      float ut[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) ut[i] = reinterpret_cast<const float*>(rec + R_UT)[i * D + e];
       wait_or_abort(mma3, par, abort, status);
       if (e == 0 && c + 1 < nch && !*abort) {                          // B3 free again
         load_b3(c + 1);
@@ -748,20 +759,29 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       if (c > 0) wait_or_abort(oempty, (c - 1) & 1, abort, status);   // staging read by loaders
       tc::fence_after_sync();
       // U^T = U~^T - (W S)^T  -> A4
+      {
+        uint32_t rv[64];
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        float v[16];
-        tc::tmem_ld16(lane_base + 192 + c0, v);
+        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nw(lane_base + 192 + 16 * q, rv + 16 * q);
+        tc::tmem_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = ut[c0 + k] - v[k];
+        for (int q = 0; q < 4; ++q) tc::reg_fence16(rv + 16 * q);
+        float v[64];
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int k = 0; k < 64; ++k) v[k] = ut[k] - __uint_as_float(rv[k]);
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
           uint4 hh, ll;
           split8(v + 8 * g, hh, ll);
-          const uint32_t off = tc::kmajor_off(e, c0 + 8 * g, 64);
+          const uint32_t off = tc::kmajor_off(e, 8 * g, 64);
           st_unit(a4h, off, hh);
           st_unit(a4l, off, ll);
         }
+      }
+      if (c + 1 < nch) {
+        const float* un = reinterpret_cast<const float*>(rec_of(c + 1) + R_UT);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) ut[i] = un[i * D + e];
       }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -786,19 +806,25 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       }
       tc::fence_after_sync();
       // O^T row e (tokens 0..63) -> staging (A4 is free once MMA4 completed); loaders normalise
-      float o[64];
+      {
+        uint32_t rv[64];
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) tc::tmem_ld16(lane_base + 128 + c0, o + c0);
+        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nw(lane_base + 128 + 16 * q, rv + 16 * q);
+        tc::tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 64; ++i) Ost[i * D + e] = o[i];
+        for (int q = 0; q < 4; ++q) tc::reg_fence16(rv + 16 * q);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) Ost[i * D + e] = __uint_as_float(rv[i]);
+      }
       mbar_arrive(ofull);
       tc::fence_before_sync();
       bar_sync_main();
     }
     // after a timeout: wait (bounded) for bulk copies still in flight before the CTA exits
+    // (copy c + 1 is only issued once copy c was consumed, so at most the last one is pending)
     if (e == 0 && *abort) {
-      for (int c = 0; c < issued3; ++c) tc::mbar_wait(b3full, c & 1, 100000000ull);
-      for (int c = 0; c < issued4; ++c) tc::mbar_wait(b4full, c & 1, 100000000ull);
+      if (issued3 > 0) tc::mbar_wait(b3full, (issued3 - 1) & 1, 100000000ull);
+      if (issued4 > 0) tc::mbar_wait(b4full, (issued4 - 1) & 1, 100000000ull);
     }
     // final state back to the slot
     if (valid) {
@@ -814,11 +840,15 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     // ================= epilogue warps: z-gated RMSNorm of every chunk's staged outputs
     const int lt = tid - 128;
     const float4 wn4 = Act<T>::ldg4(norm_w + 4 * (lt & 31));
+    float4 zz[16];   // z of the next chunk to normalise, loaded while the MMAs run
+    if (nch > 0) chunk_load_z<T>(z, zz, seq_start, min(CH, len), h, d.Hv);
     for (int c = 0; c < nch; ++c) {
       wait_or_abort(ofull, c & 1, abort, status);
-      chunk_epilogue<T>(Ost, z, out, wn4, seq_start + c * CH, min(CH, len - c * CH), h, d.Hv,
+      chunk_epilogue<T>(Ost, zz, out, wn4, seq_start + c * CH, min(CH, len - c * CH), h, d.Hv,
                         d.norm_eps, valid);
       mbar_arrive(oempty);
+      if (c + 1 < nch)
+        chunk_load_z<T>(z, zz, seq_start + (c + 1) * CH, min(CH, len - (c + 1) * CH), h, d.Hv);
     }
   }
   tc::fence_before_sync();
@@ -856,7 +886,7 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
     return GDN_ERR_CUDA;
   float* wsf = static_cast<float*>(ws);
   if (total > 0)
-    k1<<<dim3(nc_max, d.Hv), 256, IntraSmem::BYTES, stream>>>(
+    k1<<<dim3(nc_max, d.Hv), NTI, IntraSmem::BYTES, stream>>>(
         d, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
         static_cast<const T*>(pool->conv_state), pool->num_slots, cu, slot_idx, has_init, num_seqs,
         total, static_cast<const T*>(qkv), static_cast<const T*>(a), static_cast<const T*>(b), wsf,
