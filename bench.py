@@ -64,6 +64,29 @@ def dist_env():
     return ws, rank, local
 
 
+def reduce_over_ranks(dist, ms: float, units: float, device="cpu"):
+    """(max over ranks of the timed region in ms, sum over ranks of the work done).
+
+    Every rank runs an independent replica of the workload (decode rows and slots shard with no
+    exchange), so the job's throughput is the summed work over the slowest rank's time."""
+    if dist is None:
+        return ms, units
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def decode_config(wl, ws: int) -> dict:
+    geo = wl.geo
+    return {"workload": wl.name, "batch_rows": wl.batch, "k_heads": geo.Hk, "v_heads": geo.Hv,
+            "head_dim": geo.dk, "slots": wl.num_slots, "act_dtype": "bf16", "state_dtype": "f32",
+            "l2": "no flush: 402.65 MB state working set per step > 129 MB L2",
+            "parallelism": f"replicas x{ws} (rows/slots shard, no exchange)"}
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 100 ms while the GPU is busy."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -183,13 +206,11 @@ def run_ours(args, ws, rank, local):
             i += 1
         torch.cuda.synchronize()
     clocks = sampler.stop()
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms_local = ms
+    ms, total_bytes_moved = reduce_over_ranks(dist, ms, float(state_bytes) * args.steps, "cuda")
     ms_step = ms / args.steps
-    gbs = state_bytes * args.steps * ws / (ms * 1e-3) / 1e9
-    per_launch_gbs = state_bytes / (ms_step * 1e-3) / 1e9
+    gbs = total_bytes_moved / (ms * 1e-3) / 1e9
+    per_launch_gbs = state_bytes / (ms_local / args.steps * 1e-3) / 1e9
 
     if args.only == "decode":
         if rank == 0:
@@ -223,11 +244,8 @@ def run_ours(args, ws, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_gbs = state_bytes * args.steps * ws / (e2e_ms * 1e-3) / 1e9
+    e2e_ms, e2e_bytes = reduce_over_ranks(dist, e2e_ms, float(state_bytes) * args.steps, "cuda")
+    e2e_gbs = e2e_bytes / (e2e_ms * 1e-3) / 1e9
     del ring, host, dev_in
 
     # ---------------- compaction at step 256 of the B=64 workload (56 survivors -> [0,56))
@@ -272,11 +290,7 @@ def run_ours(args, ws, rank, local):
         "metric": METRIC, "value": round(gbs, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "batch_rows": wl.batch, "k_heads": geo.Hk,
-                   "v_heads": geo.Hv, "head_dim": geo.dk, "slots": wl.num_slots,
-                   "act_dtype": "bf16", "state_dtype": "f32",
-                   "l2": "no flush: 402.65 MB state working set per step > 129 MB L2",
-                   "parallelism": f"replicas x{ws} (rows/slots shard, no exchange)"},
+        "config": decode_config(wl, ws),
         "row_steps_per_s": round(wl.batch * ws * args.steps / (ms * 1e-3), 1),
         "hbm_frac_state": round(per_launch_gbs / hbm_peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(per_launch_gbs, 2), "peak": hbm_peak,
@@ -356,6 +370,11 @@ def _oracle_decode_steps(n_steps, rows):
     return time.perf_counter() - t0, geo
 
 
+def synth_workload():
+    from gated_deltanet_linear_09_gb300 import synth
+    return synth.workloads()[DECODE_WL]
+
+
 def synth_inputs(wl, t, rows):
     from gated_deltanet_linear_09_gb300 import synth
     return synth.make_token_inputs(wl.geo, rows, wl.seed, 100, t)
@@ -391,7 +410,7 @@ def run_reference(args, ws, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3 / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "decode_B64_Hk16_Hv48_d128_bf16", "batch_rows": rows},
+        "config": decode_config(synth_workload(), ws),
         "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} full B=64 decode steps, float64 C oracle, "
                                    "single thread"},

@@ -24,14 +24,24 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lib = None
 
 
+def compile_to(src: str, out: str) -> None:
+    """Compile an oracle source file into a shared library (gcc, -O2, no FMA contraction)."""
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle into oracle/_build/liboracle.so (gcc, -O2, no FMA contraction)."""
+    """Compile the oracle into oracle/_build/liboracle.so.  GDN_ORACLE_LIB, when set, names an
+    already built library to load instead (the mutation tests point it at deliberately broken
+    copies of the oracle)."""
+    override = os.environ.get("GDN_ORACLE_LIB")
+    if override:
+        return override
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-               "-o", tmp, _SRC, "-lm"]
-        subprocess.run(cmd, check=True)
+        compile_to(_SRC, tmp)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 

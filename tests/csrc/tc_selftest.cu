@@ -83,3 +83,29 @@ extern "C" int tc_gemm(const float* A, const float* B, float* D, int N, int K, i
   if (cudaGetLastError() != cudaSuccess) return -3;
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
 }
+
+// A bounded wait that nothing completes: the mbarrier is initialised for one arrival that never
+// comes, so the wait must give up after limit_ns and report it instead of hanging.
+__global__ void mbar_timeout_kernel(unsigned long long limit_ns, int* __restrict__ status,
+                                    unsigned long long* __restrict__ waited_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const uint64_t t0 = globaltimer_ns();
+  const bool ok = mbar_wait(&bar, 0, limit_ns);
+  const uint64_t t1 = globaltimer_ns();
+  if (threadIdx.x == 0) {
+    *status = ok ? 0 : 4;
+    *waited_ns = t1 - t0;
+  }
+}
+
+extern "C" int tc_timeout_probe(unsigned long long limit_ns, int* status,
+                                unsigned long long* waited_ns) {
+  mbar_timeout_kernel<<<1, 32>>>(limit_ns, status, waited_ns);
+  if (cudaGetLastError() != cudaSuccess) return -3;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
+}

@@ -56,3 +56,17 @@ def test_tc_gemm(lib, N, K):
     e1 = np.max(np.abs(ref1 - ref)) / np.max(np.abs(ref))
     assert e3 < 2e-5, e3
     assert e3 < e1 / 20
+
+
+def test_bounded_wait_gives_up_and_reports(lib):
+    """A wait on an mbarrier phase that never completes returns after its limit with the
+    timeout status; the GPU context stays usable (a GEMM runs right after)."""
+    lib.tc_timeout_probe.restype = ctypes.c_int
+    lib.tc_timeout_probe.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p, ctypes.c_void_p]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    limit = 2_000_000  # 2 ms
+    assert lib.tc_timeout_probe(limit, status.data_ptr(), waited.data_ptr()) == 0
+    assert int(status.item()) == 4
+    assert limit <= int(waited.item()) < 1_000_000_000
+    test_tc_gemm(lib, 64, 128)
