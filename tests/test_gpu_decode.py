@@ -248,3 +248,40 @@ def test_compaction_many_pairs():
     exp = before.copy()
     exp[dst] = before[src]
     np.testing.assert_array_equal(_np(layer.rec_state), exp)
+
+
+def test_decode_step_captured_in_cuda_graph():
+    """gdn_decode_step is one launch with no host reads and no allocation: it can be captured in
+    a CUDA graph and replayed; replays are bit-identical to eager calls on the same inputs."""
+    geo = synth.Geometry(4, 8, 128, 128, 4, synth.BF16)
+    layer, w, rec, conv = _layer(geo, 560, 10, True)
+    slots = torch.tensor([3, 7, -1, 0, 9], dtype=torch.int32, device="cuda")
+    steps = [layer.inputs(synth.make_token_inputs(geo, 5, 561, t)) for t in range(4)]
+    # eager reference
+    eager = []
+    for x in steps:
+        eager.append(_np(layer.decode_step(slots, **x)))
+    eager_state = _np(layer.rec_state).copy()
+    # captured: static input buffers refilled before each replay
+    layer.load_state(rec, conv)
+    static = {k: torch.empty_like(v) for k, v in steps[0].items()}
+    out = torch.empty((5, geo.zdim), dtype=torch.bfloat16, device="cuda")
+    for k in static:
+        static[k].copy_(steps[0][k])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            layer.decode_step(slots, static["qkv"], static["z"], static["a"], static["b"], out,
+                              stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    # capture does not run the kernel: state still at its initial value
+    np.testing.assert_array_equal(_np(layer.rec_state), rec)
+    for t, x in enumerate(steps):
+        for k in static:
+            static[k].copy_(x[k])
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(_np(out), eager[t])
+    np.testing.assert_array_equal(_np(layer.rec_state), eager_state)
