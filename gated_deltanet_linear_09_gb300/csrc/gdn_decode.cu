@@ -13,6 +13,8 @@
 //   kv = S^T k,  sq = S^T q           (one pass over the old S, held in registers)
 //   delta = beta (v - e^g kv),  o = e^g sq + (k.q) delta
 //   S' = e^g S + k delta^T            (written back from the same registers)
+#include <mutex>
+
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -88,24 +90,49 @@ decode_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict_
     return;
   }
 
-  // ---- conv update + SiLU over the channels this unit owns
+  // ---- conv update + SiLU over the channels this unit owns.  The loads of a thread's channels
+  // are all issued before any of them is used (one memory round trip for the prologue).
   const T* x_row = qkv + (size_t)row * d.cqkv;
   T* cs = conv_state + (size_t)s * 3 * d.cqkv;
   const int nch = 2 * DK + r * DV;
-  for (int c = tid; c < nch; c += kDecodeThreads) {
-    int ch;
-    float* dst;
-    if (c < DK) {
-      ch = kh * DK + c;
-      dst = qs + c;
-    } else if (c < 2 * DK) {
-      ch = d.Hk * DK + kh * DK + (c - DK);
-      dst = ks + (c - DK);
-    } else {
-      ch = 2 * d.Hk * DK + kh * r * DV + (c - 2 * DK);
-      dst = vs + (c - 2 * DK);
+  for (int c0 = 0; c0 < nch; c0 += 3 * kDecodeThreads) {
+    int chs[3];
+    float* dsts[3];
+    T xr[3], s0[3], s1[3], s2[3];
+    float wv[3][4];
+#pragma unroll
+    for (int m = 0; m < 3; ++m) {
+      const int c = min(c0 + tid + m * kDecodeThreads, nch - 1);   // clamped: always a valid channel
+      if (c < DK) {
+        chs[m] = kh * DK + c;
+        dsts[m] = qs + c;
+      } else if (c < 2 * DK) {
+        chs[m] = d.Hk * DK + kh * DK + (c - DK);
+        dsts[m] = ks + (c - DK);
+      } else {
+        chs[m] = 2 * d.Hk * DK + kh * r * DV + (c - 2 * DK);
+        dsts[m] = vs + (c - 2 * DK);
+      }
+      xr[m] = x_row[chs[m]];
+      s0[m] = cs[chs[m]];
+      s1[m] = cs[d.cqkv + chs[m]];
+      s2[m] = cs[2 * d.cqkv + chs[m]];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) wv[m][j] = Act<T>::ldg(conv_w + (size_t)chs[m] * 4 + j);
     }
-    *dst = conv_channel<T>(conv_w, cs, d.cqkv, ch, x_row[ch]);
+#pragma unroll
+    for (int m = 0; m < 3; ++m) {
+      if (c0 + tid + m * kDecodeThreads < nch) {
+        float acc = wv[m][3] * Act<T>::load(&xr[m]);
+        acc = fmaf(wv[m][0], Act<T>::load(&s0[m]), acc);
+        acc = fmaf(wv[m][1], Act<T>::load(&s1[m]), acc);
+        acc = fmaf(wv[m][2], Act<T>::load(&s2[m]), acc);
+        cs[chs[m]] = s1[m];
+        cs[d.cqkv + chs[m]] = s2[m];
+        cs[2 * d.cqkv + chs[m]] = xr[m];
+        *dsts[m] = siluf_(acc);
+      }
+    }
   }
   __syncthreads();
 
@@ -194,11 +221,18 @@ decode_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict_
       ss = warp_sum(ss);
       const float inv = 1.0f / sqrtf(ss / (float)DV + d.norm_eps);
       const T* zr = z + (size_t)row * d.Hv * DV + (size_t)h * DV;
+      if constexpr (CPT == 4) {
+        const float4 zz = Act<T>::ldg4(zr + lane * 4), ww = Act<T>::ldg4(norm_w + lane * 4);
+        Act<T>::store4(out_row + (size_t)h * DV + lane * 4,
+                       make_float4(o[0] * inv * ww.x * siluf_(zz.x), o[1] * inv * ww.y * siluf_(zz.y),
+                                   o[2] * inv * ww.z * siluf_(zz.z), o[3] * inv * ww.w * siluf_(zz.w)));
+      } else {
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) {
-        const int j = lane * CPT + c;
-        const float zz = Act<T>::ldg(zr + j);
-        Act<T>::store(out_row + (size_t)h * DV + j, o[c] * inv * Act<T>::ldg(norm_w + j) * siluf_(zz));
+        for (int c = 0; c < CPT; ++c) {
+          const int j = lane * CPT + c;
+          const float zz = Act<T>::ldg(zr + j);
+          Act<T>::store(out_row + (size_t)h * DV + j, o[c] * inv * Act<T>::ldg(norm_w + j) * siluf_(zz));
+        }
       }
     }
   }
@@ -230,11 +264,19 @@ int launch_decode_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
                     const void* b, void* out, cudaStream_t stream) {
   const size_t smem = sizeof(float) * (2 * DK + d.r * DV + 4 * kDecodeWarps * DV + 4);
   auto kern = decode_kernel<DK, DV, T>;
-  if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return GDN_ERR_TOO_LARGE;
-  }
+  // Raised once per kernel (to the per-block maximum), so that launches -- also those recorded
+  // into a CUDA graph -- never need to change the attribute.
+  static std::once_flag once;
+  static int attr_rc = 0;
+  std::call_once(once, [&] {
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess)
+      attr_rc = GDN_ERR_CUDA;
+  });
+  if (attr_rc != 0) return attr_rc;
+  if (smem > 227 * 1024) return GDN_ERR_TOO_LARGE;
   dim3 grid(d.Hk, B);
   kern<<<grid, kDecodeThreads, smem, stream>>>(
       d, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
