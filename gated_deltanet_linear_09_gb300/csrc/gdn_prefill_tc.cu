@@ -171,30 +171,35 @@ __device__ bool seq_chunk_offset(const int32_t* __restrict__ cu, int num_seqs, i
 
 constexpr int XS = 132;   // row stride (floats) of the f32 staging tile
 constexpr int AS = 68;    // row stride of the A matrix (16-byte aligned rows)
+constexpr int NTI = 256;  // threads of the intra kernel (8 warps); two CTAs share an SM
 
+// Shared memory, ~100 KB so that two CTAs fit on one SM.  Regions are reused along the kernel:
+//   A1  [0, 64K)   : [K;Q] split-bf16 operand of MMA1  (hi K | hi Q | lo K | lo Q, 16 KiB each);
+//                    after MMA1: (beta e^g K)^T hi/lo in the Q quarters, (beta V)^T hi/lo in the
+//                    K quarters (each [128 x 64] tile is exactly 16 KiB).
+//   X   [64K, +33792): f32 staging [64][XS]; after the V tiles: A [64][AS] (17,408 B) followed by
+//                    the B2 tile (T rows, hi 8 KiB + lo 8 KiB); after MMA2: the W readout.
 struct IntraSmem {
-  static constexpr uint32_t A1 = 0;                    // hi [128x128] then lo
-  static constexpr uint32_t A2A = A1 + 2 * 32768;      // (beta e^g K)^T, hi then lo [128x64]
-  static constexpr uint32_t A2B = A2A + 2 * 16384;     // (beta V)^T
-  static constexpr uint32_t B2 = A2B + 2 * 16384;      // T rows [64x64]
-  static constexpr uint32_t X = B2 + 2 * 8192;         // f32 [64][XS]
-  static constexpr uint32_t AM = X + 4 * 64 * XS;      // f32 [64][AS]
-  static constexpr uint32_t VEC = AM + 4 * 64 * AS;    // f32 gam, bet, eg, dec, bgk [5][64]
-  static constexpr uint32_t BAR = VEC + 4 * 5 * 64;    // mbarrier
-  static constexpr uint32_t MISC = BAR + 16;           // tmem slot, flags
+  static constexpr uint32_t A1 = 0;
+  static constexpr uint32_t K_HI = 0, Q_HI = 16384, K_LO = 32768, Q_LO = 49152;
+  static constexpr uint32_t X = 65536;
+  static constexpr uint32_t AM = X;                        // aliases X
+  static constexpr uint32_t B2 = X + 4 * 64 * AS;          // aliases X (17,408 B in)
+  static constexpr uint32_t VEC = X + 4 * 64 * XS;         // f32 gam, bet, eg, dec, bgk [5][64]
+  static constexpr uint32_t BAR = VEC + 4 * 5 * 64;        // mbarrier
+  static constexpr uint32_t MISC = BAR + 16;               // tmem slot, flags
   static constexpr uint32_t BYTES = MISC + 64;
 };
-
-constexpr int NTI = 512;   // threads of the intra kernel (16 warps)
+static_assert(IntraSmem::B2 + 16384 <= IntraSmem::VEC, "A and B2 must fit in the staging tile");
 
 // conv + SiLU of 128 channels [cb, cb+128) over the chunk's tokens into X (rows >= L zero), split
 // into a load step (all loads in flight, results in registers) and a compute step, so that the
 // next channel group's loads overlap the current group's processing.
-// Thread t: channel t & 127, tokens [16 (t >> 7), +16).
+// Thread t: channel t & 127, tokens [32 (t >> 7), +32).
 struct ConvIn {
   float w[4];
   float hist[3];
-  float xs[16];
+  float xs[32];
 };
 
 template <typename T>
@@ -203,7 +208,7 @@ __device__ __forceinline__ void conv_load(const KDims& d, const T* __restrict__ 
                                           bool init, int cb, int seq_start, int seq_len, int t0,
                                           int L, ConvIn& in) {
   const int tid = threadIdx.x;
-  const int f = tid & 127, i0 = (tid >> 7) * 16;
+  const int f = tid & 127, i0 = (tid >> 7) * 32;
   const int ch = cb + f;
 #pragma unroll
   for (int q = 0; q < 4; ++q) in.w[q] = Act<T>::ldg(conv_w + (size_t)ch * 4 + q);
@@ -220,16 +225,16 @@ __device__ __forceinline__ void conv_load(const KDims& d, const T* __restrict__ 
     in.hist[m] = (p >= seq_len) ? 0.f : (p >= 0 ? xq : (init ? xc : 0.f));
   }
 #pragma unroll
-  for (int k = 0; k < 16; ++k)
+  for (int k = 0; k < 32; ++k)
     in.xs[k] = Act<T>::ldg(qkv + (size_t)(t0 + min(i0 + k, L - 1)) * d.cqkv + ch);
 }
 
 __device__ __forceinline__ void conv_compute(const ConvIn& in, int L, float* X) {
   const int tid = threadIdx.x;
-  const int f = tid & 127, i0 = (tid >> 7) * 16;
+  const int f = tid & 127, i0 = (tid >> 7) * 32;
   float xm3 = in.hist[0], xm2 = in.hist[1], xm1 = in.hist[2];
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
+  for (int k = 0; k < 32; ++k) {
     float acc = in.w[3] * in.xs[k];
     acc = fmaf(in.w[0], xm3, acc);
     acc = fmaf(in.w[1], xm2, acc);
@@ -253,10 +258,9 @@ __device__ __forceinline__ void l2norm_rows(float* X, float eps, float scale) {
   }
 }
 
-// Rows of X -> rows [row0, row0+64) of a 128-column K-major shared tile (hi / lo).
+// Rows [0,64) of X -> rows [0,64) of a 128-column K-major shared tile (hi / lo quarter).
 // Unit u: row & 7 = u & 7, k-group = (u >> 3) & 15, row group = u >> 7 (conflict-free stores).
-__device__ __forceinline__ void x_rows_to_tile(const float* X, unsigned char* hi, unsigned char* lo,
-                                               int row0) {
+__device__ __forceinline__ void x_rows_to_tile(const float* X, unsigned char* hi, unsigned char* lo) {
   for (int u = threadIdx.x; u < 1024; u += NTI) {
     const int r = ((u >> 7) << 3) + (u & 7), kg = (u >> 3) & 15;
     const float4 a = *reinterpret_cast<const float4*>(X + r * XS + kg * 8);
@@ -264,9 +268,8 @@ __device__ __forceinline__ void x_rows_to_tile(const float* X, unsigned char* hi
     const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     uint4 hh, ll;
     split8(v, hh, ll);
-    const uint32_t off = (uint32_t)(row0 * 256) + (uint32_t)u * 16u;
-    st_unit(hi, off, hh);
-    st_unit(lo, off, ll);
+    st_unit(hi, (uint32_t)u * 16u, hh);
+    st_unit(lo, (uint32_t)u * 16u, ll);
   }
 }
 
@@ -286,8 +289,31 @@ __device__ __forceinline__ void x_cols_to_tile(const float* X, const float* scal
   }
 }
 
+// (scale_j * K_j)^T tile [128 features][64 tokens] built from the K rows of A1 (hi + lo, about
+// 16 significant bits), written into other shared memory (hi / lo).
+__device__ __forceinline__ void a1k_cols_to_tile(const unsigned char* khi, const unsigned char* klo,
+                                                 const float* scale, unsigned char* hi,
+                                                 unsigned char* lo) {
+  for (int u = threadIdx.x; u < 1024; u += NTI) {
+    const int f = ((u >> 6) << 3) + (u & 7), jg = (u >> 3) & 7;
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int j = jg * 8 + q;
+      const uint32_t off = tc::kmajor_off(j, f, 128);
+      const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(khi + off)) +
+                       __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(klo + off));
+      v[q] = kv * scale[j];
+    }
+    uint4 hh, ll;
+    split8(v, hh, ll);
+    st_unit(hi, (uint32_t)u * 16u, hh);
+    st_unit(lo, (uint32_t)u * 16u, ll);
+  }
+}
+
 template <typename T>
-__global__ void __launch_bounds__(NTI, 1)
+__global__ void __launch_bounds__(NTI, 2)
 tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict__ dt_bias,
                 const T* __restrict__ conv_w, const T* __restrict__ conv_state, int num_slots,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ slot_idx,
@@ -296,16 +322,11 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
                 float* __restrict__ ws, int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
   using S = IntraSmem;
-  unsigned char* a1h = sm + S::A1;
-  unsigned char* a1l = a1h + 32768;
-  unsigned char* a2ah = sm + S::A2A;
-  unsigned char* a2al = a2ah + 16384;
-  unsigned char* a2bh = sm + S::A2B;
-  unsigned char* a2bl = a2bh + 16384;
-  unsigned char* b2h = sm + S::B2;
-  unsigned char* b2l = b2h + 8192;
+  unsigned char* a1 = sm + S::A1;
   float* X = reinterpret_cast<float*>(sm + S::X);
   float* Am = reinterpret_cast<float*>(sm + S::AM);
+  unsigned char* b2h = sm + S::B2;
+  unsigned char* b2l = b2h + 8192;
   float* gam = reinterpret_cast<float*>(sm + S::VEC);
   float* bet = gam + 64;
   float* eg = bet + 64;
@@ -384,35 +405,34 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     bgk[tid] = bet[tid] * expf(gam[tid]);
   }
 
-  // ---- K: conv, l2norm, A1 rows 0-63, (beta e^g K)^T, K~^T rows of B4
-  ConvIn cin, cnext;
+  // ---- K: conv, l2norm, A1 K rows, K~^T rows of B4
+  ConvIn cin;
   conv_load<T>(d, qkv, conv_w, cs, init, d.Hk * D + kh * D, seq_start, seq_len, t0, L, cin);
-  conv_load<T>(d, qkv, conv_w, cs, init, kh * D, seq_start, seq_len, t0, L, cnext);
   conv_compute(cin, L, X);
+  conv_load<T>(d, qkv, conv_w, cs, init, kh * D, seq_start, seq_len, t0, L, cin);   // Q, in flight
   __syncthreads();
   l2norm_rows(X, d.l2_eps, 1.0f);
   __syncthreads();
-  x_rows_to_tile(X, a1h, a1l, 0);
-  x_cols_to_tile(X, bgk, a2ah, a2al);
+  x_rows_to_tile(X, a1 + S::K_HI, a1 + S::K_LO);
   x_cols_to_gtile64(X, dec, rec + R_B4, rec + R_B4 + B4_HALF);
   __syncthreads();
-  // ---- Q: conv, l2norm (times q_scale), A1 rows 64-127, Q~ rows of B3
-  conv_compute(cnext, L, X);
-  conv_load<T>(d, qkv, conv_w, cs, init, 2 * d.Hk * D + h * D, seq_start, seq_len, t0, L, cin);
+  // ---- Q: conv, l2norm (times q_scale), A1 Q rows, Q~ rows of B3
+  conv_compute(cin, L, X);
+  conv_load<T>(d, qkv, conv_w, cs, init, 2 * d.Hk * D + h * D, seq_start, seq_len, t0, L, cin);  // V
   __syncthreads();
   l2norm_rows(X, d.l2_eps, d.q_scale);
   __syncthreads();
-  x_rows_to_tile(X, a1h, a1l, 64);
+  x_rows_to_tile(X, a1 + S::Q_HI, a1 + S::Q_LO);
   x_rows_to_gtile128(X, eg, rec + R_B3, rec + R_B3 + B3_HALF, 0);
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tb = *tslot;
-  // ---- D1 = [K;Q] K^T  (cols [0,64))
+  // ---- D1 = [K;Q] K^T  (cols [0,64)); A1's hi quarters [K|Q] and lo quarters form 128-row tiles
   if (tid == 0) {
     const uint32_t id = tc::idesc_bf16(128, 64);
-    const uint32_t ah = tc::smem_u32(a1h), al = tc::smem_u32(a1l);
+    const uint32_t ah = tc::smem_u32(a1 + S::K_HI), al = tc::smem_u32(a1 + S::K_LO);
     for (int k = 0; k < 8; ++k) {
       tc::mma_bf16(tb, tc::kstep_desc(ah, 128, k), tc::kstep_desc(ah, 128, k), id, k > 0);
       tc::mma_bf16(tb, tc::kstep_desc(ah, 128, k), tc::kstep_desc(al, 128, k), id, 1);
@@ -420,24 +440,28 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     }
     tc::mma_commit(bar);
   }
-  // ---- V (overlaps the MMA): conv, (beta V)^T
+  // ---- V (overlaps the MMA): conv into X
   conv_compute(cin, L, X);
-  __syncthreads();
-  x_cols_to_tile(X, bet, a2bh, a2bl);
-  // ---- A and P from D1
+  // ---- A1 is free once MMA1 completed: (beta e^g K)^T into its Q quarters, then (beta V)^T
+  // into its K quarters
   wait_or_abort(bar, 0, abort, status);
   tc::fence_after_sync();
+  a1k_cols_to_tile(a1 + S::K_HI, a1 + S::K_LO, bgk, a1 + S::Q_HI, a1 + S::Q_LO);
+  __syncthreads();
+  x_cols_to_tile(X, bet, a1 + S::K_HI, a1 + S::K_LO);
+  __syncthreads();   // X (V) consumed: A and B2 take its place
+  // ---- A and P from D1: warp w reads TMEM lanes 32 (w % 4) and the 32 columns of half w / 4
   {
-    // warp w reads TMEM lanes 32 (w % 4) .. +31 and the 16 columns of quarter w / 4
-    const int r = (warp & 3) * 32 + lane, j0 = (warp >> 2) * 16;
-    float v[16];
+    const int r = (warp & 3) * 32 + lane, j0 = (warp >> 2) * 32;
+    float v[32];
     tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, j0), v);
+    tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, j0 + 16), v + 16);
     // branch-free: exponents clamped to <= 0, masked entries multiplied by zero
     if (r < 64) {
       const int i = r;
       const float gi = gam[i], bi = (i < L) ? bet[i] : 0.f;
 #pragma unroll
-      for (int q = 0; q < 16; ++q) {
+      for (int q = 0; q < 32; ++q) {
         const int j = j0 + q;
         const float m = (j < i) ? bi : 0.f;
         Am[i * AS + j] = m * exp_fast(fminf(gi - gam[j], 0.f)) * v[q];
@@ -446,7 +470,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
       const int i = r - 64;
       const float gi = gam[i], vi = (i < L) ? 1.f : 0.f;
 #pragma unroll
-      for (int q = 0; q < 16; q += 8) {
+      for (int q = 0; q < 32; q += 8) {
         float p8[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -463,16 +487,16 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   }
   __syncthreads();
   // ---- T = (I + A)^{-1} by forward substitution, T_i = e_i - sum_{j<i} A_ij T_j.  Warp w owns
-  // columns 4w..4w+3, lane l rows l and l + 32; at step j the owner of row j (already final)
+  // columns 8w..8w+7, lane l rows l and l + 32; at step j the owner of row j (already final)
   // broadcasts it.  A_ij = 0 for j >= i, so rows <= j are left unchanged.  T goes straight into
-  // the split-bf16 B2 tile (rows i, K = j): 4 consecutive columns are half a 16-byte unit.
+  // the split-bf16 B2 tile (rows i, K = j): 8 consecutive columns are one 16-byte unit.
   {
-    const int c0 = 4 * warp;
-    float t0[4], t1[4];
+    const int c0 = 8 * warp;
+    float t0r[8], t1r[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      t0[q] = (lane == c0 + q) ? 1.f : 0.f;
-      t1[q] = (lane + 32 == c0 + q) ? 1.f : 0.f;
+    for (int q = 0; q < 8; ++q) {
+      t0r[q] = (lane == c0 + q) ? 1.f : 0.f;
+      t1r[q] = (lane + 32 == c0 + q) ? 1.f : 0.f;
     }
 #pragma unroll
     for (int j4 = 0; j4 < 64; j4 += 4) {
@@ -482,25 +506,23 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) {
         const int j = j4 + jj;
-        float tj[4];
+        float tj[8];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tj[q] = __shfl_sync(0xffffffffu, j < 32 ? t0[q] : t1[q], j & 31);
+        for (int q = 0; q < 8; ++q) tj[q] = __shfl_sync(0xffffffffu, j < 32 ? t0r[q] : t1r[q], j & 31);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          t0[q] = fmaf(-a0s[jj], tj[q], t0[q]);
-          t1[q] = fmaf(-a1s[jj], tj[q], t1[q]);
+        for (int q = 0; q < 8; ++q) {
+          t0r[q] = fmaf(-a0s[jj], tj[q], t0r[q]);
+          t1r[q] = fmaf(-a1s[jj], tj[q], t1r[q]);
         }
       }
     }
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      const float* tv = half ? t1 : t0;
-      __nv_bfloat16 hq[4], lq[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tc::split_bf16(tv[q], hq[q], lq[q]);
+      uint4 hh, ll;
+      split8(half ? t1r : t0r, hh, ll);
       const uint32_t off = tc::kmajor_off(lane + 32 * half, c0, 64);
-      *reinterpret_cast<uint2*>(b2h + off) = *reinterpret_cast<const uint2*>(hq);
-      *reinterpret_cast<uint2*>(b2l + off) = *reinterpret_cast<const uint2*>(lq);
+      st_unit(b2h, off, hh);
+      st_unit(b2l, off, ll);
     }
   }
   tc::fence_proxy_async_smem();
@@ -511,8 +533,8 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   if (tid == 0 && !*abort) {
     const uint32_t id = tc::idesc_bf16(128, 64);
     const uint32_t bh = tc::smem_u32(b2h), bl = tc::smem_u32(b2l);
-    const uint32_t srcs[2][2] = {{tc::smem_u32(a2ah), tc::smem_u32(a2al)},
-                                 {tc::smem_u32(a2bh), tc::smem_u32(a2bl)}};
+    const uint32_t srcs[2][2] = {{tc::smem_u32(a1 + S::Q_HI), tc::smem_u32(a1 + S::Q_LO)},
+                                 {tc::smem_u32(a1 + S::K_HI), tc::smem_u32(a1 + S::K_LO)}};
     for (int m = 0; m < 2; ++m) {
       const uint32_t dt = tb + 64 + 64 * m;
       for (int k = 0; k < 4; ++k) {
@@ -526,19 +548,21 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   wait_or_abort(bar, 1, abort, status);
   tc::fence_after_sync();
   {
-    // warp w: lanes 32 (w % 4); w / 4 = 0, 1: W^T column halves -> X staging [token][feature];
-    // w / 4 = 2, 3: U~^T column halves -> U~ rows
-    const int r = (warp & 3) * 32 + lane, part = warp >> 2, i0 = (part & 1) * 32;
-    float v[32];
-    const int col = (part < 2 ? 64 : 128) + i0;
-    tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, col), v);
-    tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, col + 16), v + 16);
-    if (part < 2) {
+    // warps 0-3: W^T lanes -> X staging [token][feature]; warps 4-7: U~^T lanes -> U~ rows
+    const int r = (warp & 3) * 32 + lane;
+    const int col = warp < 4 ? 64 : 128;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) X[(i0 + i) * XS + r] = v[i];
-    } else {
+    for (int hb = 0; hb < 64; hb += 32) {
+      float v[32];
+      tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, col + hb), v);
+      tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, col + hb + 16), v + 16);
+      if (warp < 4) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) rec_ut[(i0 + i) * D + r] = v[i];
+        for (int i = 0; i < 32; ++i) X[(hb + i) * XS + r] = v[i];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) rec_ut[(hb + i) * D + r] = v[i];
+      }
     }
   }
   __syncthreads();
