@@ -4,19 +4,21 @@
 // Same chunk algebra as the CUDA-core path (UT transform of the gated delta rule; Yang et al.,
 // "Parallelizing Linear Transformers with the Delta Rule over Sequence Length", NeurIPS 2024,
 // section 3; chunked prefill chain and its scratch from "pegainfer PR #1003"), arranged so that
-// every tensor-core product has M = 128 by working with transposed state S^T (dv x dk):
+// every tensor-core product has M = 128:
 //
-//   intra kernel (chunk x V-head, all in parallel):
+//   intra kernel (chunk x V-head, all in parallel, two CTAs per SM):
 //     conv + SiLU + l2norm + gates of the chunk's 64 tokens,
 //     D1 = [K;Q] K^T                     -> A = beta_i e^{g_i-g_j} KK^T (j<i),  P = QK^T o Gamma
-//     T  = (I + A)^{-1}                  (blocked 16 x 16 forward substitution, CUDA cores)
-//     D2 = (beta e^gamma K)^T T^T, (beta V)^T T^T   -> W, U~
-//     writes Q~ = e^gamma Q, W, K~ = e^{gamma_L - gamma} K, U~, P, e^{gamma_L}  (f32)
-//   state kernel (sequence x V-head, serial over the chunks, S^T held in TMEM):
-//     D3 = S^T [Q~^T | W^T]              -> (Q~ S)^T, (W S)^T
-//     U^T = U~^T - (W S)^T
-//     S^T <- e^{gamma_L} S^T + U^T K~ ;  O^T = (Q~ S)^T + U^T P^T   (one MMA group, N = 192)
-//     z-gated RMSNorm of O -> out
+//     T  = (I + A)^{-1}                  (forward substitution, CUDA cores)
+//     D2 = (beta e^gamma K)^T T^T, (beta V)^T T^T   -> W^T, U~^T
+//     writes [Q~ ; W] and [P ; K~^T] as split-bf16 operand images (Q~ = e^gamma Q,
+//     K~ = e^{gamma_L - gamma} K), U~ (f32) and e^{gamma_L}
+//   state kernel (sequence x V-head x 4 dv slices, a cluster of 4 CTAs; serial over the chunks,
+//   the 128 x 32 state slice S held in TMEM):
+//     D3 = [Q~ ; W] S                    -> rows 0-63 Q~ S, rows 64-127 W S
+//     U  = U~ - W S
+//     S <- e^{gamma_L} S + K~^T U ;  D3 += [P ; K~^T_(0..63)] U  (rows 0-63: O = Q~ S + P U)
+//     z-gated RMSNorm of O -> out, the sum of squares over dv shared within the cluster
 //
 // Precision: every product runs as three bf16 passes on split operands
 // (x = hi + lo, hi = bf16(x), lo = bf16(x - hi): A_hi B_hi + A_hi B_lo + A_lo B_hi) with f32
@@ -35,7 +37,7 @@ constexpr int D = 128;
 // images of the state kernel's B operands (split bf16, K-major core-matrix layout, hi then lo), so
 // the state kernel brings each in with one bulk copy.  Offsets in bytes.
 constexpr uint32_t R_B3 = 0;                     // [Q~ ; W] rows, 128 x 128: hi 32 KiB, lo 32 KiB
-constexpr uint32_t R_B4 = R_B3 + 65536;          // [K~^T ; P] rows, 192 x 64: hi 24 KiB, lo 24 KiB
+constexpr uint32_t R_B4 = R_B3 + 65536;          // [P ; K~^T] rows, 192 x 64: hi 24 KiB, lo 24 KiB
 constexpr uint32_t R_UT = R_B4 + 49152;          // f32 [64][128] U~ rows
 constexpr uint32_t R_SC = R_UT + 32768;          // f32 e^{gamma_L}
 constexpr uint32_t REC_BYTES = R_SC + 256;       // 147,712 bytes (multiple of 256)
@@ -414,7 +416,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   l2norm_rows(X, d.l2_eps, 1.0f);
   __syncthreads();
   x_rows_to_tile(X, a1 + S::K_HI, a1 + S::K_LO);
-  x_cols_to_gtile64(X, dec, rec + R_B4, rec + R_B4 + B4_HALF);
+  x_cols_to_gtile64(X, dec, rec + R_B4 + 8192, rec + R_B4 + B4_HALF + 8192);   // rows 64..191
   __syncthreads();
   // ---- Q: conv, l2norm (times q_scale), A1 Q rows, Q~ rows of B3
   conv_compute(cin, L, X);
@@ -479,7 +481,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
         }
         uint4 hh, ll;
         split8(p8, hh, ll);
-        const uint32_t off = tc::kmajor_off(128 + i, j0 + q, 64);   // P rows of B4
+        const uint32_t off = tc::kmajor_off(i, j0 + q, 64);   // P rows 0..63 of B4
         gst_unit(rec + R_B4, off, hh);
         gst_unit(rec + R_B4 + B4_HALF, off, ll);
       }
@@ -574,60 +576,34 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
 }
 
 // ================================================================== serial state kernel
+//
+// One cluster of four CTAs per (sequence, V-head); CTA sigma owns the state columns
+// [32 sigma, 32 sigma + 32) of S (dk x dv) -- the chunk recurrence never mixes dv columns, so the
+// four slices run independently and only the output RMSNorm (over all dv) needs an exchange of
+// per-token partial sums of squares between the CTAs of the cluster.
+
+constexpr int NSL = 4;                        // dv slices (CTAs) per head
+constexpr int SW = D / NSL;                   // 32 columns per slice
+constexpr uint32_t PLBO = 144;                // padded K-direction core-matrix stride (bytes)
+constexpr uint32_t SOP_SBO = (D / 8) * PLBO;  // S operand: N = 32 rows, K = 128 (dk)
+constexpr uint32_t SOP_HALF = (SW / 8) * SOP_SBO;
+constexpr uint32_t UOP_SBO = (CH / 8) * PLBO; // U operand: N = 32 rows, K = 64 (tokens)
+constexpr uint32_t UOP_HALF = (SW / 8) * UOP_SBO;
+constexpr int NTS = 192;                      // 4 main warps + 2 epilogue warps
 
 struct StateSmem {
-  static constexpr uint32_t A3 = 0;                 // S^T   [128 x 128] hi then lo
-  static constexpr uint32_t B3 = A3 + 2 * 32768;    // [Q~ ; W] rows [128 x 128]
-  static constexpr uint32_t A4 = B3 + 2 * 32768;    // U^T   [128 x 64]
-  static constexpr uint32_t B4 = A4 + 2 * 16384;    // [K~^T ; P] rows [192 x 64]
-  static constexpr uint32_t BAR = B4 + 2 * 24576;   // 6 mbarriers
-  static constexpr uint32_t MISC = BAR + 48;
+  static constexpr uint32_t B3 = 0;                        // [Q~ ; W] rows [128 x 128], hi then lo
+  static constexpr uint32_t B4 = B3 + 2 * 32768;           // [P ; K~^T] rows [192 x 64], hi then lo
+  static constexpr uint32_t SOP = B4 + 2 * 24576;          // S slice as B operand, hi then lo
+  static constexpr uint32_t UOP = SOP + 2 * SOP_HALF;      // U slice as B operand, hi then lo
+  static constexpr uint32_t XBUF = UOP + 2 * UOP_HALF;     // f32 [2][NSL][64] partial sums
+  static constexpr uint32_t BAR = XBUF + 2 * NSL * 64 * 4; // 10 mbarriers
+  static constexpr uint32_t MISC = BAR + 80;
   static constexpr uint32_t BYTES = MISC + 64;
 };
 
-// z-gated RMSNorm of one chunk's outputs, by the four epilogue warps: O (f32 [64 tokens][128],
-// staged in shared memory) -> out.  Warp w takes tokens w, w+4, ...; lane l the 4 channels 4l..4l+3.
 template <typename T>
-__device__ __forceinline__ void chunk_load_z(const T* __restrict__ z, float4* zz, int t0, int L,
-                                             int h, int Hv) {
-  const int w = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
-  const size_t ld = (size_t)Hv * D;
-#pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const int i = min(w + 4 * m, L - 1);
-    zz[m] = Act<T>::ldg4(z + (size_t)(t0 + i) * ld + (size_t)h * D + 4 * lane);
-  }
-}
-
-template <typename T>
-__device__ __forceinline__ void chunk_epilogue(const float* Ost, const float4* zz,
-                                               T* __restrict__ out, const float4 wn4, int t0, int L,
-                                               int h, int Hv, float eps, bool valid) {
-  const int w = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
-  const size_t ld = (size_t)Hv * D;
-  float4 o[16];
-  float ss[16];
-#pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    o[m] = *reinterpret_cast<const float4*>(Ost + (w + 4 * m) * D + 4 * lane);
-    ss[m] = o[m].x * o[m].x + o[m].y * o[m].y + o[m].z * o[m].z + o[m].w * o[m].w;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-    for (int m = 0; m < 16; ++m) ss[m] += __shfl_xor_sync(0xffffffffu, ss[m], off);
-#pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const int i = w + 4 * m;
-    const float inv = valid ? rsqrtf(ss[m] * (1.0f / (float)D) + eps) : 0.f;
-    const float4 r = make_float4(o[m].x * inv * wn4.x * silu_fast(zz[m].x), o[m].y * inv * wn4.y * silu_fast(zz[m].y),
-                                 o[m].z * inv * wn4.z * silu_fast(zz[m].z), o[m].w * inv * wn4.w * silu_fast(zz[m].w));
-    if (i < L) Act<T>::store4(out + (size_t)(t0 + i) * ld + (size_t)h * D + 4 * lane, r);
-  }
-}
-
-template <typename T>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __cluster_dims__(NSL, 1, 1) __launch_bounds__(NTS, 1)
 tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_state,
                 T* __restrict__ conv_state, int num_slots, const int32_t* __restrict__ cu,
                 const int32_t* __restrict__ slot_idx, const uint8_t* __restrict__ has_init,
@@ -635,31 +611,33 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
                 T* __restrict__ out, const float* __restrict__ ws, int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
   using S = StateSmem;
-  unsigned char* a3h = sm + S::A3;
-  unsigned char* a3l = a3h + 32768;
   unsigned char* b3h = sm + S::B3;
   unsigned char* b3l = b3h + 32768;
-  unsigned char* a4h = sm + S::A4;
-  unsigned char* a4l = a4h + 16384;
   unsigned char* b4h = sm + S::B4;
   unsigned char* b4l = b4h + 24576;
+  unsigned char* soph = sm + S::SOP;
+  unsigned char* sopl = soph + SOP_HALF;
+  unsigned char* uoph = sm + S::UOP;
+  unsigned char* uopl = uoph + UOP_HALF;
+  float* xbuf = reinterpret_cast<float*>(sm + S::XBUF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::BAR);
   uint64_t* b3full = bars + 0;
   uint64_t* b4full = bars + 1;
   uint64_t* mma3 = bars + 2;
   uint64_t* mma4 = bars + 3;
-  uint64_t* ofull = bars + 4;    // O of the chunk staged (main -> loaders)
-  uint64_t* oempty = bars + 5;   // staged O consumed (loaders -> main)
-  float* Ost = reinterpret_cast<float*>(a4h);   // O staging aliases the U^T operand
+  uint64_t* dfull = bars + 4;    // [2] O of the chunk complete in D3[b] (MMA -> epilogue)
+  uint64_t* dempty = bars + 6;   // [2] D3[b] read by the epilogue (epilogue -> MMA)
+  uint64_t* xfull = bars + 8;    // [2] partial sums of the 4 slices arrived
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
   int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);
 
-  const int n = blockIdx.x, h = blockIdx.y;
+  const int n = blockIdx.x / NSL, sig = blockIdx.x % NSL, h = blockIdx.y;
+  const uint32_t crank = tc::cluster_ctarank();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (warp == 0) {
     int off = 0;
     const bool ok = seq_chunk_offset(cu, num_seqs, total, n, off);
-    if (lane == 0 && !ok && n == 0 && h == 0) set_status(status, GDN_STATUS_BAD_SEQLENS);
+    if (lane == 0 && !ok && n == 0 && h == 0 && sig == 0) set_status(status, GDN_STATUS_BAD_SEQLENS);
     if (lane == 0) {
       sh[0] = ok;
       sh[1] = off;
@@ -671,35 +649,39 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     tc::mbar_init(b4full, 1);
     tc::mbar_init(mma3, 1);
     tc::mbar_init(mma4, 1);
-    tc::mbar_init(ofull, 128);
-    tc::mbar_init(oempty, 128);
+    tc::mbar_init(dfull + 0, 1);
+    tc::mbar_init(dfull + 1, 1);
+    tc::mbar_init(dempty + 0, 64);
+    tc::mbar_init(dempty + 1, 64);
+    tc::mbar_init(xfull + 0, 1);
+    tc::mbar_init(xfull + 1, 1);
     tc::mbar_fence_init();
+    tc::mbar_arrive_expect_tx(xfull, NSL * 64 * 4);   // chunk 0's partial sums
   }
-  __syncthreads();
-  if (!sh[0]) return;
-  if (warp == 0) tc::tmem_alloc(tslot, 256);
-  const int choff = sh[1];
-  volatile int* abort = sh + 2;
-  const int seq_start = __ldg(cu + n), len = __ldg(cu + n + 1) - seq_start;
-  const int nch = (len + CH - 1) / CH;
-  const int s = __ldg(slot_idx + n);
-  const bool valid = s >= 0 && s < num_slots;
-  if (!valid && s >= num_slots && h == 0 && tid == 0) set_status(status, GDN_STATUS_SLOT_RANGE);
-  const bool init = valid && has_init != nullptr && __ldg(has_init + n) != 0;
-  float* Sg = rec_state + ((size_t)(valid ? s : 0) * d.Hv + h) * D * D;
+  if (warp == 0) tc::tmem_alloc(tslot, 128);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  tc::cluster_sync_all();   // peers' mbarriers initialised before any exchange
   const uint32_t tb = *tslot;
+  const int choff = sh[1];
+  volatile int* abort = sh + 2;
+  const int seq_start = __ldg(cu + n), len = __ldg(cu + n + 1) - seq_start;
+  const int nch = sh[0] ? (len + CH - 1) / CH : 0;
+  const int s = __ldg(slot_idx + n);
+  // invalid cu_seqlens: nothing is read or written (the CTA still takes part in the cluster syncs)
+  const bool valid = sh[0] && s >= 0 && s < num_slots;
+  if (sh[0] && s >= num_slots && h == 0 && sig == 0 && tid == 0) set_status(status, GDN_STATUS_SLOT_RANGE);
+  const bool init = valid && has_init != nullptr && __ldg(has_init + n) != 0;
+  float* Sg = rec_state + ((size_t)(valid ? s : 0) * d.Hv + h) * D * D + sig * SW;
+  auto rec_of = [&](int c) {
+    return reinterpret_cast<const unsigned char*>(ws) + ((size_t)(choff + c) * d.Hv + h) * REC_BYTES;
+  };
 
   if (warp < 4) {
-    // ================= main warps: thread e owns TMEM lane e = row e of S^T (dv index)
+    // ================= main warps: thread e owns TMEM lane e = row e (dk index) of the S slice
     const int e = tid;
     const uint32_t lane_base = tc::taddr(tb, warp * 32, 0);
-    // B operands of chunk c arrive by bulk copy from the workspace (one per tile image)
-    auto rec_of = [&](int c) {
-      return reinterpret_cast<const unsigned char*>(ws) + ((size_t)(choff + c) * d.Hv + h) * REC_BYTES;
-    };
     auto load_b3 = [&](int c) {
       tc::mbar_arrive_expect_tx(b3full, 2 * B3_HALF);
       tc::bulk_g2s(b3h, rec_of(c) + R_B3, 2 * B3_HALF, b3full);
@@ -714,98 +696,113 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       load_b4(0);
       issued3 = issued4 = 1;
     }
+    {
+      float v[SW];
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 16) {
-      float v[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) v[k] = Sg[(size_t)(c0 + k) * D + e];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) v[k] = init ? v[k] : 0.f;
-      tc::tmem_st16(lane_base + c0, v);
-    }
-    float ut[64];   // U~ column e of the current chunk, loaded one chunk ahead
-    if (nch > 0) {
-#pragma unroll
-      for (int i = 0; i < 64; ++i) ut[i] = reinterpret_cast<const float*>(rec_of(0) + R_UT)[i * D + e];
-    }
-    for (int c = 0; c < nch; ++c) {
-      const unsigned char* rec = rec_of(c);
-      const uint32_t par = c & 1;
-      // A3 = split(S^T) from TMEM, and S^T <- e^{gamma_L} S^T in the same pass (MMA3 reads the
-      // unscaled copy in shared memory; MMA4 accumulates onto the scaled one)
-      const float egL = *reinterpret_cast<const float*>(rec + R_SC);
-#pragma unroll
-      for (int hb = 0; hb < D; hb += 64) {
-        uint32_t rv[64];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nw(lane_base + hb + 16 * q, rv + 16 * q);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tc::reg_fence16(rv + 16 * q);
-        float v[64];
-#pragma unroll
-        for (int k = 0; k < 64; ++k) v[k] = __uint_as_float(rv[k]);
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          uint4 hh, ll;
-          split8(v + 8 * g, hh, ll);
-          const uint32_t off = tc::kmajor_off(e, hb + 8 * g, 128);
-          st_unit(a3h, off, hh);
-          st_unit(a3l, off, ll);
-        }
-#pragma unroll
-        for (int k = 0; k < 64; ++k) v[k] *= egL;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tc::tmem_st16_nw(lane_base + hb + 16 * q, v + 16 * q);
+      for (int q = 0; q < SW; q += 4) {
+        const float4 x = init ? *reinterpret_cast<const float4*>(Sg + (size_t)e * D + q)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[q] = x.x;
+        v[q + 1] = x.y;
+        v[q + 2] = x.z;
+        v[q + 3] = x.w;
       }
-      tc::tmem_wait_st();
+      tc::tmem_st16(lane_base, v);
+      tc::tmem_st16(lane_base + 16, v + 16);
+    }
+    const int t = e - 64;             // token row of W S / U for warps 2 and 3
+    float ut[SW];                     // U~ slice of token t, loaded one chunk ahead
+    if (warp >= 2 && nch > 0) {
+      const float* u0 = reinterpret_cast<const float*>(rec_of(0) + R_UT) + t * D + sig * SW;
+#pragma unroll
+      for (int q = 0; q < SW; q += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(u0 + q);
+        ut[q] = x.x;
+        ut[q + 1] = x.y;
+        ut[q + 2] = x.z;
+        ut[q + 3] = x.w;
+      }
+    }
+    float egL_next = nch > 0 ? *reinterpret_cast<const float*>(rec_of(0) + R_SC) : 1.f;
+    for (int c = 0; c < nch; ++c) {
+      const uint32_t par = c & 1, b = c & 1;
+      const uint32_t d3 = tb + SW + SW * b;   // D3[b]: rows 0-63 O (Q~ S + P U), rows 64-127 W S
+      // S slice -> B operand (split bf16, unscaled: W S and Q~ S use the chunk's initial state),
+      // and S <- e^{gamma_L} S in TMEM for the K~^T U accumulation
+      const float egL = egL_next;
+      if (c + 1 < nch) egL_next = *reinterpret_cast<const float*>(rec_of(c + 1) + R_SC);
+      {
+        uint32_t rv[SW];
+        tc::tmem_ld16_nw(lane_base, rv);
+        tc::tmem_ld16_nw(lane_base + 16, rv + 16);
+        tc::tmem_wait_ld();
+        tc::reg_fence16(rv);
+        tc::reg_fence16(rv + 16);
+        float v[SW];
+#pragma unroll
+        for (int q = 0; q < SW; ++q) {
+          v[q] = __uint_as_float(rv[q]);
+          __nv_bfloat16 hi, lo;
+          tc::split_bf16(v[q], hi, lo);
+          const uint32_t off = tc::kmajor_off_p(q, e, PLBO, SOP_SBO);
+          *reinterpret_cast<__nv_bfloat16*>(soph + off) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(sopl + off) = lo;
+          v[q] *= egL;
+        }
+        tc::tmem_st16_nw(lane_base, v);
+        tc::tmem_st16_nw(lane_base + 16, v + 16);
+        tc::tmem_wait_st();
+      }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       bar_sync_main();
       tc::fence_after_sync();
-      if (e == 0 && wait_or_abort(b3full, par, abort, status)) {
+      if (e == 0 && wait_or_abort(b3full, par, abort, status) &&
+          (c < 2 || wait_or_abort(dempty + b, ((c >> 1) - 1) & 1, abort, status))) {
         tc::fence_after_sync();
-        const uint32_t id = tc::idesc_bf16(128, 128);
-        const uint32_t ah = tc::smem_u32(a3h), al = tc::smem_u32(a3l);
-        const uint32_t bh = tc::smem_u32(b3h), bl = tc::smem_u32(b3l);
+        const uint32_t id = tc::idesc_bf16(128, SW);
+        const uint32_t ah = tc::smem_u32(b3h), al = tc::smem_u32(b3l);
+        const uint32_t bh = tc::smem_u32(soph), bl = tc::smem_u32(sopl);
         for (int k = 0; k < 8; ++k) {
-          tc::mma_bf16(tb + 128, tc::kstep_desc(ah, 128, k), tc::kstep_desc(bh, 128, k), id, k > 0);
-          tc::mma_bf16(tb + 128, tc::kstep_desc(ah, 128, k), tc::kstep_desc(bl, 128, k), id, 1);
-          tc::mma_bf16(tb + 128, tc::kstep_desc(al, 128, k), tc::kstep_desc(bh, 128, k), id, 1);
+          tc::mma_bf16(d3, tc::kstep_desc(ah, 128, k), tc::kstep_desc_p(bh, PLBO, SOP_SBO, k), id, k > 0);
+          tc::mma_bf16(d3, tc::kstep_desc(ah, 128, k), tc::kstep_desc_p(bl, PLBO, SOP_SBO, k), id, 1);
+          tc::mma_bf16(d3, tc::kstep_desc(al, 128, k), tc::kstep_desc_p(bh, PLBO, SOP_SBO, k), id, 1);
         }
         tc::mma_commit(mma3);
       }
       wait_or_abort(mma3, par, abort, status);
-      if (e == 0 && c + 1 < nch && !*abort) {                          // B3 free again
+      if (e == 0 && c + 1 < nch && !*abort) {   // B3 free again
         load_b3(c + 1);
         ++issued3;
       }
-      if (c > 0) wait_or_abort(oempty, (c - 1) & 1, abort, status);   // staging read by loaders
       tc::fence_after_sync();
-      // U^T = U~^T - (W S)^T  -> A4
-      {
-        uint32_t rv[64];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nw(lane_base + 192 + 16 * q, rv + 16 * q);
+      // U = U~ - W S (tokens 0..63 on lanes 64..127) -> B operand
+      if (warp >= 2) {
+        uint32_t rv[SW];
+        tc::tmem_ld16_nw(tc::taddr(d3, warp * 32, 0), rv);
+        tc::tmem_ld16_nw(tc::taddr(d3, warp * 32, 16), rv + 16);
         tc::tmem_wait_ld();
+        tc::reg_fence16(rv);
+        tc::reg_fence16(rv + 16);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tc::reg_fence16(rv + 16 * q);
-        float v[64];
-#pragma unroll
-        for (int k = 0; k < 64; ++k) v[k] = ut[k] - __uint_as_float(rv[k]);
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          uint4 hh, ll;
-          split8(v + 8 * g, hh, ll);
-          const uint32_t off = tc::kmajor_off(e, 8 * g, 64);
-          st_unit(a4h, off, hh);
-          st_unit(a4l, off, ll);
+        for (int q = 0; q < SW; ++q) {
+          __nv_bfloat16 hi, lo;
+          tc::split_bf16(ut[q] - __uint_as_float(rv[q]), hi, lo);
+          const uint32_t off = tc::kmajor_off_p(q, t, PLBO, UOP_SBO);
+          *reinterpret_cast<__nv_bfloat16*>(uoph + off) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(uopl + off) = lo;
         }
-      }
-      if (c + 1 < nch) {
-        const float* un = reinterpret_cast<const float*>(rec_of(c + 1) + R_UT);
+        if (c + 1 < nch) {
+          const float* un = reinterpret_cast<const float*>(rec_of(c + 1) + R_UT) + t * D + sig * SW;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) ut[i] = un[i * D + e];
+          for (int q = 0; q < SW; q += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(un + q);
+            ut[q] = x.x;
+            ut[q + 1] = x.y;
+            ut[q + 2] = x.z;
+            ut[q + 3] = x.w;
+          }
+        }
       }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
@@ -813,36 +810,30 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       tc::fence_after_sync();
       if (e == 0 && wait_or_abort(b4full, par, abort, status)) {
         tc::fence_after_sync();
-        const uint32_t id = tc::idesc_bf16(128, 192);
-        const uint32_t ah = tc::smem_u32(a4h), al = tc::smem_u32(a4l);
-        const uint32_t bh = tc::smem_u32(b4h), bl = tc::smem_u32(b4l);
+        const uint32_t id = tc::idesc_bf16(128, SW);
+        const uint32_t ph = tc::smem_u32(b4h), pl = tc::smem_u32(b4l);
+        const uint32_t bh = tc::smem_u32(uoph), bl = tc::smem_u32(uopl);
+        for (int k = 0; k < 4; ++k) {   // S += K~^T U   (B4 rows 64..191)
+          tc::mma_bf16(tb, tc::kstep_desc(ph + 8192, 64, k), tc::kstep_desc_p(bh, PLBO, UOP_SBO, k), id, 1);
+          tc::mma_bf16(tb, tc::kstep_desc(ph + 8192, 64, k), tc::kstep_desc_p(bl, PLBO, UOP_SBO, k), id, 1);
+          tc::mma_bf16(tb, tc::kstep_desc(pl + 8192, 64, k), tc::kstep_desc_p(bh, PLBO, UOP_SBO, k), id, 1);
+        }
+        // D3 += [P ; K~^T rows 0..63] U: rows 0..63 become O; rows 64..127 (W S, consumed) are
+        // left as scratch
         for (int k = 0; k < 4; ++k) {
-          tc::mma_bf16(tb, tc::kstep_desc(ah, 64, k), tc::kstep_desc(bh, 64, k), id, 1);
-          tc::mma_bf16(tb, tc::kstep_desc(ah, 64, k), tc::kstep_desc(bl, 64, k), id, 1);
-          tc::mma_bf16(tb, tc::kstep_desc(al, 64, k), tc::kstep_desc(bh, 64, k), id, 1);
+          tc::mma_bf16(d3, tc::kstep_desc(ph, 64, k), tc::kstep_desc_p(bh, PLBO, UOP_SBO, k), id, 1);
+          tc::mma_bf16(d3, tc::kstep_desc(ph, 64, k), tc::kstep_desc_p(bl, PLBO, UOP_SBO, k), id, 1);
+          tc::mma_bf16(d3, tc::kstep_desc(pl, 64, k), tc::kstep_desc_p(bh, PLBO, UOP_SBO, k), id, 1);
         }
         tc::mma_commit(mma4);
+        tc::mma_commit(dfull + b);
       }
       wait_or_abort(mma4, par, abort, status);
-      if (e == 0 && c + 1 < nch && !*abort) {                          // B4 free again
+      if (e == 0 && c + 1 < nch && !*abort) {   // B4 free again
         load_b4(c + 1);
         ++issued4;
       }
       tc::fence_after_sync();
-      // O^T row e (tokens 0..63) -> staging (A4 is free once MMA4 completed); loaders normalise
-      {
-        uint32_t rv[64];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nw(lane_base + 128 + 16 * q, rv + 16 * q);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tc::reg_fence16(rv + 16 * q);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) Ost[i * D + e] = __uint_as_float(rv[i]);
-      }
-      mbar_arrive(ofull);
-      tc::fence_before_sync();
-      bar_sync_main();
     }
     // after a timeout: wait (bounded) for bulk copies still in flight before the CTA exits
     // (copy c + 1 is only issued once copy c was consumed, so at most the last one is pending)
@@ -850,38 +841,92 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       if (issued3 > 0) tc::mbar_wait(b3full, (issued3 - 1) & 1, 100000000ull);
       if (issued4 > 0) tc::mbar_wait(b4full, (issued4 - 1) & 1, 100000000ull);
     }
-    // final state back to the slot
+    // final state slice back to the slot
     if (valid) {
+      float v[SW];
+      tc::tmem_ld16(lane_base, v);
+      tc::tmem_ld16(lane_base + 16, v + 16);
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
-        float v[16];
-        tc::tmem_ld16(lane_base + c0, v);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) Sg[(size_t)(c0 + k) * D + e] = v[k];
-      }
+      for (int q = 0; q < SW; q += 4)
+        *reinterpret_cast<float4*>(Sg + (size_t)e * D + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
     }
   } else {
-    // ================= epilogue warps: z-gated RMSNorm of every chunk's staged outputs
-    const int lt = tid - 128;
-    const float4 wn4 = Act<T>::ldg4(norm_w + 4 * (lt & 31));
-    float4 zz[16];   // z of the next chunk to normalise, loaded while the MMAs run
-    if (nch > 0) chunk_load_z<T>(z, zz, seq_start, min(CH, len), h, d.Hv);
+    // ================= epilogue warps: thread t owns token t of the chunk (TMEM lane t of D3)
+    const int t = tid - 128;
+    const size_t ld = (size_t)d.Hv * D;
+    const size_t col0 = (size_t)h * D + sig * SW;
+    float wn[SW];
+#pragma unroll
+    for (int q = 0; q < SW; q += 4) {
+      const float4 x = Act<T>::ldg4(norm_w + sig * SW + q);
+      wn[q] = x.x;
+      wn[q + 1] = x.y;
+      wn[q + 2] = x.z;
+      wn[q + 3] = x.w;
+    }
+    float4 zz[SW / 4];   // z of the next chunk, loaded while the MMAs run
+    auto load_z = [&](int c) {
+      const int i = min(t, min(CH, len - c * CH) - 1);
+      const T* zp = z + (size_t)(seq_start + c * CH + i) * ld + col0;
+#pragma unroll
+      for (int q = 0; q < SW / 4; ++q) zz[q] = Act<T>::ldg4(zp + 4 * q);
+    };
+    if (nch > 0) load_z(0);
+    const uint32_t xb_local = tc::smem_u32(xbuf);
+    const uint32_t xf_local = tc::smem_u32(xfull);
+    bool xok = true;
     for (int c = 0; c < nch; ++c) {
-      wait_or_abort(ofull, c & 1, abort, status);
-      chunk_epilogue<T>(Ost, zz, out, wn4, seq_start + c * CH, min(CH, len - c * CH), h, d.Hv,
-                        d.norm_eps, valid);
-      mbar_arrive(oempty);
-      if (c + 1 < nch)
-        chunk_load_z<T>(z, zz, seq_start + (c + 1) * CH, min(CH, len - (c + 1) * CH), h, d.Hv);
+      const uint32_t b = c & 1;
+      const int L = min(CH, len - c * CH);
+      wait_or_abort(dfull + b, (c >> 1) & 1, abort, status);
+      tc::fence_after_sync();
+      float o[SW];
+      tc::tmem_ld16(tc::taddr(tb + SW + SW * b, (warp & 3) * 32, 0), o);
+      tc::tmem_ld16(tc::taddr(tb + SW + SW * b, (warp & 3) * 32, 16), o + 16);
+      tc::fence_before_sync();
+      mbar_arrive(dempty + b);
+      float ss = 0.f;
+#pragma unroll
+      for (int q = 0; q < SW; ++q) ss = fmaf(o[q], o[q], ss);
+      if (t == 0 && c + 1 < nch) {   // the next use of the other buffer
+        tc::mbar_arrive_expect_tx(xfull + ((c + 1) & 1), NSL * 64 * 4);
+        tc::fence_acq_rel_cluster();
+      }
+      const uint32_t slot_off = ((b * NSL + crank) * 64 + t) * 4;
+#pragma unroll
+      for (uint32_t r = 0; r < NSL; ++r)
+        tc::st_async_f32(tc::mapa_shared(xb_local + slot_off, r), ss,
+                         tc::mapa_shared(xf_local + b * 8, r));
+      if (xok && !tc::mbar_wait_cluster(xfull + b, (c >> 1) & 1)) {
+        xok = false;
+        *abort = 1;
+        set_status(status, GDN_STATUS_TIMEOUT);
+      }
+      float tot = 0.f;
+#pragma unroll
+      for (int r = 0; r < NSL; ++r) tot += xbuf[(b * NSL + r) * 64 + t];
+      const float inv = valid ? rsqrtf(tot * (1.0f / (float)D) + d.norm_eps) : 0.f;
+      if (t < L) {
+        T* op = out + (size_t)(seq_start + c * CH + t) * ld + col0;
+#pragma unroll
+        for (int q = 0; q < SW / 4; ++q) {
+          const float4 r4 = make_float4(o[4 * q] * inv * wn[4 * q] * silu_fast(zz[q].x),
+                                        o[4 * q + 1] * inv * wn[4 * q + 1] * silu_fast(zz[q].y),
+                                        o[4 * q + 2] * inv * wn[4 * q + 2] * silu_fast(zz[q].z),
+                                        o[4 * q + 3] * inv * wn[4 * q + 3] * silu_fast(zz[q].w));
+          Act<T>::store4(op + 4 * q, r4);
+        }
+      }
+      if (c + 1 < nch) load_z(c + 1);
     }
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tb, 256);
+  if (warp == 0) tc::tmem_dealloc(tb, 128);
   // conv state <- the sequence's last K-1 raw inputs (older ones kept when continuing)
-  if (valid && h == 0) {
+  if (valid && h == 0 && sig == 0) {
     T* csw = conv_state + (size_t)s * 3 * d.cqkv;
-    for (int cch = tid; cch < d.cqkv; cch += 256) {
+    for (int cch = tid; cch < d.cqkv; cch += NTS) {
       T v3[3];
 #pragma unroll
       for (int m = 0; m < 3; ++m) {
@@ -893,6 +938,7 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       for (int m = 0; m < 3; ++m) csw[(size_t)m * d.cqkv + cch] = v3[m];
     }
   }
+  tc::cluster_sync_all();   // no CTA leaves while a peer may still store into its shared memory
 }
 
 template <typename T>
@@ -915,7 +961,7 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
         static_cast<const T*>(pool->conv_state), pool->num_slots, cu, slot_idx, has_init, num_seqs,
         total, static_cast<const T*>(qkv), static_cast<const T*>(a), static_cast<const T*>(b), wsf,
         pool->status);
-  k2<<<dim3(num_seqs, d.Hv), 256, StateSmem::BYTES, stream>>>(
+  k2<<<dim3(NSL * num_seqs, d.Hv), NTS, StateSmem::BYTES, stream>>>(
       d, static_cast<const T*>(w->norm_weight), pool->rec_state, static_cast<T*>(pool->conv_state),
       pool->num_slots, cu, slot_idx, has_init, num_seqs, total, static_cast<const T*>(qkv),
       static_cast<const T*>(z), static_cast<T*>(out), wsf, pool->status);

@@ -33,6 +33,20 @@ __device__ __forceinline__ uint64_t kstep_desc(uint32_t tile_saddr, int kt, int 
   return sdesc(tile_saddr + (uint32_t)s * 256u, 128u, (uint32_t)(kt >> 3) * 128u);
 }
 
+// Byte offset of element (row, k) in a K-major no-swizzle bf16 tile whose K-direction core
+// matrices are lbo bytes apart (lbo >= 128, a multiple of 16) and whose 8-row groups are sbo bytes
+// apart.  With lbo = 144 a warp whose 32 threads hold 32 consecutive k of one row stores 2-byte
+// elements without bank conflicts (the four 8-k groups land 4 banks apart).
+__host__ __device__ constexpr uint32_t kmajor_off_p(int row, int k, uint32_t lbo, uint32_t sbo) {
+  return (uint32_t)(row >> 3) * sbo + (uint32_t)(k >> 3) * lbo + (uint32_t)((row & 7) << 4) +
+         (uint32_t)((k & 7) << 1);
+}
+
+// Descriptor of the K-step s (16 bf16 = two core matrices along K) of such a tile.
+__device__ __forceinline__ uint64_t kstep_desc_p(uint32_t tile_saddr, uint32_t lbo, uint32_t sbo, int s) {
+  return sdesc(tile_saddr + (uint32_t)s * 2u * lbo, lbo, sbo);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B, f32 accumulator, both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
@@ -203,6 +217,61 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint3
           smem_u32(smem_dst)),
       "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// ------------------------------------------------------------------ thread-block clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+
+// Shared::cluster address of the same shared-memory location in the CTA of rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// 4-byte store into (possibly another CTA's) shared memory that completes 4 transaction bytes
+// on the mbarrier at rbar (a shared::cluster address in the same CTA as raddr).
+__device__ __forceinline__ void st_async_f32(uint32_t raddr, float v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];\n" ::"r"(raddr),
+               "r"(__float_as_uint(v)), "r"(rbar)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;\n" ::: "memory");
+}
+
+// All threads of all CTAs of the cluster (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\nbarrier.cluster.wait.acquire;\n" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait (acquire at cluster scope) for data other CTAs of the cluster stored with
+// st_async_f32; false on timeout.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
 }
 
 // ------------------------------------------------------------------ split bf16

@@ -7,16 +7,18 @@
 
 using namespace gdn::tc;
 
+// B's K-direction core matrices are b_lbo bytes apart (128: the dense layout).
 __global__ void tc_gemm_kernel(const float* __restrict__ A, const float* __restrict__ B,
                                float* __restrict__ D, int N, int K, int passes, uint32_t ncols,
-                               int* __restrict__ err) {
+                               uint32_t b_lbo, int* __restrict__ err) {
   extern __shared__ __align__(1024) unsigned char sm[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   unsigned char* a_hi = sm;
   unsigned char* a_lo = a_hi + 128 * K * 2;
   unsigned char* b_hi = a_lo + 128 * K * 2;
-  unsigned char* b_lo = b_hi + N * K * 2;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(b_lo + N * K * 2);
+  const uint32_t b_sbo = (uint32_t)(K / 8) * b_lbo, b_bytes = (uint32_t)(N / 8) * b_sbo;
+  unsigned char* b_lo = b_hi + b_bytes;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(b_lo + b_bytes);
   uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
   for (int idx = tid; idx < 128 * K; idx += blockDim.x) {
     const int r = idx / K, k = idx - r * K;
@@ -29,8 +31,8 @@ __global__ void tc_gemm_kernel(const float* __restrict__ A, const float* __restr
     const int r = idx / K, k = idx - r * K;
     __nv_bfloat16 h, l;
     split_bf16(B[idx], h, l);
-    *reinterpret_cast<__nv_bfloat16*>(b_hi + kmajor_off(r, k, K)) = h;
-    *reinterpret_cast<__nv_bfloat16*>(b_lo + kmajor_off(r, k, K)) = l;
+    *reinterpret_cast<__nv_bfloat16*>(b_hi + kmajor_off_p(r, k, b_lbo, b_sbo)) = h;
+    *reinterpret_cast<__nv_bfloat16*>(b_lo + kmajor_off_p(r, k, b_lbo, b_sbo)) = l;
   }
   if (tid == 0) {
     mbar_init(bar, 1);
@@ -47,10 +49,10 @@ __global__ void tc_gemm_kernel(const float* __restrict__ A, const float* __restr
     const uint32_t id = idesc_bf16(128, N);
     const uint32_t ah = smem_u32(a_hi), al = smem_u32(a_lo), bh = smem_u32(b_hi), bl = smem_u32(b_lo);
     for (int s = 0; s < K / 16; ++s) {
-      mma_bf16(tbase, kstep_desc(ah, K, s), kstep_desc(bh, K, s), id, s > 0 ? 1u : 0u);
+      mma_bf16(tbase, kstep_desc(ah, K, s), kstep_desc_p(bh, b_lbo, b_sbo, s), id, s > 0 ? 1u : 0u);
       if (passes == 3) {
-        mma_bf16(tbase, kstep_desc(ah, K, s), kstep_desc(bl, K, s), id, 1u);
-        mma_bf16(tbase, kstep_desc(al, K, s), kstep_desc(bh, K, s), id, 1u);
+        mma_bf16(tbase, kstep_desc(ah, K, s), kstep_desc_p(bl, b_lbo, b_sbo, s), id, 1u);
+        mma_bf16(tbase, kstep_desc(al, K, s), kstep_desc_p(bh, b_lbo, b_sbo, s), id, 1u);
       }
     }
     mma_commit(bar);
@@ -71,15 +73,68 @@ __global__ void tc_gemm_kernel(const float* __restrict__ A, const float* __restr
   if (warp == 0) tmem_dealloc(tbase, ncols);
 }
 
-extern "C" int tc_gemm(const float* A, const float* B, float* D, int N, int K, int passes, int* err) {
-  if (N < 16 || N > 256 || N % 16 || K < 16 || K % 16) return -1;
+extern "C" int tc_gemm_p(const float* A, const float* B, float* D, int N, int K, int passes,
+                         int b_lbo, int* err) {
+  if (N < 16 || N > 256 || N % 16 || K < 16 || K % 16 || b_lbo < 128 || b_lbo % 16) return -1;
   uint32_t ncols = 32;
   while (ncols < (uint32_t)N) ncols <<= 1;
-  const size_t smem = (size_t)2 * (128 + N) * K * 2 + 64;
+  const size_t b_bytes = (size_t)(N / 8) * (K / 8) * b_lbo;
+  const size_t smem = (size_t)2 * 128 * K * 2 + 2 * b_bytes + 64;
+  if (smem > 200 * 1024) return -1;
   if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return -2;
-  tc_gemm_kernel<<<1, 128, smem>>>(A, B, D, N, K, passes, ncols, err);
+  tc_gemm_kernel<<<1, 128, smem>>>(A, B, D, N, K, passes, ncols, (uint32_t)b_lbo, err);
+  if (cudaGetLastError() != cudaSuccess) return -3;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
+}
+
+extern "C" int tc_gemm(const float* A, const float* B, float* D, int N, int K, int passes, int* err) {
+  return tc_gemm_p(A, B, D, N, K, passes, 128, err);
+}
+
+// Per-round exchange of one float per thread among the 4 CTAs of a cluster, the way the prefill
+// state kernel shares per-token partial sums of squares: every thread stores its value into slot
+// [round & 1][own rank][thread] of all four CTAs with st.async (completing bytes on that CTA's
+// mbarrier for the buffer), then waits for its own CTA's buffer to fill and sums the 4 slots.
+// Thread 0 posts the expected byte count of round r + 1 before it sends round r.
+__global__ void __cluster_dims__(4, 1, 1) cluster_xchg_kernel(int rounds, float* __restrict__ out,
+                                                              int* __restrict__ err) {
+  __shared__ float xbuf[2][4][64];
+  __shared__ __align__(8) uint64_t xfull[2];
+  const int t = threadIdx.x;
+  const uint32_t rank = cluster_ctarank();
+  if (t == 0) {
+    mbar_init(&xfull[0], 1);
+    mbar_init(&xfull[1], 1);
+    mbar_fence_init();
+    mbar_arrive_expect_tx(&xfull[0], 4 * 64 * 4);
+  }
+  cluster_sync_all();
+  bool ok = true;
+  for (int c = 0; c < rounds; ++c) {
+    const int b = c & 1;
+    if (t == 0 && c + 1 < rounds) {
+      mbar_arrive_expect_tx(&xfull[(c + 1) & 1], 4 * 64 * 4);
+      fence_acq_rel_cluster();
+    }
+    const float v = (float)(rank * 1000 + t) + 0.25f * (float)c;
+#pragma unroll
+    for (uint32_t r = 0; r < 4; ++r)
+      st_async_f32(mapa_shared(smem_u32(&xbuf[b][rank][t]), r), v, mapa_shared(smem_u32(&xfull[b]), r));
+    if (ok) ok = mbar_wait_cluster(&xfull[b], (uint32_t)(c >> 1) & 1u);
+    float sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) sum += xbuf[b][r][t];
+    out[((size_t)blockIdx.x * rounds + c) * 64 + t] = ok ? sum : -1.f;
+  }
+  if (!ok) atomicOr(err, 4);
+  cluster_sync_all();
+}
+
+extern "C" int tc_cluster_xchg(int nclusters, int rounds, float* out, int* err) {
+  if (nclusters < 1 || rounds < 1) return -1;
+  cluster_xchg_kernel<<<4 * nclusters, 64>>>(rounds, out, err);
   if (cudaGetLastError() != cudaSuccess) return -3;
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
 }

@@ -27,6 +27,10 @@ def lib():
     l = ctypes.CDLL(so)
     l.tc_gemm.restype = ctypes.c_int
     l.tc_gemm.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    l.tc_gemm_p.restype = ctypes.c_int
+    l.tc_gemm_p.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p]
+    l.tc_cluster_xchg.restype = ctypes.c_int
+    l.tc_cluster_xchg.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
     return l
 
 
@@ -56,6 +60,39 @@ def test_tc_gemm(lib, N, K):
     e1 = np.max(np.abs(ref1 - ref)) / np.max(np.abs(ref))
     assert e3 < 2e-5, e3
     assert e3 < e1 / 20
+
+
+@pytest.mark.parametrize("N,K", [(32, 128), (32, 64), (64, 64)])
+def test_tc_gemm_padded_b(lib, N, K):
+    """B operand with its K-direction core matrices 144 bytes apart (the layout the prefill
+    state kernel writes with conflict-free 2-byte stores)."""
+    rng = np.random.default_rng(N * 7 + K)
+    A = rng.standard_normal((128, K)).astype(np.float32)
+    B = rng.standard_normal((N, K)).astype(np.float32)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = A.astype(np.float64) @ B.astype(np.float64).T
+    D = torch.zeros((128, N), dtype=torch.float32, device="cuda")
+    assert lib.tc_gemm_p(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, K, 3, 144, err.data_ptr()) == 0
+    assert int(err.item()) == 0
+    e3 = np.max(np.abs(D.cpu().numpy() - ref)) / np.max(np.abs(ref))
+    assert e3 < 2e-5, e3
+
+
+def test_cluster_exchange(lib):
+    """st.async exchange among the 4 CTAs of a cluster, double-buffered over rounds: every CTA
+    sees the sum of the four ranks' values of each round."""
+    ncl, rounds = 6, 9
+    out = torch.zeros((4 * ncl, rounds, 64), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert lib.tc_cluster_xchg(ncl, rounds, out.data_ptr(), err.data_ptr()) == 0
+    assert int(err.item()) == 0
+    t = np.arange(64)[None, :]
+    c = np.arange(rounds)[:, None]
+    want = (0 + 1000 + 2000 + 3000) + 4 * t + 4 * 0.25 * c
+    got = out.cpu().numpy()
+    for blk in range(4 * ncl):
+        np.testing.assert_array_equal(got[blk], want.astype(np.float32))
 
 
 def test_bounded_wait_gives_up_and_reports(lib):
