@@ -435,10 +435,13 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   if (tid == 0) {
     const uint32_t id = tc::idesc_bf16(128, 64);
     const uint32_t ah = tc::smem_u32(a1 + S::K_HI), al = tc::smem_u32(a1 + S::K_LO);
+    const uint64_t dh = tc::kstep_desc(ah, 128, 0), dl = tc::kstep_desc(al, 128, 0);
+#pragma unroll
     for (int k = 0; k < 8; ++k) {
-      tc::mma_bf16(tb, tc::kstep_desc(ah, 128, k), tc::kstep_desc(ah, 128, k), id, k > 0);
-      tc::mma_bf16(tb, tc::kstep_desc(ah, 128, k), tc::kstep_desc(al, 128, k), id, 1);
-      tc::mma_bf16(tb, tc::kstep_desc(al, 128, k), tc::kstep_desc(ah, 128, k), id, 1);
+      const uint64_t h = tc::desc_add(dh, 256 * k), l = tc::desc_add(dl, 256 * k);
+      tc::mma_bf16(tb, h, h, id, k > 0);
+      tc::mma_bf16(tb, h, l, id, 1);
+      tc::mma_bf16(tb, l, h, id, 1);
     }
     tc::mma_commit(bar);
   }
@@ -537,12 +540,17 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     const uint32_t bh = tc::smem_u32(b2h), bl = tc::smem_u32(b2l);
     const uint32_t srcs[2][2] = {{tc::smem_u32(a1 + S::Q_HI), tc::smem_u32(a1 + S::Q_LO)},
                                  {tc::smem_u32(a1 + S::K_HI), tc::smem_u32(a1 + S::K_LO)}};
+    const uint64_t dbh = tc::kstep_desc(bh, 64, 0), dbl = tc::kstep_desc(bl, 64, 0);
+#pragma unroll
     for (int m = 0; m < 2; ++m) {
       const uint32_t dt = tb + 64 + 64 * m;
+      const uint64_t dah = tc::kstep_desc(srcs[m][0], 64, 0), dal = tc::kstep_desc(srcs[m][1], 64, 0);
+#pragma unroll
       for (int k = 0; k < 4; ++k) {
-        tc::mma_bf16(dt, tc::kstep_desc(srcs[m][0], 64, k), tc::kstep_desc(bh, 64, k), id, k > 0);
-        tc::mma_bf16(dt, tc::kstep_desc(srcs[m][0], 64, k), tc::kstep_desc(bl, 64, k), id, 1);
-        tc::mma_bf16(dt, tc::kstep_desc(srcs[m][1], 64, k), tc::kstep_desc(bh, 64, k), id, 1);
+        const uint32_t o = 256 * k;
+        tc::mma_bf16(dt, tc::desc_add(dah, o), tc::desc_add(dbh, o), id, k > 0);
+        tc::mma_bf16(dt, tc::desc_add(dah, o), tc::desc_add(dbl, o), id, 1);
+        tc::mma_bf16(dt, tc::desc_add(dal, o), tc::desc_add(dbh, o), id, 1);
       }
     }
     tc::mma_commit(bar);
@@ -589,16 +597,25 @@ constexpr uint32_t SOP_SBO = (D / 8) * PLBO;  // S operand: N = 32 rows, K = 128
 constexpr uint32_t SOP_HALF = (SW / 8) * SOP_SBO;
 constexpr uint32_t UOP_SBO = (CH / 8) * PLBO; // U operand: N = 32 rows, K = 64 (tokens)
 constexpr uint32_t UOP_HALF = (SW / 8) * UOP_SBO;
-constexpr int NTS = 192;                      // 4 main warps + 2 epilogue warps
+constexpr int NTS = 320;   // warps 0-3 main, 4-5 and 8-9 epilogue, 6 loader (7 idle)
+constexpr int NDB = 4;     // D3 (output) accumulators in flight between the MMAs and the epilogue
+constexpr int XH = 2;      // epilogue column halves: partial sums per token and CTA
+
+// TMEM columns (lanes 0-127).  Each product runs as two N = 64 MMAs per K-step, A_hi [B_hi ; B_lo]
+// and A_lo [B_hi ; B_lo] (the B operand holds the hi rows 0-31 and the lo rows 32-63), so every
+// accumulator occupies 64 columns whose two 32-column halves add up to the result.
+constexpr uint32_t TC_S = 0;          // S slice, halves [0, 32) + [32, 64)
+constexpr uint32_t TC_D3 = 64;        // NDB x 64 columns: rows 0-63 O, rows 64-127 W S
+constexpr uint32_t TC_COLS = 512;
 
 struct StateSmem {
-  static constexpr uint32_t B3 = 0;                        // [Q~ ; W] rows [128 x 128], hi then lo
-  static constexpr uint32_t B4 = B3 + 2 * 32768;           // [P ; K~^T] rows [192 x 64], hi then lo
+  static constexpr uint32_t B3 = 0;                        // 2 slots: [Q~ ; W] rows [128 x 128], hi then lo
+  static constexpr uint32_t B4 = B3 + 2 * 65536;           // [P ; K~^T] rows [192 x 64], hi then lo
   static constexpr uint32_t SOP = B4 + 2 * 24576;          // S slice as B operand, hi then lo
   static constexpr uint32_t UOP = SOP + 2 * SOP_HALF;      // U slice as B operand, hi then lo
-  static constexpr uint32_t XBUF = UOP + 2 * UOP_HALF;     // f32 [2][NSL][64] partial sums
-  static constexpr uint32_t BAR = XBUF + 2 * NSL * 64 * 4; // 10 mbarriers
-  static constexpr uint32_t MISC = BAR + 80;
+  static constexpr uint32_t XBUF = UOP + 2 * UOP_HALF;     // f32 [2][NSL][XH][64] partial sums
+  static constexpr uint32_t BAR = XBUF + 2 * NSL * XH * 64 * 4;   // 18 mbarriers
+  static constexpr uint32_t MISC = BAR + 144;
   static constexpr uint32_t BYTES = MISC + 64;
 };
 
@@ -611,8 +628,6 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
                 T* __restrict__ out, const float* __restrict__ ws, int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
   using S = StateSmem;
-  unsigned char* b3h = sm + S::B3;
-  unsigned char* b3l = b3h + 32768;
   unsigned char* b4h = sm + S::B4;
   unsigned char* b4l = b4h + 24576;
   unsigned char* soph = sm + S::SOP;
@@ -621,13 +636,15 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   unsigned char* uopl = uoph + UOP_HALF;
   float* xbuf = reinterpret_cast<float*>(sm + S::XBUF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::BAR);
-  uint64_t* b3full = bars + 0;
-  uint64_t* b4full = bars + 1;
-  uint64_t* mma3 = bars + 2;
-  uint64_t* mma4 = bars + 3;
-  uint64_t* dfull = bars + 4;    // [2] O of the chunk complete in D3[b] (MMA -> epilogue)
-  uint64_t* dempty = bars + 6;   // [2] D3[b] read by the epilogue (epilogue -> MMA)
-  uint64_t* xfull = bars + 8;    // [2] partial sums of the 4 slices arrived
+  uint64_t* b3full = bars + 0;   // [2] B3 slot landed (loader -> MMA)
+  uint64_t* b3empty = bars + 2;  // [2] B3 slot read by MMA3 (MMA -> loader)
+  uint64_t* b4full = bars + 4;   // B4 landed
+  uint64_t* b4empty = bars + 5;  // B4 read by MMA4
+  uint64_t* mma3 = bars + 6;
+  uint64_t* mma4 = bars + 7;
+  uint64_t* dfull = bars + 8;    // [NDB] O of the chunk complete in D3[j] (MMA -> epilogue)
+  uint64_t* dempty = bars + 12;  // [NDB] D3[j] read by the epilogue (epilogue -> MMA)
+  uint64_t* xfull = bars + 16;   // [2] partial sums of the 4 slices arrived
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
   int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);
 
@@ -645,20 +662,11 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     }
   }
   if (tid == 0) {
-    tc::mbar_init(b3full, 1);
-    tc::mbar_init(b4full, 1);
-    tc::mbar_init(mma3, 1);
-    tc::mbar_init(mma4, 1);
-    tc::mbar_init(dfull + 0, 1);
-    tc::mbar_init(dfull + 1, 1);
-    tc::mbar_init(dempty + 0, 64);
-    tc::mbar_init(dempty + 1, 64);
-    tc::mbar_init(xfull + 0, 1);
-    tc::mbar_init(xfull + 1, 1);
+    for (int i = 0; i < 18; ++i) tc::mbar_init(bars + i, (i >= 12 && i < 16) ? 128 : 1);
     tc::mbar_fence_init();
-    tc::mbar_arrive_expect_tx(xfull, NSL * 64 * 4);   // chunk 0's partial sums
+    tc::mbar_arrive_expect_tx(xfull, NSL * XH * 64 * 4);   // chunk 0's partial sums
   }
-  if (warp == 0) tc::tmem_alloc(tslot, 128);
+  if (warp == 0) tc::tmem_alloc(tslot, TC_COLS);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -682,20 +690,6 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     // ================= main warps: thread e owns TMEM lane e = row e (dk index) of the S slice
     const int e = tid;
     const uint32_t lane_base = tc::taddr(tb, warp * 32, 0);
-    auto load_b3 = [&](int c) {
-      tc::mbar_arrive_expect_tx(b3full, 2 * B3_HALF);
-      tc::bulk_g2s(b3h, rec_of(c) + R_B3, 2 * B3_HALF, b3full);
-    };
-    auto load_b4 = [&](int c) {
-      tc::mbar_arrive_expect_tx(b4full, 2 * B4_HALF);
-      tc::bulk_g2s(b4h, rec_of(c) + R_B4, 2 * B4_HALF, b4full);
-    };
-    int issued3 = 0, issued4 = 0;   // bulk copies issued (thread 0); chunk c waits copy c
-    if (e == 0 && nch > 0) {
-      load_b3(0);
-      load_b4(0);
-      issued3 = issued4 = 1;
-    }
     {
       float v[SW];
 #pragma unroll
@@ -707,8 +701,12 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         v[q + 2] = x.z;
         v[q + 3] = x.w;
       }
-      tc::tmem_st16(lane_base, v);
-      tc::tmem_st16(lane_base + 16, v + 16);
+      tc::tmem_st16(lane_base + TC_S, v);
+      tc::tmem_st16(lane_base + TC_S + 16, v + 16);
+#pragma unroll
+      for (int q = 0; q < SW; ++q) v[q] = 0.f;
+      tc::tmem_st16(lane_base + TC_S + 32, v);
+      tc::tmem_st16(lane_base + TC_S + 48, v + 16);
     }
     const int t = e - 64;             // token row of W S / U for warps 2 and 3
     float ut[SW];                     // U~ slice of token t, loaded one chunk ahead
@@ -724,24 +722,36 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       }
     }
     float egL_next = nch > 0 ? *reinterpret_cast<const float*>(rec_of(0) + R_SC) : 1.f;
+    // operand descriptors, built once (K-step k: + 256 bytes for the dense tiles, + 2 PLBO for
+    // the padded ones)
+    const uint32_t id64 = tc::idesc_bf16(128, 2 * SW);
+    const uint64_t dA3h = tc::kstep_desc(tc::smem_u32(sm + S::B3), 128, 0);   // slot 0; slot 1 + 64 KiB
+    const uint64_t dA3l = tc::kstep_desc(tc::smem_u32(sm + S::B3 + B3_HALF), 128, 0);
+    const uint64_t dKh = tc::kstep_desc(tc::smem_u32(b4h) + 8192, 64, 0);
+    const uint64_t dKl = tc::kstep_desc(tc::smem_u32(b4l) + 8192, 64, 0);
+    const uint64_t dPh = tc::kstep_desc(tc::smem_u32(b4h), 64, 0);
+    const uint64_t dPl = tc::kstep_desc(tc::smem_u32(b4l), 64, 0);
+    const uint64_t dS = tc::kstep_desc_p(tc::smem_u32(soph), PLBO, SOP_SBO, 0);
+    const uint64_t dU = tc::kstep_desc_p(tc::smem_u32(uoph), PLBO, UOP_SBO, 0);
     for (int c = 0; c < nch; ++c) {
       const uint32_t par = c & 1, b = c & 1;
-      const uint32_t d3 = tb + SW + SW * b;   // D3[b]: rows 0-63 O (Q~ S + P U), rows 64-127 W S
+      const uint32_t jd = c & (NDB - 1);
+      const uint32_t d3 = tb + TC_D3 + 64 * jd;   // D3[jd]: rows 0-63 O (Q~ S + P U), rows 64-127 W S
       // S slice -> B operand (split bf16, unscaled: W S and Q~ S use the chunk's initial state),
       // and S <- e^{gamma_L} S in TMEM for the K~^T U accumulation
       const float egL = egL_next;
       if (c + 1 < nch) egL_next = *reinterpret_cast<const float*>(rec_of(c + 1) + R_SC);
       {
-        uint32_t rv[SW];
-        tc::tmem_ld16_nw(lane_base, rv);
-        tc::tmem_ld16_nw(lane_base + 16, rv + 16);
+        uint32_t rv[2 * SW];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nw(lane_base + TC_S + 16 * q, rv + 16 * q);
         tc::tmem_wait_ld();
-        tc::reg_fence16(rv);
-        tc::reg_fence16(rv + 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::reg_fence16(rv + 16 * q);
         float v[SW];
 #pragma unroll
         for (int q = 0; q < SW; ++q) {
-          v[q] = __uint_as_float(rv[q]);
+          v[q] = __uint_as_float(rv[q]) + __uint_as_float(rv[q + SW]);
           __nv_bfloat16 hi, lo;
           tc::split_bf16(v[q], hi, lo);
           const uint32_t off = tc::kmajor_off_p(q, e, PLBO, SOP_SBO);
@@ -749,45 +759,45 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
           *reinterpret_cast<__nv_bfloat16*>(sopl + off) = lo;
           v[q] *= egL;
         }
-        tc::tmem_st16_nw(lane_base, v);
-        tc::tmem_st16_nw(lane_base + 16, v + 16);
+        tc::tmem_st16_nw(lane_base + TC_S, v);
+        tc::tmem_st16_nw(lane_base + TC_S + 16, v + 16);
+#pragma unroll
+        for (int q = 0; q < SW; ++q) v[q] = 0.f;
+        tc::tmem_st16_nw(lane_base + TC_S + 32, v);
+        tc::tmem_st16_nw(lane_base + TC_S + 48, v + 16);
         tc::tmem_wait_st();
       }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       bar_sync_main();
       tc::fence_after_sync();
-      if (e == 0 && wait_or_abort(b3full, par, abort, status) &&
-          (c < 2 || wait_or_abort(dempty + b, ((c >> 1) - 1) & 1, abort, status))) {
+      if (e == 0 && wait_or_abort(b3full + b, (c >> 1) & 1, abort, status) &&
+          (c < NDB || wait_or_abort(dempty + jd, ((c / NDB) - 1) & 1, abort, status))) {
         tc::fence_after_sync();
-        const uint32_t id = tc::idesc_bf16(128, SW);
-        const uint32_t ah = tc::smem_u32(b3h), al = tc::smem_u32(b3l);
-        const uint32_t bh = tc::smem_u32(soph), bl = tc::smem_u32(sopl);
-        for (int k = 0; k < 8; ++k) {
-          tc::mma_bf16(d3, tc::kstep_desc(ah, 128, k), tc::kstep_desc_p(bh, PLBO, SOP_SBO, k), id, k > 0);
-          tc::mma_bf16(d3, tc::kstep_desc(ah, 128, k), tc::kstep_desc_p(bl, PLBO, SOP_SBO, k), id, 1);
-          tc::mma_bf16(d3, tc::kstep_desc(al, 128, k), tc::kstep_desc_p(bh, PLBO, SOP_SBO, k), id, 1);
+        const uint32_t so = 65536u * b;   // B3 slot of the chunk
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {   // B = [S_hi ; S_lo], 64 rows
+          const uint64_t bk = tc::desc_add(dS, 2 * PLBO * k);
+          tc::mma_bf16(d3, tc::desc_add(dA3h, so + 256 * k), bk, id64, k > 0);
+          tc::mma_bf16(d3, tc::desc_add(dA3l, so + 256 * k), bk, id64, 1);
         }
         tc::mma_commit(mma3);
+        tc::mma_commit(b3empty + b);
       }
       wait_or_abort(mma3, par, abort, status);
-      if (e == 0 && c + 1 < nch && !*abort) {   // B3 free again
-        load_b3(c + 1);
-        ++issued3;
-      }
       tc::fence_after_sync();
       // U = U~ - W S (tokens 0..63 on lanes 64..127) -> B operand
       if (warp >= 2) {
-        uint32_t rv[SW];
-        tc::tmem_ld16_nw(tc::taddr(d3, warp * 32, 0), rv);
-        tc::tmem_ld16_nw(tc::taddr(d3, warp * 32, 16), rv + 16);
+        uint32_t rv[2 * SW];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nw(tc::taddr(d3, warp * 32, 16 * q), rv + 16 * q);
         tc::tmem_wait_ld();
-        tc::reg_fence16(rv);
-        tc::reg_fence16(rv + 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::reg_fence16(rv + 16 * q);
 #pragma unroll
         for (int q = 0; q < SW; ++q) {
           __nv_bfloat16 hi, lo;
-          tc::split_bf16(ut[q] - __uint_as_float(rv[q]), hi, lo);
+          tc::split_bf16(ut[q] - (__uint_as_float(rv[q]) + __uint_as_float(rv[q + SW])), hi, lo);
           const uint32_t off = tc::kmajor_off_p(q, t, PLBO, UOP_SBO);
           *reinterpret_cast<__nv_bfloat16*>(uoph + off) = hi;
           *reinterpret_cast<__nv_bfloat16*>(uopl + off) = lo;
@@ -810,89 +820,123 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       tc::fence_after_sync();
       if (e == 0 && wait_or_abort(b4full, par, abort, status)) {
         tc::fence_after_sync();
-        const uint32_t id = tc::idesc_bf16(128, SW);
-        const uint32_t ph = tc::smem_u32(b4h), pl = tc::smem_u32(b4l);
-        const uint32_t bh = tc::smem_u32(uoph), bl = tc::smem_u32(uopl);
-        for (int k = 0; k < 4; ++k) {   // S += K~^T U   (B4 rows 64..191)
-          tc::mma_bf16(tb, tc::kstep_desc(ph + 8192, 64, k), tc::kstep_desc_p(bh, PLBO, UOP_SBO, k), id, 1);
-          tc::mma_bf16(tb, tc::kstep_desc(ph + 8192, 64, k), tc::kstep_desc_p(bl, PLBO, UOP_SBO, k), id, 1);
-          tc::mma_bf16(tb, tc::kstep_desc(pl + 8192, 64, k), tc::kstep_desc_p(bh, PLBO, UOP_SBO, k), id, 1);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {   // S += K~^T U   (B4 rows 64..191; B = [U_hi ; U_lo])
+          const uint64_t bk = tc::desc_add(dU, 2 * PLBO * k);
+          tc::mma_bf16(tb + TC_S, tc::desc_add(dKh, 256 * k), bk, id64, 1);
+          tc::mma_bf16(tb + TC_S, tc::desc_add(dKl, 256 * k), bk, id64, 1);
         }
         // D3 += [P ; K~^T rows 0..63] U: rows 0..63 become O; rows 64..127 (W S, consumed) are
         // left as scratch
+#pragma unroll
         for (int k = 0; k < 4; ++k) {
-          tc::mma_bf16(d3, tc::kstep_desc(ph, 64, k), tc::kstep_desc_p(bh, PLBO, UOP_SBO, k), id, 1);
-          tc::mma_bf16(d3, tc::kstep_desc(ph, 64, k), tc::kstep_desc_p(bl, PLBO, UOP_SBO, k), id, 1);
-          tc::mma_bf16(d3, tc::kstep_desc(pl, 64, k), tc::kstep_desc_p(bh, PLBO, UOP_SBO, k), id, 1);
+          const uint64_t bk = tc::desc_add(dU, 2 * PLBO * k);
+          tc::mma_bf16(d3, tc::desc_add(dPh, 256 * k), bk, id64, 1);
+          tc::mma_bf16(d3, tc::desc_add(dPl, 256 * k), bk, id64, 1);
         }
         tc::mma_commit(mma4);
-        tc::mma_commit(dfull + b);
+        tc::mma_commit(b4empty);
+        tc::mma_commit(dfull + jd);
       }
       wait_or_abort(mma4, par, abort, status);
-      if (e == 0 && c + 1 < nch && !*abort) {   // B4 free again
-        load_b4(c + 1);
-        ++issued4;
-      }
       tc::fence_after_sync();
-    }
-    // after a timeout: wait (bounded) for bulk copies still in flight before the CTA exits
-    // (copy c + 1 is only issued once copy c was consumed, so at most the last one is pending)
-    if (e == 0 && *abort) {
-      if (issued3 > 0) tc::mbar_wait(b3full, (issued3 - 1) & 1, 100000000ull);
-      if (issued4 > 0) tc::mbar_wait(b4full, (issued4 - 1) & 1, 100000000ull);
     }
     // final state slice back to the slot
     if (valid) {
-      float v[SW];
-      tc::tmem_ld16(lane_base, v);
-      tc::tmem_ld16(lane_base + 16, v + 16);
+      float v[2 * SW];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tc::tmem_ld16(lane_base + TC_S + 16 * q, v + 16 * q);
+#pragma unroll
+      for (int q = 0; q < SW; ++q) v[q] += v[q + SW];
 #pragma unroll
       for (int q = 0; q < SW; q += 4)
         *reinterpret_cast<float4*>(Sg + (size_t)e * D + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
     }
+  } else if (warp == 7) {
+    // idle
+  } else if (warp == 6) {
+    // ================= loader warp: bulk copies of the chunks' operand images, each issued as soon
+    // as MMA has finished reading the buffer it refills (B3 double-buffered, B4 single)
+    if (lane == 0) {
+      int n3a = 0, n3b = 0, n4 = 0;   // copies issued per buffer
+      auto load_b3 = [&](int c) {
+        const int j = c & 1;
+        tc::mbar_arrive_expect_tx(b3full + j, 2 * B3_HALF);
+        tc::bulk_g2s(sm + S::B3 + j * 65536, rec_of(c) + R_B3, 2 * B3_HALF, b3full + j);
+        if (j) ++n3b;
+        else ++n3a;
+      };
+      auto load_b4 = [&](int c) {
+        tc::mbar_arrive_expect_tx(b4full, 2 * B4_HALF);
+        tc::bulk_g2s(b4h, rec_of(c) + R_B4, 2 * B4_HALF, b4full);
+        ++n4;
+      };
+      if (nch > 0) load_b3(0);
+      if (nch > 0) load_b4(0);
+      if (nch > 1) load_b3(1);
+      for (int c = 0; c + 1 < nch; ++c) {
+        if (!wait_or_abort(b4empty, c & 1, abort, status)) break;
+        load_b4(c + 1);
+        if (c + 2 < nch) {
+          if (!wait_or_abort(b3empty + (c & 1), (c >> 1) & 1, abort, status)) break;
+          load_b3(c + 2);
+        }
+      }
+      // after a timeout: wait (bounded) for the copies still in flight before the CTA exits
+      if (*abort) {
+        if (n3a > 0) tc::mbar_wait(b3full, (n3a - 1) & 1, 100000000ull);
+        if (n3b > 0) tc::mbar_wait(b3full + 1, (n3b - 1) & 1, 100000000ull);
+        if (n4 > 0) tc::mbar_wait(b4full, (n4 - 1) & 1, 100000000ull);
+      }
+    }
   } else {
-    // ================= epilogue warps: thread t owns token t of the chunk (TMEM lane t of D3)
-    const int t = tid - 128;
+    // ================= epilogue warps 4, 5, 8, 9: thread t owns token t of the chunk (TMEM lane t of
+    // D3) and the 16 columns of half xh of the slice
+    const int t = (warp & 3) * 32 + lane, xh = warp >> 3;
+    constexpr int EW = SW / XH;
     const size_t ld = (size_t)d.Hv * D;
-    const size_t col0 = (size_t)h * D + sig * SW;
-    float wn[SW];
+    const size_t col0 = (size_t)h * D + sig * SW + xh * EW;
+    float wn[EW];
 #pragma unroll
-    for (int q = 0; q < SW; q += 4) {
-      const float4 x = Act<T>::ldg4(norm_w + sig * SW + q);
+    for (int q = 0; q < EW; q += 4) {
+      const float4 x = Act<T>::ldg4(norm_w + sig * SW + xh * EW + q);
       wn[q] = x.x;
       wn[q + 1] = x.y;
       wn[q + 2] = x.z;
       wn[q + 3] = x.w;
     }
-    float4 zz[SW / 4];   // z of the next chunk, loaded while the MMAs run
+    float4 zz[EW / 4];   // z of the next chunk, loaded while the MMAs run
     auto load_z = [&](int c) {
       const int i = min(t, min(CH, len - c * CH) - 1);
       const T* zp = z + (size_t)(seq_start + c * CH + i) * ld + col0;
 #pragma unroll
-      for (int q = 0; q < SW / 4; ++q) zz[q] = Act<T>::ldg4(zp + 4 * q);
+      for (int q = 0; q < EW / 4; ++q) zz[q] = Act<T>::ldg4(zp + 4 * q);
     };
     if (nch > 0) load_z(0);
     const uint32_t xb_local = tc::smem_u32(xbuf);
     const uint32_t xf_local = tc::smem_u32(xfull);
     bool xok = true;
     for (int c = 0; c < nch; ++c) {
-      const uint32_t b = c & 1;
+      const uint32_t b = c & 1, jd = c & (NDB - 1);
       const int L = min(CH, len - c * CH);
-      wait_or_abort(dfull + b, (c >> 1) & 1, abort, status);
+      wait_or_abort(dfull + jd, (c / NDB) & 1, abort, status);
       tc::fence_after_sync();
-      float o[SW];
-      tc::tmem_ld16(tc::taddr(tb + SW + SW * b, (warp & 3) * 32, 0), o);
-      tc::tmem_ld16(tc::taddr(tb + SW + SW * b, (warp & 3) * 32, 16), o + 16);
+      float o[2 * EW];
+      const uint32_t da = tc::taddr(tb + TC_D3 + 64 * jd, (warp & 3) * 32, xh * EW);
+      tc::tmem_ld16(da, o);
+      tc::tmem_ld16(da + SW, o + EW);
+#pragma unroll
+      for (int q = 0; q < EW; ++q) o[q] += o[q + EW];
       tc::fence_before_sync();
-      mbar_arrive(dempty + b);
+      mbar_arrive(dempty + jd);
       float ss = 0.f;
 #pragma unroll
-      for (int q = 0; q < SW; ++q) ss = fmaf(o[q], o[q], ss);
-      if (t == 0 && c + 1 < nch) {   // the next use of the other buffer
-        tc::mbar_arrive_expect_tx(xfull + ((c + 1) & 1), NSL * 64 * 4);
+      for (int q = 0; q < EW; ++q) ss = fmaf(o[q], o[q], ss);
+      if (warp == 4 && lane == 0 && c + 1 < nch) {   // the next use of the other buffer
+        tc::mbar_arrive_expect_tx(xfull + ((c + 1) & 1), NSL * XH * 64 * 4);
         tc::fence_acq_rel_cluster();
       }
-      const uint32_t slot_off = ((b * NSL + crank) * 64 + t) * 4;
+      const uint32_t slot_off = (((b * NSL + crank) * XH + xh) * 64 + t) * 4;
 #pragma unroll
       for (uint32_t r = 0; r < NSL; ++r)
         tc::st_async_f32(tc::mapa_shared(xb_local + slot_off, r), ss,
@@ -904,12 +948,12 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       }
       float tot = 0.f;
 #pragma unroll
-      for (int r = 0; r < NSL; ++r) tot += xbuf[(b * NSL + r) * 64 + t];
+      for (int r = 0; r < NSL * XH; ++r) tot += xbuf[(b * NSL * XH + r) * 64 + t];
       const float inv = valid ? rsqrtf(tot * (1.0f / (float)D) + d.norm_eps) : 0.f;
       if (t < L) {
         T* op = out + (size_t)(seq_start + c * CH + t) * ld + col0;
 #pragma unroll
-        for (int q = 0; q < SW / 4; ++q) {
+        for (int q = 0; q < EW / 4; ++q) {
           const float4 r4 = make_float4(o[4 * q] * inv * wn[4 * q] * silu_fast(zz[q].x),
                                         o[4 * q + 1] * inv * wn[4 * q + 1] * silu_fast(zz[q].y),
                                         o[4 * q + 2] * inv * wn[4 * q + 2] * silu_fast(zz[q].z),
@@ -922,7 +966,7 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tb, 128);
+  if (warp == 0) tc::tmem_dealloc(tb, TC_COLS);
   // conv state <- the sequence's last K-1 raw inputs (older ones kept when continuing)
   if (valid && h == 0 && sig == 0) {
     T* csw = conv_state + (size_t)s * 3 * d.cqkv;

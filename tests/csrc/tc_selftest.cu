@@ -89,6 +89,91 @@ extern "C" int tc_gemm_p(const float* A, const float* B, float* D, int N, int K,
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
 }
 
+// The same GEMM with A moved into TMEM by tcgen05.cp (hi at columns [N, N + K/2), lo after it)
+// and the MMAs reading A from TMEM.
+__global__ void tc_gemm_ta_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                                  float* __restrict__ D, int N, int K, int passes, uint32_t ncols,
+                                  int* __restrict__ err) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned char* a_hi = sm;
+  unsigned char* a_lo = a_hi + 128 * K * 2;
+  unsigned char* b_hi = a_lo + 128 * K * 2;
+  unsigned char* b_lo = b_hi + N * K * 2;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(b_lo + N * K * 2);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+  for (int idx = tid; idx < 128 * K; idx += blockDim.x) {
+    const int r = idx / K, k = idx - r * K;
+    __nv_bfloat16 h, l;
+    split_bf16(A[idx], h, l);
+    *reinterpret_cast<__nv_bfloat16*>(a_hi + kmajor_off(r, k, K)) = h;
+    *reinterpret_cast<__nv_bfloat16*>(a_lo + kmajor_off(r, k, K)) = l;
+  }
+  for (int idx = tid; idx < N * K; idx += blockDim.x) {
+    const int r = idx / K, k = idx - r * K;
+    __nv_bfloat16 h, l;
+    split_bf16(B[idx], h, l);
+    *reinterpret_cast<__nv_bfloat16*>(b_hi + kmajor_off(r, k, K)) = h;
+    *reinterpret_cast<__nv_bfloat16*>(b_lo + kmajor_off(r, k, K)) = l;
+  }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (warp == 0) tmem_alloc(slot, ncols);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *slot;
+  if (tid == 0) {
+    const uint32_t id = idesc_bf16(128, N);
+    const uint32_t ah = smem_u32(a_hi), al = smem_u32(a_lo), bh = smem_u32(b_hi), bl = smem_u32(b_lo);
+    const uint32_t ta_hi = tbase + (uint32_t)N, ta_lo = ta_hi + (uint32_t)(K / 2);
+    for (int s = 0; s < K / 16; ++s) {
+      tmem_cp_128x256b(ta_hi + 8 * s, kstep_desc(ah, K, s));
+      tmem_cp_128x256b(ta_lo + 8 * s, kstep_desc(al, K, s));
+    }
+    for (int s = 0; s < K / 16; ++s) {
+      mma_bf16_ta(tbase, ta_hi + 8 * s, kstep_desc(bh, K, s), id, s > 0 ? 1u : 0u);
+      if (passes == 3) {
+        mma_bf16_ta(tbase, ta_hi + 8 * s, kstep_desc(bl, K, s), id, 1u);
+        mma_bf16_ta(tbase, ta_lo + 8 * s, kstep_desc(bh, K, s), id, 1u);
+      }
+    }
+    mma_commit(bar);
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(bar, 0);
+  if (!ok && lane == 0) atomicOr(err, 1);
+  fence_after_sync();
+  if (ok) {
+    for (int c0 = 0; c0 < N; c0 += 16) {
+      float v[16];
+      tmem_ld16(taddr(tbase, warp * 32, c0), v);
+      for (int i = 0; i < 16; ++i) D[(size_t)(warp * 32 + lane) * N + c0 + i] = v[i];
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, ncols);
+}
+
+extern "C" int tc_gemm_ta(const float* A, const float* B, float* D, int N, int K, int passes, int* err) {
+  if (N < 16 || N > 256 || N % 16 || K < 16 || K % 16 || N + K > 512) return -1;
+  uint32_t ncols = 32;
+  while (ncols < (uint32_t)(N + K)) ncols <<= 1;
+  const size_t smem = (size_t)2 * (128 + N) * K * 2 + 64;
+  if (smem > 200 * 1024) return -1;
+  if (cudaFuncSetAttribute(tc_gemm_ta_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return -2;
+  tc_gemm_ta_kernel<<<1, 128, smem>>>(A, B, D, N, K, passes, ncols, err);
+  if (cudaGetLastError() != cudaSuccess) return -3;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
+}
+
 extern "C" int tc_gemm(const float* A, const float* B, float* D, int N, int K, int passes, int* err) {
   return tc_gemm_p(A, B, D, N, K, passes, 128, err);
 }

@@ -29,6 +29,8 @@ def lib():
     l.tc_gemm.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
     l.tc_gemm_p.restype = ctypes.c_int
     l.tc_gemm_p.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p]
+    l.tc_gemm_ta.restype = ctypes.c_int
+    l.tc_gemm_ta.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
     l.tc_cluster_xchg.restype = ctypes.c_int
     l.tc_cluster_xchg.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
     return l
@@ -74,6 +76,27 @@ def test_tc_gemm_padded_b(lib, N, K):
     ref = A.astype(np.float64) @ B.astype(np.float64).T
     D = torch.zeros((128, N), dtype=torch.float32, device="cuda")
     assert lib.tc_gemm_p(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, K, 3, 144, err.data_ptr()) == 0
+    assert int(err.item()) == 0
+    e3 = np.max(np.abs(D.cpu().numpy() - ref)) / np.max(np.abs(ref))
+    assert e3 < 2e-5, e3
+
+
+@pytest.mark.parametrize("N,K", [(32, 128), (32, 64), (64, 128)])
+def test_tc_gemm_tmem_a(lib, N, K):
+    """A operand copied into TMEM with tcgen05.cp and read from there by the MMAs."""
+    rng = np.random.default_rng(N * 11 + K)
+    A = rng.standard_normal((128, K)).astype(np.float32)
+    B = rng.standard_normal((N, K)).astype(np.float32)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = A.astype(np.float64) @ B.astype(np.float64).T
+    D = torch.zeros((128, N), dtype=torch.float32, device="cuda")
+    assert lib.tc_gemm_ta(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, K, 1, err.data_ptr()) == 0
+    assert int(err.item()) == 0
+    ref1 = _bf16(A) @ _bf16(B).T
+    np.testing.assert_allclose(D.cpu().numpy(), ref1, rtol=0, atol=2e-4 * np.sqrt(K))
+    D.zero_()
+    assert lib.tc_gemm_ta(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, K, 3, err.data_ptr()) == 0
     assert int(err.item()) == 0
     e3 = np.max(np.abs(D.cpu().numpy() - ref)) / np.max(np.abs(ref))
     assert e3 < 2e-5, e3
