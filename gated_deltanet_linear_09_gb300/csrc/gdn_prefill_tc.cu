@@ -43,7 +43,7 @@ constexpr uint32_t R_SC = R_UT + 32768;          // f32 e^{gamma_L}
 constexpr uint32_t REC_BYTES = R_SC + 256;       // 147,712 bytes (multiple of 256)
 constexpr uint32_t B3_HALF = 32768, B4_HALF = 24576;
 
-__device__ __forceinline__ void bar_sync_main() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+__device__ __forceinline__ void bar_sync_main() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(bar)) : "memory");
@@ -597,9 +597,11 @@ constexpr uint32_t SOP_SBO = (D / 8) * PLBO;  // S operand: N = 32 rows, K = 128
 constexpr uint32_t SOP_HALF = (SW / 8) * SOP_SBO;
 constexpr uint32_t UOP_SBO = (CH / 8) * PLBO; // U operand: N = 32 rows, K = 64 (tokens)
 constexpr uint32_t UOP_HALF = (SW / 8) * UOP_SBO;
-constexpr int NTS = 320;   // warps 0-3 main, 4-5 and 8-9 epilogue, 6 loader (7 idle)
+constexpr int NTS = 448;   // warps 0-7 main, 8-9 and 12-13 epilogue, 10 loader (11 idle)
+constexpr int MH = SW / 2; // columns per main warp: warp w takes lanes 32 (w % 4) and half w / 4
 constexpr int NDB = 4;     // D3 (output) accumulators in flight between the MMAs and the epilogue
 constexpr int XH = 2;      // epilogue column halves: partial sums per token and CTA
+constexpr int NXB = 4;     // exchange buffers: chunk c's sums are sent one epilogue step before use
 
 // TMEM columns (lanes 0-127).  Each product runs as two N = 64 MMAs per K-step, A_hi [B_hi ; B_lo]
 // and A_lo [B_hi ; B_lo] (the B operand holds the hi rows 0-31 and the lo rows 32-63), so every
@@ -613,9 +615,9 @@ struct StateSmem {
   static constexpr uint32_t B4 = B3 + 2 * 65536;           // [P ; K~^T] rows [192 x 64], hi then lo
   static constexpr uint32_t SOP = B4 + 2 * 24576;          // S slice as B operand, hi then lo
   static constexpr uint32_t UOP = SOP + 2 * SOP_HALF;      // U slice as B operand, hi then lo
-  static constexpr uint32_t XBUF = UOP + 2 * UOP_HALF;     // f32 [2][NSL][XH][64] partial sums
-  static constexpr uint32_t BAR = XBUF + 2 * NSL * XH * 64 * 4;   // 18 mbarriers
-  static constexpr uint32_t MISC = BAR + 144;
+  static constexpr uint32_t XBUF = UOP + 2 * UOP_HALF;     // f32 [NXB][NSL][XH][64] partial sums
+  static constexpr uint32_t BAR = XBUF + NXB * NSL * XH * 64 * 4;   // 20 mbarriers
+  static constexpr uint32_t MISC = BAR + 160;
   static constexpr uint32_t BYTES = MISC + 64;
 };
 
@@ -644,7 +646,7 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   uint64_t* mma4 = bars + 7;
   uint64_t* dfull = bars + 8;    // [NDB] O of the chunk complete in D3[j] (MMA -> epilogue)
   uint64_t* dempty = bars + 12;  // [NDB] D3[j] read by the epilogue (epilogue -> MMA)
-  uint64_t* xfull = bars + 16;   // [2] partial sums of the 4 slices arrived
+  uint64_t* xfull = bars + 16;   // [NXB] partial sums of the 4 slices arrived
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
   int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);
 
@@ -662,9 +664,9 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     }
   }
   if (tid == 0) {
-    for (int i = 0; i < 18; ++i) tc::mbar_init(bars + i, (i >= 12 && i < 16) ? 128 : 1);
+    for (int i = 0; i < 20; ++i) tc::mbar_init(bars + i, (i >= 12 && i < 16) ? 128 : 1);
     tc::mbar_fence_init();
-    tc::mbar_arrive_expect_tx(xfull, NSL * XH * 64 * 4);   // chunk 0's partial sums
+    for (int i = 0; i < NXB; ++i) tc::mbar_arrive_expect_tx(xfull + i, NSL * XH * 64 * 4);   // chunks 0-3
   }
   if (warp == 0) tc::tmem_alloc(tslot, TC_COLS);
   tc::fence_before_sync();
@@ -686,34 +688,34 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     return reinterpret_cast<const unsigned char*>(ws) + ((size_t)(choff + c) * d.Hv + h) * REC_BYTES;
   };
 
-  if (warp < 4) {
-    // ================= main warps: thread e owns TMEM lane e = row e (dk index) of the S slice
-    const int e = tid;
-    const uint32_t lane_base = tc::taddr(tb, warp * 32, 0);
+  if (warp < 8) {
+    // ================= main warps: thread e owns TMEM lane e = row e (dk index) of the S slice and
+    // its columns [mh, mh + 16) (of both accumulator halves)
+    const int e = (warp & 3) * 32 + lane, mh = (warp >> 2) * MH;
+    const uint32_t lane_base = tc::taddr(tb, (warp & 3) * 32, 0);
     {
-      float v[SW];
+      float v[MH];
 #pragma unroll
-      for (int q = 0; q < SW; q += 4) {
-        const float4 x = init ? *reinterpret_cast<const float4*>(Sg + (size_t)e * D + q)
+      for (int q = 0; q < MH; q += 4) {
+        const float4 x = init ? *reinterpret_cast<const float4*>(Sg + (size_t)e * D + mh + q)
                               : make_float4(0.f, 0.f, 0.f, 0.f);
         v[q] = x.x;
         v[q + 1] = x.y;
         v[q + 2] = x.z;
         v[q + 3] = x.w;
       }
-      tc::tmem_st16(lane_base + TC_S, v);
-      tc::tmem_st16(lane_base + TC_S + 16, v + 16);
+      tc::tmem_st16(lane_base + TC_S + mh, v);
 #pragma unroll
-      for (int q = 0; q < SW; ++q) v[q] = 0.f;
-      tc::tmem_st16(lane_base + TC_S + 32, v);
-      tc::tmem_st16(lane_base + TC_S + 48, v + 16);
+      for (int q = 0; q < MH; ++q) v[q] = 0.f;
+      tc::tmem_st16(lane_base + TC_S + SW + mh, v);
     }
-    const int t = e - 64;             // token row of W S / U for warps 2 and 3
-    float ut[SW];                     // U~ slice of token t, loaded one chunk ahead
-    if (warp >= 2 && nch > 0) {
-      const float* u0 = reinterpret_cast<const float*>(rec_of(0) + R_UT) + t * D + sig * SW;
+    const int t = e - 64;             // token row of W S / U for lanes 64..127
+    const bool urow = (warp & 3) >= 2;
+    float ut[MH];                     // U~ of token t, columns mh.., loaded one chunk ahead
+    if (urow && nch > 0) {
+      const float* u0 = reinterpret_cast<const float*>(rec_of(0) + R_UT) + t * D + sig * SW + mh;
 #pragma unroll
-      for (int q = 0; q < SW; q += 4) {
+      for (int q = 0; q < MH; q += 4) {
         const float4 x = *reinterpret_cast<const float4*>(u0 + q);
         ut[q] = x.x;
         ut[q + 1] = x.y;
@@ -742,36 +744,34 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       const float egL = egL_next;
       if (c + 1 < nch) egL_next = *reinterpret_cast<const float*>(rec_of(c + 1) + R_SC);
       {
-        uint32_t rv[2 * SW];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nw(lane_base + TC_S + 16 * q, rv + 16 * q);
+        uint32_t rv[2 * MH];
+        tc::tmem_ld16_nw(lane_base + TC_S + mh, rv);
+        tc::tmem_ld16_nw(lane_base + TC_S + SW + mh, rv + MH);
         tc::tmem_wait_ld();
+        tc::reg_fence16(rv);
+        tc::reg_fence16(rv + MH);
+        float v[MH];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tc::reg_fence16(rv + 16 * q);
-        float v[SW];
-#pragma unroll
-        for (int q = 0; q < SW; ++q) {
-          v[q] = __uint_as_float(rv[q]) + __uint_as_float(rv[q + SW]);
+        for (int q = 0; q < MH; ++q) {
+          v[q] = __uint_as_float(rv[q]) + __uint_as_float(rv[q + MH]);
           __nv_bfloat16 hi, lo;
           tc::split_bf16(v[q], hi, lo);
-          const uint32_t off = tc::kmajor_off_p(q, e, PLBO, SOP_SBO);
+          const uint32_t off = tc::kmajor_off_p(mh + q, e, PLBO, SOP_SBO);
           *reinterpret_cast<__nv_bfloat16*>(soph + off) = hi;
           *reinterpret_cast<__nv_bfloat16*>(sopl + off) = lo;
           v[q] *= egL;
         }
-        tc::tmem_st16_nw(lane_base + TC_S, v);
-        tc::tmem_st16_nw(lane_base + TC_S + 16, v + 16);
+        tc::tmem_st16_nw(lane_base + TC_S + mh, v);
 #pragma unroll
-        for (int q = 0; q < SW; ++q) v[q] = 0.f;
-        tc::tmem_st16_nw(lane_base + TC_S + 32, v);
-        tc::tmem_st16_nw(lane_base + TC_S + 48, v + 16);
+        for (int q = 0; q < MH; ++q) v[q] = 0.f;
+        tc::tmem_st16_nw(lane_base + TC_S + SW + mh, v);
         tc::tmem_wait_st();
       }
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       bar_sync_main();
       tc::fence_after_sync();
-      if (e == 0 && wait_or_abort(b3full + b, (c >> 1) & 1, abort, status) &&
+      if (tid == 0 && wait_or_abort(b3full + b, (c >> 1) & 1, abort, status) &&
           (c < NDB || wait_or_abort(dempty + jd, ((c / NDB) - 1) & 1, abort, status))) {
         tc::fence_after_sync();
         const uint32_t so = 65536u * b;   // B3 slot of the chunk
@@ -787,25 +787,25 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       wait_or_abort(mma3, par, abort, status);
       tc::fence_after_sync();
       // U = U~ - W S (tokens 0..63 on lanes 64..127) -> B operand
-      if (warp >= 2) {
-        uint32_t rv[2 * SW];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tc::tmem_ld16_nw(tc::taddr(d3, warp * 32, 16 * q), rv + 16 * q);
+      if (urow) {
+        uint32_t rv[2 * MH];
+        tc::tmem_ld16_nw(tc::taddr(d3, (warp & 3) * 32, mh), rv);
+        tc::tmem_ld16_nw(tc::taddr(d3, (warp & 3) * 32, SW + mh), rv + MH);
         tc::tmem_wait_ld();
+        tc::reg_fence16(rv);
+        tc::reg_fence16(rv + MH);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tc::reg_fence16(rv + 16 * q);
-#pragma unroll
-        for (int q = 0; q < SW; ++q) {
+        for (int q = 0; q < MH; ++q) {
           __nv_bfloat16 hi, lo;
-          tc::split_bf16(ut[q] - (__uint_as_float(rv[q]) + __uint_as_float(rv[q + SW])), hi, lo);
-          const uint32_t off = tc::kmajor_off_p(q, t, PLBO, UOP_SBO);
+          tc::split_bf16(ut[q] - (__uint_as_float(rv[q]) + __uint_as_float(rv[q + MH])), hi, lo);
+          const uint32_t off = tc::kmajor_off_p(mh + q, t, PLBO, UOP_SBO);
           *reinterpret_cast<__nv_bfloat16*>(uoph + off) = hi;
           *reinterpret_cast<__nv_bfloat16*>(uopl + off) = lo;
         }
         if (c + 1 < nch) {
-          const float* un = reinterpret_cast<const float*>(rec_of(c + 1) + R_UT) + t * D + sig * SW;
+          const float* un = reinterpret_cast<const float*>(rec_of(c + 1) + R_UT) + t * D + sig * SW + mh;
 #pragma unroll
-          for (int q = 0; q < SW; q += 4) {
+          for (int q = 0; q < MH; q += 4) {
             const float4 x = *reinterpret_cast<const float4*>(un + q);
             ut[q] = x.x;
             ut[q + 1] = x.y;
@@ -818,7 +818,7 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       tc::fence_before_sync();
       bar_sync_main();
       tc::fence_after_sync();
-      if (e == 0 && wait_or_abort(b4full, par, abort, status)) {
+      if (tid == 0 && wait_or_abort(b4full, par, abort, status)) {
         tc::fence_after_sync();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {   // S += K~^T U   (B4 rows 64..191; B = [U_hi ; U_lo])
@@ -843,18 +843,18 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     }
     // final state slice back to the slot
     if (valid) {
-      float v[2 * SW];
+      float v[2 * MH];
+      tc::tmem_ld16(lane_base + TC_S + mh, v);
+      tc::tmem_ld16(lane_base + TC_S + SW + mh, v + MH);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tc::tmem_ld16(lane_base + TC_S + 16 * q, v + 16 * q);
+      for (int q = 0; q < MH; ++q) v[q] += v[q + MH];
 #pragma unroll
-      for (int q = 0; q < SW; ++q) v[q] += v[q + SW];
-#pragma unroll
-      for (int q = 0; q < SW; q += 4)
-        *reinterpret_cast<float4*>(Sg + (size_t)e * D + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+      for (int q = 0; q < MH; q += 4)
+        *reinterpret_cast<float4*>(Sg + (size_t)e * D + mh + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
     }
-  } else if (warp == 7) {
+  } else if (warp == 11) {
     // idle
-  } else if (warp == 6) {
+  } else if (warp == 10) {
     // ================= loader warp: bulk copies of the chunks' operand images, each issued as soon
     // as MMA has finished reading the buffer it refills (B3 double-buffered, B4 single)
     if (lane == 0) {
@@ -890,9 +890,9 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       }
     }
   } else {
-    // ================= epilogue warps 4, 5, 8, 9: thread t owns token t of the chunk (TMEM lane t of
-    // D3) and the 16 columns of half xh of the slice
-    const int t = (warp & 3) * 32 + lane, xh = warp >> 3;
+    // ================= epilogue warps 8, 9, 12, 13: thread t owns token t of the chunk (TMEM lane t
+    // of D3) and the 16 columns of half xh of the slice
+    const int t = (warp & 3) * 32 + lane, xh = (warp >> 2) & 1;
     constexpr int EW = SW / XH;
     const size_t ld = (size_t)d.Hv * D;
     const size_t col0 = (size_t)h * D + sig * SW + xh * EW;
@@ -905,63 +905,79 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       wn[q + 2] = x.z;
       wn[q + 3] = x.w;
     }
-    float4 zz[EW / 4];   // z of the next chunk, loaded while the MMAs run
-    auto load_z = [&](int c) {
+    // software-pipelined over the chunks: step c reads chunk c's outputs and sends their partial
+    // sums of squares to the cluster, then normalises and stores chunk c - 1, whose sums were
+    // sent one step earlier (so the exchange latency overlaps a step of work)
+    auto load_z = [&](int c, float4* zz) {
       const int i = min(t, min(CH, len - c * CH) - 1);
       const T* zp = z + (size_t)(seq_start + c * CH + i) * ld + col0;
 #pragma unroll
       for (int q = 0; q < EW / 4; ++q) zz[q] = Act<T>::ldg4(zp + 4 * q);
     };
-    if (nch > 0) load_z(0);
+    float4 zc[EW / 4], zp[EW / 4];   // z of chunk c (loaded at step c) and of chunk c - 1
+    float oc[EW], op[EW];
     const uint32_t xb_local = tc::smem_u32(xbuf);
     const uint32_t xf_local = tc::smem_u32(xfull);
     bool xok = true;
-    for (int c = 0; c < nch; ++c) {
-      const uint32_t b = c & 1, jd = c & (NDB - 1);
-      const int L = min(CH, len - c * CH);
-      wait_or_abort(dfull + jd, (c / NDB) & 1, abort, status);
-      tc::fence_after_sync();
-      float o[2 * EW];
-      const uint32_t da = tc::taddr(tb + TC_D3 + 64 * jd, (warp & 3) * 32, xh * EW);
-      tc::tmem_ld16(da, o);
-      tc::tmem_ld16(da + SW, o + EW);
+    for (int c = 0; c <= nch; ++c) {
 #pragma unroll
-      for (int q = 0; q < EW; ++q) o[q] += o[q + EW];
-      tc::fence_before_sync();
-      mbar_arrive(dempty + jd);
-      float ss = 0.f;
+      for (int q = 0; q < EW; ++q) op[q] = oc[q];
 #pragma unroll
-      for (int q = 0; q < EW; ++q) ss = fmaf(o[q], o[q], ss);
-      if (warp == 4 && lane == 0 && c + 1 < nch) {   // the next use of the other buffer
-        tc::mbar_arrive_expect_tx(xfull + ((c + 1) & 1), NSL * XH * 64 * 4);
-        tc::fence_acq_rel_cluster();
+      for (int q = 0; q < EW / 4; ++q) zp[q] = zc[q];
+      if (c < nch) {
+        const uint32_t jd = c & (NDB - 1), xb = c & (NXB - 1);
+        wait_or_abort(dfull + jd, (c / NDB) & 1, abort, status);
+        tc::fence_after_sync();
+        float o2[2 * EW];
+        const uint32_t da = tc::taddr(tb + TC_D3 + 64 * jd, (warp & 3) * 32, xh * EW);
+        tc::tmem_ld16(da, o2);
+        tc::tmem_ld16(da + SW, o2 + EW);
+        tc::fence_before_sync();
+        mbar_arrive(dempty + jd);
+        float ss = 0.f;
+#pragma unroll
+        for (int q = 0; q < EW; ++q) {
+          oc[q] = o2[q] + o2[q + EW];
+          ss = fmaf(oc[q], oc[q], ss);
+        }
+        const uint32_t slot_off = (((xb * NSL + crank) * XH + xh) * 64 + t) * 4;
+#pragma unroll
+        for (uint32_t r = 0; r < NSL; ++r)
+          tc::st_async_f32(tc::mapa_shared(xb_local + slot_off, r), ss,
+                           tc::mapa_shared(xf_local + xb * 8, r));
+        load_z(c, zc);
       }
-      const uint32_t slot_off = (((b * NSL + crank) * XH + xh) * 64 + t) * 4;
+      if (c >= 1) {
+        const int cp = c - 1;
+        const uint32_t xb = cp & (NXB - 1);
+        const int L = min(CH, len - cp * CH);
+        if (xok && !tc::mbar_wait_cluster(xfull + xb, (cp / NXB) & 1)) {
+          xok = false;
+          *abort = 1;
+          set_status(status, GDN_STATUS_TIMEOUT);
+        }
+        // this buffer's next use is chunk cp + NXB: its peers send that only after this CTA has
+        // sent chunk cp + 2, so posting the expected bytes now comes first
+        if (warp == 8 && lane == 0 && cp + NXB < nch) {
+          tc::mbar_arrive_expect_tx(xfull + xb, NSL * XH * 64 * 4);
+          tc::fence_acq_rel_cluster();
+        }
+        float tot = 0.f;
 #pragma unroll
-      for (uint32_t r = 0; r < NSL; ++r)
-        tc::st_async_f32(tc::mapa_shared(xb_local + slot_off, r), ss,
-                         tc::mapa_shared(xf_local + b * 8, r));
-      if (xok && !tc::mbar_wait_cluster(xfull + b, (c >> 1) & 1)) {
-        xok = false;
-        *abort = 1;
-        set_status(status, GDN_STATUS_TIMEOUT);
-      }
-      float tot = 0.f;
+        for (int r = 0; r < NSL * XH; ++r) tot += xbuf[(xb * NSL * XH + r) * 64 + t];
+        const float inv = valid ? rsqrtf(tot * (1.0f / (float)D) + d.norm_eps) : 0.f;
+        if (t < L) {
+          T* o_ptr = out + (size_t)(seq_start + cp * CH + t) * ld + col0;
 #pragma unroll
-      for (int r = 0; r < NSL * XH; ++r) tot += xbuf[(b * NSL * XH + r) * 64 + t];
-      const float inv = valid ? rsqrtf(tot * (1.0f / (float)D) + d.norm_eps) : 0.f;
-      if (t < L) {
-        T* op = out + (size_t)(seq_start + c * CH + t) * ld + col0;
-#pragma unroll
-        for (int q = 0; q < EW / 4; ++q) {
-          const float4 r4 = make_float4(o[4 * q] * inv * wn[4 * q] * silu_fast(zz[q].x),
-                                        o[4 * q + 1] * inv * wn[4 * q + 1] * silu_fast(zz[q].y),
-                                        o[4 * q + 2] * inv * wn[4 * q + 2] * silu_fast(zz[q].z),
-                                        o[4 * q + 3] * inv * wn[4 * q + 3] * silu_fast(zz[q].w));
-          Act<T>::store4(op + 4 * q, r4);
+          for (int q = 0; q < EW / 4; ++q) {
+            const float4 r4 = make_float4(op[4 * q] * inv * wn[4 * q] * silu_fast(zp[q].x),
+                                          op[4 * q + 1] * inv * wn[4 * q + 1] * silu_fast(zp[q].y),
+                                          op[4 * q + 2] * inv * wn[4 * q + 2] * silu_fast(zp[q].z),
+                                          op[4 * q + 3] * inv * wn[4 * q + 3] * silu_fast(zp[q].w));
+            Act<T>::store4(o_ptr + 4 * q, r4);
+          }
         }
       }
-      if (c + 1 < nch) load_z(c + 1);
     }
   }
   tc::fence_before_sync();
