@@ -491,43 +491,96 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     }
   }
   __syncthreads();
-  // ---- T = (I + A)^{-1} by forward substitution, T_i = e_i - sum_{j<i} A_ij T_j.  Warp w owns
-  // columns 8w..8w+7, lane l rows l and l + 32; at step j the owner of row j (already final)
-  // broadcasts it.  A_ij = 0 for j >= i, so rows <= j are left unchanged.  T goes straight into
-  // the split-bf16 B2 tile (rows i, K = j): 8 consecutive columns are one 16-byte unit.
+  // ---- T = (I + A)^{-1}, A strictly lower triangular, in 16 x 16 blocks: the diagonal inverses
+  // D_b = (I + A_bb)^{-1} by forward substitution (the four in parallel), then block row by block
+  // row  T_ik = -D_i sum_{j=k}^{i-1} A_ij T_jk  (k < i), each a few dense 16 x 16 products over
+  // all threads instead of one 64-step dependent chain.  T replaces A in Am (D_b over A_bb, T_ik
+  // over A_ik once block row i of A has been used); the partial sums X_ik live in the unused
+  // upper block (k, i).  Each final block also goes to the split-bf16 B2 tile (rows i, K = j).
   {
-    const int c0 = 8 * warp;
-    float t0r[8], t1r[8];
+    auto put_b2 = [&](int row, int col, float v) {
+      __nv_bfloat16 hi, lo;
+      tc::split_bf16(v, hi, lo);
+      const uint32_t off = tc::kmajor_off(row, col, 64);
+      *reinterpret_cast<__nv_bfloat16*>(b2h + off) = hi;
+      *reinterpret_cast<__nv_bfloat16*>(b2l + off) = lo;
+    };
+    float dcol[16];
+    const int db = tid >> 4, dc = tid & 15;   // threads 0-63: column dc of D_db
+    if (tid < 64) {
+      const float* ab = Am + (16 * db) * AS + 16 * db;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      t0r[q] = (lane == c0 + q) ? 1.f : 0.f;
-      t1r[q] = (lane + 32 == c0 + q) ? 1.f : 0.f;
-    }
+      for (int i = 0; i < 16; ++i) {
+        float arow[16];
 #pragma unroll
-    for (int j4 = 0; j4 < 64; j4 += 4) {
-      const float4 a04 = *reinterpret_cast<const float4*>(Am + lane * AS + j4);
-      const float4 a14 = *reinterpret_cast<const float4*>(Am + (lane + 32) * AS + j4);
-      const float a0s[4] = {a04.x, a04.y, a04.z, a04.w}, a1s[4] = {a14.x, a14.y, a14.z, a14.w};
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int j = j4 + jj;
-        float tj[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) tj[q] = __shfl_sync(0xffffffffu, j < 32 ? t0r[q] : t1r[q], j & 31);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          t0r[q] = fmaf(-a0s[jj], tj[q], t0r[q]);
-          t1r[q] = fmaf(-a1s[jj], tj[q], t1r[q]);
+        for (int m = 0; m < 16; m += 4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(ab + i * AS + m);
+          arow[m] = a4.x;
+          arow[m + 1] = a4.y;
+          arow[m + 2] = a4.z;
+          arow[m + 3] = a4.w;
         }
+        float acc = (i == dc) ? 1.f : 0.f;
+#pragma unroll
+        for (int j = 0; j < i; ++j) acc = fmaf(-arow[j], dcol[j], acc);
+        dcol[i] = acc;
+      }
+    } else {
+      // the six upper blocks of B2 are zero
+      for (int u = tid - 64; u < 6 * 256; u += NTI - 64) {
+        const int blk = u >> 8, el = u & 255;
+        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        put_b2(16 * bi + (el >> 4), 16 * bj + (el & 15), 0.f);
       }
     }
+    __syncthreads();
+    if (tid < 64) {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint4 hh, ll;
-      split8(half ? t1r : t0r, hh, ll);
-      const uint32_t off = tc::kmajor_off(lane + 32 * half, c0, 64);
-      st_unit(b2h, off, hh);
-      st_unit(b2l, off, ll);
+      for (int i = 0; i < 16; ++i) {
+        Am[(16 * db + i) * AS + 16 * db + dc] = dcol[i];
+        put_b2(16 * db + i, 16 * db + dc, dcol[i]);
+      }
+    }
+    __syncthreads();
+    const int r = tid >> 4, cc = tid & 15;   // element (r, cc) of every 16 x 16 block
+#pragma unroll
+    for (int i = 1; i < 4; ++i) {
+      const float* arow = Am + (16 * i + r) * AS;
+#pragma unroll
+      for (int k = 0; k < i; ++k) {   // X_ik -> block (k, i)
+        float acc = 0.f;
+#pragma unroll
+        for (int j = k; j < i; ++j) {
+          const float* tcol = Am + (16 * j) * AS + 16 * k + cc;
+#pragma unroll
+          for (int m = 0; m < 16; m += 4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(arow + 16 * j + m);
+            acc = fmaf(a4.x, tcol[m * AS], acc);
+            acc = fmaf(a4.y, tcol[(m + 1) * AS], acc);
+            acc = fmaf(a4.z, tcol[(m + 2) * AS], acc);
+            acc = fmaf(a4.w, tcol[(m + 3) * AS], acc);
+          }
+        }
+        Am[(16 * k + r) * AS + 16 * i + cc] = acc;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < i; ++k) {   // T_ik = -D_i X_ik -> block (i, k)
+        const float* xcol = Am + (16 * k) * AS + 16 * i + cc;
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; m += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(arow + 16 * i + m);
+          acc = fmaf(d4.x, xcol[m * AS], acc);
+          acc = fmaf(d4.y, xcol[(m + 1) * AS], acc);
+          acc = fmaf(d4.z, xcol[(m + 2) * AS], acc);
+          acc = fmaf(d4.w, xcol[(m + 3) * AS], acc);
+        }
+        Am[(16 * i + r) * AS + 16 * k + cc] = -acc;
+        put_b2(16 * i + r, 16 * k + cc, -acc);
+      }
+      if (i < 3) __syncthreads();
     }
   }
   tc::fence_proxy_async_smem();
