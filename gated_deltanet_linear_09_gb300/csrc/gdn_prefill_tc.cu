@@ -34,7 +34,7 @@ constexpr int CH = 64;
 constexpr int D = 128;
 
 // Per (chunk, V-head) record of the workspace.  B3 and B4 are stored as the exact shared-memory
-// images of the state kernel's B operands (split bf16, K-major core-matrix layout, hi then lo), so
+// images of the state kernel's A operands (split bf16, K-major core-matrix layout, hi then lo), so
 // the state kernel brings each in with one bulk copy.  Offsets in bytes.
 constexpr uint32_t R_B3 = 0;                     // [Q~ ; W] rows, 128 x 128: hi 32 KiB, lo 32 KiB
 constexpr uint32_t R_B4 = R_B3 + 65536;          // [P ; K~^T] rows, 192 x 64: hi 24 KiB, lo 24 KiB
