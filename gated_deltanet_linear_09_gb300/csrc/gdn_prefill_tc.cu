@@ -231,6 +231,23 @@ __device__ __forceinline__ void conv_load(const KDims& d, const T* __restrict__ 
     in.xs[k] = Act<T>::ldg(qkv + (size_t)(t0 + min(i0 + k, L - 1)) * d.cqkv + ch);
 }
 
+// The same, into registers (tokens i0..i0+31 of channel f, zero past L).
+__device__ __forceinline__ void conv_compute_regs(const ConvIn& in, int L, float* y) {
+  const int i0 = (threadIdx.x >> 7) * 32;
+  float xm3 = in.hist[0], xm2 = in.hist[1], xm1 = in.hist[2];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    float acc = in.w[3] * in.xs[k];
+    acc = fmaf(in.w[0], xm3, acc);
+    acc = fmaf(in.w[1], xm2, acc);
+    acc = fmaf(in.w[2], xm1, acc);
+    y[k] = (i0 + k < L) ? silu_fast(acc) : 0.f;
+    xm3 = xm2;
+    xm2 = xm1;
+    xm1 = in.xs[k];
+  }
+}
+
 __device__ __forceinline__ void conv_compute(const ConvIn& in, int L, float* X) {
   const int tid = threadIdx.x;
   const int f = tid & 127, i0 = (tid >> 7) * 32;
@@ -249,14 +266,26 @@ __device__ __forceinline__ void conv_compute(const ConvIn& in, int L, float* X) 
 }
 
 // Per-row l2 normalisation of X (64 rows x 128), times scale.
+// Warp w normalises rows w, w + 8, ..., all eight at once (their reductions interleave).
 __device__ __forceinline__ void l2norm_rows(float* X, float eps, float scale) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = warp; i < CH; i += NTI / 32) {
-    const float4 v = *reinterpret_cast<const float4*>(X + i * XS + 4 * lane);
-    float ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    ss = warp_sum(ss);
-    const float inv = scale / sqrtf(ss + eps);
-    *reinterpret_cast<float4*>(X + i * XS + 4 * lane) = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+  constexpr int RPW = CH / (NTI / 32);
+  float4 v[RPW];
+  float ss[RPW];
+#pragma unroll
+  for (int m = 0; m < RPW; ++m) {
+    v[m] = *reinterpret_cast<const float4*>(X + (warp + m * (NTI / 32)) * XS + 4 * lane);
+    ss[m] = v[m].x * v[m].x + v[m].y * v[m].y + v[m].z * v[m].z + v[m].w * v[m].w;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int m = 0; m < RPW; ++m) ss[m] += __shfl_xor_sync(0xffffffffu, ss[m], off);
+#pragma unroll
+  for (int m = 0; m < RPW; ++m) {
+    const float inv = scale * rsqrtf(ss[m] + eps);
+    *reinterpret_cast<float4*>(X + (warp + m * (NTI / 32)) * XS + 4 * lane) =
+        make_float4(v[m].x * inv, v[m].y * inv, v[m].z * inv, v[m].w * inv);
   }
 }
 
@@ -268,22 +297,6 @@ __device__ __forceinline__ void x_rows_to_tile(const float* X, unsigned char* hi
     const float4 a = *reinterpret_cast<const float4*>(X + r * XS + kg * 8);
     const float4 b = *reinterpret_cast<const float4*>(X + r * XS + kg * 8 + 4);
     const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-    uint4 hh, ll;
-    split8(v, hh, ll);
-    st_unit(hi, (uint32_t)u * 16u, hh);
-    st_unit(lo, (uint32_t)u * 16u, ll);
-  }
-}
-
-// Columns of X scaled per token -> K-major shared tile [128 features][64 tokens] (hi / lo).
-// Unit u: feature & 7 = u & 7, token group = (u >> 3) & 7, feature group = u >> 6.
-__device__ __forceinline__ void x_cols_to_tile(const float* X, const float* scale,
-                                               unsigned char* hi, unsigned char* lo) {
-  for (int u = threadIdx.x; u < 1024; u += NTI) {
-    const int f = ((u >> 6) << 3) + (u & 7), jg = (u >> 3) & 7;
-    float v[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = X[(jg * 8 + q) * XS + f] * scale[jg * 8 + q];
     uint4 hh, ll;
     split8(v, hh, ll);
     st_unit(hi, (uint32_t)u * 16u, hh);
@@ -366,6 +379,9 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   unsigned char* rec = reinterpret_cast<unsigned char*>(ws) + ((size_t)c * d.Hv + h) * REC_BYTES;
   float* rec_ut = reinterpret_cast<float*>(rec + R_UT);
 
+  // K inputs in flight while the gates are formed
+  ConvIn cin;
+  conv_load<T>(d, qkv, conv_w, cs, init, d.Hk * D + kh * D, seq_start, seq_len, t0, L, cin);
   if (tid == 0) {
     tc::mbar_init(bar, 1);
     tc::mbar_fence_init();
@@ -408,8 +424,6 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   }
 
   // ---- K: conv, l2norm, A1 K rows, K~^T rows of B4
-  ConvIn cin;
-  conv_load<T>(d, qkv, conv_w, cs, init, d.Hk * D + kh * D, seq_start, seq_len, t0, L, cin);
   conv_compute(cin, L, X);
   conv_load<T>(d, qkv, conv_w, cs, init, kh * D, seq_start, seq_len, t0, L, cin);   // Q, in flight
   __syncthreads();
@@ -445,16 +459,30 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     }
     tc::mma_commit(bar);
   }
-  // ---- V (overlaps the MMA): conv into X
-  conv_compute(cin, L, X);
+  // ---- V (overlaps the MMA): conv into registers
+  float vy[32];
+  conv_compute_regs(cin, L, vy);
   // ---- A1 is free once MMA1 completed: (beta e^g K)^T into its Q quarters, then (beta V)^T
-  // into its K quarters
+  // into its K quarters, straight from the V registers (thread: feature f, tokens i0..i0+31,
+  // i.e. four 8-token units of the K-major [128 features][64 tokens] tile)
   wait_or_abort(bar, 0, abort, status);
   tc::fence_after_sync();
   a1k_cols_to_tile(a1 + S::K_HI, a1 + S::K_LO, bgk, a1 + S::Q_HI, a1 + S::Q_LO);
   __syncthreads();
-  x_cols_to_tile(X, bet, a1 + S::K_HI, a1 + S::K_LO);
-  __syncthreads();   // X (V) consumed: A and B2 take its place
+  {
+    const int f = tid & 127, i0 = (tid >> 7) * 32;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float v8[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v8[q] = vy[8 * g + q] * bet[i0 + 8 * g + q];
+      uint4 hh, ll;
+      split8(v8, hh, ll);
+      const uint32_t off = tc::kmajor_off(f, i0 + 8 * g, 64);
+      st_unit(a1 + S::K_HI, off, hh);
+      st_unit(a1 + S::K_LO, off, ll);
+    }
+  }
   // ---- A and P from D1: warp w reads TMEM lanes 32 (w % 4) and the 32 columns of half w / 4
   {
     const int r = (warp & 3) * 32 + lane, j0 = (warp >> 2) * 32;
@@ -466,10 +494,15 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
       const int i = r;
       const float gi = gam[i], bi = (i < L) ? bet[i] : 0.f;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int j = j0 + q;
-        const float m = (j < i) ? bi : 0.f;
-        Am[i * AS + j] = m * exp_fast(fminf(gi - gam[j], 0.f)) * v[q];
+      for (int q = 0; q < 32; q += 4) {
+        float a4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + q + u;
+          const float m = (j < i) ? bi : 0.f;
+          a4[u] = m * exp_fast(fminf(gi - gam[j], 0.f)) * v[q + u];
+        }
+        *reinterpret_cast<float4*>(Am + i * AS + j0 + q) = make_float4(a4[0], a4[1], a4[2], a4[3]);
       }
     } else {
       const int i = r - 64;
