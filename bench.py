@@ -34,6 +34,7 @@ METRIC = "GDN decode state GB/s (% of HBM peak) at B=64; chunked prefill tokens/
 UNIT = "GB/s"
 DECODE_WL = 2
 PREFILL_WL = 3
+MULTI_T = 4   # tokens per row of the multi-token decode line
 
 # Per-launch DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of the decode kernel
 # from one ncu capture at B=64, keyed by the SHA-256 of the kernel source it was taken on.  A
@@ -261,6 +262,26 @@ def run_ours(args, ws, rank, local):
     e2e_gbs = e2e_bytes / (e2e_ms * 1e-3) / 1e9
     del ring, host, dev_in, dev_pack
 
+    # ---------------- multi-token decode: the same 64 rows, MULTI_T tokens per row per call
+    mt_in = []
+    for j in range(2):
+        toks = [synth.decode_step_inputs(wl, 1000 + MULTI_T * j + t, wl.batch) for t in range(MULTI_T)]
+        mt_in.append(layer.inputs({k: np.ascontiguousarray(np.stack([x[k] for x in toks], axis=1))
+                                   for k in toks[0]}))
+    mt_out = torch.empty((wl.batch, MULTI_T, geo.zdim), dtype=layer.act, device="cuda")
+    for j in range(3):
+        layer.decode_multi(slots, out=mt_out, **mt_in[j % 2])
+    torch.cuda.synchronize()
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    mreps = 50
+    m0.record(stream)
+    for j in range(mreps):
+        layer.decode_multi(slots, out=mt_out, **mt_in[j % 2])
+    m1.record(stream)
+    torch.cuda.synchronize()
+    multi_ms = m0.elapsed_time(m1) / mreps
+    del mt_in, mt_out
+
     # ---------------- compaction at step 256 of the B=64 workload (56 survivors -> [0,56))
     retire = synth.retire_choice(wl.seed, wl.batch, 8, 256)
     keep = [i for i in range(wl.batch) if i not in set(retire.tolist())]
@@ -322,6 +343,11 @@ def run_ours(args, ws, rank, local):
                                  "peak": bf16_peak, "unit": "TFLOP/s",
                                  "frac": round(p_tflops / bf16_peak, 5), "peak_kind": peak_kind},
                     "io_bytes": p_bytes, "launches_per_call": 2},
+        "decode_multi": {"tokens_per_row": MULTI_T, "rows": wl.batch, "ms": round(multi_ms, 5),
+                         "tokens_per_s": round(wl.batch * MULTI_T / (multi_ms * 1e-3), 1),
+                         "state_gbs": round(state_bytes / (multi_ms * 1e-3) / 1e9, 1),
+                         "state_bytes_per_token": state_bytes // (wl.batch * MULTI_T),
+                         "single_step_tokens_per_s": round(wl.batch / (ms_step * 1e-3), 1)},
         "compact": {"pairs": len(keep), "bytes": comp_bytes, "ms": round(comp_ms, 4),
                     "gbs": round(comp_bytes / (comp_ms * 1e-3) / 1e9, 1),
                     "hbm_frac": round(comp_bytes / (comp_ms * 1e-3) / 1e9 / hbm_peak, 4)},

@@ -97,6 +97,23 @@ int gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* 
   return gdn::launch_decode(d, w, pool, slot_idx, B, qkv, z, a, b, out, stream);
 }
 
+int gdn_decode_multi(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
+                     const int32_t* slot_idx, int32_t B, int32_t T, const void* qkv,
+                     const void* z, const void* a, const void* b, void* out, cudaStream_t stream) {
+  gdn::KDims d;
+  int rc;
+  if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
+  if ((rc = check_weights(w)) != GDN_OK) return rc;
+  if ((rc = check_pool(pool)) != GDN_OK) return rc;
+  if (T < 1 || T > GDN_MAX_DECODE_TOKENS) return GDN_ERR_INVALID_ARG;
+  if (B < 0 || B > 65535) return B < 0 ? GDN_ERR_INVALID_ARG : GDN_ERR_TOO_LARGE;
+  if (B == 0) return GDN_OK;
+  if (!slot_idx || !qkv || !z || !a || !b || !out) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(z) || !aligned16(out) || !aligned16(slot_idx))
+    return GDN_ERR_MISALIGNED;
+  return gdn::launch_decode_multi(d, w, pool, slot_idx, B, T, qkv, z, a, b, out, stream);
+}
+
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t num_seqs, int32_t total_tokens) {
   gdn::KDims d;
   if (check_dims(dims, &d) != GDN_OK || num_seqs < 0 || total_tokens < 0) return 0;

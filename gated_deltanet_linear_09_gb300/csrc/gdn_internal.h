@@ -9,6 +9,10 @@ int launch_decode(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
                   const int32_t* slot_idx, int B, const void* qkv, const void* z, const void* a,
                   const void* b, void* out, cudaStream_t stream);
 
+int launch_decode_multi(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
+                        const int32_t* slot_idx, int B, int TT, const void* qkv, const void* z,
+                        const void* a, const void* b, void* out, cudaStream_t stream);
+
 int launch_conv1d_update(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
                          const int32_t* slot_idx, int B, const void* in, void* out,
                          cudaStream_t stream);

@@ -28,9 +28,10 @@ _CODES = {
 }
 
 # Every symbol include/gdn.h declares.
-EXPORTED = ("gdn_state_slot_bytes", "gdn_conv1d_update", "gdn_decode_step",
+EXPORTED = ("gdn_state_slot_bytes", "gdn_conv1d_update", "gdn_decode_step", "gdn_decode_multi",
             "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_state_compact",
             "gdn_status_string", "gdn_prefill_chunked_noalloc")
+GDN_MAX_DECODE_TOKENS = 8
 GDN_NOALLOC_PREFILL_SCRATCH_BYTES = 64 << 20
 
 
@@ -86,6 +87,8 @@ def load(build_if_missing: bool = False):
     lib.gdn_decode_step.restype = ctypes.c_int
     lib.gdn_decode_step.argtypes = [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P]
     lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
+    lib.gdn_decode_multi.argtypes = [_P, _P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P]
+    lib.gdn_decode_multi.restype = ctypes.c_int
     lib.gdn_prefill_workspace_bytes.argtypes = [_P, _I32, _I32]
     lib.gdn_prefill_chunked.restype = ctypes.c_int
     lib.gdn_prefill_chunked.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P,
@@ -160,6 +163,14 @@ def gdn_decode_step(dims, weights, pool, slot_idx, qkv, z, a, b, out, stream=Non
     B = slot_idx.shape[0]
     _check("gdn_decode_step", load().gdn_decode_step(
         ctypes.byref(dims), ctypes.byref(weights), ctypes.byref(pool), _ptr(slot_idx), B,
+        _ptr(qkv), _ptr(z), _ptr(a), _ptr(b), _ptr(out), _stream(stream)))
+
+
+def gdn_decode_multi(dims, weights, pool, slot_idx, qkv, z, a, b, out, stream=None):
+    """T tokens per row: qkv [B][T][Cqkv], z/out [B][T][Hv*dv], a/b [B][T][Hv]."""
+    B, T = int(qkv.shape[0]), int(qkv.shape[1])
+    _check("gdn_decode_multi", load().gdn_decode_multi(
+        ctypes.byref(dims), ctypes.byref(weights), ctypes.byref(pool), _ptr(slot_idx), B, T,
         _ptr(qkv), _ptr(z), _ptr(a), _ptr(b), _ptr(out), _stream(stream)))
 
 

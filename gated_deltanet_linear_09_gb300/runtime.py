@@ -60,6 +60,14 @@ class GatedDeltaNetLayer:
         gdn.gdn_decode_step(self.dims, self.w, self.pool, slot_idx, qkv, z, a, b, out, stream)
         return out
 
+    def decode_multi(self, slot_idx: torch.Tensor, qkv, z, a, b, out=None, stream=None):
+        """T consecutive tokens per row: qkv [B][T][Cqkv], z [B][T][Hv*dv], a/b [B][T][Hv]."""
+        if out is None:
+            out = torch.empty((qkv.shape[0], qkv.shape[1], self.geo.zdim), dtype=self.act,
+                              device=self.device)
+        gdn.gdn_decode_multi(self.dims, self.w, self.pool, slot_idx, qkv, z, a, b, out, stream)
+        return out
+
     def conv1d_update(self, slot_idx: torch.Tensor, qkv_in, out=None, stream=None):
         if out is None:
             out = torch.empty_like(qkv_in)

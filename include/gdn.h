@@ -131,6 +131,24 @@ int gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* 
                     const int32_t* slot_idx, int32_t B, const void* qkv, const void* z,
                     const void* a, const void* b, void* out, cudaStream_t stream);
 
+/* Largest number of tokens per row of one gdn_decode_multi call. */
+#define GDN_MAX_DECODE_TOKENS 8
+
+/* Multi-token decode (speculative verify / multi-token append; the decode step of "pegainfer
+ * issue #1001", Split 2, run over T consecutive tokens per row): row i appends tokens
+ * 0..T-1 in order to slot s = slot_idx[i], with the same result as T successive
+ * gdn_decode_step calls, token t of every row in call t -- but each V-head state is read and
+ * written once per call instead of once per token.  1 <= T <= GDN_MAX_DECODE_TOKENS.
+ *   qkv  [B][T][Cqkv], z and out [B][T][Hv*dv], a and b [B][T][Hv], activation dtype, device,
+ *        row-major; qkv, z, out 16-byte aligned.  slot_idx: device int32[B], distinct slots.
+ *   On return the slot holds the state after token T-1 and its last K-1 raw inputs.
+ * One kernel launch; no host reads of device data (graph-capturable).  An out-of-range s sets
+ * GDN_STATUS_SLOT_RANGE and zeroes that row's outputs.  T outside [1, GDN_MAX_DECODE_TOKENS]:
+ * GDN_ERR_INVALID_ARG, nothing launched. */
+int gdn_decode_multi(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
+                     const int32_t* slot_idx, int32_t B, int32_t T, const void* qkv,
+                     const void* z, const void* a, const void* b, void* out, cudaStream_t stream);
+
 /* Workspace bytes gdn_prefill_chunked needs for num_seqs sequences of total_tokens tokens
  * (the chunkwise scratch, "GdrChunkwiseScratch35" of "pegainfer PR #1003"). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t num_seqs, int32_t total_tokens);

@@ -83,6 +83,22 @@ def test_decode_host_checks(lib):
     assert _call_decode(lib, D(), aligned=False) == -7
 
 
+def test_decode_multi_host_checks(lib):
+    d = D()
+    w = gdn.gdn_weights(0x20000, 0x20000, 0x20000, 0x20000, gdn.GDN_BF16)
+    p = gdn.gdn_pool(0x30000, 0x30000, 4, None)
+
+    def call(B, T, fake=0x10000):
+        return lib.gdn_decode_multi(ctypes.byref(d), ctypes.byref(w), ctypes.byref(p), 0x40000, B,
+                                    T, fake, fake, fake, fake, fake, None)
+    assert call(1, 0) == -1                           # T outside [1, GDN_MAX_DECODE_TOKENS]
+    assert call(1, gdn.GDN_MAX_DECODE_TOKENS + 1) == -1
+    assert call(-1, 2) == -1
+    assert call(70000, 2) == -9
+    assert call(0, 2) == 0                            # empty batch: no-op
+    assert call(1, 2, fake=0x10008 + 2) == -7
+
+
 def test_prefill_and_compact_host_checks(lib):
     d = D()
     w = gdn.gdn_weights(0x20000, 0x20000, 0x20000, 0x20000, gdn.GDN_BF16)
