@@ -1,15 +1,17 @@
 // gdn_decode_multi.cu -- multi-token decode: T = 1..GDN_MAX_DECODE_TOKENS consecutive tokens per
 // row (speculative-verify or multi-token append), each recurrent state read and written once.
 //
-// Per token the arithmetic is exactly the single-token decode step's: the causal conv + SiLU of
+// Per token it computes what the single-token decode step computes: the causal conv + SiLU of
 // the fused [q | k | v] channels ("helexa/cortex commit 95dc874 (tp_qwen3_5)",
 // TpQwen3_5GatedDeltaNet bullet), l2norm of q and k, the gates g = -exp(A_log) softplus(a +
 // dt_bias) and beta = sigmoid(b), the delta-rule update of the dk x dv state and the z-gated
 // RMSNorm of the output ("pegainfer PR #1003", description bullets).  The T tokens of a row are
-// applied in order to the state while it sits in registers, so a step of T tokens costs one
-// state read and one state write instead of T of each -- the HBM cost that bounds decode.
-// At T <= 8 this token-by-token form does less work than the chunkwise (UT) form with C = T,
-// which would add a T x T triangular solve, and reads the state the same single time.
+// taken together in the chunkwise (UT) form of the gated delta rule with C = T (Yang et al.,
+// "Parallelizing Linear Transformers with the Delta Rule over Sequence Length", NeurIPS 2024,
+// section 3): one pass over the old state S0 gives S0^T k_t and S0^T q_t for all tokens, a
+// T x T unit lower-triangular solve per state column gives the deltas, and the state takes one
+// rank-T update -- so a call of T tokens reads and writes each state once, the HBM cost that
+// bounds decode, and synchronises once per V-head instead of once per token.
 //
 // As in the single-token kernel, one CTA owns one (row, K-head) unit: the K-head's q and k conv
 // channels, the v channels of its r = Hv/Hk V-heads and their states, which keeps the conv-state
