@@ -143,7 +143,7 @@ def run_ours(args, ws, rank, local):
     import torch
     from gated_deltanet_linear_09_gb300 import build as gbuild
     from gated_deltanet_linear_09_gb300 import gdn, synth
-    from gated_deltanet_linear_09_gb300.runtime import GatedDeltaNetLayer
+    from gated_deltanet_linear_09_gb300.runtime import DecodeGraphs, GatedDeltaNetLayer
 
     gbuild.build()
     gdn.load()
@@ -282,6 +282,36 @@ def run_ours(args, ws, rank, local):
     multi_ms = m0.elapsed_time(m1) / mreps
     del mt_in, mt_out
 
+    # ---------------- CUDA-graph decode against eager calls: one row and all 64 rows, per-step
+    # time on the GPU timeline (the gaps between eager launches included)
+    graphs = DecodeGraphs(layer, [1, 2, 4, 8, 16, 32, 64])
+    graph_us = {}
+    for B in (1, wl.batch):
+        gx = layer.inputs(synth.decode_step_inputs(wl, 2000, B))
+        graphs.slot_idx[:B].copy_(slots[:B])
+        for k in ("qkv", "z", "a", "b"):
+            getattr(graphs, k)[:B].copy_(gx[k])
+        eo = torch.empty((B, geo.zdim), dtype=layer.act, device="cuda")
+        for mode in ("eager", "graph"):
+            def one():
+                if mode == "graph":
+                    graphs.step(B)
+                else:
+                    layer.decode_step(slots[:B], gx["qkv"], gx["z"], gx["a"], gx["b"], eo)
+            for _ in range(10):
+                one()
+            torch.cuda.synchronize()
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            greps = 200
+            g0.record(stream)
+            for _ in range(greps):
+                one()
+            g1.record(stream)
+            torch.cuda.synchronize()
+            graph_us[f"B{B}_{mode}_us"] = round(g0.elapsed_time(g1) / greps * 1e3, 2)
+    graphs.close()
+    del graphs
+
     # ---------------- compaction at step 256 of the B=64 workload (56 survivors -> [0,56))
     retire = synth.retire_choice(wl.seed, wl.batch, 8, 256)
     keep = [i for i in range(wl.batch) if i not in set(retire.tolist())]
@@ -348,6 +378,7 @@ def run_ours(args, ws, rank, local):
                          "state_gbs": round(state_bytes / (multi_ms * 1e-3) / 1e9, 1),
                          "state_bytes_per_token": state_bytes // (wl.batch * MULTI_T),
                          "single_step_tokens_per_s": round(wl.batch / (ms_step * 1e-3), 1)},
+        "decode_graphs": dict(graph_us, buckets=[1, 2, 4, 8, 16, 32, 64]),
         "compact": {"pairs": len(keep), "bytes": comp_bytes, "ms": round(comp_ms, 4),
                     "gbs": round(comp_bytes / (comp_ms * 1e-3) / 1e9, 1),
                     "hbm_frac": round(comp_bytes / (comp_ms * 1e-3) / 1e9 / hbm_peak, 4)},

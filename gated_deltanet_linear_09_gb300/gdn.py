@@ -30,8 +30,10 @@ _CODES = {
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_state_slot_bytes", "gdn_conv1d_update", "gdn_decode_step", "gdn_decode_multi",
             "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_state_compact",
-            "gdn_status_string", "gdn_prefill_chunked_noalloc")
+            "gdn_status_string", "gdn_prefill_chunked_noalloc", "gdn_decode_graphs_create",
+            "gdn_decode_graphs_buffers", "gdn_decode_graphs_launch", "gdn_decode_graphs_destroy")
 GDN_MAX_DECODE_TOKENS = 8
+GDN_MAX_GRAPH_BUCKETS = 16
 GDN_NOALLOC_PREFILL_SCRATCH_BYTES = 64 << 20
 
 
@@ -89,6 +91,14 @@ def load(build_if_missing: bool = False):
     lib.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
     lib.gdn_decode_multi.argtypes = [_P, _P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P]
     lib.gdn_decode_multi.restype = ctypes.c_int
+    lib.gdn_decode_graphs_create.argtypes = [_P, _P, _P, _P, _I32, _P]
+    lib.gdn_decode_graphs_create.restype = ctypes.c_int
+    lib.gdn_decode_graphs_buffers.argtypes = [_P] + [_P] * 7
+    lib.gdn_decode_graphs_buffers.restype = ctypes.c_int
+    lib.gdn_decode_graphs_launch.argtypes = [_P, _I32, _P]
+    lib.gdn_decode_graphs_launch.restype = ctypes.c_int
+    lib.gdn_decode_graphs_destroy.argtypes = [_P]
+    lib.gdn_decode_graphs_destroy.restype = None
     lib.gdn_prefill_workspace_bytes.argtypes = [_P, _I32, _I32]
     lib.gdn_prefill_chunked.restype = ctypes.c_int
     lib.gdn_prefill_chunked.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P,
@@ -172,6 +182,35 @@ def gdn_decode_multi(dims, weights, pool, slot_idx, qkv, z, a, b, out, stream=No
     _check("gdn_decode_multi", load().gdn_decode_multi(
         ctypes.byref(dims), ctypes.byref(weights), ctypes.byref(pool), _ptr(slot_idx), B, T,
         _ptr(qkv), _ptr(z), _ptr(a), _ptr(b), _ptr(out), _stream(stream)))
+
+
+def gdn_decode_graphs_create(dims, weights, pool, buckets) -> int:
+    """Returns the object handle (an address)."""
+    arr = (ctypes.c_int32 * len(buckets))(*[int(x) for x in buckets])
+    h = ctypes.c_void_p()
+    _check("gdn_decode_graphs_create", load().gdn_decode_graphs_create(
+        ctypes.byref(dims), ctypes.byref(weights), ctypes.byref(pool), arr, len(buckets),
+        ctypes.byref(h)))
+    return h.value
+
+
+def gdn_decode_graphs_buffers(handle) -> dict:
+    """Device addresses of the static buffers and the largest bucket."""
+    ptrs = [ctypes.c_void_p() for _ in range(6)]
+    mb = ctypes.c_int32()
+    _check("gdn_decode_graphs_buffers", load().gdn_decode_graphs_buffers(
+        handle, *[ctypes.byref(p) for p in ptrs], ctypes.byref(mb)))
+    d = dict(zip(("slot_idx", "qkv", "z", "a", "b", "out"), (p.value for p in ptrs)))
+    d["max_batch"] = mb.value
+    return d
+
+
+def gdn_decode_graphs_launch(handle, B: int, stream=None):
+    _check("gdn_decode_graphs_launch", load().gdn_decode_graphs_launch(handle, B, _stream(stream)))
+
+
+def gdn_decode_graphs_destroy(handle):
+    load().gdn_decode_graphs_destroy(handle)
 
 
 def gdn_prefill_workspace_bytes(dims, num_seqs: int, total_tokens: int) -> int:

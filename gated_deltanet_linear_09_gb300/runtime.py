@@ -94,3 +94,51 @@ class GatedDeltaNetLayer:
     def compact(self, src, dst, stream=None):
         gdn.gdn_state_compact(self.dims, gdn.act_code(self.act), self.pool, list(src), list(dst),
                               stream)
+
+
+class _DeviceView:
+    """A raw device buffer seen through __cuda_array_interface__ (no copy, no ownership)."""
+
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 2}
+
+
+class DecodeGraphs:
+    """Bucketed CUDA-graph decode over a layer (gdn_decode_graphs_*): write rows [0, B) of the
+    static input tensors, call step(B), read rows [0, B) of `out`."""
+
+    def __init__(self, layer: GatedDeltaNetLayer, buckets):
+        self.layer = layer
+        self.handle = gdn.gdn_decode_graphs_create(layer.dims, layer.w, layer.pool, buckets)
+        buf = gdn.gdn_decode_graphs_buffers(self.handle)
+        self.max_batch = buf["max_batch"]
+        geo, mb = layer.geo, buf["max_batch"]
+        ts = "<f2" if layer.act == torch.bfloat16 else "<f4"
+
+        def view(key, shape, typestr, dtype):
+            t = torch.as_tensor(_DeviceView(buf[key], shape, typestr), device=layer.device)
+            return t.view(dtype) if dtype is not None else t
+        act = layer.act if layer.act == torch.bfloat16 else None
+        self.slot_idx = view("slot_idx", (mb,), "<i4", None)
+        self.qkv = view("qkv", (mb, geo.cqkv), ts, act)
+        self.z = view("z", (mb, geo.zdim), ts, act)
+        self.a = view("a", (mb, geo.Hv), ts, act)
+        self.b = view("b", (mb, geo.Hv), ts, act)
+        self.out = view("out", (mb, geo.zdim), ts, act)
+
+    def step(self, B: int, stream=None):
+        gdn.gdn_decode_graphs_launch(self.handle, B, stream)
+        return self.out[:B]
+
+    def close(self):
+        if self.handle:
+            torch.cuda.synchronize()
+            gdn.gdn_decode_graphs_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -149,6 +149,39 @@ int gdn_decode_multi(const gdn_dims* dims, const gdn_weights* w, const gdn_pool*
                      const int32_t* slot_idx, int32_t B, int32_t T, const void* qkv,
                      const void* z, const void* a, const void* b, void* out, cudaStream_t stream);
 
+/* Bucketed CUDA-graph decode (the pages' CUDA-graph-versus-eager decode, "pegainfer issue
+ * #1001", Split 3 bullet): gdn_decode_step captured once per batch bucket over static device
+ * buffers owned by the object, so that a decode step is one padding memset and one graph
+ * launch.  The object keeps the dims, weights and pool given at creation (their device memory
+ * must outlive it).  Not thread-safe; one object per stream of decode steps. */
+#define GDN_MAX_GRAPH_BUCKETS 16
+typedef struct gdn_decode_graphs gdn_decode_graphs;
+
+/* buckets: host int32[n_buckets], strictly increasing, each in [1, 65535]; 1 <= n_buckets <=
+ * GDN_MAX_GRAPH_BUCKETS.  Allocates the static buffers for the largest bucket (slot_idx,
+ * qkv, z, a, b, out in the gdn_decode_step layouts), runs one padding-row decode (touching no
+ * state) and captures one graph per bucket on an internal stream; synchronous.  On success
+ * *out is the new object; on error nothing is left allocated and *out is NULL.  Errors: the
+ * host checks of gdn_decode_step, GDN_ERR_INVALID_ARG for bad buckets, GDN_ERR_TOO_LARGE for a
+ * bucket above 65535, GDN_ERR_CUDA for a failed allocation or capture. */
+int gdn_decode_graphs_create(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
+                             const int32_t* buckets, int32_t n_buckets, gdn_decode_graphs** out);
+
+/* The static device buffers (each may be NULL to skip): the caller writes rows [0, B) of
+ * slot_idx and of the inputs, launches, and reads rows [0, B) of out.  *max_batch = the largest
+ * bucket. */
+int gdn_decode_graphs_buffers(const gdn_decode_graphs* g, int32_t** slot_idx, void** qkv,
+                              void** z, void** a, void** b, void** out, int32_t* max_batch);
+
+/* One decode step of B rows on `stream`: sets slot_idx rows [B, bucket) to -1 (padding) for
+ * the smallest bucket >= B and launches that bucket's graph.  The writes of the buffers must
+ * be ordered before it on `stream`.  B = 0: no-op.  B above the largest bucket:
+ * GDN_ERR_TOO_LARGE, nothing launched. */
+int gdn_decode_graphs_launch(gdn_decode_graphs* g, int32_t B, cudaStream_t stream);
+
+/* Frees the graphs and buffers (after the work launched from them has completed). */
+void gdn_decode_graphs_destroy(gdn_decode_graphs* g);
+
 /* Workspace bytes gdn_prefill_chunked needs for num_seqs sequences of total_tokens tokens
  * (the chunkwise scratch, "GdrChunkwiseScratch35" of "pegainfer PR #1003"). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t num_seqs, int32_t total_tokens);

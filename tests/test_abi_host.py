@@ -99,6 +99,28 @@ def test_decode_multi_host_checks(lib):
     assert call(1, 2, fake=0x10008 + 2) == -7
 
 
+def test_decode_graphs_host_checks(lib):
+    d = D()
+    w = gdn.gdn_weights(0x20000, 0x20000, 0x20000, 0x20000, gdn.GDN_BF16)
+    p = gdn.gdn_pool(0x30000, 0x30000, 4, None)
+    h = ctypes.c_void_p(0x1234)
+
+    def create(buckets, dims=d):
+        arr = (ctypes.c_int32 * max(1, len(buckets)))(*buckets)
+        return lib.gdn_decode_graphs_create(ctypes.byref(dims), ctypes.byref(w), ctypes.byref(p),
+                                            arr, len(buckets), ctypes.byref(h))
+    # all rejected before any allocation or CUDA call, with *out cleared
+    assert create([]) == -1 and h.value is None
+    assert create([4, 2]) == -1
+    assert create([1, 1]) == -1
+    assert create([0, 4]) == -1
+    assert create(list(range(1, gdn.GDN_MAX_GRAPH_BUCKETS + 2))) == -1
+    assert create([1, 70000]) == -9
+    assert create([1, 2], dims=D(Hv=33)) == -3
+    assert lib.gdn_decode_graphs_launch(None, 1, None) == -1
+    lib.gdn_decode_graphs_destroy(None)                # no-op
+
+
 def test_prefill_and_compact_host_checks(lib):
     d = D()
     w = gdn.gdn_weights(0x20000, 0x20000, 0x20000, 0x20000, gdn.GDN_BF16)
