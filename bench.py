@@ -260,7 +260,29 @@ def run_ours(args, ws, rank, local):
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms, e2e_bytes = reduce_over_ranks(dist, e2e_ms, float(state_bytes) * args.steps, "cuda")
     e2e_gbs = e2e_bytes / (e2e_ms * 1e-3) / 1e9
-    del ring, host, dev_in, dev_pack
+
+    # the same step with the kernel reading its inputs from, and writing its output to, the
+    # pinned host buffers directly (zero-copy over the coherent CPU-GPU link): the host<->device
+    # transfers happen inside the kernel's own loads and stores
+    hviews = [{k: host[j][o:o + nb].view(ring[0][k].dtype).view(ring[0][k].shape)
+               for k, o, nb in zip(keys, offs, nbytes)} for j in range(len(host))]
+
+    def zc_step(i):
+        hv = hviews[i % len(hviews)]
+        layer.decode_step(slots, hv["qkv"], hv["z"], hv["a"], hv["b"], host_out)
+
+    for i in range(args.warmup):
+        zc_step(i)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        zc_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    zc_ms = e0.elapsed_time(e1)
+    zc_ms, zc_bytes = reduce_over_ranks(dist, zc_ms, float(state_bytes) * args.steps, "cuda")
+    zc_gbs = zc_bytes / (zc_ms * 1e-3) / 1e9
+    del ring, host, dev_in, dev_pack, hviews
 
     # ---------------- multi-token decode: the same 64 rows, MULTI_T tokens per row per call
     mt_in = []
@@ -365,6 +387,8 @@ def run_ours(args, ws, rank, local):
                      "kernel": "decode_kernel<128,128,bf16>"},
         "e2e": {"value": round(e2e_gbs, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / args.steps, 5)},
+        "e2e_zero_copy": {"value": round(zc_gbs, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                          "d2h_bytes_per_step": d2h, "ms_per_step": round(zc_ms / args.steps, 5)},
         "gpu_launches": args.steps,
         "prefill": {"workload": pwl.name, "tokens_per_s": round(T / (p_ms * 1e-3), 1),
                     "ms": round(p_ms, 4), "contraction_gflop": round(flops / 1e9, 3),

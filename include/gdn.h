@@ -125,6 +125,10 @@ int gdn_conv1d_update(const gdn_dims* dims, const gdn_weights* w, const gdn_pool
  * delta rule on every V-head's state rec_state[s][h], o = S_t^T q, and
  *   out = o / sqrt(mean(o^2) + norm_eps) * norm_weight * SiLU(z)  (one rounding to act).
  * qkv act [B][Cqkv]; z act [B][Hv*dv]; a, b act [B][Hv]; out act [B][Hv*dv].  B <= 65535.
+ * qkv, z, a, b and out may be device memory or pinned host memory (any address the GPU can
+ * reach through unified addressing): the kernel then reads the inputs and writes the output
+ * over the CPU-GPU link itself, with no separate copies.  The state pool stays in device
+ * memory.
  * One kernel launch; no host reads of device data, so the call can be captured in a CUDA
  * graph.  An out-of-range s sets GDN_STATUS_SLOT_RANGE and skips the row. */
 int gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
