@@ -729,7 +729,7 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   uint64_t* b4full = bars + 4;   // B4 landed
   uint64_t* b4empty = bars + 5;  // B4 read by MMA4
   uint64_t* mma3 = bars + 6;
-  uint64_t* mma4 = bars + 7;
+  uint64_t* sready = bars + 7;   // S += K~^T U of the chunk done (the next chunk may read S)
   uint64_t* dfull = bars + 8;    // [NDB] O of the chunk complete in D3[j] (MMA -> epilogue)
   uint64_t* dempty = bars + 12;  // [NDB] D3[j] read by the epilogue (epilogue -> MMA)
   uint64_t* xfull = bars + 16;   // [NXB] partial sums of the 4 slices arrived
@@ -912,6 +912,7 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
           tc::mma_bf16(tb + TC_S, tc::desc_add(dKh, 256 * k), bk, id64, 1);
           tc::mma_bf16(tb + TC_S, tc::desc_add(dKl, 256 * k), bk, id64, 1);
         }
+        tc::mma_commit(sready);   // the next chunk's S conversion overlaps the O products below
         // D3 += [P ; K~^T rows 0..63] U: rows 0..63 become O; rows 64..127 (W S, consumed) are
         // left as scratch
 #pragma unroll
@@ -920,11 +921,13 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
           tc::mma_bf16(d3, tc::desc_add(dPh, 256 * k), bk, id64, 1);
           tc::mma_bf16(d3, tc::desc_add(dPl, 256 * k), bk, id64, 1);
         }
-        tc::mma_commit(mma4);
         tc::mma_commit(b4empty);
         tc::mma_commit(dfull + jd);
       }
-      wait_or_abort(mma4, par, abort, status);
+      // S is final for this chunk.  The O products may still run: they read only B4 and the U
+      // operand (rewritten only after the next chunk's MMA3, which the pipe orders after them)
+      // and write D3[jd], which the next chunk does not touch.
+      wait_or_abort(sready, par, abort, status);
       tc::fence_after_sync();
     }
     // final state slice back to the slot

@@ -285,3 +285,24 @@ def test_decode_step_captured_in_cuda_graph():
         torch.cuda.synchronize()
         np.testing.assert_array_equal(_np(out), eager[t])
     np.testing.assert_array_equal(_np(layer.rec_state), eager_state)
+
+
+def test_decode_with_pinned_host_buffers():
+    """Inputs and output in pinned host memory (read and written by the kernel over the CPU-GPU
+    link) give bit-identical results to device buffers, state included."""
+    geo = synth.Geometry(2, 6, 128, 128, 4, synth.BF16)
+    la, w, rec, conv = _layer(geo, 540, 5, True)
+    lb = GatedDeltaNetLayer(geo, w, 5)
+    lb.load_state(rec, conv)
+    slots = torch.tensor([3, 0, -1, 4], dtype=torch.int32, device="cuda")
+    for t in range(3):
+        xs = synth.make_token_inputs(geo, 4, 541, t)
+        dev = la.inputs(xs)
+        host = {k: v.cpu().pin_memory() for k, v in dev.items()}
+        out_h = torch.empty((4, geo.zdim), dtype=la.act).pin_memory()
+        out_d = la.decode_step(slots, **dev)
+        lb.decode_step(slots, host["qkv"], host["z"], host["a"], host["b"], out_h)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out_h.float().numpy(), _np(out_d))
+    np.testing.assert_array_equal(_np(la.rec_state), _np(lb.rec_state))
+    np.testing.assert_array_equal(_np(la.conv_state), _np(lb.conv_state))
