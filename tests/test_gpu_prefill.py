@@ -137,3 +137,36 @@ def test_prefill_bad_slot_and_bad_seqlens(d):
     assert int(layer.status.item()) & 2
     assert torch.all(sentinel == 7.0)
     np.testing.assert_array_equal(_np(layer.rec_state), rec)
+
+
+def test_prefill_many_short_sequences():
+    """257 sequences of 0..70 tokens (most shorter than one chunk), mixed initial states, on the
+    tensor-core path (d = 128): every output and state against the oracle."""
+    geo = synth.Geometry(2, 4, 128, 128, 4, synth.BF16)
+    rng = np.random.default_rng(640)
+    n = 257
+    lens = [int(x) for x in rng.integers(0, 71, n)]
+    has_init = rng.integers(0, 2, n).astype(np.uint8)
+    N = n + 5
+    w = synth.make_weights(geo, 641)
+    rec, conv = synth.make_pool(geo, N, 642, True)
+    layer = GatedDeltaNetLayer(geo, w, N)
+    layer.load_state(rec, conv)
+    cu = synth.cu_seqlens(lens)
+    slots = rng.permutation(N)[:n].astype(np.int32)
+    xs = synth.make_token_inputs(geo, int(cu[-1]), 643)
+    out = layer.prefill(_dev_i32(cu), _dev_i32(slots), torch.from_numpy(has_init).cuda(),
+                        **layer.inputs(xs))
+    r64, c64 = rec.astype(np.float64), conv.astype(np.float64)
+    rc, ref = oracle.prefill(geo.oracle_dims(), f64(w), r64, c64, cu, slots, has_init, **f64(xs))
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert_out_close(_np(out), ref, geo.act, "prefill outputs")
+    g_rec, g_conv = _np(layer.rec_state), _np(layer.conv_state)
+    for s in slots:
+        assert_state_close(g_rec[s], r64[s], f"slot {s}")
+        np.testing.assert_array_equal(g_conv[s], c64[s])
+    untouched = sorted(set(range(N)) - set(slots.tolist()))
+    for s in untouched:
+        np.testing.assert_array_equal(g_rec[s], rec[s])
+    assert int(layer.status.item()) == 0
