@@ -15,7 +15,10 @@ namespace gdn {
 namespace {
 
 constexpr int kCompactThreads = 256;
-constexpr int kUnitsPerThread = 16;                       // 16-byte units held in registers
+// 16-byte units held in registers per thread.  8 (a 32 KiB column tile per CTA over all pairs)
+// moves the 56-pair compaction of the B=64 workload at the rate of a plain contiguous copy of
+// the same bytes; 16 units per thread (fewer CTAs per SM) was ~16 % slower.
+constexpr int kUnitsPerThread = 8;
 constexpr int kUnitsPerCta = kCompactThreads * kUnitsPerThread;
 
 __global__ void __launch_bounds__(kCompactThreads)
