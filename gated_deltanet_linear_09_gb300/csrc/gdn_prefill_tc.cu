@@ -9,7 +9,7 @@
 //   intra kernel (chunk x V-head, all in parallel, two CTAs per SM):
 //     conv + SiLU + l2norm + gates of the chunk's 64 tokens,
 //     D1 = [K;Q] K^T                     -> A = beta_i e^{g_i-g_j} KK^T (j<i),  P = QK^T o Gamma
-//     T  = (I + A)^{-1}                  (forward substitution, CUDA cores)
+//     T  = (I + A)^{-1}                  (16 x 16 blocks: diagonal inverses, then block rows)
 //     D2 = (beta e^gamma K)^T T^T, (beta V)^T T^T   -> W^T, U~^T
 //     writes [Q~ ; W] and [P ; K~^T] as split-bf16 operand images (Q~ = e^gamma Q,
 //     K~ = e^{gamma_L - gamma} K), U~ (f32) and e^{gamma_L}

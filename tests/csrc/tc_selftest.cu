@@ -7,6 +7,28 @@
 
 using namespace gdn::tc;
 
+// Two primitives the library does not use, kept here to measure them: a shared -> TMEM operand
+// copy and an MMA reading its A operand from TMEM (with the A operand in TMEM the per-MMA cost
+// at small N did not drop, so the prefill kernels keep both operands in shared memory).
+// D[tmem] (+)= A[tmem] * B[smem]^T -- A (M = 128 rows on TMEM lanes 0-127, 16 bf16 of K packed
+// in 8 columns per K-step) was put there by tmem_cp_128x256b.  Issued by one thread.
+static __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Asynchronous shared -> TMEM copy of one 128-row x 32-byte block (one K-step of a 128-row bf16
+// operand in the K-major core-matrix layout the descriptor describes) to lanes 0-127, 8 columns
+// from taddr.  Ordered with the MMAs the same thread issues afterwards; tracked by mma_commit.
+static __device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;\n" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+
 // B's K-direction core matrices are b_lbo bytes apart (128: the dense layout).
 __global__ void tc_gemm_kernel(const float* __restrict__ A, const float* __restrict__ B,
                                float* __restrict__ D, int N, int K, int passes, uint32_t ncols,

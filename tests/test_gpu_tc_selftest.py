@@ -1,6 +1,8 @@
-"""The tcgen05 / TMEM / shared-memory-descriptor primitives the prefill uses, checked in
-isolation: a 128 x N x K GEMM with bf16 operands (one pass) and with split-bf16 operands
-(hi*hi + hi*lo + lo*hi, three passes) against float64 products on the CPU."""
+"""The tcgen05 / TMEM / shared-memory-descriptor / cluster primitives the prefill kernels use,
+checked in isolation: a 128 x N x K GEMM with bf16 operands (one pass) and with split-bf16
+operands (hi*hi + hi*lo + lo*hi, three passes) against float64 products on the CPU, with dense
+and padded (144-byte) B layouts and with the A operand copied into TMEM; the st.async exchange
+among the CTAs of a cluster; and a bounded mbarrier wait that gives up."""
 import ctypes
 import os
 import subprocess
