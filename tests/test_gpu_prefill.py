@@ -170,3 +170,35 @@ def test_prefill_many_short_sequences():
     for s in untouched:
         np.testing.assert_array_equal(g_rec[s], rec[s])
     assert int(layer.status.item()) == 0
+
+
+def test_prefill_long_sequence_state_accuracy():
+    """One 16384-token sequence (256 dependent chunk steps of the split-bf16 tensor-core chain)
+    at the full head count, continuing from a pre-filled slot: outputs and the final state of
+    two K-heads (with their V-heads) against the oracle."""
+    wl = synth.workloads()[3]
+    geo = wl.geo
+    T = 16384
+    w = synth.make_weights(geo, 660)
+    rec, conv = synth.make_pool(geo, 2, 662, True)
+    layer = GatedDeltaNetLayer(geo, w, 2)
+    layer.load_state(rec, conv)
+    xs = synth.make_token_inputs(geo, T, 661)
+    cu = np.array([0, T], np.int32)
+    slots = np.array([1], np.int32)
+    has_init = np.array([1], np.uint8)
+    out = layer.prefill(_dev_i32(cu), _dev_i32(slots), torch.from_numpy(has_init).cuda(),
+                        **layer.inputs(xs))
+    torch.cuda.synchronize()
+    got = _np(out)
+    g_rec, g_conv = _np(layer.rec_state), _np(layer.conv_state)
+    for k_heads in ([5], [12]):
+        hs = HeadSlice(geo, k_heads)
+        r64 = hs.rec(rec).astype(np.float64)
+        c64 = hs.conv(conv).astype(np.float64)
+        rc, ref = oracle.prefill(hs.sub.oracle_dims(), hs.weights(w), r64, c64, cu, slots,
+                                 has_init, **hs.inputs(xs))
+        assert rc == 0
+        assert_out_close(hs.out_cols(got), ref, geo.act, f"heads {k_heads}")
+        assert_state_close(hs.rec(g_rec)[1], r64[1], f"final state heads {k_heads}")
+        np.testing.assert_array_equal(hs.conv(g_conv)[1], c64[1])
