@@ -416,7 +416,7 @@ def run_ours(args, ws, rank, local):
                     "hbm_frac": round(comp_bytes / (comp_ms * 1e-3) / 1e9 / hbm_peak, 4)},
         "clocks": clocks,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and ws == 1:   # the oracle baseline: rank 0 at N = 1 only
         line["cpu_baseline"] = cpu_baseline(args)
     print(json.dumps(line), flush=True)
     if dist:

@@ -49,7 +49,9 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
     extra = ["-Xptxas", "-v"] if ptxas_v else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        # per-process object names: concurrent builders (one per rank) never share a file, and the
+        # library appears by an atomic rename
+        obj = os.path.join(BUILD, f"{os.path.basename(src)[:-3]}.{os.getpid()}.o")
         cmd = [cc] + flags(extra) + ["-c", src, "-o", obj]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
@@ -65,6 +67,11 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [cc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
     res = subprocess.run(cmd, capture_output=True, text=True)
+    for o, _ in results:
+        try:
+            os.remove(o)
+        except OSError:
+            pass
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stderr}")
     os.replace(tmp, LIB)
