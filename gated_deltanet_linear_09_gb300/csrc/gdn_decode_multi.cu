@@ -69,9 +69,11 @@ template <> struct SmVec<2> {
   }
 };
 
-template <int DK, int DV, typename T>
+// NT > 0: the token count is the compile-time NT (tight code for that T); NT = 0: the runtime
+// count tt, with the loops unrolled to GDN_MAX_DECODE_TOKENS and guarded.
+template <int DK, int DV, typename T, int NT>
 __global__ void __launch_bounds__(kMT, 2)
-decode_multi_kernel(KDims d, int TT, const float* __restrict__ A_log,
+decode_multi_kernel(KDims d, int tt, const float* __restrict__ A_log,
                     const float* __restrict__ dt_bias, const T* __restrict__ conv_w,
                     const T* __restrict__ norm_w, float* __restrict__ rec,
                     T* __restrict__ conv_state, int num_slots, int32_t* __restrict__ status,
@@ -81,7 +83,8 @@ decode_multi_kernel(KDims d, int TT, const float* __restrict__ A_log,
   constexpr int NW = kMW;
   constexpr int CPT = DV / 32;   // state columns per lane
   constexpr int RPW = DK / NW;   // state rows per warp
-  constexpr int MT = GDN_MAX_DECODE_TOKENS;
+  constexpr int MT = NT > 0 ? NT : GDN_MAX_DECODE_TOKENS;
+  const int TT = NT > 0 ? NT : tt;
   extern __shared__ __align__(16) float smem[];
   const int kh = blockIdx.x, row = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -341,14 +344,14 @@ decode_multi_kernel(KDims d, int TT, const float* __restrict__ A_log,
   }
 }
 
-template <int DK, int DV, typename T>
+template <int DK, int DV, typename T, int NT>
 int launch_multi_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
                    const int32_t* slot_idx, int B, int TT, const void* qkv, const void* z,
                    const void* a, const void* b, void* out, cudaStream_t stream) {
   const int nch = 2 * DK + d.r * DV;
   const size_t smem = sizeof(float) * ((size_t)TT * nch + (size_t)(kMW + 1) * 2 * TT * DV +
                                        2 * TT * TT + (size_t)d.r * (4 * TT + 2 * TT * TT));
-  auto kern = decode_multi_kernel<DK, DV, T>;
+  auto kern = decode_multi_kernel<DK, DV, T, NT>;
   // raised once per kernel to the per-block maximum, so that captured launches never change it
   static std::once_flag once;
   static int attr_rc = 0;
@@ -374,14 +377,24 @@ template <typename T>
 int launch_multi_dims(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
                       const int32_t* slot_idx, int B, int TT, const void* qkv, const void* z,
                       const void* a, const void* b, void* out, cudaStream_t stream) {
-  if (d.dk == 128 && d.dv == 128)
-    return launch_multi_t<128, 128, T>(d, w, pool, slot_idx, B, TT, qkv, z, a, b, out, stream);
+  if (d.dk == 128 && d.dv == 128) {
+    // the main head size: one instance per token count
+    switch (TT) {
+#define GDN_MULTI_CASE(n) \
+  case n: return launch_multi_t<128, 128, T, n>(d, w, pool, slot_idx, B, TT, qkv, z, a, b, out, stream);
+      GDN_MULTI_CASE(1) GDN_MULTI_CASE(2) GDN_MULTI_CASE(3) GDN_MULTI_CASE(4)
+      GDN_MULTI_CASE(5) GDN_MULTI_CASE(6) GDN_MULTI_CASE(7) GDN_MULTI_CASE(8)
+#undef GDN_MULTI_CASE
+      default: break;
+    }
+    return launch_multi_t<128, 128, T, 0>(d, w, pool, slot_idx, B, TT, qkv, z, a, b, out, stream);
+  }
   if (d.dk == 64 && d.dv == 64)
-    return launch_multi_t<64, 64, T>(d, w, pool, slot_idx, B, TT, qkv, z, a, b, out, stream);
+    return launch_multi_t<64, 64, T, 0>(d, w, pool, slot_idx, B, TT, qkv, z, a, b, out, stream);
   if (d.dk == 128 && d.dv == 64)
-    return launch_multi_t<128, 64, T>(d, w, pool, slot_idx, B, TT, qkv, z, a, b, out, stream);
+    return launch_multi_t<128, 64, T, 0>(d, w, pool, slot_idx, B, TT, qkv, z, a, b, out, stream);
   if (d.dk == 64 && d.dv == 128)
-    return launch_multi_t<64, 128, T>(d, w, pool, slot_idx, B, TT, qkv, z, a, b, out, stream);
+    return launch_multi_t<64, 128, T, 0>(d, w, pool, slot_idx, B, TT, qkv, z, a, b, out, stream);
   return GDN_ERR_UNSUPPORTED_SHAPE;
 }
 
