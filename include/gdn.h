@@ -24,7 +24,9 @@
  *
  * Conventions shared by every call
  *   Ownership: the caller owns every buffer.  The library allocates and frees no memory,
- *     never synchronises the device and launches only on the given stream.
+ *     never synchronises the device and launches only on the given stream -- except the
+ *     CUDA-graph decode object: gdn_decode_graphs_create allocates its static buffers and
+ *     captures on an internal stream (synchronously), gdn_decode_graphs_destroy frees them.
  *   Pointers: device pointers unless marked "host"; base addresses 16-byte aligned; all
  *     tensors dense, row-major, in the layouts below.
  *   Layouts (Cqkv = 2*Hk*dk + Hv*dv, r = Hv/Hk):

@@ -164,3 +164,31 @@ def test_product_path_has_no_oracle_or_fallback():
                 src = open(os.path.join(dirpath, fn)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, flags=re.M), fn
                 assert "liboracle" not in src and "gdn_oracle" not in src, fn
+
+
+def test_header_is_c_and_links(lib, tmp_path):
+    """A C99 program compiled against include/gdn.h (gcc, not nvcc) links with libgdn.so and
+    runs the host-side entry points."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    cuda_inc = None
+    for cand in ("/usr/local/cuda/include", "/usr/local/cuda/targets/x86_64-linux/include",
+                 "/usr/local/cuda/targets/sbsa-linux/include"):
+        if os.path.exists(os.path.join(cand, "cuda_runtime_api.h")):
+            cuda_inc = cand
+            break
+    if cuda_inc is None:
+        pytest.skip("CUDA headers not found")
+    libpath = gdn.lib_path()
+    exe = tmp_path / "abi_c_check"
+    src = os.path.join(ROOT, "tests", "csrc", "abi_c_check.c")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-I", cuda_inc, src, "-o", str(exe), libpath,
+                    "-Wl,-rpath," + os.path.dirname(libpath)], check=True)
+    env = dict(os.environ)
+    res = subprocess.run([str(exe)], capture_output=True, text=True, env=env)
+    assert res.returncode == 0, (res.returncode, res.stdout, res.stderr)
+    assert res.stdout.startswith("ok")
