@@ -160,6 +160,11 @@ def run_ours(args, ws, rank, local):
         if rank == 0:
             print(json.dumps({"only": "prefill", "ms": p_ms, "tokens_per_s": T / (p_ms * 1e-3)}))
         return
+    if args.only == "proj":
+        pr = time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak, args.steps)
+        if rank == 0:
+            print(json.dumps({"only": "proj", **pr}))
+        return
     # ---------------- decode, B = 64
     wl = synth.workloads()[DECODE_WL]
     geo = wl.geo
@@ -358,6 +363,9 @@ def run_ours(args, ws, rank, local):
     del layer
     torch.cuda.empty_cache()
 
+    # ---------------- the projections around the step
+    proj = time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak)
+
     # ---------------- chunked prefill, one sequence of T = 4096
     p_ms, T = time_prefill(torch, synth, GatedDeltaNetLayer, 10, 3)
     pwl = synth.workloads()[PREFILL_WL]
@@ -411,6 +419,7 @@ def run_ours(args, ws, rank, local):
                          "state_bytes_per_token": state_bytes // (wl.batch * MULTI_T),
                          "single_step_tokens_per_s": round(wl.batch / (ms_step * 1e-3), 1)},
         "decode_graphs": dict(graph_us, buckets=[1, 2, 4, 8, 16, 32, 64]),
+        "proj": proj,
         "compact": {"pairs": len(keep), "bytes": comp_bytes, "ms": round(comp_ms, 4),
                     "gbs": round(comp_bytes / (comp_ms * 1e-3) / 1e9, 1),
                     "hbm_frac": round(comp_bytes / (comp_ms * 1e-3) / 1e9 / hbm_peak, 4)},
@@ -421,6 +430,91 @@ def run_ours(args, ws, rank, local):
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak, reps=20):
+    """The projections around the step.  Decode-shaped: in_proj and out_proj of the 64 rows of
+    the B=64 workload (hidden 5120), weight-streaming bound, reported as GB/s of algorithmic
+    bytes (weights + activations + outputs) against the HBM peak; each launch reads weights
+    the previous launches did not touch (copies rotated, > 2 x L2 per rotation).
+    Prefill-shaped: in_proj of the T = 4096 sequence (hidden 4096), tensor bound, TFLOP/s
+    against the bf16 peak."""
+    stream = torch.cuda.current_stream()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(77)
+    res = {}
+
+    def randn(shape, scale):
+        return (torch.randn(shape, device="cuda", generator=gen) * scale).to(torch.bfloat16)
+
+    def timed(fn, n):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    wl = synth.workloads()[DECODE_WL]
+    geo = wl.geo
+    H = synth.PROJ_HIDDEN[geo.Hv]
+    layer = GatedDeltaNetLayer(geo, synth.make_weights(geo, wl.seed), 1)
+    B = wl.batch
+    n_in, n_out = synth.proj_rows(geo), H
+    l2 = 129e6
+    r_in = max(2, int(2 * l2 // (n_in * H * 2)) + 1)
+    r_out = max(2, int(2 * l2 // (n_out * geo.zdim * 2)) + 1)
+    w_in = [randn((n_in, H), H ** -0.5) for _ in range(r_in)]
+    w_out = [randn((n_out, geo.zdim), geo.zdim ** -0.5) for _ in range(r_out)]
+    x = randn((B, H), 1.0)
+    o = randn((B, geo.zdim), 1.0)
+    t = {"qkv": torch.empty((B, geo.cqkv), dtype=torch.bfloat16, device="cuda"),
+         "z": torch.empty((B, geo.zdim), dtype=torch.bfloat16, device="cuda"),
+         "a": torch.empty((B, geo.Hv), dtype=torch.bfloat16, device="cuda"),
+         "b": torch.empty((B, geo.Hv), dtype=torch.bfloat16, device="cuda")}
+    y = torch.empty((B, H), dtype=torch.bfloat16, device="cuda")
+    ms_in = timed(lambda i: gdn.gdn_in_proj(layer.dims, x, w_in[i % r_in], t["qkv"], t["z"],
+                                            t["b"], t["a"], layer.status), reps)
+    ms_out = timed(lambda i: gdn.gdn_out_proj(layer.dims, o, w_out[i % r_out], y, layer.status),
+                   reps)
+    b_in = n_in * H * 2 + B * H * 2 + B * n_in * 2
+    b_out = n_out * geo.zdim * 2 + B * geo.zdim * 2 + B * H * 2
+    for name, ms, nbytes, n, k in (("in_proj", ms_in, b_in, n_in, H),
+                                   ("out_proj", ms_out, b_out, n_out, geo.zdim)):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[f"decode_{name}"] = {
+            "rows": B, "features": n, "hidden" if name == "in_proj" else "k": k,
+            "us": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / hbm_peak, 4),
+            "tflops": round(2.0 * B * n * k / (ms * 1e-3) / 1e12, 2)}
+    del w_in, w_out, layer
+    torch.cuda.empty_cache()
+
+    pwl = synth.workloads()[PREFILL_WL]
+    pgeo = pwl.geo
+    PH = synth.PROJ_HIDDEN[pgeo.Hv]
+    T = pwl.seq_lens[0]
+    player = GatedDeltaNetLayer(pgeo, synth.make_weights(pgeo, pwl.seed), 1)
+    pn = synth.proj_rows(pgeo)
+    pw = randn((pn, PH), PH ** -0.5)
+    px = randn((T, PH), 1.0)
+    pt = {"qkv": torch.empty((T, pgeo.cqkv), dtype=torch.bfloat16, device="cuda"),
+          "z": torch.empty((T, pgeo.zdim), dtype=torch.bfloat16, device="cuda"),
+          "a": torch.empty((T, pgeo.Hv), dtype=torch.bfloat16, device="cuda"),
+          "b": torch.empty((T, pgeo.Hv), dtype=torch.bfloat16, device="cuda")}
+    ms_p = timed(lambda i: gdn.gdn_in_proj(player.dims, px, pw, pt["qkv"], pt["z"], pt["b"],
+                                           pt["a"], player.status), max(5, reps // 4))
+    fl = 2.0 * T * pn * PH
+    tf = fl / (ms_p * 1e-3) / 1e12
+    res["prefill_in_proj"] = {"rows": T, "features": pn, "hidden": PH, "us": round(ms_p * 1e3, 2),
+                              "tflops": round(tf, 1), "bf16_frac": round(tf / bf16_peak, 4)}
+    res["hidden_sizes"] = {str(k): v for k, v in synth.PROJ_HIDDEN.items()}
+    res["kernel"] = "proj_kernel (tcgen05 128x64 tiles, cp.async ring, cluster split-K)"
+    return res
 
 
 def time_prefill(torch, synth, GatedDeltaNetLayer, reps, warmup):
@@ -566,7 +660,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill"],
+    ap.add_argument("--only", default="all", choices=["all", "decode", "prefill", "proj"],
                     help="decode: only the B=64 decode timing (used for profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:

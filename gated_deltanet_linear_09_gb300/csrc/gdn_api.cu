@@ -179,6 +179,76 @@ int gdn_state_compact(const gdn_dims* dims, gdn_dtype act, const gdn_pool* pool,
                              stream);
 }
 
+int gdn_linear_bf16(const void* x, const void* w, int32_t M, int32_t N, int32_t K,
+                    const gdn_proj_route* route, int32_t k_split, int32_t* status,
+                    cudaStream_t stream) {
+  if (M < 0 || N < 1 || K < 1) return GDN_ERR_INVALID_ARG;
+  if (K % 64 != 0) return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (M > 65535 * 64) return GDN_ERR_TOO_LARGE;
+  if (M == 0) return GDN_OK;   // empty batch: nothing read or written (x may be NULL)
+  if (!x || !w || !route) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w)) return GDN_ERR_MISALIGNED;
+  const gdn_proj_route& r = *route;
+  if (r.nseg < 1 || r.nseg > GDN_MAX_PROJ_SEGMENTS || r.start[0] != 0) return GDN_ERR_INVALID_ARG;
+  gdn::ProjRoute pr = {};
+  pr.nseg = r.nseg;
+  for (int s = 0; s < r.nseg; ++s) {
+    const int end = s + 1 < r.nseg ? r.start[s + 1] : N;
+    if (r.start[s] >= end || end > N || !r.dst[s] || r.ld[s] < end - r.start[s])
+      return GDN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(r.dst[s]) & 1u) != 0) return GDN_ERR_MISALIGNED;
+    pr.start[s] = r.start[s];
+    pr.ld[s] = r.ld[s];
+    pr.ptr[s] = static_cast<__nv_bfloat16*>(r.dst[s]);
+  }
+  const int nk = K / 64;
+  if (k_split != 0 && k_split != 1 && k_split != 2 && k_split != 4 && k_split != 8)
+    return GDN_ERR_INVALID_ARG;
+  if (k_split != 0 && nk % k_split != 0) return GDN_ERR_INVALID_ARG;
+  const int ks = k_split != 0 ? k_split : gdn::proj_auto_split(M, N, K);
+  return gdn::launch_proj(x, w, M, N, K, ks, pr, status, stream);
+}
+
+int gdn_in_proj(const gdn_dims* dims, const void* hidden, const void* w_in, int32_t rows,
+                int32_t hidden_size, void* qkv, void* z, void* b, void* a, int32_t* status,
+                cudaStream_t stream) {
+  gdn::KDims d;
+  int rc;
+  if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
+  if (!qkv || !z || !b || !a || hidden_size < 1) return GDN_ERR_INVALID_ARG;
+  const long long zdim = (long long)d.Hv * d.dv;
+  const long long n = d.cqkv + zdim + 2LL * d.Hv;
+  if (n > (1LL << 30)) return GDN_ERR_TOO_LARGE;
+  gdn_proj_route r = {};
+  r.nseg = 4;
+  r.start[0] = 0;
+  r.start[1] = d.cqkv;
+  r.start[2] = (int32_t)(d.cqkv + zdim);
+  r.start[3] = (int32_t)(d.cqkv + zdim + d.Hv);
+  r.ld[0] = d.cqkv;
+  r.ld[1] = (int32_t)zdim;
+  r.ld[2] = d.Hv;
+  r.ld[3] = d.Hv;
+  r.dst[0] = qkv;
+  r.dst[1] = z;
+  r.dst[2] = b;
+  r.dst[3] = a;
+  return gdn_linear_bf16(hidden, w_in, rows, (int32_t)n, hidden_size, &r, 0, status, stream);
+}
+
+int gdn_out_proj(const gdn_dims* dims, const void* out, const void* w_out, int32_t rows,
+                 int32_t hidden_size, void* y, int32_t* status, cudaStream_t stream) {
+  gdn::KDims d;
+  int rc;
+  if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
+  if (!y || hidden_size < 1) return GDN_ERR_INVALID_ARG;
+  gdn_proj_route r = {};
+  r.nseg = 1;
+  r.ld[0] = hidden_size;
+  r.dst[0] = y;
+  return gdn_linear_bf16(out, w_out, rows, hidden_size, d.Hv * d.dv, &r, 0, status, stream);
+}
+
 const char* gdn_status_string(int code) {
   switch (code) {
     case GDN_OK: return "ok";

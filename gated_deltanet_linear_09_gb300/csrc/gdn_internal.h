@@ -50,4 +50,18 @@ int launch_prefill_tc(const KDims& d, const gdn_weights* w, const gdn_pool* pool
                       int num_seqs, int total_tokens, const void* qkv, const void* z, const void* a,
                       const void* b, void* out, void* ws, cudaStream_t stream);
 
+// Dense bf16 projection (tcgen05 GEMM) with a routing epilogue: output feature n of row m goes
+// to ptr[s][m * ld[s] + n - start[s]] for the segment s holding n.
+struct ProjRoute {
+  int nseg;
+  int start[GDN_MAX_PROJ_SEGMENTS];
+  int ld[GDN_MAX_PROJ_SEGMENTS];
+  __nv_bfloat16* ptr[GDN_MAX_PROJ_SEGMENTS];
+};
+
+// Contraction split the library picks for an M x N x K projection (1, 2, 4 or 8).
+int proj_auto_split(int M, int N, int K);
+int launch_proj(const void* x, const void* w, int M, int N, int K, int ks, const ProjRoute& route,
+                int32_t* status, cudaStream_t stream);
+
 }  // namespace gdn

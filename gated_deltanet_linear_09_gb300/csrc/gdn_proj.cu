@@ -1,0 +1,245 @@
+// gdn_proj.cu -- the dense projections on either side of the GDN step as one bf16 tcgen05 GEMM
+// kernel: the input projection of the hidden states into the step's [q | k | v], z, b and a
+// inputs, and the output projection of the gated-normed output back to the hidden size (the
+// in_proj_qkv / in_proj_z / in_proj_b / in_proj_a and out_proj weights of "pegainfer PR #1003",
+// description bullets, and of "helexa/cortex commit 95dc874 (tp_qwen3_5)",
+// TpQwen3_5GatedDeltaNet bullet).
+//
+//   y[m][n] = bf16( sum_k x[m][k] w[n][k] ),   x [M][K] activations, w [N][K] weights.
+//
+// At decode batch sizes the weights are nearly all of the bytes, so the kernel is laid out for
+// streaming them: a CTA owns 128 output features (the MMA's M = 128 operand is the weight tile)
+// and 64 activation rows (N = 64), and walks the contraction in 64-wide chunks through a ring
+// of shared-memory stages filled with cp.async.  The f32 accumulator lives in TMEM (lane =
+// output feature, column = activation row).  When there are too few tiles to cover the SMs,
+// the contraction is split over the CTAs of a thread-block cluster (grid z); each CTA parks its
+// partial tile in its own shared memory and every CTA of the cluster adds up one slice of the
+// columns over distributed shared memory, in a fixed order.  The epilogue routes each output
+// feature to one of up to four destination tensors, which is how the input projection writes
+// the step's four input buffers in one launch.
+#include <mutex>
+
+#include "gdn_internal.h"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int PM = 128;         // output features per CTA (MMA M, TMEM lanes)
+constexpr int PN = 64;          // activation rows per CTA (MMA N, TMEM columns)
+constexpr int PK = 64;          // contraction elements per stage
+constexpr int PSTAGES = 4;      // ring depth; 96 KiB of stages lets two CTAs share an SM
+constexpr int PTHREADS = 256;
+constexpr uint32_t PA_BYTES = PM * PK * 2;   // weight tile, 16 KiB
+constexpr uint32_t PB_BYTES = PN * PK * 2;   // activation tile, 8 KiB
+constexpr uint32_t PSTAGE_BYTES = PA_BYTES + PB_BYTES;
+constexpr uint32_t PRED_BYTES = PM * PN * 4;  // f32 partial tile [PN][PM], aliases the stages
+constexpr uint32_t PBAR_OFF = PSTAGES * PSTAGE_BYTES;
+constexpr uint32_t PSMEM = PBAR_OFF + PSTAGES * 8 + 16;
+constexpr int PCOPIES = (PM + PN) * (PK / 8) / PTHREADS;   // 16-byte copies per thread per stage
+constexpr int PW_COPIES = PM * (PK / 8) / PTHREADS;        // ... of which weight rows
+static_assert(PRED_BYTES <= PBAR_OFF, "partial tile must fit in the stage ring");
+static_assert(PCOPIES * PTHREADS == (PM + PN) * (PK / 8) && PW_COPIES * PTHREADS == PM * (PK / 8),
+              "copies must divide evenly over the threads");
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(g),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// One stage: the weight tile (PM rows) and the activation tile (PN rows), PK wide, in the
+// K-major no-swizzle core-matrix layout.  Copy u covers row 8*(u/64) + u%8, elements
+// 8*((u/8)%8) .. +8, which is byte u*16 of the tile: consecutive threads fill consecutive 16-byte
+// slots (no shared-memory bank conflicts) while each 8-thread group reads 8 rows' 16-byte
+// pieces.  Rows past the end of w or x are zero-filled (source size 0, address kept in range).
+__device__ __forceinline__ void load_stage(uint32_t sa, const __nv_bfloat16* __restrict__ W,
+                                           const __nv_bfloat16* __restrict__ X, int N, int M,
+                                           int K, int n0, int m0, int k0) {
+#pragma unroll
+  for (int i = 0; i < PCOPIES; ++i) {
+    const int u = (int)threadIdx.x + i * PTHREADS;
+    const int kg = (u >> 3) & 7;
+    if (i < PW_COPIES) {
+      const int n = n0 + (((u >> 6) << 3) | (u & 7));
+      const __nv_bfloat16* src = W + (size_t)min(n, N - 1) * K + k0 + 8 * kg;
+      cp_async16(sa + (uint32_t)u * 16u, src, n < N ? 16u : 0u);
+    } else {
+      const int v = u - PM * (PK / 8);
+      const int m = m0 + (((v >> 6) << 3) | (v & 7));
+      const __nv_bfloat16* src = X + (size_t)min(m, M - 1) * K + k0 + 8 * kg;
+      cp_async16(sa + PA_BYTES + (uint32_t)v * 16u, src, m < M ? 16u : 0u);
+    }
+  }
+}
+
+// Grid (ceil(N/PM), ceil(M/PN), ks), cluster (1, 1, ks): CTA z of a cluster takes contraction
+// chunks [z*nkc, (z+1)*nkc) and adds up columns [z*PN/ks, (z+1)*PN/ks) of the cluster's tile.
+__global__ void __launch_bounds__(PTHREADS, 2)
+proj_kernel(const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ W, int M,
+            int N, int K, int nkc, const ProjRoute route, int32_t* __restrict__ status) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PBAR_OFF);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + PSTAGES);
+  const int n0 = blockIdx.x * PM, m0 = blockIdx.y * PN;
+  const int ks = (int)gridDim.z, z = (int)blockIdx.z;
+  const int kbase = z * nkc * PK;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t s0 = tc::smem_u32(sm);
+  if (tid == 0) {
+    for (int i = 0; i < PSTAGES; ++i) tc::mbar_init(bars + i, 1);
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) tc::tmem_alloc(tslot, PN);
+  // the first PSTAGES - 1 chunks in flight, one commit group each (empty groups included, so
+  // that the group count stays in step with the chunk index)
+#pragma unroll
+  for (int j = 0; j < PSTAGES - 1; ++j) {
+    if (j < nkc) load_stage(s0 + j * PSTAGE_BYTES, W, X, N, M, K, n0, m0, kbase + j * PK);
+    cp_async_commit();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tb = *tslot;
+  constexpr uint32_t kIdesc = tc::idesc_bf16(PM, PN);
+  bool ok = true;
+  for (int kc = 0; kc < nkc; ++kc) {
+    const int st = kc % PSTAGES;
+    cp_async_wait<PSTAGES - 2>();   // this thread's copies of chunk kc have landed ...
+    tc::fence_proxy_async_smem();   // ... and are visible to the tensor core
+    __syncthreads();
+    if (tid == 0 && ok) {
+      tc::fence_after_sync();
+      const uint32_t sa = s0 + st * PSTAGE_BYTES;
+      const uint64_t da = tc::kstep_desc(sa, PK, 0), db = tc::kstep_desc(sa + PA_BYTES, PK, 0);
+#pragma unroll
+      for (int k = 0; k < PK / 16; ++k)
+        tc::mma_bf16(tb, tc::desc_add(da, 256u * k), tc::desc_add(db, 256u * k), kIdesc,
+                     (kc > 0 || k > 0) ? 1u : 0u);
+      tc::mma_commit(bars + st);
+    }
+    // refill the stage of chunk kc - 1 with chunk kc + PSTAGES - 1 once its MMAs are done
+    const int nxt = kc + PSTAGES - 1;
+    if (nxt < nkc) {
+      if (kc > 0 && ok && !tc::mbar_wait(bars + (kc - 1) % PSTAGES, ((kc - 1) / PSTAGES) & 1))
+        ok = false;
+      if (ok) load_stage(s0 + (nxt % PSTAGES) * PSTAGE_BYTES, W, X, N, M, K, n0, m0, kbase + nxt * PK);
+    }
+    cp_async_commit();
+  }
+  // the last chunk's commit covers every MMA issued before it
+  if (ok && !tc::mbar_wait(bars + (nkc - 1) % PSTAGES, ((nkc - 1) / PSTAGES) & 1)) ok = false;
+  cp_async_wait<0>();
+  ok = __syncthreads_and(ok) != 0;
+  if (!ok && tid == 0 && status) atomicOr(status, GDN_STATUS_TIMEOUT);
+  tc::fence_after_sync();
+  // the partial tile, [column][lane] f32, into this CTA's stage ring (free now): warp w holds
+  // TMEM lanes 32*(w%4).. and columns 32*(w/4)..
+  float* red = reinterpret_cast<float*>(sm);
+  if (ok) {
+    const int lq = (warp & 3) * 32, c0 = (warp >> 2) * 32;
+    float v[32];
+    tc::tmem_ld16(tc::taddr(tb, lq, c0), v);
+    tc::tmem_ld16(tc::taddr(tb, lq, c0 + 16), v + 16);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) red[(c0 + i) * PM + lq + lane] = v[i];
+  }
+  tc::fence_before_sync();
+  tc::cluster_sync_all();   // every partial tile of the cluster is written and visible
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tb, PN);
+  // this CTA's column slice: thread -> lane r = tid % 128, columns cw0 + tid/128 + 2j
+  const int r = tid & (PM - 1);
+  const int n = n0 + r;
+  const int cw = PN / ks, cw0 = z * cw;
+  __nv_bfloat16* base = route.ptr[0];
+  int seg_start = 0, seg_ld = route.ld[0];
+#pragma unroll
+  for (int q = 1; q < GDN_MAX_PROJ_SEGMENTS; ++q)
+    if (q < route.nseg && n >= route.start[q]) {
+      base = route.ptr[q];
+      seg_start = route.start[q];
+      seg_ld = route.ld[q];
+    }
+  __nv_bfloat16* dst = base + (n - seg_start);
+  const size_t ld = (size_t)seg_ld;
+  const uint32_t red_s = tc::smem_u32(red);
+  for (int c = cw0 + (tid >> 7); c < cw0 + cw; c += PTHREADS / PM) {
+    const int m = m0 + c;
+    if (m >= M || n >= N) continue;
+    const uint32_t off = red_s + (uint32_t)(c * PM + r) * 4u;
+    float s = 0.f;
+    for (int q = 0; q < ks; ++q) s += ld_cluster_f32(tc::mapa_shared(off, (uint32_t)q));
+    dst[(size_t)m * ld] = __float2bfloat16_rn(s);
+  }
+  tc::cluster_sync_all();   // no CTA leaves while another still reads its shared memory
+}
+
+int g_num_sms = 0;
+
+}  // namespace
+
+int proj_auto_split(int M, int N, int K) {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      g_num_sms = sms;
+    else
+      g_num_sms = 152;
+  });
+  // two CTAs fit on an SM; split the contraction while the CTAs still fit in one wave and
+  // every CTA keeps at least a full ring of chunks
+  const long long tiles = (long long)((N + PM - 1) / PM) * ((M + PN - 1) / PN);
+  const int nk = K / PK;
+  int ks = 1;
+  for (int c = 2; c <= 8; c *= 2)
+    if (tiles * c <= 2LL * g_num_sms && nk % c == 0 && nk / c >= PSTAGES) ks = c;
+  return ks;
+}
+
+int launch_proj(const void* x, const void* w, int M, int N, int K, int ks, const ProjRoute& route,
+                int32_t* status, cudaStream_t stream) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)PSMEM);
+  });
+  if (attr_err != cudaSuccess) return GDN_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((N + PM - 1) / PM), (unsigned)((M + PN - 1) / PN), (unsigned)ks);
+  cfg.blockDim = dim3(PTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = PSMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)ks;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int nkc = K / PK / ks;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, proj_kernel, static_cast<const __nv_bfloat16*>(x),
+                         static_cast<const __nv_bfloat16*>(w), M, N, K, nkc, route, status);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace gdn

@@ -31,10 +31,12 @@ _CODES = {
 EXPORTED = ("gdn_state_slot_bytes", "gdn_conv1d_update", "gdn_decode_step", "gdn_decode_multi",
             "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_state_compact",
             "gdn_status_string", "gdn_prefill_chunked_noalloc", "gdn_decode_graphs_create",
-            "gdn_decode_graphs_buffers", "gdn_decode_graphs_launch", "gdn_decode_graphs_destroy")
+            "gdn_decode_graphs_buffers", "gdn_decode_graphs_launch", "gdn_decode_graphs_destroy",
+            "gdn_linear_bf16", "gdn_in_proj", "gdn_out_proj")
 GDN_MAX_DECODE_TOKENS = 8
 GDN_MAX_GRAPH_BUCKETS = 16
 GDN_NOALLOC_PREFILL_SCRATCH_BYTES = 64 << 20
+GDN_MAX_PROJ_SEGMENTS = 4
 
 
 class GdnError(RuntimeError):
@@ -54,6 +56,12 @@ class gdn_weights(ctypes.Structure):
     _fields_ = [("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
                 ("conv_weight", ctypes.c_void_p), ("norm_weight", ctypes.c_void_p),
                 ("act", ctypes.c_int)]
+
+
+class gdn_proj_route(ctypes.Structure):
+    _fields_ = [("nseg", ctypes.c_int32), ("start", ctypes.c_int32 * GDN_MAX_PROJ_SEGMENTS),
+                ("ld", ctypes.c_int32 * GDN_MAX_PROJ_SEGMENTS),
+                ("dst", ctypes.c_void_p * GDN_MAX_PROJ_SEGMENTS)]
 
 
 class gdn_pool(ctypes.Structure):
@@ -108,6 +116,12 @@ def load(build_if_missing: bool = False):
                                                 _P, _P]
     lib.gdn_state_compact.restype = ctypes.c_int
     lib.gdn_state_compact.argtypes = [_P, ctypes.c_int, _P, _P, _P, _I32, _P]
+    lib.gdn_linear_bf16.restype = ctypes.c_int
+    lib.gdn_linear_bf16.argtypes = [_P, _P, _I32, _I32, _I32, _P, _I32, _P, _P]
+    lib.gdn_in_proj.restype = ctypes.c_int
+    lib.gdn_in_proj.argtypes = [_P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P]
+    lib.gdn_out_proj.restype = ctypes.c_int
+    lib.gdn_out_proj.argtypes = [_P, _P, _P, _I32, _I32, _P, _P, _P]
     lib.gdn_status_string.restype = ctypes.c_char_p
     lib.gdn_status_string.argtypes = [ctypes.c_int]
     _lib = lib
@@ -242,6 +256,42 @@ def gdn_state_compact(dims, act: int, pool, src_slots, dst_slots, stream=None):
         raise ValueError("src_slots and dst_slots differ in length")
     _check("gdn_state_compact", load().gdn_state_compact(
         ctypes.byref(dims), act, ctypes.byref(pool), src, dst, len(src_slots), _stream(stream)))
+
+
+def make_route(segments) -> gdn_proj_route:
+    """segments: [(start, ld, dst tensor or address), ...] in increasing start order."""
+    r = gdn_proj_route()
+    r.nseg = len(segments)
+    for i, (start, ld, dst) in enumerate(segments):
+        r.start[i] = int(start)
+        r.ld[i] = int(ld)
+        r.dst[i] = _ptr(dst)
+    return r
+
+
+def gdn_linear_bf16(x, w, route: gdn_proj_route, k_split: int = 0, status=None, stream=None):
+    """y = x w^T (bf16, f32 sums): x [M][K], w [N][K]; the outputs go where route says."""
+    M, K = int(x.shape[0]), int(x.shape[1])
+    N = int(w.shape[0])
+    _check("gdn_linear_bf16", load().gdn_linear_bf16(
+        _ptr(x), _ptr(w), M, N, K, ctypes.byref(route), int(k_split), _ptr(status),
+        _stream(stream)))
+
+
+def gdn_in_proj(dims, hidden, w_in, qkv, z, b, a, status=None, stream=None):
+    """hidden [rows][H], w_in [Cqkv + Hv*dv + 2*Hv][H] -> qkv, z, b, a (bf16, step layouts)."""
+    rows, H = int(hidden.shape[0]), int(hidden.shape[1])
+    _check("gdn_in_proj", load().gdn_in_proj(
+        ctypes.byref(dims), _ptr(hidden), _ptr(w_in), rows, H, _ptr(qkv), _ptr(z), _ptr(b),
+        _ptr(a), _ptr(status), _stream(stream)))
+
+
+def gdn_out_proj(dims, out, w_out, y, status=None, stream=None):
+    """out [rows][Hv*dv], w_out [H][Hv*dv] -> y [rows][H] (bf16)."""
+    rows, H = int(out.shape[0]), int(w_out.shape[0])
+    _check("gdn_out_proj", load().gdn_out_proj(
+        ctypes.byref(dims), _ptr(out), _ptr(w_out), rows, H, _ptr(y), _ptr(status),
+        _stream(stream)))
 
 
 def gdn_status_string(code: int) -> str:

@@ -68,6 +68,27 @@ class GatedDeltaNetLayer:
         gdn.gdn_decode_multi(self.dims, self.w, self.pool, slot_idx, qkv, z, a, b, out, stream)
         return out
 
+    def in_proj(self, hidden: torch.Tensor, w_in: torch.Tensor, stream=None) -> dict:
+        """Input projection of bf16 hidden states [rows][H] through the stacked weight w_in
+        [Cqkv + Hv*dv + 2*Hv][H]: returns the step inputs qkv, z, a, b as new device tensors."""
+        rows, g = hidden.shape[0], self.geo
+        dev = hidden.device
+        t = {"qkv": torch.empty((rows, g.cqkv), dtype=torch.bfloat16, device=dev),
+             "z": torch.empty((rows, g.zdim), dtype=torch.bfloat16, device=dev),
+             "a": torch.empty((rows, g.Hv), dtype=torch.bfloat16, device=dev),
+             "b": torch.empty((rows, g.Hv), dtype=torch.bfloat16, device=dev)}
+        gdn.gdn_in_proj(self.dims, hidden, w_in, t["qkv"], t["z"], t["b"], t["a"], self.status,
+                        stream)
+        return t
+
+    def out_proj(self, out: torch.Tensor, w_out: torch.Tensor, y=None, stream=None):
+        """Output projection of the step's bf16 output [rows][Hv*dv] through w_out [H][Hv*dv]."""
+        if y is None:
+            y = torch.empty((out.shape[0], w_out.shape[0]), dtype=torch.bfloat16,
+                            device=out.device)
+        gdn.gdn_out_proj(self.dims, out, w_out, y, self.status, stream)
+        return y
+
     def conv1d_update(self, slot_idx: torch.Tensor, qkv_in, out=None, stream=None):
         if out is None:
             out = torch.empty_like(qkv_in)

@@ -156,3 +156,28 @@ def cu_seqlens(lens) -> np.ndarray:
 def retire_choice(seed: int, batch: int, n_retire: int, tag: int) -> np.ndarray:
     """Indices (into the current rows) of the rows that retire at a schedule point."""
     return np.sort(rng_for(seed, 5, tag).choice(batch, n_retire, replace=False)).astype(np.int32)
+
+
+# Hidden sizes of the projections around the layer.  The pages print none; these are round
+# model widths at the scale of the models they serve (a reading, not a quoted figure).
+PROJ_HIDDEN = {32: 4096, 48: 5120}
+
+
+def proj_rows(geo: Geometry) -> int:
+    """Rows of the stacked input-projection weight: Cqkv + Hv*dv (z) + Hv (b) + Hv (a)."""
+    return geo.cqkv + geo.zdim + 2 * geo.Hv
+
+
+def make_proj_weights(geo: Geometry, hidden: int, seed: int) -> dict:
+    """w_in [Cqkv + Hv*dv + 2*Hv][hidden] ~ N(0, 1/hidden) and w_out [hidden][Hv*dv] ~
+    N(0, 1/(Hv*dv)), bf16 values: with N(0, 1) activations the projections come out at unit
+    scale, the distribution the step's inputs are drawn from."""
+    rng = rng_for(seed, 5)
+    w_in = rng.standard_normal((proj_rows(geo), hidden), dtype=np.float32) / np.float32(np.sqrt(hidden))
+    w_out = rng.standard_normal((hidden, geo.zdim), dtype=np.float32) / np.float32(np.sqrt(geo.zdim))
+    return dict(w_in=round_to_bf16(w_in), w_out=round_to_bf16(w_out))
+
+
+def make_hidden(n: int, hidden: int, seed: int, *tags: int) -> np.ndarray:
+    """Hidden states [n][hidden] ~ N(0, 1), bf16 values."""
+    return round_to_bf16(rng_for(seed, 6, *tags).standard_normal((n, hidden), dtype=np.float32))

@@ -73,6 +73,8 @@ def _load():
         lib.oracle_prefill_chunkwise.argtypes = lib.oracle_prefill.argtypes + [_I]
         lib.oracle_state_compact.restype = _I
         lib.oracle_state_compact.argtypes = [_P, _P, _I, ctypes.c_int64, ctypes.c_int64, _P, _P, _I]
+        lib.oracle_linear.argtypes = [_I, _I, _I, _P, _P, _P]
+        lib.oracle_in_proj.argtypes = [_I] * 6 + [_P] * 6
         _lib = lib
     return _lib
 
@@ -242,3 +244,39 @@ def state_compact(rec_state, conv_state, src, dst):
                                         rec_state[0].size if N else 0,
                                         conv_state[0].size if N else 0, _ptr(src), _ptr(dst),
                                         src.shape[0])
+
+
+# ---------------------------------------------------------------- projections
+
+def linear(x, w) -> np.ndarray:
+    """y = x w^T for x [M][K] and w [N][K] (weight row n = output feature n)."""
+    x = _f64(x)
+    w = _f64(w)
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("x and w disagree on K")
+    y = np.zeros((M, N))
+    _load().oracle_linear(M, N, K, _ptr(x), _ptr(w), _ptr(y))
+    return y
+
+
+def in_proj(dims, x, w_in):
+    """The stacked input projection; returns dict(qkv, z, b, a) of [rows][...] float64."""
+    Hk, Hv, dk, dv = (int(dims[k]) for k in ("Hk", "Hv", "dk", "dv"))
+    x = _f64(x)
+    w_in = _f64(w_in)
+    rows, hidden = x.shape
+    cqkv = 2 * Hk * dk + Hv * dv
+    if w_in.shape != (cqkv + Hv * dv + 2 * Hv, hidden):
+        raise ValueError("w_in must be [Cqkv + Hv*dv + 2*Hv][hidden]")
+    out = {"qkv": np.zeros((rows, cqkv)), "z": np.zeros((rows, Hv * dv)),
+           "b": np.zeros((rows, Hv)), "a": np.zeros((rows, Hv))}
+    _load().oracle_in_proj(Hk, Hv, dk, dv, rows, hidden, _ptr(x), _ptr(w_in), _ptr(out["qkv"]),
+                           _ptr(out["z"]), _ptr(out["b"]), _ptr(out["a"]))
+    return out
+
+
+def out_proj(o, w_out) -> np.ndarray:
+    """y [rows][hidden] = o [rows][Hv*dv] w_out^T."""
+    return linear(o, w_out)

@@ -476,3 +476,40 @@ int oracle_state_compact(double* rec_state, double* conv_state, int num_slots,
   free(snap_c);
   return 0;
 }
+
+/* ------------------------------------------------------------ projections */
+
+/* A linear layer without bias, the in_proj / out_proj weights around the layer
+ * ("pegainfer PR #1003", description bullets: the z/b/a row shards and the out_proj
+ * column shard of one weight surface; "helexa/cortex commit 95dc874
+ * (tp_qwen3_5)", TpQwen3_5GatedDeltaNet bullet).  Weight row n holds output
+ * feature n, as a linear layer stores it:
+ *     y[m][n] = sum_k x[m][k] * w[n][k],   summed in ascending k.             */
+void oracle_linear(int M, int N, int K, const double* x, const double* w, double* y) {
+  for (int m = 0; m < M; ++m)
+    for (int n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (int k = 0; k < K; ++k) acc += x[(size_t)m * K + k] * w[(size_t)n * K + k];
+      y[(size_t)m * N + n] = acc;
+    }
+}
+
+/* The input projection: the weights of in_proj_qkv (Cqkv rows), in_proj_z (Hv*dv
+ * rows), in_proj_b (Hv rows) and in_proj_a (Hv rows) stacked in that order, one
+ * linear layer over the stack, its output columns split back into the four
+ * inputs of the layer (qkv [rows][Cqkv], z [rows][Hv*dv], b and a [rows][Hv]). */
+void oracle_in_proj(int Hk, int Hv, int dk, int dv, int rows, int hidden, const double* x,
+                    const double* w_in, double* qkv, double* z, double* b, double* a) {
+  const int cqkv = 2 * Hk * dk + Hv * dv, zd = Hv * dv;
+  const int n = cqkv + zd + 2 * Hv;
+  double* y = (double*)malloc(sizeof(double) * (size_t)(rows > 0 ? rows : 1) * n);
+  oracle_linear(rows, n, hidden, x, w_in, y);
+  for (int m = 0; m < rows; ++m) {
+    const double* yr = y + (size_t)m * n;
+    memcpy(qkv + (size_t)m * cqkv, yr, sizeof(double) * cqkv);
+    memcpy(z + (size_t)m * zd, yr + cqkv, sizeof(double) * zd);
+    memcpy(b + (size_t)m * Hv, yr + cqkv + zd, sizeof(double) * Hv);
+    memcpy(a + (size_t)m * Hv, yr + cqkv + zd + Hv, sizeof(double) * Hv);
+  }
+  free(y);
+}

@@ -36,6 +36,11 @@ int main(void) {
   if (gdn_decode_graphs_launch(0, 1, 0) != GDN_ERR_INVALID_ARG) return 6;
   gdn_decode_graphs_destroy(0);
   if (!gdn_status_string(GDN_ERR_TOO_LARGE)) return 7;
+  gdn_proj_route r;
+  memset(&r, 0, sizeof(r));
+  if (gdn_linear_bf16(0, 0, 1, 64, 64, &r, 0, 0, 0) != GDN_ERR_INVALID_ARG) return 8;
+  if (gdn_in_proj(&d, &p, &p, 1, 100, &p, &p, &p, &p, 0, 0) != GDN_ERR_UNSUPPORTED_SHAPE) return 9;
+  if (gdn_out_proj(&d, 0, 0, 0, 64, 0, 0, 0) != GDN_ERR_INVALID_ARG) return 10;
   printf("ok %s\n", gdn_status_string(GDN_OK));
   return 0;
 }

@@ -121,6 +121,42 @@ def test_decode_graphs_host_checks(lib):
     lib.gdn_decode_graphs_destroy(None)                # no-op
 
 
+def test_projection_host_checks(lib):
+    """gdn_linear_bf16 / gdn_in_proj / gdn_out_proj: every bad argument is refused before any
+    CUDA call (the fake addresses are never dereferenced); M = 0 is a no-op."""
+    X, W, Y = 0x10000, 0x20000, 0x30000
+
+    def route(starts=(0,), lds=(64,), dsts=(Y,)):
+        return gdn.make_route(list(zip(starts, lds, dsts)))
+
+    def lin(M=4, N=64, K=128, r=None, ks=0, x=X, w=W):
+        r = route() if r is None else r
+        return lib.gdn_linear_bf16(x, w, M, N, K, ctypes.byref(r), ks, None, None)
+    assert lin(x=0) == -1
+    assert lin(N=0) == -1
+    assert lin(M=-1) == -1
+    assert lin(K=100) == -2                               # K not a multiple of 64
+    assert lin(M=65535 * 64 + 1) == -9
+    assert lin(x=X + 8) == -7                             # 16-byte alignment of x and w
+    assert lin(r=route((), (), ())) == -1                  # no segment
+    assert lin(r=route((1,))) == -1                        # start[0] != 0
+    assert lin(N=64, r=route((0, 32, 32), (32, 32, 32), (Y, Y, Y))) == -1   # empty segment
+    assert lin(N=64, r=route((0, 70), (70, 70), (Y, Y))) == -1              # start beyond N
+    assert lin(r=route((0,), (63,))) == -1                 # ld below the segment's width
+    assert lin(r=route(dsts=(Y + 1,))) == -7               # bf16 destination alignment
+    assert lin(ks=3) == -1
+    assert lin(K=128, ks=4) == -1                         # split must divide K / 64
+    assert lin(M=0, ks=3, x=0) == 0                       # empty: nothing read or launched
+    d = D()
+    assert lib.gdn_in_proj(ctypes.byref(D(Hv=33)), X, W, 4, 256, Y, Y, Y, Y, None, None) == -3
+    assert lib.gdn_in_proj(ctypes.byref(d), X, W, 4, 100, Y, Y, Y, Y, None, None) == -2
+    assert lib.gdn_in_proj(ctypes.byref(d), X, W, 4, 256, Y, None, Y, Y, None, None) == -1
+    assert lib.gdn_in_proj(ctypes.byref(d), X, W, 0, 256, Y, Y, Y, Y, None, None) == 0
+    assert lib.gdn_out_proj(ctypes.byref(d), X, W, 4, 256, None, None, None) == -1
+    assert lib.gdn_out_proj(ctypes.byref(d), X + 4, W, 4, 256, Y, None, None) == -7
+    assert lib.gdn_out_proj(ctypes.byref(d), X, W, 0, 256, Y, None, None) == 0
+
+
 def test_prefill_and_compact_host_checks(lib):
     d = D()
     w = gdn.gdn_weights(0x20000, 0x20000, 0x20000, 0x20000, gdn.GDN_BF16)

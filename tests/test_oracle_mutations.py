@@ -33,6 +33,15 @@ MUTATIONS = {
                        "            for (int f = 0; f < dk; ++f) v += Wm[(size_t)i * dk + f] * S0[(size_t)f * dv + e];\n            Um[(size_t)i * dv + e] -= 0.0 * v;"),
     "chunk_gamma_sign": ("              v = BETA(i) * exp(gam[i] - gam[j]) * kk;",
                          "              v = BETA(i) * exp(gam[j] - gam[i]) * kk;"),
+    "linear_transposed_weight": (
+        "      for (int k = 0; k < K; ++k) acc += x[(size_t)m * K + k] * w[(size_t)n * K + k];",
+        "      for (int k = 0; k < K; ++k) acc += x[(size_t)m * K + k] * w[(size_t)k * N + n];"),
+    "linear_drops_last_term": (
+        "      for (int k = 0; k < K; ++k) acc += x[(size_t)m * K + k] * w[(size_t)n * K + k];",
+        "      for (int k = 0; k < K - 1; ++k) acc += x[(size_t)m * K + k] * w[(size_t)n * K + k];"),
+    "in_proj_b_a_swapped": (
+        "    memcpy(b + (size_t)m * Hv, yr + cqkv + zd, sizeof(double) * Hv);",
+        "    memcpy(b + (size_t)m * Hv, yr + cqkv + zd + Hv, sizeof(double) * Hv);"),
     "compact_no_snapshot": (
         "    memcpy(rec_state + (size_t)dst[i] * rec_slot_elems, snap_r + (size_t)i * rec_slot_elems,",
         "    memcpy(rec_state + (size_t)dst[i] * rec_slot_elems, rec_state + (size_t)src[i] * rec_slot_elems,"),

@@ -11,7 +11,9 @@ The pages print no worked values for the gated delta rule, so the oracle is pinn
     GQA by explicit head duplication),
   * the chunkwise WY/UT form equals the token-by-token recurrence,
   * continuation: prefill(T) then decode(T+1) equals prefill(T+1),
-  * invariants: row permutation, untouched slots, padding rows, snapshot compaction.
+  * invariants: row permutation, untouched slots, padding rows, snapshot compaction,
+  * the projections: integer brute force against exact Python arithmetic, permutation
+    weights, and the stacked input projection's split checked feature by feature.
 """
 import math
 import os
@@ -460,3 +462,61 @@ def test_compaction_is_snapshot_gather():
     # duplicate destinations are rejected
     assert oracle.state_compact(rec.copy(), conv.copy(), np.array([0, 1], np.int32),
                                 np.array([2, 2], np.int32)) == -1
+
+
+# ----------------------------------------------------------------------------- projections
+
+def test_linear_integer_brute_force():
+    """Small integers are exact in float64, so the oracle's y = x w^T must equal Python's exact
+    integer sum of x[m][k] * w[n][k] -- with N != K, so a transposed weight index cannot pass."""
+    rng = np.random.default_rng(11)
+    M, N, K = 3, 5, 7
+    x = rng.integers(-9, 10, size=(M, K))
+    w = rng.integers(-9, 10, size=(N, K))
+    y = oracle.linear(x, w)
+    assert y.shape == (M, N)
+    for m in range(M):
+        for n in range(N):
+            exact = sum(int(x[m][k]) * int(w[n][k]) for k in range(K))
+            assert y[m][n] == exact, (m, n)
+
+
+def test_linear_permutation_weight_selects_features():
+    """A permutation matrix as the weight reorders the input features: y[:, n] = x[:, p[n]]."""
+    rng = np.random.default_rng(12)
+    K = 9
+    p = rng.permutation(K)
+    w = np.zeros((K, K))
+    w[np.arange(K), p] = 1.0
+    x = rng.standard_normal((4, K))
+    np.testing.assert_array_equal(oracle.linear(x, w), x[:, p])
+
+
+def test_in_proj_split_order_and_boundaries():
+    """Weight row n = (n + 1) e_0 and x[m][0] = m + 1 make output feature n of row m equal
+    (m + 1)(n + 1), so every output says which stacked row produced it: qkv takes rows
+    [0, Cqkv), z the next Hv*dv, then b (Hv rows), then a (Hv rows)."""
+    dims = dict(Hk=2, Hv=4, dk=8, dv=6)
+    cqkv, zd, Hv = 2 * 2 * 8 + 4 * 6, 4 * 6, 4
+    n = cqkv + zd + 2 * Hv
+    hidden, rows = 5, 3
+    w_in = np.zeros((n, hidden))
+    w_in[:, 0] = np.arange(1, n + 1)
+    x = np.zeros((rows, hidden))
+    x[:, 0] = np.arange(1, rows + 1)
+    got = oracle.in_proj(dims, x, w_in)
+    r = np.arange(1, rows + 1)[:, None]
+    np.testing.assert_array_equal(got["qkv"], r * np.arange(1, cqkv + 1))
+    np.testing.assert_array_equal(got["z"], r * np.arange(cqkv + 1, cqkv + zd + 1))
+    np.testing.assert_array_equal(got["b"], r * np.arange(cqkv + zd + 1, cqkv + zd + Hv + 1))
+    np.testing.assert_array_equal(got["a"], r * np.arange(cqkv + zd + Hv + 1, n + 1))
+
+
+def test_out_proj_shape_and_linearity():
+    """out_proj maps [rows][Hv*dv] to [rows][hidden] and is linear in its input."""
+    rng = np.random.default_rng(13)
+    o1, o2 = rng.standard_normal((2, 3, 12))
+    w = rng.standard_normal((7, 12))
+    y1, y2, y12 = oracle.out_proj(o1, w), oracle.out_proj(o2, w), oracle.out_proj(2 * o1 - o2, w)
+    assert y1.shape == (3, 7)
+    np.testing.assert_allclose(y12, 2 * y1 - y2, rtol=0, atol=1e-12)
