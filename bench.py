@@ -439,6 +439,7 @@ def time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak, reps=2
     the previous launches did not touch (copies rotated, > 2 x L2 per rotation).
     Prefill-shaped: in_proj of the T = 4096 sequence (hidden 4096), tensor bound, TFLOP/s
     against the bf16 peak."""
+    from gated_deltanet_linear_09_gb300.runtime import pack_weight
     stream = torch.cuda.current_stream()
     gen = torch.Generator(device="cuda")
     gen.manual_seed(77)
@@ -468,8 +469,8 @@ def time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak, reps=2
     l2 = 129e6
     r_in = max(2, int(2 * l2 // (n_in * H * 2)) + 1)
     r_out = max(2, int(2 * l2 // (n_out * geo.zdim * 2)) + 1)
-    w_in = [randn((n_in, H), H ** -0.5) for _ in range(r_in)]
-    w_out = [randn((n_out, geo.zdim), geo.zdim ** -0.5) for _ in range(r_out)]
+    w_in = [pack_weight(randn((n_in, H), H ** -0.5)) for _ in range(r_in)]
+    w_out = [pack_weight(randn((n_out, geo.zdim), geo.zdim ** -0.5)) for _ in range(r_out)]
     x = randn((B, H), 1.0)
     o = randn((B, geo.zdim), 1.0)
     t = {"qkv": torch.empty((B, geo.cqkv), dtype=torch.bfloat16, device="cuda"),
@@ -500,7 +501,7 @@ def time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak, reps=2
     T = pwl.seq_lens[0]
     player = GatedDeltaNetLayer(pgeo, synth.make_weights(pgeo, pwl.seed), 1)
     pn = synth.proj_rows(pgeo)
-    pw = randn((pn, PH), PH ** -0.5)
+    pw = pack_weight(randn((pn, PH), PH ** -0.5))
     px = randn((T, PH), 1.0)
     pt = {"qkv": torch.empty((T, pgeo.cqkv), dtype=torch.bfloat16, device="cuda"),
           "z": torch.empty((T, pgeo.zdim), dtype=torch.bfloat16, device="cuda"),
@@ -513,7 +514,8 @@ def time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak, reps=2
     res["prefill_in_proj"] = {"rows": T, "features": pn, "hidden": PH, "us": round(ms_p * 1e3, 2),
                               "tflops": round(tf, 1), "bf16_frac": round(tf / bf16_peak, 4)}
     res["hidden_sizes"] = {str(k): v for k, v in synth.PROJ_HIDDEN.items()}
-    res["kernel"] = "proj_kernel (tcgen05 128x64 tiles, cp.async ring, cluster split-K)"
+    res["kernel"] = ("proj_kernel (tcgen05 128x64 tiles, packed weight blocks by bulk copy, "
+                     "cluster split-K)")
     return res
 
 

@@ -179,6 +179,21 @@ int gdn_state_compact(const gdn_dims* dims, gdn_dtype act, const gdn_pool* pool,
                              stream);
 }
 
+size_t gdn_proj_packed_bytes(int32_t N, int32_t K) {
+  if (N < 1 || K < 1 || K % 64 != 0) return 0;
+  return gdn::proj_packed_bytes(N, K);
+}
+
+int gdn_proj_pack(const void* w, int32_t N, int32_t K, void* packed, size_t packed_bytes,
+                  cudaStream_t stream) {
+  if (!w || !packed || N < 1 || K < 1) return GDN_ERR_INVALID_ARG;
+  if (K % 64 != 0) return GDN_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)N * K > (1LL << 40)) return GDN_ERR_TOO_LARGE;
+  if (!aligned16(w) || !aligned16(packed)) return GDN_ERR_MISALIGNED;
+  if (packed_bytes < gdn::proj_packed_bytes(N, K)) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  return gdn::launch_proj_pack(w, N, K, packed, stream);
+}
+
 int gdn_linear_bf16(const void* x, const void* w, int32_t M, int32_t N, int32_t K,
                     const gdn_proj_route* route, int32_t k_split, int32_t* status,
                     cudaStream_t stream) {

@@ -61,7 +61,9 @@ struct ProjRoute {
 
 // Contraction split the library picks for an M x N x K projection (1, 2, 4 or 8).
 int proj_auto_split(int M, int N, int K);
-int launch_proj(const void* x, const void* w, int M, int N, int K, int ks, const ProjRoute& route,
+size_t proj_packed_bytes(int N, int K);
+int launch_proj_pack(const void* w, int N, int K, void* packed, cudaStream_t stream);
+int launch_proj(const void* x, const void* wp, int M, int N, int K, int ks, const ProjRoute& route,
                 int32_t* status, cudaStream_t stream);
 
 }  // namespace gdn

@@ -8,15 +8,18 @@
 //   y[m][n] = bf16( sum_k x[m][k] w[n][k] ),   x [M][K] activations, w [N][K] weights.
 //
 // At decode batch sizes the weights are nearly all of the bytes, so the kernel is laid out for
-// streaming them: a CTA owns 128 output features (the MMA's M = 128 operand is the weight tile)
-// and 64 activation rows (N = 64), and walks the contraction in 64-wide chunks through a ring
-// of shared-memory stages filled with cp.async.  The f32 accumulator lives in TMEM (lane =
-// output feature, column = activation row).  When there are too few tiles to cover the SMs,
-// the contraction is split over the CTAs of a thread-block cluster (grid z); each CTA parks its
-// partial tile in its own shared memory and every CTA of the cluster adds up one slice of the
-// columns over distributed shared memory, in a fixed order.  The epilogue routes each output
-// feature to one of up to four destination tensors, which is how the input projection writes
-// the step's four input buffers in one launch.
+// streaming them.  The weights are packed once (proj_pack_kernel) into 16 KiB blocks, each the
+// exact shared-memory image of one 128-feature x 64-element tile in the MMA's K-major core-matrix
+// layout, ordered so that the blocks one CTA consumes are contiguous: a pipeline stage is then a
+// single bulk async copy and DRAM sees long sequential runs instead of 128 scattered 128-byte row
+// pieces.  A CTA owns 128 output features (the MMA's M = 128 operand is the weight tile) and 64
+// activation rows (N = 64, loaded with cp.async from L2), and walks the contraction through a
+// ring of stages.  The f32 accumulator lives in TMEM (lane = output feature, column = activation
+// row).  When there are too few tiles to cover the SMs, the contraction is split over the CTAs of
+// a thread-block cluster (grid z); each CTA parks its partial tile in its own shared memory and
+// every CTA of the cluster adds up one slice of the columns over distributed shared memory, in a
+// fixed order.  The epilogue routes each output feature to one of up to four destination tensors,
+// which is how the input projection writes the step's four input buffers in one launch.
 #include <mutex>
 
 #include "gdn_internal.h"
@@ -36,12 +39,11 @@ constexpr uint32_t PB_BYTES = PN * PK * 2;   // activation tile, 8 KiB
 constexpr uint32_t PSTAGE_BYTES = PA_BYTES + PB_BYTES;
 constexpr uint32_t PRED_BYTES = PM * PN * 4;  // f32 partial tile [PN][PM], aliases the stages
 constexpr uint32_t PBAR_OFF = PSTAGES * PSTAGE_BYTES;
-constexpr uint32_t PSMEM = PBAR_OFF + PSTAGES * 8 + 16;
-constexpr int PCOPIES = (PM + PN) * (PK / 8) / PTHREADS;   // 16-byte copies per thread per stage
-constexpr int PW_COPIES = PM * (PK / 8) / PTHREADS;        // ... of which weight rows
+constexpr uint32_t PSMEM = PBAR_OFF + 2 * PSTAGES * 8 + 16;
+constexpr int PX_COPIES = PN * (PK / 8) / PTHREADS;   // 16-byte activation copies per thread
 static_assert(PRED_BYTES <= PBAR_OFF, "partial tile must fit in the stage ring");
-static_assert(PCOPIES * PTHREADS == (PM + PN) * (PK / 8) && PW_COPIES * PTHREADS == PM * (PK / 8),
-              "copies must divide evenly over the threads");
+static_assert(PX_COPIES * PTHREADS == PN * (PK / 8), "copies must divide evenly over the threads");
+static_assert(PA_BYTES == GDN_PROJ_BLOCK_BYTES, "a packed block is one weight stage");
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(g),
@@ -62,89 +64,127 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
   return v;
 }
 
-// One stage: the weight tile (PM rows) and the activation tile (PN rows), PK wide, in the
-// K-major no-swizzle core-matrix layout.  Copy u covers row 8*(u/64) + u%8, elements
-// 8*((u/8)%8) .. +8, which is byte u*16 of the tile: consecutive threads fill consecutive 16-byte
-// slots (no shared-memory bank conflicts) while each 8-thread group reads 8 rows' 16-byte
-// pieces.  Rows past the end of w or x are zero-filled (source size 0, address kept in range).
-__device__ __forceinline__ void load_stage(uint32_t sa, const __nv_bfloat16* __restrict__ W,
-                                           const __nv_bfloat16* __restrict__ X, int N, int M,
-                                           int K, int n0, int m0, int k0) {
+// The activation tile of one stage (PN rows x PK) in the K-major no-swizzle core-matrix layout.
+// Copy u covers row 8*(u/64) + u%8, elements 8*((u/8)%8) .. +8, which is byte u*16 of the tile:
+// consecutive threads fill consecutive 16-byte slots (no shared-memory bank conflicts).  Rows past
+// M are zero-filled (source size 0, address kept in range).
+__device__ __forceinline__ void load_x(uint32_t sb, const __nv_bfloat16* __restrict__ X, int M,
+                                       int K, int m0, int k0) {
 #pragma unroll
-  for (int i = 0; i < PCOPIES; ++i) {
+  for (int i = 0; i < PX_COPIES; ++i) {
     const int u = (int)threadIdx.x + i * PTHREADS;
-    const int kg = (u >> 3) & 7;
-    if (i < PW_COPIES) {
-      const int n = n0 + (((u >> 6) << 3) | (u & 7));
-      const __nv_bfloat16* src = W + (size_t)min(n, N - 1) * K + k0 + 8 * kg;
-      cp_async16(sa + (uint32_t)u * 16u, src, n < N ? 16u : 0u);
-    } else {
-      const int v = u - PM * (PK / 8);
-      const int m = m0 + (((v >> 6) << 3) | (v & 7));
-      const __nv_bfloat16* src = X + (size_t)min(m, M - 1) * K + k0 + 8 * kg;
-      cp_async16(sa + PA_BYTES + (uint32_t)v * 16u, src, m < M ? 16u : 0u);
-    }
+    const int m = m0 + (((u >> 6) << 3) | (u & 7));
+    const __nv_bfloat16* src = X + (size_t)min(m, M - 1) * K + k0 + 8 * ((u >> 3) & 7);
+    cp_async16(sb + (uint32_t)u * 16u, src, m < M ? 16u : 0u);
+  }
+}
+
+// Packs w [N][K] into the block layout: block (nt, kc) = features [128 nt, 128 nt + 128) x
+// elements [64 kc, 64 kc + 64) at byte (nt * K/64 + kc) * 16384; inside a block element (r, k) at
+// byte ((r/8) * 8 + k/8) * 128 + (r%8) * 16 + (k%8) * 2; features past N are zero.  One thread
+// writes one 16-byte unit (8 consecutive elements of one row), so the writes are coalesced.
+__global__ void proj_pack_kernel(const __nv_bfloat16* __restrict__ W, int N, int K,
+                                 uint4* __restrict__ P, long long units) {
+  const int kcs = K / PK;
+  for (long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x; u < units;
+       u += (long long)gridDim.x * blockDim.x) {
+    const long long blk = u >> 10;
+    const int v = (int)(u & 1023);
+    const int nt = (int)(blk / kcs), kc = (int)(blk % kcs);
+    const int n = nt * PM + (((v >> 6) << 3) | (v & 7));
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (n < N) val = *reinterpret_cast<const uint4*>(W + (size_t)n * K + kc * PK + 8 * ((v >> 3) & 7));
+    P[u] = val;
   }
 }
 
 // Grid (ceil(N/PM), ceil(M/PN), ks), cluster (1, 1, ks): CTA z of a cluster takes contraction
 // chunks [z*nkc, (z+1)*nkc) and adds up columns [z*PN/ks, (z+1)*PN/ks) of the cluster's tile.
+// Thread 0 issues the weight copies and the MMAs; every thread copies its share of the
+// activation tiles.
 __global__ void __launch_bounds__(PTHREADS, 2)
-proj_kernel(const __nv_bfloat16* __restrict__ X, const __nv_bfloat16* __restrict__ W, int M,
+proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict__ WP, int M,
             int N, int K, int nkc, const ProjRoute route, int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PBAR_OFF);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + PSTAGES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + PBAR_OFF);   // weight block landed
+  uint64_t* done = full + PSTAGES;                                // the stage's MMAs completed
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + PSTAGES);
   const int n0 = blockIdx.x * PM, m0 = blockIdx.y * PN;
   const int ks = (int)gridDim.z, z = (int)blockIdx.z;
   const int kbase = z * nkc * PK;
+  const unsigned char* wblk = WP + ((size_t)blockIdx.x * (K / PK) + (size_t)z * nkc) * PA_BYTES;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned char* stage0 = sm;
   const uint32_t s0 = tc::smem_u32(sm);
   if (tid == 0) {
-    for (int i = 0; i < PSTAGES; ++i) tc::mbar_init(bars + i, 1);
+    for (int i = 0; i < 2 * PSTAGES; ++i) tc::mbar_init(full + i, 1);
     tc::mbar_fence_init();
   }
   if (warp == 0) tc::tmem_alloc(tslot, PN);
-  // the first PSTAGES - 1 chunks in flight, one commit group each (empty groups included, so
-  // that the group count stays in step with the chunk index)
-#pragma unroll
-  for (int j = 0; j < PSTAGES - 1; ++j) {
-    if (j < nkc) load_stage(s0 + j * PSTAGE_BYTES, W, X, N, M, K, n0, m0, kbase + j * PK);
-    cp_async_commit();
-  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tb = *tslot;
+  int issued = 0, landed = 0;   // weight blocks issued / waited for (thread 0)
+  // the first PSTAGES - 1 chunks in flight, one cp.async group each (empty groups included, so
+  // that the group count stays in step with the chunk index)
+#pragma unroll
+  for (int j = 0; j < PSTAGES - 1; ++j) {
+    if (j < nkc) {
+      if (tid == 0) {
+        tc::mbar_arrive_expect_tx(full + j, PA_BYTES);
+        tc::bulk_g2s(stage0 + j * PSTAGE_BYTES, wblk + (size_t)j * PA_BYTES, PA_BYTES, full + j);
+        ++issued;
+      }
+      load_x(s0 + j * PSTAGE_BYTES + PA_BYTES, X, M, K, m0, kbase + j * PK);
+    }
+    cp_async_commit();
+  }
   constexpr uint32_t kIdesc = tc::idesc_bf16(PM, PN);
   bool ok = true;
   for (int kc = 0; kc < nkc; ++kc) {
     const int st = kc % PSTAGES;
-    cp_async_wait<PSTAGES - 2>();   // this thread's copies of chunk kc have landed ...
+    cp_async_wait<PSTAGES - 2>();   // this thread's activation copies of chunk kc landed ...
     tc::fence_proxy_async_smem();   // ... and are visible to the tensor core
     __syncthreads();
     if (tid == 0 && ok) {
-      tc::fence_after_sync();
-      const uint32_t sa = s0 + st * PSTAGE_BYTES;
-      const uint64_t da = tc::kstep_desc(sa, PK, 0), db = tc::kstep_desc(sa + PA_BYTES, PK, 0);
+      if (!tc::mbar_wait(full + st, (kc / PSTAGES) & 1)) {
+        ok = false;
+      } else {
+        ++landed;
+        tc::fence_after_sync();
+        const uint32_t sa = s0 + st * PSTAGE_BYTES;
+        const uint64_t da = tc::kstep_desc(sa, PK, 0), db = tc::kstep_desc(sa + PA_BYTES, PK, 0);
 #pragma unroll
-      for (int k = 0; k < PK / 16; ++k)
-        tc::mma_bf16(tb, tc::desc_add(da, 256u * k), tc::desc_add(db, 256u * k), kIdesc,
-                     (kc > 0 || k > 0) ? 1u : 0u);
-      tc::mma_commit(bars + st);
+        for (int k = 0; k < PK / 16; ++k)
+          tc::mma_bf16(tb, tc::desc_add(da, 256u * k), tc::desc_add(db, 256u * k), kIdesc,
+                       (kc > 0 || k > 0) ? 1u : 0u);
+        tc::mma_commit(done + st);
+      }
     }
     // refill the stage of chunk kc - 1 with chunk kc + PSTAGES - 1 once its MMAs are done
     const int nxt = kc + PSTAGES - 1;
     if (nxt < nkc) {
-      if (kc > 0 && ok && !tc::mbar_wait(bars + (kc - 1) % PSTAGES, ((kc - 1) / PSTAGES) & 1))
+      if (kc > 0 && ok && !tc::mbar_wait(done + (kc - 1) % PSTAGES, ((kc - 1) / PSTAGES) & 1))
         ok = false;
-      if (ok) load_stage(s0 + (nxt % PSTAGES) * PSTAGE_BYTES, W, X, N, M, K, n0, m0, kbase + nxt * PK);
+      if (ok) {
+        const int ns = nxt % PSTAGES;
+        if (tid == 0) {
+          tc::mbar_arrive_expect_tx(full + ns, PA_BYTES);
+          tc::bulk_g2s(stage0 + ns * PSTAGE_BYTES, wblk + (size_t)nxt * PA_BYTES, PA_BYTES, full + ns);
+          ++issued;
+        }
+        load_x(s0 + ns * PSTAGE_BYTES + PA_BYTES, X, M, K, m0, kbase + nxt * PK);
+      }
     }
     cp_async_commit();
   }
   // the last chunk's commit covers every MMA issued before it
-  if (ok && !tc::mbar_wait(bars + (nkc - 1) % PSTAGES, ((nkc - 1) / PSTAGES) & 1)) ok = false;
+  if (ok && !tc::mbar_wait(done + (nkc - 1) % PSTAGES, ((nkc - 1) / PSTAGES) & 1)) ok = false;
   cp_async_wait<0>();
+  // after a timeout, let the weight copies still in flight land before the memory is reused
+  if (tid == 0)
+    for (int c = landed; c < issued; ++c) tc::mbar_wait(full + c % PSTAGES, (c / PSTAGES) & 1);
   ok = __syncthreads_and(ok) != 0;
   if (!ok && tid == 0 && status) atomicOr(status, GDN_STATUS_TIMEOUT);
   tc::fence_after_sync();
@@ -214,7 +254,19 @@ int proj_auto_split(int M, int N, int K) {
   return ks;
 }
 
-int launch_proj(const void* x, const void* w, int M, int N, int K, int ks, const ProjRoute& route,
+size_t proj_packed_bytes(int N, int K) { return (size_t)((N + PM - 1) / PM) * PM * (size_t)K * 2; }
+
+int launch_proj_pack(const void* w, int N, int K, void* packed, cudaStream_t stream) {
+  const long long units = (long long)proj_packed_bytes(N, K) / 16;
+  const int threads = 256;
+  const long long want = (units + threads - 1) / threads;
+  const int blocks = (int)(want < 4096 ? want : 4096);
+  proj_pack_kernel<<<blocks, threads, 0, stream>>>(static_cast<const __nv_bfloat16*>(w), N, K,
+                                                   static_cast<uint4*>(packed), units);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+int launch_proj(const void* x, const void* wp, int M, int N, int K, int ks, const ProjRoute& route,
                 int32_t* status, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -238,7 +290,7 @@ int launch_proj(const void* x, const void* w, int M, int N, int K, int ks, const
   const int nkc = K / PK / ks;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, proj_kernel, static_cast<const __nv_bfloat16*>(x),
-                         static_cast<const __nv_bfloat16*>(w), M, N, K, nkc, route, status);
+                         static_cast<const unsigned char*>(wp), M, N, K, nkc, route, status);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

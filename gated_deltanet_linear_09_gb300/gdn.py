@@ -32,11 +32,13 @@ EXPORTED = ("gdn_state_slot_bytes", "gdn_conv1d_update", "gdn_decode_step", "gdn
             "gdn_prefill_workspace_bytes", "gdn_prefill_chunked", "gdn_state_compact",
             "gdn_status_string", "gdn_prefill_chunked_noalloc", "gdn_decode_graphs_create",
             "gdn_decode_graphs_buffers", "gdn_decode_graphs_launch", "gdn_decode_graphs_destroy",
-            "gdn_linear_bf16", "gdn_in_proj", "gdn_out_proj")
+            "gdn_proj_packed_bytes", "gdn_proj_pack", "gdn_linear_bf16", "gdn_in_proj",
+            "gdn_out_proj")
 GDN_MAX_DECODE_TOKENS = 8
 GDN_MAX_GRAPH_BUCKETS = 16
 GDN_NOALLOC_PREFILL_SCRATCH_BYTES = 64 << 20
 GDN_MAX_PROJ_SEGMENTS = 4
+GDN_PROJ_BLOCK_BYTES = 16384
 
 
 class GdnError(RuntimeError):
@@ -116,6 +118,10 @@ def load(build_if_missing: bool = False):
                                                 _P, _P]
     lib.gdn_state_compact.restype = ctypes.c_int
     lib.gdn_state_compact.argtypes = [_P, ctypes.c_int, _P, _P, _P, _I32, _P]
+    lib.gdn_proj_packed_bytes.restype = ctypes.c_size_t
+    lib.gdn_proj_packed_bytes.argtypes = [_I32, _I32]
+    lib.gdn_proj_pack.restype = ctypes.c_int
+    lib.gdn_proj_pack.argtypes = [_P, _I32, _I32, _P, ctypes.c_size_t, _P]
     lib.gdn_linear_bf16.restype = ctypes.c_int
     lib.gdn_linear_bf16.argtypes = [_P, _P, _I32, _I32, _I32, _P, _I32, _P, _P]
     lib.gdn_in_proj.restype = ctypes.c_int
@@ -269,28 +275,39 @@ def make_route(segments) -> gdn_proj_route:
     return r
 
 
-def gdn_linear_bf16(x, w, route: gdn_proj_route, k_split: int = 0, status=None, stream=None):
-    """y = x w^T (bf16, f32 sums): x [M][K], w [N][K]; the outputs go where route says."""
+def gdn_proj_packed_bytes(N: int, K: int) -> int:
+    return int(load().gdn_proj_packed_bytes(int(N), int(K)))
+
+
+def gdn_proj_pack(w, packed, stream=None):
+    """Packs a bf16 linear weight w [N][K] into the tile layout (packed: a uint8 device tensor)."""
+    N, K = int(w.shape[0]), int(w.shape[1])
+    _check("gdn_proj_pack", load().gdn_proj_pack(
+        _ptr(w), N, K, _ptr(packed), packed.numel() * packed.element_size(), _stream(stream)))
+
+
+def gdn_linear_bf16(x, w_packed, N: int, route: gdn_proj_route, k_split: int = 0, status=None,
+                    stream=None):
+    """y = x w^T (bf16, f32 sums): x [M][K], w packed from [N][K]; outputs go where route says."""
     M, K = int(x.shape[0]), int(x.shape[1])
-    N = int(w.shape[0])
     _check("gdn_linear_bf16", load().gdn_linear_bf16(
-        _ptr(x), _ptr(w), M, N, K, ctypes.byref(route), int(k_split), _ptr(status),
+        _ptr(x), _ptr(w_packed), M, int(N), K, ctypes.byref(route), int(k_split), _ptr(status),
         _stream(stream)))
 
 
-def gdn_in_proj(dims, hidden, w_in, qkv, z, b, a, status=None, stream=None):
-    """hidden [rows][H], w_in [Cqkv + Hv*dv + 2*Hv][H] -> qkv, z, b, a (bf16, step layouts)."""
+def gdn_in_proj(dims, hidden, w_in_packed, qkv, z, b, a, status=None, stream=None):
+    """hidden [rows][H], packed w_in [Cqkv + Hv*dv + 2*Hv][H] -> qkv, z, b, a (step layouts)."""
     rows, H = int(hidden.shape[0]), int(hidden.shape[1])
     _check("gdn_in_proj", load().gdn_in_proj(
-        ctypes.byref(dims), _ptr(hidden), _ptr(w_in), rows, H, _ptr(qkv), _ptr(z), _ptr(b),
-        _ptr(a), _ptr(status), _stream(stream)))
+        ctypes.byref(dims), _ptr(hidden), _ptr(w_in_packed), rows, H, _ptr(qkv), _ptr(z),
+        _ptr(b), _ptr(a), _ptr(status), _stream(stream)))
 
 
-def gdn_out_proj(dims, out, w_out, y, status=None, stream=None):
-    """out [rows][Hv*dv], w_out [H][Hv*dv] -> y [rows][H] (bf16)."""
-    rows, H = int(out.shape[0]), int(w_out.shape[0])
+def gdn_out_proj(dims, out, w_out_packed, y, status=None, stream=None):
+    """out [rows][Hv*dv], packed w_out [H][Hv*dv] -> y [rows][H] (bf16)."""
+    rows, H = int(out.shape[0]), int(y.shape[1])
     _check("gdn_out_proj", load().gdn_out_proj(
-        ctypes.byref(dims), _ptr(out), _ptr(w_out), rows, H, _ptr(y), _ptr(status),
+        ctypes.byref(dims), _ptr(out), _ptr(w_out_packed), rows, H, _ptr(y), _ptr(status),
         _stream(stream)))
 
 

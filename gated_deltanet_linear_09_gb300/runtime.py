@@ -21,6 +21,16 @@ def to_device(x: np.ndarray, dtype, device="cuda") -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(device=device, dtype=dtype)
 
 
+def pack_weight(w: torch.Tensor, stream=None) -> torch.Tensor:
+    """A bf16 linear weight [N][K] on the device -> its packed tile layout (uint8 tensor)."""
+    nbytes = gdn.gdn_proj_packed_bytes(w.shape[0], w.shape[1])
+    if nbytes == 0:
+        raise ValueError(f"cannot pack a weight of shape {tuple(w.shape)} (K must be a multiple of 64)")
+    packed = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    gdn.gdn_proj_pack(w, packed, stream)
+    return packed
+
+
 class GatedDeltaNetLayer:
     """Weights, state pool (rec f32 [N][Hv][dk][dv], conv act [N][K-1][Cqkv]) and status word."""
 
@@ -68,25 +78,26 @@ class GatedDeltaNetLayer:
         gdn.gdn_decode_multi(self.dims, self.w, self.pool, slot_idx, qkv, z, a, b, out, stream)
         return out
 
-    def in_proj(self, hidden: torch.Tensor, w_in: torch.Tensor, stream=None) -> dict:
-        """Input projection of bf16 hidden states [rows][H] through the stacked weight w_in
-        [Cqkv + Hv*dv + 2*Hv][H]: returns the step inputs qkv, z, a, b as new device tensors."""
+    def in_proj(self, hidden: torch.Tensor, w_in_packed: torch.Tensor, stream=None) -> dict:
+        """Input projection of bf16 hidden states [rows][H] through the packed stacked weight
+        (pack_weight of [Cqkv + Hv*dv + 2*Hv][H]): returns the step inputs qkv, z, a, b."""
         rows, g = hidden.shape[0], self.geo
         dev = hidden.device
         t = {"qkv": torch.empty((rows, g.cqkv), dtype=torch.bfloat16, device=dev),
              "z": torch.empty((rows, g.zdim), dtype=torch.bfloat16, device=dev),
              "a": torch.empty((rows, g.Hv), dtype=torch.bfloat16, device=dev),
              "b": torch.empty((rows, g.Hv), dtype=torch.bfloat16, device=dev)}
-        gdn.gdn_in_proj(self.dims, hidden, w_in, t["qkv"], t["z"], t["b"], t["a"], self.status,
-                        stream)
+        gdn.gdn_in_proj(self.dims, hidden, w_in_packed, t["qkv"], t["z"], t["b"], t["a"],
+                        self.status, stream)
         return t
 
-    def out_proj(self, out: torch.Tensor, w_out: torch.Tensor, y=None, stream=None):
-        """Output projection of the step's bf16 output [rows][Hv*dv] through w_out [H][Hv*dv]."""
+    def out_proj(self, out: torch.Tensor, w_out_packed: torch.Tensor, hidden_size: int, y=None,
+                 stream=None):
+        """Output projection of the step's bf16 output [rows][Hv*dv] through the packed
+        out_proj weight (pack_weight of [hidden_size][Hv*dv])."""
         if y is None:
-            y = torch.empty((out.shape[0], w_out.shape[0]), dtype=torch.bfloat16,
-                            device=out.device)
-        gdn.gdn_out_proj(self.dims, out, w_out, y, self.status, stream)
+            y = torch.empty((out.shape[0], hidden_size), dtype=torch.bfloat16, device=out.device)
+        gdn.gdn_out_proj(self.dims, out, w_out_packed, y, self.status, stream)
         return y
 
     def conv1d_update(self, slot_idx: torch.Tensor, qkv_in, out=None, stream=None):

@@ -251,8 +251,23 @@ int gdn_state_compact(const gdn_dims* dims, gdn_dtype act, const gdn_pool* pool,
  * and output projection (out_proj) of "pegainfer PR #1003", description bullets, and of
  * "helexa/cortex commit 95dc874 (tp_qwen3_5)", TpQwen3_5GatedDeltaNet bullet, as one bf16
  * tensor-core GEMM whose epilogue writes each output feature straight into the buffer that
- * consumes it. */
+ * consumes it.  The weights are packed once, at load time, into the kernel's tile layout. */
 #define GDN_MAX_PROJ_SEGMENTS 4
+#define GDN_PROJ_BLOCK_BYTES 16384
+
+/* Bytes of a packed weight of N output features by K inputs: ceil(N/128) * 128 * K * 2.
+ * Returns 0 unless N >= 1 and K is a positive multiple of 64. */
+size_t gdn_proj_packed_bytes(int32_t N, int32_t K);
+
+/* Packs a linear layer's weight w bf16 [N][K] (row n = output feature n, as stored) into the
+ * tile layout gdn_linear_bf16 streams.  Block (nt, kc) -- features [128 nt, 128 nt + 128), inputs
+ * [64 kc, 64 kc + 64) -- is GDN_PROJ_BLOCK_BYTES long at byte (nt * K/64 + kc) * 16384; inside it
+ * element (r, k) sits at byte ((r/8) * 8 + k/8) * 128 + (r%8) * 16 + (k%8) * 2 (the K-major
+ * core-matrix order of the MMA operand); features past N are zero.  w, packed: device, 16-byte
+ * aligned, not overlapping; packed_bytes >= gdn_proj_packed_bytes(N, K)
+ * (GDN_ERR_WORKSPACE_TOO_SMALL otherwise).  One kernel launch. */
+int gdn_proj_pack(const void* w, int32_t N, int32_t K, void* packed, size_t packed_bytes,
+                  cudaStream_t stream);
 
 /* Where the output features of gdn_linear_bf16 go.  Segment s holds features
  * [start[s], start[s+1]) (the last one ends at N); feature n of row m is written to
@@ -266,11 +281,11 @@ typedef struct {
 } gdn_proj_route;
 
 /* y = x w^T with one rounding to bf16:  y[m][n] = bf16( sum_k x[m][k] * w[n][k] ), summed in
- * f32 (w row n = output feature n, the layout of a linear layer's weight).
- *   x bf16 [M][K], w bf16 [N][K]: device, 16-byte aligned.  K a positive multiple of 64
+ * f32, with w given packed (gdn_proj_pack).
+ *   x bf16 [M][K], w_packed: device, 16-byte aligned.  K a positive multiple of 64
  *     (GDN_ERR_UNSUPPORTED_SHAPE otherwise); N >= 1; 0 <= M <= 4194240 (GDN_ERR_TOO_LARGE
  *     above); M = 0 returns GDN_OK after those checks, launching nothing and reading no
- *     other argument.  Destinations: device bf16, disjoint from x and w.
+ *     other argument.  Destinations: device bf16, disjoint from x and w_packed.
  *   k_split: 0 lets the library choose; 1, 2, 4 or 8 splits the contraction over that many
  *     CTAs of a thread-block cluster whose f32 partial sums are added in a fixed order (it
  *     must divide K / 64; GDN_ERR_INVALID_ARG otherwise).  For a given k_split the result is
@@ -278,26 +293,28 @@ typedef struct {
  *   status: optional device int32 word; GDN_STATUS_TIMEOUT is OR-ed in if a bounded wait
  *     inside the kernel gave up (the outputs are then invalid).
  * One kernel launch; no host reads of device data (graph-capturable). */
-int gdn_linear_bf16(const void* x, const void* w, int32_t M, int32_t N, int32_t K,
+int gdn_linear_bf16(const void* x, const void* w_packed, int32_t M, int32_t N, int32_t K,
                     const gdn_proj_route* route, int32_t k_split, int32_t* status,
                     cudaStream_t stream);
 
 /* Input projection of `rows` tokens (rows = B for gdn_decode_step, B*T for gdn_decode_multi,
  * the packed token count for gdn_prefill_chunked):
- *   hidden bf16 [rows][hidden_size];  w_in bf16 [Cqkv + Hv*dv + 2*Hv][hidden_size], the rows of
- *   in_proj_qkv, in_proj_z, in_proj_b and in_proj_a stacked in that order;
+ *   hidden bf16 [rows][hidden_size];  w_in_packed = gdn_proj_pack of the bf16 weight
+ *   [Cqkv + Hv*dv + 2*Hv][hidden_size] that stacks the rows of in_proj_qkv, in_proj_z,
+ *   in_proj_b and in_proj_a in that order;
  *   writes qkv bf16 [rows][Cqkv], z bf16 [rows][Hv*dv], b bf16 [rows][Hv], a bf16 [rows][Hv]
  *   -- the input layouts of the step calls with act = GDN_BF16.
  * hidden_size a positive multiple of 64.  Geometry checks as for the step calls.  One launch of
  * gdn_linear_bf16's kernel with the library's k_split. */
-int gdn_in_proj(const gdn_dims* dims, const void* hidden, const void* w_in, int32_t rows,
+int gdn_in_proj(const gdn_dims* dims, const void* hidden, const void* w_in_packed, int32_t rows,
                 int32_t hidden_size, void* qkv, void* z, void* b, void* a, int32_t* status,
                 cudaStream_t stream);
 
 /* Output projection: y bf16 [rows][hidden_size] = out [rows][Hv*dv] * w_out^T, with out the
- * step's bf16 output and w_out bf16 [hidden_size][Hv*dv] (out_proj's weight).  hidden_size
- * >= 1.  One launch of gdn_linear_bf16's kernel with the library's k_split. */
-int gdn_out_proj(const gdn_dims* dims, const void* out, const void* w_out, int32_t rows,
+ * step's bf16 output and w_out_packed = gdn_proj_pack of out_proj's bf16 weight
+ * [hidden_size][Hv*dv].  hidden_size >= 1.  One launch of gdn_linear_bf16's kernel with the
+ * library's k_split. */
+int gdn_out_proj(const gdn_dims* dims, const void* out, const void* w_out_packed, int32_t rows,
                  int32_t hidden_size, void* y, int32_t* status, cudaStream_t stream);
 
 /* Text for a return code. */

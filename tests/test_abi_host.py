@@ -155,6 +155,12 @@ def test_projection_host_checks(lib):
     assert lib.gdn_out_proj(ctypes.byref(d), X, W, 4, 256, None, None, None) == -1
     assert lib.gdn_out_proj(ctypes.byref(d), X + 4, W, 4, 256, Y, None, None) == -7
     assert lib.gdn_out_proj(ctypes.byref(d), X, W, 0, 256, Y, None, None) == 0
+    assert lib.gdn_proj_packed_bytes(300, 192) == 3 * 128 * 192 * 2
+    assert lib.gdn_proj_packed_bytes(300, 100) == 0 and lib.gdn_proj_packed_bytes(0, 64) == 0
+    assert lib.gdn_proj_pack(W, 300, 192, Y, 3 * 128 * 192 * 2 - 1, None) == -5
+    assert lib.gdn_proj_pack(W, 300, 100, Y, 1 << 20, None) == -2
+    assert lib.gdn_proj_pack(W + 8, 300, 192, Y, 1 << 20, None) == -7
+    assert lib.gdn_proj_pack(None, 300, 192, Y, 1 << 20, None) == -1
 
 
 def test_prefill_and_compact_host_checks(lib):

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from gated_deltanet_linear_09_gb300 import gdn, synth
-from gated_deltanet_linear_09_gb300.runtime import GatedDeltaNetLayer
+from gated_deltanet_linear_09_gb300.runtime import GatedDeltaNetLayer, pack_weight
 from gpu_util import assert_out_close, f64, rel_l2
 
 pytestmark = pytest.mark.gpu
@@ -26,6 +26,10 @@ def _np(t):
 
 def _bf16_dev(x):
     return torch.from_numpy(np.ascontiguousarray(x, np.float32)).cuda().to(torch.bfloat16)
+
+
+def _packed(w):
+    return pack_weight(_bf16_dev(w))
 
 
 def _operands(M, N, K, seed):
@@ -47,11 +51,28 @@ def test_linear_matches_oracle(M, N, K, ks):
     x, w = _operands(M, N, K, 900 + M)
     y = torch.full((M, N), 7.0, dtype=torch.bfloat16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    gdn.gdn_linear_bf16(_bf16_dev(x), _bf16_dev(w), gdn.make_route([(0, N, y)]), ks, status)
+    gdn.gdn_linear_bf16(_bf16_dev(x), _packed(w), N, gdn.make_route([(0, N, y)]), ks, status)
     torch.cuda.synchronize()
     ref = oracle.linear(x, w)
     assert_out_close(_np(y), ref, synth.BF16, f"M={M} N={N} K={K} ks={ks}")
     assert int(status.item()) == 0
+
+
+def test_pack_layout():
+    """The packed weight is the documented tile layout: block (nt, kc) at (nt*K/64 + kc) * 16384
+    bytes, element (r, k) at ((r//8)*8 + k//8)*128 + (r%8)*16 + (k%8)*2 inside it, zero rows
+    past N (bit-exact; built here from that statement with numpy index arithmetic)."""
+    N, K = 300, 192
+    w = synth.round_to_bf16(synth.rng_for(940, 9).standard_normal((N, K), dtype=np.float32))
+    got = _packed(w).cpu().numpy()
+    assert got.size == gdn.gdn_proj_packed_bytes(N, K) == 3 * 128 * K * 2
+    bits = (w.view(np.uint32) >> 16).astype(np.uint16)
+    want = np.zeros(got.size // 2, np.uint16)
+    n, k = np.meshgrid(np.arange(N), np.arange(K), indexing="ij")
+    nt, r, kc, kk = n // 128, n % 128, k // 64, k % 64
+    off = (nt * (K // 64) + kc) * 16384 + ((r // 8) * 8 + kk // 8) * 128 + (r % 8) * 16 + (kk % 8) * 2
+    want[(off // 2).ravel()] = bits.ravel()
+    np.testing.assert_array_equal(got.view(np.uint16), want)
 
 
 def test_linear_routing_segments_and_padding_columns():
@@ -61,7 +82,7 @@ def test_linear_routing_segments_and_padding_columns():
     x, w = _operands(M, N, K, 910)
     starts, widths, lds = [0, 130, 257], [130, 127, 43], [136, 128, 50]
     dsts = [torch.full((M, ld), -3.0, dtype=torch.bfloat16, device="cuda") for ld in lds]
-    gdn.gdn_linear_bf16(_bf16_dev(x), _bf16_dev(w),
+    gdn.gdn_linear_bf16(_bf16_dev(x), _packed(w), N,
                         gdn.make_route(list(zip(starts, lds, dsts))), 0)
     torch.cuda.synchronize()
     ref = oracle.linear(x, w)
@@ -75,12 +96,12 @@ def test_linear_is_deterministic_and_splits_agree():
     """Same call twice: bitwise equal.  Different contraction splits: each within the bound."""
     M, N, K = 64, 512, 4096
     x, w = _operands(M, N, K, 920)
-    xd, wd = _bf16_dev(x), _bf16_dev(w)
+    xd, wd = _bf16_dev(x), _packed(w)
     ref = oracle.linear(x, w)
     outs = {}
     for ks in (1, 2, 4, 8, 8):
         y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        gdn.gdn_linear_bf16(xd, wd, gdn.make_route([(0, N, y)]), ks)
+        gdn.gdn_linear_bf16(xd, wd, N, gdn.make_route([(0, N, y)]), ks)
         torch.cuda.synchronize()
         g = _np(y)
         assert_out_close(g, ref, synth.BF16, f"ks={ks}")
@@ -91,9 +112,9 @@ def test_linear_is_deterministic_and_splits_agree():
 
 def test_linear_empty_batch_is_a_noop():
     x = torch.zeros((0, 128), dtype=torch.bfloat16, device="cuda")
-    w = torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda")
+    w = pack_weight(torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda"))
     y = torch.full((1, 64), 5.0, dtype=torch.bfloat16, device="cuda")
-    gdn.gdn_linear_bf16(x, w, gdn.make_route([(0, 64, y)]), 0)
+    gdn.gdn_linear_bf16(x, w, 64, gdn.make_route([(0, 64, y)]), 0)
     torch.cuda.synchronize()
     assert torch.all(y == 5.0)
 
@@ -112,13 +133,13 @@ def test_in_and_out_proj_full_size():
     H = synth.PROJ_HIDDEN[geo.Hv]
     pw = synth.make_proj_weights(geo, H, wl.seed)
     x = synth.make_hidden(wl.batch, H, wl.seed, 0)
-    got = layer.in_proj(_bf16_dev(x), _bf16_dev(pw["w_in"]))
+    got = layer.in_proj(_bf16_dev(x), _packed(pw["w_in"]))
     ref = oracle.in_proj(geo.oracle_dims(), x, pw["w_in"])
     for k in ("qkv", "z", "b", "a"):
         assert_out_close(_np(got[k]), ref[k], synth.BF16, k)
     o = synth.round_to_bf16(synth.rng_for(wl.seed, 7).standard_normal((wl.batch, geo.zdim),
                                                                        dtype=np.float32))
-    y = layer.out_proj(_bf16_dev(o), _bf16_dev(pw["w_out"]))
+    y = layer.out_proj(_bf16_dev(o), _packed(pw["w_out"]), H)
     torch.cuda.synchronize()
     assert_out_close(_np(y), oracle.out_proj(o, pw["w_out"]), synth.BF16, "out_proj")
     assert int(layer.status.item()) == 0
@@ -133,7 +154,7 @@ def test_prefill_shaped_in_proj_sampled():
     T = wl.seq_lens[0]
     pw = synth.make_proj_weights(geo, H, wl.seed)
     x = synth.make_hidden(T, H, wl.seed, 1)
-    got = layer.in_proj(_bf16_dev(x), _bf16_dev(pw["w_in"]))
+    got = layer.in_proj(_bf16_dev(x), _packed(pw["w_in"]))
     torch.cuda.synchronize()
     rows = np.sort(synth.rng_for(wl.seed, 8).choice(T, 48, replace=False))
     ref = oracle.in_proj(geo.oracle_dims(), x[rows], pw["w_in"])
@@ -156,12 +177,12 @@ def test_projections_around_the_decode_step():
     pw = synth.make_proj_weights(geo, H, 930)
     slots = np.array([3, 0, 5, 1, 4], np.int32)
     r64, c64 = rec.astype(np.float64), conv.astype(np.float64)
-    w_in, w_out = _bf16_dev(pw["w_in"]), _bf16_dev(pw["w_out"])
+    w_in, w_out = _packed(pw["w_in"]), _packed(pw["w_out"])
     for step in range(3):
         x = synth.make_hidden(B, H, 931, step)
         t = layer.in_proj(_bf16_dev(x), w_in)
         o = layer.decode_step(torch.from_numpy(slots).cuda(), t["qkv"], t["z"], t["a"], t["b"])
-        y = _np(layer.out_proj(o, w_out))
+        y = _np(layer.out_proj(o, w_out, H))
         ri = {k: synth.round_to_bf16(v.astype(np.float32)).astype(np.float64)
               for k, v in oracle.in_proj(geo.oracle_dims(), x, pw["w_in"]).items()}
         rc, ro = oracle.decode_step(geo.oracle_dims(), f64(w), r64, c64, slots, **ri)
