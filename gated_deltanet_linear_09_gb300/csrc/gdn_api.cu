@@ -217,8 +217,7 @@ int gdn_linear_bf16(const void* x, const void* w, int32_t M, int32_t N, int32_t 
     pr.ptr[s] = static_cast<__nv_bfloat16*>(r.dst[s]);
   }
   const int nk = K / 64;
-  if (k_split != 0 && k_split != 1 && k_split != 2 && k_split != 4 && k_split != 8)
-    return GDN_ERR_INVALID_ARG;
+  if (k_split < 0 || k_split > 8) return GDN_ERR_INVALID_ARG;
   if (k_split != 0 && nk % k_split != 0) return GDN_ERR_INVALID_ARG;
   const int ks = k_split != 0 ? k_split : gdn::proj_auto_split(M, N, K);
   return gdn::launch_proj(x, w, M, N, K, ks, pr, status, stream);

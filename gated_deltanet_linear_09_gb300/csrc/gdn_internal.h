@@ -59,7 +59,7 @@ struct ProjRoute {
   __nv_bfloat16* ptr[GDN_MAX_PROJ_SEGMENTS];
 };
 
-// Contraction split the library picks for an M x N x K projection (1, 2, 4 or 8).
+// Contraction split the library picks for an M x N x K projection (1 to 8).
 int proj_auto_split(int M, int N, int K);
 size_t proj_packed_bytes(int N, int K);
 int launch_proj_pack(const void* w, int N, int K, void* packed, cudaStream_t stream);

@@ -16,7 +16,7 @@
 // activation rows (N = 64, loaded with cp.async from L2), and walks the contraction through a
 // ring of stages.  The f32 accumulator lives in TMEM (lane = output feature, column = activation
 // row).  When there are too few tiles to cover the SMs, the contraction is split over the CTAs of
-// a thread-block cluster (grid z); each CTA parks its partial tile in its own shared memory and
+// a thread-block cluster (grid z, any size up to 8); each CTA parks its partial tile in its own shared memory and
 // every CTA of the cluster adds up one slice of the columns over distributed shared memory, in a
 // fixed order.  The epilogue routes each output feature to one of up to four destination tensors,
 // which is how the input projection writes the step's four input buffers in one launch.
@@ -32,7 +32,9 @@ namespace {
 constexpr int PM = 128;         // output features per CTA (MMA M, TMEM lanes)
 constexpr int PN = 64;          // activation rows per CTA (MMA N, TMEM columns)
 constexpr int PK = 64;          // contraction elements per stage
-constexpr int PSTAGES = 4;      // ring depth; 96 KiB of stages lets two CTAs share an SM
+constexpr int PSTAGES = 9;      // ring depth (216 KiB: one CTA per SM)
+constexpr int PLAG = 3;         // a stage is refilled PLAG chunks after its MMAs were issued ...
+constexpr int PDIST = PSTAGES - PLAG;   // ... so PDIST chunks are in flight
 constexpr int PTHREADS = 256;
 constexpr uint32_t PA_BYTES = PM * PK * 2;   // weight tile, 16 KiB
 constexpr uint32_t PB_BYTES = PN * PK * 2;   // activation tile, 8 KiB
@@ -99,10 +101,12 @@ __global__ void proj_pack_kernel(const __nv_bfloat16* __restrict__ W, int N, int
 }
 
 // Grid (ceil(N/PM), ceil(M/PN), ks), cluster (1, 1, ks): CTA z of a cluster takes contraction
-// chunks [z*nkc, (z+1)*nkc) and adds up columns [z*PN/ks, (z+1)*PN/ks) of the cluster's tile.
+// chunks [z*nkc, (z+1)*nkc) and adds up columns [z*PN/ks, (z+1)*PN/ks) (rounded down) of the
+// cluster's tile (ks = 1: a plain launch, no cluster).  One CTA per SM: the stage ring takes
+// most of the shared memory and keeps PDIST weight blocks in flight.
 // Thread 0 issues the weight copies and the MMAs; every thread copies its share of the
 // activation tiles.
-__global__ void __launch_bounds__(PTHREADS, 2)
+__global__ void __launch_bounds__(PTHREADS, 1)
 proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict__ WP, int M,
             int N, int K, int nkc, const ProjRoute route, int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
@@ -126,10 +130,10 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   tc::fence_after_sync();
   const uint32_t tb = *tslot;
   int issued = 0, landed = 0;   // weight blocks issued / waited for (thread 0)
-  // the first PSTAGES - 1 chunks in flight, one cp.async group each (empty groups included, so
-  // that the group count stays in step with the chunk index)
+  // the first PDIST chunks in flight, one cp.async group each (empty groups included, so that
+  // the group count stays in step with the chunk index)
 #pragma unroll
-  for (int j = 0; j < PSTAGES - 1; ++j) {
+  for (int j = 0; j < PDIST; ++j) {
     if (j < nkc) {
       if (tid == 0) {
         tc::mbar_arrive_expect_tx(full + j, PA_BYTES);
@@ -144,7 +148,7 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   bool ok = true;
   for (int kc = 0; kc < nkc; ++kc) {
     const int st = kc % PSTAGES;
-    cp_async_wait<PSTAGES - 2>();   // this thread's activation copies of chunk kc landed ...
+    cp_async_wait<PDIST - 1>();     // this thread's activation copies of chunk kc landed ...
     tc::fence_proxy_async_smem();   // ... and are visible to the tensor core
     __syncthreads();
     if (tid == 0 && ok) {
@@ -162,10 +166,12 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
         tc::mma_commit(done + st);
       }
     }
-    // refill the stage of chunk kc - 1 with chunk kc + PSTAGES - 1 once its MMAs are done
-    const int nxt = kc + PSTAGES - 1;
+    // refill the stage of chunk kc - PLAG with chunk kc + PDIST once its MMAs are done: waiting
+    // on MMAs issued PLAG iterations ago keeps the tensor pipe's latency off this loop
+    const int nxt = kc + PDIST;
     if (nxt < nkc) {
-      if (kc > 0 && ok && !tc::mbar_wait(done + (kc - 1) % PSTAGES, ((kc - 1) / PSTAGES) & 1))
+      const int prev = kc - PLAG;
+      if (prev >= 0 && ok && !tc::mbar_wait(done + prev % PSTAGES, (prev / PSTAGES) & 1))
         ok = false;
       if (ok) {
         const int ns = nxt % PSTAGES;
@@ -199,14 +205,18 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
 #pragma unroll
     for (int i = 0; i < 32; ++i) red[(c0 + i) * PM + lq + lane] = v[i];
   }
+  const bool clustered = ks > 1;
   tc::fence_before_sync();
-  tc::cluster_sync_all();   // every partial tile of the cluster is written and visible
+  if (clustered)
+    tc::cluster_sync_all();   // every partial tile of the cluster is written and visible
+  else
+    __syncthreads();
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tb, PN);
   // this CTA's column slice: thread -> lane r = tid % 128, columns cw0 + tid/128 + 2j
   const int r = tid & (PM - 1);
   const int n = n0 + r;
-  const int cw = PN / ks, cw0 = z * cw;
+  const int cw0 = z * PN / ks, cw1 = (z + 1) * PN / ks;
   __nv_bfloat16* base = route.ptr[0];
   int seg_start = 0, seg_ld = route.ld[0];
 #pragma unroll
@@ -219,15 +229,20 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   __nv_bfloat16* dst = base + (n - seg_start);
   const size_t ld = (size_t)seg_ld;
   const uint32_t red_s = tc::smem_u32(red);
-  for (int c = cw0 + (tid >> 7); c < cw0 + cw; c += PTHREADS / PM) {
+  for (int c = cw0 + (tid >> 7); c < cw1; c += PTHREADS / PM) {
     const int m = m0 + c;
     if (m >= M || n >= N) continue;
     const uint32_t off = red_s + (uint32_t)(c * PM + r) * 4u;
-    float s = 0.f;
-    for (int q = 0; q < ks; ++q) s += ld_cluster_f32(tc::mapa_shared(off, (uint32_t)q));
+    float s;
+    if (clustered) {
+      s = 0.f;
+      for (int q = 0; q < ks; ++q) s += ld_cluster_f32(tc::mapa_shared(off, (uint32_t)q));
+    } else {
+      s = red[c * PM + r];
+    }
     dst[(size_t)m * ld] = __float2bfloat16_rn(s);
   }
-  tc::cluster_sync_all();   // no CTA leaves while another still reads its shared memory
+  if (clustered) tc::cluster_sync_all();   // no CTA leaves while another reads its memory
 }
 
 int g_num_sms = 0;
@@ -244,13 +259,13 @@ int proj_auto_split(int M, int N, int K) {
     else
       g_num_sms = 152;
   });
-  // two CTAs fit on an SM; split the contraction while the CTAs still fit in one wave and
-  // every CTA keeps at least a full ring of chunks
+  // one CTA per SM: split the contraction while the grid still fits in one wave and every CTA
+  // keeps at least a full ring of chunks
   const long long tiles = (long long)((N + PM - 1) / PM) * ((M + PN - 1) / PN);
   const int nk = K / PK;
   int ks = 1;
-  for (int c = 2; c <= 8; c *= 2)
-    if (tiles * c <= 2LL * g_num_sms && nk % c == 0 && nk / c >= PSTAGES) ks = c;
+  for (int c = 2; c <= 8; ++c)
+    if (tiles * c <= (long long)g_num_sms && nk % c == 0 && nk / c >= PSTAGES) ks = c;
   return ks;
 }
 
@@ -286,7 +301,7 @@ int launch_proj(const void* x, const void* wp, int M, int N, int K, int ks, cons
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = (unsigned)ks;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = ks > 1 ? 1 : 0;   // no cluster without a split: nothing to exchange
   const int nkc = K / PK / ks;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, proj_kernel, static_cast<const __nv_bfloat16*>(x),

@@ -286,9 +286,9 @@ typedef struct {
  *     (GDN_ERR_UNSUPPORTED_SHAPE otherwise); N >= 1; 0 <= M <= 4194240 (GDN_ERR_TOO_LARGE
  *     above); M = 0 returns GDN_OK after those checks, launching nothing and reading no
  *     other argument.  Destinations: device bf16, disjoint from x and w_packed.
- *   k_split: 0 lets the library choose; 1, 2, 4 or 8 splits the contraction over that many
- *     CTAs of a thread-block cluster whose f32 partial sums are added in a fixed order (it
- *     must divide K / 64; GDN_ERR_INVALID_ARG otherwise).  For a given k_split the result is
+ *   k_split: 0 lets the library choose; 1 to 8 splits the contraction over that many CTAs of
+ *     a thread-block cluster whose f32 partial sums are added in a fixed order (it must
+ *     divide K / 64; GDN_ERR_INVALID_ARG otherwise).  For a given k_split the result is
  *     bitwise reproducible.
  *   status: optional device int32 word; GDN_STATUS_TIMEOUT is OR-ed in if a bounded wait
  *     inside the kernel gave up (the outputs are then invalid).
