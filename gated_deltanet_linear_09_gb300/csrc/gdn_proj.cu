@@ -10,11 +10,11 @@
 // At decode batch sizes the weights are nearly all of the bytes, so the kernel is laid out for
 // streaming them.  The weights are packed once (proj_pack_kernel) into 16 KiB blocks, each the
 // exact shared-memory image of one 128-feature x 64-element tile in the MMA's K-major core-matrix
-// layout, ordered so that the blocks one CTA consumes are contiguous: a pipeline stage is then a
-// single bulk async copy and DRAM sees long sequential runs instead of 128 scattered 128-byte row
-// pieces.  A CTA owns 128 output features (the MMA's M = 128 operand is the weight tile) and 64
-// activation rows (N = 64, loaded with cp.async from L2), and walks the contraction through a
-// ring of stages.  The f32 accumulator lives in TMEM (lane = output feature, column = activation
+// layout, ordered so that the blocks one CTA consumes are contiguous: a pipeline stage then reads
+// 16 KiB of consecutive bytes and DRAM sees long sequential runs instead of 128 scattered 128-byte
+// row pieces.  A CTA owns 128 output features (the MMA's M = 128 operand is the weight tile) and
+// 64 activation rows (N = 64), and walks the contraction through a ring of shared-memory stages
+// filled with cp.async.  The f32 accumulator lives in TMEM (lane = output feature, column = activation
 // row).  When there are too few tiles to cover the SMs, the contraction is split over the CTAs of
 // a thread-block cluster (grid z, any size up to 8); each CTA parks its partial tile in its own shared memory and
 // every CTA of the cluster adds up one slice of the columns over distributed shared memory, in a
@@ -41,8 +41,9 @@ constexpr uint32_t PB_BYTES = PN * PK * 2;   // activation tile, 8 KiB
 constexpr uint32_t PSTAGE_BYTES = PA_BYTES + PB_BYTES;
 constexpr uint32_t PRED_BYTES = PM * PN * 4;  // f32 partial tile [PN][PM], aliases the stages
 constexpr uint32_t PBAR_OFF = PSTAGES * PSTAGE_BYTES;
-constexpr uint32_t PSMEM = PBAR_OFF + 2 * PSTAGES * 8 + 16;
+constexpr uint32_t PSMEM = PBAR_OFF + PSTAGES * 8 + 16;
 constexpr int PX_COPIES = PN * (PK / 8) / PTHREADS;   // 16-byte activation copies per thread
+constexpr int PW_UNITS = PA_BYTES / 16 / PTHREADS;    // 16-byte weight copies per thread
 static_assert(PRED_BYTES <= PBAR_OFF, "partial tile must fit in the stage ring");
 static_assert(PX_COPIES * PTHREADS == PN * (PK / 8), "copies must divide evenly over the threads");
 static_assert(PA_BYTES == GDN_PROJ_BLOCK_BYTES, "a packed block is one weight stage");
@@ -100,28 +101,42 @@ __global__ void proj_pack_kernel(const __nv_bfloat16* __restrict__ W, int N, int
   }
 }
 
+// One pipeline stage: weight block c of this CTA (a contiguous 16 KiB copy: 256 threads x 4 x 16
+// bytes, every warp reading 512 consecutive bytes) and the matching activation tile.
+__device__ __forceinline__ void load_chunk(uint32_t sa, const unsigned char* __restrict__ wblk,
+                                           const __nv_bfloat16* __restrict__ X, int M, int K,
+                                           int m0, int kbase, int c) {
+#pragma unroll
+  for (int i = 0; i < PW_UNITS; ++i) {
+    const uint32_t o = (threadIdx.x + i * PTHREADS) * 16u;
+    cp_async16(sa + o, wblk + (size_t)c * PA_BYTES + o, 16u);
+  }
+  load_x(sa + PA_BYTES, X, M, K, m0, kbase + c * PK);
+}
+
 // Grid (ceil(N/PM), ceil(M/PN), ks), cluster (1, 1, ks): CTA z of a cluster takes contraction
 // chunks [z*nkc, (z+1)*nkc) and adds up columns [z*PN/ks, (z+1)*PN/ks) (rounded down) of the
 // cluster's tile (ks = 1: a plain launch, no cluster).  One CTA per SM: the stage ring takes
-// most of the shared memory and keeps PDIST weight blocks in flight.
-// Thread 0 issues the weight copies and the MMAs; every thread copies its share of the
-// activation tiles.
+// most of the shared memory and keeps PDIST chunks in flight.  Every thread copies its share of
+// each stage; thread 0 issues the MMAs.  The CTAs of one launch walk their chunks from different
+// starting points (a rotation by feature tile), so that they do not all read the same
+// activation lines from L2 at the same moment.
 __global__ void __launch_bounds__(PTHREADS, 1)
 proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict__ WP, int M,
             int N, int K, int nkc, const ProjRoute route, int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + PBAR_OFF);   // weight block landed
-  uint64_t* done = full + PSTAGES;                                // the stage's MMAs completed
+  uint64_t* done = reinterpret_cast<uint64_t*>(sm + PBAR_OFF);   // the stage's MMAs completed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + PSTAGES);
   const int n0 = blockIdx.x * PM, m0 = blockIdx.y * PN;
   const int ks = (int)gridDim.z, z = (int)blockIdx.z;
   const int kbase = z * nkc * PK;
   const unsigned char* wblk = WP + ((size_t)blockIdx.x * (K / PK) + (size_t)z * nkc) * PA_BYTES;
+  const int rot = (int)(((unsigned long long)blockIdx.x * nkc / gridDim.x + blockIdx.y * 7ull) %
+                        (unsigned)nkc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  unsigned char* stage0 = sm;
   const uint32_t s0 = tc::smem_u32(sm);
   if (tid == 0) {
-    for (int i = 0; i < 2 * PSTAGES; ++i) tc::mbar_init(full + i, 1);
+    for (int i = 0; i < PSTAGES; ++i) tc::mbar_init(done + i, 1);
     tc::mbar_fence_init();
   }
   if (warp == 0) tc::tmem_alloc(tslot, PN);
@@ -129,68 +144,46 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tb = *tslot;
-  int issued = 0, landed = 0;   // weight blocks issued / waited for (thread 0)
-  // the first PDIST chunks in flight, one cp.async group each (empty groups included, so that
-  // the group count stays in step with the chunk index)
+  // step j of the walk reads chunk (j + rot) mod nkc
+  auto chunk = [&](int j) { const int c = j + rot; return c < nkc ? c : c - nkc; };
+  // the first PDIST steps in flight, one cp.async group each (empty groups included, so that the
+  // group count stays in step with the step index)
 #pragma unroll
   for (int j = 0; j < PDIST; ++j) {
-    if (j < nkc) {
-      if (tid == 0) {
-        tc::mbar_arrive_expect_tx(full + j, PA_BYTES);
-        tc::bulk_g2s(stage0 + j * PSTAGE_BYTES, wblk + (size_t)j * PA_BYTES, PA_BYTES, full + j);
-        ++issued;
-      }
-      load_x(s0 + j * PSTAGE_BYTES + PA_BYTES, X, M, K, m0, kbase + j * PK);
-    }
+    if (j < nkc) load_chunk(s0 + j * PSTAGE_BYTES, wblk, X, M, K, m0, kbase, chunk(j));
     cp_async_commit();
   }
   constexpr uint32_t kIdesc = tc::idesc_bf16(PM, PN);
   bool ok = true;
   for (int kc = 0; kc < nkc; ++kc) {
     const int st = kc % PSTAGES;
-    cp_async_wait<PDIST - 1>();     // this thread's activation copies of chunk kc landed ...
+    cp_async_wait<PDIST - 1>();     // this thread's copies of step kc landed ...
     tc::fence_proxy_async_smem();   // ... and are visible to the tensor core
     __syncthreads();
     if (tid == 0 && ok) {
-      if (!tc::mbar_wait(full + st, (kc / PSTAGES) & 1)) {
-        ok = false;
-      } else {
-        ++landed;
-        tc::fence_after_sync();
-        const uint32_t sa = s0 + st * PSTAGE_BYTES;
-        const uint64_t da = tc::kstep_desc(sa, PK, 0), db = tc::kstep_desc(sa + PA_BYTES, PK, 0);
+      tc::fence_after_sync();
+      const uint32_t sa = s0 + st * PSTAGE_BYTES;
+      const uint64_t da = tc::kstep_desc(sa, PK, 0), db = tc::kstep_desc(sa + PA_BYTES, PK, 0);
 #pragma unroll
-        for (int k = 0; k < PK / 16; ++k)
-          tc::mma_bf16(tb, tc::desc_add(da, 256u * k), tc::desc_add(db, 256u * k), kIdesc,
-                       (kc > 0 || k > 0) ? 1u : 0u);
-        tc::mma_commit(done + st);
-      }
+      for (int k = 0; k < PK / 16; ++k)
+        tc::mma_bf16(tb, tc::desc_add(da, 256u * k), tc::desc_add(db, 256u * k), kIdesc,
+                     (kc > 0 || k > 0) ? 1u : 0u);
+      tc::mma_commit(done + st);
     }
-    // refill the stage of chunk kc - PLAG with chunk kc + PDIST once its MMAs are done: waiting
+    // refill the stage of step kc - PLAG with step kc + PDIST once its MMAs are done: waiting
     // on MMAs issued PLAG iterations ago keeps the tensor pipe's latency off this loop
     const int nxt = kc + PDIST;
     if (nxt < nkc) {
       const int prev = kc - PLAG;
       if (prev >= 0 && ok && !tc::mbar_wait(done + prev % PSTAGES, (prev / PSTAGES) & 1))
         ok = false;
-      if (ok) {
-        const int ns = nxt % PSTAGES;
-        if (tid == 0) {
-          tc::mbar_arrive_expect_tx(full + ns, PA_BYTES);
-          tc::bulk_g2s(stage0 + ns * PSTAGE_BYTES, wblk + (size_t)nxt * PA_BYTES, PA_BYTES, full + ns);
-          ++issued;
-        }
-        load_x(s0 + ns * PSTAGE_BYTES + PA_BYTES, X, M, K, m0, kbase + nxt * PK);
-      }
+      if (ok) load_chunk(s0 + (nxt % PSTAGES) * PSTAGE_BYTES, wblk, X, M, K, m0, kbase, chunk(nxt));
     }
     cp_async_commit();
   }
   // the last chunk's commit covers every MMA issued before it
   if (ok && !tc::mbar_wait(done + (nkc - 1) % PSTAGES, ((nkc - 1) / PSTAGES) & 1)) ok = false;
   cp_async_wait<0>();
-  // after a timeout, let the weight copies still in flight land before the memory is reused
-  if (tid == 0)
-    for (int c = landed; c < issued; ++c) tc::mbar_wait(full + c % PSTAGES, (c / PSTAGES) & 1);
   ok = __syncthreads_and(ok) != 0;
   if (!ok && tid == 0 && status) atomicOr(status, GDN_STATUS_TIMEOUT);
   tc::fence_after_sync();
