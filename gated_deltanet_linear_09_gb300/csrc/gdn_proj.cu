@@ -10,16 +10,17 @@
 // At decode batch sizes the weights are nearly all of the bytes, so the kernel is laid out for
 // streaming them.  The weights are packed once (proj_pack_kernel) into 16 KiB blocks, each the
 // exact shared-memory image of one 128-feature x 64-element tile in the MMA's K-major core-matrix
-// layout, ordered so that the blocks one CTA consumes are contiguous: a pipeline stage then reads
-// 16 KiB of consecutive bytes and DRAM sees long sequential runs instead of 128 scattered 128-byte
-// row pieces.  A CTA owns 128 output features (the MMA's M = 128 operand is the weight tile) and
-// 64 activation rows (N = 64), and walks the contraction through a ring of shared-memory stages
-// filled with cp.async.  The f32 accumulator lives in TMEM (lane = output feature, column = activation
-// row).  When there are too few tiles to cover the SMs, the contraction is split over the CTAs of
-// a thread-block cluster (grid z, any size up to 8); each CTA parks its partial tile in its own shared memory and
-// every CTA of the cluster adds up one slice of the columns over distributed shared memory, in a
-// fixed order.  The epilogue routes each output feature to one of up to four destination tensors,
-// which is how the input projection writes the step's four input buffers in one launch.
+// layout, ordered so that the blocks of one feature tile are contiguous: a pipeline stage reads
+// 16 KiB runs of consecutive bytes and DRAM sees long sequential streams instead of 128 scattered
+// 128-byte row pieces.  A CTA owns 256 output features -- two weight tiles, each the MMA's M = 128
+// operand with its own f32 accumulator in TMEM (lane = output feature, column = activation row)
+// -- and 64 activation rows (N = 64), so one activation tile serves twice the weight bytes; it
+// walks the contraction through a ring of shared-memory stages filled with cp.async.  When there
+// are too few tiles to cover the SMs, the contraction is split over the CTAs of a thread-block
+// cluster (grid z, any size up to 8); each CTA parks its partial tiles in its own shared memory
+// and every CTA of the cluster adds up one slice of the columns over distributed shared memory,
+// in a fixed order.  The epilogue routes each output feature to one of up to four destination
+// tensors, which is how the input projection writes the step's four input buffers in one launch.
 #include <mutex>
 
 #include "gdn_internal.h"
@@ -29,24 +30,26 @@ namespace gdn {
 
 namespace {
 
-constexpr int PM = 128;         // output features per CTA (MMA M, TMEM lanes)
-constexpr int PN = 64;          // activation rows per CTA (MMA N, TMEM columns)
+constexpr int PM = 128;         // output features per weight tile (MMA M, TMEM lanes)
+constexpr int PT = 2;           // weight tiles per CTA: 256 features share one activation tile
+constexpr int PN = 64;          // activation rows per CTA (MMA N, TMEM columns per tile)
 constexpr int PK = 64;          // contraction elements per stage
-constexpr int PSTAGES = 9;      // ring depth (216 KiB: one CTA per SM)
-constexpr int PLAG = 3;         // a stage is refilled PLAG chunks after its MMAs were issued ...
+constexpr int PSTAGES = 5;      // ring depth (200 KiB: one CTA per SM)
+constexpr int PLAG = 1;         // a stage is refilled PLAG chunks after its MMAs were issued ...
 constexpr int PDIST = PSTAGES - PLAG;   // ... so PDIST chunks are in flight
 constexpr int PTHREADS = 256;
-constexpr uint32_t PA_BYTES = PM * PK * 2;   // weight tile, 16 KiB
+constexpr uint32_t PA_BYTES = PM * PK * 2;   // one weight tile, 16 KiB
 constexpr uint32_t PB_BYTES = PN * PK * 2;   // activation tile, 8 KiB
-constexpr uint32_t PSTAGE_BYTES = PA_BYTES + PB_BYTES;
-constexpr uint32_t PRED_BYTES = PM * PN * 4;  // f32 partial tile [PN][PM], aliases the stages
+constexpr uint32_t PSTAGE_BYTES = PT * PA_BYTES + PB_BYTES;
+constexpr uint32_t PRED_BYTES = PT * PM * PN * 4;  // f32 partial tiles [PT][PN][PM] (stages)
 constexpr uint32_t PBAR_OFF = PSTAGES * PSTAGE_BYTES;
 constexpr uint32_t PSMEM = PBAR_OFF + PSTAGES * 8 + 16;
 constexpr int PX_COPIES = PN * (PK / 8) / PTHREADS;   // 16-byte activation copies per thread
 constexpr int PW_UNITS = PA_BYTES / 16 / PTHREADS;    // 16-byte weight copies per thread
 static_assert(PRED_BYTES <= PBAR_OFF, "partial tile must fit in the stage ring");
 static_assert(PX_COPIES * PTHREADS == PN * (PK / 8), "copies must divide evenly over the threads");
-static_assert(PA_BYTES == GDN_PROJ_BLOCK_BYTES, "a packed block is one weight stage");
+static_assert(PA_BYTES == GDN_PROJ_BLOCK_BYTES, "a packed block is one weight tile's stage");
+static_assert(PTHREADS == PT * PM, "the reduction maps one thread to one output feature");
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(g),
@@ -101,20 +104,27 @@ __global__ void proj_pack_kernel(const __nv_bfloat16* __restrict__ W, int N, int
   }
 }
 
-// One pipeline stage: weight block c of this CTA (a contiguous 16 KiB copy: 256 threads x 4 x 16
-// bytes, every warp reading 512 consecutive bytes) and the matching activation tile.
+// One pipeline stage: block c of each of this CTA's weight tiles (contiguous 16 KiB copies: 256
+// threads x 4 x 16 bytes, every warp reading 512 consecutive bytes; a second tile past the end
+// of the packed weight is skipped) and the matching activation tile.
 __device__ __forceinline__ void load_chunk(uint32_t sa, const unsigned char* __restrict__ wblk,
+                                           size_t tile_stride, int ntiles,
                                            const __nv_bfloat16* __restrict__ X, int M, int K,
                                            int m0, int kbase, int c) {
 #pragma unroll
-  for (int i = 0; i < PW_UNITS; ++i) {
-    const uint32_t o = (threadIdx.x + i * PTHREADS) * 16u;
-    cp_async16(sa + o, wblk + (size_t)c * PA_BYTES + o, 16u);
+  for (int t = 0; t < PT; ++t) {
+    if (t < ntiles) {
+#pragma unroll
+      for (int i = 0; i < PW_UNITS; ++i) {
+        const uint32_t o = (threadIdx.x + i * PTHREADS) * 16u;
+        cp_async16(sa + t * PA_BYTES + o, wblk + t * tile_stride + (size_t)c * PA_BYTES + o, 16u);
+      }
+    }
   }
-  load_x(sa + PA_BYTES, X, M, K, m0, kbase + c * PK);
+  load_x(sa + PT * PA_BYTES, X, M, K, m0, kbase + c * PK);
 }
 
-// Grid (ceil(N/PM), ceil(M/PN), ks), cluster (1, 1, ks): CTA z of a cluster takes contraction
+// Grid (ceil(N/(PT*PM)), ceil(M/PN), ks), cluster (1, 1, ks): CTA z of a cluster takes contraction
 // chunks [z*nkc, (z+1)*nkc) and adds up columns [z*PN/ks, (z+1)*PN/ks) (rounded down) of the
 // cluster's tile (ks = 1: a plain launch, no cluster).  One CTA per SM: the stage ring takes
 // most of the shared memory and keeps PDIST chunks in flight.  Every thread copies its share of
@@ -127,10 +137,13 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   extern __shared__ __align__(1024) unsigned char sm[];
   uint64_t* done = reinterpret_cast<uint64_t*>(sm + PBAR_OFF);   // the stage's MMAs completed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + PSTAGES);
-  const int n0 = blockIdx.x * PM, m0 = blockIdx.y * PN;
+  const int n0 = blockIdx.x * PT * PM, m0 = blockIdx.y * PN;
   const int ks = (int)gridDim.z, z = (int)blockIdx.z;
   const int kbase = z * nkc * PK;
-  const unsigned char* wblk = WP + ((size_t)blockIdx.x * (K / PK) + (size_t)z * nkc) * PA_BYTES;
+  const int nt0 = blockIdx.x * PT, ntot = (N + PM - 1) / PM;
+  const int ntiles = min(PT, ntot - nt0);   // weight tiles this CTA holds (the last may hold 1)
+  const size_t tile_stride = (size_t)(K / PK) * PA_BYTES;
+  const unsigned char* wblk = WP + (size_t)nt0 * tile_stride + (size_t)z * nkc * PA_BYTES;
   const int rot = (int)(((unsigned long long)blockIdx.x * nkc / gridDim.x + blockIdx.y * 7ull) %
                         (unsigned)nkc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -139,7 +152,7 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
     for (int i = 0; i < PSTAGES; ++i) tc::mbar_init(done + i, 1);
     tc::mbar_fence_init();
   }
-  if (warp == 0) tc::tmem_alloc(tslot, PN);
+  if (warp == 0) tc::tmem_alloc(tslot, PT * PN);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -150,7 +163,8 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   // group count stays in step with the step index)
 #pragma unroll
   for (int j = 0; j < PDIST; ++j) {
-    if (j < nkc) load_chunk(s0 + j * PSTAGE_BYTES, wblk, X, M, K, m0, kbase, chunk(j));
+    if (j < nkc)
+      load_chunk(s0 + j * PSTAGE_BYTES, wblk, tile_stride, ntiles, X, M, K, m0, kbase, chunk(j));
     cp_async_commit();
   }
   constexpr uint32_t kIdesc = tc::idesc_bf16(PM, PN);
@@ -163,11 +177,17 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
     if (tid == 0 && ok) {
       tc::fence_after_sync();
       const uint32_t sa = s0 + st * PSTAGE_BYTES;
-      const uint64_t da = tc::kstep_desc(sa, PK, 0), db = tc::kstep_desc(sa + PA_BYTES, PK, 0);
+      const uint64_t db = tc::kstep_desc(sa + PT * PA_BYTES, PK, 0);
 #pragma unroll
-      for (int k = 0; k < PK / 16; ++k)
-        tc::mma_bf16(tb, tc::desc_add(da, 256u * k), tc::desc_add(db, 256u * k), kIdesc,
-                     (kc > 0 || k > 0) ? 1u : 0u);
+      for (int t = 0; t < PT; ++t) {
+        if (t < ntiles) {
+          const uint64_t da = tc::kstep_desc(sa + t * PA_BYTES, PK, 0);
+#pragma unroll
+          for (int k = 0; k < PK / 16; ++k)
+            tc::mma_bf16(tb + t * PN, tc::desc_add(da, 256u * k), tc::desc_add(db, 256u * k),
+                         kIdesc, (kc > 0 || k > 0) ? 1u : 0u);
+        }
+      }
       tc::mma_commit(done + st);
     }
     // refill the stage of step kc - PLAG with step kc + PDIST once its MMAs are done: waiting
@@ -177,7 +197,9 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
       const int prev = kc - PLAG;
       if (prev >= 0 && ok && !tc::mbar_wait(done + prev % PSTAGES, (prev / PSTAGES) & 1))
         ok = false;
-      if (ok) load_chunk(s0 + (nxt % PSTAGES) * PSTAGE_BYTES, wblk, X, M, K, m0, kbase, chunk(nxt));
+      if (ok)
+        load_chunk(s0 + (nxt % PSTAGES) * PSTAGE_BYTES, wblk, tile_stride, ntiles, X, M, K, m0,
+                   kbase, chunk(nxt));
     }
     cp_async_commit();
   }
@@ -187,16 +209,19 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   ok = __syncthreads_and(ok) != 0;
   if (!ok && tid == 0 && status) atomicOr(status, GDN_STATUS_TIMEOUT);
   tc::fence_after_sync();
-  // the partial tile, [column][lane] f32, into this CTA's stage ring (free now): warp w holds
-  // TMEM lanes 32*(w%4).. and columns 32*(w/4)..
+  // the partial tiles, [tile][column][lane] f32, into this CTA's stage ring (free now): warp w
+  // holds TMEM lanes 32*(w%4).. of tile w/4 (columns 64*(w/4) ..)
   float* red = reinterpret_cast<float*>(sm);
   if (ok) {
-    const int lq = (warp & 3) * 32, c0 = (warp >> 2) * 32;
-    float v[32];
-    tc::tmem_ld16(tc::taddr(tb, lq, c0), v);
-    tc::tmem_ld16(tc::taddr(tb, lq, c0 + 16), v + 16);
+    const int lq = (warp & 3) * 32, t = warp >> 2;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) red[(c0 + i) * PM + lq + lane] = v[i];
+    for (int h = 0; h < 2; ++h) {
+      float v[32];
+      tc::tmem_ld16(tc::taddr(tb, lq, t * PN + 32 * h), v);
+      tc::tmem_ld16(tc::taddr(tb, lq, t * PN + 32 * h + 16), v + 16);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) red[(t * PN + 32 * h + i) * PM + lq + lane] = v[i];
+    }
   }
   const bool clustered = ks > 1;
   tc::fence_before_sync();
@@ -205,10 +230,10 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   else
     __syncthreads();
   tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tb, PN);
-  // this CTA's column slice: thread -> lane r = tid % 128, columns cw0 + tid/128 + 2j
-  const int r = tid & (PM - 1);
-  const int n = n0 + r;
+  if (warp == 0) tc::tmem_dealloc(tb, PT * PN);
+  // this CTA's column slice: thread -> lane r = tid % 128 of tile tid / 128, every column
+  const int r = tid & (PM - 1), tt = tid >> 7;
+  const int n = n0 + tt * PM + r;
   const int cw0 = z * PN / ks, cw1 = (z + 1) * PN / ks;
   __nv_bfloat16* base = route.ptr[0];
   int seg_start = 0, seg_ld = route.ld[0];
@@ -222,16 +247,17 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   __nv_bfloat16* dst = base + (n - seg_start);
   const size_t ld = (size_t)seg_ld;
   const uint32_t red_s = tc::smem_u32(red);
-  for (int c = cw0 + (tid >> 7); c < cw1; c += PTHREADS / PM) {
+  for (int c = cw0; c < cw1; ++c) {
     const int m = m0 + c;
     if (m >= M || n >= N) continue;
-    const uint32_t off = red_s + (uint32_t)(c * PM + r) * 4u;
+    const int e = (tt * PN + c) * PM + r;
     float s;
     if (clustered) {
       s = 0.f;
+      const uint32_t off = red_s + (uint32_t)e * 4u;
       for (int q = 0; q < ks; ++q) s += ld_cluster_f32(tc::mapa_shared(off, (uint32_t)q));
     } else {
-      s = red[c * PM + r];
+      s = red[e];
     }
     dst[(size_t)m * ld] = __float2bfloat16_rn(s);
   }
@@ -254,7 +280,7 @@ int proj_auto_split(int M, int N, int K) {
   });
   // one CTA per SM: split the contraction while the grid still fits in one wave and every CTA
   // keeps at least a full ring of chunks
-  const long long tiles = (long long)((N + PM - 1) / PM) * ((M + PN - 1) / PN);
+  const long long tiles = (long long)((N + PT * PM - 1) / (PT * PM)) * ((M + PN - 1) / PN);
   const int nk = K / PK;
   int ks = 1;
   for (int c = 2; c <= 8; ++c)
@@ -284,7 +310,8 @@ int launch_proj(const void* x, const void* wp, int M, int N, int K, int ks, cons
   });
   if (attr_err != cudaSuccess) return GDN_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((N + PM - 1) / PM), (unsigned)((M + PN - 1) / PN), (unsigned)ks);
+  cfg.gridDim = dim3((unsigned)((N + PT * PM - 1) / (PT * PM)), (unsigned)((M + PN - 1) / PN),
+                     (unsigned)ks);
   cfg.blockDim = dim3(PTHREADS, 1, 1);
   cfg.dynamicSmemBytes = PSMEM;
   cfg.stream = stream;
