@@ -5,7 +5,8 @@ Headline: batched decode at B=64 rows (K-heads 16, V-heads 48, dk = dv = 128, bf
 f32 state pool of 128 slots), reported as GB/s of recurrent-state traffic (each step reads and
 writes 64 x 48 x 128 x 128 x 4 B = 402.65 MB) and as a fraction of the measured HBM peak.  The
 same JSON line carries the chunked prefill of one T = 4096 sequence (tokens/s, contraction
-TFLOP/s) and the slot compaction on retire (GB/s).  A step is one batched decode step; the
+TFLOP/s), the slot compaction on retire (GB/s), the multi-token and CUDA-graph decode, and the
+bf16 projections around the step (weight-streaming GB/s at B=64, TFLOP/s at 4096 rows).  A step is one batched decode step; the
 state working set (402.65 MB) exceeds the 129 MB L2, so no L2 flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -41,6 +42,8 @@ E2E_RING = 64   # pinned input buffers cycled by the end-to-end lines (64 x 2.1 
 # from one ncu capture at B=64, keyed by the SHA-256 of the kernel source it was taken on.  A
 # changed kernel reports null until it is captured again.
 DECODE_TRAFFIC = {"77a6812566ec1ef2": 352663552}
+# The same for the projection kernel's B=64 input projection (hidden 5120, 16480 features).
+PROJ_IN_TRAFFIC = {"8188d272fe54a75a": 173359104}
 
 
 def _src_sha(name: str) -> str:
@@ -492,6 +495,10 @@ def time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak, reps=2
             "us": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
             "hbm_frac": round(gbs / hbm_peak, 4),
             "tflops": round(2.0 * B * n * k / (ms * 1e-3) / 1e12, 2)}
+    res["decode_in_proj"]["roofline"] = {
+        "bound": "hbm", "achieved": res["decode_in_proj"]["gbs"], "peak": hbm_peak,
+        "unit": "GB/s", "frac": res["decode_in_proj"]["hbm_frac"],
+        "traffic": PROJ_IN_TRAFFIC.get(_src_sha("gdn_proj.cu"))}
     del w_in, w_out, layer
     torch.cuda.empty_cache()
 
@@ -514,8 +521,8 @@ def time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak, reps=2
     res["prefill_in_proj"] = {"rows": T, "features": pn, "hidden": PH, "us": round(ms_p * 1e3, 2),
                               "tflops": round(tf, 1), "bf16_frac": round(tf / bf16_peak, 4)}
     res["hidden_sizes"] = {str(k): v for k, v in synth.PROJ_HIDDEN.items()}
-    res["kernel"] = ("proj_kernel (tcgen05 128x64 tiles, packed weight blocks by bulk copy, "
-                     "cluster split-K)")
+    res["kernel"] = ("proj_kernel: 256 features x 64 rows per CTA (two tcgen05 M=128 x N=64 "
+                     "accumulators), packed weight blocks, cp.async ring, cluster split-K")
     return res
 
 
