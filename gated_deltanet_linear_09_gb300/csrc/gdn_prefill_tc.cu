@@ -38,10 +38,14 @@ constexpr int D = 128;
 // the state kernel brings each in with one bulk copy.  Offsets in bytes.
 constexpr uint32_t R_B3 = 0;                     // [Q~ ; W] rows, 128 x 128: hi 32 KiB, lo 32 KiB
 constexpr uint32_t R_B4 = R_B3 + 65536;          // [P ; K~^T] rows, 192 x 64: hi 24 KiB, lo 24 KiB
-constexpr uint32_t R_UT = R_B4 + 49152;          // f32 [64][128] U~ rows
+constexpr uint32_t R_UT = R_B4 + 49152;          // f32 U~, [column / 4][token][4]
 constexpr uint32_t R_SC = R_UT + 32768;          // f32 e^{gamma_L}
 constexpr uint32_t REC_BYTES = R_SC + 256;       // 147,712 bytes (multiple of 256)
 constexpr uint32_t B3_HALF = 32768, B4_HALF = 24576;
+
+// Float index of U~ element (token t, column col) in its record: [col / 4][t][4], so that 32
+// consecutive tokens' 4-column pieces are 512 contiguous bytes for the writer and the reader.
+__host__ __device__ constexpr int ut_index(int t, int col) { return ((col >> 2) * CH + t) * 4 + (col & 3); }
 
 __device__ __forceinline__ void bar_sync_main() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
 
@@ -62,11 +66,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 
 // Packs 8 floats as split bf16 hi / lo 16-byte units.
 __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
-  __nv_bfloat16 h[8], l[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) tc::split_bf16(v[q], h[q], l[q]);
-  hi = *reinterpret_cast<const uint4*>(h);
-  lo = *reinterpret_cast<const uint4*>(l);
+  tc::split2_bf16(v[0], v[1], hi.x, lo.x);
+  tc::split2_bf16(v[2], v[3], hi.y, lo.y);
+  tc::split2_bf16(v[4], v[5], hi.z, lo.z);
+  tc::split2_bf16(v[6], v[7], hi.w, lo.w);
 }
 
 __device__ __forceinline__ void st_unit(unsigned char* tile, uint32_t off, const uint4& v) {
@@ -75,41 +78,6 @@ __device__ __forceinline__ void st_unit(unsigned char* tile, uint32_t off, const
 
 __device__ __forceinline__ void gst_unit(unsigned char* g, uint32_t off, const uint4& v) {
   *reinterpret_cast<uint4*>(g + off) = v;
-}
-
-// Rows [0,64) of X (f32 [64][XS], each row scaled by rs[row]) -> rows [row0, row0+64) of a
-// 128-column K-major tile image in global memory.  Consecutive threads write consecutive
-// 16-byte units (unit u: row & 7 = u & 7, k-group = (u >> 3) & 15, row group = u >> 7).
-__device__ __forceinline__ void x_rows_to_gtile128(const float* X, const float* rs,
-                                                   unsigned char* ghi, unsigned char* glo, int row0) {
-  for (int u = threadIdx.x; u < 1024; u += blockDim.x) {
-    const int r = ((u >> 7) << 3) + (u & 7), kg = (u >> 3) & 15;
-    const float sc = rs ? rs[r] : 1.f;
-    const float4 a = *reinterpret_cast<const float4*>(X + r * 132 + kg * 8);
-    const float4 b = *reinterpret_cast<const float4*>(X + r * 132 + kg * 8 + 4);
-    const float v[8] = {a.x * sc, a.y * sc, a.z * sc, a.w * sc, b.x * sc, b.y * sc, b.z * sc, b.w * sc};
-    uint4 hh, ll;
-    split8(v, hh, ll);
-    const uint32_t off = (uint32_t)(row0 * 16 * 16) + (uint32_t)u * 16u;   // row0 is a multiple of 8
-    gst_unit(ghi, off, hh);
-    gst_unit(glo, off, ll);
-  }
-}
-
-// Columns of X scaled per token by cs[j] -> a [128 features][64 tokens] K-major tile image in
-// global memory (unit u: feature & 7 = u & 7, token group = (u >> 3) & 7, feature group = u >> 6).
-__device__ __forceinline__ void x_cols_to_gtile64(const float* X, const float* cs,
-                                                  unsigned char* ghi, unsigned char* glo) {
-  for (int u = threadIdx.x; u < 1024; u += blockDim.x) {
-    const int f = ((u >> 6) << 3) + (u & 7), jg = (u >> 3) & 7;
-    float v[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = X[(jg * 8 + q) * 132 + f] * cs[jg * 8 + q];
-    uint4 hh, ll;
-    split8(v, hh, ll);
-    gst_unit(ghi, (uint32_t)u * 16u, hh);
-    gst_unit(glo, (uint32_t)u * 16u, ll);
-  }
 }
 
 // Warp-wide: global chunk -> (sequence, first token, length); false if cu_seqlens is invalid.
@@ -170,155 +138,371 @@ __device__ bool seq_chunk_offset(const int32_t* __restrict__ cu, int num_seqs, i
 }
 
 // ================================================================== intra-chunk kernel
+//
+// One CTA per (chunk, K-head): the K-head's conv / l2norm of k and q and the product
+// D1 = [K;Q] K^T are formed once and serve its r V-heads, which then run one after another
+// (the next V-head's conv, A / P and inverse overlap the current V-head's MMAs).  Every input
+// row the chunk needs (the k, q and v channels of its tokens plus three rows of history) and
+// the conv weights stream into a shared-memory ring with asynchronous copies at the start, so
+// the CTA pays one global-memory round trip instead of one per phase.
 
-constexpr int XS = 132;   // row stride (floats) of the f32 staging tile
-constexpr int AS = 68;    // row stride of the A matrix (16-byte aligned rows)
-constexpr int NTI = 256;  // threads of the intra kernel (8 warps); two CTAs share an SM
+constexpr int AS = 68;    // row stride of the A / T matrix (16-byte aligned rows)
+constexpr int NTI = 512;  // threads of the intra kernel (16 warps), one CTA per SM
+constexpr int RMAX = 4;   // V-heads per K-head on the tensor-core path
+constexpr int NROW = CH + 3;   // input rows per chunk: three of history, then the 64 tokens
 
-// Shared memory, ~100 KB so that two CTAs fit on one SM.  Regions are reused along the kernel:
-//   A1  [0, 64K)   : [K;Q] split-bf16 operand of MMA1  (hi K | hi Q | lo K | lo Q, 16 KiB each);
-//                    after MMA1: (beta e^g K)^T hi/lo in the Q quarters, (beta V)^T hi/lo in the
-//                    K quarters (each [128 x 64] tile is exactly 16 KiB).
-//   X   [64K, +33792): f32 staging [64][XS]; after the V tiles: A [64][AS] (17,408 B) followed by
-//                    the B2 tile (T rows, hi 8 KiB + lo 8 KiB); after MMA2: the W readout.
+// TMEM columns of the intra kernel (lanes 0-127): D1 = [K;Q] K^T, then per V-head the two
+// row-major products of the A operand [T diag(beta e^gamma) ; T diag(beta)] (128 x 64) with
+// K^T (W in lanes 0-63) and with V^T (U~ in lanes 64-127).
+constexpr uint32_t TI_D1 = 0, TI_W = 128, TI_U = 256, TI_COLS = 512;
+
+// Input ring: one slot per input tensor (k, q, then the V-heads' v), each NROW rows of 128
+// channels followed by the 128 channels' conv weights; 4 slots of bf16 or 2 of f32.
+template <typename T>
+struct InRing {
+  static constexpr uint32_t ROW = 128 * sizeof(T);
+  static constexpr uint32_t PITCH = ROW + 16;   // one unit of padding: conflict-free column reads
+  static constexpr uint32_t W_OFF = NROW * PITCH;
+  static constexpr uint32_t SLOT = W_OFF + 128 * 4 * sizeof(T);
+  static constexpr int NSLOT = 8 / (int)sizeof(T);
+};
+constexpr uint32_t IN_BYTES = 4 * InRing<__nv_bfloat16>::SLOT > 2 * InRing<float>::SLOT
+                                  ? 4 * InRing<__nv_bfloat16>::SLOT : 2 * InRing<float>::SLOT;
+
+// Shared memory (one CTA per SM):
+//   A1  [K;Q] split-bf16 operand, 128 rows x 128 K: hi (K rows | Q rows) then lo     64 KiB
+//   VT  V rows of the current V-head, 64 x 128 K, hi then lo                         32 KiB
+//   B2  [T diag(beta e^gamma) ; T diag(beta)] rows, 128 x 64 K, hi then lo            32 KiB
+//   IN  the input ring                                                             71 KiB
+//   AT  f32 [64][AS]: A of the V-head, overwritten by T = (I + A)^{-1}               17 KiB
+//   VEC f32 [RMAX][5][64]: per V-head gamma, beta, e^gamma, e^{gamma_L - gamma}, beta e^gamma
+//   PART f32 [2][64]: per token, the two warps' partial sums of squares of the l2norm
 struct IntraSmem {
   static constexpr uint32_t A1 = 0;
   static constexpr uint32_t K_HI = 0, Q_HI = 16384, K_LO = 32768, Q_LO = 49152;
-  static constexpr uint32_t X = 65536;
-  static constexpr uint32_t AM = X;                        // aliases X
-  static constexpr uint32_t B2 = X + 4 * 64 * AS;          // aliases X (17,408 B in)
-  static constexpr uint32_t VEC = X + 4 * 64 * XS;         // f32 gam, bet, eg, dec, bgk [5][64]
-  static constexpr uint32_t BAR = VEC + 4 * 5 * 64;        // mbarrier
-  static constexpr uint32_t MISC = BAR + 16;               // tmem slot, flags
+  static constexpr uint32_t VT = 65536;
+  static constexpr uint32_t B2 = VT + 32768;
+  static constexpr uint32_t IN = B2 + 32768;
+  static constexpr uint32_t AT = IN + IN_BYTES;
+  static constexpr uint32_t VEC = AT + 4 * 64 * AS;
+  static constexpr uint32_t PART = VEC + 4 * RMAX * 5 * 64;  // f32 [2][64] l2norm partial sums
+  static constexpr uint32_t BAR = PART + 4 * 2 * 64;         // 2 mbarriers
+  static constexpr uint32_t MISC = BAR + 16;                  // tmem slot, flags
   static constexpr uint32_t BYTES = MISC + 64;
 };
-static_assert(IntraSmem::B2 + 16384 <= IntraSmem::VEC, "A and B2 must fit in the staging tile");
+static_assert(IntraSmem::BYTES <= 227 * 1024, "intra kernel shared memory");
 
-// conv + SiLU of 128 channels [cb, cb+128) over the chunk's tokens into X (rows >= L zero), split
-// into a load step (all loads in flight, results in registers) and a compute step, so that the
-// next channel group's loads overlap the current group's processing.
-// Thread t: channel t & 127, tokens [32 (t >> 7), +32).
-struct ConvIn {
-  float w[4];
-  float hist[3];
-  float xs[32];
-};
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(tc::smem_u32(sdst)), "l"(gsrc),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+// Waits until at most n of this thread's committed copy groups are still in flight (n <= 3).
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;\n" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;\n" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;\n" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 3;\n" ::: "memory"); break;
+  }
+}
 
+// Issues (one commit group) the copies of 128 input channels [cb, cb+128) of the chunk: ring row
+// m holds the raw input at position p0 - 3 + m of the sequence (p0 = the chunk's first position);
+// positions before the sequence come from the slot's conv state when init, else zero; positions
+// past the sequence are zero.  Then the channels' conv weights.
 template <typename T>
-__device__ __forceinline__ void conv_load(const KDims& d, const T* __restrict__ qkv,
-                                          const T* __restrict__ conv_w, const T* __restrict__ cs,
-                                          bool init, int cb, int seq_start, int seq_len, int t0,
-                                          int L, ConvIn& in) {
-  const int tid = threadIdx.x;
-  const int f = tid & 127, i0 = (tid >> 7) * 32;
-  const int ch = cb + f;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) in.w[q] = Act<T>::ldg(conv_w + (size_t)ch * 4 + q);
-  const int p0 = (t0 - seq_start) + i0;   // position of token i0 inside its sequence
-  // Every load reads a valid address (rows clamped into the sequence / the conv state) and is
-  // selected afterwards, so all of them can be in flight at once.
-#pragma unroll
-  for (int m = 0; m < 3; ++m) {
+__device__ __forceinline__ void ring_issue(const KDims& d, const T* __restrict__ qkv,
+                                           const T* __restrict__ conv_w, const T* __restrict__ cs,
+                                           bool init, int cb, int seq_start, int seq_len, int p0,
+                                           unsigned char* slot) {
+  using R = InRing<T>;
+  constexpr int UPR = R::ROW / 16;   // 16-byte units per row
+  for (int q = threadIdx.x; q < NROW * UPR; q += NTI) {
+    const int m = q / UPR, uu = q - m * UPR;
     const int p = p0 - 3 + m;
-    const int pr = min(max(p, 0), seq_len - 1);
-    const int pc = min(max(p, -3), -1);
-    const float xq = Act<T>::ldg(qkv + (size_t)(seq_start + pr) * d.cqkv + ch);
-    const float xc = Act<T>::ldg(cs + (size_t)(3 + pc) * d.cqkv + ch);
-    in.hist[m] = (p >= seq_len) ? 0.f : (p >= 0 ? xq : (init ? xc : 0.f));
+    const T* src = qkv;
+    uint32_t bytes = 0;
+    if (p >= 0 && p < seq_len) {
+      src = qkv + (size_t)(seq_start + p) * d.cqkv + cb;
+      bytes = 16;
+    } else if (p < 0 && init) {
+      src = cs + (size_t)(3 + p) * d.cqkv + cb;
+      bytes = 16;
+    }
+    cp_async16(slot + m * R::PITCH + uu * 16, reinterpret_cast<const unsigned char*>(src) + (bytes ? uu * 16 : 0),
+               bytes);
   }
-#pragma unroll
-  for (int k = 0; k < 32; ++k)
-    in.xs[k] = Act<T>::ldg(qkv + (size_t)(t0 + min(i0 + k, L - 1)) * d.cqkv + ch);
+  for (int q = threadIdx.x; q < (int)(128 * 4 * sizeof(T) / 16); q += NTI)
+    cp_async16(slot + R::W_OFF + q * 16,
+               reinterpret_cast<const unsigned char*>(conv_w + (size_t)cb * 4) + q * 16, 16);
+  cp_async_commit();
 }
 
-// The same, into registers (tokens i0..i0+31 of channel f, zero past L).
-__device__ __forceinline__ void conv_compute_regs(const ConvIn& in, int L, float* y) {
-  const int i0 = (threadIdx.x >> 7) * 32;
-  float xm3 = in.hist[0], xm2 = in.hist[1], xm1 = in.hist[2];
+__device__ __forceinline__ void unpack_unit(const uint4& u, float* f, __nv_bfloat16*) {
+  const uint32_t q[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    float acc = in.w[3] * in.xs[k];
-    acc = fmaf(in.w[0], xm3, acc);
-    acc = fmaf(in.w[1], xm2, acc);
-    acc = fmaf(in.w[2], xm1, acc);
-    y[k] = (i0 + k < L) ? silu_fast(acc) : 0.f;
-    xm3 = xm2;
-    xm2 = xm1;
-    xm1 = in.xs[k];
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q[i]));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ void unpack_unit(const uint4& u, float* f, float*) {
+  f[0] = __uint_as_float(u.x);
+  f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z);
+  f[3] = __uint_as_float(u.w);
+}
+
+// Thread layout of the conv: token t = 8 (warp % 8) + lane % 8 and the 16 channels
+// [16 cg, 16 cg + 16), cg = 4 (warp / 8) + lane / 8.  A warp holds 8 consecutive tokens x 64
+// channels, so its ring reads (padded rows) and its 16-byte stores into K-major tiles (8
+// distinct rows per 128-byte line) are free of bank conflicts.
+__device__ __forceinline__ int conv_t() { return 8 * ((threadIdx.x >> 5) & 7) + (threadIdx.x & 7); }
+__device__ __forceinline__ int conv_cg() { return 4 * (threadIdx.x >> 8) + ((threadIdx.x >> 3) & 3); }
+
+// y[e] = SiLU(sum_j w[c][j] x[t - 3 + j][c]), c = 16 cg + e, from a ring slot (zero past L).
+template <typename T>
+__device__ __forceinline__ void conv_slot(const unsigned char* slot, int L, float* y) {
+  using R = InRing<T>;
+  constexpr int CPU = 16 / (int)sizeof(T);   // channels per 16-byte unit (8 bf16, 4 f32)
+  constexpr int UPT = 16 / CPU;              // units per thread
+  const int t = conv_t(), cg = conv_cg();
+#pragma unroll
+  for (int u = 0; u < UPT; ++u) {
+    const int unit = cg * UPT + u;
+    float wf[4 * CPU];   // [channel][tap]
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      unpack_unit(*reinterpret_cast<const uint4*>(slot + R::W_OFF + unit * 64 + q * 16), wf + q * CPU,
+                  (T*)nullptr);
+    float xf[4][CPU];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      unpack_unit(*reinterpret_cast<const uint4*>(slot + (t + m) * R::PITCH + unit * 16), xf[m],
+                  (T*)nullptr);
+#pragma unroll
+    for (int e = 0; e < CPU; ++e) {
+      float acc = wf[e * 4 + 3] * xf[3][e];
+      acc = fmaf(wf[e * 4 + 0], xf[0][e], acc);
+      acc = fmaf(wf[e * 4 + 1], xf[1][e], acc);
+      acc = fmaf(wf[e * 4 + 2], xf[2][e], acc);
+      y[u * CPU + e] = (t < L) ? silu_fast(acc) : 0.f;
+    }
   }
 }
 
-__device__ __forceinline__ void conv_compute(const ConvIn& in, int L, float* X) {
-  const int tid = threadIdx.x;
-  const int f = tid & 127, i0 = (tid >> 7) * 32;
-  float xm3 = in.hist[0], xm2 = in.hist[1], xm1 = in.hist[2];
+// l2 normalisation (times scale) of the thread's 16 values: the 8 threads holding token t's 128
+// channels sit in two warps; each warp sums over its 64 channels with shuffles, the two partial
+// sums meet in shared memory.  Contains a barrier.
+__device__ __forceinline__ void l2norm16(float* y, float* part, float eps, float scale) {
+  const int t = conv_t(), lane = threadIdx.x & 31;
+  float ss = 0.f;
 #pragma unroll
-  for (int k = 0; k < 32; ++k) {
-    float acc = in.w[3] * in.xs[k];
-    acc = fmaf(in.w[0], xm3, acc);
-    acc = fmaf(in.w[1], xm2, acc);
-    acc = fmaf(in.w[2], xm1, acc);
-    X[(i0 + k) * XS + f] = (i0 + k < L) ? silu_fast(acc) : 0.f;
-    xm3 = xm2;
-    xm2 = xm1;
-    xm1 = in.xs[k];
-  }
+  for (int e = 0; e < 16; ++e) ss = fmaf(y[e], y[e], ss);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 8);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+  if (lane < 8) part[(threadIdx.x >> 8) * 64 + t] = ss;
+  __syncthreads();
+  const float inv = scale * rsqrtf(part[t] + part[64 + t] + eps);
+#pragma unroll
+  for (int e = 0; e < 16; ++e) y[e] *= inv;
 }
 
-// Per-row l2 normalisation of X (64 rows x 128), times scale.
-// Warp w normalises rows w, w + 8, ..., all eight at once (their reductions interleave).
-__device__ __forceinline__ void l2norm_rows(float* X, float eps, float scale) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int RPW = CH / (NTI / 32);
-  float4 v[RPW];
-  float ss[RPW];
+// The thread's 16 values of row t, split, into a 128-column K-major tile (shared or global):
+// two 16-byte units.
+__device__ __forceinline__ void put_row16(unsigned char* hi, unsigned char* lo, const float* v) {
+  const int t = conv_t(), cg = conv_cg();
 #pragma unroll
-  for (int m = 0; m < RPW; ++m) {
-    v[m] = *reinterpret_cast<const float4*>(X + (warp + m * (NTI / 32)) * XS + 4 * lane);
-    ss[m] = v[m].x * v[m].x + v[m].y * v[m].y + v[m].z * v[m].z + v[m].w * v[m].w;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-    for (int m = 0; m < RPW; ++m) ss[m] += __shfl_xor_sync(0xffffffffu, ss[m], off);
-#pragma unroll
-  for (int m = 0; m < RPW; ++m) {
-    const float inv = scale * rsqrtf(ss[m] + eps);
-    *reinterpret_cast<float4*>(X + (warp + m * (NTI / 32)) * XS + 4 * lane) =
-        make_float4(v[m].x * inv, v[m].y * inv, v[m].z * inv, v[m].w * inv);
-  }
-}
-
-// Rows [0,64) of X -> rows [0,64) of a 128-column K-major shared tile (hi / lo quarter).
-// Unit u: row & 7 = u & 7, k-group = (u >> 3) & 15, row group = u >> 7 (conflict-free stores).
-__device__ __forceinline__ void x_rows_to_tile(const float* X, unsigned char* hi, unsigned char* lo) {
-  for (int u = threadIdx.x; u < 1024; u += NTI) {
-    const int r = ((u >> 7) << 3) + (u & 7), kg = (u >> 3) & 15;
-    const float4 a = *reinterpret_cast<const float4*>(X + r * XS + kg * 8);
-    const float4 b = *reinterpret_cast<const float4*>(X + r * XS + kg * 8 + 4);
-    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  for (int u = 0; u < 2; ++u) {
     uint4 hh, ll;
-    split8(v, hh, ll);
-    st_unit(hi, (uint32_t)u * 16u, hh);
-    st_unit(lo, (uint32_t)u * 16u, ll);
+    split8(v + 8 * u, hh, ll);
+    const uint32_t off = tc::kmajor_off(t, 16 * cg + 8 * u, 128);
+    *reinterpret_cast<uint4*>(hi + off) = hh;
+    *reinterpret_cast<uint4*>(lo + off) = ll;
   }
 }
 
-// (scale_j * K_j)^T tile [128 features][64 tokens] built from the K rows of A1 (hi + lo, about
-// 16 significant bits), written into other shared memory (hi / lo).
-__device__ __forceinline__ void a1k_cols_to_tile(const unsigned char* khi, const unsigned char* klo,
-                                                 const float* scale, unsigned char* hi,
-                                                 unsigned char* lo) {
-  for (int u = threadIdx.x; u < 1024; u += NTI) {
-    const int f = ((u >> 6) << 3) + (u & 7), jg = (u >> 3) & 7;
-    float v[8];
+// The gates of one V-head over the chunk (warp-wide, 2 tokens per lane): gamma (cumulative g
+// inside the chunk), beta (0 past L) and the derived per-token scales, into vec[5][64]; returns
+// gamma_L on every lane.
+template <typename T>
+__device__ __forceinline__ float chunk_gates(const KDims& d, const float* __restrict__ A_log,
+                                             const float* __restrict__ dt_bias,
+                                             const T* __restrict__ a, const T* __restrict__ b,
+                                             int h, int t0, int L, float* vec) {
+  const int lane = threadIdx.x & 31;
+  float g2[2], b2[2];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int j = jg * 8 + q;
-      const uint32_t off = tc::kmajor_off(j, f, 128);
-      const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(khi + off)) +
-                       __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(klo + off));
-      v[q] = kv * scale[j];
+  for (int q = 0; q < 2; ++q) {
+    const int i = 2 * lane + q;
+    const int ic = min(i, L - 1);
+    gates(__ldg(A_log + h), __ldg(dt_bias + h), Act<T>::ldg(a + (size_t)(t0 + ic) * d.Hv + h),
+          Act<T>::ldg(b + (size_t)(t0 + ic) * d.Hv + h), g2[q], b2[q]);
+    if (i >= L) {
+      g2[q] = 0.f;
+      b2[q] = 0.f;
+    }
+  }
+  const float pair = g2[0] + g2[1];
+  float incl = pair;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const float gm0 = incl - pair + g2[0], gm1 = incl;
+  const float gsel = ((L - 1) & 1) ? gm1 : gm0;
+  const float gL = __shfl_sync(0xffffffffu, gsel, (L - 1) >> 1);
+  float* gam = vec;
+  float* bet = vec + 64;
+  float* eg = vec + 128;
+  float* dec = vec + 192;
+  float* bgk = vec + 256;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int i = 2 * lane + q;
+    const float gm = q ? gm1 : gm0;
+    const float e = expf(gm);
+    gam[i] = gm;
+    bet[i] = b2[q];
+    eg[i] = e;
+    dec[i] = i < L ? expf(gL - gm) : 0.f;
+    bgk[i] = b2[q] * e;
+  }
+  return gL;
+}
+
+// sum_q row[q] * col[q * cs .. + 3] over 16 terms: four adjacent outputs (row and col 16-byte
+// aligned).
+__device__ __forceinline__ float4 dot16x4(const float* row, const float* col, int cs) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int q = 0; q < 16; q += 4) {
+    const float4 r4 = *reinterpret_cast<const float4*>(row + q);
+    const float rq[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 c4 = *reinterpret_cast<const float4*>(col + (q + k) * cs);
+      acc.x = fmaf(rq[k], c4.x, acc.x);
+      acc.y = fmaf(rq[k], c4.y, acc.y);
+      acc.z = fmaf(rq[k], c4.z, acc.z);
+      acc.w = fmaf(rq[k], c4.w, acc.w);
+    }
+  }
+  return acc;
+}
+__device__ __forceinline__ void add4(float4& a, const float4& b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
+__device__ __forceinline__ float4 neg4(const float4& a) { return make_float4(-a.x, -a.y, -a.z, -a.w); }
+
+// Scratch block q (q < 4) of the inverse: the upper blocks (0,1), (0,2), (0,3), (1,2) of M, which
+// hold only zeros of A and are never read as T.
+__device__ __forceinline__ float* xblk(float* M, int q) {
+  return M + (q < 3 ? 16 * (q + 1) : 16 * 2 + 16 * AS);
+}
+
+// In place: M holds the strictly lower-triangular 64 x 64 A (f32, row stride AS, zero on and
+// above the diagonal) on entry and the lower blocks of T = (I + A)^{-1} on exit (the upper
+// blocks are then undefined; readers mask them).  In 16 x 16 blocks (block (i, k) = rows 16i..,
+// columns 16k..):
+//   1. the diagonal inverses D_b = (I + A_bb)^{-1} by forward substitution (four warps, one
+//      column per lane);
+//   2. the two 32 x 32 diagonal halves: T_10 = -D_1 (A_10 D_0), T_32 = -D_3 (A_32 D_2);
+//   3. the 32 x 32 off-diagonal half, -T2 (A21 T1) with T1, T2 the halves of step 2: first
+//      Y = A21 T1, then T_ik = -sum_m T2_im Y_mk.
+// Each block of A is read before T overwrites it.  Five barriers; ends with one.
+__device__ __forceinline__ void tri_inverse(float* M) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp < 4) {
+    const int b = warp, c = lane & 15;
+    float* mb = M + (16 * b) * AS + 16 * b;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      // x_i = [i == c] - sum_{m<i} A_im x_m; A_im = 0 for m >= i and x_m = 0 for m >= i, so
+      // the sum may run over whole groups of four
+      float p0 = (i == c) ? 1.f : 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+      for (int m = 0; m < i; m += 4) {
+        const float4 a4 = *reinterpret_cast<const float4*>(mb + i * AS + m);
+        p0 = fmaf(-a4.x, x[m], p0);
+        p1 = fmaf(-a4.y, x[m + 1], p1);
+        p2 = fmaf(-a4.z, x[m + 2], p2);
+        p3 = fmaf(-a4.w, x[m + 3], p3);
+      }
+      x[i] = (p0 + p1) + (p2 + p3);
+    }
+    __syncwarp();
+    if (lane < 16) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mb[i * AS + c] = x[i];
+    }
+  }
+  __syncthreads();
+  // steps 2 and 3: thread e computes columns [4 cq, 4 cq + 4) of row rr of a block
+  if (tid < 128) {  // step 2: X = A_{bi,bi-1} D_{bi-1} for bi = 1, 3 (scratch blocks 0, 1)
+    const int which = tid >> 6, rr = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+    const int bi = which ? 3 : 1, bk = bi - 1;
+    *reinterpret_cast<float4*>(xblk(M, which) + rr * AS + c4) =
+        dot16x4(M + (16 * bi + rr) * AS + 16 * bk, M + (16 * bk) * AS + 16 * bk + c4, AS);
+  }
+  __syncthreads();
+  if (tid < 128) {  //         T_{bi,bi-1} = -D_bi X
+    const int which = tid >> 6, rr = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+    const int bi = which ? 3 : 1, bk = bi - 1;
+    *reinterpret_cast<float4*>(M + (16 * bi + rr) * AS + 16 * bk + c4) =
+        neg4(dot16x4(M + (16 * bi + rr) * AS + 16 * bi, xblk(M, which) + c4, AS));
+  }
+  __syncthreads();
+  // step 3: blocks (bi, bk), bi in {2, 3}, bk in {0, 1}:
+  //   Y_{bi,bk} = sum_{m=bk}^{1} A_{bi,m} T_{m,bk}  (scratch block (bi - 2) * 2 + bk)
+  if (tid < 256) {
+    const int blk = tid >> 6, rr = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+    const int bi = 2 + (blk >> 1), bk = blk & 1;
+    float4 acc = dot16x4(M + (16 * bi + rr) * AS + 16 * bk, M + (16 * bk) * AS + 16 * bk + c4, AS);
+    if (bk == 0) add4(acc, dot16x4(M + (16 * bi + rr) * AS + 16, M + 16 * AS + c4, AS));
+    *reinterpret_cast<float4*>(xblk(M, blk) + rr * AS + c4) = acc;
+  }
+  __syncthreads();
+  //   T_{bi,bk} = -sum_{m=2}^{bi} T_{bi,m} Y_{m,bk}
+  if (tid < 256) {
+    const int blk = tid >> 6, rr = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+    const int bi = 2 + (blk >> 1), bk = blk & 1;
+    float4 acc = dot16x4(M + (16 * bi + rr) * AS + 32, xblk(M, bk) + c4, AS);
+    if (bi == 3) add4(acc, dot16x4(M + (16 * bi + rr) * AS + 48, xblk(M, 2 + bk) + c4, AS));
+    *reinterpret_cast<float4*>(M + (16 * bi + rr) * AS + 16 * bk + c4) = neg4(acc);
+  }
+  __syncthreads();
+}
+
+// [T diag(cw) ; T diag(cu)] -> the split-bf16 K-major A operand (128 rows x 64 K) of D2.
+// Unit u: row & 7 = u & 7, k-group = (u >> 3) & 7, row group = u >> 6 (consecutive 16-byte
+// units); entries above the diagonal are zero.
+__device__ __forceinline__ void t_to_b2(const float* Tm, const float* cw, const float* cu,
+                                        unsigned char* hi, unsigned char* lo) {
+  for (int u = threadIdx.x; u < 1024; u += NTI) {
+    const int row = ((u >> 6) << 3) + (u & 7), jg = (u >> 3) & 7;
+    const int i = row & 63;
+    const float* sc = row < 64 ? cw : cu;
+    float v[8];
+    if ((jg >> 1) <= (i >> 4)) {
+      const float4 a = *reinterpret_cast<const float4*>(Tm + i * AS + 8 * jg);
+      const float4 b = *reinterpret_cast<const float4*>(Tm + i * AS + 8 * jg + 4);
+      const float t8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = (8 * jg + q <= i) ? t8[q] * sc[8 * jg + q] : 0.f;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = 0.f;
     }
     uint4 hh, ll;
     split8(v, hh, ll);
@@ -328,7 +512,7 @@ __device__ __forceinline__ void a1k_cols_to_tile(const unsigned char* khi, const
 }
 
 template <typename T>
-__global__ void __launch_bounds__(NTI, 2)
+__global__ void __launch_bounds__(NTI, 1)
 tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict__ dt_bias,
                 const T* __restrict__ conv_w, const T* __restrict__ conv_state, int num_slots,
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ slot_idx,
@@ -337,26 +521,25 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
                 float* __restrict__ ws, int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
   using S = IntraSmem;
+  using R = InRing<T>;
   unsigned char* a1 = sm + S::A1;
-  float* X = reinterpret_cast<float*>(sm + S::X);
-  float* Am = reinterpret_cast<float*>(sm + S::AM);
-  unsigned char* b2h = sm + S::B2;
-  unsigned char* b2l = b2h + 8192;
-  float* gam = reinterpret_cast<float*>(sm + S::VEC);
-  float* bet = gam + 64;
-  float* eg = bet + 64;
-  float* dec = eg + 64;
-  float* bgk = dec + 64;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S::BAR);
+  unsigned char* vt = sm + S::VT;
+  unsigned char* b2 = sm + S::B2;
+  unsigned char* ring = sm + S::IN;
+  float* At = reinterpret_cast<float*>(sm + S::AT);
+  float* vecs = reinterpret_cast<float*>(sm + S::VEC);
+  float* part = reinterpret_cast<float*>(sm + S::PART);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S::BAR);   // [0] D1, [1] D2
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
   int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);   // ok, t0, L, seq, seq_start, abort
 
-  const int c = blockIdx.x, h = blockIdx.y;
+  const int c = blockIdx.x, kh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = d.r, h0 = kh * r;
   if (warp == 0) {
     int seq, t0 = 0, len = 0, ss = 0;
     const bool ok = find_chunk(cu, num_seqs, total, c, seq, t0, len, ss);
-    if (lane == 0 && !ok && c == 0 && h == 0) set_status(status, GDN_STATUS_BAD_SEQLENS);
+    if (lane == 0 && !ok && c == 0 && kh == 0) set_status(status, GDN_STATUS_BAD_SEQLENS);
     if (lane == 0) {
       sh[0] = ok && seq >= 0;
       sh[1] = t0;
@@ -375,145 +558,150 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   const bool valid = s >= 0 && s < num_slots;
   const bool init = valid && has_init != nullptr && __ldg(has_init + seq) != 0;
   const T* cs = conv_state + (size_t)(valid ? s : 0) * 3 * d.cqkv;
-  const int kh = h / d.r;
-  unsigned char* rec = reinterpret_cast<unsigned char*>(ws) + ((size_t)c * d.Hv + h) * REC_BYTES;
-  float* rec_ut = reinterpret_cast<float*>(rec + R_UT);
+  auto rec_of = [&](int j) {
+    return reinterpret_cast<unsigned char*>(ws) + ((size_t)c * d.Hv + h0 + j) * REC_BYTES;
+  };
 
-  // K inputs in flight while the gates are formed
-  ConvIn cin;
-  conv_load<T>(d, qkv, conv_w, cs, init, d.Hk * D + kh * D, seq_start, seq_len, t0, L, cin);
-  if (tid == 0) {
+  // ---- every input tensor of the chunk into the ring: k, q, v of V-head 0, 1, ... (tensor i in
+  // slot i % NSLOT; later tensors as slots free up)
+  const int ntens = 2 + r;
+  auto tens_base = [&](int i) {
+    return i == 0 ? d.Hk * D + kh * D : (i == 1 ? kh * D : 2 * d.Hk * D + (h0 + i - 2) * D);
+  };
+  auto slot_of = [&](int i) { return ring + (i % R::NSLOT) * R::SLOT; };
+  const int p0 = t0 - seq_start;
+  int issued = 0;
+  for (; issued < min(ntens, R::NSLOT); ++issued)
+    ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), seq_start, seq_len, p0, slot_of(issued));
+  // waits for tensor i's copies (all threads), then a barrier makes every thread's copies visible
+  auto ring_wait = [&](int i) {
+    cp_async_wait_pending(issued - 1 - i);
+    __syncthreads();
+  };
+  if (tid == 32) {
     tc::mbar_init(bar, 1);
+    tc::mbar_init(bar + 1, 1);
     tc::mbar_fence_init();
   }
-  if (warp == 0) tc::tmem_alloc(tslot, 256);
-
-  // ---- gates of the chunk: gamma (cumulative g), beta and the derived per-token scales
-  if (warp == 0) {
-    float g2[2], b2[2];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int i = 2 * lane + q;
-      const int ic = min(i, L - 1);
-      gates(__ldg(A_log + h), __ldg(dt_bias + h), Act<T>::ldg(a + (size_t)(t0 + ic) * d.Hv + h),
-            Act<T>::ldg(b + (size_t)(t0 + ic) * d.Hv + h), g2[q], b2[q]);
-      if (i >= L) {
-        g2[q] = 0.f;
-        b2[q] = 0.f;
-      }
-    }
-    const float pair = g2[0] + g2[1];
-    float incl = pair;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const float ex = incl - pair;
-    gam[2 * lane] = ex + g2[0];
-    gam[2 * lane + 1] = ex + g2[0] + g2[1];
-    bet[2 * lane] = b2[0];
-    bet[2 * lane + 1] = b2[1];
+  if (warp == 1) tc::tmem_alloc(tslot, TI_COLS);
+  if (warp >= 2 && warp - 2 < r) {
+    const int j = warp - 2;
+    const float gL = chunk_gates<T>(d, A_log, dt_bias, a, b, h0 + j, t0, L, vecs + j * 320);
+    if (lane == 0) *reinterpret_cast<float*>(rec_of(j) + R_SC) = expf(gL);
   }
-  __syncthreads();
-  const float gL = gam[L - 1];
-  if (tid < CH) {
-    eg[tid] = expf(gam[tid]);
-    dec[tid] = tid < L ? expf(gL - gam[tid]) : 0.f;
-    bgk[tid] = bet[tid] * expf(gam[tid]);
-  }
+  const int tt = conv_t();
+  float y[16];   // conv outputs of token tt, channels [16 cg, 16 cg + 16)
 
-  // ---- K: conv, l2norm, A1 K rows, K~^T rows of B4
-  conv_compute(cin, L, X);
-  conv_load<T>(d, qkv, conv_w, cs, init, kh * D, seq_start, seq_len, t0, L, cin);   // Q, in flight
-  __syncthreads();
-  l2norm_rows(X, d.l2_eps, 1.0f);
-  __syncthreads();
-  x_rows_to_tile(X, a1 + S::K_HI, a1 + S::K_LO);
-  x_cols_to_gtile64(X, dec, rec + R_B4 + 8192, rec + R_B4 + B4_HALF + 8192);   // rows 64..191
-  __syncthreads();
-  // ---- Q: conv, l2norm (times q_scale), A1 Q rows, Q~ rows of B3
-  conv_compute(cin, L, X);
-  conv_load<T>(d, qkv, conv_w, cs, init, 2 * d.Hk * D + h * D, seq_start, seq_len, t0, L, cin);  // V
-  __syncthreads();
-  l2norm_rows(X, d.l2_eps, d.q_scale);
-  __syncthreads();
-  x_rows_to_tile(X, a1 + S::Q_HI, a1 + S::Q_LO);
-  x_rows_to_gtile128(X, eg, rec + R_B3, rec + R_B3 + B3_HALF, 0);
+  // ---- K: conv, l2norm, A1 K rows
+  ring_wait(0);   // also publishes the gates
+  conv_slot<T>(slot_of(0), L, y);
+  l2norm16(y, part, d.l2_eps, 1.0f);
+  put_row16(a1 + S::K_HI, a1 + S::K_LO, y);
+  // ---- Q: conv, l2norm (times q_scale), A1 Q rows and per V-head the Q~ rows of B3
+  ring_wait(1);   // also: K rows complete, slot 0 and the partial sums free
+  if (issued < ntens) {
+    ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), seq_start, seq_len, p0, slot_of(issued));
+    ++issued;
+  }
+  conv_slot<T>(slot_of(1), L, y);
+  l2norm16(y, part, d.l2_eps, d.q_scale);
+  put_row16(a1 + S::Q_HI, a1 + S::Q_LO, y);
+  for (int j = 0; j < r; ++j) {
+    const float e = vecs[j * 320 + 128 + tt];
+    float v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = y[q] * e;
+    unsigned char* rec = rec_of(j);
+    put_row16(rec + R_B3, rec + R_B3 + B3_HALF, v);
+  }
+  // per V-head K~^T = (diag(e^{gamma_L - gamma}) K)^T rows of B4, from the K tile (hi + lo carry
+  // about 16 significant bits): unit (feature f, 8 tokens), consecutive threads take consecutive
+  // features, so every warp stores whole 128-byte lines
+  for (int u = tid; u < 1024; u += NTI) {
+    const int f = u & 127, jg = u >> 7;
+    float kx[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t off = tc::kmajor_off(8 * jg + q, f, 128);
+      kx[q] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(a1 + S::K_HI + off)) +
+              __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(a1 + S::K_LO + off));
+    }
+    const uint32_t off = 8192u + (uint32_t)(f >> 3) * 1024u + (uint32_t)jg * 128u + (uint32_t)(f & 7) * 16u;
+    for (int j = 0; j < r; ++j) {
+      const float* dec = vecs + j * 320 + 192 + 8 * jg;
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = kx[q] * dec[q];
+      uint4 hh, ll;
+      split8(v, hh, ll);
+      unsigned char* rec = rec_of(j);
+      gst_unit(rec + R_B4, off, hh);
+      gst_unit(rec + R_B4 + B4_HALF, off, ll);
+    }
+  }
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tb = *tslot;
-  // ---- D1 = [K;Q] K^T  (cols [0,64)); A1's hi quarters [K|Q] and lo quarters form 128-row tiles
+  // ---- D1 = [K;Q] K^T  (columns [0,64)); A1's hi quarters [K|Q] and lo quarters are 128-row tiles
   if (tid == 0) {
     const uint32_t id = tc::idesc_bf16(128, 64);
-    const uint32_t ah = tc::smem_u32(a1 + S::K_HI), al = tc::smem_u32(a1 + S::K_LO);
-    const uint64_t dh = tc::kstep_desc(ah, 128, 0), dl = tc::kstep_desc(al, 128, 0);
+    const uint64_t dh = tc::kstep_desc(tc::smem_u32(a1 + S::K_HI), 128, 0);
+    const uint64_t dl = tc::kstep_desc(tc::smem_u32(a1 + S::K_LO), 128, 0);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint64_t h = tc::desc_add(dh, 256 * k), l = tc::desc_add(dl, 256 * k);
-      tc::mma_bf16(tb, h, h, id, k > 0);
-      tc::mma_bf16(tb, h, l, id, 1);
-      tc::mma_bf16(tb, l, h, id, 1);
+      const uint64_t hk = tc::desc_add(dh, 256 * k), lk = tc::desc_add(dl, 256 * k);
+      tc::mma_bf16(tb + TI_D1, hk, hk, id, k > 0);
+      tc::mma_bf16(tb + TI_D1, hk, lk, id, 1);
+      tc::mma_bf16(tb + TI_D1, lk, hk, id, 1);
     }
     tc::mma_commit(bar);
   }
-  // ---- V (overlaps the MMA): conv into registers
-  float vy[32];
-  conv_compute_regs(cin, L, vy);
-  // ---- A1 is free once MMA1 completed: (beta e^g K)^T into its Q quarters, then (beta V)^T
-  // into its K quarters, straight from the V registers (thread: feature f, tokens i0..i0+31,
-  // i.e. four 8-token units of the K-major [128 features][64 tokens] tile)
+  // ---- V of the first V-head straight into its tile (overlaps MMA1)
+  ring_wait(2);   // also: slot 1 free
+  if (issued < ntens) {
+    ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), seq_start, seq_len, p0, slot_of(issued));
+    ++issued;
+  }
+  conv_slot<T>(slot_of(2), L, y);
+  put_row16(vt, vt + 16384, y);
   wait_or_abort(bar, 0, abort, status);
   tc::fence_after_sync();
-  a1k_cols_to_tile(a1 + S::K_HI, a1 + S::K_LO, bgk, a1 + S::Q_HI, a1 + S::Q_LO);
-  __syncthreads();
-  {
-    const int f = tid & 127, i0 = (tid >> 7) * 32;
+
+  // A (to At) and P (to the record) of V-head j from D1: warp w reads TMEM lanes 32 (w % 4) and
+  // the 16 columns of quarter w / 4.  Lanes 0-63 are K-rows (A), lanes 64-127 Q-rows (P).
+  auto a_and_p = [&](int j) {
+    const float* gam = vecs + j * 320;
+    const float* bet = gam + 64;
+    const int rr = (warp & 3) * 32 + lane, j0 = (warp >> 2) * 16;
+    float v[16];
+    tc::tmem_ld16(tc::taddr(tb + TI_D1, (warp & 3) * 32, j0), v);
+    if (rr < 64) {
+      const int i = rr;
+      const float gi = gam[i], bi = bet[i];   // beta is 0 past L: rows past L vanish
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      float v8[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) v8[q] = vy[8 * g + q] * bet[i0 + 8 * g + q];
-      uint4 hh, ll;
-      split8(v8, hh, ll);
-      const uint32_t off = tc::kmajor_off(f, i0 + 8 * g, 64);
-      st_unit(a1 + S::K_HI, off, hh);
-      st_unit(a1 + S::K_LO, off, ll);
-    }
-  }
-  // ---- A and P from D1: warp w reads TMEM lanes 32 (w % 4) and the 32 columns of half w / 4
-  {
-    const int r = (warp & 3) * 32 + lane, j0 = (warp >> 2) * 32;
-    float v[32];
-    tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, j0), v);
-    tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, j0 + 16), v + 16);
-    // branch-free: exponents clamped to <= 0, masked entries multiplied by zero
-    if (r < 64) {
-      const int i = r;
-      const float gi = gam[i], bi = (i < L) ? bet[i] : 0.f;
-#pragma unroll
-      for (int q = 0; q < 32; q += 4) {
+      for (int q = 0; q < 16; q += 4) {
         float a4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int j = j0 + q + u;
-          const float m = (j < i) ? bi : 0.f;
-          a4[u] = m * exp_fast(fminf(gi - gam[j], 0.f)) * v[q + u];
+          const int jj = j0 + q + u;
+          const float m = (jj < i) ? bi : 0.f;
+          a4[u] = m * exp_fast(fminf(gi - gam[jj], 0.f)) * v[q + u];
         }
-        *reinterpret_cast<float4*>(Am + i * AS + j0 + q) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+        *reinterpret_cast<float4*>(At + i * AS + j0 + q) = make_float4(a4[0], a4[1], a4[2], a4[3]);
       }
     } else {
-      const int i = r - 64;
+      const int i = rr - 64;
       const float gi = gam[i], vi = (i < L) ? 1.f : 0.f;
+      unsigned char* rec = rec_of(j);
 #pragma unroll
-      for (int q = 0; q < 32; q += 8) {
+      for (int q = 0; q < 16; q += 8) {
         float p8[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int j = j0 + q + u;
-          p8[u] = ((j <= i) ? vi : 0.f) * exp_fast(fminf(gi - gam[j], 0.f)) * v[q + u];
+          const int jj = j0 + q + u;
+          p8[u] = ((jj <= i) ? vi : 0.f) * exp_fast(fminf(gi - gam[jj], 0.f)) * v[q + u];
         }
         uint4 hh, ll;
         split8(p8, hh, ll);
@@ -522,151 +710,98 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
         gst_unit(rec + R_B4 + B4_HALF, off, ll);
       }
     }
-  }
+  };
+
+  // ---- prologue of V-head 0: A / P, T, the D2 operand
+  a_and_p(0);
   __syncthreads();
-  // ---- T = (I + A)^{-1}, A strictly lower triangular, in 16 x 16 blocks: the diagonal inverses
-  // D_b = (I + A_bb)^{-1} by forward substitution (the four in parallel), then block row by block
-  // row  T_ik = -D_i sum_{j=k}^{i-1} A_ij T_jk  (k < i), each a few dense 16 x 16 products over
-  // all threads instead of one 64-step dependent chain.  T replaces A in Am (D_b over A_bb, T_ik
-  // over A_ik once block row i of A has been used); the partial sums X_ik live in the unused
-  // upper block (k, i).  Each final block also goes to the split-bf16 B2 tile (rows i, K = j).
-  {
-    auto put_b2 = [&](int row, int col, float v) {
-      __nv_bfloat16 hi, lo;
-      tc::split_bf16(v, hi, lo);
-      const uint32_t off = tc::kmajor_off(row, col, 64);
-      *reinterpret_cast<__nv_bfloat16*>(b2h + off) = hi;
-      *reinterpret_cast<__nv_bfloat16*>(b2l + off) = lo;
-    };
-    float dcol[16];
-    const int db = tid >> 4, dc = tid & 15;   // threads 0-63: column dc of D_db
-    if (tid < 64) {
-      const float* ab = Am + (16 * db) * AS + 16 * db;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float arow[16];
-#pragma unroll
-        for (int m = 0; m < 16; m += 4) {
-          const float4 a4 = *reinterpret_cast<const float4*>(ab + i * AS + m);
-          arow[m] = a4.x;
-          arow[m + 1] = a4.y;
-          arow[m + 2] = a4.z;
-          arow[m + 3] = a4.w;
-        }
-        float acc = (i == dc) ? 1.f : 0.f;
-#pragma unroll
-        for (int j = 0; j < i; ++j) acc = fmaf(-arow[j], dcol[j], acc);
-        dcol[i] = acc;
-      }
-    } else {
-      // the six upper blocks of B2 are zero
-      for (int u = tid - 64; u < 6 * 256; u += NTI - 64) {
-        const int blk = u >> 8, el = u & 255;
-        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-        put_b2(16 * bi + (el >> 4), 16 * bj + (el & 15), 0.f);
-      }
-    }
-    __syncthreads();
-    if (tid < 64) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        Am[(16 * db + i) * AS + 16 * db + dc] = dcol[i];
-        put_b2(16 * db + i, 16 * db + dc, dcol[i]);
-      }
-    }
-    __syncthreads();
-    const int r = tid >> 4, cc = tid & 15;   // element (r, cc) of every 16 x 16 block
-#pragma unroll
-    for (int i = 1; i < 4; ++i) {
-      const float* arow = Am + (16 * i + r) * AS;
-#pragma unroll
-      for (int k = 0; k < i; ++k) {   // X_ik -> block (k, i)
-        float acc = 0.f;
-#pragma unroll
-        for (int j = k; j < i; ++j) {
-          const float* tcol = Am + (16 * j) * AS + 16 * k + cc;
-#pragma unroll
-          for (int m = 0; m < 16; m += 4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(arow + 16 * j + m);
-            acc = fmaf(a4.x, tcol[m * AS], acc);
-            acc = fmaf(a4.y, tcol[(m + 1) * AS], acc);
-            acc = fmaf(a4.z, tcol[(m + 2) * AS], acc);
-            acc = fmaf(a4.w, tcol[(m + 3) * AS], acc);
-          }
-        }
-        Am[(16 * k + r) * AS + 16 * i + cc] = acc;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int k = 0; k < i; ++k) {   // T_ik = -D_i X_ik -> block (i, k)
-        const float* xcol = Am + (16 * k) * AS + 16 * i + cc;
-        float acc = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; m += 4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(arow + 16 * i + m);
-          acc = fmaf(d4.x, xcol[m * AS], acc);
-          acc = fmaf(d4.y, xcol[(m + 1) * AS], acc);
-          acc = fmaf(d4.z, xcol[(m + 2) * AS], acc);
-          acc = fmaf(d4.w, xcol[(m + 3) * AS], acc);
-        }
-        Am[(16 * i + r) * AS + 16 * k + cc] = -acc;
-        put_b2(16 * i + r, 16 * k + cc, -acc);
-      }
-      if (i < 3) __syncthreads();
-    }
-  }
+  tri_inverse(At);
+  t_to_b2(At, vecs + 256, vecs + 64, b2, b2 + 16384);
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  // ---- D2a = (beta e^g K)^T T^T = W^T (cols [64,128)),  D2b = (beta V)^T T^T = U~^T ([128,192))
-  if (tid == 0 && !*abort) {
-    const uint32_t id = tc::idesc_bf16(128, 64);
-    const uint32_t bh = tc::smem_u32(b2h), bl = tc::smem_u32(b2l);
-    const uint32_t srcs[2][2] = {{tc::smem_u32(a1 + S::Q_HI), tc::smem_u32(a1 + S::Q_LO)},
-                                 {tc::smem_u32(a1 + S::K_HI), tc::smem_u32(a1 + S::K_LO)}};
-    const uint64_t dbh = tc::kstep_desc(bh, 64, 0), dbl = tc::kstep_desc(bl, 64, 0);
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      const uint32_t dt = tb + 64 + 64 * m;
-      const uint64_t dah = tc::kstep_desc(srcs[m][0], 64, 0), dal = tc::kstep_desc(srcs[m][1], 64, 0);
+
+  const uint32_t idn = tc::idesc_bf16_bmn(128, 128);
+  for (int j = 0; j < r; ++j) {
+    // ---- D2 of V-head j: [T diag(bgk) ; T diag(beta)] x K^T -> W rows (lanes 0-63);
+    //      the same x V^T -> U~ rows (lanes 64-127).  K^T and V^T are read MN-major straight
+    //      out of the token-row tiles (N-direction core stride 128 B, 8-token stride 2 KiB).
+    if (tid == 0 && !*abort) {
+      const uint64_t dah = tc::kstep_desc(tc::smem_u32(b2), 64, 0);
+      const uint64_t dal = tc::kstep_desc(tc::smem_u32(b2 + 16384), 64, 0);
+      const uint64_t dkh = tc::sdesc(tc::smem_u32(a1 + S::K_HI), 2048, 128);
+      const uint64_t dkl = tc::sdesc(tc::smem_u32(a1 + S::K_LO), 2048, 128);
+      const uint64_t dvh = tc::sdesc(tc::smem_u32(vt), 2048, 128);
+      const uint64_t dvl = tc::sdesc(tc::smem_u32(vt + 16384), 2048, 128);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t o = 256 * k;
-        tc::mma_bf16(dt, tc::desc_add(dah, o), tc::desc_add(dbh, o), id, k > 0);
-        tc::mma_bf16(dt, tc::desc_add(dah, o), tc::desc_add(dbl, o), id, 1);
-        tc::mma_bf16(dt, tc::desc_add(dal, o), tc::desc_add(dbh, o), id, 1);
+        const uint64_t ah = tc::desc_add(dah, 256 * k), al = tc::desc_add(dal, 256 * k);
+        const uint32_t o = 4096u * k;
+        tc::mma_bf16(tb + TI_W, ah, tc::desc_add(dkh, o), idn, k > 0);
+        tc::mma_bf16(tb + TI_W, ah, tc::desc_add(dkl, o), idn, 1);
+        tc::mma_bf16(tb + TI_W, al, tc::desc_add(dkh, o), idn, 1);
+        tc::mma_bf16(tb + TI_U, ah, tc::desc_add(dvh, o), idn, k > 0);
+        tc::mma_bf16(tb + TI_U, ah, tc::desc_add(dvl, o), idn, 1);
+        tc::mma_bf16(tb + TI_U, al, tc::desc_add(dvh, o), idn, 1);
       }
+      tc::mma_commit(bar + 1);
     }
-    tc::mma_commit(bar);
-  }
-  wait_or_abort(bar, 1, abort, status);
-  tc::fence_after_sync();
-  {
-    // warps 0-3: W^T lanes -> X staging [token][feature]; warps 4-7: U~^T lanes -> U~ rows
-    const int r = (warp & 3) * 32 + lane;
-    const int col = warp < 4 ? 64 : 128;
-#pragma unroll
-    for (int hb = 0; hb < 64; hb += 32) {
+    // ---- while it runs: the next V-head's V conv (held in registers), A / P and inverse
+    if (j + 1 < r) {
+      ring_wait(j + 3);   // tensor 2 + (j + 1); also: slot of tensor j + 2 free
+      if (issued < ntens) {
+        ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), seq_start, seq_len, p0, slot_of(issued));
+        ++issued;
+      }
+      conv_slot<T>(slot_of(j + 3), L, y);
+      a_and_p(j + 1);
+      __syncthreads();
+      tri_inverse(At);
+    }
+    // ---- W and U~ rows of V-head j straight from TMEM into the record
+    wait_or_abort(bar + 1, j & 1, abort, status);
+    tc::fence_after_sync();
+    {
+      unsigned char* rec = rec_of(j);
+      const int lg = warp & 3, cq = (warp >> 2) * 32;
+      const int i = (lg & 1) * 32 + lane;
       float v[32];
-      tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, col + hb), v);
-      tc::tmem_ld16(tc::taddr(tb, (warp & 3) * 32, col + hb + 16), v + 16);
-      if (warp < 4) {
+      if (lg < 2) {
+        tc::tmem_ld16(tc::taddr(tb + TI_W, lg * 32, cq), v);
+        tc::tmem_ld16(tc::taddr(tb + TI_W, lg * 32, cq + 16), v + 16);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) X[(hb + i) * XS + r] = v[i];
+        for (int u = 0; u < 4; ++u) {
+          uint4 hh, ll;
+          split8(v + 8 * u, hh, ll);
+          const uint32_t off = tc::kmajor_off(64 + i, cq + 8 * u, 128);   // W rows of B3
+          gst_unit(rec + R_B3, off, hh);
+          gst_unit(rec + R_B3 + B3_HALF, off, ll);
+        }
       } else {
+        tc::tmem_ld16(tc::taddr(tb + TI_U, lg * 32, cq), v);
+        tc::tmem_ld16(tc::taddr(tb + TI_U, lg * 32, cq + 16), v + 16);
+        // U~ record layout [column / 4][token][4]: a warp stores 32 consecutive tokens' float4
+        float* ut = reinterpret_cast<float*>(rec + R_UT);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) rec_ut[(hb + i) * D + r] = v[i];
+        for (int q = 0; q < 32; q += 4)
+          *reinterpret_cast<float4*>(ut + ut_index(i, cq + q)) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
       }
     }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (j + 1 < r) {
+      // the D2 operands of V-head j + 1 (VT and B2 were read by the MMAs just completed)
+      put_row16(vt, vt + 16384, y);
+      t_to_b2(At, vecs + (j + 1) * 320 + 256, vecs + (j + 1) * 320 + 64, b2, b2 + 16384);
+      tc::fence_proxy_async_smem();
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+    }
   }
-  __syncthreads();
-  x_rows_to_gtile128(X, nullptr, rec + R_B3, rec + R_B3 + B3_HALF, 64);   // W rows of B3
-  if (tid == 0) *reinterpret_cast<float*>(rec + R_SC) = expf(gL);
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tb, 256);
+  if (warp == 1) tc::tmem_dealloc(tb, TI_COLS);
 }
 
 // ================================================================== serial state kernel
@@ -799,10 +934,10 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     const bool urow = (warp & 3) >= 2;
     float ut[MH];                     // U~ of token t, columns mh.., loaded one chunk ahead
     if (urow && nch > 0) {
-      const float* u0 = reinterpret_cast<const float*>(rec_of(0) + R_UT) + t * D + sig * SW + mh;
+      const float* u0 = reinterpret_cast<const float*>(rec_of(0) + R_UT);
 #pragma unroll
       for (int q = 0; q < MH; q += 4) {
-        const float4 x = *reinterpret_cast<const float4*>(u0 + q);
+        const float4 x = *reinterpret_cast<const float4*>(u0 + ut_index(t, sig * SW + mh + q));
         ut[q] = x.x;
         ut[q + 1] = x.y;
         ut[q + 2] = x.z;
@@ -889,10 +1024,10 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
           *reinterpret_cast<__nv_bfloat16*>(uopl + off) = lo;
         }
         if (c + 1 < nch) {
-          const float* un = reinterpret_cast<const float*>(rec_of(c + 1) + R_UT) + t * D + sig * SW + mh;
+          const float* un = reinterpret_cast<const float*>(rec_of(c + 1) + R_UT);
 #pragma unroll
           for (int q = 0; q < MH; q += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(un + q);
+            const float4 x = *reinterpret_cast<const float4*>(un + ut_index(t, sig * SW + mh + q));
             ut[q] = x.x;
             ut[q + 1] = x.y;
             ut[q + 2] = x.z;
@@ -1105,7 +1240,7 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
     return GDN_ERR_CUDA;
   float* wsf = static_cast<float*>(ws);
   if (total > 0)
-    k1<<<dim3(nc_max, d.Hv), NTI, IntraSmem::BYTES, stream>>>(
+    k1<<<dim3(nc_max, d.Hk), NTI, IntraSmem::BYTES, stream>>>(
         d, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
         static_cast<const T*>(pool->conv_state), pool->num_slots, cu, slot_idx, has_init, num_seqs,
         total, static_cast<const T*>(qkv), static_cast<const T*>(a), static_cast<const T*>(b), wsf,
@@ -1119,7 +1254,7 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
 
 }  // namespace
 
-bool prefill_tc_supported(const KDims& d) { return d.dk == D && d.dv == D; }
+bool prefill_tc_supported(const KDims& d) { return d.dk == D && d.dv == D && d.r <= RMAX; }
 
 size_t prefill_tc_ws_bytes(const KDims& d, int num_seqs, int total) {
   return (size_t)(total / CH + num_seqs) * d.Hv * REC_BYTES;

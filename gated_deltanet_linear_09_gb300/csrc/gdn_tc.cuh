@@ -60,6 +60,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with the B operand MN-major (bit 16, "transpose B"): B's core matrices hold 8
+// consecutive N-elements (16 bytes) in each of their 8 rows, one row per K index.  A tile
+// stored K-major for a matrix X [K rows][N cols] is, read this way, the operand B = X^T with no
+// data movement: its descriptor takes the N-direction core-matrix stride as the stride byte
+// offset and the K-direction (8-row group) stride as the leading byte offset.
+__host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) {
+  return idesc_bf16(M, N) | (1u << 16);
+}
+
 // ------------------------------------------------------------------ TMEM
 
 // Warp-wide.  Writes the TMEM base address to *slot (shared memory).
@@ -288,6 +297,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(x);
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+// The same split for two values at once with the paired conversions (bf16x2 words, element 0
+// in the low half): bit-identical to two split_bf16 calls, about half the instructions.
+__device__ __forceinline__ void split2_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 }  // namespace tc

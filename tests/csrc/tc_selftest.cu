@@ -200,6 +200,92 @@ extern "C" int tc_gemm(const float* A, const float* B, float* D, int N, int K, i
   return tc_gemm_p(A, B, D, N, K, passes, 128, err);
 }
 
+// D = A B^T with the B operand MN-major: Bt (= B^T, [K][N] row-major) is stored the way the
+// prefill keeps its token-row tiles (rows = k, 16-byte units of 8 consecutive n, 8-row groups
+// (N/8) * 128 bytes apart) and the MMA reads it as B through an MN-major descriptor:
+// N-direction core-matrix stride 128 bytes, K-direction (8 k) stride (N/8) * 128 bytes.
+__global__ void tc_gemm_mnb_kernel(const float* __restrict__ A, const float* __restrict__ Bt,
+                                   float* __restrict__ D, int N, int K, int passes, uint32_t ncols,
+                                   int* __restrict__ err) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned char* a_hi = sm;
+  unsigned char* a_lo = a_hi + 128 * K * 2;
+  unsigned char* b_hi = a_lo + 128 * K * 2;
+  unsigned char* b_lo = b_hi + N * K * 2;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(b_lo + N * K * 2);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+  for (int idx = tid; idx < 128 * K; idx += blockDim.x) {
+    const int r = idx / K, k = idx - r * K;
+    __nv_bfloat16 h, l;
+    split_bf16(A[idx], h, l);
+    *reinterpret_cast<__nv_bfloat16*>(a_hi + kmajor_off(r, k, K)) = h;
+    *reinterpret_cast<__nv_bfloat16*>(a_lo + kmajor_off(r, k, K)) = l;
+  }
+  for (int idx = tid; idx < K * N; idx += blockDim.x) {
+    const int k = idx / N, n = idx - k * N;   // Bt[k][n] = B[n][k]
+    __nv_bfloat16 h, l;
+    split_bf16(Bt[idx], h, l);
+    *reinterpret_cast<__nv_bfloat16*>(b_hi + kmajor_off(k, n, N)) = h;
+    *reinterpret_cast<__nv_bfloat16*>(b_lo + kmajor_off(k, n, N)) = l;
+  }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (warp == 0) tmem_alloc(slot, ncols);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *slot;
+  if (tid == 0) {
+    const uint32_t id = idesc_bf16_bmn(128, N);
+    const uint32_t ah = smem_u32(a_hi), al = smem_u32(a_lo), bh = smem_u32(b_hi), bl = smem_u32(b_lo);
+    const uint32_t lbo = (uint32_t)(N / 8) * 128u;   // one K-step (16 k) = two 8-row groups
+    for (int s = 0; s < K / 16; ++s) {
+      const uint64_t dbh = sdesc(bh + 2u * lbo * (uint32_t)s, lbo, 128u);
+      const uint64_t dbl = sdesc(bl + 2u * lbo * (uint32_t)s, lbo, 128u);
+      mma_bf16(tbase, kstep_desc(ah, K, s), dbh, id, s > 0 ? 1u : 0u);
+      if (passes == 3) {
+        mma_bf16(tbase, kstep_desc(ah, K, s), dbl, id, 1u);
+        mma_bf16(tbase, kstep_desc(al, K, s), dbh, id, 1u);
+      }
+    }
+    mma_commit(bar);
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(bar, 0);
+  if (!ok && lane == 0) atomicOr(err, 1);
+  fence_after_sync();
+  if (ok) {
+    for (int c0 = 0; c0 < N; c0 += 16) {
+      float v[16];
+      tmem_ld16(taddr(tbase, warp * 32, c0), v);
+      for (int i = 0; i < 16; ++i) D[(size_t)(warp * 32 + lane) * N + c0 + i] = v[i];
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, ncols);
+}
+
+extern "C" int tc_gemm_mnb(const float* A, const float* Bt, float* D, int N, int K, int passes,
+                           int* err) {
+  if (N < 16 || N > 256 || N % 16 || K < 16 || K % 16) return -1;
+  uint32_t ncols = 32;
+  while (ncols < (uint32_t)N) ncols <<= 1;
+  const size_t smem = (size_t)2 * (128 + N) * K * 2 + 64;
+  if (smem > 200 * 1024) return -1;
+  if (cudaFuncSetAttribute(tc_gemm_mnb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return -2;
+  tc_gemm_mnb_kernel<<<1, 128, smem>>>(A, Bt, D, N, K, passes, ncols, err);
+  if (cudaGetLastError() != cudaSuccess) return -3;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
+}
+
 // Per-round exchange of one float per thread among the 4 CTAs of a cluster, the way the prefill
 // state kernel shares per-token partial sums of squares: every thread stores its value into slot
 // [round & 1][own rank][thread] of all four CTAs with st.async (completing bytes on that CTA's
