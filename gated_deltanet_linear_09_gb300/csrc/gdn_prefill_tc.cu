@@ -813,11 +813,27 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
 
 constexpr int NSL = 4;                        // dv slices (CTAs) per head
 constexpr int SW = D / NSL;                   // 32 columns per slice
-constexpr uint32_t PLBO = 144;                // padded K-direction core-matrix stride (bytes)
-constexpr uint32_t SOP_SBO = (D / 8) * PLBO;  // S operand: N = 32 rows, K = 128 (dk)
+// The S and U slices enter the MMAs as MN-major B operands [X_hi ; X_lo] (N = 2 SW): core
+// matrices of 8 K-rows x 8 consecutive N-elements, the K-direction ones 128 bytes apart, the
+// N-direction ones (K / 8) * 128 bytes apart.  A thread holding row k of 16 consecutive columns
+// stores four 16-byte units, and a warp's 32 consecutive rows fill 512 contiguous bytes.
+constexpr uint32_t SOP_SBO = (D / 8) * 128;   // S operand: K = 128 (dk)
 constexpr uint32_t SOP_HALF = (SW / 8) * SOP_SBO;
-constexpr uint32_t UOP_SBO = (CH / 8) * PLBO; // U operand: N = 32 rows, K = 64 (tokens)
+constexpr uint32_t UOP_SBO = (CH / 8) * 128;  // U operand: K = 64 (tokens)
 constexpr uint32_t UOP_HALF = (SW / 8) * UOP_SBO;
+
+// Row k, columns [n0, n0 + 16) of an MN-major split operand: four 16-byte stores.
+__device__ __forceinline__ void put_mn16(unsigned char* hi, unsigned char* lo, uint32_t sbo, int k,
+                                         int n0, const float* v) {
+  uint32_t hw[8], lw[8];
+#pragma unroll
+  for (int p = 0; p < 8; ++p) tc::split2_bf16(v[2 * p], v[2 * p + 1], hw[p], lw[p]);
+  const uint32_t off = (uint32_t)(n0 >> 3) * sbo + (uint32_t)(k >> 3) * 128u + (uint32_t)(k & 7) * 16u;
+  *reinterpret_cast<uint4*>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4*>(hi + off + sbo) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+  *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  *reinterpret_cast<uint4*>(lo + off + sbo) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+}
 constexpr int NTS = 448;   // warps 0-7 main, 8-9 and 12-13 epilogue, 10 loader (11 idle)
 constexpr int MH = SW / 2; // columns per main warp: warp w takes lanes 32 (w % 4) and half w / 4
 constexpr int NDB = 4;     // D3 (output) accumulators in flight between the MMAs and the epilogue
@@ -945,17 +961,17 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       }
     }
     float egL_next = nch > 0 ? *reinterpret_cast<const float*>(rec_of(0) + R_SC) : 1.f;
-    // operand descriptors, built once (K-step k: + 256 bytes for the dense tiles, + 2 PLBO for
-    // the padded ones)
-    const uint32_t id64 = tc::idesc_bf16(128, 2 * SW);
+    // operand descriptors, built once (K-step k: + 256 bytes for every tile; the S and U
+    // operands are MN-major)
+    const uint32_t id64 = tc::idesc_bf16_bmn(128, 2 * SW);
     const uint64_t dA3h = tc::kstep_desc(tc::smem_u32(sm + S::B3), 128, 0);   // slot 0; slot 1 + 64 KiB
     const uint64_t dA3l = tc::kstep_desc(tc::smem_u32(sm + S::B3 + B3_HALF), 128, 0);
     const uint64_t dKh = tc::kstep_desc(tc::smem_u32(b4h) + 8192, 64, 0);
     const uint64_t dKl = tc::kstep_desc(tc::smem_u32(b4l) + 8192, 64, 0);
     const uint64_t dPh = tc::kstep_desc(tc::smem_u32(b4h), 64, 0);
     const uint64_t dPl = tc::kstep_desc(tc::smem_u32(b4l), 64, 0);
-    const uint64_t dS = tc::kstep_desc_p(tc::smem_u32(soph), PLBO, SOP_SBO, 0);
-    const uint64_t dU = tc::kstep_desc_p(tc::smem_u32(uoph), PLBO, UOP_SBO, 0);
+    const uint64_t dS = tc::sdesc(tc::smem_u32(soph), 128, SOP_SBO);
+    const uint64_t dU = tc::sdesc(tc::smem_u32(uoph), 128, UOP_SBO);
     for (int c = 0; c < nch; ++c) {
       const uint32_t par = c & 1, b = c & 1;
       const uint32_t jd = c & (NDB - 1);
@@ -973,15 +989,10 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         tc::reg_fence16(rv + MH);
         float v[MH];
 #pragma unroll
-        for (int q = 0; q < MH; ++q) {
-          v[q] = __uint_as_float(rv[q]) + __uint_as_float(rv[q + MH]);
-          __nv_bfloat16 hi, lo;
-          tc::split_bf16(v[q], hi, lo);
-          const uint32_t off = tc::kmajor_off_p(mh + q, e, PLBO, SOP_SBO);
-          *reinterpret_cast<__nv_bfloat16*>(soph + off) = hi;
-          *reinterpret_cast<__nv_bfloat16*>(sopl + off) = lo;
-          v[q] *= egL;
-        }
+        for (int q = 0; q < MH; ++q) v[q] = __uint_as_float(rv[q]) + __uint_as_float(rv[q + MH]);
+        put_mn16(soph, sopl, SOP_SBO, e, mh, v);
+#pragma unroll
+        for (int q = 0; q < MH; ++q) v[q] *= egL;
         tc::tmem_st16_nw(lane_base + TC_S + mh, v);
 #pragma unroll
         for (int q = 0; q < MH; ++q) v[q] = 0.f;
@@ -998,7 +1009,7 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         const uint32_t so = 65536u * b;   // B3 slot of the chunk
 #pragma unroll
         for (int k = 0; k < 8; ++k) {   // B = [S_hi ; S_lo], 64 rows
-          const uint64_t bk = tc::desc_add(dS, 2 * PLBO * k);
+          const uint64_t bk = tc::desc_add(dS, 256 * k);
           tc::mma_bf16(d3, tc::desc_add(dA3h, so + 256 * k), bk, id64, k > 0);
           tc::mma_bf16(d3, tc::desc_add(dA3l, so + 256 * k), bk, id64, 1);
         }
@@ -1015,14 +1026,10 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         tc::tmem_wait_ld();
         tc::reg_fence16(rv);
         tc::reg_fence16(rv + MH);
+        float u[MH];
 #pragma unroll
-        for (int q = 0; q < MH; ++q) {
-          __nv_bfloat16 hi, lo;
-          tc::split_bf16(ut[q] - (__uint_as_float(rv[q]) + __uint_as_float(rv[q + MH])), hi, lo);
-          const uint32_t off = tc::kmajor_off_p(mh + q, t, PLBO, UOP_SBO);
-          *reinterpret_cast<__nv_bfloat16*>(uoph + off) = hi;
-          *reinterpret_cast<__nv_bfloat16*>(uopl + off) = lo;
-        }
+        for (int q = 0; q < MH; ++q) u[q] = ut[q] - (__uint_as_float(rv[q]) + __uint_as_float(rv[q + MH]));
+        put_mn16(uoph, uopl, UOP_SBO, t, mh, u);
         if (c + 1 < nch) {
           const float* un = reinterpret_cast<const float*>(rec_of(c + 1) + R_UT);
 #pragma unroll
@@ -1043,7 +1050,7 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         tc::fence_after_sync();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {   // S += K~^T U   (B4 rows 64..191; B = [U_hi ; U_lo])
-          const uint64_t bk = tc::desc_add(dU, 2 * PLBO * k);
+          const uint64_t bk = tc::desc_add(dU, 256 * k);
           tc::mma_bf16(tb + TC_S, tc::desc_add(dKh, 256 * k), bk, id64, 1);
           tc::mma_bf16(tb + TC_S, tc::desc_add(dKl, 256 * k), bk, id64, 1);
         }
@@ -1052,7 +1059,7 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         // left as scratch
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint64_t bk = tc::desc_add(dU, 2 * PLBO * k);
+          const uint64_t bk = tc::desc_add(dU, 256 * k);
           tc::mma_bf16(d3, tc::desc_add(dPh, 256 * k), bk, id64, 1);
           tc::mma_bf16(d3, tc::desc_add(dPl, 256 * k), bk, id64, 1);
         }
