@@ -843,7 +843,7 @@ constexpr int NXB = 4;     // exchange buffers: chunk c's sums are sent one epil
 // TMEM columns (lanes 0-127).  Each product runs as two N = 64 MMAs per K-step, A_hi [B_hi ; B_lo]
 // and A_lo [B_hi ; B_lo] (the B operand holds the hi rows 0-31 and the lo rows 32-63), so every
 // accumulator occupies 64 columns whose two 32-column halves add up to the result.
-constexpr uint32_t TC_S = 0;          // S slice, halves [0, 32) + [32, 64)
+constexpr uint32_t TC_S = 0;          // K~^T U of the chunk, halves [0, 32) + [32, 64)
 constexpr uint32_t TC_D3 = 64;        // NDB x 64 columns: rows 0-63 O, rows 64-127 W S
 constexpr uint32_t TC_COLS = 512;
 
@@ -926,25 +926,20 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   };
 
   if (warp < 8) {
-    // ================= main warps: thread e owns TMEM lane e = row e (dk index) of the S slice and
-    // its columns [mh, mh + 16) (of both accumulator halves)
+    // ================= main warps: thread e owns row e (dk index) of the S slice, columns
+    // [mh, mh + 16), in registers (sv); TMEM lane e of the K~^T U accumulator carries the same
+    // columns (both halves)
     const int e = (warp & 3) * 32 + lane, mh = (warp >> 2) * MH;
     const uint32_t lane_base = tc::taddr(tb, (warp & 3) * 32, 0);
-    {
-      float v[MH];
+    float sv[MH];
 #pragma unroll
-      for (int q = 0; q < MH; q += 4) {
-        const float4 x = init ? *reinterpret_cast<const float4*>(Sg + (size_t)e * D + mh + q)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[q] = x.x;
-        v[q + 1] = x.y;
-        v[q + 2] = x.z;
-        v[q + 3] = x.w;
-      }
-      tc::tmem_st16(lane_base + TC_S + mh, v);
-#pragma unroll
-      for (int q = 0; q < MH; ++q) v[q] = 0.f;
-      tc::tmem_st16(lane_base + TC_S + SW + mh, v);
+    for (int q = 0; q < MH; q += 4) {
+      const float4 x = init ? *reinterpret_cast<const float4*>(Sg + (size_t)e * D + mh + q)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      sv[q] = x.x;
+      sv[q + 1] = x.y;
+      sv[q + 2] = x.z;
+      sv[q + 3] = x.w;
     }
     const int t = e - 64;             // token row of W S / U for lanes 64..127
     const bool urow = (warp & 3) >= 2;
@@ -976,29 +971,10 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       const uint32_t par = c & 1, b = c & 1;
       const uint32_t jd = c & (NDB - 1);
       const uint32_t d3 = tb + TC_D3 + 64 * jd;   // D3[jd]: rows 0-63 O (Q~ S + P U), rows 64-127 W S
-      // S slice -> B operand (split bf16, unscaled: W S and Q~ S use the chunk's initial state),
-      // and S <- e^{gamma_L} S in TMEM for the K~^T U accumulation
+      // S slice (the chunk's initial state) -> B operand of W S and Q~ S
       const float egL = egL_next;
       if (c + 1 < nch) egL_next = *reinterpret_cast<const float*>(rec_of(c + 1) + R_SC);
-      {
-        uint32_t rv[2 * MH];
-        tc::tmem_ld16_nw(lane_base + TC_S + mh, rv);
-        tc::tmem_ld16_nw(lane_base + TC_S + SW + mh, rv + MH);
-        tc::tmem_wait_ld();
-        tc::reg_fence16(rv);
-        tc::reg_fence16(rv + MH);
-        float v[MH];
-#pragma unroll
-        for (int q = 0; q < MH; ++q) v[q] = __uint_as_float(rv[q]) + __uint_as_float(rv[q + MH]);
-        put_mn16(soph, sopl, SOP_SBO, e, mh, v);
-#pragma unroll
-        for (int q = 0; q < MH; ++q) v[q] *= egL;
-        tc::tmem_st16_nw(lane_base + TC_S + mh, v);
-#pragma unroll
-        for (int q = 0; q < MH; ++q) v[q] = 0.f;
-        tc::tmem_st16_nw(lane_base + TC_S + SW + mh, v);
-        tc::tmem_wait_st();
-      }
+      put_mn16(soph, sopl, SOP_SBO, e, mh, sv);
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       bar_sync_main();
@@ -1049,9 +1025,9 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       if (tid == 0 && wait_or_abort(b4full, par, abort, status)) {
         tc::fence_after_sync();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {   // S += K~^T U   (B4 rows 64..191; B = [U_hi ; U_lo])
+        for (int k = 0; k < 4; ++k) {   // K~^T U, fresh   (B4 rows 64..191; B = [U_hi ; U_lo])
           const uint64_t bk = tc::desc_add(dU, 256 * k);
-          tc::mma_bf16(tb + TC_S, tc::desc_add(dKh, 256 * k), bk, id64, 1);
+          tc::mma_bf16(tb + TC_S, tc::desc_add(dKh, 256 * k), bk, id64, k > 0);
           tc::mma_bf16(tb + TC_S, tc::desc_add(dKl, 256 * k), bk, id64, 1);
         }
         tc::mma_commit(sready);   // the next chunk's S conversion overlaps the O products below
@@ -1066,22 +1042,28 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         tc::mma_commit(b4empty);
         tc::mma_commit(dfull + jd);
       }
-      // S is final for this chunk.  The O products may still run: they read only B4 and the U
+      // S <- e^{gamma_L} S + K~^T U.  The O products may still run: they read only B4 and the U
       // operand (rewritten only after the next chunk's MMA3, which the pipe orders after them)
       // and write D3[jd], which the next chunk does not touch.
       wait_or_abort(sready, par, abort, status);
       tc::fence_after_sync();
+      {
+        uint32_t rv[2 * MH];
+        tc::tmem_ld16_nw(lane_base + TC_S + mh, rv);
+        tc::tmem_ld16_nw(lane_base + TC_S + SW + mh, rv + MH);
+        tc::tmem_wait_ld();
+        tc::reg_fence16(rv);
+        tc::reg_fence16(rv + MH);
+#pragma unroll
+        for (int q = 0; q < MH; ++q)
+          sv[q] = fmaf(egL, sv[q], __uint_as_float(rv[q]) + __uint_as_float(rv[q + MH]));
+      }
     }
     // final state slice back to the slot
     if (valid) {
-      float v[2 * MH];
-      tc::tmem_ld16(lane_base + TC_S + mh, v);
-      tc::tmem_ld16(lane_base + TC_S + SW + mh, v + MH);
-#pragma unroll
-      for (int q = 0; q < MH; ++q) v[q] += v[q + MH];
 #pragma unroll
       for (int q = 0; q < MH; q += 4)
-        *reinterpret_cast<float4*>(Sg + (size_t)e * D + mh + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+        *reinterpret_cast<float4*>(Sg + (size_t)e * D + mh + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
     }
   } else if (warp == 11) {
     // idle
