@@ -47,8 +47,6 @@ constexpr uint32_t B3_HALF = 32768, B4_HALF = 24576;
 // consecutive tokens' 4-column pieces are 512 contiguous bytes for the writer and the reader.
 __host__ __device__ constexpr int ut_index(int t, int col) { return ((col >> 2) * CH + t) * 4 + (col & 3); }
 
-__device__ __forceinline__ void bar_sync_main() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
-
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(bar)) : "memory");
 }
@@ -834,7 +832,7 @@ __device__ __forceinline__ void put_mn16(unsigned char* hi, unsigned char* lo, u
   *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   *reinterpret_cast<uint4*>(lo + off + sbo) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
 }
-constexpr int NTS = 448;   // warps 0-7 main, 8-9 and 12-13 epilogue, 10 loader (11 idle)
+constexpr int NTS = 448;   // warps 0-7 main, 8-9 and 12-13 epilogue, 10 loader, 11 MMA issue
 constexpr int MH = SW / 2; // columns per main warp: warp w takes lanes 32 (w % 4) and half w / 4
 constexpr int NDB = 4;     // D3 (output) accumulators in flight between the MMAs and the epilogue
 constexpr int XH = 2;      // epilogue column halves: partial sums per token and CTA
@@ -853,8 +851,8 @@ struct StateSmem {
   static constexpr uint32_t SOP = B4 + 2 * 24576;          // S slice as B operand, hi then lo
   static constexpr uint32_t UOP = SOP + 2 * SOP_HALF;      // U slice as B operand, hi then lo
   static constexpr uint32_t XBUF = UOP + 2 * UOP_HALF;     // f32 [NXB][NSL][XH][64] partial sums
-  static constexpr uint32_t BAR = XBUF + NXB * NSL * XH * 64 * 4;   // 20 mbarriers
-  static constexpr uint32_t MISC = BAR + 160;
+  static constexpr uint32_t BAR = XBUF + NXB * NSL * XH * 64 * 4;   // 22 mbarriers
+  static constexpr uint32_t MISC = BAR + 192;
   static constexpr uint32_t BYTES = MISC + 64;
 };
 
@@ -884,6 +882,8 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   uint64_t* dfull = bars + 8;    // [NDB] O of the chunk complete in D3[j] (MMA -> epilogue)
   uint64_t* dempty = bars + 12;  // [NDB] D3[j] read by the epilogue (epilogue -> MMA)
   uint64_t* xfull = bars + 16;   // [NXB] partial sums of the 4 slices arrived
+  uint64_t* sopf = bars + 20;    // S operand of the chunk written (main warps -> MMA warp)
+  uint64_t* uopf = bars + 21;    // U operand written, K~^T U read (main warps -> MMA warp)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
   int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);
 
@@ -901,7 +901,7 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     }
   }
   if (tid == 0) {
-    for (int i = 0; i < 20; ++i) tc::mbar_init(bars + i, (i >= 12 && i < 16) ? 128 : 1);
+    for (int i = 0; i < 22; ++i) tc::mbar_init(bars + i, (i >= 12 && i < 16) ? 128 : (i >= 20 ? 256 : 1));
     tc::mbar_fence_init();
     for (int i = 0; i < NXB; ++i) tc::mbar_arrive_expect_tx(xfull + i, NSL * XH * 64 * 4);   // chunks 0-3
   }
@@ -956,42 +956,16 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       }
     }
     float egL_next = nch > 0 ? *reinterpret_cast<const float*>(rec_of(0) + R_SC) : 1.f;
-    // operand descriptors, built once (K-step k: + 256 bytes for every tile; the S and U
-    // operands are MN-major)
-    const uint32_t id64 = tc::idesc_bf16_bmn(128, 2 * SW);
-    const uint64_t dA3h = tc::kstep_desc(tc::smem_u32(sm + S::B3), 128, 0);   // slot 0; slot 1 + 64 KiB
-    const uint64_t dA3l = tc::kstep_desc(tc::smem_u32(sm + S::B3 + B3_HALF), 128, 0);
-    const uint64_t dKh = tc::kstep_desc(tc::smem_u32(b4h) + 8192, 64, 0);
-    const uint64_t dKl = tc::kstep_desc(tc::smem_u32(b4l) + 8192, 64, 0);
-    const uint64_t dPh = tc::kstep_desc(tc::smem_u32(b4h), 64, 0);
-    const uint64_t dPl = tc::kstep_desc(tc::smem_u32(b4l), 64, 0);
-    const uint64_t dS = tc::sdesc(tc::smem_u32(soph), 128, SOP_SBO);
-    const uint64_t dU = tc::sdesc(tc::smem_u32(uoph), 128, UOP_SBO);
     for (int c = 0; c < nch; ++c) {
-      const uint32_t par = c & 1, b = c & 1;
-      const uint32_t jd = c & (NDB - 1);
-      const uint32_t d3 = tb + TC_D3 + 64 * jd;   // D3[jd]: rows 0-63 O (Q~ S + P U), rows 64-127 W S
+      const uint32_t par = c & 1;
+      const uint32_t d3 = tb + TC_D3 + 64 * (c & (NDB - 1));   // D3 of the chunk (W S in rows 64-127)
       // S slice (the chunk's initial state) -> B operand of W S and Q~ S
       const float egL = egL_next;
       if (c + 1 < nch) egL_next = *reinterpret_cast<const float*>(rec_of(c + 1) + R_SC);
       put_mn16(soph, sopl, SOP_SBO, e, mh, sv);
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
-      bar_sync_main();
-      tc::fence_after_sync();
-      if (tid == 0 && wait_or_abort(b3full + b, (c >> 1) & 1, abort, status) &&
-          (c < NDB || wait_or_abort(dempty + jd, ((c / NDB) - 1) & 1, abort, status))) {
-        tc::fence_after_sync();
-        const uint32_t so = 65536u * b;   // B3 slot of the chunk
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {   // B = [S_hi ; S_lo], 64 rows
-          const uint64_t bk = tc::desc_add(dS, 256 * k);
-          tc::mma_bf16(d3, tc::desc_add(dA3h, so + 256 * k), bk, id64, k > 0);
-          tc::mma_bf16(d3, tc::desc_add(dA3l, so + 256 * k), bk, id64, 1);
-        }
-        tc::mma_commit(mma3);
-        tc::mma_commit(b3empty + b);
-      }
+      mbar_arrive(sopf);
       wait_or_abort(mma3, par, abort, status);
       tc::fence_after_sync();
       // U = U~ - W S (tokens 0..63 on lanes 64..127) -> B operand
@@ -1018,30 +992,10 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
           }
         }
       }
+      // (every main thread arrives: its TMEM reads of the previous K~^T U are complete too)
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
-      bar_sync_main();
-      tc::fence_after_sync();
-      if (tid == 0 && wait_or_abort(b4full, par, abort, status)) {
-        tc::fence_after_sync();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {   // K~^T U, fresh   (B4 rows 64..191; B = [U_hi ; U_lo])
-          const uint64_t bk = tc::desc_add(dU, 256 * k);
-          tc::mma_bf16(tb + TC_S, tc::desc_add(dKh, 256 * k), bk, id64, k > 0);
-          tc::mma_bf16(tb + TC_S, tc::desc_add(dKl, 256 * k), bk, id64, 1);
-        }
-        tc::mma_commit(sready);   // the next chunk's S conversion overlaps the O products below
-        // D3 += [P ; K~^T rows 0..63] U: rows 0..63 become O; rows 64..127 (W S, consumed) are
-        // left as scratch
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t bk = tc::desc_add(dU, 256 * k);
-          tc::mma_bf16(d3, tc::desc_add(dPh, 256 * k), bk, id64, 1);
-          tc::mma_bf16(d3, tc::desc_add(dPl, 256 * k), bk, id64, 1);
-        }
-        tc::mma_commit(b4empty);
-        tc::mma_commit(dfull + jd);
-      }
+      mbar_arrive(uopf);
       // S <- e^{gamma_L} S + K~^T U.  The O products may still run: they read only B4 and the U
       // operand (rewritten only after the next chunk's MMA3, which the pipe orders after them)
       // and write D3[jd], which the next chunk does not touch.
@@ -1066,7 +1020,59 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         *reinterpret_cast<float4*>(Sg + (size_t)e * D + mh + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
     }
   } else if (warp == 11) {
-    // idle
+    // ================= MMA warp: one thread issues every product of the chunk step, so that no
+    // main thread waits on the tensor pipe's instruction queue
+    if (lane == 0) {
+    // operand descriptors, built once (K-step k: + 256 bytes for every tile; the S and U
+      // operands are MN-major)
+      const uint32_t id64 = tc::idesc_bf16_bmn(128, 2 * SW);
+      const uint64_t dA3h = tc::kstep_desc(tc::smem_u32(sm + S::B3), 128, 0);   // slot 0; slot 1 + 64 KiB
+      const uint64_t dA3l = tc::kstep_desc(tc::smem_u32(sm + S::B3 + B3_HALF), 128, 0);
+      const uint64_t dKh = tc::kstep_desc(tc::smem_u32(b4h) + 8192, 64, 0);
+      const uint64_t dKl = tc::kstep_desc(tc::smem_u32(b4l) + 8192, 64, 0);
+      const uint64_t dPh = tc::kstep_desc(tc::smem_u32(b4h), 64, 0);
+      const uint64_t dPl = tc::kstep_desc(tc::smem_u32(b4l), 64, 0);
+      const uint64_t dS = tc::sdesc(tc::smem_u32(soph), 128, SOP_SBO);
+      const uint64_t dU = tc::sdesc(tc::smem_u32(uoph), 128, UOP_SBO);
+      for (int c = 0; c < nch; ++c) {
+        const uint32_t par = c & 1, b = c & 1;
+        const uint32_t jd = c & (NDB - 1);
+        const uint32_t d3 = tb + TC_D3 + 64 * jd;   // D3[jd]: rows 0-63 O (Q~ S + P U), rows 64-127 W S
+        if (wait_or_abort(sopf, par, abort, status) && wait_or_abort(b3full + b, (c >> 1) & 1, abort, status) &&
+            (c < NDB || wait_or_abort(dempty + jd, ((c / NDB) - 1) & 1, abort, status))) {
+          tc::fence_after_sync();
+          const uint32_t so = 65536u * b;   // B3 slot of the chunk
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {   // B = [S_hi ; S_lo], 64 rows
+            const uint64_t bk = tc::desc_add(dS, 256 * k);
+            tc::mma_bf16(d3, tc::desc_add(dA3h, so + 256 * k), bk, id64, k > 0);
+            tc::mma_bf16(d3, tc::desc_add(dA3l, so + 256 * k), bk, id64, 1);
+          }
+          tc::mma_commit(mma3);
+          tc::mma_commit(b3empty + b);
+        }
+        if (wait_or_abort(uopf, par, abort, status) && wait_or_abort(b4full, par, abort, status)) {
+          tc::fence_after_sync();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {   // K~^T U, fresh   (B4 rows 64..191; B = [U_hi ; U_lo])
+            const uint64_t bk = tc::desc_add(dU, 256 * k);
+            tc::mma_bf16(tb + TC_S, tc::desc_add(dKh, 256 * k), bk, id64, k > 0);
+            tc::mma_bf16(tb + TC_S, tc::desc_add(dKl, 256 * k), bk, id64, 1);
+          }
+          tc::mma_commit(sready);   // the next chunk's S conversion overlaps the O products below
+          // D3 += [P ; K~^T rows 0..63] U: rows 0..63 become O; rows 64..127 (W S, consumed) are
+          // left as scratch
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t bk = tc::desc_add(dU, 256 * k);
+            tc::mma_bf16(d3, tc::desc_add(dPh, 256 * k), bk, id64, 1);
+            tc::mma_bf16(d3, tc::desc_add(dPl, 256 * k), bk, id64, 1);
+          }
+          tc::mma_commit(b4empty);
+          tc::mma_commit(dfull + jd);
+        }
+      }
+    }
   } else if (warp == 10) {
     // ================= loader warp: bulk copies of the chunks' operand images, each issued as soon
     // as MMA has finished reading the buffer it refills (B3 double-buffered, B4 single)
