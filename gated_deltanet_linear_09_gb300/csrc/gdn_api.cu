@@ -69,6 +69,7 @@ size_t gdn_state_slot_bytes(const gdn_dims* dims, gdn_dtype act) {
 int gdn_conv1d_update(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
                       const int32_t* slot_idx, int32_t B, const void* qkv_in, void* qkv_out,
                       cudaStream_t stream) {
+  GDN_CALL_RANGE("gdn_conv1d_update");
   gdn::KDims d;
   int rc;
   if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
@@ -84,6 +85,7 @@ int gdn_conv1d_update(const gdn_dims* dims, const gdn_weights* w, const gdn_pool
 int gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
                     const int32_t* slot_idx, int32_t B, const void* qkv, const void* z,
                     const void* a, const void* b, void* out, cudaStream_t stream) {
+  GDN_CALL_RANGE("gdn_decode_step");
   gdn::KDims d;
   int rc;
   if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
@@ -100,6 +102,7 @@ int gdn_decode_step(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* 
 int gdn_decode_multi(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
                      const int32_t* slot_idx, int32_t B, int32_t T, const void* qkv,
                      const void* z, const void* a, const void* b, void* out, cudaStream_t stream) {
+  GDN_CALL_RANGE("gdn_decode_multi");
   gdn::KDims d;
   int rc;
   if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
@@ -126,6 +129,7 @@ int gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, const gdn_po
                         const uint8_t* has_initial_state, int32_t num_seqs, int32_t total_tokens,
                         const void* qkv, const void* z, const void* a, const void* b, void* out,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  GDN_CALL_RANGE("gdn_prefill_chunked");
   gdn::KDims d;
   int rc;
   if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
@@ -139,13 +143,15 @@ int gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, const gdn_po
   if (total_tokens > 0 && (!aligned16(qkv) || !aligned16(z) || !aligned16(out)))
     return GDN_ERR_MISALIGNED;
   const bool tc = gdn::prefill_tc_supported(d);
-  const size_t need = tc ? gdn::prefill_tc_ws_bytes(d, num_seqs, total_tokens)
+  // the tensor-core path takes any workspace of at least one chunk's records (windows of whole
+  // chunks); the CUDA-core path needs the full size
+  const size_t need = tc ? gdn::prefill_tc_ws_min_bytes(d)
                          : gdn::prefill_ws_layout(d, num_seqs, total_tokens, nullptr).bytes;
   if (!workspace || workspace_bytes < need) return GDN_ERR_WORKSPACE_TOO_SMALL;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return GDN_ERR_MISALIGNED;
   if (tc)
     return gdn::launch_prefill_tc(d, w, pool, cu_seqlens, slot_idx, has_initial_state, num_seqs,
-                                  total_tokens, qkv, z, a, b, out, workspace, stream);
+                                  total_tokens, qkv, z, a, b, out, workspace, workspace_bytes, stream);
   const gdn::PrefillWs ws = gdn::prefill_ws_layout(d, num_seqs, total_tokens, workspace);
   return gdn::launch_prefill(d, w, pool, cu_seqlens, slot_idx, has_initial_state, num_seqs,
                              total_tokens, qkv, z, a, b, out, ws, stream);
@@ -154,6 +160,7 @@ int gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, const gdn_po
 int gdn_state_compact(const gdn_dims* dims, gdn_dtype act, const gdn_pool* pool,
                       const int32_t* src_slots, const int32_t* dst_slots, int32_t n,
                       cudaStream_t stream) {
+  GDN_CALL_RANGE("gdn_state_compact");
   gdn::KDims d;
   int rc;
   if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
@@ -186,6 +193,7 @@ size_t gdn_proj_packed_bytes(int32_t N, int32_t K) {
 
 int gdn_proj_pack(const void* w, int32_t N, int32_t K, void* packed, size_t packed_bytes,
                   cudaStream_t stream) {
+  GDN_CALL_RANGE("gdn_proj_pack");
   if (!w || !packed || N < 1 || K < 1) return GDN_ERR_INVALID_ARG;
   if (K % 64 != 0) return GDN_ERR_UNSUPPORTED_SHAPE;
   if ((long long)N * K > (1LL << 40)) return GDN_ERR_TOO_LARGE;
@@ -197,6 +205,7 @@ int gdn_proj_pack(const void* w, int32_t N, int32_t K, void* packed, size_t pack
 int gdn_linear_bf16(const void* x, const void* w, int32_t M, int32_t N, int32_t K,
                     const gdn_proj_route* route, int32_t k_split, int32_t* status,
                     cudaStream_t stream) {
+  GDN_CALL_RANGE("gdn_linear_bf16");
   if (M < 0 || N < 1 || K < 1) return GDN_ERR_INVALID_ARG;
   if (K % 64 != 0) return GDN_ERR_UNSUPPORTED_SHAPE;
   if (M > 65535 * 64) return GDN_ERR_TOO_LARGE;
@@ -226,6 +235,7 @@ int gdn_linear_bf16(const void* x, const void* w, int32_t M, int32_t N, int32_t 
 int gdn_in_proj(const gdn_dims* dims, const void* hidden, const void* w_in, int32_t rows,
                 int32_t hidden_size, void* qkv, void* z, void* b, void* a, int32_t* status,
                 cudaStream_t stream) {
+  GDN_CALL_RANGE("gdn_in_proj");
   gdn::KDims d;
   int rc;
   if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;
@@ -252,6 +262,7 @@ int gdn_in_proj(const gdn_dims* dims, const void* hidden, const void* w_in, int3
 
 int gdn_out_proj(const gdn_dims* dims, const void* out, const void* w_out, int32_t rows,
                  int32_t hidden_size, void* y, int32_t* status, cudaStream_t stream) {
+  GDN_CALL_RANGE("gdn_out_proj");
   gdn::KDims d;
   int rc;
   if ((rc = check_dims(dims, &d)) != GDN_OK) return rc;

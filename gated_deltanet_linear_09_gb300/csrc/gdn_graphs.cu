@@ -46,6 +46,7 @@ extern "C" {
 
 int gdn_decode_graphs_create(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
                              const int32_t* buckets, int32_t n_buckets, gdn_decode_graphs** out) {
+  GDN_CALL_RANGE("gdn_decode_graphs_create");
   if (!out) return GDN_ERR_INVALID_ARG;
   *out = nullptr;
   if (!dims || !w || !pool || !buckets) return GDN_ERR_INVALID_ARG;
@@ -127,6 +128,7 @@ int gdn_decode_graphs_buffers(const gdn_decode_graphs* g, int32_t** slot_idx, vo
 }
 
 int gdn_decode_graphs_launch(gdn_decode_graphs* g, int32_t B, cudaStream_t stream) {
+  GDN_CALL_RANGE("gdn_decode_graphs_launch");
   if (!g || B < 0) return GDN_ERR_INVALID_ARG;
   if (B > g->buckets[g->nb - 1]) return GDN_ERR_TOO_LARGE;
   if (B == 0) return GDN_OK;

@@ -3,7 +3,35 @@
 
 #include "gdn_common.cuh"
 
+// NVTX ranges around the C-ABI calls: a profiler or tracer attached to the process sees each call
+// as a named range on the calling thread (with none attached a range costs a few nanoseconds).
+// Compiled out when the NVTX headers are not available.
+#if defined(__has_include)
+#if __has_include(<nvtx3/nvToolsExt.h>)
+#include <nvtx3/nvToolsExt.h>
+#define GDN_NVTX 1
+#endif
+#endif
+
 namespace gdn {
+
+struct CallRange {
+  explicit CallRange(const char* name) {
+#ifdef GDN_NVTX
+    nvtxRangePushA(name);
+#else
+    (void)name;
+#endif
+  }
+  ~CallRange() {
+#ifdef GDN_NVTX
+    nvtxRangePop();
+#endif
+  }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+#define GDN_CALL_RANGE(name) ::gdn::CallRange gdn_call_range_(name)
 
 int launch_decode(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
                   const int32_t* slot_idx, int B, const void* qkv, const void* z, const void* a,
@@ -45,10 +73,13 @@ int launch_prefill(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
 // Tensor-core (tcgen05) prefill for dk = dv = 128.
 bool prefill_tc_supported(const KDims& d);
 size_t prefill_tc_ws_bytes(const KDims& d, int num_seqs, int total_tokens);
+// The smallest workspace the tensor-core prefill accepts: the records of one chunk.  Smaller
+// workspaces than prefill_tc_ws_bytes run the call in windows of whole chunks.
+size_t prefill_tc_ws_min_bytes(const KDims& d);
 int launch_prefill_tc(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
                       const int32_t* cu_seqlens, const int32_t* slot_idx, const uint8_t* has_init,
                       int num_seqs, int total_tokens, const void* qkv, const void* z, const void* a,
-                      const void* b, void* out, void* ws, cudaStream_t stream);
+                      const void* b, void* out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 // Dense bf16 projection (tcgen05 GEMM) with a routing epilogue: output feature n of row m goes
 // to ptr[s][m * ld[s] + n - start[s]] for the segment s holding n.

@@ -43,15 +43,19 @@ extern "C" int gdn_prefill_chunked_noalloc(const gdn_dims* dims, const gdn_weigh
                                            int32_t total_tokens, const void* qkv, const void* z,
                                            const void* a, const void* b, void* out,
                                            cudaStream_t stream) {
+  GDN_CALL_RANGE("gdn_prefill_chunked_noalloc");
   if (num_seqs < 0 || total_tokens < 0) return GDN_ERR_INVALID_ARG;
+  // The address comes first, so that even an empty call (no sequences) makes the driver create
+  // the array on this device: with lazy module loading that happens on first use, and a caller
+  // that reserves the rest of the device memory afterwards wants it to have happened already.
+  void* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc != GDN_OK) return rc;
   const size_t need = gdn_prefill_workspace_bytes(dims, num_seqs, total_tokens);
   if (need == 0) return gdn_prefill_chunked(dims, w, pool, cu_seqlens, slot_idx, has_initial_state,
                                             num_seqs, total_tokens, qkv, z, a, b, out, nullptr, 0,
                                             stream);
   if (need > (size_t)GDN_NOALLOC_PREFILL_SCRATCH_BYTES) return GDN_ERR_TOO_LARGE;
-  void* scratch = nullptr;
-  const int rc = scratch_address(&scratch);
-  if (rc != GDN_OK) return rc;
   return gdn_prefill_chunked(dims, w, pool, cu_seqlens, slot_idx, has_initial_state, num_seqs,
                              total_tokens, qkv, z, a, b, out, scratch,
                              (size_t)GDN_NOALLOC_PREFILL_SCRATCH_BYTES, stream);

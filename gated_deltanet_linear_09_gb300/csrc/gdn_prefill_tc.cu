@@ -23,6 +23,8 @@
 // Precision: every product runs as three bf16 passes on split operands
 // (x = hi + lo, hi = bf16(x), lo = bf16(x - hi): A_hi B_hi + A_hi B_lo + A_lo B_hi) with f32
 // accumulation in TMEM, which keeps about 16 significant bits per operand.
+#include <algorithm>
+
 #include "gdn_internal.h"
 #include "gdn_tc.cuh"
 
@@ -516,7 +518,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ slot_idx,
                 const uint8_t* __restrict__ has_init, int num_seqs, int total,
                 const T* __restrict__ qkv, const T* __restrict__ a, const T* __restrict__ b,
-                float* __restrict__ ws, int32_t* __restrict__ status) {
+                float* __restrict__ ws, int cw0, int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
   using S = IntraSmem;
   using R = InRing<T>;
@@ -531,7 +533,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
   int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);   // ok, t0, L, seq, seq_start, abort
 
-  const int c = blockIdx.x, kh = blockIdx.y;
+  const int c = cw0 + blockIdx.x, kh = blockIdx.y;   // global chunk index; records from cw0
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = d.r, h0 = kh * r;
   if (warp == 0) {
@@ -557,7 +559,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   const bool init = valid && has_init != nullptr && __ldg(has_init + seq) != 0;
   const T* cs = conv_state + (size_t)(valid ? s : 0) * 3 * d.cqkv;
   auto rec_of = [&](int j) {
-    return reinterpret_cast<unsigned char*>(ws) + ((size_t)c * d.Hv + h0 + j) * REC_BYTES;
+    return reinterpret_cast<unsigned char*>(ws) + ((size_t)(c - cw0) * d.Hv + h0 + j) * REC_BYTES;
   };
 
   // ---- every input tensor of the chunk into the ring: k, q, v of V-head 0, 1, ... (tensor i in
@@ -862,7 +864,8 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
                 T* __restrict__ conv_state, int num_slots, const int32_t* __restrict__ cu,
                 const int32_t* __restrict__ slot_idx, const uint8_t* __restrict__ has_init,
                 int num_seqs, int total, const T* __restrict__ qkv, const T* __restrict__ z,
-                T* __restrict__ out, const float* __restrict__ ws, int32_t* __restrict__ status) {
+                T* __restrict__ out, const float* __restrict__ ws, int cw0, int cw1,
+                int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
   using S = StateSmem;
   unsigned char* b4h = sm + S::B4;
@@ -913,16 +916,26 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   const uint32_t tb = *tslot;
   const int choff = sh[1];
   volatile int* abort = sh + 2;
-  const int seq_start = __ldg(cu + n), len = __ldg(cu + n + 1) - seq_start;
-  const int nch = sh[0] ? (len + CH - 1) / CH : 0;
+  const int seq_start0 = __ldg(cu + n), len0 = __ldg(cu + n + 1) - seq_start0;
+  const int nch_seq = sh[0] ? (len0 + CH - 1) / CH : 0;
+  // The call's global chunks [cw0, cw1) form this window: the sequence's chunks [ca, cb) of it
+  // run here, as local chunks 0 .. nch - 1, starting from the slot's state when an earlier window
+  // (or has_initial_state) left one there.
+  const int ca = max(0, cw0 - choff), cb = min(nch_seq, cw1 - choff);
+  const int nch = max(0, cb - ca);
+  const bool empty_here = nch_seq == 0 && cw0 == 0;   // an empty sequence resets its slot once
+  const int seq_start = seq_start0 + ca * CH, len = len0 - ca * CH;   // tokens from the window on
   const int s = __ldg(slot_idx + n);
   // invalid cu_seqlens: nothing is read or written (the CTA still takes part in the cluster syncs)
-  const bool valid = sh[0] && s >= 0 && s < num_slots;
-  if (sh[0] && s >= num_slots && h == 0 && sig == 0 && tid == 0) set_status(status, GDN_STATUS_SLOT_RANGE);
-  const bool init = valid && has_init != nullptr && __ldg(has_init + n) != 0;
+  const bool valid = sh[0] && s >= 0 && s < num_slots && (nch > 0 || empty_here);
+  if (sh[0] && s >= num_slots && h == 0 && sig == 0 && tid == 0 && (nch > 0 || empty_here))
+    set_status(status, GDN_STATUS_SLOT_RANGE);
+  const bool init_seq = valid && has_init != nullptr && __ldg(has_init + n) != 0;
+  const bool init = valid && (init_seq || ca > 0);
+  const bool seq_ends = valid && ((nch > 0 && cb == nch_seq) || empty_here);
   float* Sg = rec_state + ((size_t)(valid ? s : 0) * d.Hv + h) * D * D + sig * SW;
   auto rec_of = [&](int c) {
-    return reinterpret_cast<const unsigned char*>(ws) + ((size_t)(choff + c) * d.Hv + h) * REC_BYTES;
+    return reinterpret_cast<const unsigned char*>(ws) + ((size_t)(choff + ca + c - cw0) * d.Hv + h) * REC_BYTES;
   };
 
   if (warp < 8) {
@@ -1203,15 +1216,15 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, TC_COLS);
   // conv state <- the sequence's last K-1 raw inputs (older ones kept when continuing)
-  if (valid && h == 0 && sig == 0) {
+  if (seq_ends && h == 0 && sig == 0) {
     T* csw = conv_state + (size_t)s * 3 * d.cqkv;
     for (int cch = tid; cch < d.cqkv; cch += NTS) {
       T v3[3];
 #pragma unroll
       for (int m = 0; m < 3; ++m) {
-        const int rel = len - 3 + m;
-        if (rel >= 0) v3[m] = qkv[(size_t)(seq_start + rel) * d.cqkv + cch];
-        else v3[m] = init ? csw[(size_t)(3 + rel) * d.cqkv + cch] : Act<T>::cvt(0.f);
+        const int rel = len0 - 3 + m;
+        if (rel >= 0) v3[m] = qkv[(size_t)(seq_start0 + rel) * d.cqkv + cch];
+        else v3[m] = init_seq ? csw[(size_t)(3 + rel) * d.cqkv + cch] : Act<T>::cvt(0.f);
       }
 #pragma unroll
       for (int m = 0; m < 3; ++m) csw[(size_t)m * d.cqkv + cch] = v3[m];
@@ -1224,8 +1237,15 @@ template <typename T>
 int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const int32_t* cu,
              const int32_t* slot_idx, const uint8_t* has_init, int num_seqs, int total,
              const void* qkv, const void* z, const void* a, const void* b, void* out, void* ws,
-             cudaStream_t stream) {
+             size_t ws_bytes, cudaStream_t stream) {
+  // Chunks are numbered across the sequences; at most total / 64 + num_seqs of them exist.  The
+  // records of `win` consecutive chunks fit the workspace, so the call runs in windows of that
+  // many chunks: each window's intra kernel, then its state kernel, which carries every
+  // sequence's state to the next window through the slot.
   const int nc_max = total / CH + num_seqs;
+  const size_t per_chunk = (size_t)d.Hv * REC_BYTES;
+  const int win = (int)std::min<size_t>((size_t)nc_max, ws_bytes / per_chunk);
+  if (win < 1) return GDN_ERR_WORKSPACE_TOO_SMALL;
   auto k1 = tc_intra_kernel<T>;
   auto k2 = tc_state_kernel<T>;
   if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IntraSmem::BYTES) !=
@@ -1234,17 +1254,21 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
           cudaSuccess)
     return GDN_ERR_CUDA;
   float* wsf = static_cast<float*>(ws);
-  if (total > 0)
-    k1<<<dim3(nc_max, d.Hk), NTI, IntraSmem::BYTES, stream>>>(
-        d, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
-        static_cast<const T*>(pool->conv_state), pool->num_slots, cu, slot_idx, has_init, num_seqs,
-        total, static_cast<const T*>(qkv), static_cast<const T*>(a), static_cast<const T*>(b), wsf,
-        pool->status);
-  k2<<<dim3(NSL * num_seqs, d.Hv), NTS, StateSmem::BYTES, stream>>>(
-      d, static_cast<const T*>(w->norm_weight), pool->rec_state, static_cast<T*>(pool->conv_state),
-      pool->num_slots, cu, slot_idx, has_init, num_seqs, total, static_cast<const T*>(qkv),
-      static_cast<const T*>(z), static_cast<T*>(out), wsf, pool->status);
-  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  for (int cw0 = 0; cw0 < nc_max; cw0 += win) {
+    const int cw1 = std::min(nc_max, cw0 + win);
+    if (total > 0)
+      k1<<<dim3(cw1 - cw0, d.Hk), NTI, IntraSmem::BYTES, stream>>>(
+          d, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
+          static_cast<const T*>(pool->conv_state), pool->num_slots, cu, slot_idx, has_init, num_seqs,
+          total, static_cast<const T*>(qkv), static_cast<const T*>(a), static_cast<const T*>(b), wsf,
+          cw0, pool->status);
+    k2<<<dim3(NSL * num_seqs, d.Hv), NTS, StateSmem::BYTES, stream>>>(
+        d, static_cast<const T*>(w->norm_weight), pool->rec_state, static_cast<T*>(pool->conv_state),
+        pool->num_slots, cu, slot_idx, has_init, num_seqs, total, static_cast<const T*>(qkv),
+        static_cast<const T*>(z), static_cast<T*>(out), wsf, cw0, cw1, pool->status);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  return GDN_OK;
 }
 
 }  // namespace
@@ -1255,15 +1279,17 @@ size_t prefill_tc_ws_bytes(const KDims& d, int num_seqs, int total) {
   return (size_t)(total / CH + num_seqs) * d.Hv * REC_BYTES;
 }
 
+size_t prefill_tc_ws_min_bytes(const KDims& d) { return (size_t)d.Hv * REC_BYTES; }
+
 int launch_prefill_tc(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
                       const int32_t* cu, const int32_t* slot_idx, const uint8_t* has_init,
                       int num_seqs, int total, const void* qkv, const void* z, const void* a,
-                      const void* b, void* out, void* ws, cudaStream_t stream) {
+                      const void* b, void* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (w->act == GDN_BF16)
     return launch_t<__nv_bfloat16>(d, w, pool, cu, slot_idx, has_init, num_seqs, total, qkv, z, a,
-                                   b, out, ws, stream);
+                                   b, out, ws, ws_bytes, stream);
   return launch_t<float>(d, w, pool, cu, slot_idx, has_init, num_seqs, total, qkv, z, a, b, out,
-                         ws, stream);
+                         ws, ws_bytes, stream);
 }
 
 }  // namespace gdn

@@ -52,6 +52,7 @@ class GatedDeltaNetLayer:
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.pool = gdn.make_pool(self.rec_state, self.conv_state, self.status)
         self._ws = None
+        self.ws_cap = None   # bytes: a smaller prefill workspace (windows of whole chunks)
 
     @property
     def num_slots(self) -> int:
@@ -108,9 +109,12 @@ class GatedDeltaNetLayer:
 
     def workspace(self, num_seqs: int, total_tokens: int) -> torch.Tensor:
         need = gdn.gdn_prefill_workspace_bytes(self.dims, num_seqs, total_tokens)
+        if self.ws_cap is not None:
+            # head dims 128: the prefill runs in windows of whole chunks that fit the workspace
+            need = max(gdn.gdn_prefill_workspace_bytes(self.dims, 1, 1), min(need, self.ws_cap))
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
-        return self._ws
+        return self._ws[:max(need, 256)]
 
     def prefill(self, cu_seqlens, slot_idx, has_init, qkv, z, a, b, out=None, stream=None):
         """cu_seqlens/slot_idx/has_init: device tensors (int32, int32, uint8 or None)."""

@@ -221,7 +221,11 @@ int gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, const gdn_po
  *   Size limit: returns GDN_ERR_TOO_LARGE, launching nothing, when
  *     gdn_prefill_workspace_bytes(dims, num_seqs, total_tokens) > GDN_NOALLOC_PREFILL_SCRATCH_BYTES.
  *   First call per device: looks up the array's device address (cudaGetSymbolAddress, with that
- *     device current) and caches it; make that first call before any stream capture.
+ *     device current) and caches it; make that first call before any stream capture.  With lazy
+ *     module loading (the CUDA default) the driver creates the array at that lookup, so a caller
+ *     that reserves the rest of device memory at start-up should first make one empty call
+ *     (num_seqs = 0, total_tokens = 0) on each device.  The cached address belongs to the
+ *     device's current context: a cudaDeviceReset between calls is not supported.
  *   Sharing: every call uses the same array, which keeps the last call's contents; the prefill
  *     writes every scratch value before it reads it, so nothing needs clearing.  Calls whose
  *     kernels overlap on the GPU (other streams, other host threads) race on the array:

@@ -14,6 +14,9 @@ and the oracle's outputs compared with the matching columns of the GPU outputs.
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 from gated_deltanet_linear_09_gb300 import synth
@@ -40,8 +43,20 @@ def out_err(gpu, ref, act):
     return excess <= 0.0, float(err.max()) if err.size else 0.0, excess
 
 
+def record(kind: str, what: str, value: float):
+    """Appends one measured parity figure (raw output max-abs, state rel-L2) as a JSON line to the
+    file named by GDN_PARITY_REPORT, when that variable is set."""
+    path = os.environ.get("GDN_PARITY_REPORT")
+    if not path:
+        return
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    with open(path, "a") as f:
+        f.write(json.dumps({"test": test, "kind": kind, "what": what, "value": value}) + "\n")
+
+
 def assert_out_close(gpu, ref, act, what=""):
     ok, mx, ex = out_err(gpu, ref, act)
+    record("out_max_abs_" + act, what, mx)
     assert ok, f"{what}: output max-abs {mx:.3e} exceeds the bound by {ex:.3e}"
     return mx
 
@@ -55,8 +70,38 @@ def rel_l2(gpu, ref):
 
 def assert_state_close(gpu, ref, what=""):
     r = rel_l2(gpu, ref)
+    record("state_rel_l2", what, r)
     assert r <= STATE_RTOL, f"{what}: state rel-L2 {r:.3e} > {STATE_RTOL}"
     return r
+
+
+GUARD_BYTES = 4096
+CANARY = 0xA5
+
+
+class Guarded:
+    """A device buffer with canary bytes before and after it: the stand-in for an out-of-bounds
+    write checker.  `view` is the buffer proper (GUARD_BYTES past a 512-byte aligned allocation,
+    so it keeps the alignments the ABI asks for); check() asserts that both guard regions still
+    hold the canary pattern, byte for byte."""
+
+    def __init__(self, shape, dtype, fill=None):
+        import torch
+        n = 1
+        for x in shape:
+            n *= int(x)
+        self.nbytes = n * torch.empty((), dtype=dtype).element_size()
+        self.buf = torch.full((GUARD_BYTES + self.nbytes + GUARD_BYTES,), CANARY, dtype=torch.uint8,
+                              device="cuda")
+        self.view = self.buf[GUARD_BYTES:GUARD_BYTES + self.nbytes].view(dtype).view(tuple(shape))
+        if fill is not None:
+            self.view.fill_(fill)
+
+    def check(self, what=""):
+        head = self.buf[:GUARD_BYTES]
+        tail = self.buf[GUARD_BYTES + self.nbytes:]
+        assert bool((head == CANARY).all()), f"{what}: write before the buffer"
+        assert bool((tail == CANARY).all()), f"{what}: write past the end of the buffer"
 
 
 class HeadSlice:

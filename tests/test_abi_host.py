@@ -169,9 +169,19 @@ def test_prefill_and_compact_host_checks(lib):
     w = gdn.gdn_weights(0x20000, 0x20000, 0x20000, 0x20000, gdn.GDN_BF16)
     p = gdn.gdn_pool(0x30000, 0x30000, 4, None)
     need = lib.gdn_prefill_workspace_bytes(ctypes.byref(d), 2, 100)
+    # head dims 128 run in windows of whole chunks: the smallest workspace is one chunk's records
+    # (the size quoted for one token), a byte less is refused
+    least = lib.gdn_prefill_workspace_bytes(ctypes.byref(d), 1, 1)
+    assert 0 < least < need and least == lib.gdn_prefill_workspace_bytes(ctypes.byref(d), 1, 63)
     f = 0x10000
     rc = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(w), ctypes.byref(p), f, f, None, 2,
-                                 100, f, f, f, f, f, 0x50000, need - 1, None)
+                                 100, f, f, f, f, f, 0x50000, least - 1, None)
+    assert rc == -5
+    # head dims 64 (CUDA-core path) still need the full size
+    d64 = D(dk=64, dv=64)
+    need64 = lib.gdn_prefill_workspace_bytes(ctypes.byref(d64), 2, 100)
+    rc = lib.gdn_prefill_chunked(ctypes.byref(d64), ctypes.byref(w), ctypes.byref(p), f, f, None, 2,
+                                 100, f, f, f, f, f, 0x50000, need64 - 1, None)
     assert rc == -5
     rc = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(w), ctypes.byref(p), f, f, None, 2,
                                  100, f, f, f, f, f, 0x50000 + 16, need, None)

@@ -186,6 +186,17 @@ def test_decode_large_B64_512_steps_with_compaction():
     _run_decode_workload(wl, rows=[0, 13, 31, 47, 63], k_heads=[0, 15], retire_at=256, n_retire=8)
 
 
+def test_decode_production_geometry_f32_outputs():
+    """The production head geometry (Hk=16, Hv=48, dk=dv=128, B=64 of 128 slots) in the f32
+    activation mode, where the outputs carry no bf16 rounding: every sampled output within a bare
+    2e-3 and the state within rel-L2 1e-4 after 256 steps."""
+    base = synth.workloads()[2]
+    wl = synth.Workload("decode_B64_Hk16_Hv48_d128_f32", synth.Geometry(16, 48, 128, 128, 4, synth.F32),
+                        base.seed + 100, num_slots=128, batch=64, steps=256, prefill_state=True)
+    _, mx = _run_decode_workload(wl, rows=[0, 21, 42, 63], k_heads=[0, 9, 15])
+    assert mx <= 2e-3
+
+
 # ------------------------------------------------------------------ conv1d and compaction
 
 @pytest.mark.parametrize("act", [synth.F32, synth.BF16])

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from gated_deltanet_linear_09_gb300 import synth
+from gated_deltanet_linear_09_gb300 import gdn, synth
 from gated_deltanet_linear_09_gb300.runtime import GatedDeltaNetLayer
 from gpu_util import HeadSlice, assert_out_close, assert_state_close, f64
 
@@ -202,3 +202,81 @@ def test_prefill_long_sequence_state_accuracy():
         assert_out_close(hs.out_cols(got), ref, geo.act, f"heads {k_heads}")
         assert_state_close(hs.rec(g_rec)[1], r64[1], f"final state heads {k_heads}")
         np.testing.assert_array_equal(hs.conv(g_conv)[1], c64[1])
+
+
+def _varlen_case(geo, seed):
+    lens = [1, 63, 0, 64, 65, 130, 2, 200, 129]
+    has_init = np.array([0, 1, 1, 0, 1, 0, 1, 1, 0], np.uint8)
+    n = len(lens)
+    N = n + 3
+    w = synth.make_weights(geo, seed)
+    rec, conv = synth.make_pool(geo, N, seed + 1, True)
+    cu = synth.cu_seqlens(lens)
+    slots = np.array([9, 0, 4, 2, 10, 5, 1, 7, 11], np.int32)
+    xs = synth.make_token_inputs(geo, int(cu[-1]), seed + 2)
+    return w, rec, conv, cu, slots, has_init, xs, N
+
+
+@pytest.mark.parametrize("cap_chunks", [1, 2, 5])
+def test_prefill_windowed_workspace(cap_chunks):
+    """A workspace of only `cap_chunks` chunks' records: the call runs in windows of whole chunks
+    (sequences cross window edges, an empty sequence, mixed initial states).  Outputs and states
+    against the oracle, and bit-equal to the same call with the full workspace."""
+    geo = synth.Geometry(2, 4, 128, 128, 4, synth.BF16)
+    w, rec, conv, cu, slots, has_init, xs, N = _varlen_case(geo, 670)
+    full = GatedDeltaNetLayer(geo, w, N)
+    capd = GatedDeltaNetLayer(geo, w, N)
+    one = gdn.gdn_prefill_workspace_bytes(capd.dims, 1, 1)
+    capd.ws_cap = cap_chunks * one
+    assert gdn.gdn_prefill_workspace_bytes(capd.dims, len(slots), int(cu[-1])) > capd.ws_cap
+    outs = []
+    for layer in (full, capd):
+        layer.load_state(rec, conv)
+        outs.append(layer.prefill(_dev_i32(cu), _dev_i32(slots), torch.from_numpy(has_init).cuda(),
+                                  **layer.inputs(xs)))
+    torch.cuda.synchronize()
+    assert capd._ws[:capd.ws_cap].numel() == capd.ws_cap
+    r64, c64 = rec.astype(np.float64), conv.astype(np.float64)
+    rc, ref = oracle.prefill(geo.oracle_dims(), f64(w), r64, c64, cu, slots, has_init, **f64(xs))
+    assert rc == 0
+    assert_out_close(_np(outs[1]), ref, geo.act, "windowed prefill outputs")
+    g_rec, g_conv = _np(capd.rec_state), _np(capd.conv_state)
+    for s in slots:
+        assert_state_close(g_rec[s], r64[s], f"slot {s}")
+        np.testing.assert_array_equal(g_conv[s], c64[s])
+    for s in (3, 6, 8):
+        np.testing.assert_array_equal(g_rec[s], rec[s])
+    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(full.rec_state, capd.rec_state)
+    assert torch.equal(full.conv_state, capd.conv_state)
+    assert int(capd.status.item()) == 0
+
+
+def test_prefill_65536_tokens_bounded_workspace():
+    """One 65,536-token sequence at the full head count (Hk=16, Hv=32, d=128) with the workspace
+    capped at 256 MiB (the single-window size would be 4.85 GB): outputs and final state of one
+    K-head (and its two V-heads) against the oracle."""
+    geo = synth.workloads()[3].geo
+    T = 65536
+    w = synth.make_weights(geo, 680)
+    layer = GatedDeltaNetLayer(geo, w, 1)
+    layer.ws_cap = 256 << 20
+    assert gdn.gdn_prefill_workspace_bytes(layer.dims, 1, T) > 4 * layer.ws_cap
+    xs = synth.make_token_inputs(geo, T, 681)
+    cu = np.array([0, T], np.int32)
+    slots = np.array([0], np.int32)
+    out = layer.prefill(_dev_i32(cu), _dev_i32(slots), None, **layer.inputs(xs))
+    torch.cuda.synchronize()
+    assert layer._ws.numel() <= layer.ws_cap
+    got = _np(out)
+    g_rec, g_conv = _np(layer.rec_state), _np(layer.conv_state)
+    hs = HeadSlice(geo, [9])
+    r64 = np.zeros((1, hs.sub.Hv, geo.dk, geo.dv))
+    c64 = np.zeros((1, geo.K - 1, hs.sub.cqkv))
+    rc, ref = oracle.prefill(hs.sub.oracle_dims(), hs.weights(w), r64, c64, cu, slots, None,
+                             **hs.inputs(xs))
+    assert rc == 0
+    assert_out_close(hs.out_cols(got), ref, geo.act, "65,536-token outputs, K-head 9")
+    assert_state_close(hs.rec(g_rec)[0], r64[0], "65,536-token final state, K-head 9")
+    np.testing.assert_array_equal(hs.conv(g_conv)[0], c64[0])
+    assert int(layer.status.item()) == 0

@@ -71,3 +71,14 @@ def test_noalloc_prefill_rejects_sizes_beyond_the_array():
         gdn.gdn_prefill_chunked_noalloc(layer.dims, layer.w, layer.pool, cu, sl, None, 1, T, x, x,
                                         x, x, x)
     assert e.value.code == -9
+
+
+def test_noalloc_empty_call_sets_up_the_array():
+    """An empty call (no sequences) returns GDN_OK after looking up the array's address, so a
+    caller can make the driver create the array before reserving the rest of device memory."""
+    gbuild.build()
+    geo = synth.Geometry(2, 4, 128, 128, 4, synth.BF16)
+    layer = GatedDeltaNetLayer(geo, synth.make_weights(geo, 904), 1)
+    gdn.gdn_prefill_chunked_noalloc(layer.dims, layer.w, layer.pool, None, None, None, 0, 0,
+                                    None, None, None, None, None)
+    torch.cuda.synchronize()
