@@ -194,7 +194,15 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.3)
+    # keep the GPU busy (not idle) between the warm-up and the timed region, so that the clocks
+    # and the memory system are in their loaded state when timing starts
+    t_busy = time.time() + 0.3
+    i = 0
+    while time.time() < t_busy:
+        for _ in range(50):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
@@ -366,6 +374,11 @@ def run_ours(args, ws, rank, local):
     del layer
     torch.cuda.empty_cache()
 
+    # ---------------- workload 1: B=16 decode with an L2 flush between steps; workload 4: mixed
+    # serving (varlen prefill, decode steps, retire / compact / admit)
+    b16 = time_decode_b16(torch, synth, GatedDeltaNetLayer, hbm_peak)
+    mixed = time_mixed(torch, synth, GatedDeltaNetLayer)
+
     # ---------------- the projections around the step
     proj = time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak)
 
@@ -422,6 +435,8 @@ def run_ours(args, ws, rank, local):
                          "state_bytes_per_token": state_bytes // (wl.batch * MULTI_T),
                          "single_step_tokens_per_s": round(wl.batch / (ms_step * 1e-3), 1)},
         "decode_graphs": dict(graph_us, buckets=[1, 2, 4, 8, 16, 32, 64]),
+        "decode_b16": b16,
+        "mixed_serving": mixed,
         "proj": proj,
         "compact": {"pairs": len(keep), "bytes": comp_bytes, "ms": round(comp_ms, 4),
                     "gbs": round(comp_bytes / (comp_ms * 1e-3) / 1e9, 1),
@@ -526,6 +541,119 @@ def time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak, reps=2
     return res
 
 
+def time_decode_b16(torch, synth, GatedDeltaNetLayer, hbm_peak, steps=64):
+    """Workload 1: B=16 rows of a 64-slot pool, Hk=16, Hv=32.  Its 67.1 MB of state traffic per
+    step would sit in the 129 MB L2, so every timed step is preceded (outside its events) by a
+    write of a 256 MB buffer that evicts it; the step times are summed from per-step events."""
+    wl = synth.workloads()[1]
+    geo = wl.geo
+    layer = GatedDeltaNetLayer(geo, synth.make_weights(geo, wl.seed), wl.num_slots)
+    rec, conv = synth.make_pool(geo, wl.num_slots, wl.seed, True)
+    layer.load_state(rec, conv)
+    del rec, conv
+    slots = torch.from_numpy(synth.make_slot_idx(wl.num_slots, wl.batch, wl.seed)).cuda()
+    ring = [layer.inputs(synth.decode_step_inputs(wl, t)) for t in range(4)]
+    out = torch.empty((wl.batch, geo.zdim), dtype=layer.act, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    state_bytes = 2 * wl.batch * geo.Hv * geo.dk * geo.dv * 4
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(3):
+        layer.decode_step(slots, out=out, **ring[i % 4])
+    for i in range(steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        layer.decode_step(slots, out=out, **ring[i % 4])
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+    gbs = state_bytes / (ms * 1e-3) / 1e9
+    del layer, flush, ring
+    torch.cuda.empty_cache()
+    return {"workload": wl.name, "rows": wl.batch, "us_per_step": round(ms * 1e3, 2),
+            "state_bytes_per_step": state_bytes, "gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / hbm_peak, 4),
+            "row_steps_per_s": round(wl.batch / (ms * 1e-3), 1),
+            "l2": "256 MB buffer written between steps, outside the timed events", "steps": steps}
+
+
+def time_mixed(torch, synth, GatedDeltaNetLayer):
+    """Workload 4, mixed serving: varlen prefill of 8 sequences (lengths ~ U[128, 8192]) into a
+    16-slot pool, then 512 decode steps over the 8 rows; every 64 steps 2 rows retire, the live
+    slots are compacted to the pool's prefix and 2 new sequences are admitted by prefill.  Every
+    input is staged on the device first; each call is timed with its own events and the phases
+    are summed (prefill tokens/s over all prefills, decode row-steps/s over all decode steps)."""
+    wl = synth.workloads()[4]
+    geo = wl.geo
+    layer = GatedDeltaNetLayer(geo, synth.make_weights(geo, wl.seed), wl.num_slots)
+    B = wl.batch
+    stream = torch.cuda.current_stream()
+
+    def i32(x):
+        return torch.from_numpy(np.asarray(x, np.int32)).cuda()
+
+    # the schedule, staged: (kind, args) in call order
+    plan = []
+    lens = synth.mixed_seq_lens(wl.seed, B, tag=0)
+    row_slots = synth.make_slot_idx(wl.num_slots, B, wl.seed)
+    plan.append(("prefill", lens, row_slots.copy(), 0))
+    for t in range(wl.steps):
+        if t > 0 and t % 64 == 0:
+            retire = synth.retire_choice(wl.seed, B, 2, t)
+            keep = np.array([i for i in range(B) if i not in set(retire.tolist())], np.int32)
+            dst = np.arange(len(keep), dtype=np.int32)
+            plan.append(("compact", row_slots[keep].tolist(), dst.tolist(), t))
+            new_lens = synth.mixed_seq_lens(wl.seed, 2, tag=t)
+            new_slots = np.array([len(keep), len(keep) + 1], np.int32)
+            plan.append(("prefill", new_lens, new_slots, t))
+            row_slots = np.concatenate([dst, new_slots]).astype(np.int32)
+        plan.append(("decode", None, row_slots.copy(), t))
+    staged = []
+    for kind, a, sl, t in plan:
+        if kind == "prefill":
+            cu = synth.cu_seqlens(a)
+            xs = layer.inputs(synth.make_token_inputs(geo, int(cu[-1]), wl.seed, 7, t))
+            staged.append((kind, (i32(cu), i32(sl), xs, int(cu[-1]))))
+        elif kind == "decode":
+            staged.append((kind, (i32(sl), layer.inputs(synth.make_token_inputs(geo, B, wl.seed, 100, t)))))
+        else:
+            staged.append((kind, (a, sl)))
+    max_tokens = max(v[3] for k, v in staged if k == "prefill")
+    layer.workspace(B, max_tokens)
+    out_p = torch.empty((max_tokens, geo.zdim), dtype=layer.act, device="cuda")
+    out_d = torch.empty((B, geo.zdim), dtype=layer.act, device="cuda")
+    torch.cuda.synchronize()
+    times = {"prefill": [], "decode": [], "compact": []}
+    tokens = 0
+    for kind, v in staged:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        if kind == "prefill":
+            cu, sl, xs, T = v
+            layer.prefill(cu, sl, None, out=out_p[:T], **xs)
+            tokens += T
+        elif kind == "decode":
+            sl, xs = v
+            layer.decode_step(sl, out=out_d, **xs)
+        else:
+            layer.compact(*v)
+        e1.record(stream)
+        times[kind].append((e0, e1))
+    torch.cuda.synchronize()
+    ms = {k: sum(a.elapsed_time(b) for a, b in evs) for k, evs in times.items()}
+    status = int(layer.status.item())
+    del layer, staged, out_p
+    torch.cuda.empty_cache()
+    return {"workload": wl.name, "prefill_tokens": tokens, "prefill_calls": len(times["prefill"]),
+            "prefill_ms": round(ms["prefill"], 3),
+            "prefill_tokens_per_s": round(tokens / (ms["prefill"] * 1e-3), 1),
+            "decode_steps": len(times["decode"]), "rows": B, "decode_ms": round(ms["decode"], 3),
+            "decode_row_steps_per_s": round(B * len(times["decode"]) / (ms["decode"] * 1e-3), 1),
+            "compactions": len(times["compact"]), "compact_ms": round(ms["compact"], 3),
+            "total_ms": round(sum(ms.values()), 3), "status": status}
+
+
 def time_prefill(torch, synth, GatedDeltaNetLayer, reps, warmup):
     """Average time of one chunked prefill of the T = 4096 sequence (inputs resident in HBM)."""
     pwl = synth.workloads()[PREFILL_WL]
@@ -600,6 +728,56 @@ def _oracle_rows_parallel(n_steps, rows):
     return max(secs), nw
 
 
+def _oracle_prefill_worker(job):
+    """One worker of the oracle prefill sample: the T-token prefix of the T = 4096 workload's
+    sequence, run by the float64 oracle over the given K-heads (each with its V-heads and its
+    slice of the [q | k | v] channels; heads are independent).  Returns its compute seconds."""
+    T, k_heads = job
+    import oracle
+    from gated_deltanet_linear_09_gb300 import synth
+    wl = synth.workloads()[PREFILL_WL]
+    geo = wl.geo
+    w = synth.make_weights(geo, wl.seed)
+    xs = synth.make_token_inputs(geo, T, wl.seed, 0)
+    r = geo.Hv // geo.Hk
+    secs = 0.0
+    for kh in k_heads:
+        vh = list(range(kh * r, kh * r + r))
+        ch = ([kh * geo.dk + e for e in range(geo.dk)] +
+              [geo.Hk * geo.dk + kh * geo.dk + e for e in range(geo.dk)] +
+              [2 * geo.Hk * geo.dk + h * geo.dv + e for h in vh for e in range(geo.dv)])
+        zc = [h * geo.dv + e for h in vh for e in range(geo.dv)]
+        sub = synth.Geometry(1, r, geo.dk, geo.dv, geo.K, geo.act)
+        ws = dict(A_log=np.asarray(w["A_log"], np.float64)[vh],
+                  dt_bias=np.asarray(w["dt_bias"], np.float64)[vh],
+                  conv_w=np.asarray(w["conv_w"], np.float64)[ch],
+                  norm_w=np.asarray(w["norm_w"], np.float64))
+        xin = dict(qkv=np.ascontiguousarray(np.asarray(xs["qkv"], np.float64)[:, ch]),
+                   z=np.ascontiguousarray(np.asarray(xs["z"], np.float64)[:, zc]),
+                   a=np.ascontiguousarray(np.asarray(xs["a"], np.float64)[:, vh]),
+                   b=np.ascontiguousarray(np.asarray(xs["b"], np.float64)[:, vh]))
+        rec = np.zeros((1, r, geo.dk, geo.dv))
+        conv = np.zeros((1, geo.K - 1, sub.cqkv))
+        t0 = time.perf_counter()
+        oracle.prefill(sub.oracle_dims(), ws, rec, conv, [0, T], [0], None, **xin)
+        secs += time.perf_counter() - t0
+    return secs
+
+
+def _oracle_prefill(T, workers):
+    """(span seconds, workers used): the 16 K-heads split over spawned worker processes."""
+    import multiprocessing as mp
+    from gated_deltanet_linear_09_gb300 import synth
+    Hk = synth.workloads()[PREFILL_WL].geo.Hk
+    nw = max(1, min(workers, Hk))
+    jobs = [(T, list(range(j, Hk, nw))) for j in range(nw)]
+    if nw == 1:
+        return _oracle_prefill_worker(jobs[0]), 1
+    with mp.get_context("spawn").Pool(nw) as pool:
+        secs = pool.map(_oracle_prefill_worker, jobs)
+    return max(secs), nw
+
+
 def synth_workload():
     from gated_deltanet_linear_09_gb300 import synth
     return synth.workloads()[DECODE_WL]
@@ -622,6 +800,19 @@ def cpu_baseline(args):
     span, nw = _oracle_rows_parallel(n_par, rows)
     n_one = 48
     sec, _ = _oracle_decode_steps(n_one, rows)
+    # the chunked prefill's workload (T = 4096, Hk = 16, Hv = 32): the oracle's sequential
+    # recurrence over a prefix of the sequence, all K-heads, on all cores and on one thread
+    tp_all, tp_one = 4096, 1024
+    p_span, p_nw = _oracle_prefill(tp_all, os.cpu_count() or 1)
+    p_one, _ = _oracle_prefill(tp_one, 1)
+    prefill = {"tokens_per_s": round(tp_all / p_span, 1), "unit": "tokens/s", "cores": p_nw,
+               "kind": "oracle",
+               "sample": f"{tp_all} tokens of the T=4096 workload's sequence, all 16 "
+                         f"K-heads split over {p_nw} processes, float64 C oracle",
+               "seconds": round(p_span, 2),
+               "single_thread": {"tokens_per_s": round(tp_one / p_one, 1), "cores": 1,
+                                 "sample": f"the first {tp_one} tokens, all 16 K-heads, one thread",
+                                 "seconds": round(p_one, 2)}}
     return {"value": round(per_row_step * rows * n_par / span / 1e9, 4), "unit": UNIT,
             "cores": nw, "kind": "oracle",
             "sample": f"{n_par} decode steps x {rows} rows of the B=64 workload, rows split over "
@@ -630,7 +821,8 @@ def cpu_baseline(args):
             "single_thread": {"value": round(per_row_step * rows * n_one / sec / 1e9, 4),
                               "unit": UNIT, "cores": 1,
                               "sample": f"{n_one} decode steps x {rows} rows, one thread",
-                              "seconds": round(sec, 2)}}
+                              "seconds": round(sec, 2)},
+            "prefill": prefill}
 
 
 def run_reference(args, ws, rank):
