@@ -199,9 +199,14 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t num_seqs, int32
  * the gated delta rule).  has_initial_state (device uint8[num_seqs], or NULL = all zero):
  * 0 starts from zero recurrent and conv state, 1 continues from slot slot_idx[n] (device
  * int32[num_seqs]).  On return the slot holds the state after the sequence's last token and
- * its last K-1 raw inputs.  workspace: device, >= gdn_prefill_workspace_bytes(...), 256-byte
- * aligned, contents undefined on entry and exit.  Several kernels on `stream`; no host reads
- * of device data. */
+ * its last K-1 raw inputs.  workspace: device, 256-byte aligned, contents undefined on entry
+ * and exit.  gdn_prefill_workspace_bytes(...) is the size for one pass over all the chunks (the
+ * fastest).  For head dims dk = dv = 128 any workspace of at least
+ * gdn_prefill_workspace_bytes(dims, 1, 1) bytes (one chunk's records for every V-head) is also
+ * accepted: the call then runs in windows of as many whole 64-token chunks as fit, each
+ * sequence's state carried from window to window through its slot, with the same results;
+ * other head dims need the full size (GDN_ERR_WORKSPACE_TOO_SMALL otherwise).  Several
+ * kernels on `stream` (two per window); no host reads of device data. */
 int gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
                         const int32_t* cu_seqlens, const int32_t* slot_idx,
                         const uint8_t* has_initial_state, int32_t num_seqs, int32_t total_tokens,
