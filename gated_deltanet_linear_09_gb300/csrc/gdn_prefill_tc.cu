@@ -147,7 +147,7 @@ __device__ bool seq_chunk_offset(const int32_t* __restrict__ cu, int num_seqs, i
 // the CTA pays one global-memory round trip instead of one per phase.
 
 constexpr int AS = 68;    // row stride of the A / T matrix (16-byte aligned rows)
-constexpr int NTI = 512;  // threads of the intra kernel (16 warps), one CTA per SM
+constexpr int NTI = 1024; // threads of the intra kernel (32 warps), one CTA per SM
 constexpr int RMAX = 4;   // V-heads per K-head on the tensor-core path
 constexpr int NROW = CH + 3;   // input rows per chunk: three of history, then the 64 tokens
 
@@ -176,7 +176,7 @@ constexpr uint32_t IN_BYTES = 4 * InRing<__nv_bfloat16>::SLOT > 2 * InRing<float
 //   IN  the input ring                                                             71 KiB
 //   AT  f32 [64][AS]: A of the V-head, overwritten by T = (I + A)^{-1}               17 KiB
 //   VEC f32 [RMAX][5][64]: per V-head gamma, beta, e^gamma, e^{gamma_L - gamma}, beta e^gamma
-//   PART f32 [2][64]: per token, the two warps' partial sums of squares of the l2norm
+//   PART f32 [4][64]: per token, the four warps' partial sums of squares of the l2norm
 struct IntraSmem {
   static constexpr uint32_t A1 = 0;
   static constexpr uint32_t K_HI = 0, Q_HI = 16384, K_LO = 32768, Q_LO = 49152;
@@ -185,8 +185,8 @@ struct IntraSmem {
   static constexpr uint32_t IN = B2 + 32768;
   static constexpr uint32_t AT = IN + IN_BYTES;
   static constexpr uint32_t VEC = AT + 4 * 64 * AS;
-  static constexpr uint32_t PART = VEC + 4 * RMAX * 5 * 64;  // f32 [2][64] l2norm partial sums
-  static constexpr uint32_t BAR = PART + 4 * 2 * 64;         // 2 mbarriers
+  static constexpr uint32_t PART = VEC + 4 * RMAX * 5 * 64;  // f32 [4][64] l2norm partial sums
+  static constexpr uint32_t BAR = PART + 4 * 4 * 64;         // 2 mbarriers
   static constexpr uint32_t MISC = BAR + 16;                  // tmem slot, flags
   static constexpr uint32_t BYTES = MISC + 64;
 };
@@ -256,73 +256,68 @@ __device__ __forceinline__ void unpack_unit(const uint4& u, float* f, float*) {
   f[3] = __uint_as_float(u.w);
 }
 
-// Thread layout of the conv: token t = 8 (warp % 8) + lane % 8 and the 16 channels
-// [16 cg, 16 cg + 16), cg = 4 (warp / 8) + lane / 8.  A warp holds 8 consecutive tokens x 64
+// Thread layout of the conv: token t = 8 (warp % 8) + lane % 8 and the 8 channels
+// [8 cg, 8 cg + 8), cg = 4 (warp / 8) + lane / 8.  A warp holds 8 consecutive tokens x 32
 // channels, so its ring reads (padded rows) and its 16-byte stores into K-major tiles (8
 // distinct rows per 128-byte line) are free of bank conflicts.
 __device__ __forceinline__ int conv_t() { return 8 * ((threadIdx.x >> 5) & 7) + (threadIdx.x & 7); }
 __device__ __forceinline__ int conv_cg() { return 4 * (threadIdx.x >> 8) + ((threadIdx.x >> 3) & 3); }
 
-// y[e] = SiLU(sum_j w[c][j] x[t - 3 + j][c]), c = 16 cg + e, from a ring slot (zero past L).
+// y[e] = SiLU(sum_j w[c][j] x[t - 3 + j][c]), c = 8 cg + e, from a ring slot (zero past L).
+// The four input rows and the weights of one 16-byte unit are read packed and unpacked channel
+// by channel (few registers live at once).
 template <typename T>
 __device__ __forceinline__ void conv_slot(const unsigned char* slot, int L, float* y) {
   using R = InRing<T>;
   constexpr int CPU = 16 / (int)sizeof(T);   // channels per 16-byte unit (8 bf16, 4 f32)
-  constexpr int UPT = 16 / CPU;              // units per thread
+  constexpr int UPT = 8 / CPU;               // units per thread
   const int t = conv_t(), cg = conv_cg();
 #pragma unroll
   for (int u = 0; u < UPT; ++u) {
     const int unit = cg * UPT + u;
-    float wf[4 * CPU];   // [channel][tap]
+    uint4 wq[4], xq[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      unpack_unit(*reinterpret_cast<const uint4*>(slot + R::W_OFF + unit * 64 + q * 16), wf + q * CPU,
-                  (T*)nullptr);
-    float xf[4][CPU];
+    for (int q = 0; q < 4; ++q) wq[q] = *reinterpret_cast<const uint4*>(slot + R::W_OFF + unit * 64 + q * 16);
 #pragma unroll
-    for (int m = 0; m < 4; ++m)
-      unpack_unit(*reinterpret_cast<const uint4*>(slot + (t + m) * R::PITCH + unit * 16), xf[m],
-                  (T*)nullptr);
+    for (int m = 0; m < 4; ++m) xq[m] = *reinterpret_cast<const uint4*>(slot + (t + m) * R::PITCH + unit * 16);
+    const T* wv = reinterpret_cast<const T*>(wq);   // [channel][tap]
+    const T* xv = reinterpret_cast<const T*>(xq);   // [row][channel]
 #pragma unroll
     for (int e = 0; e < CPU; ++e) {
-      float acc = wf[e * 4 + 3] * xf[3][e];
-      acc = fmaf(wf[e * 4 + 0], xf[0][e], acc);
-      acc = fmaf(wf[e * 4 + 1], xf[1][e], acc);
-      acc = fmaf(wf[e * 4 + 2], xf[2][e], acc);
+      float acc = Act<T>::load(wv + e * 4 + 3) * Act<T>::load(xv + 3 * CPU + e);
+      acc = fmaf(Act<T>::load(wv + e * 4 + 0), Act<T>::load(xv + 0 * CPU + e), acc);
+      acc = fmaf(Act<T>::load(wv + e * 4 + 1), Act<T>::load(xv + 1 * CPU + e), acc);
+      acc = fmaf(Act<T>::load(wv + e * 4 + 2), Act<T>::load(xv + 2 * CPU + e), acc);
       y[u * CPU + e] = (t < L) ? silu_fast(acc) : 0.f;
     }
   }
 }
 
-// l2 normalisation (times scale) of the thread's 16 values: the 8 threads holding token t's 128
-// channels sit in two warps; each warp sums over its 64 channels with shuffles, the two partial
-// sums meet in shared memory.  Contains a barrier.
-__device__ __forceinline__ void l2norm16(float* y, float* part, float eps, float scale) {
+// l2 normalisation (times scale) of the thread's 8 values: the 16 threads holding token t's 128
+// channels sit in four warps; each warp sums over its 32 channels with shuffles, the four
+// partial sums meet in shared memory.  Contains a barrier.
+__device__ __forceinline__ void l2norm8(float* y, float* part, float eps, float scale) {
   const int t = conv_t(), lane = threadIdx.x & 31;
   float ss = 0.f;
 #pragma unroll
-  for (int e = 0; e < 16; ++e) ss = fmaf(y[e], y[e], ss);
+  for (int e = 0; e < 8; ++e) ss = fmaf(y[e], y[e], ss);
   ss += __shfl_xor_sync(0xffffffffu, ss, 8);
   ss += __shfl_xor_sync(0xffffffffu, ss, 16);
   if (lane < 8) part[(threadIdx.x >> 8) * 64 + t] = ss;
   __syncthreads();
-  const float inv = scale * rsqrtf(part[t] + part[64 + t] + eps);
+  const float inv = scale * rsqrtf((part[t] + part[64 + t]) + (part[128 + t] + part[192 + t]) + eps);
 #pragma unroll
-  for (int e = 0; e < 16; ++e) y[e] *= inv;
+  for (int e = 0; e < 8; ++e) y[e] *= inv;
 }
 
-// The thread's 16 values of row t, split, into a 128-column K-major tile (shared or global):
-// two 16-byte units.
-__device__ __forceinline__ void put_row16(unsigned char* hi, unsigned char* lo, const float* v) {
-  const int t = conv_t(), cg = conv_cg();
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    uint4 hh, ll;
-    split8(v + 8 * u, hh, ll);
-    const uint32_t off = tc::kmajor_off(t, 16 * cg + 8 * u, 128);
-    *reinterpret_cast<uint4*>(hi + off) = hh;
-    *reinterpret_cast<uint4*>(lo + off) = ll;
-  }
+// The thread's 8 values of row t, split, into a 128-column K-major tile (shared or global):
+// one 16-byte unit each for hi and lo.
+__device__ __forceinline__ void put_row8(unsigned char* hi, unsigned char* lo, const float* v) {
+  uint4 hh, ll;
+  split8(v, hh, ll);
+  const uint32_t off = tc::kmajor_off(conv_t(), 8 * conv_cg(), 128);
+  *reinterpret_cast<uint4*>(hi + off) = hh;
+  *reinterpret_cast<uint4*>(lo + off) = ll;
 }
 
 // The gates of one V-head over the chunk (warp-wide, 2 tokens per lane): gamma (cumulative g
@@ -590,13 +585,13 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     if (lane == 0) *reinterpret_cast<float*>(rec_of(j) + R_SC) = expf(gL);
   }
   const int tt = conv_t();
-  float y[16];   // conv outputs of token tt, channels [16 cg, 16 cg + 16)
+  float y[8];   // conv outputs of token tt, channels [8 cg, 8 cg + 8)
 
   // ---- K: conv, l2norm, A1 K rows
   ring_wait(0);   // also publishes the gates
   conv_slot<T>(slot_of(0), L, y);
-  l2norm16(y, part, d.l2_eps, 1.0f);
-  put_row16(a1 + S::K_HI, a1 + S::K_LO, y);
+  l2norm8(y, part, d.l2_eps, 1.0f);
+  put_row8(a1 + S::K_HI, a1 + S::K_LO, y);
   // ---- Q: conv, l2norm (times q_scale), A1 Q rows and per V-head the Q~ rows of B3
   ring_wait(1);   // also: K rows complete, slot 0 and the partial sums free
   if (issued < ntens) {
@@ -604,15 +599,15 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     ++issued;
   }
   conv_slot<T>(slot_of(1), L, y);
-  l2norm16(y, part, d.l2_eps, d.q_scale);
-  put_row16(a1 + S::Q_HI, a1 + S::Q_LO, y);
+  l2norm8(y, part, d.l2_eps, d.q_scale);
+  put_row8(a1 + S::Q_HI, a1 + S::Q_LO, y);
   for (int j = 0; j < r; ++j) {
     const float e = vecs[j * 320 + 128 + tt];
-    float v[16];
+    float v[8];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) v[q] = y[q] * e;
+    for (int q = 0; q < 8; ++q) v[q] = y[q] * e;
     unsigned char* rec = rec_of(j);
-    put_row16(rec + R_B3, rec + R_B3 + B3_HALF, v);
+    put_row8(rec + R_B3, rec + R_B3 + B3_HALF, v);
   }
   // per V-head K~^T = (diag(e^{gamma_L - gamma}) K)^T rows of B4, from the K tile (hi + lo carry
   // about 16 significant bits): unit (feature f, 8 tokens), consecutive threads take consecutive
@@ -665,23 +660,23 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     ++issued;
   }
   conv_slot<T>(slot_of(2), L, y);
-  put_row16(vt, vt + 16384, y);
+  put_row8(vt, vt + 16384, y);
   wait_or_abort(bar, 0, abort, status);
   tc::fence_after_sync();
 
   // A (to At) and P (to the record) of V-head j from D1: warp w reads TMEM lanes 32 (w % 4) and
-  // the 16 columns of quarter w / 4.  Lanes 0-63 are K-rows (A), lanes 64-127 Q-rows (P).
+  // the 8 columns of eighth w / 4.  Lanes 0-63 are K-rows (A), lanes 64-127 Q-rows (P).
   auto a_and_p = [&](int j) {
     const float* gam = vecs + j * 320;
     const float* bet = gam + 64;
-    const int rr = (warp & 3) * 32 + lane, j0 = (warp >> 2) * 16;
-    float v[16];
-    tc::tmem_ld16(tc::taddr(tb + TI_D1, (warp & 3) * 32, j0), v);
+    const int rr = (warp & 3) * 32 + lane, j0 = (warp >> 2) * 8;
+    float v[8];
+    tc::tmem_ld8(tc::taddr(tb + TI_D1, (warp & 3) * 32, j0), v);
     if (rr < 64) {
       const int i = rr;
       const float gi = gam[i], bi = bet[i];   // beta is 0 past L: rows past L vanish
 #pragma unroll
-      for (int q = 0; q < 16; q += 4) {
+      for (int q = 0; q < 8; q += 4) {
         float a4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -695,20 +690,17 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
       const int i = rr - 64;
       const float gi = gam[i], vi = (i < L) ? 1.f : 0.f;
       unsigned char* rec = rec_of(j);
+      float p8[8];
 #pragma unroll
-      for (int q = 0; q < 16; q += 8) {
-        float p8[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int jj = j0 + q + u;
-          p8[u] = ((jj <= i) ? vi : 0.f) * exp_fast(fminf(gi - gam[jj], 0.f)) * v[q + u];
-        }
-        uint4 hh, ll;
-        split8(p8, hh, ll);
-        const uint32_t off = tc::kmajor_off(i, j0 + q, 64);   // P rows 0..63 of B4
-        gst_unit(rec + R_B4, off, hh);
-        gst_unit(rec + R_B4 + B4_HALF, off, ll);
+      for (int u = 0; u < 8; ++u) {
+        const int jj = j0 + u;
+        p8[u] = ((jj <= i) ? vi : 0.f) * exp_fast(fminf(gi - gam[jj], 0.f)) * v[u];
       }
+      uint4 hh, ll;
+      split8(p8, hh, ll);
+      const uint32_t off = tc::kmajor_off(i, j0, 64);   // P rows 0..63 of B4
+      gst_unit(rec + R_B4, off, hh);
+      gst_unit(rec + R_B4 + B4_HALF, off, ll);
     }
   };
 
@@ -764,14 +756,13 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     tc::fence_after_sync();
     {
       unsigned char* rec = rec_of(j);
-      const int lg = warp & 3, cq = (warp >> 2) * 32;
+      const int lg = warp & 3, cq = (warp >> 2) * 16;   // 16 of the 128 columns per warp
       const int i = (lg & 1) * 32 + lane;
-      float v[32];
+      float v[16];
       if (lg < 2) {
         tc::tmem_ld16(tc::taddr(tb + TI_W, lg * 32, cq), v);
-        tc::tmem_ld16(tc::taddr(tb + TI_W, lg * 32, cq + 16), v + 16);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 2; ++u) {
           uint4 hh, ll;
           split8(v + 8 * u, hh, ll);
           const uint32_t off = tc::kmajor_off(64 + i, cq + 8 * u, 128);   // W rows of B3
@@ -780,11 +771,10 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
         }
       } else {
         tc::tmem_ld16(tc::taddr(tb + TI_U, lg * 32, cq), v);
-        tc::tmem_ld16(tc::taddr(tb + TI_U, lg * 32, cq + 16), v + 16);
         // U~ record layout [column / 4][token][4]: a warp stores 32 consecutive tokens' float4
         float* ut = reinterpret_cast<float*>(rec + R_UT);
 #pragma unroll
-        for (int q = 0; q < 32; q += 4)
+        for (int q = 0; q < 16; q += 4)
           *reinterpret_cast<float4*>(ut + ut_index(i, cq + q)) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
       }
     }
@@ -793,7 +783,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     tc::fence_after_sync();
     if (j + 1 < r) {
       // the D2 operands of V-head j + 1 (VT and B2 were read by the MMAs just completed)
-      put_row16(vt, vt + 16384, y);
+      put_row8(vt, vt + 16384, y);
       t_to_b2(At, vecs + (j + 1) * 320 + 256, vecs + (j + 1) * 320 + 64, b2, b2 + 16384);
       tc::fence_proxy_async_smem();
       tc::fence_before_sync();
