@@ -217,12 +217,17 @@ def _varlen_case(geo, seed):
     return w, rec, conv, cu, slots, has_init, xs, N
 
 
-@pytest.mark.parametrize("cap_chunks", [1, 2, 5])
-def test_prefill_windowed_workspace(cap_chunks):
+@pytest.mark.parametrize("cap_chunks,geo", [
+    (1, synth.Geometry(2, 4, 128, 128, 4, synth.BF16)),
+    (2, synth.Geometry(2, 4, 128, 128, 4, synth.BF16)),
+    (5, synth.Geometry(2, 4, 128, 128, 4, synth.BF16)),
+    (2, synth.Geometry(2, 2, 128, 128, 4, synth.F32)),
+    (3, synth.Geometry(1, 3, 128, 128, 4, synth.BF16)),
+], ids=lambda x: f"{x.Hk}x{x.Hv}{x.act}" if isinstance(x, synth.Geometry) else f"cap{x}")
+def test_prefill_windowed_workspace(cap_chunks, geo):
     """A workspace of only `cap_chunks` chunks' records: the call runs in windows of whole chunks
     (sequences cross window edges, an empty sequence, mixed initial states).  Outputs and states
     against the oracle, and bit-equal to the same call with the full workspace."""
-    geo = synth.Geometry(2, 4, 128, 128, 4, synth.BF16)
     w, rec, conv, cu, slots, has_init, xs, N = _varlen_case(geo, 670)
     full = GatedDeltaNetLayer(geo, w, N)
     capd = GatedDeltaNetLayer(geo, w, N)

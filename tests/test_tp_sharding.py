@@ -75,11 +75,11 @@ def _worker(rank, world, port, q):
         dist.destroy_process_group()
 
 
-def test_sharded_chain_all_reduce_equals_unsharded_gloo_two_ranks():
+@pytest.mark.parametrize("world", [2, 4])
+def test_sharded_chain_all_reduce_equals_unsharded_gloo(world):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    world = 2
     procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
     for p in procs:
         p.start()
