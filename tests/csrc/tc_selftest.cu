@@ -196,6 +196,92 @@ extern "C" int tc_gemm_ta(const float* A, const float* B, float* D, int N, int K
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
 }
 
+// The same GEMM with A written into TMEM from registers: thread i of the four warps holds row i
+// of A, splits it into bf16 hi / lo pairs (element 2c in the low half of column c) and stores
+// them with tcgen05.st (hi at columns [N, N + K/2), lo after it), the way the prefill chain
+// kernel puts its S^T and U^T operands in place; the MMAs read A from TMEM.
+__global__ void tc_gemm_tast_kernel(const float* __restrict__ A, const float* __restrict__ B,
+                                    float* __restrict__ D, int N, int K, int passes, uint32_t ncols,
+                                    int* __restrict__ err) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  unsigned char* b_hi = sm;
+  unsigned char* b_lo = b_hi + N * K * 2;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(b_lo + N * K * 2);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+  for (int idx = tid; idx < N * K; idx += blockDim.x) {
+    const int r = idx / K, k = idx - r * K;
+    __nv_bfloat16 h, l;
+    split_bf16(B[idx], h, l);
+    *reinterpret_cast<__nv_bfloat16*>(b_hi + kmajor_off(r, k, K)) = h;
+    *reinterpret_cast<__nv_bfloat16*>(b_lo + kmajor_off(r, k, K)) = l;
+  }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (warp == 0) tmem_alloc(slot, ncols);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *slot;
+  const uint32_t ta_hi = tbase + (uint32_t)N, ta_lo = ta_hi + (uint32_t)(K / 2);
+  const float* arow = A + (size_t)(warp * 32 + lane) * K;
+  for (int c0 = 0; c0 < K / 2; c0 += 16) {   // 16 columns = 32 elements of the row at a time
+    uint32_t hw[16], lw[16];
+    for (int p = 0; p < 16; ++p) split2_bf16(arow[2 * (c0 + p)], arow[2 * (c0 + p) + 1], hw[p], lw[p]);
+    tmem_st16_nw(taddr(ta_hi, warp * 32, c0), reinterpret_cast<const float*>(hw));
+    tmem_st16_nw(taddr(ta_lo, warp * 32, c0), reinterpret_cast<const float*>(lw));
+  }
+  tmem_wait_st();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (tid == 0) {
+    const uint32_t id = idesc_bf16(128, N);
+    const uint32_t bh = smem_u32(b_hi), bl = smem_u32(b_lo);
+    for (int s = 0; s < K / 16; ++s) {
+      mma_bf16_ta(tbase, ta_hi + 8 * s, kstep_desc(bh, K, s), id, s > 0 ? 1u : 0u);
+      if (passes == 3) {
+        mma_bf16_ta(tbase, ta_hi + 8 * s, kstep_desc(bl, K, s), id, 1u);
+        mma_bf16_ta(tbase, ta_lo + 8 * s, kstep_desc(bh, K, s), id, 1u);
+      }
+    }
+    mma_commit(bar);
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(bar, 0);
+  if (!ok && lane == 0) atomicOr(err, 1);
+  fence_after_sync();
+  if (ok) {
+    for (int c0 = 0; c0 < N; c0 += 16) {
+      float v[16];
+      tmem_ld16(taddr(tbase, warp * 32, c0), v);
+      for (int i = 0; i < 16; ++i) D[(size_t)(warp * 32 + lane) * N + c0 + i] = v[i];
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, ncols);
+}
+
+extern "C" int tc_gemm_tast(const float* A, const float* B, float* D, int N, int K, int passes,
+                            int* err) {
+  if (N < 16 || N > 256 || N % 16 || K < 32 || K % 32 || N + K > 512) return -1;
+  uint32_t ncols = 32;
+  while (ncols < (uint32_t)(N + K)) ncols <<= 1;
+  const size_t smem = (size_t)2 * N * K * 2 + 64;
+  if (smem > 200 * 1024) return -1;
+  if (cudaFuncSetAttribute(tc_gemm_tast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return -2;
+  tc_gemm_tast_kernel<<<1, 128, smem>>>(A, B, D, N, K, passes, ncols, err);
+  if (cudaGetLastError() != cudaSuccess) return -3;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
+}
+
 extern "C" int tc_gemm(const float* A, const float* B, float* D, int N, int K, int passes, int* err) {
   return tc_gemm_p(A, B, D, N, K, passes, 128, err);
 }

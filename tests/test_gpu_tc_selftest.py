@@ -33,6 +33,8 @@ def lib():
     l.tc_gemm_p.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p]
     l.tc_gemm_ta.restype = ctypes.c_int
     l.tc_gemm_ta.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    l.tc_gemm_tast.restype = ctypes.c_int
+    l.tc_gemm_tast.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
     l.tc_gemm_mnb.restype = ctypes.c_int
     l.tc_gemm_mnb.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
     l.tc_cluster_xchg.restype = ctypes.c_int
@@ -101,6 +103,29 @@ def test_tc_gemm_tmem_a(lib, N, K):
     np.testing.assert_allclose(D.cpu().numpy(), ref1, rtol=0, atol=2e-4 * np.sqrt(K))
     D.zero_()
     assert lib.tc_gemm_ta(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, K, 3, err.data_ptr()) == 0
+    assert int(err.item()) == 0
+    e3 = np.max(np.abs(D.cpu().numpy() - ref)) / np.max(np.abs(ref))
+    assert e3 < 2e-5, e3
+
+
+@pytest.mark.parametrize("N,K", [(128, 128), (128, 64), (64, 64), (256, 64)])
+def test_tc_gemm_tmem_a_from_registers(lib, N, K):
+    """A operand written into TMEM from registers with tcgen05.st (bf16 pairs, element 2c in the
+    low half of column c) and read from there by the MMAs: one pass equals the product of the
+    bf16 operands, three passes are close to the float32 product."""
+    rng = np.random.default_rng(N * 17 + K)
+    A = rng.standard_normal((128, K)).astype(np.float32)
+    B = rng.standard_normal((N, K)).astype(np.float32)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = A.astype(np.float64) @ B.astype(np.float64).T
+    D = torch.zeros((128, N), dtype=torch.float32, device="cuda")
+    assert lib.tc_gemm_tast(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, K, 1, err.data_ptr()) == 0
+    assert int(err.item()) == 0
+    ref1 = _bf16(A) @ _bf16(B).T
+    np.testing.assert_allclose(D.cpu().numpy(), ref1, rtol=0, atol=2e-4 * np.sqrt(K))
+    D.zero_()
+    assert lib.tc_gemm_tast(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), N, K, 3, err.data_ptr()) == 0
     assert int(err.item()) == 0
     e3 = np.max(np.abs(D.cpu().numpy() - ref)) / np.max(np.abs(ref))
     assert e3 < 2e-5, e3
