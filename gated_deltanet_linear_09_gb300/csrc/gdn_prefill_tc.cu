@@ -6,19 +6,21 @@
 // section 3; chunked prefill chain and its scratch from "pegainfer PR #1003"), arranged so that
 // every tensor-core product has M = 128:
 //
-//   intra kernel (chunk x V-head, all in parallel, two CTAs per SM):
+//   intra kernel (chunk x K-head, all in parallel, one CTA per SM):
 //     conv + SiLU + l2norm + gates of the chunk's 64 tokens,
-//     D1 = [K;Q] K^T                     -> A = beta_i e^{g_i-g_j} KK^T (j<i),  P = QK^T o Gamma
-//     T  = (I + A)^{-1}                  (16 x 16 blocks: diagonal inverses, then block rows)
-//     D2 = (beta e^gamma K)^T T^T, (beta V)^T T^T   -> W^T, U~^T
+//     D1 = [K;Q] K^T (once per K-head)   -> A = beta_i e^{g_i-g_j} KK^T (j<i),  P = QK^T o Gamma
+//     per V-head: T = (I + A)^{-1}       (16 x 16 blocks: diagonal inverses, then block rows)
+//     D2 = [T diag(beta e^gamma) ; T diag(beta)] [K^T | V^T]   -> W (rows 0-63), U~ (rows 64-127)
 //     writes [Q~ ; W] and [P ; K~^T] as split-bf16 operand images (Q~ = e^gamma Q,
 //     K~ = e^{gamma_L - gamma} K), U~ (f32) and e^{gamma_L}
-//   state kernel (sequence x V-head x 4 dv slices, a cluster of 4 CTAs; serial over the chunks,
-//   the 128 x 32 state slice S held in TMEM):
-//     D3 = [Q~ ; W] S                    -> rows 0-63 Q~ S, rows 64-127 W S
-//     U  = U~ - W S
-//     S <- e^{gamma_L} S + K~^T U ;  D3 += [P ; K~^T_(0..63)] U  (rows 0-63: O = Q~ S + P U)
-//     z-gated RMSNorm of O -> out, the sum of squares over dv shared within the cluster
+//   chain kernel (sequence x V-head, one CTA each, serial over the chunks; transposed products
+//   with S^T and U^T as TMEM A operands and the records as B operands):
+//     D3^T = S^T [Q~ ; W]^T              -> columns 0-63 (Q~ S)^T, 64-127 (W S)^T
+//     U^T  = U~^T - (W S)^T
+//     S^T <- e^{gamma_L} S^T + U^T K~ ;  D3^T[:, 0:64] += U^T P^T  (O^T = (Q~ S + P U)^T)
+//     z-gated RMSNorm of O over dv -> out
+//   The call runs in windows of chunks; a window's intra kernel runs beside the previous window's
+//   chains (programmatic dependent launch).
 //
 // Precision: every product runs as three bf16 passes on split operands
 // (x = hi + lo, hi = bf16(x), lo = bf16(x - hi): A_hi B_hi + A_hi B_lo + A_lo B_hi) with f32
@@ -36,18 +38,18 @@ constexpr int CH = 64;
 constexpr int D = 128;
 
 // Per (chunk, V-head) record of the workspace.  B3 and B4 are stored as the exact shared-memory
-// images of the state kernel's A operands (split bf16, K-major core-matrix layout, hi then lo), so
-// the state kernel brings each in with one bulk copy.  Offsets in bytes.
+// images of the chain kernel's B operands (split bf16, K-major core-matrix layout, hi then lo),
+// so the chain kernel brings each in with one bulk copy.  Offsets in bytes.
 constexpr uint32_t R_B3 = 0;                     // [Q~ ; W] rows, 128 x 128: hi 32 KiB, lo 32 KiB
 constexpr uint32_t R_B4 = R_B3 + 65536;          // [P ; K~^T] rows, 192 x 64: hi 24 KiB, lo 24 KiB
-constexpr uint32_t R_UT = R_B4 + 49152;          // f32 U~, [column / 4][token][4]
+constexpr uint32_t R_UT = R_B4 + 49152;          // f32 U~, [token][column]
 constexpr uint32_t R_SC = R_UT + 32768;          // f32 e^{gamma_L}
 constexpr uint32_t REC_BYTES = R_SC + 256;       // 147,712 bytes (multiple of 256)
 constexpr uint32_t B3_HALF = 32768, B4_HALF = 24576;
 
-// Float index of U~ element (token t, column col) in its record: [col / 4][t][4], so that 32
-// consecutive tokens' 4-column pieces are 512 contiguous bytes for the writer and the reader.
-__host__ __device__ constexpr int ut_index(int t, int col) { return ((col >> 2) * CH + t) * 4 + (col & 3); }
+// Float index of U~ element (token t, column col) in its record: row-major, so that a warp of
+// the chain kernel reading 32 consecutive columns of a token touches 32 consecutive floats.
+__host__ __device__ constexpr int ut_index(int t, int col) { return t * D + col; }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tc::smem_u32(bar)) : "memory");
@@ -513,7 +515,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
                 const int32_t* __restrict__ cu, const int32_t* __restrict__ slot_idx,
                 const uint8_t* __restrict__ has_init, int num_seqs, int total,
                 const T* __restrict__ qkv, const T* __restrict__ a, const T* __restrict__ b,
-                float* __restrict__ ws, int cw0, int32_t* __restrict__ status) {
+                float* __restrict__ ws, int cw0, int rec_base, int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
   using S = IntraSmem;
   using R = InRing<T>;
@@ -545,7 +547,10 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     }
   }
   __syncthreads();
-  if (!sh[0]) return;
+  if (!sh[0]) {
+    tc::pdl_wait_primary();   // no CTA of a pipelined window completes before the previous chains
+    return;
+  }
   const int t0 = sh[1], L = sh[2], seq = sh[3], seq_start = sh[4];
   const int seq_len = __ldg(cu + seq + 1) - seq_start;
   volatile int* abort = sh + 5;
@@ -554,7 +559,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   const bool init = valid && has_init != nullptr && __ldg(has_init + seq) != 0;
   const T* cs = conv_state + (size_t)(valid ? s : 0) * 3 * d.cqkv;
   auto rec_of = [&](int j) {
-    return reinterpret_cast<unsigned char*>(ws) + ((size_t)(c - cw0) * d.Hv + h0 + j) * REC_BYTES;
+    return reinterpret_cast<unsigned char*>(ws) + ((size_t)(rec_base + c - cw0) * d.Hv + h0 + j) * REC_BYTES;
   };
 
   // ---- every input tensor of the chunk into the ring: k, q, v of V-head 0, 1, ... (tensor i in
@@ -771,7 +776,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
         }
       } else {
         tc::tmem_ld16(tc::taddr(tb + TI_U, lg * 32, cq), v);
-        // U~ record layout [column / 4][token][4]: a warp stores 32 consecutive tokens' float4
+        // U~ record row-major: each thread stores 16 consecutive columns of its token
         float* ut = reinterpret_cast<float*>(rec + R_UT);
 #pragma unroll
         for (int q = 0; q < 16; q += 4)
@@ -792,101 +797,122 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     }
   }
   if (warp == 1) tc::tmem_dealloc(tb, TI_COLS);
+  // Launched as a programmatic dependent of the previous window's chain kernel, the CTA may have
+  // run beside it; it completes only after that kernel has, which orders this window's chain
+  // kernel after the previous one.  (A no-op for an ordinary launch.)
+  tc::pdl_wait_primary();
 }
 
-// ================================================================== serial state kernel
+// ================================================================== serial chain kernel
 //
-// One cluster of four CTAs per (sequence, V-head); CTA sigma owns the state columns
-// [32 sigma, 32 sigma + 32) of S (dk x dv) -- the chunk recurrence never mixes dv columns, so the
-// four slices run independently and only the output RMSNorm (over all dv) needs an exchange of
-// per-token partial sums of squares between the CTAs of the cluster.
+// One CTA per (sequence, V-head), serial over the sequence's chunks in the window.  The products
+// run in transposed form: the state S^T (dv x dk) and the chunk's U^T (dv x 64 tokens) are the A
+// operands, written into TMEM as split bf16 from registers, and the chunk records (shared memory,
+// one bulk copy each) are the B operands.  Every product then has M = dv = 128 with both the
+// A reads and the accumulator in TMEM, and one CTA carries the whole head:
+//   D3^T = S^T [Q~ ; W]^T           N = 128: columns 0-63 (Q~ S)^T, 64-127 (W S)^T
+//   U^T  = U~^T - (W S)^T
+//   S^T  <- e^{gamma_L} S^T + U^T K~      N = 128 (dk), accumulated onto the scaled f32 S^T
+//   D3^T[:, 0:64] += U^T P^T        -> O^T (dv on the TMEM lanes, tokens on the columns)
+//   z-gated RMSNorm over dv (across the lanes) -> out
+// A head's chain takes a single SM, so a window's chains leave most SMs to the next window's
+// intra kernel, which the launcher starts as a programmatic dependent of this kernel.
 
-constexpr int NSL = 4;                        // dv slices (CTAs) per head
-constexpr int SW = D / NSL;                   // 32 columns per slice
-// The S and U slices enter the MMAs as MN-major B operands [X_hi ; X_lo] (N = 2 SW): core
-// matrices of 8 K-rows x 8 consecutive N-elements, the K-direction ones 128 bytes apart, the
-// N-direction ones (K / 8) * 128 bytes apart.  A thread holding row k of 16 consecutive columns
-// stores four 16-byte units, and a warp's 32 consecutive rows fill 512 contiguous bytes.
-constexpr uint32_t SOP_SBO = (D / 8) * 128;   // S operand: K = 128 (dk)
-constexpr uint32_t SOP_HALF = (SW / 8) * SOP_SBO;
-constexpr uint32_t UOP_SBO = (CH / 8) * 128;  // U operand: K = 64 (tokens)
-constexpr uint32_t UOP_HALF = (SW / 8) * UOP_SBO;
-
-// Row k, columns [n0, n0 + 16) of an MN-major split operand: four 16-byte stores.
-__device__ __forceinline__ void put_mn16(unsigned char* hi, unsigned char* lo, uint32_t sbo, int k,
-                                         int n0, const float* v) {
-  uint32_t hw[8], lw[8];
-#pragma unroll
-  for (int p = 0; p < 8; ++p) tc::split2_bf16(v[2 * p], v[2 * p + 1], hw[p], lw[p]);
-  const uint32_t off = (uint32_t)(n0 >> 3) * sbo + (uint32_t)(k >> 3) * 128u + (uint32_t)(k & 7) * 16u;
-  *reinterpret_cast<uint4*>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-  *reinterpret_cast<uint4*>(hi + off + sbo) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-  *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-  *reinterpret_cast<uint4*>(lo + off + sbo) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-}
-constexpr int NTS = 448;   // warps 0-7 main, 8-9 and 12-13 epilogue, 10 loader, 11 MMA issue
-constexpr int MH = SW / 2; // columns per main warp: warp w takes lanes 32 (w % 4) and half w / 4
-constexpr int NDB = 4;     // D3 (output) accumulators in flight between the MMAs and the epilogue
-constexpr int XH = 2;      // epilogue column halves: partial sums per token and CTA
-constexpr int NXB = 4;     // exchange buffers: chunk c's sums are sent one epilogue step before use
-
-// TMEM columns (lanes 0-127).  Each product runs as two N = 64 MMAs per K-step, A_hi [B_hi ; B_lo]
-// and A_lo [B_hi ; B_lo] (the B operand holds the hi rows 0-31 and the lo rows 32-63), so every
-// accumulator occupies 64 columns whose two 32-column halves add up to the result.
-constexpr uint32_t TC_S = 0;          // K~^T U of the chunk, halves [0, 32) + [32, 64)
-constexpr uint32_t TC_D3 = 64;        // NDB x 64 columns: rows 0-63 O, rows 64-127 W S
+constexpr int NTC = 576;   // warps 0-7 main, 8-15 output epilogue, 16 loader, 17 MMA issue
+// TMEM columns (lanes 0-127 = dv)
+constexpr uint32_t TA_S = 0;     // S^T as split bf16 pairs of dk: hi [0, 64), lo [64, 128)
+constexpr uint32_t TA_U = 128;   // U^T as split bf16 pairs of tokens: hi [128, 160), lo [160, 192)
+constexpr uint32_t TC_D3 = 192;  // D3^T: 128 columns (tokens of [Q~ ; W])
+constexpr uint32_t TC_S = 320;   // f32 S^T, 128 columns (dk): holds e^{gamma_L} S^T while the
+                                 // chunk's U^T K~ products accumulate onto it
 constexpr uint32_t TC_COLS = 512;
 
-struct StateSmem {
-  static constexpr uint32_t B3 = 0;                        // 2 slots: [Q~ ; W] rows [128 x 128], hi then lo
-  static constexpr uint32_t B4 = B3 + 2 * 65536;           // [P ; K~^T] rows [192 x 64], hi then lo
-  static constexpr uint32_t SOP = B4 + 2 * 24576;          // S slice as B operand, hi then lo
-  static constexpr uint32_t UOP = SOP + 2 * SOP_HALF;      // U slice as B operand, hi then lo
-  static constexpr uint32_t XBUF = UOP + 2 * UOP_HALF;     // f32 [NXB][NSL][XH][64] partial sums
-  static constexpr uint32_t BAR = XBUF + NXB * NSL * XH * 64 * 4;   // 22 mbarriers
-  static constexpr uint32_t MISC = BAR + 192;
+struct ChainSmem {
+  static constexpr uint32_t B3 = 0;                          // [Q~ ; W] image, 64 KiB
+  static constexpr uint32_t B4 = B3 + 65536;                 // [P ; K~^T] image, 48 KiB
+  static constexpr uint32_t UT = B4 + 49152;                 // f32 U~ [64 tokens][128 dv], 32 KiB
+  static constexpr uint32_t OT = UT + 32768;                 // f32 O [2 halves][32 tokens][128], 32 KiB
+  static constexpr uint32_t BAR = OT + 32768;                // 14 mbarriers
+  static constexpr uint32_t MISC = BAR + 128;
   static constexpr uint32_t BYTES = MISC + 64;
 };
+static_assert(ChainSmem::BYTES <= 227 * 1024, "chain kernel shared memory");
+
+// 16 consecutive dk values v of S^T row (TMEM lane) lb: the split-bf16 operand words and the
+// f32 copy scaled by eg (the next chunk's e^{gamma_L}).  No wait.
+__device__ __forceinline__ void put_s16(uint32_t lb, int f0, const float* v, float eg) {
+  uint32_t hw[8], lw[8], sw[16];
+#pragma unroll
+  for (int p = 0; p < 8; ++p) tc::split2_bf16(v[2 * p], v[2 * p + 1], hw[p], lw[p]);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) sw[i] = __float_as_uint(eg * v[i]);
+  tc::tmem_st8w_nw(lb + TA_S + f0 / 2, hw);
+  tc::tmem_st8w_nw(lb + TA_S + 64 + f0 / 2, lw);
+  tc::tmem_st16w_nw(lb + TC_S + f0, sw);
+}
+
+// 8 consecutive activations held as loaded (16 bytes of bf16 or 32 of f32), converted on use.
+template <typename T> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+  uint4 u;
+  __device__ __forceinline__ void ldg(const __nv_bfloat16* p) { u = __ldg(reinterpret_cast<const uint4*>(p)); }
+  __device__ __forceinline__ float get(int m) const {
+    const uint32_t w = m < 2 ? u.x : (m < 4 ? u.y : (m < 6 ? u.z : u.w));
+    return __uint_as_float((m & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+};
+template <> struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void ldg(const float* p) {
+    a = __ldg(reinterpret_cast<const float4*>(p));
+    b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  }
+  __device__ __forceinline__ float get(int m) const {
+    const float4& v = m < 4 ? a : b;
+    const int k = m & 3;
+    return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+  }
+};
+
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
 
 template <typename T>
-__global__ void __cluster_dims__(NSL, 1, 1) __launch_bounds__(NTS, 1)
-tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_state,
+__global__ void __launch_bounds__(NTC, 1)
+tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_state,
                 T* __restrict__ conv_state, int num_slots, const int32_t* __restrict__ cu,
                 const int32_t* __restrict__ slot_idx, const uint8_t* __restrict__ has_init,
                 int num_seqs, int total, const T* __restrict__ qkv, const T* __restrict__ z,
-                T* __restrict__ out, const float* __restrict__ ws, int cw0, int cw1,
+                T* __restrict__ out, const float* __restrict__ ws, int cw0, int cw1, int rec_base,
                 int32_t* __restrict__ status) {
+  tc::pdl_launch_dependents();   // the next window's intra kernel may take the SMs left free
   extern __shared__ __align__(1024) unsigned char sm[];
-  using S = StateSmem;
-  unsigned char* b4h = sm + S::B4;
-  unsigned char* b4l = b4h + 24576;
-  unsigned char* soph = sm + S::SOP;
-  unsigned char* sopl = soph + SOP_HALF;
-  unsigned char* uoph = sm + S::UOP;
-  unsigned char* uopl = uoph + UOP_HALF;
-  float* xbuf = reinterpret_cast<float*>(sm + S::XBUF);
+  using S = ChainSmem;
+  const float* ut_s = reinterpret_cast<const float*>(sm + S::UT);
+  float* ot = reinterpret_cast<float*>(sm + S::OT);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::BAR);
-  uint64_t* b3full = bars + 0;   // [2] B3 slot landed (loader -> MMA)
-  uint64_t* b3empty = bars + 2;  // [2] B3 slot read by MMA3 (MMA -> loader)
+  uint64_t* b3full = bars + 0;   // B3 landed (loader -> MMA)
+  uint64_t* b3empty = bars + 2;  // B3 read by the D3 products (MMA -> loader)
   uint64_t* b4full = bars + 4;   // B4 landed
-  uint64_t* b4empty = bars + 5;  // B4 read by MMA4
-  uint64_t* mma3 = bars + 6;
-  uint64_t* sready = bars + 7;   // S += K~^T U of the chunk done (the next chunk may read S)
-  uint64_t* dfull = bars + 8;    // [NDB] O of the chunk complete in D3[j] (MMA -> epilogue)
-  uint64_t* dempty = bars + 12;  // [NDB] D3[j] read by the epilogue (epilogue -> MMA)
-  uint64_t* xfull = bars + 16;   // [NXB] partial sums of the 4 slices arrived
-  uint64_t* sopf = bars + 20;    // S operand of the chunk written (main warps -> MMA warp)
-  uint64_t* uopf = bars + 21;    // U operand written, K~^T U read (main warps -> MMA warp)
+  uint64_t* b4empty = bars + 5;  // B4 read by the chunk's U^T products
+  uint64_t* utfull = bars + 6;   // U~ landed
+  uint64_t* utempty = bars + 7;  // U~ read by the main warps (8 arrivals)
+  uint64_t* sopf = bars + 8;     // S^T operand and the scaled S^T written (8 arrivals)
+  uint64_t* mma3 = bars + 9;     // D3^T complete
+  uint64_t* uopf = bars + 10;    // U^T operand written (8 arrivals)
+  uint64_t* sready = bars + 11;  // S^T += U^T K~ complete
+  uint64_t* dfull = bars + 12;   // O^T complete in D3^T columns 0-63
+  uint64_t* dempty = bars + 13;  // O^T read by the output warps (8 arrivals)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
   int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);
 
-  const int n = blockIdx.x / NSL, sig = blockIdx.x % NSL, h = blockIdx.y;
-  const uint32_t crank = tc::cluster_ctarank();
+  const int n = blockIdx.x, h = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (warp == 0) {
     int off = 0;
     const bool ok = seq_chunk_offset(cu, num_seqs, total, n, off);
-    if (lane == 0 && !ok && n == 0 && h == 0 && sig == 0) set_status(status, GDN_STATUS_BAD_SEQLENS);
+    if (lane == 0 && !ok && n == 0 && h == 0) set_status(status, GDN_STATUS_BAD_SEQLENS);
     if (lane == 0) {
       sh[0] = ok;
       sh[1] = off;
@@ -894,15 +920,18 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     }
   }
   if (tid == 0) {
-    for (int i = 0; i < 22; ++i) tc::mbar_init(bars + i, (i >= 12 && i < 16) ? 128 : (i >= 20 ? 256 : 1));
+    for (int i = 0; i < 14; ++i)
+      tc::mbar_init(bars + i, (i == 7 || i == 8 || i == 10 || i == 13) ? 8 : 1);
     tc::mbar_fence_init();
-    for (int i = 0; i < NXB; ++i) tc::mbar_arrive_expect_tx(xfull + i, NSL * XH * 64 * 4);   // chunks 0-3
   }
   if (warp == 0) tc::tmem_alloc(tslot, TC_COLS);
+  // Launched as a programmatic dependent of the window's intra kernel: everything above touches
+  // only this CTA's own resources; the records, the slot's state and the rest come after the
+  // intra kernel (and with it the previous window's chains) has completed.
+  tc::pdl_wait_primary();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  tc::cluster_sync_all();   // peers' mbarriers initialised before any exchange
   const uint32_t tb = *tslot;
   const int choff = sh[1];
   volatile int* abort = sh + 2;
@@ -916,288 +945,269 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   const bool empty_here = nch_seq == 0 && cw0 == 0;   // an empty sequence resets its slot once
   const int seq_start = seq_start0 + ca * CH, len = len0 - ca * CH;   // tokens from the window on
   const int s = __ldg(slot_idx + n);
-  // invalid cu_seqlens: nothing is read or written (the CTA still takes part in the cluster syncs)
+  // invalid cu_seqlens: nothing is read or written
   const bool valid = sh[0] && s >= 0 && s < num_slots && (nch > 0 || empty_here);
-  if (sh[0] && s >= num_slots && h == 0 && sig == 0 && tid == 0 && (nch > 0 || empty_here))
+  if (sh[0] && s >= num_slots && h == 0 && tid == 0 && (nch > 0 || empty_here))
     set_status(status, GDN_STATUS_SLOT_RANGE);
   const bool init_seq = valid && has_init != nullptr && __ldg(has_init + n) != 0;
   const bool init = valid && (init_seq || ca > 0);
   const bool seq_ends = valid && ((nch > 0 && cb == nch_seq) || empty_here);
-  float* Sg = rec_state + ((size_t)(valid ? s : 0) * d.Hv + h) * D * D + sig * SW;
+  float* Sg = rec_state + ((size_t)(valid ? s : 0) * d.Hv + h) * D * D;
   auto rec_of = [&](int c) {
-    return reinterpret_cast<const unsigned char*>(ws) + ((size_t)(choff + ca + c - cw0) * d.Hv + h) * REC_BYTES;
+    return reinterpret_cast<const unsigned char*>(ws) +
+           ((size_t)(rec_base + choff + ca + c - cw0) * d.Hv + h) * REC_BYTES;
   };
 
   if (warp < 8) {
-    // ================= main warps: thread e owns row e (dk index) of the S slice, columns
-    // [mh, mh + 16), in registers (sv); TMEM lane e of the K~^T U accumulator carries the same
-    // columns (both halves)
-    const int e = (warp & 3) * 32 + lane, mh = (warp >> 2) * MH;
-    const uint32_t lane_base = tc::taddr(tb, (warp & 3) * 32, 0);
-    float sv[MH];
+    // ================= main warps: thread (q, hf) is dv row j = 32 q + lane (its TMEM lane) of
+    // S^T for dk [64 hf, 64 hf + 64), and of U^T for tokens [32 hf, 32 hf + 32)
+    const int q = warp & 3, hf = warp >> 2;
+    const int j = 32 * q + lane;
+    const uint32_t lb = tb + ((uint32_t)(32 * q) << 16);
+    {
+      const float eg0 = nch > 0 ? *reinterpret_cast<const float*>(rec_of(0) + R_SC) : 1.f;
+      float v[64];
 #pragma unroll
-    for (int q = 0; q < MH; q += 4) {
-      const float4 x = init ? *reinterpret_cast<const float4*>(Sg + (size_t)e * D + mh + q)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-      sv[q] = x.x;
-      sv[q + 1] = x.y;
-      sv[q + 2] = x.z;
-      sv[q + 3] = x.w;
-    }
-    const int t = e - 64;             // token row of W S / U for lanes 64..127
-    const bool urow = (warp & 3) >= 2;
-    float ut[MH];                     // U~ of token t, columns mh.., loaded one chunk ahead
-    if (urow && nch > 0) {
-      const float* u0 = reinterpret_cast<const float*>(rec_of(0) + R_UT);
+      for (int i = 0; i < 64; ++i) v[i] = init ? Sg[(size_t)(64 * hf + i) * D + j] : 0.f;
 #pragma unroll
-      for (int q = 0; q < MH; q += 4) {
-        const float4 x = *reinterpret_cast<const float4*>(u0 + ut_index(t, sig * SW + mh + q));
-        ut[q] = x.x;
-        ut[q + 1] = x.y;
-        ut[q + 2] = x.z;
-        ut[q + 3] = x.w;
-      }
-    }
-    float egL_next = nch > 0 ? *reinterpret_cast<const float*>(rec_of(0) + R_SC) : 1.f;
-    for (int c = 0; c < nch; ++c) {
-      const uint32_t par = c & 1;
-      const uint32_t d3 = tb + TC_D3 + 64 * (c & (NDB - 1));   // D3 of the chunk (W S in rows 64-127)
-      // S slice (the chunk's initial state) -> B operand of W S and Q~ S
-      const float egL = egL_next;
-      if (c + 1 < nch) egL_next = *reinterpret_cast<const float*>(rec_of(c + 1) + R_SC);
-      put_mn16(soph, sopl, SOP_SBO, e, mh, sv);
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      mbar_arrive(sopf);
-      wait_or_abort(mma3, par, abort, status);
-      tc::fence_after_sync();
-      // U = U~ - W S (tokens 0..63 on lanes 64..127) -> B operand
-      if (urow) {
-        uint32_t rv[2 * MH];
-        tc::tmem_ld16_nw(tc::taddr(d3, (warp & 3) * 32, mh), rv);
-        tc::tmem_ld16_nw(tc::taddr(d3, (warp & 3) * 32, SW + mh), rv + MH);
-        tc::tmem_wait_ld();
-        tc::reg_fence16(rv);
-        tc::reg_fence16(rv + MH);
-        float u[MH];
+      for (int p = 0; p < 4; ++p) {
+        const int f0 = 64 * hf + 16 * p;
+        if (nch > 0) {
+          put_s16(lb, f0, v + 16 * p, eg0);
+        } else if (valid && !init) {   // an empty sequence without a state: the slot is reset
 #pragma unroll
-        for (int q = 0; q < MH; ++q) u[q] = ut[q] - (__uint_as_float(rv[q]) + __uint_as_float(rv[q + MH]));
-        put_mn16(uoph, uopl, UOP_SBO, t, mh, u);
-        if (c + 1 < nch) {
-          const float* un = reinterpret_cast<const float*>(rec_of(c + 1) + R_UT);
-#pragma unroll
-          for (int q = 0; q < MH; q += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(un + ut_index(t, sig * SW + mh + q));
-            ut[q] = x.x;
-            ut[q + 1] = x.y;
-            ut[q + 2] = x.z;
-            ut[q + 3] = x.w;
-          }
+          for (int i = 0; i < 16; ++i) Sg[(size_t)(f0 + i) * D + j] = 0.f;
         }
       }
-      // (every main thread arrives: its TMEM reads of the previous K~^T U are complete too)
-      tc::fence_proxy_async_smem();
+      tc::tmem_wait_st();
       tc::fence_before_sync();
-      mbar_arrive(uopf);
-      // S <- e^{gamma_L} S + K~^T U.  The O products may still run: they read only B4 and the U
-      // operand (rewritten only after the next chunk's MMA3, which the pipe orders after them)
-      // and write D3[jd], which the next chunk does not touch.
-      wait_or_abort(sready, par, abort, status);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sopf);
+    }
+#pragma unroll 1
+    for (int c = 0; c < nch; ++c) {
+      const uint32_t par = c & 1;
+      const float egn = (c + 1 < nch) ? *reinterpret_cast<const float*>(rec_of(c + 1) + R_SC) : 1.f;
+      // U^T = U~^T - (W S)^T -> the U^T operand
+      const bool ok1 = wait_or_abort(mma3, par, abort, status) && wait_or_abort(utfull, par, abort, status);
       tc::fence_after_sync();
-      {
-        uint32_t rv[2 * MH];
-        tc::tmem_ld16_nw(lane_base + TC_S + mh, rv);
-        tc::tmem_ld16_nw(lane_base + TC_S + SW + mh, rv + MH);
+      if (ok1) {
+        uint32_t rv[32];
+        tc::tmem_ld16_nw(lb + TC_D3 + 64 + 32 * hf, rv);
+        tc::tmem_ld16_nw(lb + TC_D3 + 64 + 32 * hf + 16, rv + 16);
         tc::tmem_wait_ld();
         tc::reg_fence16(rv);
-        tc::reg_fence16(rv + MH);
+        tc::reg_fence16(rv + 16);
+        uint32_t hw[16], lw[16];
 #pragma unroll
-        for (int q = 0; q < MH; ++q)
-          sv[q] = fmaf(egL, sv[q], __uint_as_float(rv[q]) + __uint_as_float(rv[q + MH]));
+        for (int p = 0; p < 16; ++p) {
+          const int t = 32 * hf + 2 * p;
+          const float u0 = ut_s[t * D + j] - __uint_as_float(rv[2 * p]);
+          const float u1 = ut_s[(t + 1) * D + j] - __uint_as_float(rv[2 * p + 1]);
+          tc::split2_bf16(u0, u1, hw[p], lw[p]);
+        }
+        tc::tmem_st16w_nw(lb + TA_U + 16 * hf, hw);
+        tc::tmem_st16w_nw(lb + TA_U + 32 + 16 * hf, lw);
+        tc::tmem_wait_st();
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(uopf);
+        mbar_arrive(utempty);
+      }
+      // S^T of the next chunk = the accumulated e^{gamma_L} S^T + U^T K~: its operand and its
+      // copy scaled by the next e^{gamma_L}; after the last chunk, the final state to the slot
+      const bool ok2 = wait_or_abort(sready, par, abort, status);
+      tc::fence_after_sync();
+      if (ok2) {
+#pragma unroll 1
+        for (int hp = 0; hp < 2; ++hp) {
+          const int f0 = 64 * hf + 32 * hp;
+          uint32_t rv[32];
+          tc::tmem_ld16_nw(lb + TC_S + f0, rv);
+          tc::tmem_ld16_nw(lb + TC_S + f0 + 16, rv + 16);
+          tc::tmem_wait_ld();
+          tc::reg_fence16(rv);
+          tc::reg_fence16(rv + 16);
+          const float* v = reinterpret_cast<const float*>(rv);
+          if (c + 1 < nch) {
+            put_s16(lb, f0, v, egn);
+            put_s16(lb, f0 + 16, v + 16, egn);
+          } else if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) Sg[(size_t)(f0 + i) * D + j] = v[i];
+          }
+        }
+        tc::tmem_wait_st();
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0 && c + 1 < nch) mbar_arrive(sopf);
+    }
+  } else if (warp < 16) {
+    // ================= output warps: warps 8-11 take the tokens [0, 32) of the chunk, 12-15 the
+    // tokens [32, 64).  O^T comes out of TMEM one dv row per thread (lane j) and goes through
+    // shared memory as O (token rows), so that thread r of the half then owns 8 consecutive
+    // columns (8 (r & 15) ..) of the tokens r / 16 + 8 b, b = 0..3: the sum of squares over dv
+    // adds up across 16 consecutive lanes, and z and the output move as 16-byte vectors.
+    const int q = warp & 3, th = (warp - 8) >> 2;
+    const int r = 32 * q + lane;               // thread of the half, 0..127
+    const int o8 = r & 15, tr = r >> 4;        // column octet, first token row
+    const uint32_t lb = tb + ((uint32_t)(32 * q) << 16);
+    float* oth = ot + th * 32 * D;             // this half's 32 token rows
+    const size_t ld = (size_t)d.Hv * D;
+    const size_t col = (size_t)h * D + 8 * o8;
+    float wv[8];
+    {
+      const float4 w0 = Act<T>::ldg4(norm_w + 8 * o8), w1 = Act<T>::ldg4(norm_w + 8 * o8 + 4);
+      wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
+      wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
+    }
+    Raw8<T> zr[4];   // z of the tokens 32 th + tr + 8 b, one chunk ahead
+    auto load_z = [&](int c) {
+      const int last = min(CH, len - c * CH) - 1;
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const int t = min(32 * th + tr + 8 * bb, last);
+        zr[bb].ldg(z + (size_t)(seq_start + c * CH + t) * ld + col);
+      }
+    };
+    if (nch > 0) load_z(0);
+#pragma unroll 1
+    for (int c = 0; c < nch; ++c) {
+      const int L = min(CH, len - c * CH);
+      const bool ok = wait_or_abort(dfull, c & 1, abort, status);
+      tc::fence_after_sync();
+      float o[32];
+      if (ok) {
+        uint32_t* ou = reinterpret_cast<uint32_t*>(o);
+        tc::tmem_ld16_nw(lb + TC_D3 + 32 * th, ou);
+        tc::tmem_ld16_nw(lb + TC_D3 + 32 * th + 16, ou + 16);
+        tc::tmem_wait_ld();
+        tc::reg_fence16(ou);
+        tc::reg_fence16(ou + 16);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0.f;
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dempty);   // D3^T may be overwritten from here on
+      if (c > 0) named_sync(1 + th, 128);   // the previous chunk's rows have been read
+#pragma unroll
+      for (int i = 0; i < 32; ++i) oth[i * D + r] = o[i];
+      named_sync(1 + th, 128);
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        const int tl = tr + 8 * bb;   // token of the half
+        const float4 v0 = *reinterpret_cast<const float4*>(oth + tl * D + 8 * o8);
+        const float4 v1 = *reinterpret_cast<const float4*>(oth + tl * D + 8 * o8 + 4);
+        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        float ss = 0.f;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) ss = fmaf(v[m], v[m], ss);
+#pragma unroll
+        for (int ofs = 1; ofs < 16; ofs <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, ofs);
+        const float inv = valid ? rsqrtf(ss * (1.0f / (float)D) + d.norm_eps) : 0.f;
+        const int t = 32 * th + tl;
+        if (t < L) {
+          T* op = out + (size_t)(seq_start + c * CH + t) * ld + col;
+          float y[8];
+#pragma unroll
+          for (int m = 0; m < 8; ++m) y[m] = v[m] * inv * wv[m] * silu_fast(zr[bb].get(m));
+          Act<T>::store4(op, make_float4(y[0], y[1], y[2], y[3]));
+          Act<T>::store4(op + 4, make_float4(y[4], y[5], y[6], y[7]));
+        }
+      }
+      if (c + 1 < nch) load_z(c + 1);
+    }
+  } else if (warp == 16) {
+    // ================= loader warp: bulk copies of each chunk's B3 (double-buffered), B4 and U~,
+    // each issued as soon as the buffer it refills has been read
+    if (lane == 0) {
+      int n3 = 0, n4 = 0, nu = 0;   // copies issued per buffer
+      auto load_b3 = [&](int c) {
+        tc::mbar_arrive_expect_tx(b3full, 2 * B3_HALF);
+        tc::bulk_g2s(sm + S::B3, rec_of(c) + R_B3, 2 * B3_HALF, b3full);
+        ++n3;
+      };
+      auto load_b4 = [&](int c) {
+        tc::mbar_arrive_expect_tx(b4full, 2 * B4_HALF);
+        tc::bulk_g2s(sm + S::B4, rec_of(c) + R_B4, 2 * B4_HALF, b4full);
+        ++n4;
+      };
+      auto load_ut = [&](int c) {
+        tc::mbar_arrive_expect_tx(utfull, 32768);
+        tc::bulk_g2s(sm + S::UT, rec_of(c) + R_UT, 32768, utfull);
+        ++nu;
+      };
+      if (nch > 0) {
+        load_b3(0);
+        load_b4(0);
+        load_ut(0);
+      }
+      for (int c = 0; c + 1 < nch; ++c) {
+        if (!wait_or_abort(b3empty, c & 1, abort, status)) break;
+        load_b3(c + 1);
+        if (!wait_or_abort(utempty, c & 1, abort, status)) break;
+        load_ut(c + 1);
+        if (!wait_or_abort(b4empty, c & 1, abort, status)) break;
+        load_b4(c + 1);
+      }
+      // after a timeout: wait (bounded) for the copies still in flight before the CTA exits
+      if (*abort) {
+        if (n3 > 0) tc::mbar_wait(b3full, (n3 - 1) & 1, 100000000ull);
+        if (n4 > 0) tc::mbar_wait(b4full, (n4 - 1) & 1, 100000000ull);
+        if (nu > 0) tc::mbar_wait(utfull, (nu - 1) & 1, 100000000ull);
       }
     }
-    // final state slice back to the slot
-    if (valid) {
-#pragma unroll
-      for (int q = 0; q < MH; q += 4)
-        *reinterpret_cast<float4*>(Sg + (size_t)e * D + mh + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
-    }
-  } else if (warp == 11) {
-    // ================= MMA warp: one thread issues every product of the chunk step, so that no
-    // main thread waits on the tensor pipe's instruction queue
+  } else {
+    // ================= MMA warp: one thread issues every product of the chunk step
     if (lane == 0) {
-    // operand descriptors, built once (K-step k: + 256 bytes for every tile; the S and U
-      // operands are MN-major)
-      const uint32_t id64 = tc::idesc_bf16_bmn(128, 2 * SW);
-      const uint64_t dA3h = tc::kstep_desc(tc::smem_u32(sm + S::B3), 128, 0);   // slot 0; slot 1 + 64 KiB
-      const uint64_t dA3l = tc::kstep_desc(tc::smem_u32(sm + S::B3 + B3_HALF), 128, 0);
-      const uint64_t dKh = tc::kstep_desc(tc::smem_u32(b4h) + 8192, 64, 0);
-      const uint64_t dKl = tc::kstep_desc(tc::smem_u32(b4l) + 8192, 64, 0);
-      const uint64_t dPh = tc::kstep_desc(tc::smem_u32(b4h), 64, 0);
-      const uint64_t dPl = tc::kstep_desc(tc::smem_u32(b4l), 64, 0);
-      const uint64_t dS = tc::sdesc(tc::smem_u32(soph), 128, SOP_SBO);
-      const uint64_t dU = tc::sdesc(tc::smem_u32(uoph), 128, UOP_SBO);
+      const uint32_t id128 = tc::idesc_bf16(128, 128), id64 = tc::idesc_bf16(128, 64);
+      const uint64_t dB3h = tc::kstep_desc(tc::smem_u32(sm + S::B3), 128, 0);
+      const uint64_t dB3l = tc::kstep_desc(tc::smem_u32(sm + S::B3 + B3_HALF), 128, 0);
+      const uint64_t dKh = tc::kstep_desc(tc::smem_u32(sm + S::B4) + 8192, 64, 0);   // K~^T rows
+      const uint64_t dKl = tc::kstep_desc(tc::smem_u32(sm + S::B4 + B4_HALF) + 8192, 64, 0);
+      const uint64_t dPh = tc::kstep_desc(tc::smem_u32(sm + S::B4), 64, 0);          // P rows
+      const uint64_t dPl = tc::kstep_desc(tc::smem_u32(sm + S::B4 + B4_HALF), 64, 0);
+      const uint32_t aSh = tb + TA_S, aSl = tb + TA_S + 64, aUh = tb + TA_U, aUl = tb + TA_U + 32;
+      const uint32_t d3 = tb + TC_D3, xs = tb + TC_S;
       for (int c = 0; c < nch; ++c) {
-        const uint32_t par = c & 1, b = c & 1;
-        const uint32_t jd = c & (NDB - 1);
-        const uint32_t d3 = tb + TC_D3 + 64 * jd;   // D3[jd]: rows 0-63 O (Q~ S + P U), rows 64-127 W S
-        if (wait_or_abort(sopf, par, abort, status) && wait_or_abort(b3full + b, (c >> 1) & 1, abort, status) &&
-            (c < NDB || wait_or_abort(dempty + jd, ((c / NDB) - 1) & 1, abort, status))) {
+        const uint32_t par = c & 1;
+        if (wait_or_abort(sopf, par, abort, status) && wait_or_abort(b3full, par, abort, status) &&
+            (c == 0 || wait_or_abort(dempty, (c - 1) & 1, abort, status))) {
           tc::fence_after_sync();
-          const uint32_t so = 65536u * b;   // B3 slot of the chunk
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {   // B = [S_hi ; S_lo], 64 rows
-            const uint64_t bk = tc::desc_add(dS, 256 * k);
-            tc::mma_bf16(d3, tc::desc_add(dA3h, so + 256 * k), bk, id64, k > 0);
-            tc::mma_bf16(d3, tc::desc_add(dA3l, so + 256 * k), bk, id64, 1);
+          for (int k = 0; k < 8; ++k) {   // D3^T = S^T [Q~ ; W]^T, K = dk
+            const uint64_t bh = tc::desc_add(dB3h, 256 * k), bl = tc::desc_add(dB3l, 256 * k);
+            tc::mma_bf16_tmem_a(d3, aSh + 8 * k, bh, id128, k > 0);
+            tc::mma_bf16_tmem_a(d3, aSh + 8 * k, bl, id128, 1);
+            tc::mma_bf16_tmem_a(d3, aSl + 8 * k, bh, id128, 1);
           }
           tc::mma_commit(mma3);
-          tc::mma_commit(b3empty + b);
+          tc::mma_commit(b3empty);
         }
         if (wait_or_abort(uopf, par, abort, status) && wait_or_abort(b4full, par, abort, status)) {
           tc::fence_after_sync();
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {   // K~^T U, fresh   (B4 rows 64..191; B = [U_hi ; U_lo])
-            const uint64_t bk = tc::desc_add(dU, 256 * k);
-            tc::mma_bf16(tb + TC_S, tc::desc_add(dKh, 256 * k), bk, id64, k > 0);
-            tc::mma_bf16(tb + TC_S, tc::desc_add(dKl, 256 * k), bk, id64, 1);
+          for (int k = 0; k < 4; ++k) {   // S^T += U^T K~, K = tokens
+            const uint64_t kh = tc::desc_add(dKh, 256 * k), kl = tc::desc_add(dKl, 256 * k);
+            tc::mma_bf16_tmem_a(xs, aUh + 8 * k, kh, id128, 1);
+            tc::mma_bf16_tmem_a(xs, aUh + 8 * k, kl, id128, 1);
+            tc::mma_bf16_tmem_a(xs, aUl + 8 * k, kh, id128, 1);
           }
-          tc::mma_commit(sready);   // the next chunk's S conversion overlaps the O products below
-          // D3 += [P ; K~^T rows 0..63] U: rows 0..63 become O; rows 64..127 (W S, consumed) are
-          // left as scratch
+          tc::mma_commit(sready);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t bk = tc::desc_add(dU, 256 * k);
-            tc::mma_bf16(d3, tc::desc_add(dPh, 256 * k), bk, id64, 1);
-            tc::mma_bf16(d3, tc::desc_add(dPl, 256 * k), bk, id64, 1);
+          for (int k = 0; k < 4; ++k) {   // O^T = (Q~ S)^T + U^T P^T in D3^T columns 0-63
+            const uint64_t ph = tc::desc_add(dPh, 256 * k), pl = tc::desc_add(dPl, 256 * k);
+            tc::mma_bf16_tmem_a(d3, aUh + 8 * k, ph, id64, 1);
+            tc::mma_bf16_tmem_a(d3, aUh + 8 * k, pl, id64, 1);
+            tc::mma_bf16_tmem_a(d3, aUl + 8 * k, ph, id64, 1);
           }
           tc::mma_commit(b4empty);
-          tc::mma_commit(dfull + jd);
-        }
-      }
-    }
-  } else if (warp == 10) {
-    // ================= loader warp: bulk copies of the chunks' operand images, each issued as soon
-    // as MMA has finished reading the buffer it refills (B3 double-buffered, B4 single)
-    if (lane == 0) {
-      int n3a = 0, n3b = 0, n4 = 0;   // copies issued per buffer
-      auto load_b3 = [&](int c) {
-        const int j = c & 1;
-        tc::mbar_arrive_expect_tx(b3full + j, 2 * B3_HALF);
-        tc::bulk_g2s(sm + S::B3 + j * 65536, rec_of(c) + R_B3, 2 * B3_HALF, b3full + j);
-        if (j) ++n3b;
-        else ++n3a;
-      };
-      auto load_b4 = [&](int c) {
-        tc::mbar_arrive_expect_tx(b4full, 2 * B4_HALF);
-        tc::bulk_g2s(b4h, rec_of(c) + R_B4, 2 * B4_HALF, b4full);
-        ++n4;
-      };
-      if (nch > 0) load_b3(0);
-      if (nch > 0) load_b4(0);
-      if (nch > 1) load_b3(1);
-      for (int c = 0; c + 1 < nch; ++c) {
-        if (!wait_or_abort(b4empty, c & 1, abort, status)) break;
-        load_b4(c + 1);
-        if (c + 2 < nch) {
-          if (!wait_or_abort(b3empty + (c & 1), (c >> 1) & 1, abort, status)) break;
-          load_b3(c + 2);
-        }
-      }
-      // after a timeout: wait (bounded) for the copies still in flight before the CTA exits
-      if (*abort) {
-        if (n3a > 0) tc::mbar_wait(b3full, (n3a - 1) & 1, 100000000ull);
-        if (n3b > 0) tc::mbar_wait(b3full + 1, (n3b - 1) & 1, 100000000ull);
-        if (n4 > 0) tc::mbar_wait(b4full, (n4 - 1) & 1, 100000000ull);
-      }
-    }
-  } else {
-    // ================= epilogue warps 8, 9, 12, 13: thread t owns token t of the chunk (TMEM lane t
-    // of D3) and the 16 columns of half xh of the slice
-    const int t = (warp & 3) * 32 + lane, xh = (warp >> 2) & 1;
-    constexpr int EW = SW / XH;
-    const size_t ld = (size_t)d.Hv * D;
-    const size_t col0 = (size_t)h * D + sig * SW + xh * EW;
-    float wn[EW];
-#pragma unroll
-    for (int q = 0; q < EW; q += 4) {
-      const float4 x = Act<T>::ldg4(norm_w + sig * SW + xh * EW + q);
-      wn[q] = x.x;
-      wn[q + 1] = x.y;
-      wn[q + 2] = x.z;
-      wn[q + 3] = x.w;
-    }
-    // software-pipelined over the chunks: step c reads chunk c's outputs and sends their partial
-    // sums of squares to the cluster, then normalises and stores chunk c - 1, whose sums were
-    // sent one step earlier (so the exchange latency overlaps a step of work)
-    auto load_z = [&](int c, float4* zz) {
-      const int i = min(t, min(CH, len - c * CH) - 1);
-      const T* zp = z + (size_t)(seq_start + c * CH + i) * ld + col0;
-#pragma unroll
-      for (int q = 0; q < EW / 4; ++q) zz[q] = Act<T>::ldg4(zp + 4 * q);
-    };
-    float4 zc[EW / 4], zp[EW / 4];   // z of chunk c (loaded at step c) and of chunk c - 1
-    float oc[EW], op[EW];
-    const uint32_t xb_local = tc::smem_u32(xbuf);
-    const uint32_t xf_local = tc::smem_u32(xfull);
-    bool xok = true;
-    for (int c = 0; c <= nch; ++c) {
-#pragma unroll
-      for (int q = 0; q < EW; ++q) op[q] = oc[q];
-#pragma unroll
-      for (int q = 0; q < EW / 4; ++q) zp[q] = zc[q];
-      if (c < nch) {
-        const uint32_t jd = c & (NDB - 1), xb = c & (NXB - 1);
-        wait_or_abort(dfull + jd, (c / NDB) & 1, abort, status);
-        tc::fence_after_sync();
-        float o2[2 * EW];
-        const uint32_t da = tc::taddr(tb + TC_D3 + 64 * jd, (warp & 3) * 32, xh * EW);
-        tc::tmem_ld16(da, o2);
-        tc::tmem_ld16(da + SW, o2 + EW);
-        tc::fence_before_sync();
-        mbar_arrive(dempty + jd);
-        float ss = 0.f;
-#pragma unroll
-        for (int q = 0; q < EW; ++q) {
-          oc[q] = o2[q] + o2[q + EW];
-          ss = fmaf(oc[q], oc[q], ss);
-        }
-        const uint32_t slot_off = (((xb * NSL + crank) * XH + xh) * 64 + t) * 4;
-#pragma unroll
-        for (uint32_t r = 0; r < NSL; ++r)
-          tc::st_async_f32(tc::mapa_shared(xb_local + slot_off, r), ss,
-                           tc::mapa_shared(xf_local + xb * 8, r));
-        load_z(c, zc);
-      }
-      if (c >= 1) {
-        const int cp = c - 1;
-        const uint32_t xb = cp & (NXB - 1);
-        const int L = min(CH, len - cp * CH);
-        if (xok && !tc::mbar_wait_cluster(xfull + xb, (cp / NXB) & 1)) {
-          xok = false;
-          *abort = 1;
-          set_status(status, GDN_STATUS_TIMEOUT);
-        }
-        // this buffer's next use is chunk cp + NXB: its peers send that only after this CTA has
-        // sent chunk cp + 2, so posting the expected bytes now comes first
-        if (warp == 8 && lane == 0 && cp + NXB < nch) {
-          tc::mbar_arrive_expect_tx(xfull + xb, NSL * XH * 64 * 4);
-          tc::fence_acq_rel_cluster();
-        }
-        float tot = 0.f;
-#pragma unroll
-        for (int r = 0; r < NSL * XH; ++r) tot += xbuf[(xb * NSL * XH + r) * 64 + t];
-        const float inv = valid ? rsqrtf(tot * (1.0f / (float)D) + d.norm_eps) : 0.f;
-        if (t < L) {
-          T* o_ptr = out + (size_t)(seq_start + cp * CH + t) * ld + col0;
-#pragma unroll
-          for (int q = 0; q < EW / 4; ++q) {
-            const float4 r4 = make_float4(op[4 * q] * inv * wn[4 * q] * silu_fast(zp[q].x),
-                                          op[4 * q + 1] * inv * wn[4 * q + 1] * silu_fast(zp[q].y),
-                                          op[4 * q + 2] * inv * wn[4 * q + 2] * silu_fast(zp[q].z),
-                                          op[4 * q + 3] * inv * wn[4 * q + 3] * silu_fast(zp[q].w));
-            Act<T>::store4(o_ptr + 4 * q, r4);
-          }
+          tc::mma_commit(dfull);
         }
       }
     }
@@ -1206,9 +1216,9 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, TC_COLS);
   // conv state <- the sequence's last K-1 raw inputs (older ones kept when continuing)
-  if (seq_ends && h == 0 && sig == 0) {
+  if (seq_ends && h == 0) {
     T* csw = conv_state + (size_t)s * 3 * d.cqkv;
-    for (int cch = tid; cch < d.cqkv; cch += NTS) {
+    for (int cch = tid; cch < d.cqkv; cch += NTC) {
       T v3[3];
 #pragma unroll
       for (int m = 0; m < 3; ++m) {
@@ -1220,7 +1230,6 @@ tc_state_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       for (int m = 0; m < 3; ++m) csw[(size_t)m * d.cqkv + cch] = v3[m];
     }
   }
-  tc::cluster_sync_all();   // no CTA leaves while a peer may still store into its shared memory
 }
 
 template <typename T>
@@ -1229,34 +1238,83 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
              const void* qkv, const void* z, const void* a, const void* b, void* out, void* ws,
              size_t ws_bytes, cudaStream_t stream) {
   // Chunks are numbered across the sequences; at most total / 64 + num_seqs of them exist.  The
-  // records of `win` consecutive chunks fit the workspace, so the call runs in windows of that
-  // many chunks: each window's intra kernel, then its state kernel, which carries every
-  // sequence's state to the next window through the slot.
-  const int nc_max = total / CH + num_seqs;
+  // call runs in windows of consecutive chunks: each window's intra kernel writes its records,
+  // then its chain kernel carries every sequence's state through the window to the slot.
+  // Pipelined: windows alternate between two halves of the workspace, and window w + 1's intra
+  // kernel is a programmatic dependent launch of window w's chain kernel, so it starts on the SMs
+  // the chains leave free.  Its CTAs wait for that chain kernel to complete before they exit.
+  // Each chain kernel is a programmatic dependent launch of its window's intra kernel (which
+  // signals only by completing), so it is set up as soon as that kernel ends and waits for it
+  // before reading anything: window w + 1's chains read the slots only after window w's chains
+  // have completed, and the half window w + 1's records go to was last read by window w - 1's
+  // chains, complete before window w's chain kernel could even start.  Serial (a workspace of fewer than two pipelined windows, or more chains than SMs):
+  // every window from the start of the workspace, each launch after the previous one.
+  // Chunk count bound: sum over sequences of ceil(len / 64) <= (total + 63 num_seqs) / 64.
+  const int nc_max = std::max(1, (int)(((long long)total + (long long)(CH - 1) * num_seqs) / CH));
   const size_t per_chunk = (size_t)d.Hv * REC_BYTES;
-  const int win = (int)std::min<size_t>((size_t)nc_max, ws_bytes / per_chunk);
-  if (win < 1) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  const size_t cap = ws_bytes / per_chunk;
+  if (cap < 1) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  // Pipelined windows are as large as the intra CTAs that fit beside the chains (one per SM).
+  const int chains = num_seqs * d.Hv;
+  const bool pipe = cap >= 2 && chains < nsm && total > 0 && nc_max > 1;
+  const int pwin = std::max(1, (nsm - chains) / d.Hk);
+  const int win = pipe ? (int)std::min<size_t>({(size_t)pwin, cap / 2, (size_t)nc_max})
+                       : (int)std::min<size_t>((size_t)nc_max, cap);
   auto k1 = tc_intra_kernel<T>;
-  auto k2 = tc_state_kernel<T>;
+  auto k2 = tc_chain_kernel<T>;
   if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IntraSmem::BYTES) !=
           cudaSuccess ||
-      cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)StateSmem::BYTES) !=
+      cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ChainSmem::BYTES) !=
           cudaSuccess)
     return GDN_ERR_CUDA;
   float* wsf = static_cast<float*>(ws);
-  for (int cw0 = 0; cw0 < nc_max; cw0 += win) {
+  const T* conv_w = static_cast<const T*>(w->conv_weight);
+  const T* conv_s = static_cast<const T*>(pool->conv_state);
+  const T* qkv_t = static_cast<const T*>(qkv);
+  const T* a_t = static_cast<const T*>(a);
+  const T* b_t = static_cast<const T*>(b);
+  int wi = 0;
+  for (int cw0 = 0; cw0 < nc_max; cw0 += win, ++wi) {
     const int cw1 = std::min(nc_max, cw0 + win);
-    if (total > 0)
-      k1<<<dim3(cw1 - cw0, d.Hk), NTI, IntraSmem::BYTES, stream>>>(
-          d, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
-          static_cast<const T*>(pool->conv_state), pool->num_slots, cu, slot_idx, has_init, num_seqs,
-          total, static_cast<const T*>(qkv), static_cast<const T*>(a), static_cast<const T*>(b), wsf,
-          cw0, pool->status);
-    k2<<<dim3(NSL * num_seqs, d.Hv), NTS, StateSmem::BYTES, stream>>>(
-        d, static_cast<const T*>(w->norm_weight), pool->rec_state, static_cast<T*>(pool->conv_state),
-        pool->num_slots, cu, slot_idx, has_init, num_seqs, total, static_cast<const T*>(qkv),
-        static_cast<const T*>(z), static_cast<T*>(out), wsf, cw0, cw1, pool->status);
-    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+    const int rec_base = pipe ? (wi & 1) * win : 0;
+    if (total > 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(cw1 - cw0), (unsigned)d.Hk);
+      cfg.blockDim = dim3(NTI);
+      cfg.dynamicSmemBytes = IntraSmem::BYTES;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = (pipe && wi > 0) ? 1 : 0;
+      if (cudaLaunchKernelEx(&cfg, k1, d, w->A_log, w->dt_bias, conv_w, conv_s, pool->num_slots, cu,
+                             slot_idx, has_init, num_seqs, total, qkv_t, a_t, b_t, wsf, cw0, rec_base,
+                             pool->status) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    }
+    {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)num_seqs, (unsigned)d.Hv);
+      cfg.blockDim = dim3(NTC);
+      cfg.dynamicSmemBytes = ChainSmem::BYTES;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[0].val.programmaticStreamSerializationAllowed = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = pipe ? 1 : 0;
+      if (cudaLaunchKernelEx(&cfg, k2, d, static_cast<const T*>(w->norm_weight), pool->rec_state,
+                             static_cast<T*>(pool->conv_state), pool->num_slots, cu, slot_idx,
+                             has_init, num_seqs, total, qkv_t, static_cast<const T*>(z),
+                             static_cast<T*>(out), static_cast<const float*>(wsf), cw0, cw1, rec_base,
+                             pool->status) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    }
   }
   return GDN_OK;
 }

@@ -105,6 +105,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T -- A (M = 128 rows on TMEM lanes 0-127, the 16 bf16 of a K-step
+// packed in 8 consecutive columns, element 2c in the low half of column c).  Issued by one thread.
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives (once) on the mbarrier when all previously issued MMAs of this thread complete.
 __device__ __forceinline__ void mma_commit(uint64_t* mbar) {
   asm volatile(
@@ -177,6 +188,21 @@ __device__ __forceinline__ void tmem_st16_nw(uint32_t taddr, const float* v) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
+// 32 lanes x 8 / 16 columns of raw 32-bit words (thread i of the warp writes lane base + i); no wait.
+__device__ __forceinline__ void tmem_st8w_nw(uint32_t taddr, const uint32_t* w) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
+               "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st16w_nw(uint32_t taddr, const uint32_t* w) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+          taddr),
+      "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]),
+      "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+      : "memory");
+}
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
   asm volatile(
@@ -304,6 +330,17 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
+
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Lets a grid launched as a programmatic dependent of this one start once every CTA of this grid
+// has executed it (or exited).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+// Waits until the grid(s) this one was launched as a programmatic dependent of have completed
+// and their memory operations are visible; returns at once for an ordinary launch.
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 
 // ------------------------------------------------------------------ split bf16
 
