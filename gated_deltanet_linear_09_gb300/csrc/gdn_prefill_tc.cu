@@ -1215,10 +1215,13 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, TC_COLS);
-  // conv state <- the sequence's last K-1 raw inputs (older ones kept when continuing)
-  if (seq_ends && h == 0) {
+  // conv state <- the sequence's last K-1 raw inputs (older ones kept when continuing); the
+  // sequence's Hv CTAs take one slice of the channels each
+  if (seq_ends) {
     T* csw = conv_state + (size_t)s * 3 * d.cqkv;
-    for (int cch = tid; cch < d.cqkv; cch += NTC) {
+    const int per = (d.cqkv + d.Hv - 1) / d.Hv;
+    const int c_end = min(d.cqkv, (h + 1) * per);
+    for (int cch = h * per + tid; cch < c_end; cch += NTC) {
       T v3[3];
 #pragma unroll
       for (int m = 0; m < 3; ++m) {
@@ -1258,12 +1261,15 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return GDN_ERR_CUDA;
-  // Pipelined windows are as large as the intra CTAs that fit beside the chains (one per SM).
+  // Pipelined windows are as large as the intra CTAs that fit beside the chains (one per SM);
+  // the first one, which runs alone, as large as a full wave of intra CTAs.
   const int chains = num_seqs * d.Hv;
   const bool pipe = cap >= 2 && chains < nsm && total > 0 && nc_max > 1;
   const int pwin = std::max(1, (nsm - chains) / d.Hk);
   const int win = pipe ? (int)std::min<size_t>({(size_t)pwin, cap / 2, (size_t)nc_max})
                        : (int)std::min<size_t>((size_t)nc_max, cap);
+  const int win0 = pipe ? (int)std::min<size_t>({(size_t)std::max(win, nsm / d.Hk), cap / 2, (size_t)nc_max})
+                        : win;
   auto k1 = tc_intra_kernel<T>;
   auto k2 = tc_chain_kernel<T>;
   if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IntraSmem::BYTES) !=
@@ -1277,10 +1283,10 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
   const T* qkv_t = static_cast<const T*>(qkv);
   const T* a_t = static_cast<const T*>(a);
   const T* b_t = static_cast<const T*>(b);
-  int wi = 0;
-  for (int cw0 = 0; cw0 < nc_max; cw0 += win, ++wi) {
-    const int cw1 = std::min(nc_max, cw0 + win);
-    const int rec_base = pipe ? (wi & 1) * win : 0;
+  int cw1 = 0;
+  for (int wi = 0, cw0 = 0; cw0 < nc_max; ++wi, cw0 = cw1) {
+    cw1 = std::min(nc_max, cw0 + (wi == 0 ? win0 : win));
+    const int rec_base = pipe ? (wi & 1) * win0 : 0;
     if (total > 0) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)(cw1 - cw0), (unsigned)d.Hk);
