@@ -414,11 +414,13 @@ __device__ __forceinline__ float* xblk(float* M, int q) {
 //   2. the two 32 x 32 diagonal halves: T_10 = -D_1 (A_10 D_0), T_32 = -D_3 (A_32 D_2);
 //   3. the 32 x 32 off-diagonal half, -T2 (A21 T1) with T1, T2 the halves of step 2: first
 //      Y = A21 T1, then T_ik = -sum_m T2_im Y_mk.
-// Each block of A is read before T overwrites it.  Five barriers; ends with one.
-__device__ __forceinline__ void tri_inverse(float* M) {
+// Each block of A is read before T overwrites it.  Five barriers; ends with one.  tri_inverse_n
+// inverts nm = 1 or 2 independent matrices at once (the second on the next threads).
+__device__ __forceinline__ void tri_inverse_n(float* M0, float* M1, int nm) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (warp < 4) {
-    const int b = warp, c = lane & 15;
+  if (warp < 4 * nm) {
+    float* M = (warp >> 2) ? M1 : M0;
+    const int b = warp & 3, c = lane & 15;
     float* mb = M + (16 * b) * AS + 16 * b;
     float x[16];
 #pragma unroll
@@ -445,16 +447,21 @@ __device__ __forceinline__ void tri_inverse(float* M) {
     }
   }
   __syncthreads();
-  // steps 2 and 3: thread e computes columns [4 cq, 4 cq + 4) of row rr of a block
-  if (tid < 128) {  // step 2: X = A_{bi,bi-1} D_{bi-1} for bi = 1, 3 (scratch blocks 0, 1)
-    const int which = tid >> 6, rr = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+  // steps 2 and 3: thread e of a matrix's group computes columns [4 cq, 4 cq + 4) of row rr of a
+  // block; matrix 1 takes the threads after matrix 0's
+  if (tid < 128 * nm) {  // step 2: X = A_{bi,bi-1} D_{bi-1} for bi = 1, 3 (scratch blocks 0, 1)
+    float* M = (tid >> 7) ? M1 : M0;
+    const int t = tid & 127;
+    const int which = t >> 6, rr = (t >> 2) & 15, c4 = 4 * (t & 3);
     const int bi = which ? 3 : 1, bk = bi - 1;
     *reinterpret_cast<float4*>(xblk(M, which) + rr * AS + c4) =
         dot16x4(M + (16 * bi + rr) * AS + 16 * bk, M + (16 * bk) * AS + 16 * bk + c4, AS);
   }
   __syncthreads();
-  if (tid < 128) {  //         T_{bi,bi-1} = -D_bi X
-    const int which = tid >> 6, rr = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+  if (tid < 128 * nm) {  //         T_{bi,bi-1} = -D_bi X
+    float* M = (tid >> 7) ? M1 : M0;
+    const int t = tid & 127;
+    const int which = t >> 6, rr = (t >> 2) & 15, c4 = 4 * (t & 3);
     const int bi = which ? 3 : 1, bk = bi - 1;
     *reinterpret_cast<float4*>(M + (16 * bi + rr) * AS + 16 * bk + c4) =
         neg4(dot16x4(M + (16 * bi + rr) * AS + 16 * bi, xblk(M, which) + c4, AS));
@@ -462,8 +469,10 @@ __device__ __forceinline__ void tri_inverse(float* M) {
   __syncthreads();
   // step 3: blocks (bi, bk), bi in {2, 3}, bk in {0, 1}:
   //   Y_{bi,bk} = sum_{m=bk}^{1} A_{bi,m} T_{m,bk}  (scratch block (bi - 2) * 2 + bk)
-  if (tid < 256) {
-    const int blk = tid >> 6, rr = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+  if (tid < 256 * nm) {
+    float* M = (tid >> 8) ? M1 : M0;
+    const int t = tid & 255;
+    const int blk = t >> 6, rr = (t >> 2) & 15, c4 = 4 * (t & 3);
     const int bi = 2 + (blk >> 1), bk = blk & 1;
     float4 acc = dot16x4(M + (16 * bi + rr) * AS + 16 * bk, M + (16 * bk) * AS + 16 * bk + c4, AS);
     if (bk == 0) add4(acc, dot16x4(M + (16 * bi + rr) * AS + 16, M + 16 * AS + c4, AS));
@@ -471,8 +480,10 @@ __device__ __forceinline__ void tri_inverse(float* M) {
   }
   __syncthreads();
   //   T_{bi,bk} = -sum_{m=2}^{bi} T_{bi,m} Y_{m,bk}
-  if (tid < 256) {
-    const int blk = tid >> 6, rr = (tid >> 2) & 15, c4 = 4 * (tid & 3);
+  if (tid < 256 * nm) {
+    float* M = (tid >> 8) ? M1 : M0;
+    const int t = tid & 255;
+    const int blk = t >> 6, rr = (t >> 2) & 15, c4 = 4 * (t & 3);
     const int bi = 2 + (blk >> 1), bk = blk & 1;
     float4 acc = dot16x4(M + (16 * bi + rr) * AS + 32, xblk(M, bk) + c4, AS);
     if (bi == 3) add4(acc, dot16x4(M + (16 * bi + rr) * AS + 48, xblk(M, 2 + bk) + c4, AS));
@@ -480,6 +491,7 @@ __device__ __forceinline__ void tri_inverse(float* M) {
   }
   __syncthreads();
 }
+__device__ __forceinline__ void tri_inverse(float* M) { tri_inverse_n(M, M, 1); }
 
 // [T diag(cw) ; T diag(cu)] -> the split-bf16 K-major A operand (128 rows x 64 K) of D2.
 // Unit u: row & 7 = u & 7, k-group = (u >> 3) & 7, row group = u >> 6 (consecutive 16-byte
@@ -671,7 +683,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
 
   // A (to At) and P (to the record) of V-head j from D1: warp w reads TMEM lanes 32 (w % 4) and
   // the 8 columns of eighth w / 4.  Lanes 0-63 are K-rows (A), lanes 64-127 Q-rows (P).
-  auto a_and_p = [&](int j) {
+  auto a_and_p = [&](int j, float* Aj) {
     const float* gam = vecs + j * 320;
     const float* bet = gam + 64;
     const int rr = (warp & 3) * 32 + lane, j0 = (warp >> 2) * 8;
@@ -689,7 +701,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
           const float m = (jj < i) ? bi : 0.f;
           a4[u] = m * exp_fast(fminf(gi - gam[jj], 0.f)) * v[q + u];
         }
-        *reinterpret_cast<float4*>(At + i * AS + j0 + q) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+        *reinterpret_cast<float4*>(Aj + i * AS + j0 + q) = make_float4(a4[0], a4[1], a4[2], a4[3]);
       }
     } else {
       const int i = rr - 64;
@@ -709,21 +721,11 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     }
   };
 
-  // ---- prologue of V-head 0: A / P, T, the D2 operand
-  a_and_p(0);
-  __syncthreads();
-  tri_inverse(At);
-  t_to_b2(At, vecs + 256, vecs + 64, b2, b2 + 16384);
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-
+  // D2 of V-head j into TMEM columns (wc: W rows, lanes 0-63; uc: U~ rows, lanes 64-127):
+  // [T diag(bgk) ; T diag(beta)] x K^T and the same x V^T.  K^T and V^T are read MN-major straight
+  // out of the token-row tiles (N-direction core stride 128 B, 8-token stride 2 KiB).
   const uint32_t idn = tc::idesc_bf16_bmn(128, 128);
-  for (int j = 0; j < r; ++j) {
-    // ---- D2 of V-head j: [T diag(bgk) ; T diag(beta)] x K^T -> W rows (lanes 0-63);
-    //      the same x V^T -> U~ rows (lanes 64-127).  K^T and V^T are read MN-major straight
-    //      out of the token-row tiles (N-direction core stride 128 B, 8-token stride 2 KiB).
+  auto issue_d2 = [&](uint32_t wc, uint32_t uc) {
     if (tid == 0 && !*abort) {
       const uint64_t dah = tc::kstep_desc(tc::smem_u32(b2), 64, 0);
       const uint64_t dal = tc::kstep_desc(tc::smem_u32(b2 + 16384), 64, 0);
@@ -735,65 +737,108 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
       for (int k = 0; k < 4; ++k) {
         const uint64_t ah = tc::desc_add(dah, 256 * k), al = tc::desc_add(dal, 256 * k);
         const uint32_t o = 4096u * k;
-        tc::mma_bf16(tb + TI_W, ah, tc::desc_add(dkh, o), idn, k > 0);
-        tc::mma_bf16(tb + TI_W, ah, tc::desc_add(dkl, o), idn, 1);
-        tc::mma_bf16(tb + TI_W, al, tc::desc_add(dkh, o), idn, 1);
-        tc::mma_bf16(tb + TI_U, ah, tc::desc_add(dvh, o), idn, k > 0);
-        tc::mma_bf16(tb + TI_U, ah, tc::desc_add(dvl, o), idn, 1);
-        tc::mma_bf16(tb + TI_U, al, tc::desc_add(dvh, o), idn, 1);
+        tc::mma_bf16(tb + wc, ah, tc::desc_add(dkh, o), idn, k > 0);
+        tc::mma_bf16(tb + wc, ah, tc::desc_add(dkl, o), idn, 1);
+        tc::mma_bf16(tb + wc, al, tc::desc_add(dkh, o), idn, 1);
+        tc::mma_bf16(tb + uc, ah, tc::desc_add(dvh, o), idn, k > 0);
+        tc::mma_bf16(tb + uc, ah, tc::desc_add(dvl, o), idn, 1);
+        tc::mma_bf16(tb + uc, al, tc::desc_add(dvh, o), idn, 1);
       }
       tc::mma_commit(bar + 1);
     }
-    // ---- while it runs: the next V-head's V conv (held in registers), A / P and inverse
-    if (j + 1 < r) {
-      ring_wait(j + 3);   // tensor 2 + (j + 1); also: slot of tensor j + 2 free
-      if (issued < ntens) {
-        ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), seq_start, seq_len, p0, slot_of(issued));
-        ++issued;
-      }
-      conv_slot<T>(slot_of(j + 3), L, y);
-      a_and_p(j + 1);
-      __syncthreads();
-      tri_inverse(At);
-    }
-    // ---- W and U~ rows of V-head j straight from TMEM into the record
-    wait_or_abort(bar + 1, j & 1, abort, status);
-    tc::fence_after_sync();
-    {
-      unsigned char* rec = rec_of(j);
-      const int lg = warp & 3, cq = (warp >> 2) * 16;   // 16 of the 128 columns per warp
-      const int i = (lg & 1) * 32 + lane;
-      float v[16];
-      if (lg < 2) {
-        tc::tmem_ld16(tc::taddr(tb + TI_W, lg * 32, cq), v);
+  };
+  // W and U~ rows of V-head j straight from TMEM (columns wc / uc) into the record
+  auto readout = [&](int j, uint32_t wc, uint32_t uc) {
+    unsigned char* rec = rec_of(j);
+    const int lg = warp & 3, cq = (warp >> 2) * 16;   // 16 of the 128 columns per warp
+    const int i = (lg & 1) * 32 + lane;
+    float v[16];
+    if (lg < 2) {
+      tc::tmem_ld16(tc::taddr(tb + wc, lg * 32, cq), v);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          uint4 hh, ll;
-          split8(v + 8 * u, hh, ll);
-          const uint32_t off = tc::kmajor_off(64 + i, cq + 8 * u, 128);   // W rows of B3
-          gst_unit(rec + R_B3, off, hh);
-          gst_unit(rec + R_B3 + B3_HALF, off, ll);
-        }
-      } else {
-        tc::tmem_ld16(tc::taddr(tb + TI_U, lg * 32, cq), v);
-        // U~ record row-major: each thread stores 16 consecutive columns of its token
-        float* ut = reinterpret_cast<float*>(rec + R_UT);
-#pragma unroll
-        for (int q = 0; q < 16; q += 4)
-          *reinterpret_cast<float4*>(ut + ut_index(i, cq + q)) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+      for (int u = 0; u < 2; ++u) {
+        uint4 hh, ll;
+        split8(v + 8 * u, hh, ll);
+        const uint32_t off = tc::kmajor_off(64 + i, cq + 8 * u, 128);   // W rows of B3
+        gst_unit(rec + R_B3, off, hh);
+        gst_unit(rec + R_B3 + B3_HALF, off, ll);
       }
+    } else {
+      tc::tmem_ld16(tc::taddr(tb + uc, lg * 32, cq), v);
+      // U~ record row-major: each thread stores 16 consecutive columns of its token
+      float* ut = reinterpret_cast<float*>(rec + R_UT);
+#pragma unroll
+      for (int q = 0; q < 16; q += 4)
+        *reinterpret_cast<float4*>(ut + ut_index(i, cq + q)) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
     }
+  };
+  auto sync_operands = [&]() {
+    tc::fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    if (j + 1 < r) {
-      // the D2 operands of V-head j + 1 (VT and B2 were read by the MMAs just completed)
-      put_row8(vt, vt + 16384, y);
-      t_to_b2(At, vecs + (j + 1) * 320 + 256, vecs + (j + 1) * 320 + 64, b2, b2 + 16384);
-      tc::fence_proxy_async_smem();
+  };
+
+  if (r == 2) {
+    // ---- two V-heads: both A / P and both inverses at once (the second A in the ring slot of
+    // V-head 0's input, consumed by its conv), and V-head 0's readout beside V-head 1's MMAs, which
+    // go to the TMEM columns of D1 (consumed) and the last 128
+    static_assert(R::SLOT >= 4 * 64 * AS, "a ring slot holds an A matrix");
+    float* At1 = reinterpret_cast<float*>(slot_of(2));
+    a_and_p(0, At);
+    a_and_p(1, At1);
+    __syncthreads();
+    tri_inverse_n(At, At1, 2);
+    t_to_b2(At, vecs + 256, vecs + 64, b2, b2 + 16384);
+    sync_operands();
+    issue_d2(TI_W, TI_U);
+    ring_wait(3);
+    conv_slot<T>(slot_of(3), L, y);
+    wait_or_abort(bar + 1, 0, abort, status);
+    tc::fence_after_sync();
+    put_row8(vt, vt + 16384, y);
+    t_to_b2(At1, vecs + 320 + 256, vecs + 320 + 64, b2, b2 + 16384);
+    sync_operands();
+    issue_d2(TI_D1, TI_COLS - 128);
+    readout(0, TI_W, TI_U);
+    wait_or_abort(bar + 1, 1, abort, status);
+    tc::fence_after_sync();
+    readout(1, TI_D1, TI_COLS - 128);
+    tc::fence_before_sync();
+    __syncthreads();
+  } else {
+    // ---- one V-head after another: the next V-head's conv, A / P and inverse overlap the
+    // current V-head's MMAs
+    a_and_p(0, At);
+    __syncthreads();
+    tri_inverse(At);
+    t_to_b2(At, vecs + 256, vecs + 64, b2, b2 + 16384);
+    sync_operands();
+    for (int j = 0; j < r; ++j) {
+      issue_d2(TI_W, TI_U);
+      if (j + 1 < r) {
+        ring_wait(j + 3);   // tensor 2 + (j + 1); also: slot of tensor j + 2 free
+        if (issued < ntens) {
+          ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), seq_start, seq_len, p0, slot_of(issued));
+          ++issued;
+        }
+        conv_slot<T>(slot_of(j + 3), L, y);
+        a_and_p(j + 1, At);
+        __syncthreads();
+        tri_inverse(At);
+      }
+      wait_or_abort(bar + 1, j & 1, abort, status);
+      tc::fence_after_sync();
+      readout(j, TI_W, TI_U);
       tc::fence_before_sync();
       __syncthreads();
       tc::fence_after_sync();
+      if (j + 1 < r) {
+        // the D2 operands of V-head j + 1 (VT and B2 were read by the MMAs just completed)
+        put_row8(vt, vt + 16384, y);
+        t_to_b2(At, vecs + (j + 1) * 320 + 256, vecs + (j + 1) * 320 + 64, b2, b2 + 16384);
+        sync_operands();
+      }
     }
   }
   if (warp == 1) tc::tmem_dealloc(tb, TI_COLS);
