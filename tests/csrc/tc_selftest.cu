@@ -282,6 +282,67 @@ extern "C" int tc_gemm_tast(const float* A, const float* B, float* D, int N, int
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
 }
 
+// Issue cost of back-to-back MMAs: nmma M = 128, K = 16 bf16 MMAs into one accumulator (the K
+// steps of a 128 x 128 A tile in turn), A from shared memory or from TMEM, then one commit and
+// its wait; the smallest clock64 span over `reps` repetitions after the first.  The operands
+// hold arbitrary bits: only the time is of interest.
+__global__ void mma_cost_kernel(int N, int tmem_a, int nmma, int reps, long long* out, int* err) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  unsigned char* a = sm;             // 128 x 128 bf16
+  unsigned char* b = sm + 32768;     // up to 256 x 128 bf16
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 32768 + 65536);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+  for (int i = threadIdx.x; i < (32768 + 65536) / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t*>(sm)[i] = 0x3f803f80u;   // bf16 1.0 pairs
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (threadIdx.x < 32) tmem_alloc(slot, 512);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tb = *slot;
+  if (threadIdx.x == 0) {
+    const uint32_t id = idesc_bf16(128, N);
+    const uint64_t da = kstep_desc(smem_u32(a), 128, 0), db = kstep_desc(smem_u32(b), 128, 0);
+    const uint32_t ta = tb + 256;   // A in TMEM: 8 columns per K-step, columns 256 .. 319
+    long long best = 1LL << 62;
+    for (int r = 0; r < reps; ++r) {
+      const long long t0 = clock64();
+      for (int i = 0; i < nmma; ++i) {
+        const int k = i & 7;
+        if (tmem_a) mma_bf16_ta(tb, ta + 8 * k, desc_add(db, 256 * k), id, i > 0);
+        else mma_bf16(tb, desc_add(da, 256 * k), desc_add(db, 256 * k), id, i > 0);
+      }
+      mma_commit(bar);
+      if (!mbar_wait(bar, (uint32_t)(r & 1))) {
+        atomicOr(err, 1);
+        break;
+      }
+      const long long t1 = clock64();
+      if (r > 0 && t1 - t0 < best) best = t1 - t0;
+    }
+    *out = best;
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x < 32) tmem_dealloc(tb, 512);
+}
+
+extern "C" int tc_mma_cost(int N, int tmem_a, int nmma, long long* out, int* err) {
+  if (N < 16 || N > 256 || N % 16 || nmma < 1) return -1;
+  const size_t smem = 32768 + 65536 + 64;
+  if (cudaFuncSetAttribute(mma_cost_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return -2;
+  mma_cost_kernel<<<1, 128, smem>>>(N, tmem_a, nmma, 20, out, err);
+  if (cudaGetLastError() != cudaSuccess) return -3;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
+}
+
 extern "C" int tc_gemm(const float* A, const float* B, float* D, int N, int K, int passes, int* err) {
   return tc_gemm_p(A, B, D, N, K, passes, 128, err);
 }

@@ -37,6 +37,8 @@ def lib():
     l.tc_gemm_tast.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
     l.tc_gemm_mnb.restype = ctypes.c_int
     l.tc_gemm_mnb.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 + [ctypes.c_void_p]
+    l.tc_mma_cost.restype = ctypes.c_int
+    l.tc_mma_cost.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
     l.tc_cluster_xchg.restype = ctypes.c_int
     l.tc_cluster_xchg.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
     return l
@@ -152,6 +154,27 @@ def test_tc_gemm_mn_major_b(lib, N, K):
     assert int(err.item()) == 0
     e3 = np.max(np.abs(D.cpu().numpy() - ref)) / np.max(np.abs(ref))
     assert e3 < 2e-5, e3
+
+
+def test_mma_issue_cost(lib):
+    """Cycles per MMA (M = 128, K = 16, bf16) over 24 back-to-back MMAs, A in shared memory or
+    in TMEM, N = 64 / 128 / 256 (printed with -s; the prefill chain kernel keeps its A operands in
+    TMEM because of this).  Checked: every run completes and the figures are sane."""
+    out = torch.zeros(1, dtype=torch.int64, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rows = []
+    for tmem_a in (0, 1):
+        for N in (64, 128, 256):
+            spans = []
+            for nmma in (8, 24):
+                assert lib.tc_mma_cost(N, tmem_a, nmma, out.data_ptr(), err.data_ptr()) == 0
+                assert int(err.item()) == 0
+                spans.append(int(out.item()))
+            per = (spans[1] - spans[0]) / 16.0   # the marginal cost of one more MMA
+            rows.append(("tmem" if tmem_a else "smem", N, per))
+            assert 10.0 < per < 2000.0, (tmem_a, N, per)
+    for where, N, per in rows:
+        print(f"A in {where}: N = {N:3d}: {per:6.1f} cycles per MMA")
 
 
 def test_cluster_exchange(lib):
