@@ -82,19 +82,27 @@ __device__ __forceinline__ void gst_unit(unsigned char* g, uint32_t off, const u
   *reinterpret_cast<uint4*>(g + off) = v;
 }
 
-// Warp-wide: global chunk -> (sequence, first token, length); false if cu_seqlens is invalid.
-__device__ bool find_chunk(const int32_t* __restrict__ cu, int num_seqs, int total, int c, int& seq,
-                           int& t0, int& len, int& seq_start) {
+// Warp-wide: global chunk -> (sequence, first token, length, the sequence's start and length, its
+// slot and has_initial_state flag); false if cu_seqlens is invalid.  Each lane loads its
+// sequence's slot and flag beside its cu_seqlens entries, so the lookup costs one round trip.
+struct ChunkInfo {
+  int seq, t0, len, seq_start, seq_len, slot, init;
+};
+__device__ bool find_chunk(const int32_t* __restrict__ cu, const int32_t* __restrict__ slot_idx,
+                           const uint8_t* __restrict__ has_init, int num_seqs, int total, int c,
+                           ChunkInfo& ci) {
   const int lane = threadIdx.x & 31;
   bool ok = (__ldg(cu) == 0) && (__ldg(cu + num_seqs) == total);
   int base = 0;
-  seq = -1;
+  ci.seq = -1;
   for (int n0 = 0; n0 < num_seqs; n0 += 32) {
     const int n = n0 + lane;
-    int lo = 0, hi = 0, nch = 0;
+    int lo = 0, hi = 0, nch = 0, sl = -1, hinit = 0;
     if (n < num_seqs) {
       lo = __ldg(cu + n);
       hi = __ldg(cu + n + 1);
+      sl = __ldg(slot_idx + n);
+      hinit = has_init != nullptr ? (int)__ldg(has_init + n) : 0;
       if (hi < lo) ok = false;
       else nch = (hi - lo + CH - 1) / CH;
     }
@@ -106,14 +114,17 @@ __device__ bool find_chunk(const int32_t* __restrict__ cu, int num_seqs, int tot
     }
     const bool mine = (n < num_seqs) && (c >= base + incl - nch) && (c < base + incl);
     const unsigned m = __ballot_sync(0xffffffffu, mine);
-    if (m && seq < 0) {
+    if (m && ci.seq < 0) {
       const int src = __ffs(m) - 1;
-      seq = __shfl_sync(0xffffffffu, n, src);
-      seq_start = __shfl_sync(0xffffffffu, lo, src);
+      ci.seq = __shfl_sync(0xffffffffu, n, src);
+      ci.seq_start = __shfl_sync(0xffffffffu, lo, src);
       const int hi_s = __shfl_sync(0xffffffffu, hi, src);
       const int ex = __shfl_sync(0xffffffffu, base + incl - nch, src);
-      t0 = seq_start + (c - ex) * CH;
-      len = min(CH, hi_s - t0);
+      ci.slot = __shfl_sync(0xffffffffu, sl, src);
+      ci.init = __shfl_sync(0xffffffffu, hinit, src);
+      ci.seq_len = hi_s - ci.seq_start;
+      ci.t0 = ci.seq_start + (c - ex) * CH;
+      ci.len = min(CH, hi_s - ci.t0);
     }
     base += __shfl_sync(0xffffffffu, incl, 31);
   }
@@ -540,22 +551,24 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   float* part = reinterpret_cast<float*>(sm + S::PART);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S::BAR);   // [0] D1, [1] D2
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
-  int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);   // ok, t0, L, seq, seq_start, abort
+  int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);   // ok, t0, L, seq_len, seq_start, abort, slot, init
 
   const int c = cw0 + blockIdx.x, kh = blockIdx.y;   // global chunk index; records from cw0
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = d.r, h0 = kh * r;
   if (warp == 0) {
-    int seq, t0 = 0, len = 0, ss = 0;
-    const bool ok = find_chunk(cu, num_seqs, total, c, seq, t0, len, ss);
+    ChunkInfo ci = {-1, 0, 0, 0, 0, -1, 0};
+    const bool ok = find_chunk(cu, slot_idx, has_init, num_seqs, total, c, ci);
     if (lane == 0 && !ok && c == 0 && kh == 0) set_status(status, GDN_STATUS_BAD_SEQLENS);
     if (lane == 0) {
-      sh[0] = ok && seq >= 0;
-      sh[1] = t0;
-      sh[2] = len;
-      sh[3] = seq;
-      sh[4] = ss;
+      sh[0] = ok && ci.seq >= 0;
+      sh[1] = ci.t0;
+      sh[2] = ci.len;
+      sh[3] = ci.seq_len;
+      sh[4] = ci.seq_start;
       sh[5] = 0;
+      sh[6] = ci.slot;
+      sh[7] = ci.init;
     }
   }
   __syncthreads();
@@ -563,12 +576,11 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     tc::pdl_wait_primary();   // no CTA of a pipelined window completes before the previous chains
     return;
   }
-  const int t0 = sh[1], L = sh[2], seq = sh[3], seq_start = sh[4];
-  const int seq_len = __ldg(cu + seq + 1) - seq_start;
+  const int t0 = sh[1], L = sh[2], seq_len = sh[3], seq_start = sh[4];
   volatile int* abort = sh + 5;
-  const int s = __ldg(slot_idx + seq);
+  const int s = sh[6];
   const bool valid = s >= 0 && s < num_slots;
-  const bool init = valid && has_init != nullptr && __ldg(has_init + seq) != 0;
+  const bool init = valid && sh[7] != 0;
   const T* cs = conv_state + (size_t)(valid ? s : 0) * 3 * d.cqkv;
   auto rec_of = [&](int j) {
     return reinterpret_cast<unsigned char*>(ws) + ((size_t)(rec_base + c - cw0) * d.Hv + h0 + j) * REC_BYTES;
