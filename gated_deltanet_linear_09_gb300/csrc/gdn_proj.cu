@@ -32,24 +32,42 @@ namespace {
 
 constexpr int PM = 128;         // output features per weight tile (MMA M, TMEM lanes)
 constexpr int PT = 2;           // weight tiles per CTA: 256 features share one activation tile
-constexpr int PN = 64;          // activation rows per CTA (MMA N, TMEM columns per tile)
 constexpr int PK = 64;          // contraction elements per stage
-constexpr int PSTAGES = 5;      // ring depth (200 KiB: one CTA per SM)
-constexpr int PLAG = 1;         // a stage is refilled PLAG chunks after its MMAs were issued ...
-constexpr int PDIST = PSTAGES - PLAG;   // ... so PDIST chunks are in flight
+constexpr int PLAG = 1;         // a stage is refilled PLAG chunks after its MMAs were issued
 constexpr int PTHREADS = 256;
 constexpr uint32_t PA_BYTES = PM * PK * 2;   // one weight tile, 16 KiB
-constexpr uint32_t PB_BYTES = PN * PK * 2;   // activation tile, 8 KiB
-constexpr uint32_t PSTAGE_BYTES = PT * PA_BYTES + PB_BYTES;
-constexpr uint32_t PRED_BYTES = PT * PM * PN * 4;  // f32 partial tiles [PT][PN][PM] (stages)
-constexpr uint32_t PBAR_OFF = PSTAGES * PSTAGE_BYTES;
-constexpr uint32_t PSMEM = PBAR_OFF + PSTAGES * 8 + 16;
-constexpr int PX_COPIES = PN * (PK / 8) / PTHREADS;   // 16-byte activation copies per thread
-constexpr int PW_UNITS = PA_BYTES / 16 / PTHREADS;    // 16-byte weight copies per thread
-static_assert(PRED_BYTES <= PBAR_OFF, "partial tile must fit in the stage ring");
-static_assert(PX_COPIES * PTHREADS == PN * (PK / 8), "copies must divide evenly over the threads");
+constexpr int PROWS_WIDE = 256;   // activation rows per CTA of the wide form
+constexpr int WIDE_MIN_ROWS = 512;  // row counts from which an unsplit launch takes the wide form
 static_assert(PA_BYTES == GDN_PROJ_BLOCK_BYTES, "a packed block is one weight tile's stage");
-static_assert(PTHREADS == PT * PM, "the reduction maps one thread to one output feature");
+static_assert(PTHREADS == PT * PM, "the epilogue maps one thread to one output feature");
+
+// Two forms of the kernel, by activation rows per CTA (the MMA's N, TMEM columns per tile):
+//   PN = 64: decode batches; the weight bytes dominate; a 5-stage ring; the contraction can be
+//     split over a cluster and reduced through distributed shared memory;
+//   PN = 256: prefill-sized row counts; one N = 256 MMA costs ~160 cycles against ~109 for an
+//     N = 64 one, so four times the rows per instruction run the tensor pipe faster and each
+//     stage's bytes serve four times the FLOPs; 3 stages of 64 KiB; no split (there are tiles
+//     enough for every SM).  (Six stages of 32 elements ran slower: the stage fill, not its
+//     latency, is the limit.)
+template <int PN_>
+struct ProjCfg {
+  static constexpr int PN = PN_;
+  static constexpr int KS = 64;   // contraction elements per stage (32 is supported too)
+  static constexpr int STAGES = PN_ == 64 ? 5 : 3;
+  static constexpr int DIST = STAGES - PLAG;   // chunks in flight
+  static constexpr uint32_t A_BYTES = PM * KS * 2;   // one weight tile's part of a stage
+  static constexpr uint32_t B_BYTES = PN * KS * 2;   // activation tile
+  static constexpr uint32_t STAGE_BYTES = PT * A_BYTES + B_BYTES;
+  static constexpr uint32_t BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr uint32_t SMEM = BAR_OFF + STAGES * 8 + 16;
+  static constexpr uint32_t RED_BYTES = PT * PM * PN * 4;   // f32 partial tiles (split only)
+  static_assert(PN_ != 64 || RED_BYTES <= BAR_OFF, "partial tile must fit in the stage ring");
+  static constexpr int X_COPIES = PN * (KS / 8) / PTHREADS;   // 16-byte activation copies
+  static constexpr int W_UNITS = A_BYTES / 16 / PTHREADS;     // 16-byte weight copies per tile
+  static_assert(X_COPIES * PTHREADS == PN * (KS / 8), "copies must divide evenly over the threads");
+  static_assert(SMEM <= 227 * 1024, "one CTA per SM");
+  static_assert(PT * PN <= 512, "both accumulators fit TMEM");
+};
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(saddr), "l"(g),
@@ -74,13 +92,15 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
 // Copy u covers row 8*(u/64) + u%8, elements 8*((u/8)%8) .. +8, which is byte u*16 of the tile:
 // consecutive threads fill consecutive 16-byte slots (no shared-memory bank conflicts).  Rows past
 // M are zero-filled (source size 0, address kept in range).
+template <int PN>
 __device__ __forceinline__ void load_x(uint32_t sb, const __nv_bfloat16* __restrict__ X, int M,
                                        int K, int m0, int k0) {
+  constexpr int KG = ProjCfg<PN>::KS / 8;   // 16-byte units per row of the stage
 #pragma unroll
-  for (int i = 0; i < PX_COPIES; ++i) {
+  for (int i = 0; i < ProjCfg<PN>::X_COPIES; ++i) {
     const int u = (int)threadIdx.x + i * PTHREADS;
-    const int m = m0 + (((u >> 6) << 3) | (u & 7));
-    const __nv_bfloat16* src = X + (size_t)min(m, M - 1) * K + k0 + 8 * ((u >> 3) & 7);
+    const int m = m0 + ((u / (8 * KG)) << 3 | (u & 7));
+    const __nv_bfloat16* src = X + (size_t)min(m, M - 1) * K + k0 + 8 * ((u >> 3) % KG);
     cp_async16(sb + (uint32_t)u * 16u, src, m < M ? 16u : 0u);
   }
 }
@@ -104,24 +124,37 @@ __global__ void proj_pack_kernel(const __nv_bfloat16* __restrict__ W, int N, int
   }
 }
 
-// One pipeline stage: block c of each of this CTA's weight tiles (contiguous 16 KiB copies: 256
-// threads x 4 x 16 bytes, every warp reading 512 consecutive bytes; a second tile past the end
-// of the packed weight is skipped) and the matching activation tile.
+// One pipeline stage: chunk c of each of this CTA's weight tiles and the matching activation
+// tile.  With 64-element stages chunk c is packed block c (a contiguous 16 KiB copy: 256 threads
+// x 4 x 16 bytes, every warp reading 512 consecutive bytes); with 32-element stages it is half h
+// = c % 2 of block c / 2, gathered into the stage's own 32-element K-major layout (unit u of the
+// half: 8-row group u / 32, 16-byte column u / 8 % 4, row u % 8).  A second tile past the end of
+// the packed weight is skipped.
+template <int PN>
 __device__ __forceinline__ void load_chunk(uint32_t sa, const unsigned char* __restrict__ wblk,
                                            size_t tile_stride, int ntiles,
                                            const __nv_bfloat16* __restrict__ X, int M, int K,
                                            int m0, int kbase, int c) {
+  using C = ProjCfg<PN>;
 #pragma unroll
   for (int t = 0; t < PT; ++t) {
     if (t < ntiles) {
 #pragma unroll
-      for (int i = 0; i < PW_UNITS; ++i) {
-        const uint32_t o = (threadIdx.x + i * PTHREADS) * 16u;
-        cp_async16(sa + t * PA_BYTES + o, wblk + t * tile_stride + (size_t)c * PA_BYTES + o, 16u);
+      for (int i = 0; i < C::W_UNITS; ++i) {
+        const uint32_t u = threadIdx.x + i * PTHREADS;
+        size_t src;
+        if constexpr (C::KS == PK) {
+          src = (size_t)c * PA_BYTES + u * 16u;
+        } else {
+          const uint32_t half = (uint32_t)c & 1u;
+          src = (size_t)(c >> 1) * PA_BYTES +
+                (((u >> 5) * 8u + half * 4u + ((u >> 3) & 3u)) * 128u + (u & 7u) * 16u);
+        }
+        cp_async16(sa + t * C::A_BYTES + u * 16u, wblk + t * tile_stride + src, 16u);
       }
     }
   }
-  load_x(sa + PT * PA_BYTES, X, M, K, m0, kbase + c * PK);
+  load_x<PN>(sa + PT * C::A_BYTES, X, M, K, m0, kbase + c * C::KS);
 }
 
 // Grid (ceil(N/(PT*PM)), ceil(M/PN), ks), cluster (1, 1, ks): CTA z of a cluster takes contraction
@@ -131,19 +164,23 @@ __device__ __forceinline__ void load_chunk(uint32_t sa, const unsigned char* __r
 // each stage; thread 0 issues the MMAs.  The CTAs of one launch walk their chunks from different
 // starting points (a rotation by feature tile), so that they do not all read the same
 // activation lines from L2 at the same moment.
+template <int PN>
 __global__ void __launch_bounds__(PTHREADS, 1)
 proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict__ WP, int M,
             int N, int K, int nkc, const ProjRoute route, int32_t* __restrict__ status) {
+  using C = ProjCfg<PN>;
+  constexpr int PSTAGES = C::STAGES, PDIST = C::DIST;
+  constexpr uint32_t PSTAGE_BYTES = C::STAGE_BYTES, PBAR_OFF = C::BAR_OFF;
   extern __shared__ __align__(1024) unsigned char sm[];
   uint64_t* done = reinterpret_cast<uint64_t*>(sm + PBAR_OFF);   // the stage's MMAs completed
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + PSTAGES);
   const int n0 = blockIdx.x * PT * PM, m0 = blockIdx.y * PN;
   const int ks = (int)gridDim.z, z = (int)blockIdx.z;
-  const int kbase = z * nkc * PK;
+  const int kbase = z * nkc * C::KS;
   const int nt0 = blockIdx.x * PT, ntot = (N + PM - 1) / PM;
   const int ntiles = min(PT, ntot - nt0);   // weight tiles this CTA holds (the last may hold 1)
   const size_t tile_stride = (size_t)(K / PK) * PA_BYTES;
-  const unsigned char* wblk = WP + (size_t)nt0 * tile_stride + (size_t)z * nkc * PA_BYTES;
+  const unsigned char* wblk = WP + (size_t)nt0 * tile_stride + (size_t)z * nkc * C::A_BYTES;
   const int rot = (int)(((unsigned long long)blockIdx.x * nkc / gridDim.x + blockIdx.y * 7ull) %
                         (unsigned)nkc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -164,7 +201,7 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
 #pragma unroll
   for (int j = 0; j < PDIST; ++j) {
     if (j < nkc)
-      load_chunk(s0 + j * PSTAGE_BYTES, wblk, tile_stride, ntiles, X, M, K, m0, kbase, chunk(j));
+      load_chunk<PN>(s0 + j * PSTAGE_BYTES, wblk, tile_stride, ntiles, X, M, K, m0, kbase, chunk(j));
     cp_async_commit();
   }
   constexpr uint32_t kIdesc = tc::idesc_bf16(PM, PN);
@@ -177,13 +214,13 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
     if (tid == 0 && ok) {
       tc::fence_after_sync();
       const uint32_t sa = s0 + st * PSTAGE_BYTES;
-      const uint64_t db = tc::kstep_desc(sa + PT * PA_BYTES, PK, 0);
+      const uint64_t db = tc::kstep_desc(sa + PT * C::A_BYTES, C::KS, 0);
 #pragma unroll
       for (int t = 0; t < PT; ++t) {
         if (t < ntiles) {
-          const uint64_t da = tc::kstep_desc(sa + t * PA_BYTES, PK, 0);
+          const uint64_t da = tc::kstep_desc(sa + t * C::A_BYTES, C::KS, 0);
 #pragma unroll
-          for (int k = 0; k < PK / 16; ++k)
+          for (int k = 0; k < C::KS / 16; ++k)
             tc::mma_bf16(tb + t * PN, tc::desc_add(da, 256u * k), tc::desc_add(db, 256u * k),
                          kIdesc, (kc > 0 || k > 0) ? 1u : 0u);
         }
@@ -198,8 +235,8 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
       if (prev >= 0 && ok && !tc::mbar_wait(done + prev % PSTAGES, (prev / PSTAGES) & 1))
         ok = false;
       if (ok)
-        load_chunk(s0 + (nxt % PSTAGES) * PSTAGE_BYTES, wblk, tile_stride, ntiles, X, M, K, m0,
-                   kbase, chunk(nxt));
+        load_chunk<PN>(s0 + (nxt % PSTAGES) * PSTAGE_BYTES, wblk, tile_stride, ntiles, X, M, K, m0,
+                       kbase, chunk(nxt));
     }
     cp_async_commit();
   }
@@ -209,59 +246,90 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   ok = __syncthreads_and(ok) != 0;
   if (!ok && tid == 0 && status) atomicOr(status, GDN_STATUS_TIMEOUT);
   tc::fence_after_sync();
-  // the partial tiles, [tile][column][lane] f32, into this CTA's stage ring (free now): warp w
-  // holds TMEM lanes 32*(w%4).. of tile w/4 (columns 64*(w/4) ..)
-  float* red = reinterpret_cast<float*>(sm);
-  if (ok) {
+  // the destination of output feature n (thread -> TMEM lane of one tile)
+  auto route_of = [&](int n, size_t& ld) {
+    __nv_bfloat16* base = route.ptr[0];
+    int seg_start = 0, seg_ld = route.ld[0];
+#pragma unroll
+    for (int q = 1; q < GDN_MAX_PROJ_SEGMENTS; ++q)
+      if (q < route.nseg && n >= route.start[q]) {
+        base = route.ptr[q];
+        seg_start = route.start[q];
+        seg_ld = route.ld[q];
+      }
+    ld = (size_t)seg_ld;
+    return base + (n - seg_start);
+  };
+  if constexpr (PN == PROWS_WIDE) {
+    // wide form: warp w reads TMEM lanes 32 (w % 4) .. of tile w / 4, 16 columns (rows) at a
+    // time, and writes them straight out: a warp stores 32 consecutive features of a row
     const int lq = (warp & 3) * 32, t = warp >> 2;
+    const int n = n0 + t * PM + lq + lane;
+    size_t ld;
+    __nv_bfloat16* dst = route_of(n, ld);
+    if (ok) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < PN; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(tc::taddr(tb, lq, t * PN + c0), v);
+        if (n < N) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float v[32];
-      tc::tmem_ld16(tc::taddr(tb, lq, t * PN + 32 * h), v);
-      tc::tmem_ld16(tc::taddr(tb, lq, t * PN + 32 * h + 16), v + 16);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) red[(t * PN + 32 * h + i) * PM + lq + lane] = v[i];
+          for (int i = 0; i < 16; ++i) {
+            const int m = m0 + c0 + i;
+            if (m < M) dst[(size_t)m * ld] = __float2bfloat16_rn(v[i]);
+          }
+        }
+      }
     }
-  }
-  const bool clustered = ks > 1;
-  tc::fence_before_sync();
-  if (clustered)
-    tc::cluster_sync_all();   // every partial tile of the cluster is written and visible
-  else
+    tc::fence_before_sync();
     __syncthreads();
-  tc::fence_after_sync();
-  if (warp == 0) tc::tmem_dealloc(tb, PT * PN);
-  // this CTA's column slice: thread -> lane r = tid % 128 of tile tid / 128, every column
-  const int r = tid & (PM - 1), tt = tid >> 7;
-  const int n = n0 + tt * PM + r;
-  const int cw0 = z * PN / ks, cw1 = (z + 1) * PN / ks;
-  __nv_bfloat16* base = route.ptr[0];
-  int seg_start = 0, seg_ld = route.ld[0];
+    if (warp == 0) tc::tmem_dealloc(tb, PT * PN);
+  } else {
+    // the partial tiles, [tile][column][lane] f32, into this CTA's stage ring (free now): warp w
+    // holds TMEM lanes 32*(w%4).. of tile w/4 (columns 64*(w/4) ..)
+    float* red = reinterpret_cast<float*>(sm);
+    if (ok) {
+      const int lq = (warp & 3) * 32, t = warp >> 2;
 #pragma unroll
-  for (int q = 1; q < GDN_MAX_PROJ_SEGMENTS; ++q)
-    if (q < route.nseg && n >= route.start[q]) {
-      base = route.ptr[q];
-      seg_start = route.start[q];
-      seg_ld = route.ld[q];
+      for (int h = 0; h < 2; ++h) {
+        float v[32];
+        tc::tmem_ld16(tc::taddr(tb, lq, t * PN + 32 * h), v);
+        tc::tmem_ld16(tc::taddr(tb, lq, t * PN + 32 * h + 16), v + 16);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) red[(t * PN + 32 * h + i) * PM + lq + lane] = v[i];
+      }
     }
-  __nv_bfloat16* dst = base + (n - seg_start);
-  const size_t ld = (size_t)seg_ld;
-  const uint32_t red_s = tc::smem_u32(red);
-  for (int c = cw0; c < cw1; ++c) {
-    const int m = m0 + c;
-    if (m >= M || n >= N) continue;
-    const int e = (tt * PN + c) * PM + r;
-    float s;
-    if (clustered) {
-      s = 0.f;
-      const uint32_t off = red_s + (uint32_t)e * 4u;
-      for (int q = 0; q < ks; ++q) s += ld_cluster_f32(tc::mapa_shared(off, (uint32_t)q));
-    } else {
-      s = red[e];
+    const bool clustered = ks > 1;
+    tc::fence_before_sync();
+    if (clustered)
+      tc::cluster_sync_all();   // every partial tile of the cluster is written and visible
+    else
+      __syncthreads();
+    tc::fence_after_sync();
+    if (warp == 0) tc::tmem_dealloc(tb, PT * PN);
+    // this CTA's column slice: thread -> lane r = tid % 128 of tile tid / 128, every column
+    const int r = tid & (PM - 1), tt = tid >> 7;
+    const int n = n0 + tt * PM + r;
+    const int cw0 = z * PN / ks, cw1 = (z + 1) * PN / ks;
+    size_t ld;
+    __nv_bfloat16* dst = route_of(n, ld);
+    const uint32_t red_s = tc::smem_u32(red);
+    for (int c = cw0; c < cw1; ++c) {
+      const int m = m0 + c;
+      if (m >= M || n >= N) continue;
+      const int e = (tt * PN + c) * PM + r;
+      float s;
+      if (clustered) {
+        s = 0.f;
+        const uint32_t off = red_s + (uint32_t)e * 4u;
+        for (int q = 0; q < ks; ++q) s += ld_cluster_f32(tc::mapa_shared(off, (uint32_t)q));
+      } else {
+        s = red[e];
+      }
+      dst[(size_t)m * ld] = __float2bfloat16_rn(s);
     }
-    dst[(size_t)m * ld] = __float2bfloat16_rn(s);
+    if (clustered) tc::cluster_sync_all();   // no CTA leaves while another reads its memory
   }
-  if (clustered) tc::cluster_sync_all();   // no CTA leaves while another reads its memory
 }
 
 int g_num_sms = 0;
@@ -280,11 +348,12 @@ int proj_auto_split(int M, int N, int K) {
   });
   // one CTA per SM: split the contraction while the grid still fits in one wave and every CTA
   // keeps at least a full ring of chunks
+  constexpr int PN = ProjCfg<64>::PN;
   const long long tiles = (long long)((N + PT * PM - 1) / (PT * PM)) * ((M + PN - 1) / PN);
   const int nk = K / PK;
   int ks = 1;
   for (int c = 2; c <= 8; ++c)
-    if (tiles * c <= (long long)g_num_sms && nk % c == 0 && nk / c >= PSTAGES) ks = c;
+    if (tiles * c <= (long long)g_num_sms && nk % c == 0 && nk / c >= ProjCfg<64>::STAGES) ks = c;
   return ks;
 }
 
@@ -305,15 +374,22 @@ int launch_proj(const void* x, const void* wp, int M, int N, int K, int ks, cons
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)PSMEM);
+    attr_err = cudaFuncSetAttribute(proj_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)ProjCfg<64>::SMEM);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(proj_kernel<PROWS_WIDE>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)ProjCfg<PROWS_WIDE>::SMEM);
   });
   if (attr_err != cudaSuccess) return GDN_ERR_CUDA;
+  // unsplit launches over many rows take the wide form
+  const bool wide = ks == 1 && M >= WIDE_MIN_ROWS;
+  const int pn = wide ? PROWS_WIDE : ProjCfg<64>::PN;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((N + PT * PM - 1) / (PT * PM)), (unsigned)((M + PN - 1) / PN),
+  cfg.gridDim = dim3((unsigned)((N + PT * PM - 1) / (PT * PM)), (unsigned)((M + pn - 1) / pn),
                      (unsigned)ks);
   cfg.blockDim = dim3(PTHREADS, 1, 1);
-  cfg.dynamicSmemBytes = PSMEM;
+  cfg.dynamicSmemBytes = wide ? ProjCfg<PROWS_WIDE>::SMEM : ProjCfg<64>::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -322,10 +398,12 @@ int launch_proj(const void* x, const void* wp, int M, int N, int K, int ks, cons
   attr[0].val.clusterDim.z = (unsigned)ks;
   cfg.attrs = attr;
   cfg.numAttrs = ks > 1 ? 1 : 0;   // no cluster without a split: nothing to exchange
-  const int nkc = K / PK / ks;
+  const int nkc = K / (wide ? ProjCfg<PROWS_WIDE>::KS : PK) / ks;
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  const unsigned char* wb = static_cast<const unsigned char*>(wp);
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, proj_kernel, static_cast<const __nv_bfloat16*>(x),
-                         static_cast<const unsigned char*>(wp), M, N, K, nkc, route, status);
+      wide ? cudaLaunchKernelEx(&cfg, proj_kernel<PROWS_WIDE>, xb, wb, M, N, K, nkc, route, status)
+           : cudaLaunchKernelEx(&cfg, proj_kernel<64>, xb, wb, M, N, K, nkc, route, status);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -47,6 +47,9 @@ def _operands(M, N, K, seed):
     (130, 129, 512, 8),       # 3 row tiles, split over a cluster of 8
     (70, 250, 384, 3),        # a cluster of 3: column slices of 21, 21 and 22
     (200, 1000, 2048, 0),
+    (512, 300, 256, 0),       # from 512 unsplit rows on: the 256-row tile form
+    (700, 385, 512, 1),       # ragged rows (2 full row tiles + 188) and a 1-feature last tile
+    (1000, 129, 2048, 0),
 ])
 def test_linear_matches_oracle(M, N, K, ks):
     x, w = _operands(M, N, K, 900 + M)
@@ -109,6 +112,28 @@ def test_linear_is_deterministic_and_splits_agree():
         if ks in outs:
             np.testing.assert_array_equal(g, outs[ks])
         outs[ks] = g
+
+
+def test_wide_form_routes_and_repeats():
+    """The 256-row tile form (600 rows, unsplit): three destinations with row strides above
+    their widths, padding columns untouched, and the same call twice bitwise equal."""
+    M, N, K = 600, 520, 320
+    x, w = _operands(M, N, K, 930)
+    xd, wd = _bf16_dev(x), _packed(w)
+    ref = oracle.linear(x, w)
+    outs = []
+    for _ in range(2):
+        a = torch.full((M, 300), 3.0, dtype=torch.bfloat16, device="cuda")
+        b = torch.full((M, 220), 3.0, dtype=torch.bfloat16, device="cuda")
+        c = torch.full((M, 20), 3.0, dtype=torch.bfloat16, device="cuda")
+        route = gdn.make_route([(0, 300, a), (290, 220, b), (500, 20, c)])
+        gdn.gdn_linear_bf16(xd, wd, N, route, 0)
+        torch.cuda.synchronize()
+        got = np.concatenate([_np(a)[:, :290], _np(b)[:, :210], _np(c)], axis=1)
+        assert_out_close(got, ref, synth.BF16, "wide routed")
+        assert torch.all(a[:, 290:] == 3.0) and torch.all(b[:, 210:] == 3.0)
+        outs.append(got)
+    np.testing.assert_array_equal(outs[0], outs[1])
 
 
 def test_linear_empty_batch_is_a_noop():
