@@ -537,7 +537,8 @@ def time_proj(torch, gdn, synth, GatedDeltaNetLayer, hbm_peak, bf16_peak, reps=2
                               "tflops": round(tf, 1), "bf16_frac": round(tf / bf16_peak, 4)}
     res["hidden_sizes"] = {str(k): v for k, v in synth.PROJ_HIDDEN.items()}
     res["kernel"] = ("proj_kernel: 256 features x 64 rows per CTA (two tcgen05 M=128 x N=64 "
-                     "accumulators), packed weight blocks, cp.async ring, cluster split-K")
+                     "accumulators), packed weight blocks, cp.async ring, cluster split-K; from "
+                     "512 unsplit rows 256 features x 256 rows (N=256 accumulators)")
     return res
 
 
