@@ -433,8 +433,8 @@ extern "C" int tc_gemm_mnb(const float* A, const float* Bt, float* D, int N, int
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : -4;
 }
 
-// Per-round exchange of one float per thread among the 4 CTAs of a cluster, the way the prefill
-// state kernel shares per-token partial sums of squares: every thread stores its value into slot
+// Per-round exchange of one float per thread among the 4 CTAs of a cluster (per-token partial
+// sums shared over distributed shared memory): every thread stores its value into slot
 // [round & 1][own rank][thread] of all four CTAs with st.async (completing bytes on that CTA's
 // mbarrier for the buffer), then waits for its own CTA's buffer to fill and sums the 4 slots.
 // Thread 0 posts the expected byte count of round r + 1 before it sends round r.

@@ -74,8 +74,8 @@ def test_tc_gemm(lib, N, K):
 
 @pytest.mark.parametrize("N,K", [(32, 128), (32, 64), (64, 64)])
 def test_tc_gemm_padded_b(lib, N, K):
-    """B operand with its K-direction core matrices 144 bytes apart (the layout the prefill
-    state kernel writes with conflict-free 2-byte stores)."""
+    """B operand with its K-direction core matrices 144 bytes apart (a padded layout in which a
+    warp stores 2-byte elements without bank conflicts)."""
     rng = np.random.default_rng(N * 7 + K)
     A = rng.standard_normal((128, K)).astype(np.float32)
     B = rng.standard_normal((N, K)).astype(np.float32)
