@@ -390,6 +390,16 @@ def run_ours(args, ws, rank, local):
     flops = T * (Hv * (8 * C * d + 6 * d * d) + Hk * 4 * C * d)
     p_tflops = flops / (p_ms * 1e-3) / 1e12
     p_bytes = T * (pgeo.cqkv * 2 + pgeo.zdim * 2 * 2 + 2 * Hv * 2) + Hv * d * d * 4
+    # launches of one call: the library pipelines windows of chunks, the first a wave of intra
+    # CTAs (SMs // Hk chunks), the others the chunks whose intra CTAs fit beside the Hv chains
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    nch = (T + C - 1) // C
+    win = max(1, (nsm - Hv) // Hk)
+    win0 = max(win, nsm // Hk)
+    p_windows = 1 + max(0, -(-(nch - win0) // win))
+    # 64-dim heads take the CUDA-core chunkwise path: same sequence and head counts
+    g64 = synth.Geometry(Hk, Hv, 64, 64, 4, synth.BF16)
+    p64_ms, _ = time_prefill(torch, synth, GatedDeltaNetLayer, 5, 2, geo=g64)
 
     if rank != 0:
         if dist:
@@ -428,7 +438,11 @@ def run_ours(args, ws, rank, local):
                     "roofline": {"bound": "tensor", "achieved": round(p_tflops, 3),
                                  "peak": bf16_peak, "unit": "TFLOP/s",
                                  "frac": round(p_tflops / bf16_peak, 5), "peak_kind": peak_kind},
-                    "io_bytes": p_bytes, "launches_per_call": 2},
+                    "io_bytes": p_bytes, "windows_per_call": p_windows,
+                    "launches_per_call": 2 * p_windows},
+        "prefill_d64": {"workload": f"prefill_T{T}_Hk{Hk}_Hv{Hv}_d64_bf16",
+                        "path": "CUDA-core chunkwise kernels (head dims other than 128)",
+                        "ms": round(p64_ms, 4), "tokens_per_s": round(T / (p64_ms * 1e-3), 1)},
         "decode_multi": {"tokens_per_row": MULTI_T, "rows": wl.batch, "ms": round(multi_ms, 5),
                          "tokens_per_s": round(wl.batch * MULTI_T / (multi_ms * 1e-3), 1),
                          "state_gbs": round(state_bytes / (multi_ms * 1e-3) / 1e9, 1),
@@ -655,10 +669,11 @@ def time_mixed(torch, synth, GatedDeltaNetLayer):
             "total_ms": round(sum(ms.values()), 3), "status": status}
 
 
-def time_prefill(torch, synth, GatedDeltaNetLayer, reps, warmup):
-    """Average time of one chunked prefill of the T = 4096 sequence (inputs resident in HBM)."""
+def time_prefill(torch, synth, GatedDeltaNetLayer, reps, warmup, geo=None):
+    """Average time of one chunked prefill of the T = 4096 sequence (inputs resident in HBM), on
+    the workload's geometry or on `geo`."""
     pwl = synth.workloads()[PREFILL_WL]
-    pgeo = pwl.geo
+    pgeo = geo if geo is not None else pwl.geo
     player = GatedDeltaNetLayer(pgeo, synth.make_weights(pgeo, pwl.seed), pwl.num_slots)
     T = pwl.seq_lens[0]
     px = player.inputs(synth.make_token_inputs(pgeo, T, pwl.seed, 0))
