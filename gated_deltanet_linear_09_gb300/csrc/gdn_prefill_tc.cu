@@ -573,6 +573,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   }
   __syncthreads();
   if (!sh[0]) {
+    tc::pdl_launch_dependents();
     tc::pdl_wait_primary();   // no CTA of a pipelined window completes before the previous chains
     return;
   }
@@ -854,9 +855,12 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
     }
   }
   if (warp == 1) tc::tmem_dealloc(tb, TI_COLS);
-  // Launched as a programmatic dependent of the previous window's chain kernel, the CTA may have
-  // run beside it; it completes only after that kernel has, which orders this window's chain
-  // kernel after the previous one.  (A no-op for an ordinary launch.)
+  // The window's chain kernel (a programmatic dependent of this one) may be set up from here on;
+  // it reads nothing before this kernel has completed.  Launched as a programmatic dependent of
+  // the previous window's chain kernel, the CTA may have run beside it; it completes only after
+  // that kernel has, which orders this window's chain kernel after the previous one.  (Both are
+  // no-ops for an ordinary launch.)
+  tc::pdl_launch_dependents();
   tc::pdl_wait_primary();
 }
 
@@ -943,7 +947,6 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
                 int num_seqs, int total, const T* __restrict__ qkv, const T* __restrict__ z,
                 T* __restrict__ out, const float* __restrict__ ws, int cw0, int cw1, int rec_base,
                 int32_t* __restrict__ status) {
-  tc::pdl_launch_dependents();   // the next window's intra kernel may take the SMs left free
   extern __shared__ __align__(1024) unsigned char sm[];
   using S = ChainSmem;
   const float* ut_s = reinterpret_cast<const float*>(sm + S::UT);
@@ -984,8 +987,10 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   if (warp == 0) tc::tmem_alloc(tslot, TC_COLS);
   // Launched as a programmatic dependent of the window's intra kernel: everything above touches
   // only this CTA's own resources; the records, the slot's state and the rest come after the
-  // intra kernel (and with it the previous window's chains) has completed.
+  // intra kernel (and with it the previous window's chains) has completed.  Only then may the next
+  // window's intra kernel start: it writes the workspace half the previous window's chains read.
   tc::pdl_wait_primary();
+  tc::pdl_launch_dependents();   // the next window's intra kernel may take the SMs left free
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
