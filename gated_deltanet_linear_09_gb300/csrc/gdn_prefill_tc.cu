@@ -899,16 +899,21 @@ struct ChainSmem {
 };
 static_assert(ChainSmem::BYTES <= 227 * 1024, "chain kernel shared memory");
 
-// 16 consecutive dk values v of S^T row (TMEM lane) lb: the split-bf16 operand words and the
-// f32 copy scaled by eg (the next chunk's e^{gamma_L}).  No wait.
-__device__ __forceinline__ void put_s16(uint32_t lb, int f0, const float* v, float eg) {
-  uint32_t hw[8], lw[8], sw[16];
+// 16 consecutive dk values v of S^T row (TMEM lane) lb: the split-bf16 operand words of the
+// next D3^T products.  No wait.
+__device__ __forceinline__ void put_sop16(uint32_t lb, int f0, const float* v) {
+  uint32_t hw[8], lw[8];
 #pragma unroll
   for (int p = 0; p < 8; ++p) tc::split2_bf16(v[2 * p], v[2 * p + 1], hw[p], lw[p]);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) sw[i] = __float_as_uint(eg * v[i]);
   tc::tmem_st8w_nw(lb + TA_S + f0 / 2, hw);
   tc::tmem_st8w_nw(lb + TA_S + 64 + f0 / 2, lw);
+}
+// The same values scaled by eg (the next chunk's e^{gamma_L}) into the f32 copy that the next
+// U^T K~ products accumulate onto.  No wait.
+__device__ __forceinline__ void put_sscl16(uint32_t lb, int f0, const float* v, float eg) {
+  uint32_t sw[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) sw[i] = __float_as_uint(eg * v[i]);
   tc::tmem_st16w_nw(lb + TC_S + f0, sw);
 }
 
@@ -958,12 +963,13 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   uint64_t* b4empty = bars + 5;  // B4 read by the chunk's U^T products
   uint64_t* utfull = bars + 6;   // U~ landed
   uint64_t* utempty = bars + 7;  // U~ read by the main warps (8 arrivals)
-  uint64_t* sopf = bars + 8;     // S^T operand and the scaled S^T written (8 arrivals)
+  uint64_t* sopf = bars + 8;     // S^T operand written (8 arrivals)
   uint64_t* mma3 = bars + 9;     // D3^T complete
   uint64_t* uopf = bars + 10;    // U^T operand written (8 arrivals)
   uint64_t* sready = bars + 11;  // S^T += U^T K~ complete
   uint64_t* dfull = bars + 12;   // O^T complete in D3^T columns 0-63
   uint64_t* dempty = bars + 13;  // O^T read by the output warps (8 arrivals)
+  uint64_t* sscl = bars + 14;    // e^{gamma_L} S^T written for the chunk's U^T K~ (8 arrivals)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
   int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);
 
@@ -980,8 +986,8 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     }
   }
   if (tid == 0) {
-    for (int i = 0; i < 14; ++i)
-      tc::mbar_init(bars + i, (i == 7 || i == 8 || i == 10 || i == 13) ? 8 : 1);
+    for (int i = 0; i < 15; ++i)
+      tc::mbar_init(bars + i, (i == 7 || i == 8 || i == 10 || i == 13 || i == 14) ? 8 : 1);
     tc::mbar_fence_init();
   }
   if (warp == 0) tc::tmem_alloc(tslot, TC_COLS);
@@ -1035,7 +1041,7 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       for (int p = 0; p < 4; ++p) {
         const int f0 = 64 * hf + 16 * p;
         if (nch > 0) {
-          put_s16(lb, f0, v + 16 * p, eg0);
+          put_sop16(lb, f0, v + 16 * p);
         } else if (valid && !init) {   // an empty sequence without a state: the slot is reset
 #pragma unroll
           for (int i = 0; i < 16; ++i) Sg[(size_t)(f0 + i) * D + j] = 0.f;
@@ -1045,6 +1051,14 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(sopf);
+      if (nch > 0) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) put_sscl16(lb, 64 * hf + 16 * p, v + 16 * p, eg0);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sscl);
     }
 #pragma unroll 1
     for (int c = 0; c < nch; ++c) {
@@ -1078,24 +1092,28 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         mbar_arrive(uopf);
         mbar_arrive(utempty);
       }
-      // S^T of the next chunk = the accumulated e^{gamma_L} S^T + U^T K~: its operand and its
-      // copy scaled by the next e^{gamma_L}; after the last chunk, the final state to the slot
+      // S^T of the next chunk = the accumulated e^{gamma_L} S^T + U^T K~: first its operand (the
+      // next D3^T products wait for it), then its copy scaled by the next e^{gamma_L} (needed
+      // only by the next U^T K~); after the last chunk, the final state to the slot
       const bool ok2 = wait_or_abort(sready, par, abort, status);
       tc::fence_after_sync();
+      auto ld_s32 = [&](int f0, uint32_t* rv) {
+        tc::tmem_ld16_nw(lb + TC_S + f0, rv);
+        tc::tmem_ld16_nw(lb + TC_S + f0 + 16, rv + 16);
+        tc::tmem_wait_ld();
+        tc::reg_fence16(rv);
+        tc::reg_fence16(rv + 16);
+      };
       if (ok2) {
 #pragma unroll 1
         for (int hp = 0; hp < 2; ++hp) {
           const int f0 = 64 * hf + 32 * hp;
           uint32_t rv[32];
-          tc::tmem_ld16_nw(lb + TC_S + f0, rv);
-          tc::tmem_ld16_nw(lb + TC_S + f0 + 16, rv + 16);
-          tc::tmem_wait_ld();
-          tc::reg_fence16(rv);
-          tc::reg_fence16(rv + 16);
+          ld_s32(f0, rv);
           const float* v = reinterpret_cast<const float*>(rv);
           if (c + 1 < nch) {
-            put_s16(lb, f0, v, egn);
-            put_s16(lb, f0 + 16, v + 16, egn);
+            put_sop16(lb, f0, v);
+            put_sop16(lb, f0 + 16, v + 16);
           } else if (valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) Sg[(size_t)(f0 + i) * D + j] = v[i];
@@ -1105,7 +1123,24 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0 && c + 1 < nch) mbar_arrive(sopf);
+      if (c + 1 < nch) {
+        if (lane == 0) mbar_arrive(sopf);
+        if (ok2) {
+#pragma unroll 1
+          for (int hp = 0; hp < 2; ++hp) {
+            const int f0 = 64 * hf + 32 * hp;
+            uint32_t rv[32];
+            ld_s32(f0, rv);
+            const float* v = reinterpret_cast<const float*>(rv);
+            put_sscl16(lb, f0, v, egn);
+            put_sscl16(lb, f0 + 16, v + 16, egn);
+          }
+          tc::tmem_wait_st();
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sscl);
+      }
     }
   } else if (warp < 16) {
     // ================= output warps: warps 8-11 take the tokens [0, 32) of the chunk, 12-15 the
@@ -1251,7 +1286,8 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
           tc::mma_commit(mma3);
           tc::mma_commit(b3empty);
         }
-        if (wait_or_abort(uopf, par, abort, status) && wait_or_abort(b4full, par, abort, status)) {
+        if (wait_or_abort(uopf, par, abort, status) && wait_or_abort(b4full, par, abort, status) &&
+            wait_or_abort(sscl, par, abort, status)) {
           tc::fence_after_sync();
 #pragma unroll
           for (int k = 0; k < 4; ++k) {   // S^T += U^T K~, K = tokens
