@@ -1,5 +1,7 @@
 // gdn_prefill_tc.cu -- chunkwise prefill on the sm_103a tensor cores (tcgen05 + TMEM), for
-// head dims dk = dv = 128.
+// head dims 128 and, zero-padded to 128, 64 (a zero channel adds nothing to the norms, the
+// products or the state, so only the channel offsets, the state's strides, the output columns
+// and the RMSNorm's 1/dv see the real dims).
 //
 // Same chunk algebra as the CUDA-core path (UT transform of the gated delta rule; Yang et al.,
 // "Parallelizing Linear Transformers with the Delta Rule over Sequence Length", NeurIPS 2024,
@@ -221,23 +223,28 @@ __device__ __forceinline__ void cp_async_wait_pending(int n) {
   }
 }
 
-// Issues (one commit group) the copies of 128 input channels [cb, cb+128) of the chunk: ring row
-// m holds the raw input at position p0 - 3 + m of the sequence (p0 = the chunk's first position);
-// positions before the sequence come from the slot's conv state when init, else zero; positions
-// past the sequence are zero.  Then the channels' conv weights.
+// Issues (one commit group) the copies of the head's nreal (64 or 128) input channels [cb, cb +
+// nreal) of the chunk into the 128 channels of a ring slot (the rest zero: a 64-dim head runs as a
+// 128-dim one whose extra channels are zero): ring row m holds the raw input at position
+// p0 - 3 + m of the sequence (p0 = the chunk's first position); positions before the sequence
+// come from the slot's conv state when init, else zero; positions past the sequence are zero.
+// Then the channels' conv weights (zero for the extra channels).
 template <typename T>
 __device__ __forceinline__ void ring_issue(const KDims& d, const T* __restrict__ qkv,
                                            const T* __restrict__ conv_w, const T* __restrict__ cs,
-                                           bool init, int cb, int seq_start, int seq_len, int p0,
-                                           unsigned char* slot) {
+                                           bool init, int cb, int nreal, int seq_start, int seq_len,
+                                           int p0, unsigned char* slot) {
   using R = InRing<T>;
   constexpr int UPR = R::ROW / 16;   // 16-byte units per row
+  constexpr int CPU = 16 / (int)sizeof(T);   // channels per unit
   for (int q = threadIdx.x; q < NROW * UPR; q += NTI) {
     const int m = q / UPR, uu = q - m * UPR;
     const int p = p0 - 3 + m;
     const T* src = qkv;
     uint32_t bytes = 0;
-    if (p >= 0 && p < seq_len) {
+    if (uu * CPU >= nreal) {
+      // an extra channel of a 64-dim head: zero
+    } else if (p >= 0 && p < seq_len) {
       src = qkv + (size_t)(seq_start + p) * d.cqkv + cb;
       bytes = 16;
     } else if (p < 0 && init) {
@@ -247,9 +254,12 @@ __device__ __forceinline__ void ring_issue(const KDims& d, const T* __restrict__
     cp_async16(slot + m * R::PITCH + uu * 16, reinterpret_cast<const unsigned char*>(src) + (bytes ? uu * 16 : 0),
                bytes);
   }
-  for (int q = threadIdx.x; q < (int)(128 * 4 * sizeof(T) / 16); q += NTI)
+  for (int q = threadIdx.x; q < (int)(128 * 4 * sizeof(T) / 16); q += NTI) {
+    const bool real = q * 16 < nreal * 4 * (int)sizeof(T);
     cp_async16(slot + R::W_OFF + q * 16,
-               reinterpret_cast<const unsigned char*>(conv_w + (size_t)cb * 4) + q * 16, 16);
+               reinterpret_cast<const unsigned char*>(conv_w + (size_t)cb * 4) + (real ? q * 16 : 0),
+               real ? 16u : 0u);
+  }
   cp_async_commit();
 }
 
@@ -531,7 +541,7 @@ __device__ __forceinline__ void t_to_b2(const float* Tm, const float* cw, const 
   }
 }
 
-template <typename T>
+template <typename T, bool PAD>
 __global__ void __launch_bounds__(NTI, 1)
 tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict__ dt_bias,
                 const T* __restrict__ conv_w, const T* __restrict__ conv_state, int num_slots,
@@ -590,14 +600,18 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   // ---- every input tensor of the chunk into the ring: k, q, v of V-head 0, 1, ... (tensor i in
   // slot i % NSLOT; later tensors as slots free up)
   const int ntens = 2 + r;
+  // head dims: 128 unless the instance runs 64-dim heads zero-padded to 128
+  const int dk_ = PAD ? d.dk : D, dv_ = PAD ? d.dv : D;
   auto tens_base = [&](int i) {
-    return i == 0 ? d.Hk * D + kh * D : (i == 1 ? kh * D : 2 * d.Hk * D + (h0 + i - 2) * D);
+    return i == 0 ? d.Hk * dk_ + kh * dk_ : (i == 1 ? kh * dk_ : 2 * d.Hk * dk_ + (h0 + i - 2) * dv_);
   };
+  auto tens_n = [&](int i) { return i < 2 ? dk_ : dv_; };
   auto slot_of = [&](int i) { return ring + (i % R::NSLOT) * R::SLOT; };
   const int p0 = t0 - seq_start;
   int issued = 0;
   for (; issued < min(ntens, R::NSLOT); ++issued)
-    ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), seq_start, seq_len, p0, slot_of(issued));
+    ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), tens_n(issued), seq_start, seq_len,
+                  p0, slot_of(issued));
   // waits for tensor i's copies (all threads), then a barrier makes every thread's copies visible
   auto ring_wait = [&](int i) {
     cp_async_wait_pending(issued - 1 - i);
@@ -625,7 +639,8 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   // ---- Q: conv, l2norm (times q_scale), A1 Q rows and per V-head the Q~ rows of B3
   ring_wait(1);   // also: K rows complete, slot 0 and the partial sums free
   if (issued < ntens) {
-    ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), seq_start, seq_len, p0, slot_of(issued));
+    ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), tens_n(issued), seq_start, seq_len,
+                  p0, slot_of(issued));
     ++issued;
   }
   conv_slot<T>(slot_of(1), L, y);
@@ -686,7 +701,8 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   // ---- V of the first V-head straight into its tile (overlaps MMA1)
   ring_wait(2);   // also: slot 1 free
   if (issued < ntens) {
-    ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), seq_start, seq_len, p0, slot_of(issued));
+    ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), tens_n(issued), seq_start, seq_len,
+                  p0, slot_of(issued));
     ++issued;
   }
   conv_slot<T>(slot_of(2), L, y);
@@ -832,7 +848,8 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
       if (j + 1 < r) {
         ring_wait(j + 3);   // tensor 2 + (j + 1); also: slot of tensor j + 2 free
         if (issued < ntens) {
-          ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), seq_start, seq_len, p0, slot_of(issued));
+          ring_issue<T>(d, qkv, conv_w, cs, init, tens_base(issued), tens_n(issued), seq_start, seq_len,
+                  p0, slot_of(issued));
           ++issued;
         }
         conv_slot<T>(slot_of(j + 3), L, y);
@@ -944,7 +961,7 @@ __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
-template <typename T>
+template <typename T, bool PAD>
 __global__ void __launch_bounds__(NTC, 1)
 tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_state,
                 T* __restrict__ conv_state, int num_slots, const int32_t* __restrict__ cu,
@@ -954,6 +971,8 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
                 int32_t* __restrict__ status) {
   extern __shared__ __align__(1024) unsigned char sm[];
   using S = ChainSmem;
+  // head dims: 128 unless the instance runs 64-dim heads zero-padded to 128
+  const int dk_ = PAD ? d.dk : D, dv_ = PAD ? d.dv : D;
   const float* ut_s = reinterpret_cast<const float*>(sm + S::UT);
   float* ot = reinterpret_cast<float*>(sm + S::OT);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::BAR);
@@ -1020,7 +1039,8 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   const bool init_seq = valid && has_init != nullptr && __ldg(has_init + n) != 0;
   const bool init = valid && (init_seq || ca > 0);
   const bool seq_ends = valid && ((nch > 0 && cb == nch_seq) || empty_here);
-  float* Sg = rec_state + ((size_t)(valid ? s : 0) * d.Hv + h) * D * D;
+  // the slot's state, dk x dv (a 64-dim head's state is the corner of the 128 x 128 one here)
+  float* Sg = rec_state + ((size_t)(valid ? s : 0) * d.Hv + h) * dk_ * dv_;
   auto rec_of = [&](int c) {
     return reinterpret_cast<const unsigned char*>(ws) +
            ((size_t)(rec_base + choff + ca + c - cw0) * d.Hv + h) * REC_BYTES;
@@ -1032,19 +1052,23 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     const int q = warp & 3, hf = warp >> 2;
     const int j = 32 * q + lane;
     const uint32_t lb = tb + ((uint32_t)(32 * q) << 16);
+    // this thread's 64 state entries are real (dk rows 64 hf .., dv column j) or all padding
+    const bool sreal = !PAD || (64 * hf < dk_ && j < dv_);
     {
       const float eg0 = nch > 0 ? *reinterpret_cast<const float*>(rec_of(0) + R_SC) : 1.f;
       float v[64];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) v[i] = init ? Sg[(size_t)(64 * hf + i) * D + j] : 0.f;
+      for (int i = 0; i < 64; ++i) v[i] = (init && sreal) ? Sg[(size_t)(64 * hf + i) * dv_ + j] : 0.f;
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
         const int f0 = 64 * hf + 16 * p;
         if (nch > 0) {
           put_sop16(lb, f0, v + 16 * p);
         } else if (valid && !init) {   // an empty sequence without a state: the slot is reset
+          if (sreal) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) Sg[(size_t)(f0 + i) * D + j] = 0.f;
+            for (int i = 0; i < 16; ++i) Sg[(size_t)(f0 + i) * dv_ + j] = 0.f;
+          }
         }
       }
       tc::tmem_wait_st();
@@ -1114,9 +1138,9 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
           if (c + 1 < nch) {
             put_sop16(lb, f0, v);
             put_sop16(lb, f0 + 16, v + 16);
-          } else if (valid) {
+          } else if (valid && sreal) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) Sg[(size_t)(f0 + i) * D + j] = v[i];
+            for (int i = 0; i < 32; ++i) Sg[(size_t)(f0 + i) * dv_ + j] = v[i];
           }
         }
         tc::tmem_wait_st();
@@ -1153,10 +1177,11 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     const int o8 = r & 15, tr = r >> 4;        // column octet, first token row
     const uint32_t lb = tb + ((uint32_t)(32 * q) << 16);
     float* oth = ot + th * 32 * D;             // this half's 32 token rows
-    const size_t ld = (size_t)d.Hv * D;
-    const size_t col = (size_t)h * D + 8 * o8;
-    float wv[8];
-    {
+    const size_t ld = (size_t)d.Hv * dv_;
+    const bool ocol = !PAD || 8 * o8 < dv_;    // a real output column octet (dv = 64: half)
+    const size_t col = (size_t)h * dv_ + (ocol ? 8 * o8 : 0);
+    float wv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (ocol) {
       const float4 w0 = Act<T>::ldg4(norm_w + 8 * o8), w1 = Act<T>::ldg4(norm_w + 8 * o8 + 4);
       wv[0] = w0.x; wv[1] = w0.y; wv[2] = w0.z; wv[3] = w0.w;
       wv[4] = w1.x; wv[5] = w1.y; wv[6] = w1.z; wv[7] = w1.w;
@@ -1206,9 +1231,9 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         for (int m = 0; m < 8; ++m) ss = fmaf(v[m], v[m], ss);
 #pragma unroll
         for (int ofs = 1; ofs < 16; ofs <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, ofs);
-        const float inv = valid ? rsqrtf(ss * (1.0f / (float)D) + d.norm_eps) : 0.f;
+        const float inv = valid ? rsqrtf(ss * (1.0f / (float)dv_) + d.norm_eps) : 0.f;
         const int t = 32 * th + tl;
-        if (t < L) {
+        if (t < L && ocol) {
           T* op = out + (size_t)(seq_start + c * CH + t) * ld + col;
           float y[8];
 #pragma unroll
@@ -1333,7 +1358,7 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   }
 }
 
-template <typename T>
+template <typename T, bool PAD>
 int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const int32_t* cu,
              const int32_t* slot_idx, const uint8_t* has_init, int num_seqs, int total,
              const void* qkv, const void* z, const void* a, const void* b, void* out, void* ws,
@@ -1368,8 +1393,8 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
                        : (int)std::min<size_t>((size_t)nc_max, cap);
   const int win0 = pipe ? (int)std::min<size_t>({(size_t)std::max(win, nsm / d.Hk), cap / 2, (size_t)nc_max})
                         : win;
-  auto k1 = tc_intra_kernel<T>;
-  auto k2 = tc_chain_kernel<T>;
+  auto k1 = tc_intra_kernel<T, PAD>;
+  auto k2 = tc_chain_kernel<T, PAD>;
   if (cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)IntraSmem::BYTES) !=
           cudaSuccess ||
       cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ChainSmem::BYTES) !=
@@ -1425,7 +1450,8 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
 
 }  // namespace
 
-bool prefill_tc_supported(const KDims& d) { return d.dk == D && d.dv == D && d.r <= RMAX; }
+// Head dims 64 run as 128-dim heads whose extra channels, state rows and columns are zero.
+bool prefill_tc_supported(const KDims& d) { return d.dk <= D && d.dv <= D && d.r <= RMAX; }
 
 size_t prefill_tc_ws_bytes(const KDims& d, int num_seqs, int total) {
   return (size_t)(total / CH + num_seqs) * d.Hv * REC_BYTES;
@@ -1437,11 +1463,16 @@ int launch_prefill_tc(const KDims& d, const gdn_weights* w, const gdn_pool* pool
                       const int32_t* cu, const int32_t* slot_idx, const uint8_t* has_init,
                       int num_seqs, int total, const void* qkv, const void* z, const void* a,
                       const void* b, void* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  const bool pad = d.dk != D || d.dv != D;
   if (w->act == GDN_BF16)
-    return launch_t<__nv_bfloat16>(d, w, pool, cu, slot_idx, has_init, num_seqs, total, qkv, z, a,
-                                   b, out, ws, ws_bytes, stream);
-  return launch_t<float>(d, w, pool, cu, slot_idx, has_init, num_seqs, total, qkv, z, a, b, out,
-                         ws, ws_bytes, stream);
+    return pad ? launch_t<__nv_bfloat16, true>(d, w, pool, cu, slot_idx, has_init, num_seqs, total,
+                                               qkv, z, a, b, out, ws, ws_bytes, stream)
+               : launch_t<__nv_bfloat16, false>(d, w, pool, cu, slot_idx, has_init, num_seqs, total,
+                                                qkv, z, a, b, out, ws, ws_bytes, stream);
+  return pad ? launch_t<float, true>(d, w, pool, cu, slot_idx, has_init, num_seqs, total, qkv, z, a,
+                                     b, out, ws, ws_bytes, stream)
+             : launch_t<float, false>(d, w, pool, cu, slot_idx, has_init, num_seqs, total, qkv, z, a,
+                                      b, out, ws, ws_bytes, stream);
 }
 
 }  // namespace gdn

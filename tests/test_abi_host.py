@@ -177,11 +177,17 @@ def test_prefill_and_compact_host_checks(lib):
     rc = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(w), ctypes.byref(p), f, f, None, 2,
                                  100, f, f, f, f, f, 0x50000, least - 1, None)
     assert rc == -5
-    # head dims 64 (CUDA-core path) still need the full size
+    # head dims 64 take the same path (one chunk's records at least)
     d64 = D(dk=64, dv=64)
-    need64 = lib.gdn_prefill_workspace_bytes(ctypes.byref(d64), 2, 100)
+    least64 = lib.gdn_prefill_workspace_bytes(ctypes.byref(d64), 1, 1)
     rc = lib.gdn_prefill_chunked(ctypes.byref(d64), ctypes.byref(w), ctypes.byref(p), f, f, None, 2,
-                                 100, f, f, f, f, f, 0x50000, need64 - 1, None)
+                                 100, f, f, f, f, f, 0x50000, least64 - 1, None)
+    assert rc == -5
+    # more than four V-heads per K-head take the CUDA-core path, which needs the full size
+    d8 = D(Hk=1, Hv=8)
+    need8 = lib.gdn_prefill_workspace_bytes(ctypes.byref(d8), 2, 100)
+    rc = lib.gdn_prefill_chunked(ctypes.byref(d8), ctypes.byref(w), ctypes.byref(p), f, f, None, 2,
+                                 100, f, f, f, f, f, 0x50000, need8 - 1, None)
     assert rc == -5
     rc = lib.gdn_prefill_chunked(ctypes.byref(d), ctypes.byref(w), ctypes.byref(p), f, f, None, 2,
                                  100, f, f, f, f, f, 0x50000 + 16, need, None)
