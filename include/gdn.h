@@ -201,14 +201,15 @@ size_t gdn_prefill_workspace_bytes(const gdn_dims* dims, int32_t num_seqs, int32
  * int32[num_seqs]).  On return the slot holds the state after the sequence's last token and
  * its last K-1 raw inputs.  workspace: device, 256-byte aligned, contents undefined on entry
  * and exit.  gdn_prefill_workspace_bytes(...) holds the records of every chunk at once and is
- * always enough.  For head dims dk = dv = 128 the call runs in windows of whole 64-token chunks,
- * each sequence's state carried from window to window through its slot, with the same results
- * for any window size; any workspace of at least gdn_prefill_workspace_bytes(dims, 1, 1) bytes
- * (one chunk's records for every V-head) is accepted.  When the workspace holds two windows and
- * the sequences' V-heads leave SMs free, consecutive windows overlap on the GPU (programmatic
- * dependent launch; a few tens of chunks' records suffice for that).  Other head dims need the
- * full size (GDN_ERR_WORKSPACE_TOO_SMALL otherwise).  Several kernels on `stream` (two per
- * window); no host reads of device data. */
+ * always enough.  With at most four V-heads per K-head (any head dims) the call runs on the
+ * tensor cores in windows of whole 64-token chunks, each sequence's state carried from window to
+ * window through its slot, with the same results for any window size; any workspace of at least
+ * gdn_prefill_workspace_bytes(dims, 1, 1) bytes (one chunk's records for every V-head) is
+ * accepted.  When the workspace holds two windows and the sequences' V-heads leave SMs free,
+ * consecutive windows overlap on the GPU (programmatic dependent launch; a few tens of chunks'
+ * records suffice for that).  More V-heads per K-head take CUDA-core kernels that need the full
+ * size (GDN_ERR_WORKSPACE_TOO_SMALL otherwise).  Several kernels on `stream` (two per window
+ * on the tensor-core path); no host reads of device data. */
 int gdn_prefill_chunked(const gdn_dims* dims, const gdn_weights* w, const gdn_pool* pool,
                         const int32_t* cu_seqlens, const int32_t* slot_idx,
                         const uint8_t* has_initial_state, int32_t num_seqs, int32_t total_tokens,
