@@ -91,6 +91,44 @@ def test_prefill_full_size_T4096_sampled_heads():
         np.testing.assert_array_equal(hs.conv(g_conv)[0], c64[0])
 
 
+def test_prefill_pipelined_windows_four_sequences():
+    """Four sequences at the production geometry (Hk=16, Hv=32, d=128): their 128 chains leave
+    SMs free, so the call runs in pipelined windows whose chunks span sequence boundaries; one
+    sequence continues from its slot.  Sampled K-heads against the oracle, every touched slot's
+    state and conv state, and an untouched slot left alone."""
+    geo = synth.Geometry(16, 32, 128, 128, 4, synth.BF16)
+    w = synth.make_weights(geo, 620)
+    lens = [700, 130, 1500, 64]
+    cu = synth.cu_seqlens(lens)
+    T = int(cu[-1])
+    xs = synth.make_token_inputs(geo, T, 621, 0)
+    rec0, conv0 = synth.make_pool(geo, 6, 622, True)
+    layer = GatedDeltaNetLayer(geo, w, 6)
+    layer.load_state(rec0, conv0)
+    slots = np.array([4, 1, 0, 3], np.int32)
+    has_init = np.array([0, 1, 0, 0], np.uint8)
+    before = layer.rec_state[5].clone()
+    out = layer.prefill(_dev_i32(cu), _dev_i32(slots),
+                        torch.from_numpy(has_init).cuda(), **layer.inputs(xs))
+    torch.cuda.synchronize()
+    got = _np(out)
+    g_rec = _np(layer.rec_state)
+    g_conv = _np(layer.conv_state)
+    assert torch.equal(layer.rec_state[5], before)
+    for k_heads in ([3], [10, 15]):
+        hs = HeadSlice(geo, k_heads)
+        r64 = hs.rec(rec0)
+        c64 = hs.conv(conv0)
+        rc, ref = oracle.prefill(hs.sub.oracle_dims(), hs.weights(w), r64, c64, cu, slots, has_init,
+                                 **hs.inputs(xs))
+        assert rc == 0
+        assert_out_close(hs.out_cols(got), ref, geo.act, f"heads {k_heads}")
+        for sl in slots:
+            assert_state_close(hs.rec(g_rec)[sl], r64[sl], f"slot {sl} heads {k_heads}")
+            np.testing.assert_array_equal(hs.conv(g_conv)[sl], c64[sl])
+    assert int(layer.status.item()) == 0
+
+
 def test_prefill_then_decode_continues():
     geo = synth.Geometry(2, 4, 128, 128, 4, synth.BF16)
     w = synth.make_weights(geo, 610)
