@@ -18,6 +18,10 @@ template <> struct Act<float> {
   static __device__ __forceinline__ float4 ldg4(const float* p) {
     return __ldg(reinterpret_cast<const float4*>(p));
   }
+  // the same from shared memory
+  static __device__ __forceinline__ float4 lds4(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+  }
   static __device__ __forceinline__ void store4(float* p, float4 v) {
     *reinterpret_cast<float4*>(p) = v;
   }
@@ -31,6 +35,12 @@ template <> struct Act<__nv_bfloat16> {
   // 4 consecutive values (8-byte aligned address)
   static __device__ __forceinline__ float4 ldg4(const __nv_bfloat16* p) {
     const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+  }
+  static __device__ __forceinline__ float4 lds4(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
     const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
     const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
     return make_float4(lo.x, lo.y, hi.x, hi.y);

@@ -13,6 +13,11 @@
 //   kv = S^T k,  sq = S^T q           (one pass over the old S, held in registers)
 //   delta = beta (v - e^g kv),  o = e^g sq + (k.q) delta
 //   S' = e^g S + k delta^T            (written back from the same registers)
+// Each warp owns dv/8 whole columns of every state (all dk rows), so both products reduce
+// inside the warp by shuffles and the warps run through the V-heads without a CTA barrier;
+// only the RMSNorm's sum over dv meets in shared memory, once, after the last V-head.
+// The kernel is a programmatic dependent launch: in a stream of decode steps the next step's
+// CTAs are placed while this one drains and wait for its completion before any read.
 #include <mutex>
 
 #include "gdn_internal.h"
@@ -31,18 +36,33 @@ template <> struct VecF<4> {
     __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
   }
 };
-template <> struct VecF<2> {
-  static __device__ __forceinline__ void ld(const float* p, float* v) {
-    const float2 t = __ldcs(reinterpret_cast<const float2*>(p));
-    v[0] = t.x; v[1] = t.y;
-  }
-  static __device__ __forceinline__ void st(float* p, const float* v) {
-    __stcs(reinterpret_cast<float2*>(p), make_float2(v[0], v[1]));
-  }
-};
 
 constexpr int kDecodeThreads = 256;
 constexpr int kDecodeWarps = kDecodeThreads / 32;
+
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
+                   static_cast<unsigned>(__cvta_generic_to_shared(sdst))), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(
+                   static_cast<unsigned>(__cvta_generic_to_shared(sdst))), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+// 4 consecutive activation elements (8 or 16 bytes) into shared memory
+template <typename T>
+__device__ __forceinline__ void cp_async_quad(T* sdst, const T* gsrc) {
+  if constexpr (sizeof(T) == 2) cp_async8(sdst, gsrc);
+  else cp_async16(sdst, gsrc);
+}
+
+// Shared-memory layout of decode_kernel: the f32 work arrays, then the prefetched z values and
+// norm weight.
+template <int DK, int DV>
+__host__ __device__ inline int decode_float_count(int r) {
+  return ((2 * DK + 2 * r * DV + r * kDecodeWarps + 3 + 2 * r) + 3) / 4 * 4;
+}
 
 // One token of the causal conv for channel ch of the row's conv state cs ([K-1][cqkv],
 // K = 4): returns SiLU(sum_j w[j] x_{t-3+j}) and shifts the state by one raw input.
@@ -70,24 +90,56 @@ decode_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict_
               const T* __restrict__ z, const T* __restrict__ a, const T* __restrict__ b,
               T* __restrict__ out) {
   constexpr int NW = kDecodeWarps;
-  constexpr int CPT = DV / 32;   // state columns per lane
-  constexpr int RPW = DK / NW;   // state rows per warp
-  extern __shared__ float smem[];
+  // A warp owns CW whole state columns (all DK rows), so S^T k and S^T q reduce inside the
+  // warp and the V-heads need no CTA barrier.  A lane holds a float4 of 4 columns in RPL rows.
+  constexpr int CW = DV / NW;       // state columns per warp
+  constexpr int LPR = CW / 4;       // lanes per row segment
+  constexpr int G = 32 / LPR;       // row groups per warp
+  constexpr int RPL = DK / G;       // state rows per lane
+  static_assert(CW % 4 == 0 && DK % G == 0, "state tiling");
+  extern __shared__ float4 smem4[];
   const int kh = blockIdx.x, row = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane / LPR, col0 = warp * CW + (lane % LPR) * 4;
   const int r = d.r;
-  float* qs = smem;
+  float* qs = reinterpret_cast<float*>(smem4);
   float* ks = qs + DK;
   float* vs = ks + DK;
-  float* red = vs + r * DV;          // [2 buffers][kv|sq][NW][DV]
-  float* misc = red + 4 * NW * DV;   // iq, ik, k.q
+  float* os = vs + r * DV;           // raw outputs o of the r V-heads
+  float* ssq = os + r * DV;          // per-warp partial sums of o^2, [r][NW]
+  float* misc = ssq + r * NW;        // iq, ik, k.q, then (e^g, beta) per V-head
+  T* zs = reinterpret_cast<T*>(qs + decode_float_count<DK, DV>(r));   // z of the r V-heads
+  T* nws = zs + r * DV;                                                // norm weight
 
+  // A programmatic dependent of the previous kernel in the stream: nothing is read before that
+  // kernel has completed and its writes are visible.  The next kernel may be placed on the SMs
+  // as soon as every CTA of this one runs (it waits the same way).
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const int s = slot_idx[row];
   T* out_row = out + (size_t)row * d.Hv * DV;
   if (s < 0 || s >= num_slots) {
     if (s >= num_slots && tid == 0 && kh == 0) set_status(status, GDN_STATUS_SLOT_RANGE);
     for (int e = tid; e < r * DV; e += kDecodeThreads) out_row[kh * r * DV + e] = Act<T>::cvt(0.f);
     return;
+  }
+  // The z values and the norm weight go to shared memory by asynchronous copies issued before
+  // the conv prologue (their latency would otherwise fall at the end of the CTA).
+  {
+    const T* zrow = z + (size_t)row * d.Hv * DV + (size_t)kh * r * DV;
+    for (int e = tid; e < r * (DV / 4); e += kDecodeThreads) cp_async_quad(zs + 4 * e, zrow + 4 * e);
+    for (int e = tid; e < DV / 4; e += kDecodeThreads) cp_async_quad(nws + 4 * e, norm_w + 4 * e);
+    cp_async_commit();
+  }
+  // gate inputs of the r V-heads (threads 32 .. 32 + r - 1), in flight during the conv prologue
+  const int gh = tid - 32;
+  float g_alog = 0.f, g_dt = 0.f, g_a = 0.f, g_b = 0.f;
+  if (gh >= 0 && gh < r) {
+    const int h = kh * r + gh;
+    g_alog = __ldg(A_log + h);
+    g_dt = __ldg(dt_bias + h);
+    g_a = Act<T>::ldg(a + (size_t)row * d.Hv + h);
+    g_b = Act<T>::ldg(b + (size_t)row * d.Hv + h);
   }
 
   // ---- conv update + SiLU over the channels this unit owns.  The loads of a thread's channels
@@ -134,6 +186,12 @@ decode_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict_
       }
     }
   }
+  if (gh >= 0 && gh < r) {
+    float gg, beta;
+    gates(g_alog, g_dt, g_a, g_b, gg, beta);
+    misc[3 + 2 * gh] = expf(gg);
+    misc[4 + 2 * gh] = beta;
+  }
   __syncthreads();
 
   // ---- l2norm of q (times q_scale) and k, and k.q of the normalised vectors
@@ -158,83 +216,79 @@ decode_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict_
   }
   __syncthreads();
   const float iq = misc[0], ik = misc[1], kq = misc[2];
-  float kr[RPW], qr[RPW];
+  float kr[RPL], qr[RPL];
 #pragma unroll
-  for (int i = 0; i < RPW; ++i) {
-    kr[i] = ks[warp * RPW + i] * ik;
-    qr[i] = qs[warp * RPW + i] * iq;
+  for (int i = 0; i < RPL; ++i) {
+    kr[i] = ks[g + G * i] * ik;
+    qr[i] = qs[g + G * i] * iq;
   }
 
-  // ---- the r V-heads of this K-head
+  // ---- the r V-heads of this K-head; each warp runs through them on its own columns
   for (int hh = 0; hh < r; ++hh) {
     const int h = kh * r + hh;
-    float* Sp = rec + (((size_t)s * d.Hv + h) * DK) * DV;
-    float st[RPW][CPT];
+    float* Sp = rec + (((size_t)s * d.Hv + h) * DK) * DV + col0;
+    float st[RPL][4];
 #pragma unroll
-    for (int i = 0; i < RPW; ++i) VecF<CPT>::ld(Sp + (size_t)(warp * RPW + i) * DV + lane * CPT, st[i]);
+    for (int i = 0; i < RPL; ++i) VecF<4>::ld(Sp + (size_t)(g + G * i) * DV, st[i]);
+    const float eg = misc[3 + 2 * hh], beta = misc[4 + 2 * hh];
 
-    float g, beta;
-    gates(__ldg(A_log + h), __ldg(dt_bias + h), Act<T>::ldg(a + (size_t)row * d.Hv + h),
-          Act<T>::ldg(b + (size_t)row * d.Hv + h), g, beta);
-    const float eg = expf(g);
-
-    float pk[CPT], pq[CPT];
+    float pk[4], pq[4];
 #pragma unroll
-    for (int c = 0; c < CPT; ++c) pk[c] = pq[c] = 0.f;
+    for (int c = 0; c < 4; ++c) pk[c] = pq[c] = 0.f;
 #pragma unroll
-    for (int i = 0; i < RPW; ++i)
+    for (int i = 0; i < RPL; ++i)
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) {
+      for (int c = 0; c < 4; ++c) {
         pk[c] = fmaf(st[i][c], kr[i], pk[c]);
         pq[c] = fmaf(st[i][c], qr[i], pq[c]);
       }
-    float* rb = red + (hh & 1) * 2 * NW * DV;
 #pragma unroll
-    for (int c = 0; c < CPT; ++c) {
-      rb[warp * DV + lane * CPT + c] = pk[c];
-      rb[NW * DV + warp * DV + lane * CPT + c] = pq[c];
-    }
-    __syncthreads();
-    float delta[CPT], o[CPT];
+    for (int off = LPR; off < 32; off <<= 1)
 #pragma unroll
-    for (int c = 0; c < CPT; ++c) {
-      float kv = 0.f, sqv = 0.f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        kv += rb[w * DV + lane * CPT + c];
-        sqv += rb[NW * DV + w * DV + lane * CPT + c];
+      for (int c = 0; c < 4; ++c) {
+        pk[c] += __shfl_xor_sync(0xffffffffu, pk[c], off);
+        pq[c] += __shfl_xor_sync(0xffffffffu, pq[c], off);
       }
-      delta[c] = beta * (vs[hh * DV + lane * CPT + c] - eg * kv);
-      o[c] = fmaf(eg, sqv, kq * delta[c]);
+    const float4 vv = *reinterpret_cast<const float4*>(vs + hh * DV + col0);
+    const float vc[4] = {vv.x, vv.y, vv.z, vv.w};
+    float delta[4], o[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      delta[c] = beta * (vc[c] - eg * pk[c]);
+      o[c] = fmaf(eg, pq[c], kq * delta[c]);
     }
 #pragma unroll
-    for (int i = 0; i < RPW; ++i) {
+    for (int i = 0; i < RPL; ++i) {
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) st[i][c] = fmaf(eg, st[i][c], kr[i] * delta[c]);
-      VecF<CPT>::st(Sp + (size_t)(warp * RPW + i) * DV + lane * CPT, st[i]);
+      for (int c = 0; c < 4; ++c) st[i][c] = fmaf(eg, st[i][c], kr[i] * delta[c]);
+      VecF<4>::st(Sp + (size_t)(g + G * i) * DV, st[i]);
     }
-    // ---- z-gated RMSNorm over this V-head's dv outputs (one warp)
-    if (warp == (hh % NW)) {
-      float ss = 0.f;
+    if (g == 0) {
+      *reinterpret_cast<float4*>(os + hh * DV + col0) = make_float4(o[0], o[1], o[2], o[3]);
+      float ss = o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3];
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) ss = fmaf(o[c], o[c], ss);
-      ss = warp_sum(ss);
-      const float inv = 1.0f / sqrtf(ss / (float)DV + d.norm_eps);
-      const T* zr = z + (size_t)row * d.Hv * DV + (size_t)h * DV;
-      if constexpr (CPT == 4) {
-        const float4 zz = Act<T>::ldg4(zr + lane * 4), ww = Act<T>::ldg4(norm_w + lane * 4);
-        Act<T>::store4(out_row + (size_t)h * DV + lane * 4,
-                       make_float4(o[0] * inv * ww.x * siluf_(zz.x), o[1] * inv * ww.y * siluf_(zz.y),
-                                   o[2] * inv * ww.z * siluf_(zz.z), o[3] * inv * ww.w * siluf_(zz.w)));
-      } else {
-#pragma unroll
-        for (int c = 0; c < CPT; ++c) {
-          const int j = lane * CPT + c;
-          const float zz = Act<T>::ldg(zr + j);
-          Act<T>::store(out_row + (size_t)h * DV + j, o[c] * inv * Act<T>::ldg(norm_w + j) * siluf_(zz));
-        }
-      }
+      for (int off = 1; off < LPR; off <<= 1) ss += __shfl_xor_sync((1u << LPR) - 1u, ss, off);
+      if (lane == 0) ssq[hh * NW + warp] = ss;
     }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- z-gated RMSNorm over each V-head's dv outputs, 4 columns per thread
+  constexpr int Q4 = DV / 4;
+  for (int e = tid; e < r * Q4; e += kDecodeThreads) {
+    const int hh = e / Q4, j = (e - hh * Q4) * 4;
+    const int h = kh * r + hh;
+    const float4 zz = Act<T>::lds4(zs + hh * DV + j);
+    const float4 ww = Act<T>::lds4(nws + j);
+    float ss = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) ss += ssq[hh * NW + w];
+    const float inv = 1.0f / sqrtf(ss / (float)DV + d.norm_eps);
+    const float4 ov = *reinterpret_cast<const float4*>(os + hh * DV + j);
+    Act<T>::store4(out_row + (size_t)h * DV + j,
+                   make_float4(ov.x * inv * ww.x * siluf_(zz.x), ov.y * inv * ww.y * siluf_(zz.y),
+                               ov.z * inv * ww.z * siluf_(zz.z), ov.w * inv * ww.w * siluf_(zz.w)));
   }
 }
 
@@ -262,7 +316,7 @@ template <int DK, int DV, typename T>
 int launch_decode_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
                     const int32_t* slot_idx, int B, const void* qkv, const void* z, const void* a,
                     const void* b, void* out, cudaStream_t stream) {
-  const size_t smem = sizeof(float) * (2 * DK + d.r * DV + 4 * kDecodeWarps * DV + 4);
+  const size_t smem = sizeof(float) * decode_float_count<DK, DV>(d.r) + sizeof(T) * (d.r + 1) * DV;
   auto kern = decode_kernel<DK, DV, T>;
   // Raised once per kernel (to the per-block maximum), so that launches -- also those recorded
   // into a CUDA graph -- never need to change the attribute.
@@ -277,14 +331,25 @@ int launch_decode_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
   });
   if (attr_rc != 0) return attr_rc;
   if (smem > 227 * 1024) return GDN_ERR_TOO_LARGE;
-  dim3 grid(d.Hk, B);
-  kern<<<grid, kDecodeThreads, smem, stream>>>(
-      d, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
+  // programmatic stream serialization: the CTAs may be placed while the previous kernel of the
+  // stream drains, and wait for it in the kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)d.Hk, (unsigned)B);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, kern, d, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
       static_cast<const T*>(w->norm_weight), pool->rec_state, static_cast<T*>(pool->conv_state),
       pool->num_slots, pool->status, slot_idx, static_cast<const T*>(qkv),
       static_cast<const T*>(z), static_cast<const T*>(a), static_cast<const T*>(b),
       static_cast<T*>(out));
-  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 template <typename T>
