@@ -94,7 +94,8 @@ __device__ bool find_chunk(const int32_t* __restrict__ cu, const int32_t* __rest
                            const uint8_t* __restrict__ has_init, int num_seqs, int total, int c,
                            ChunkInfo& ci) {
   const int lane = threadIdx.x & 31;
-  bool ok = (__ldg(cu) == 0) && (__ldg(cu + num_seqs) == total);
+  const int cu_first = __ldg(cu), cu_last = __ldg(cu + num_seqs);   // issued beside the loop's loads
+  bool ok = true;
   int base = 0;
   ci.seq = -1;
   for (int n0 = 0; n0 < num_seqs; n0 += 32) {
@@ -130,6 +131,7 @@ __device__ bool find_chunk(const int32_t* __restrict__ cu, const int32_t* __rest
     }
     base += __shfl_sync(0xffffffffu, incl, 31);
   }
+  ok = ok && cu_first == 0 && cu_last == total;
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -910,8 +912,8 @@ struct ChainSmem {
   static constexpr uint32_t B4 = B3 + 65536;                 // [P ; K~^T] image, 48 KiB
   static constexpr uint32_t UT = B4 + 49152;                 // f32 U~ [64 tokens][128 dv], 32 KiB
   static constexpr uint32_t OT = UT + 32768;                 // f32 O [2 halves][32 tokens][128], 32 KiB
-  static constexpr uint32_t BAR = OT + 32768;                // 14 mbarriers
-  static constexpr uint32_t MISC = BAR + 128;
+  static constexpr uint32_t BAR = OT + 32768;                // 17 mbarriers
+  static constexpr uint32_t MISC = BAR + 256;
   static constexpr uint32_t BYTES = MISC + 64;
 };
 static_assert(ChainSmem::BYTES <= 227 * 1024, "chain kernel shared memory");
@@ -982,13 +984,17 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   uint64_t* b4empty = bars + 5;  // B4 read by the chunk's U^T products
   uint64_t* utfull = bars + 6;   // U~ landed
   uint64_t* utempty = bars + 7;  // U~ read by the main warps (8 arrivals)
-  uint64_t* sopf = bars + 8;     // S^T operand written (8 arrivals)
+  uint64_t* sopf = bars + 8;     // S^T operand, dk [0, 32) and [64, 96) written (8 arrivals)
   uint64_t* mma3 = bars + 9;     // D3^T complete
-  uint64_t* uopf = bars + 10;    // U^T operand written (8 arrivals)
+  uint64_t* uopf = bars + 10;    // U^T operand, tokens [0, 16) and [32, 48) written (8 arrivals)
   uint64_t* sready = bars + 11;  // S^T += U^T K~ complete
   uint64_t* dfull = bars + 12;   // O^T complete in D3^T columns 0-63
   uint64_t* dempty = bars + 13;  // O^T read by the output warps (8 arrivals)
   uint64_t* sscl = bars + 14;    // e^{gamma_L} S^T written for the chunk's U^T K~ (8 arrivals)
+  uint64_t* sopf2 = bars + 15;   // the rest of the S^T operand (8 arrivals)
+  uint64_t* uopf2 = bars + 16;   // the rest of the U^T operand (8 arrivals)
+  // The operands are handed to the MMA warp in two halves each, so that the first half's
+  // products run while the second half is written.
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::MISC);
   int* sh = reinterpret_cast<int*>(sm + S::MISC + 16);
 
@@ -1005,15 +1011,21 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
     }
   }
   if (tid == 0) {
-    for (int i = 0; i < 15; ++i)
-      tc::mbar_init(bars + i, (i == 7 || i == 8 || i == 10 || i == 13 || i == 14) ? 8 : 1);
+    for (int i = 0; i < 17; ++i)
+      tc::mbar_init(bars + i, (i == 7 || i == 8 || i == 10 || i >= 13) ? 8 : 1);
     tc::mbar_fence_init();
   }
   if (warp == 0) tc::tmem_alloc(tslot, TC_COLS);
+  // The call's own inputs (cu_seqlens, slot_idx, has_initial_state) were complete before the
+  // call's first kernel started: read before the wait.
+  const int seq_start0 = __ldg(cu + n), len0 = __ldg(cu + n + 1) - seq_start0;
+  const int s = __ldg(slot_idx + n);
+  const bool has_init_n = has_init != nullptr && __ldg(has_init + n) != 0;
   // Launched as a programmatic dependent of the window's intra kernel: everything above touches
-  // only this CTA's own resources; the records, the slot's state and the rest come after the
-  // intra kernel (and with it the previous window's chains) has completed.  Only then may the next
-  // window's intra kernel start: it writes the workspace half the previous window's chains read.
+  // only this CTA's own resources and the call's inputs; the records, the slot's state and the
+  // rest come after the intra kernel (and with it the previous window's chains) has completed.
+  // Only then may the next window's intra kernel start: it writes the workspace half the previous
+  // window's chains read.
   tc::pdl_wait_primary();
   tc::pdl_launch_dependents();   // the next window's intra kernel may take the SMs left free
   tc::fence_before_sync();
@@ -1022,7 +1034,6 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   const uint32_t tb = *tslot;
   const int choff = sh[1];
   volatile int* abort = sh + 2;
-  const int seq_start0 = __ldg(cu + n), len0 = __ldg(cu + n + 1) - seq_start0;
   const int nch_seq = sh[0] ? (len0 + CH - 1) / CH : 0;
   // The call's global chunks [cw0, cw1) form this window: the sequence's chunks [ca, cb) of it
   // run here, as local chunks 0 .. nch - 1, starting from the slot's state when an earlier window
@@ -1031,12 +1042,11 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
   const int nch = max(0, cb - ca);
   const bool empty_here = nch_seq == 0 && cw0 == 0;   // an empty sequence resets its slot once
   const int seq_start = seq_start0 + ca * CH, len = len0 - ca * CH;   // tokens from the window on
-  const int s = __ldg(slot_idx + n);
   // invalid cu_seqlens: nothing is read or written
   const bool valid = sh[0] && s >= 0 && s < num_slots && (nch > 0 || empty_here);
   if (sh[0] && s >= num_slots && h == 0 && tid == 0 && (nch > 0 || empty_here))
     set_status(status, GDN_STATUS_SLOT_RANGE);
-  const bool init_seq = valid && has_init != nullptr && __ldg(has_init + n) != 0;
+  const bool init_seq = valid && has_init_n;
   const bool init = valid && (init_seq || ca > 0);
   const bool seq_ends = valid && ((nch > 0 && cb == nch_seq) || empty_here);
   // the slot's state, dk x dv (a 64-dim head's state is the corner of the 128 x 128 one here)
@@ -1074,7 +1084,10 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       tc::tmem_wait_st();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(sopf);
+      if (lane == 0) {
+        mbar_arrive(sopf);
+        mbar_arrive(sopf2);
+      }
       if (nch > 0) {
 #pragma unroll
         for (int p = 0; p < 4; ++p) put_sscl16(lb, 64 * hf + 16 * p, v + 16 * p, eg0);
@@ -1091,31 +1104,31 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       // U^T = U~^T - (W S)^T -> the U^T operand
       const bool ok1 = wait_or_abort(mma3, par, abort, status) && wait_or_abort(utfull, par, abort, status);
       tc::fence_after_sync();
-      if (ok1) {
-        uint32_t rv[32];
-        tc::tmem_ld16_nw(lb + TC_D3 + 64 + 32 * hf, rv);
-        tc::tmem_ld16_nw(lb + TC_D3 + 64 + 32 * hf + 16, rv + 16);
-        tc::tmem_wait_ld();
-        tc::reg_fence16(rv);
-        tc::reg_fence16(rv + 16);
-        uint32_t hw[16], lw[16];
+      // in two halves of 16 tokens (K-steps 2 hf, then 2 hf + 1 of the U^T products)
 #pragma unroll
-        for (int p = 0; p < 16; ++p) {
-          const int t = 32 * hf + 2 * p;
-          const float u0 = ut_s[t * D + j] - __uint_as_float(rv[2 * p]);
-          const float u1 = ut_s[(t + 1) * D + j] - __uint_as_float(rv[2 * p + 1]);
-          tc::split2_bf16(u0, u1, hw[p], lw[p]);
+      for (int hq = 0; hq < 2; ++hq) {
+        if (ok1) {
+          uint32_t rv[16];
+          tc::tmem_ld16_nw(lb + TC_D3 + 64 + 32 * hf + 16 * hq, rv);
+          tc::tmem_wait_ld();
+          tc::reg_fence16(rv);
+          uint32_t hw[8], lw[8];
+#pragma unroll
+          for (int p = 0; p < 8; ++p) {
+            const int t = 32 * hf + 16 * hq + 2 * p;
+            const float u0 = ut_s[t * D + j] - __uint_as_float(rv[2 * p]);
+            const float u1 = ut_s[(t + 1) * D + j] - __uint_as_float(rv[2 * p + 1]);
+            tc::split2_bf16(u0, u1, hw[p], lw[p]);
+          }
+          tc::tmem_st8w_nw(lb + TA_U + 16 * hf + 8 * hq, hw);
+          tc::tmem_st8w_nw(lb + TA_U + 32 + 16 * hf + 8 * hq, lw);
+          tc::tmem_wait_st();
         }
-        tc::tmem_st16w_nw(lb + TA_U + 16 * hf, hw);
-        tc::tmem_st16w_nw(lb + TA_U + 32 + 16 * hf, lw);
-        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(hq ? uopf2 : uopf);
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(uopf);
-        mbar_arrive(utempty);
-      }
+      if (lane == 0) mbar_arrive(utempty);
       // S^T of the next chunk = the accumulated e^{gamma_L} S^T + U^T K~: first its operand (the
       // next D3^T products wait for it), then its copy scaled by the next e^{gamma_L} (needed
       // only by the next U^T K~); after the last chunk, the final state to the slot
@@ -1128,9 +1141,10 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
         tc::reg_fence16(rv);
         tc::reg_fence16(rv + 16);
       };
-      if (ok2) {
+      // in two halves of 32 dk (K-steps 4 hf, 4 hf + 1, then 4 hf + 2, 4 hf + 3 of D3^T)
 #pragma unroll 1
-        for (int hp = 0; hp < 2; ++hp) {
+      for (int hp = 0; hp < 2; ++hp) {
+        if (ok2) {
           const int f0 = 64 * hf + 32 * hp;
           uint32_t rv[32];
           ld_s32(f0, rv);
@@ -1138,17 +1152,19 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
           if (c + 1 < nch) {
             put_sop16(lb, f0, v);
             put_sop16(lb, f0 + 16, v + 16);
+            tc::tmem_wait_st();
           } else if (valid && sreal) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) Sg[(size_t)(f0 + i) * dv_ + j] = v[i];
           }
         }
-        tc::tmem_wait_st();
+        if (c + 1 < nch) {
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(hp ? sopf2 : sopf);
+        }
       }
-      tc::fence_before_sync();
-      __syncwarp();
       if (c + 1 < nch) {
-        if (lane == 0) mbar_arrive(sopf);
         if (ok2) {
 #pragma unroll 1
           for (int hp = 0; hp < 2; ++hp) {
@@ -1298,29 +1314,49 @@ tc_chain_kernel(KDims d, const T* __restrict__ norm_w, float* __restrict__ rec_s
       const uint32_t d3 = tb + TC_D3, xs = tb + TC_S;
       for (int c = 0; c < nch; ++c) {
         const uint32_t par = c & 1;
-        if (wait_or_abort(sopf, par, abort, status) && wait_or_abort(b3full, par, abort, status) &&
-            (c == 0 || wait_or_abort(dempty, (c - 1) & 1, abort, status))) {
+        // D3^T = S^T [Q~ ; W]^T, K = dk: K-steps 0, 1, 4, 5 on the first half of the operand
+        auto d3_step = [&](int k) {
+          const uint64_t bh = tc::desc_add(dB3h, 256 * k), bl = tc::desc_add(dB3l, 256 * k);
+          tc::mma_bf16_tmem_a(d3, aSh + 8 * k, bh, id128, k > 0);
+          tc::mma_bf16_tmem_a(d3, aSh + 8 * k, bl, id128, 1);
+          tc::mma_bf16_tmem_a(d3, aSl + 8 * k, bh, id128, 1);
+        };
+        const bool okA = wait_or_abort(sopf, par, abort, status) && wait_or_abort(b3full, par, abort, status) &&
+                         (c == 0 || wait_or_abort(dempty, (c - 1) & 1, abort, status));
+        if (okA) {
           tc::fence_after_sync();
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {   // D3^T = S^T [Q~ ; W]^T, K = dk
-            const uint64_t bh = tc::desc_add(dB3h, 256 * k), bl = tc::desc_add(dB3l, 256 * k);
-            tc::mma_bf16_tmem_a(d3, aSh + 8 * k, bh, id128, k > 0);
-            tc::mma_bf16_tmem_a(d3, aSh + 8 * k, bl, id128, 1);
-            tc::mma_bf16_tmem_a(d3, aSl + 8 * k, bh, id128, 1);
-          }
+          d3_step(0);
+          d3_step(1);
+          d3_step(4);
+          d3_step(5);
+        }
+        if (okA && wait_or_abort(sopf2, par, abort, status)) {
+          tc::fence_after_sync();
+          d3_step(2);
+          d3_step(3);
+          d3_step(6);
+          d3_step(7);
           tc::mma_commit(mma3);
           tc::mma_commit(b3empty);
         }
-        if (wait_or_abort(uopf, par, abort, status) && wait_or_abort(b4full, par, abort, status) &&
-            wait_or_abort(sscl, par, abort, status)) {
+        // S^T += U^T K~, K = tokens: K-steps 0, 2 on the first half of the operand
+        auto x_step = [&](int k) {
+          const uint64_t kh = tc::desc_add(dKh, 256 * k), kl = tc::desc_add(dKl, 256 * k);
+          tc::mma_bf16_tmem_a(xs, aUh + 8 * k, kh, id128, 1);
+          tc::mma_bf16_tmem_a(xs, aUh + 8 * k, kl, id128, 1);
+          tc::mma_bf16_tmem_a(xs, aUl + 8 * k, kh, id128, 1);
+        };
+        const bool okU = wait_or_abort(uopf, par, abort, status) && wait_or_abort(b4full, par, abort, status) &&
+                         wait_or_abort(sscl, par, abort, status);
+        if (okU) {
           tc::fence_after_sync();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {   // S^T += U^T K~, K = tokens
-            const uint64_t kh = tc::desc_add(dKh, 256 * k), kl = tc::desc_add(dKl, 256 * k);
-            tc::mma_bf16_tmem_a(xs, aUh + 8 * k, kh, id128, 1);
-            tc::mma_bf16_tmem_a(xs, aUh + 8 * k, kl, id128, 1);
-            tc::mma_bf16_tmem_a(xs, aUl + 8 * k, kh, id128, 1);
-          }
+          x_step(0);
+          x_step(2);
+        }
+        if (okU && wait_or_abort(uopf2, par, abort, status)) {
+          tc::fence_after_sync();
+          x_step(1);
+          x_step(3);
           tc::mma_commit(sready);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {   // O^T = (Q~ S)^T + U^T P^T in D3^T columns 0-63
