@@ -158,13 +158,13 @@ def test_tc_gemm_mn_major_b(lib, N, K):
 
 def test_mma_issue_cost(lib):
     """Cycles per MMA (M = 128, K = 16, bf16) over 24 back-to-back MMAs, A in shared memory or
-    in TMEM, N = 64 / 128 / 256 (printed with -s; the prefill chain kernel keeps its A operands in
+    in TMEM, N = 64 / 128 / 192 / 256 (printed with -s; the prefill chain kernel keeps its A operands in
     TMEM because of this).  Checked: every run completes and the figures are sane."""
     out = torch.zeros(1, dtype=torch.int64, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     rows = []
     for tmem_a in (0, 1):
-        for N in (64, 128, 256):
+        for N in (64, 128, 192, 256):
             spans = []
             for nmma in (8, 24):
                 assert lib.tc_mma_cost(N, tmem_a, nmma, out.data_ptr(), err.data_ptr()) == 0
