@@ -586,7 +586,7 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   __syncthreads();
   if (!sh[0]) {
     tc::pdl_launch_dependents();
-    tc::pdl_wait_primary();   // no CTA of a pipelined window completes before the previous chains
+    if (blockIdx.x == 0 && blockIdx.y == 0) tc::pdl_wait_primary();   // see the end of the kernel
     return;
   }
   const int t0 = sh[1], L = sh[2], seq_len = sh[3], seq_start = sh[4];
@@ -876,11 +876,12 @@ tc_intra_kernel(KDims d, const float* __restrict__ A_log, const float* __restric
   if (warp == 1) tc::tmem_dealloc(tb, TI_COLS);
   // The window's chain kernel (a programmatic dependent of this one) may be set up from here on;
   // it reads nothing before this kernel has completed.  Launched as a programmatic dependent of
-  // the previous window's chain kernel, the CTA may have run beside it; it completes only after
-  // that kernel has, which orders this window's chain kernel after the previous one.  (Both are
-  // no-ops for an ordinary launch.)
+  // the previous window's chain kernel, this kernel may have run beside it; one CTA waits for that
+  // kernel before it exits, so this kernel completes only after it, which orders this window's
+  // chain kernel after the previous one.  The other CTAs leave their SMs as soon as their work is
+  // done.  (Both are no-ops for an ordinary launch.)
   tc::pdl_launch_dependents();
-  tc::pdl_wait_primary();
+  if (blockIdx.x == 0 && blockIdx.y == 0) tc::pdl_wait_primary();
 }
 
 // ================================================================== serial chain kernel
@@ -1404,13 +1405,15 @@ int launch_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool, const i
   // then its chain kernel carries every sequence's state through the window to the slot.
   // Pipelined: windows alternate between two halves of the workspace, and window w + 1's intra
   // kernel is a programmatic dependent launch of window w's chain kernel, so it starts on the SMs
-  // the chains leave free.  Its CTAs wait for that chain kernel to complete before they exit.
-  // Each chain kernel is a programmatic dependent launch of its window's intra kernel (which
-  // signals only by completing), so it is set up as soon as that kernel ends and waits for it
+  // the chains leave free.  One of its CTAs waits for that chain kernel to complete before it
+  // exits, so the intra kernel completes after it; the others exit when their work is done.
+  // Each chain kernel is a programmatic dependent launch of its window's intra kernel (whose CTAs
+  // signal when their work is done), so it is set up as SMs free up and waits for that kernel
   // before reading anything: window w + 1's chains read the slots only after window w's chains
   // have completed, and the half window w + 1's records go to was last read by window w - 1's
-  // chains, complete before window w's chain kernel could even start.  Serial (a workspace of fewer than two pipelined windows, or more chains than SMs):
-  // every window from the start of the workspace, each launch after the previous one.
+  // chains, complete before window w's chain kernel could even start.  Serial (a workspace of
+  // fewer than two pipelined windows, or more chains than SMs): every window from the start of
+  // the workspace, each launch after the previous one.
   // Chunk count bound: sum over sequences of ceil(len / 64) <= (total + 63 num_seqs) / 64.
   const int nc_max = std::max(1, (int)(((long long)total + (long long)(CH - 1) * num_seqs) / CH));
   const size_t per_chunk = (size_t)d.Hv * REC_BYTES;
