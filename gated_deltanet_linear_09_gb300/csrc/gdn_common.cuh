@@ -84,6 +84,16 @@ __device__ __forceinline__ void gates(float A_log, float dt_bias, float a, float
   beta = sigmoidf_(b);
 }
 
+// ------------------------------------------------------------------ launch order
+
+// For a kernel launched as a programmatic dependent of the previous kernel in the stream: waits
+// until that kernel has completed and its writes are visible, then lets the next kernel be placed
+// on the SMs as they free up (it waits the same way).  A no-op for an ordinary launch.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // ------------------------------------------------------------------ reductions
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -103,6 +103,7 @@ decode_multi_kernel(KDims d, int tt, const float* __restrict__ A_log,
   float* el = eg + r * TT;               // [r][TT] e^{gamma_{TT-1} - gamma_s}
 
   const size_t zld = (size_t)d.Hv * DV;
+  pdl_begin();   // nothing is read before the previous kernel of the stream has completed
   const int s = slot_idx[row];
   if (s < 0 || s >= num_slots) {
     if (s >= num_slots && tid == 0 && kh == 0) set_status(status, GDN_STATUS_SLOT_RANGE);
@@ -364,13 +365,25 @@ int launch_multi_t(const KDims& d, const gdn_weights* w, const gdn_pool* pool,
   });
   if (attr_rc != 0) return attr_rc;
   if (smem > 227 * 1024) return GDN_ERR_TOO_LARGE;
-  kern<<<dim3(d.Hk, B), kMT, smem, stream>>>(
-      d, TT, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
+  // a programmatic dependent launch: the CTAs may be placed while the previous kernel of the
+  // stream drains, and wait for it in the kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)d.Hk, (unsigned)B);
+  cfg.blockDim = dim3(kMT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, kern, d, TT, w->A_log, w->dt_bias, static_cast<const T*>(w->conv_weight),
       static_cast<const T*>(w->norm_weight), pool->rec_state, static_cast<T*>(pool->conv_state),
       pool->num_slots, pool->status, slot_idx, static_cast<const T*>(qkv),
       static_cast<const T*>(z), static_cast<const T*>(a), static_cast<const T*>(b),
       static_cast<T*>(out));
-  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 template <typename T>

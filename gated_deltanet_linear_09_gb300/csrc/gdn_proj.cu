@@ -194,6 +194,9 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tb = *tslot;
+  // the setup above touches only this CTA's resources; the activations and the packed weights
+  // are read after the previous kernel of the stream has completed
+  pdl_begin();
   // step j of the walk reads chunk (j + rot) mod nkc
   auto chunk = [&](int j) { const int c = j + rot; return c < nkc ? c : c - nkc; };
   // the first PDIST steps in flight, one cp.async group each (empty groups included, so that the
@@ -391,13 +394,17 @@ int launch_proj(const void* x, const void* wp, int M, int N, int K, int ks, cons
   cfg.blockDim = dim3(PTHREADS, 1, 1);
   cfg.dynamicSmemBytes = wide ? ProjCfg<PROWS_WIDE>::SMEM : ProjCfg<64>::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = (unsigned)ks;
+  // a programmatic dependent launch (the CTAs may be set up while the previous kernel of the
+  // stream drains); a cluster only with a split: nothing to exchange without one
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = (unsigned)ks;
   cfg.attrs = attr;
-  cfg.numAttrs = ks > 1 ? 1 : 0;   // no cluster without a split: nothing to exchange
+  cfg.numAttrs = ks > 1 ? 2 : 1;
   const int nkc = K / (wide ? ProjCfg<PROWS_WIDE>::KS : PK) / ks;
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   const unsigned char* wb = static_cast<const unsigned char*>(wp);
