@@ -227,7 +227,7 @@ int gdn_linear_bf16(const void* x, const void* w, int32_t M, int32_t N, int32_t 
   }
   const int nk = K / 64;
   if (k_split < 0 || k_split > 8) return GDN_ERR_INVALID_ARG;
-  if (k_split != 0 && nk % k_split != 0) return GDN_ERR_INVALID_ARG;
+  if (k_split > nk) return GDN_ERR_INVALID_ARG;   // every part takes at least one chunk
   const int ks = k_split != 0 ? k_split : gdn::proj_auto_split(M, N, K);
   return gdn::launch_proj(x, w, M, N, K, ks, pr, status, stream);
 }

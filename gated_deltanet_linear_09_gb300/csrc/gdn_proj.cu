@@ -158,7 +158,8 @@ __device__ __forceinline__ void load_chunk(uint32_t sa, const unsigned char* __r
 }
 
 // Grid (ceil(N/(PT*PM)), ceil(M/PN), ks), cluster (1, 1, ks): CTA z of a cluster takes contraction
-// chunks [z*nkc, (z+1)*nkc) and adds up columns [z*PN/ks, (z+1)*PN/ks) (rounded down) of the
+// chunks [z*nk/ks, (z+1)*nk/ks) of the nk (rounded down: a split need not divide nk, the parts
+// then differ by one chunk) and adds up columns [z*PN/ks, (z+1)*PN/ks) (rounded down) of the
 // cluster's tile (ks = 1: a plain launch, no cluster).  One CTA per SM: the stage ring takes
 // most of the shared memory and keeps PDIST chunks in flight.  Every thread copies its share of
 // each stage; thread 0 issues the MMAs.  The CTAs of one launch walk their chunks from different
@@ -167,7 +168,7 @@ __device__ __forceinline__ void load_chunk(uint32_t sa, const unsigned char* __r
 template <int PN>
 __global__ void __launch_bounds__(PTHREADS, 1)
 proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict__ WP, int M,
-            int N, int K, int nkc, const ProjRoute route, int32_t* __restrict__ status) {
+            int N, int K, int nk, const ProjRoute route, int32_t* __restrict__ status) {
   using C = ProjCfg<PN>;
   constexpr int PSTAGES = C::STAGES, PDIST = C::DIST;
   constexpr uint32_t PSTAGE_BYTES = C::STAGE_BYTES, PBAR_OFF = C::BAR_OFF;
@@ -176,11 +177,13 @@ proj_kernel(const __nv_bfloat16* __restrict__ X, const unsigned char* __restrict
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + PSTAGES);
   const int n0 = blockIdx.x * PT * PM, m0 = blockIdx.y * PN;
   const int ks = (int)gridDim.z, z = (int)blockIdx.z;
-  const int kbase = z * nkc * C::KS;
+  const int c0 = (int)((long long)z * nk / ks);                  // this CTA's first chunk
+  const int nkc = (int)((long long)(z + 1) * nk / ks) - c0;      // and its chunk count (>= 1)
+  const int kbase = c0 * C::KS;
   const int nt0 = blockIdx.x * PT, ntot = (N + PM - 1) / PM;
   const int ntiles = min(PT, ntot - nt0);   // weight tiles this CTA holds (the last may hold 1)
   const size_t tile_stride = (size_t)(K / PK) * PA_BYTES;
-  const unsigned char* wblk = WP + (size_t)nt0 * tile_stride + (size_t)z * nkc * C::A_BYTES;
+  const unsigned char* wblk = WP + (size_t)nt0 * tile_stride + (size_t)c0 * C::A_BYTES;
   const int rot = (int)(((unsigned long long)blockIdx.x * nkc / gridDim.x + blockIdx.y * 7ull) %
                         (unsigned)nkc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -340,6 +343,9 @@ int g_num_sms = 0;
 }  // namespace
 
 int proj_auto_split(int M, int N, int K) {
+  // clusters of c CTAs (one per SM) that can be resident at once, c = 1..8: a cluster is placed
+  // inside one GPC, so the count is not simply SMs / c
+  static int active[9] = {0};
   static std::once_flag once;
   std::call_once(once, [] {
     int dev = 0, sms = 0;
@@ -348,15 +354,39 @@ int proj_auto_split(int M, int N, int K) {
       g_num_sms = sms;
     else
       g_num_sms = 152;
+    if (cudaFuncSetAttribute(proj_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)ProjCfg<64>::SMEM) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    for (int c = 1; c <= 8; ++c) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(1, 1, (unsigned)c);
+      cfg.blockDim = dim3(PTHREADS, 1, 1);
+      cfg.dynamicSmemBytes = ProjCfg<64>::SMEM;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 1;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = (unsigned)c;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, proj_kernel<64>, &cfg) == cudaSuccess) active[c] = n;
+      else cudaGetLastError();
+    }
   });
-  // one CTA per SM: split the contraction while the grid still fits in one wave and every CTA
-  // keeps at least a full ring of chunks
+  // one CTA per SM: split the contraction (into parts that may differ by one chunk) while every
+  // cluster of the grid is resident at once (one wave) and every CTA keeps at least a full ring
+  // of chunks
   constexpr int PN = ProjCfg<64>::PN;
   const long long tiles = (long long)((N + PT * PM - 1) / (PT * PM)) * ((M + PN - 1) / PN);
   const int nk = K / PK;
   int ks = 1;
-  for (int c = 2; c <= 8; ++c)
-    if (tiles * c <= (long long)g_num_sms && nk % c == 0 && nk / c >= ProjCfg<64>::STAGES) ks = c;
+  for (int c = 2; c <= 8; ++c) {
+    const long long fits = active[c] > 0 ? (long long)active[c] : (long long)g_num_sms / c;
+    if (tiles <= fits && nk / c >= ProjCfg<64>::STAGES) ks = c;
+  }
   return ks;
 }
 
@@ -405,12 +435,12 @@ int launch_proj(const void* x, const void* wp, int M, int N, int K, int ks, cons
   attr[1].val.clusterDim.z = (unsigned)ks;
   cfg.attrs = attr;
   cfg.numAttrs = ks > 1 ? 2 : 1;
-  const int nkc = K / (wide ? ProjCfg<PROWS_WIDE>::KS : PK) / ks;
+  const int nk = K / (wide ? ProjCfg<PROWS_WIDE>::KS : PK);   // contraction chunks, split over ks
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   const unsigned char* wb = static_cast<const unsigned char*>(wp);
   const cudaError_t e =
-      wide ? cudaLaunchKernelEx(&cfg, proj_kernel<PROWS_WIDE>, xb, wb, M, N, K, nkc, route, status)
-           : cudaLaunchKernelEx(&cfg, proj_kernel<64>, xb, wb, M, N, K, nkc, route, status);
+      wide ? cudaLaunchKernelEx(&cfg, proj_kernel<PROWS_WIDE>, xb, wb, M, N, K, nk, route, status)
+           : cudaLaunchKernelEx(&cfg, proj_kernel<64>, xb, wb, M, N, K, nk, route, status);
   return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

@@ -304,9 +304,10 @@ typedef struct {
  *     above); M = 0 returns GDN_OK after those checks, launching nothing and reading no
  *     other argument.  Destinations: device bf16, disjoint from x and w_packed.
  *   k_split: 0 lets the library choose; 1 to 8 splits the contraction over that many CTAs of
- *     a thread-block cluster whose f32 partial sums are added in a fixed order (it must
- *     divide K / 64; GDN_ERR_INVALID_ARG otherwise).  For a given k_split the result is
- *     bitwise reproducible.
+ *     a thread-block cluster whose f32 partial sums are added in a fixed order; part z takes
+ *     the 64-wide chunks [z n / k_split, (z + 1) n / k_split) of the n = K / 64 (k_split <= n;
+ *     GDN_ERR_INVALID_ARG otherwise).  For a given k_split the result is bitwise
+ *     reproducible.
  *   status: optional device int32 word; GDN_STATUS_TIMEOUT is OR-ed in if a bounded wait
  *     inside the kernel gave up (the outputs are then invalid).
  * One kernel launch; no host reads of device data (graph-capturable). */

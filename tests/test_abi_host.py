@@ -145,8 +145,8 @@ def test_projection_host_checks(lib):
     assert lin(r=route((0,), (63,))) == -1                 # ld below the segment's width
     assert lin(r=route(dsts=(Y + 1,))) == -7               # bf16 destination alignment
     assert lin(ks=9) == -1 and lin(ks=-1) == -1
-    assert lin(K=128, ks=3) == -1                         # 3 does not divide K / 64 = 2
-    assert lin(K=128, ks=4) == -1                         # split must divide K / 64
+    assert lin(K=128, ks=3) == -1                         # more parts than the 2 chunks of K / 64
+    assert lin(K=128, ks=4) == -1                         # every part takes at least one chunk
     assert lin(M=0, ks=5, x=0) == 0                       # empty: nothing read or launched
     d = D()
     assert lib.gdn_in_proj(ctypes.byref(D(Hv=33)), X, W, 4, 256, Y, Y, Y, Y, None, None) == -3

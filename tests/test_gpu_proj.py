@@ -46,6 +46,8 @@ def _operands(M, N, K, seed):
     (100, 385, 512, 4),       # ragged rows (2 row tiles) and a 1-feature last tile
     (130, 129, 512, 8),       # 3 row tiles, split over a cluster of 8
     (70, 250, 384, 3),        # a cluster of 3: column slices of 21, 21 and 22
+    (64, 300, 640, 7),        # a split that does not divide the 10 chunks: parts of 1 and 2
+    (100, 385, 2048, 5),      # 32 chunks over 5: parts of 6 and 7
     (200, 1000, 2048, 0),
     (512, 300, 256, 0),       # from 512 unsplit rows on: the 256-row tile form
     (700, 385, 512, 1),       # ragged rows (2 full row tiles + 188) and a 1-feature last tile
@@ -103,7 +105,7 @@ def test_linear_is_deterministic_and_splits_agree():
     xd, wd = _bf16_dev(x), _packed(w)
     ref = oracle.linear(x, w)
     outs = {}
-    for ks in (1, 2, 3, 4, 5, 6, 6):
+    for ks in (1, 2, 3, 4, 5, 6, 6, 7, 8, 7):   # 60 chunks: 7 and 8 split them unevenly
         y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         gdn.gdn_linear_bf16(xd, wd, N, gdn.make_route([(0, N, y)]), ks)
         torch.cuda.synchronize()
