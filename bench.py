@@ -43,7 +43,7 @@ E2E_RING = 64   # pinned input buffers cycled by the end-to-end lines (64 x 2.1 
 # changed kernel reports null until it is captured again.
 DECODE_TRAFFIC = {"2d07f0f7bcccbb6f": 357482240}
 # The same for the projection kernel's B=64 input projection (hidden 5120, 16480 features).
-PROJ_IN_TRAFFIC = {"1e6c7d6f51d11753": 172790784}
+PROJ_IN_TRAFFIC = {"e4ae6441192dab86": 173514496}
 
 
 def _src_sha(name: str) -> str:
