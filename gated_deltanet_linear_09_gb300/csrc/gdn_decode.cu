@@ -64,6 +64,38 @@ __host__ __device__ inline int decode_float_count(int r) {
   return ((2 * DK + 2 * r * DV + r * kDecodeWarps + 3 + 2 * r) + 3) / 4 * 4;
 }
 
+// Conv-state values with an L2 evict-last policy: the step's rows read and rewrite their slots'
+// conv state (a few MB) while the recurrent states stream through L2 evict-first, so the next
+// step finds it in L2.
+template <typename T> struct KeepL2;
+template <> struct KeepL2<float> {
+  static __device__ __forceinline__ float ld(const float* p, uint64_t pol) {
+    float v;
+    asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(pol));
+    return v;
+  }
+  static __device__ __forceinline__ void st(float* p, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(pol) : "memory");
+  }
+};
+template <> struct KeepL2<__nv_bfloat16> {
+  static __device__ __forceinline__ __nv_bfloat16 ld(const __nv_bfloat16* p, uint64_t pol) {
+    unsigned short v;
+    asm volatile("ld.global.L2::cache_hint.b16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
+    return __ushort_as_bfloat16(v);
+  }
+  static __device__ __forceinline__ void st(__nv_bfloat16* p, __nv_bfloat16 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(p), "h"(__bfloat16_as_ushort(v)),
+                 "l"(pol)
+                 : "memory");
+  }
+};
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // One token of the causal conv for channel ch of the row's conv state cs ([K-1][cqkv],
 // K = 4): returns SiLU(sum_j w[j] x_{t-3+j}) and shifts the state by one raw input.
 template <typename T>
@@ -147,6 +179,7 @@ decode_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict_
   const T* x_row = qkv + (size_t)row * d.cqkv;
   T* cs = conv_state + (size_t)s * 3 * d.cqkv;
   const int nch = 2 * DK + r * DV;
+  const uint64_t keep = l2_evict_last_policy();
   for (int c0 = 0; c0 < nch; c0 += 3 * kDecodeThreads) {
     int chs[3];
     float* dsts[3];
@@ -166,9 +199,9 @@ decode_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict_
         dsts[m] = vs + (c - 2 * DK);
       }
       xr[m] = x_row[chs[m]];
-      s0[m] = cs[chs[m]];
-      s1[m] = cs[d.cqkv + chs[m]];
-      s2[m] = cs[2 * d.cqkv + chs[m]];
+      s0[m] = KeepL2<T>::ld(cs + chs[m], keep);
+      s1[m] = KeepL2<T>::ld(cs + d.cqkv + chs[m], keep);
+      s2[m] = KeepL2<T>::ld(cs + 2 * d.cqkv + chs[m], keep);
 #pragma unroll
       for (int j = 0; j < 4; ++j) wv[m][j] = Act<T>::ldg(conv_w + (size_t)chs[m] * 4 + j);
     }
@@ -179,9 +212,9 @@ decode_kernel(KDims d, const float* __restrict__ A_log, const float* __restrict_
         acc = fmaf(wv[m][0], Act<T>::load(&s0[m]), acc);
         acc = fmaf(wv[m][1], Act<T>::load(&s1[m]), acc);
         acc = fmaf(wv[m][2], Act<T>::load(&s2[m]), acc);
-        cs[chs[m]] = s1[m];
-        cs[d.cqkv + chs[m]] = s2[m];
-        cs[2 * d.cqkv + chs[m]] = xr[m];
+        KeepL2<T>::st(cs + chs[m], s1[m], keep);
+        KeepL2<T>::st(cs + d.cqkv + chs[m], s2[m], keep);
+        KeepL2<T>::st(cs + 2 * d.cqkv + chs[m], xr[m], keep);
         *dsts[m] = siluf_(acc);
       }
     }
