@@ -27,6 +27,7 @@ compact_kernel(const __grid_constant__ CompactPairs pairs, int n, uint4* __restr
   uint4* base = blockIdx.y == 0 ? rec : conv;
   const size_t units = blockIdx.y == 0 ? rec_units : conv_units;
   const size_t col0 = (size_t)blockIdx.x * cols;
+  pdl_begin();   // the slots are read after the previous kernel of the stream has completed
   if (col0 >= units) return;
   const int ncol = (int)min((size_t)cols, units - col0);
   const int total = n * ncol;
@@ -62,10 +63,20 @@ int launch_compact(const CompactPairs& pairs, int n, void* rec, size_t rec_slot_
   const size_t umax = ru > cu ? ru : cu;
   const size_t tiles = (umax + cols - 1) / cols;
   if (tiles > 0x7fffffffULL) return GDN_ERR_TOO_LARGE;
-  dim3 grid((unsigned)tiles, 2);
-  compact_kernel<<<grid, kCompactThreads, 0, stream>>>(pairs, n, static_cast<uint4*>(rec), ru,
-                                                       static_cast<uint4*>(conv), cu, cols);
-  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  // a programmatic dependent launch: the CTAs may be placed while the previous kernel of the
+  // stream drains, and wait for it in the kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tiles, 2);
+  cfg.blockDim = dim3(kCompactThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, compact_kernel, pairs, n, static_cast<uint4*>(rec), ru,
+                                           static_cast<uint4*>(conv), cu, cols);
+  return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 }  // namespace gdn

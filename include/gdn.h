@@ -27,11 +27,11 @@
  *     never synchronises the device and launches only on the given stream -- except the
  *     CUDA-graph decode object: gdn_decode_graphs_create allocates its static buffers and
  *     captures on an internal stream (synchronously), gdn_decode_graphs_destroy frees them.
- *   Launch order: the decode, multi-token decode and projection kernels (and a prefill call's
- *     kernels after its first) are launched as programmatic dependents of the previous kernel
- *     on the stream: their blocks may be placed on the GPU while that kernel finishes, but they
- *     read and write nothing that kernel could touch before it has completed and its writes are
- *     visible, so stream order holds as for any launch.
+ *   Launch order: the decode, multi-token decode, projection and compaction kernels (and a
+ *     prefill call's kernels after its first) are launched as programmatic dependents of the
+ *     previous kernel on the stream: their blocks may be placed on the GPU while that kernel
+ *     finishes, but they read and write nothing that kernel could touch before it has completed
+ *     and its writes are visible, so stream order holds as for any launch.
  *   Pointers: device pointers unless marked "host"; base addresses 16-byte aligned; all
  *     tensors dense, row-major, in the layouts below.
  *   Layouts (Cqkv = 2*Hk*dk + Hv*dv, r = Hv/Hk):
