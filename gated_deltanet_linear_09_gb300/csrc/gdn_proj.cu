@@ -384,7 +384,10 @@ int proj_auto_split(int M, int N, int K) {
   const int nk = K / PK;
   int ks = 1;
   for (int c = 2; c <= 8; ++c) {
-    const long long fits = active[c] > 0 ? (long long)active[c] : (long long)g_num_sms / c;
+    // without the residency count (the query failed), only splits that divide nk, within the
+    // SM count
+    const long long fits = active[c] > 0 ? (long long)active[c]
+                                         : (nk % c == 0 ? (long long)g_num_sms / c : 0);
     if (tiles <= fits && nk / c >= ProjCfg<64>::STAGES) ks = c;
   }
   return ks;
