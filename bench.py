@@ -43,7 +43,7 @@ E2E_RING = 64   # pinned input buffers cycled by the end-to-end lines (64 x 2.1 
 # changed kernel reports null until it is captured again.
 DECODE_TRAFFIC = {"ca7142ef62f2d9c6": 353341952}
 # The same for the projection kernel's B=64 input projection (hidden 5120, 16480 features).
-PROJ_IN_TRAFFIC = {"392b95e0200d0ad8": 173206272}
+PROJ_IN_TRAFFIC = {"e339b96ae862774e": 173261568}
 
 
 def _src_sha(name: str) -> str:

@@ -342,10 +342,11 @@ int g_num_sms = 0;
 
 }  // namespace
 
-int proj_auto_split(int M, int N, int K) {
-  // clusters of c CTAs (one per SM) that can be resident at once, c = 1..8: a cluster is placed
-  // inside one GPC, so the count is not simply SMs / c
-  static int active[9] = {0};
+// Clusters of c CTAs (one per SM) that can be resident at once, c = 1..8, read once per process:
+// a cluster is placed inside one GPC, so the count is not simply SMs / c.  First done by the
+// weight packing (before any projection, normally outside any graph capture).
+int g_active_clusters[9] = {0};
+void proj_init_once() {
   static std::once_flag once;
   std::call_once(once, [] {
     int dev = 0, sms = 0;
@@ -372,10 +373,15 @@ int proj_auto_split(int M, int N, int K) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, proj_kernel<64>, &cfg) == cudaSuccess) active[c] = n;
+      if (cudaOccupancyMaxActiveClusters(&n, proj_kernel<64>, &cfg) == cudaSuccess) g_active_clusters[c] = n;
       else cudaGetLastError();
     }
   });
+}
+
+int proj_auto_split(int M, int N, int K) {
+  proj_init_once();
+  const int* active = g_active_clusters;
   // one CTA per SM: split the contraction (into parts that may differ by one chunk) while every
   // cluster of the grid is resident at once (one wave) and every CTA keeps at least a full ring
   // of chunks
@@ -396,6 +402,7 @@ int proj_auto_split(int M, int N, int K) {
 size_t proj_packed_bytes(int N, int K) { return (size_t)((N + PM - 1) / PM) * PM * (size_t)K * 2; }
 
 int launch_proj_pack(const void* w, int N, int K, void* packed, cudaStream_t stream) {
+  proj_init_once();
   const long long units = (long long)proj_packed_bytes(N, K) / 16;
   const int threads = 256;
   const long long want = (units + threads - 1) / threads;
