@@ -36,6 +36,8 @@ def _layer(geo, seed, num_slots, prefilled):
     synth.Geometry(2, 6, 128, 128, 4, synth.BF16),
     synth.Geometry(3, 3, 128, 64, 4, synth.BF16),
     synth.Geometry(1, 2, 64, 128, 4, synth.F32),
+    synth.Geometry(1, 4, 128, 128, 4, synth.BF16),
+    synth.Geometry(1, 6, 64, 64, 4, synth.F32),
 ], ids=lambda g: f"Hk{g.Hk}Hv{g.Hv}dk{g.dk}dv{g.dv}{g.act}")
 def test_decode_small_full_compare(geo):
     """Every output, every state, padding rows and untouched slots, over 12 steps."""

@@ -35,6 +35,8 @@ def _dev_i32(x):
     synth.Geometry(2, 4, 64, 128, 4, synth.F32),
     synth.Geometry(2, 4, 128, 128, 4, synth.F32),
     synth.Geometry(1, 3, 128, 128, 4, synth.BF16),
+    synth.Geometry(1, 4, 128, 128, 4, synth.BF16),   # four V-heads per K-head: the tensor-core path's limit
+    synth.Geometry(1, 6, 64, 64, 4, synth.F32),      # six: the CUDA-core kernels
 ], ids=lambda g: f"Hk{g.Hk}Hv{g.Hv}dk{g.dk}dv{g.dv}{g.act}")
 def test_prefill_varlen_full_compare(geo):
     lens = [1, 63, 0, 64, 65, 130, 2, 200]
