@@ -54,6 +54,7 @@ def _oracle_multi(geo, w64, r64, c64, slots, xs):
     synth.Geometry(2, 6, 128, 128, 4, synth.BF16),
     synth.Geometry(2, 4, 64, 64, 4, synth.F32),
     synth.Geometry(3, 3, 128, 64, 4, synth.BF16),
+    synth.Geometry(1, 4, 64, 128, 4, synth.F32),
 ], ids=lambda g: f"Hk{g.Hk}Hv{g.Hv}dk{g.dk}dv{g.dv}{g.act}")
 def test_decode_multi_full_compare(geo, T):
     """Every output and state over 3 calls of T tokens, a padding row, untouched slots."""
