@@ -140,3 +140,37 @@ def test_decode_multi_rejects_bad_token_count():
             layer.decode_multi(slots, **inp)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(_np(layer.rec_state), rec)   # nothing launched
+
+
+def test_decode_multi_captured_in_cuda_graph():
+    """gdn_decode_multi is one launch with no host reads of device data: captured in a CUDA graph
+    and replayed on refilled inputs, it matches eager calls bit for bit (outputs and state)."""
+    geo = synth.Geometry(2, 6, 128, 128, 4, synth.BF16)
+    T = 3
+    la, w, rec, conv = _layer(geo, 730, 4, True)
+    slots = torch.tensor([3, -1, 1], dtype=torch.int32, device="cuda")
+    calls = [la.inputs(_multi_inputs(geo, 3, T, 731, c)) for c in range(3)]
+    eager = [_np(la.decode_multi(slots, **x)) for x in calls]
+    torch.cuda.synchronize()
+    eager_state = _np(la.rec_state).copy()
+    la.load_state(rec, conv)
+    static = {k: torch.empty_like(v) for k, v in calls[0].items()}
+    for k in static:
+        static[k].copy_(calls[0][k])
+    out = torch.empty((3, T, geo.zdim), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            la.decode_multi(slots, static["qkv"], static["z"], static["a"], static["b"], out, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_np(la.rec_state), rec)   # capture runs nothing
+    for x, ref in zip(calls, eager):
+        for k in static:
+            static[k].copy_(x[k])
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(_np(out), ref)
+    np.testing.assert_array_equal(_np(la.rec_state), eager_state)
