@@ -48,8 +48,10 @@
  *     checks.  Errors found on the device (a slot index out of range) never trap: the row
  *     is skipped, its output zeroed, and a bit is OR-ed into *pool->status when that
  *     optional device word is given.
- *   Thread safety: no global mutable state; concurrent calls on different streams are safe
- *     when they touch disjoint slots and buffers.
+ *   Thread safety: no global mutable state beyond what the first call on a device sets up
+ *     once (kernel attributes and device properties, under a once-only guard, read-only after);
+ *     concurrent calls on different streams are safe when they touch disjoint slots and
+ *     buffers.
  */
 #ifndef GDN_H
 #define GDN_H

@@ -319,3 +319,55 @@ def test_decode_with_pinned_host_buffers():
         np.testing.assert_array_equal(out_h.float().numpy(), _np(out_d))
     np.testing.assert_array_equal(_np(la.rec_state), _np(lb.rec_state))
     np.testing.assert_array_equal(_np(la.conv_state), _np(lb.conv_state))
+
+
+def test_concurrent_calls_on_two_streams_disjoint_slots():
+    """Two host threads, each on its own stream, run decode steps over disjoint slots of one
+    pool at the same time; the states and outputs equal those of the same steps run one after
+    another (the kernels are deterministic, and disjoint slots do not interact)."""
+    import threading
+    geo = synth.Geometry(2, 4, 128, 128, 4, synth.BF16)
+    layer, w, rec, conv = _layer(geo, 580, 8, True)
+    sets = [torch.tensor([0, 3, 5], dtype=torch.int32, device="cuda"),
+            torch.tensor([6, 1, 2], dtype=torch.int32, device="cuda")]
+    steps = 24
+    xs = [[layer.inputs(synth.make_token_inputs(geo, 3, 581 + j, t)) for t in range(steps)]
+          for j in range(2)]
+    # one after another on the default stream
+    seq_out = [[], []]
+    for j in range(2):
+        for t in range(steps):
+            seq_out[j].append(_np(layer.decode_step(sets[j], **xs[j][t])))
+    torch.cuda.synchronize()
+    seq_rec, seq_conv = _np(layer.rec_state).copy(), _np(layer.conv_state).copy()
+    # concurrently, one thread and one stream per slot set
+    layer.load_state(rec, conv)
+    torch.cuda.synchronize()
+    outs = [[torch.empty((3, geo.zdim), dtype=torch.bfloat16, device="cuda") for _ in range(steps)]
+            for _ in range(2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    errors = []
+
+    def run(j):
+        try:
+            with torch.cuda.stream(streams[j]):
+                for t in range(steps):
+                    x = xs[j][t]
+                    layer.decode_step(sets[j], x["qkv"], x["z"], x["a"], x["b"], outs[j][t],
+                                      stream=streams[j])
+        except Exception as e:   # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(j,)) for j in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for j in range(2):
+        for t in range(steps):
+            np.testing.assert_array_equal(_np(outs[j][t]), seq_out[j][t])
+    np.testing.assert_array_equal(_np(layer.rec_state), seq_rec)
+    np.testing.assert_array_equal(_np(layer.conv_state), seq_conv)
+    assert int(layer.status.item()) == 0
