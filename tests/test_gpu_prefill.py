@@ -325,3 +325,54 @@ def test_prefill_65536_tokens_bounded_workspace():
     assert_state_close(hs.rec(g_rec)[0], r64[0], "65,536-token final state, K-head 9")
     np.testing.assert_array_equal(hs.conv(g_conv)[0], c64[0])
     assert int(layer.status.item()) == 0
+
+
+def test_concurrent_prefill_calls_on_two_streams():
+    """Two prefill calls over disjoint slots, each with its own workspace, issued from two host
+    threads on two streams at once, equal the same calls made one after another."""
+    import threading
+    geo = synth.Geometry(2, 4, 128, 128, 4, synth.BF16)
+    w = synth.make_weights(geo, 640)
+    rec0, conv0 = synth.make_pool(geo, 6, 641, True)
+    layer = GatedDeltaNetLayer(geo, w, 6)
+    calls = []
+    for j, (lens, slots, init) in enumerate((([300, 77], [0, 3], [1, 0]), ([450], [5], [0]))):
+        cu = synth.cu_seqlens(lens)
+        xs = layer.inputs(synth.make_token_inputs(geo, int(cu[-1]), 642 + j, 0))
+        calls.append((_dev_i32(cu), _dev_i32(slots), torch.tensor(init, dtype=torch.uint8, device="cuda"),
+                      len(lens), int(cu[-1]), xs))
+    # one after another
+    layer.load_state(rec0, conv0)
+    seq = [_np(layer.prefill(cu, sl, hi, **xs)) for cu, sl, hi, n, T, xs in calls]
+    torch.cuda.synchronize()
+    seq_rec, seq_conv = _np(layer.rec_state).copy(), _np(layer.conv_state).copy()
+    # at once, one thread and one stream per call, each with its own workspace
+    layer.load_state(rec0, conv0)
+    outs = [torch.empty((T, geo.zdim), dtype=torch.bfloat16, device="cuda") for _, _, _, _, T, _ in calls]
+    wss = [torch.empty(max(gdn.gdn_prefill_workspace_bytes(layer.dims, n, T), 256), dtype=torch.uint8,
+                       device="cuda") for _, _, _, n, T, _ in calls]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(j):
+        try:
+            cu, sl, hi, n, T, xs = calls[j]
+            with torch.cuda.stream(streams[j]):
+                gdn.gdn_prefill_chunked(layer.dims, layer.w, layer.pool, cu, sl, hi, n, T, xs["qkv"],
+                                        xs["z"], xs["a"], xs["b"], outs[j], wss[j], streams[j])
+        except Exception as e:   # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(j,)) for j in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for j in range(2):
+        np.testing.assert_array_equal(_np(outs[j]), seq[j])
+    np.testing.assert_array_equal(_np(layer.rec_state), seq_rec)
+    np.testing.assert_array_equal(_np(layer.conv_state), seq_conv)
+    assert int(layer.status.item()) == 0
