@@ -42,6 +42,14 @@ MUTATIONS = {
     "in_proj_b_a_swapped": (
         "    memcpy(b + (size_t)m * Hv, yr + cqkv + zd, sizeof(double) * Hv);",
         "    memcpy(b + (size_t)m * Hv, yr + cqkv + zd + Hv, sizeof(double) * Hv);"),
+    "prefill_keeps_state_without_init": (
+        "      memset(S, 0, sizeof(double) * rec_slot);\n      memset(cs, 0, sizeof(double) * conv_slot);\n"
+        "    }\n    for (int t = t0; t < t1; ++t)",
+        "      memset(cs, 0, sizeof(double) * conv_slot);\n    }\n    for (int t = t0; t < t1; ++t)"),
+    "chunkwise_keeps_state_without_init": (
+        "      memset(S, 0, sizeof(double) * rec_slot);\n      memset(cs, 0, sizeof(double) * conv_slot);\n"
+        "    }\n    if (T <= 0) continue;",
+        "      memset(cs, 0, sizeof(double) * conv_slot);\n    }\n    if (T <= 0) continue;"),
     "compact_no_snapshot": (
         "    memcpy(rec_state + (size_t)dst[i] * rec_slot_elems, snap_r + (size_t)i * rec_slot_elems,",
         "    memcpy(rec_state + (size_t)dst[i] * rec_slot_elems, rec_state + (size_t)src[i] * rec_slot_elems,"),
