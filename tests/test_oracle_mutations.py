@@ -50,6 +50,14 @@ MUTATIONS = {
         "      memset(S, 0, sizeof(double) * rec_slot);\n      memset(cs, 0, sizeof(double) * conv_slot);\n"
         "    }\n    if (T <= 0) continue;",
         "      memset(cs, 0, sizeof(double) * conv_slot);\n    }\n    if (T <= 0) continue;"),
+    "l2norm_eps_outside_root": ("  const double inv = 1.0 / sqrt(ss + eps);",
+                                "  const double inv = 1.0 / (sqrt(ss) + eps);"),
+    "conv_without_silu": ("    y[c] = oracle_silu(acc);", "    y[c] = acc;"),
+    "gate_sigmoid_not_silu": (
+        "  for (int j = 0; j < dv; ++j) out[j] = o[j] * inv * w[j] * oracle_silu(z[j]);",
+        "  for (int j = 0; j < dv; ++j) out[j] = o[j] * inv * w[j] * oracle_sigmoid(z[j]);"),
+    "chunk_output_strict_mask": ("            for (int j = 0; j <= i; ++j) {\n              double qk = 0.0;",
+                                 "            for (int j = 0; j < i; ++j) {\n              double qk = 0.0;"),
     "compact_no_snapshot": (
         "    memcpy(rec_state + (size_t)dst[i] * rec_slot_elems, snap_r + (size_t)i * rec_slot_elems,",
         "    memcpy(rec_state + (size_t)dst[i] * rec_slot_elems, rec_state + (size_t)src[i] * rec_slot_elems,"),
